@@ -1,0 +1,354 @@
+/*
+ * attnres_oracle.c -- plain, slow, single-threaded CPU oracle for the
+ * Attention Residuals depth-wise softmax read.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test-suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header, table or helper
+ * with the CUDA library.
+ *
+ * Every function works in IEEE double precision on the exact input values
+ * (bf16 inputs are widened exactly before they get here).  No blocking, no
+ * fusion, no reordering beyond what the definitions state; loops follow the
+ * formulas term by term so they can be checked against the pages by eye.
+ *
+ * Page labels used in the citations below:
+ *   [Summary]   b-lab.team summary of "Attention Residuals"
+ *               (sections 1 Full AttnRes, 2 Block AttnRes, 3 Infrastructure)
+ *   [Review]    dimensionstp.github.io "Attention Residuals" review
+ *               (sections 2-2, 3-2, 4-3)
+ *   [Tutorial]  ai-systems-engineering.com "Attention Residuals: 지나온 층의
+ *               출력을 선택해서 읽기" (Figs. 2-4 and their worked example)
+ *   [MSAR]      onedev.kr "깊이 방향 어텐션을 다중 스트림으로 확장한 MSAR"
+ *               (sections 무엇과 다른가, 어떻게 쓰나)
+ *   [MHAR]      chatpaper.ai "Multi-Head Attention Residuals" abstract
+ *
+ * Layouts (row-major, contiguous):
+ *   sources   src[n_src][T][d]
+ *   queries   w[n_q][d]          (MHAR: w[n_q][H][d/H])
+ *   gain      g[d] or NULL (NULL means every channel has gain 1)
+ *
+ * Return value: 0 on success, -1 on an invalid argument.
+ *
+ * Parity status: every exported function below is pinned by the non-GPU
+ * tests (worked example, closed forms, invariants, brute force); none is
+ * "parity unpinned".
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------------- */
+/* Building blocks                                                          */
+/* ---------------------------------------------------------------------- */
+
+/* RMSNorm of one vector, [Summary §1] kernel phi(q,k) = exp(q^T RMSNorm(k)),
+ * [Tutorial Fig. 3] "gain 1, epsilon omitted": y = g * x / sqrt(mean(x^2)+eps).
+ * Reading taken where the pages are silent: eps sits inside the square root,
+ * added to the mean square; a zero vector with eps = 0 normalises to zero. */
+static void rmsnorm(const double *x, const double *g, int64_t n, double eps,
+                    double *y)
+{
+    double ms = 0.0;
+    for (int64_t c = 0; c < n; ++c) ms += x[c] * x[c];
+    ms /= (double)n;
+    double denom = sqrt(ms + eps);
+    for (int64_t c = 0; c < n; ++c) {
+        double gc = g ? g[c] : 1.0;
+        y[c] = (denom > 0.0) ? gc * x[c] / denom : 0.0;
+    }
+}
+
+/* score = w^T RMSNorm(k)  [Summary §1], [Review §2-2 eq. for alpha] */
+static double score(const double *w, const double *k, const double *g,
+                    int64_t n, double eps, double *tmp)
+{
+    rmsnorm(k, g, n, eps, tmp);
+    double s = 0.0;
+    for (int64_t c = 0; c < n; ++c) s += w[c] * tmp[c];
+    return s;
+}
+
+/* softmax over depth: alpha_i = exp(s_i - max) / sum_j exp(s_j - max);
+ * also returns lse = max + log(sum_j exp(s_j - max)).  [Summary §1 alpha] */
+static double softmax(const double *s, int64_t n, double *alpha)
+{
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) if (s[i] > m) m = s[i];
+    double l = 0.0;
+    for (int64_t i = 0; i < n; ++i) { alpha[i] = exp(s[i] - m); l += alpha[i]; }
+    for (int64_t i = 0; i < n; ++i) alpha[i] /= l;
+    return m + log(l);
+}
+
+/* One depth read for one token over a list of source rows:
+ *   h = sum_i alpha_i v_i  with  alpha = softmax_i(w^T RMSNorm(v_i)).
+ * The weighted sum uses the raw (un-normalised) values: [Tutorial Fig. 3]
+ * "the sqrt(3) used for the score is not multiplied back onto the source".
+ * rows[i] points at v_i (length n).  alpha_out/lse_out may be NULL. */
+static int read_one(const double *const *rows, int64_t n_src, int64_t n,
+                    const double *w, const double *g, double eps,
+                    double *h, double *alpha_out, double *lse_out)
+{
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)n);
+    double *s = (double *)malloc(sizeof(double) * (size_t)n_src);
+    double *a = (double *)malloc(sizeof(double) * (size_t)n_src);
+    if (!tmp || !s || !a) { free(tmp); free(s); free(a); return -1; }
+    for (int64_t i = 0; i < n_src; ++i) s[i] = score(w, rows[i], g, n, eps, tmp);
+    double lse = softmax(s, n_src, a);
+    for (int64_t c = 0; c < n; ++c) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < n_src; ++i) acc += a[i] * rows[i][c];
+        h[c] = acc;
+    }
+    if (alpha_out) for (int64_t i = 0; i < n_src; ++i) alpha_out[i] = a[i];
+    if (lse_out) *lse_out = lse;
+    free(tmp); free(s); free(a);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Full AttnRes                                                            */
+/* ---------------------------------------------------------------------- */
+
+/* Full AttnRes read for one layer, [Summary §1] h_l = sum_{i<l} alpha_{i->l} v_i,
+ * [Review §3-2 1)].  src[n_src][T][d] are the sources v_0..v_{n_src-1};
+ * out[T][d]; lse[T] (may be NULL) = log sum_i exp(score_i); alpha[T][n_src]
+ * (may be NULL) receives the weights. */
+int oracle_full(const double *src, int64_t n_src, int64_t T, int64_t d,
+                const double *query, const double *gain, double eps,
+                double *out, double *lse, double *alpha)
+{
+    if (!src || !query || !out || n_src < 1 || T < 0 || d < 1 || eps < 0) return -1;
+    const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_src);
+    if (!rows) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < n_src; ++i) rows[i] = src + (i * T + t) * d;
+        if (read_one(rows, n_src, d, query, gain, eps, out + t * d,
+                     alpha ? alpha + t * n_src : NULL, lse ? lse + t : NULL)) {
+            free(rows); return -1;
+        }
+    }
+    free(rows);
+    return 0;
+}
+
+/* The weighted sum alone with given weights: h[t] = sum_i alpha[t][i] v_i[t].
+ * [Tutorial Fig. 2] table "each weight multiplies the whole source vector". */
+int oracle_weighted_sum(const double *src, int64_t n_src, int64_t T, int64_t d,
+                        const double *alpha, double *out)
+{
+    if (!src || !alpha || !out || n_src < 1 || T < 0 || d < 1) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < n_src; ++i) acc += alpha[t * n_src + i] * src[(i * T + t) * d + c];
+            out[t * d + c] = acc;
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Block AttnRes                                                           */
+/* ---------------------------------------------------------------------- */
+
+/* Block AttnRes, one block, computed one layer at a time ("one-shot").
+ * [Summary §2] value matrix of layer i of block n:
+ *   i = 1:  [b_0, ..., b_{n-1}]
+ *   i >= 2: [b_0, ..., b_{n-1}, b^{(n)}_{i-1}]   (current partial sum)
+ * [Tutorial Fig. 4]: the first sublayer of a block does not read the empty
+ * current sum.  cache[N][T][d] holds b_0..b_{N-1}; partials[S][T][d] holds
+ * the partial sum read by each layer (slot 0 is ignored: layer 1 has none);
+ * queries[S][d]; out[S][T][d]. */
+int oracle_block_oneshot(const double *cache, int64_t N, const double *partials,
+                         int64_t S, int64_t T, int64_t d, const double *queries,
+                         const double *gain, double eps, double *out)
+{
+    if (!cache || !queries || !out || N < 1 || S < 1 || T < 0 || d < 1 || eps < 0) return -1;
+    if (S > 1 && !partials) return -1;
+    const double **rows = (const double **)malloc(sizeof(double *) * (size_t)(N + 1));
+    if (!rows) return -1;
+    for (int64_t li = 0; li < S; ++li) {          /* li = i - 1 */
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t n = 0; n < N; ++n) rows[n] = cache + (n * T + t) * d;
+            int64_t n_src = N;
+            if (li >= 1) { rows[N] = partials + (li * T + t) * d; n_src = N + 1; }
+            if (read_one(rows, n_src, d, queries + li * d, gain, eps,
+                         out + (li * T + t) * d, NULL, NULL)) { free(rows); return -1; }
+        }
+    }
+    free(rows);
+    return 0;
+}
+
+/* Phase 1 of the two-phase schedule, [Summary §3 Inference, Phase 1],
+ * [Review §3-2 4)]: all n_q queries of a block read the N cached block
+ * representations; keeps the softmax state normalised as
+ *   o_q = acc_q / l_q   and   lse_q = m_q + log l_q.
+ * o[n_q][T][d], lse[n_q][T]. */
+int oracle_block_phase1(const double *cache, int64_t N, int64_t T, int64_t d,
+                        const double *queries, int64_t n_q, const double *gain,
+                        double eps, double *o, double *lse)
+{
+    if (!cache || !queries || !o || !lse || N < 1 || n_q < 1 || T < 0 || d < 1 || eps < 0) return -1;
+    for (int64_t q = 0; q < n_q; ++q)
+        if (oracle_full(cache, N, T, d, queries + q * d, gain, eps,
+                        o + q * T * d, lse + q * T, NULL)) return -1;
+    return 0;
+}
+
+/* Phase 2 of the two-phase schedule, [Summary §3 Inference, Phase 2],
+ * [Review §3-2 4) "online softmax merge"]: fold the score of the current
+ * partial sum p into the phase-1 state (o, lse):
+ *   s_p = w^T RMSNorm(p),  M = max(lse, s_p),
+ *   h = (e^{lse-M} o + e^{s_p-M} p) / (e^{lse-M} + e^{s_p-M}).
+ * partial == NULL (first layer of the block) gives h = o. */
+int oracle_block_phase2(const double *o, const double *lse, const double *partial,
+                        int64_t T, int64_t d, const double *query,
+                        const double *gain, double eps, double *out)
+{
+    if (!o || !lse || !query || !out || T < 0 || d < 1 || eps < 0) return -1;
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!tmp) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        const double *ot = o + t * d;
+        if (!partial) { for (int64_t c = 0; c < d; ++c) out[t * d + c] = ot[c]; continue; }
+        const double *pt = partial + t * d;
+        double sp = score(query, pt, gain, d, eps, tmp);
+        double M = lse[t] > sp ? lse[t] : sp;
+        double a = exp(lse[t] - M), b = exp(sp - M);
+        for (int64_t c = 0; c < d; ++c) out[t * d + c] = (a * ot[c] + b * pt[c]) / (a + b);
+    }
+    free(tmp);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* MHAR                                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* Multi-Head Attention Residuals, [MHAR abstract]: the routing query is
+ * reshaped into H heads of d/H; each head has its own softmax over the
+ * depth sources; the read is block-diagonal (head h mixes only channels of
+ * its own slice).  Reading taken: the RMSNorm of the key is taken per head
+ * over the head's slice with the slice of the gain.  queries[n_q][H][d/H],
+ * out[n_q][T][d], lse[n_q][H][T] (may be NULL). */
+int oracle_mhar(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t H,
+                const double *queries, int64_t n_q, const double *gain, double eps,
+                double *out, double *lse)
+{
+    if (!src || !queries || !out || n_src < 1 || T < 0 || d < 1 || H < 1 || d % H || n_q < 1 || eps < 0)
+        return -1;
+    const int64_t dh = d / H;
+    const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_src);
+    double *h = (double *)malloc(sizeof(double) * (size_t)dh);
+    if (!rows || !h) { free(rows); free(h); return -1; }
+    for (int64_t q = 0; q < n_q; ++q)
+        for (int64_t hd = 0; hd < H; ++hd)
+            for (int64_t t = 0; t < T; ++t) {
+                for (int64_t i = 0; i < n_src; ++i) rows[i] = src + (i * T + t) * d + hd * dh;
+                double l;
+                if (read_one(rows, n_src, dh, queries + (q * H + hd) * dh,
+                             gain ? gain + hd * dh : NULL, eps, h, NULL, &l)) {
+                    free(rows); free(h); return -1;
+                }
+                for (int64_t c = 0; c < dh; ++c) out[(q * T + t) * d + hd * dh + c] = h[c];
+                if (lse) lse[(q * H + hd) * T + t] = l;
+            }
+    free(rows); free(h);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* MSAR                                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* Stream expansion, [MSAR §무엇과 다른가]: stream 0 is the identity; stream
+ * r >= 1 is a causal depthwise 1-D convolution along the token axis with
+ * kernel size k_r.  Readings taken: left zero padding, no bias,
+ *   u^(r)[t][c] = sum_{j<k_r} cw_r[c][j] * v[t-j][c]   (v[t<0] = 0).
+ * conv_w packs the m-1 kernels one after the other, kernel r as [d][k_r].
+ * v[T][d] (one source), u[T][d]. */
+int oracle_msar_conv(const double *v, int64_t T, int64_t d, int64_t k,
+                     const double *cw, double *u)
+{
+    if (!v || !cw || !u || T < 0 || d < 1 || k < 1) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < k; ++j)
+                if (t - j >= 0) acc += cw[c * k + j] * v[(t - j) * d + c];
+            u[t * d + c] = acc;
+        }
+    return 0;
+}
+
+/* MSAR read for one target layer, [MSAR §무엇과 다른가]:
+ *   1. every source v_i is expanded into m full-width streams u_i^(r);
+ *   2. each stream r reads the depth history with its own pseudo-query
+ *      w^(r): Z^(r) = sum_i softmax_i(w^(r)T RMSNorm(u_i^(r))) u_i^(r)
+ *      (each stream's weights sum to 1);
+ *   3. H^pre mixer: z = RMSNorm(Flatten(Z)) over m*d (flattened stream-major,
+ *      element r*d + c is Z^(r)[c]); c = sigmoid(z^T P) with P [m*d][m];
+ *      h = sum_r c_r Z^(r).
+ * Readings taken: plain sigmoid, weights not renormalised, no bias.
+ * src[n_src][T][d]; ksizes[m-1]; conv_w packed; queries[m][d]; gain[d] or
+ * NULL; mix_gain[m*d] or NULL; mix_w[m*d][m]; out[T][d].
+ * Optional debug outputs (may be NULL): alpha[T][m][n_src], mixc[T][m]. */
+int oracle_msar(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                const int32_t *ksizes, const double *conv_w, const double *queries,
+                const double *gain, double eps, const double *mix_gain,
+                const double *mix_w, double mix_eps, double *out,
+                double *alpha, double *mixc)
+{
+    if (!src || !ksizes || !conv_w || !queries || !mix_w || !out || n_src < 1 || T < 0 ||
+        d < 1 || m < 1 || eps < 0 || mix_eps < 0) return -1;
+    /* expanded streams u[r][i][T][d] */
+    size_t per = (size_t)T * (size_t)d;
+    double *u = (double *)malloc(sizeof(double) * (size_t)m * (size_t)n_src * per + 1);
+    double *Z = (double *)malloc(sizeof(double) * (size_t)m * (size_t)d + 1);
+    double *zf = (double *)malloc(sizeof(double) * (size_t)m * (size_t)d + 1);
+    const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_src);
+    double *a = (double *)malloc(sizeof(double) * (size_t)n_src);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)m);
+    if (!u || !Z || !zf || !rows || !a || !logit) goto fail;
+    {
+        int64_t off = 0;
+        for (int64_t r = 0; r < m; ++r) {
+            for (int64_t i = 0; i < n_src; ++i) {
+                const double *v = src + (size_t)i * per;
+                double *ur = u + ((size_t)r * (size_t)n_src + (size_t)i) * per;
+                if (r == 0) memcpy(ur, v, sizeof(double) * per);
+                else if (oracle_msar_conv(v, T, d, ksizes[r - 1], conv_w + off, ur)) goto fail;
+            }
+            if (r >= 1) off += d * (int64_t)ksizes[r - 1];
+        }
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t r = 0; r < m; ++r) {
+                for (int64_t i = 0; i < n_src; ++i)
+                    rows[i] = u + ((size_t)r * (size_t)n_src + (size_t)i) * per + (size_t)t * (size_t)d;
+                if (read_one(rows, n_src, d, queries + r * d, gain, eps, Z + r * d, a, NULL)) goto fail;
+                if (alpha) for (int64_t i = 0; i < n_src; ++i) alpha[(t * m + r) * n_src + i] = a[i];
+            }
+            rmsnorm(Z, mix_gain, m * d, mix_eps, zf);
+            for (int64_t o = 0; o < m; ++o) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < m * d; ++k) acc += zf[k] * mix_w[k * m + o];
+                logit[o] = 1.0 / (1.0 + exp(-acc));
+                if (mixc) mixc[t * m + o] = logit[o];
+            }
+            for (int64_t c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int64_t r = 0; r < m; ++r) acc += logit[r] * Z[r * d + c];
+                out[t * d + c] = acc;
+            }
+        }
+    }
+    free(u); free(Z); free(zf); free(rows); free(a); free(logit);
+    return 0;
+fail:
+    free(u); free(Z); free(zf); free(rows); free(a); free(logit);
+    return -1;
+}

@@ -1,0 +1,432 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test fixes the oracle to something other than itself: the values the
+tutorial page prints for its worked example, closed forms, invariants of the
+method, special cases that reduce to another routine, a library routine
+(np.convolve), and brute force against the independently written NumPy twin.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import numpy_twin, oracle
+
+
+def _golden(golden_dir):
+    with open(os.path.join(golden_dir, "worked_example.json")) as f:
+        return json.load(f)
+
+
+def _example_sources(g):
+    # sources [n_src=3, T=1, d=3]
+    return np.asarray(g["sources"], np.float64)[:, None, :]
+
+
+# --------------------------------------------------------------------------
+# worked example (ai-systems-engineering.com tutorial, Figs. 2-3)
+# --------------------------------------------------------------------------
+
+def test_worked_example_alpha_and_h(golden_dir):
+    g = _golden(golden_dir)
+    src = _example_sources(g)
+    w = np.array([0.0, math.log(2.0) / math.sqrt(3.0), 0.0])
+    h, lse, alpha = oracle.full(src, w, None, eps=0.0, want_lse=True, want_alpha=True)
+    assert np.allclose(alpha[0], g["alpha"], atol=1e-12, rtol=0)
+    assert np.allclose(h[0], g["h"], atol=1e-12, rtol=0)
+    # scores [0, ln2, 0] -> sum of exp = 1 + 2 + 1 = 4
+    assert abs(lse[0] - math.log(4.0)) < 1e-12
+
+
+def test_worked_example_padded_to_d8(golden_dir):
+    """The same example padded with zero channels to d=8: every nonzero now
+    normalises to sqrt(8); w = [0, ln2/sqrt(8), 0, ...] gives the same scores,
+    weights and (padded) output.  This is the form the GPU test uses."""
+    g = _golden(golden_dir)
+    src = np.zeros((3, 1, 8))
+    src[:, :, :3] = _example_sources(g)
+    w = np.zeros(8)
+    w[1] = math.log(2.0) / math.sqrt(8.0)
+    h, alpha = oracle.full(src, w, None, eps=0.0, want_alpha=True)
+    assert np.allclose(alpha[0], g["alpha"], atol=1e-12, rtol=0)
+    assert np.allclose(h[0, :3], g["h"], atol=1e-12, rtol=0)
+    assert np.all(h[0, 3:] == 0.0)
+
+
+def test_worked_example_alternative_weights(golden_dir):
+    g = _golden(golden_dir)
+    src = _example_sources(g)
+    h = oracle.weighted_sum(src, np.asarray(g["alternative_alpha"])[None, :])
+    assert np.allclose(h[0], g["alternative_h"], atol=1e-12, rtol=0)
+
+
+def test_equal_scores_give_mean_not_residual_sum(golden_dir):
+    g = _golden(golden_dir)
+    src = _example_sources(g)
+    h, alpha = oracle.full(src, np.zeros(3), None, eps=0.0, want_alpha=True)
+    assert np.allclose(alpha, 1.0 / 3.0, atol=1e-15)
+    assert np.allclose(h[0], np.mean(src[:, 0, :], axis=0), atol=1e-15)
+    assert not np.allclose(h[0], g["residual_sum"])
+
+
+def test_values_are_raw_not_normalised(golden_dir):
+    """A uniform read of the example gives (2/3, 4/3, 2); normalised values
+    would give sqrt(3)/3 on every channel."""
+    g = _golden(golden_dir)
+    h = oracle.full(_example_sources(g), np.zeros(3), None, eps=0.0)
+    assert np.allclose(h[0], [2.0 / 3.0, 4.0 / 3.0, 2.0], atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# closed forms and invariants of the read
+# --------------------------------------------------------------------------
+
+def _rand(rng, *shape, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+def test_zero_query_gives_uniform_weights():
+    """Pseudo-queries start at zero (review 3-2 3), 4-2): uniform alpha, so h is
+    the mean of the sources."""
+    rng = np.random.default_rng(1)
+    src = _rand(rng, 5, 7, 16) * np.arange(1, 6)[:, None, None]
+    h, alpha = oracle.full(src, np.zeros(16), None, eps=1e-6, want_alpha=True)
+    assert np.allclose(alpha, 0.2, atol=1e-15)
+    assert np.allclose(h, src.mean(axis=0), atol=1e-13)
+
+
+def test_weights_sum_to_one_and_are_positive():
+    rng = np.random.default_rng(2)
+    src = _rand(rng, 9, 11, 24, scale=3.0)
+    _, alpha = oracle.full(src, _rand(rng, 24, scale=2.0), None, eps=1e-6, want_alpha=True)
+    assert np.all(alpha > 0)
+    assert np.allclose(alpha.sum(axis=1), 1.0, atol=1e-14)
+
+
+def test_eps_sits_inside_the_square_root():
+    """Constant row x on every channel: mean square x^2, so with eps inside the
+    root the normalised key is x / sqrt(x^2 + eps).  x = sqrt(3), eps = 1 gives
+    sqrt(3)/2 per channel; with w = e_0 * s the score is s*sqrt(3)/2.  Against a
+    zero source (score 0) the weight is sigmoid(s*sqrt(3)/2)."""
+    d = 4
+    src = np.zeros((2, 1, d))
+    src[0, 0, :] = math.sqrt(3.0)
+    w = np.zeros(d)
+    w[0] = 2.0
+    _, alpha = oracle.full(src, w, None, eps=1.0, want_alpha=True)
+    s = 2.0 * math.sqrt(3.0) / 2.0
+    assert abs(alpha[0, 0] - 1.0 / (1.0 + math.exp(-s))) < 1e-14
+
+
+def test_zero_source_with_zero_eps_scores_zero():
+    src = np.zeros((2, 1, 8))
+    src[1, 0, 3] = 5.0
+    w = np.zeros(8)
+    w[3] = 1.0
+    h, alpha = oracle.full(src, w, None, eps=0.0, want_alpha=True)
+    # zero source normalises to 0 -> score 0; the other scores sqrt(8)
+    e = math.exp(math.sqrt(8.0))
+    assert abs(alpha[0, 1] - e / (1.0 + e)) < 1e-14
+    assert np.all(np.isfinite(h))
+
+
+def test_scale_invariance_at_zero_eps():
+    """RMSNorm removes the magnitude of each source from its score."""
+    rng = np.random.default_rng(3)
+    src = _rand(rng, 6, 5, 32)
+    w = _rand(rng, 32)
+    _, a1 = oracle.full(src, w, None, eps=0.0, want_alpha=True)
+    scaled = src * np.array([0.1, 3.0, 7.0, 1.0, 0.5, 100.0])[:, None, None]
+    _, a2 = oracle.full(scaled, w, None, eps=0.0, want_alpha=True)
+    assert np.allclose(a1, a2, atol=1e-13)
+
+
+def test_permutation_equivariance():
+    rng = np.random.default_rng(4)
+    src = _rand(rng, 7, 6, 16)
+    w = _rand(rng, 16)
+    h1, a1 = oracle.full(src, w, None, eps=1e-6, want_alpha=True)
+    perm = rng.permutation(7)
+    h2, a2 = oracle.full(src[perm], w, None, eps=1e-6, want_alpha=True)
+    assert np.allclose(h1, h2, atol=1e-13)
+    assert np.allclose(a1[:, perm], a2, atol=1e-14)
+
+
+def test_gain_acts_on_the_key_like_a_query_scale():
+    """Gain multiplies the normalised key, so gain g equals query w*g with unit
+    gain; a zero gain channel drops out of the score but not out of h."""
+    rng = np.random.default_rng(5)
+    src = _rand(rng, 4, 3, 16)
+    w = _rand(rng, 16)
+    g = rng.uniform(0.5, 2.0, 16)
+    h1 = oracle.full(src, w, g, eps=1e-6)
+    h2 = oracle.full(src, w * g, None, eps=1e-6)
+    assert np.allclose(h1, h2, atol=1e-13)
+    g0 = np.ones(16)
+    g0[5] = 0.0
+    w2 = w.copy()
+    w2[5] = 0.0
+    h3 = oracle.full(src, w, g0, eps=1e-6)
+    h4 = oracle.full(src, w2, None, eps=1e-6)
+    assert np.allclose(h3, h4, atol=1e-13)
+
+
+def test_single_source_returns_it():
+    rng = np.random.default_rng(6)
+    src = _rand(rng, 1, 4, 8)
+    assert np.array_equal(oracle.full(src, _rand(rng, 8), None, eps=1e-6), src[0])
+
+
+# --------------------------------------------------------------------------
+# Block AttnRes
+# --------------------------------------------------------------------------
+
+def test_two_phase_equals_oneshot():
+    """The online-softmax merge of phase 2 is exact (summary section 3; review
+    3-2 4))."""
+    rng = np.random.default_rng(7)
+    N, S, T, d = 5, 4, 6, 24
+    cache = _rand(rng, N, T, d) * (1 + np.arange(N))[:, None, None]
+    partials = _rand(rng, S, T, d)
+    q = _rand(rng, S, d, scale=2.0)
+    g = rng.uniform(0.5, 1.5, d)
+    one = oracle.block_oneshot(cache, partials, q, g, eps=1e-6)
+    two = oracle.block_twophase(cache, partials, q, g, eps=1e-6)
+    assert np.allclose(one, two, atol=1e-13, rtol=0)
+
+
+def test_block_first_layer_reads_no_partial():
+    rng = np.random.default_rng(8)
+    N, S, T, d = 3, 3, 4, 16
+    cache = _rand(rng, N, T, d)
+    partials = _rand(rng, S, T, d)
+    q = _rand(rng, S, d)
+    out = oracle.block_oneshot(cache, partials, q, eps=1e-6)
+    p2 = partials.copy()
+    p2[0] += 100.0
+    out2 = oracle.block_oneshot(cache, p2, q, eps=1e-6)
+    assert np.array_equal(out[0], out2[0])
+    assert np.allclose(out[0], oracle.full(cache, q[0], None, eps=1e-6), atol=1e-14)
+    # later layers do read their partial
+    assert not np.allclose(out[1], oracle.full(cache, q[1], None, eps=1e-6))
+
+
+def test_block_size_one_is_full():
+    """Block size S=1 (N=L blocks) is Full AttnRes (review 5-2 4))."""
+    rng = np.random.default_rng(9)
+    L, T, d = 6, 5, 16
+    v = _rand(rng, L, T, d)
+    w = _rand(rng, d)
+    blk = oracle.block_oneshot(v, None, w[None, :], eps=1e-6)[0]
+    assert np.allclose(blk, oracle.full(v, w, None, eps=1e-6), atol=1e-15)
+
+
+def test_block_shares_one_weight_per_merged_source():
+    """Tutorial Fig. 4: Block keeps e, f1+f2, f3; f1 and f2 share the single
+    weight of their sum, which is not the sum of Full's two weights."""
+    e = np.array([2.0, 0, 0, 0])
+    f1 = np.array([0, 4.0, 0, 0])
+    f2 = np.array([0, 0, 6.0, 0])
+    f3 = np.array([0, 0, 0, 8.0])
+    w = np.array([0.3, 1.2, -0.7, 0.4])
+    full_h, full_a = oracle.full(np.stack([e, f1, f2, f3])[:, None, :], w, None, eps=0.0,
+                                 want_alpha=True)
+    cache = np.stack([e, f1 + f2])[:, None, :]
+    partials = np.stack([np.zeros(4), f3])[:, None, :]
+    blk = oracle.block_oneshot(cache, partials, np.stack([w, w]), None, eps=0.0)[1, 0]
+    beta1 = blk[1] / 4.0
+    beta2 = blk[2] / 6.0
+    assert abs(beta1 - beta2) < 1e-14
+    assert abs(full_h[0, 1] / 4.0 - full_h[0, 2] / 6.0) > 1e-3
+    assert abs(beta1 - (full_a[0, 1] + full_a[0, 2])) > 1e-3
+
+
+def test_phase2_without_partial_is_identity():
+    rng = np.random.default_rng(10)
+    o = _rand(rng, 3, 8)
+    out = oracle.block_phase2(o, _rand(rng, 3), None, _rand(rng, 8))
+    assert np.array_equal(out, o)
+
+
+# --------------------------------------------------------------------------
+# MHAR
+# --------------------------------------------------------------------------
+
+def test_mhar_one_head_is_attnres():
+    rng = np.random.default_rng(11)
+    src = _rand(rng, 5, 4, 32)
+    q = _rand(rng, 3, 1, 32)
+    out = oracle.mhar(src, q, eps=1e-6)
+    for i in range(3):
+        assert np.allclose(out[i], oracle.full(src, q[i, 0], None, eps=1e-6), atol=1e-15)
+
+
+def test_mhar_each_head_is_attnres_on_its_slice():
+    rng = np.random.default_rng(12)
+    H, dh = 4, 8
+    src = _rand(rng, 6, 3, H * dh)
+    q = _rand(rng, 2, H, dh, scale=2.0)
+    g = rng.uniform(0.5, 1.5, H * dh)
+    out, lse = oracle.mhar(src, q, g, eps=1e-6, want_lse=True)
+    for i in range(2):
+        for h in range(H):
+            sl = slice(h * dh, (h + 1) * dh)
+            ref, ref_lse = oracle.full(src[:, :, sl], q[i, h], g[sl], eps=1e-6, want_lse=True)
+            assert np.allclose(out[i, :, sl], ref, atol=1e-15)
+            assert np.allclose(lse[i, h], ref_lse, atol=1e-15)
+
+
+def test_mhar_read_is_block_diagonal():
+    rng = np.random.default_rng(13)
+    H, dh = 4, 8
+    src = _rand(rng, 5, 3, H * dh)
+    q = _rand(rng, 1, H, dh, scale=2.0)
+    base = oracle.mhar(src, q, eps=1e-6)
+    src2 = src.copy()
+    src2[2, :, dh:2 * dh] += _rand(rng, 3, dh, scale=5.0)   # perturb head 1 only
+    pert = oracle.mhar(src2, q, eps=1e-6)
+    changed = np.abs(pert - base).max(axis=(0, 1)) > 0
+    assert np.all(changed[dh:2 * dh])
+    assert not np.any(changed[:dh]) and not np.any(changed[2 * dh:])
+
+
+# --------------------------------------------------------------------------
+# MSAR
+# --------------------------------------------------------------------------
+
+def test_msar_conv_matches_np_convolve():
+    rng = np.random.default_rng(14)
+    T, d, k = 20, 5, 8
+    v = _rand(rng, T, d)
+    cw = _rand(rng, d, k)
+    u = oracle.msar_conv(v, cw)
+    for c in range(d):
+        assert np.allclose(u[:, c], np.convolve(v[:, c], cw[c])[:T], atol=1e-13)
+
+
+def _delta_conv(d, ksizes):
+    parts = []
+    for k in ksizes:
+        cw = np.zeros((d, k))
+        cw[:, 0] = 1.0
+        parts.append(cw.ravel())
+    return np.concatenate(parts)
+
+
+def test_msar_delta_conv_and_zero_mixer_is_two_attnres():
+    """Delta kernels make every stream the source itself; one shared query
+    makes every stream read Full AttnRes A; a zero projection gives sigmoid(0)
+    = 1/2 per stream, so h = (m/2) A = 2A for m = 4."""
+    rng = np.random.default_rng(15)
+    N, T, d = 5, 9, 16
+    ks = (4, 8, 12)
+    src = _rand(rng, N, T, d)
+    w = _rand(rng, d, scale=2.0)
+    h = oracle.msar(src, ks, _delta_conv(d, ks), np.stack([w] * 4), None, 1e-6, None,
+                    np.zeros((4 * d, 4)), 1e-6)
+    assert np.allclose(h, 2.0 * oracle.full(src, w, None, eps=1e-6), atol=1e-13)
+
+
+def test_msar_mixer_single_projection_entry_and_flatten_order():
+    """Zero conv kernels make streams 1..3 zero, so Flatten(Z) = [A, 0, 0, 0]
+    whose RMS over 4d is rms(A)/2.  A single projection entry beta at row 1
+    (stream 0, channel 1), column 0 gives c_0 = sigmoid(2 A[1] beta / rms(A))
+    and h = c_0 A.  The same entry at row d (stream 1, channel 0) sees a zero
+    and gives h = A/2; a channel-major flatten would swap these two cases."""
+    rng = np.random.default_rng(16)
+    N, T, d = 4, 6, 8
+    ks = (4, 8, 12)
+    src = _rand(rng, N, T, d)
+    q = _rand(rng, 4, d, scale=2.0)
+    cw = np.zeros(d * sum(ks))
+    A = oracle.full(src, q[0], None, eps=0.0)
+    beta = 1.7
+    P = np.zeros((4 * d, 4))
+    P[1, 0] = beta
+    h = oracle.msar(src, ks, cw, q, None, 0.0, None, P, 0.0)
+    rmsA = np.sqrt(np.mean(A * A, axis=1))
+    c0 = 1.0 / (1.0 + np.exp(-2.0 * A[:, 1] * beta / rmsA))
+    assert np.allclose(h, c0[:, None] * A, atol=1e-13)
+    P = np.zeros((4 * d, 4))
+    P[d, 0] = beta
+    h = oracle.msar(src, ks, cw, q, None, 0.0, None, P, 0.0)
+    assert np.allclose(h, 0.5 * A, atol=1e-13)
+
+
+def test_msar_stream_weights_sum_to_one():
+    rng = np.random.default_rng(17)
+    N, T, d = 6, 7, 16
+    ks = (4, 8, 12)
+    src = _rand(rng, N, T, d)
+    _, alpha, mixc = oracle.msar(src, ks, _rand(rng, d * sum(ks), scale=0.4),
+                                 _rand(rng, 4, d, scale=2.0), None, 1e-6, None,
+                                 _rand(rng, 4 * d, 4, scale=0.2), 1e-6, want_debug=True)
+    assert np.allclose(alpha.sum(axis=2), 1.0, atol=1e-14)
+    assert np.all((mixc > 0) & (mixc < 1))
+
+
+def test_msar_is_causal_with_window_twelve():
+    rng = np.random.default_rng(18)
+    N, T, d = 3, 30, 8
+    ks = (4, 8, 12)
+    src = _rand(rng, N, T, d)
+    args = (ks, _rand(rng, d * sum(ks), scale=0.4), _rand(rng, 4, d, scale=2.0), None, 1e-6,
+            None, _rand(rng, 4 * d, 4, scale=0.2), 1e-6)
+    base = oracle.msar(src, *args)
+    t = 20
+    for tp, should_change in ((t + 1, False), (t - 12, False), (t - 11, True), (t, True)):
+        s2 = src.copy()
+        s2[1, tp] += 3.0
+        h = oracle.msar(s2, *args)
+        assert (np.abs(h[t] - base[t]).max() > 0) == should_change, tp
+
+
+def test_msar_window_read_equals_full_sequence():
+    """Tokens of a 12-row window ending at t reproduce row t of the full
+    causal sequence; this is how sampled full-size checks are computed."""
+    rng = np.random.default_rng(19)
+    N, T, d = 3, 40, 8
+    ks = (4, 8, 12)
+    src = _rand(rng, N, T, d)
+    args = (ks, _rand(rng, d * sum(ks), scale=0.4), _rand(rng, 4, d, scale=2.0), None, 1e-6,
+            None, _rand(rng, 4 * d, 4, scale=0.2), 1e-6)
+    base = oracle.msar(src, *args)
+    for t in (0, 5, 11, 12, 39):
+        lo = max(0, t - 11)
+        win = oracle.msar(src[:, lo:t + 1], *args)
+        assert np.allclose(win[-1], base[t], atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# brute force: C oracle vs the NumPy twin on tiny shapes
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(4))
+def test_brute_force_against_numpy_twin(seed):
+    rng = np.random.default_rng(100 + seed)
+    n_src, T, d = rng.integers(1, 5), rng.integers(1, 5), int(rng.choice([4, 8, 16]))
+    src = _rand(rng, n_src, T, d, scale=2.0)
+    w = _rand(rng, d, scale=2.0)
+    g = rng.uniform(0.5, 1.5, d)
+    assert np.allclose(oracle.full(src, w, g, 1e-3), numpy_twin.full(src, w, g, 1e-3),
+                       atol=1e-12, rtol=0)
+    N, S = rng.integers(1, 4), rng.integers(1, 4)
+    cache = _rand(rng, N, T, d)
+    partials = _rand(rng, S, T, d)
+    q = _rand(rng, S, d, scale=2.0)
+    assert np.allclose(oracle.block_oneshot(cache, partials, q, g, 1e-6),
+                       numpy_twin.block_oneshot(cache, partials, q, g, 1e-6), atol=1e-12, rtol=0)
+    H = int(rng.choice([1, 2, 4]))
+    qh = _rand(rng, 2, H, d // H, scale=2.0)
+    assert np.allclose(oracle.mhar(src, qh, g, 1e-6), numpy_twin.mhar(src, qh, g, 1e-6),
+                       atol=1e-12, rtol=0)
+    ks = (2, 3, 5)
+    cw = _rand(rng, d * sum(ks), scale=0.5)
+    qm = _rand(rng, 4, d, scale=2.0)
+    P = _rand(rng, 4 * d, 4, scale=0.3)
+    mg = rng.uniform(0.5, 1.5, 4 * d)
+    a = oracle.msar(src, ks, cw, qm, g, 1e-6, mg, P, 1e-5)
+    b = numpy_twin.msar(src, ks, cw, qm, g, 1e-6, mg, P, 1e-5)
+    assert np.allclose(a, b, atol=1e-12, rtol=0)

@@ -1,0 +1,56 @@
+"""Mutation check of the oracle pins (CPU only).
+
+Each case plants one plausible mistake in a private copy of the C oracle
+(a dropped term, a wrong sign, a wrong or transposed index), builds it, and
+runs the pin suite against it in a subprocess: every mutant must make at
+least one pin fail.  The real oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "attnres_oracle.c")
+
+MUTANTS = {
+    "mean_square_not_divided_by_n": [("    ms /= (double)n;\n", "")],
+    "eps_outside_sqrt": [("sqrt(ms + eps)", "(sqrt(ms) + eps)")],
+    "softmax_sign": [("alpha[i] = exp(s[i] - m)", "alpha[i] = exp(m - s[i])")],
+    "first_source_dropped_from_sum": [
+        ("for (int64_t i = 0; i < n_src; ++i) acc += a[i] * rows[i][c];",
+         "for (int64_t i = 1; i < n_src; ++i) acc += a[i] * rows[i][c];")],
+    "gain_ignored": [("double gc = g ? g[c] : 1.0;", "double gc = 1.0;")],
+    "lse_drops_max": [("return m + log(l);", "return log(l);")],
+    "merge_sign": [("b = exp(sp - M);", "b = exp(M - sp);")],
+    "first_layer_reads_partial": [("if (li >= 1) { rows[N]", "if (li >= 0) { rows[N]")],
+    "mhar_query_transposed": [("queries + (q * H + hd) * dh", "queries + (hd * n_q + q) * dh")],
+    "conv_kernel_reversed": [("acc += cw[c * k + j] * v[(t - j) * d + c];",
+                              "acc += cw[c * k + (k - 1 - j)] * v[(t - j) * d + c];")],
+    "conv_anticausal": [("if (t - j >= 0) acc += cw[c * k + j] * v[(t - j) * d + c];",
+                         "if (t + j < T) acc += cw[c * k + j] * v[(t + j) * d + c];")],
+    "flatten_channel_major": [("acc += zf[k] * mix_w[k * m + o];",
+                               "acc += zf[k] * mix_w[((k % d) * m + k / d) * m + o];")],
+    "sigmoid_sign": [("logit[o] = 1.0 / (1.0 + exp(-acc));", "logit[o] = 1.0 / (1.0 + exp(acc));")],
+    "mixer_wrong_stream_weight": [("acc += logit[r] * Z[r * d + c];",
+                                   "acc += logit[0] * Z[r * d + c];")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    src = open(SRC).read()
+    for old, new in MUTANTS[name]:
+        assert src.count(old) == 1, (name, old)
+        src = src.replace(old, new)
+    c = tmp_path / "mutant.c"
+    c.write_text(src)
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-o", str(so), str(c), "-lm"])
+    env = dict(os.environ, ATTNRES_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
