@@ -1,0 +1,674 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the depth-wise softmax read on GB300.
+
+Default workload (the headline): Block AttnRes two-phase forward of one block,
+bf16, d=4096, N=8 cached block representations, S=4 layers per block,
+T=32768 tokens.  One step = phase 1 (4 queries x 8 sources, one pass over the
+cache) + 3 phase-2 merges (layers 2..4 fold in their partial sums; layer 1
+reads no partial).  Inputs are synthetic, seeded, resident in HBM and larger
+than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
+same workload instead.  Other workloads (--workload mhar|msar|full_depth|
+block_d2048) are for profiling and the design notes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Block AttnRes fwd tokens/s (d=4096,N=8,S=4); achieved HBM GB/s vs GB300 peak"
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["depth_wise_attention_gb300/csrc/depth_read.cuh",
+                  "depth_wise_attention_gb300/csrc/common.cuh",
+                  "depth_wise_attention_gb300/csrc/phase2.cuh",
+                  "depth_wise_attention_gb300/csrc/msar.cu",
+                  "depth_wise_attention_gb300/csrc/attnres_api.cu"]
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def profile_traffic(kernel_tag: str):
+    """dram bytes per launch of `kernel_tag` from the committed ncu summary, if
+    it was taken on the current kernel sources (else None)."""
+    path = os.path.join(PROFILE_DIR, f"{kernel_tag}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_sources_sha") != kernel_sources_sha():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# workloads
+# --------------------------------------------------------------------------
+
+class BlockWorkload:
+    """Block AttnRes two-phase forward of one block: phase 1 + (S-1) merges."""
+
+    def __init__(self, T=32768, d=4096, N=8, S=4, seed=0, name="block_attnres_two_phase"):
+        self.T, self.d, self.N, self.S, self.seed, self.name = T, d, N, S, seed, name
+        b = 2
+        self.phase1_bytes_per_token = N * d * b + S * d * b + S * 4
+        self.merge_bytes_per_token = 3 * d * b + 4
+        self.bytes_per_token = self.phase1_bytes_per_token + (S - 1) * self.merge_bytes_per_token
+        self.launches_per_step = 1 + (S - 1)
+        self.dominant = "depth_read_kernel (phase 1)"
+        self.profile_tag = f"ncu_phase1_block_d{d}"
+
+    def config(self):
+        return {"workload": f"{self.name} bf16 d={self.d} N={self.N} S={self.S} T={self.T}",
+                "T": self.T, "d": self.d, "N": self.N, "S": self.S, "dtype_sources": "bf16",
+                "queries": "fp32", "l2": "inputs larger than L2 (no flush)",
+                "bytes_per_token": self.bytes_per_token}
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        T, d, N, S = self.T, self.d, self.N, self.S
+        self.cache, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=self.seed,
+                                              device=device)
+        self.cache = self.cache.view(N, T, d)
+        self.queries = inputs.device_normal((S, d), (16.0 / d) ** 0.5, g, device=device)
+        self.partials = torch.empty((S, T, d), dtype=torch.bfloat16, device=device)
+        for i in range(S):
+            self.partials[i].copy_(torch.randn((T, d), generator=g, device=device))
+        self.o = torch.empty((S, T, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((S, T), dtype=torch.float32, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.attnres_block_phase1(self.cache, self.queries, None, 1e-6, o=self.o, lse=self.lse,
+                                     stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for i in range(1, self.S):
+            attnres.attnres_block_phase2_merge(self.o[i], self.lse[i], self.partials[i],
+                                               self.queries[i], None, 1e-6, out=self.o[i],
+                                               stream=stream)
+
+    def dominant_bytes_per_launch(self):
+        return self.T * self.phase1_bytes_per_token
+
+    # ---- end to end through the C ABI with host buffers
+    def setup_host(self):
+        import torch
+        self.h_cache = torch.empty(self.cache.shape, dtype=self.cache.dtype, pin_memory=True)
+        self.h_cache.copy_(self.cache)
+        self.h_parts = torch.empty((self.S - 1,) + tuple(self.partials.shape[1:]),
+                                   dtype=self.partials.dtype, pin_memory=True)
+        self.h_parts.copy_(self.partials[1:])
+        self.h_q = self.queries.cpu().pin_memory()
+        self.h_out = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
+        self.h2d = (self.h_cache.numel() + self.h_parts.numel()) * 2 + self.h_q.numel() * 4
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.partials[1:].copy_(self.h_parts, non_blocking=True)
+        self.queries.copy_(self.h_q, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.o, non_blocking=True)
+
+    # ---- oracle on a sample of tokens
+    def oracle_sample(self, n_tokens, seed=1):
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        import torch
+        it = torch.from_numpy(idx).to(self.cache.device)
+        cache = self.cache[:, it, :].float().cpu().numpy().astype(np.float64)
+        parts = self.partials[:, it, :].float().cpu().numpy().astype(np.float64)
+        q = self.queries.cpu().numpy().astype(np.float64)
+        return cache, parts, q
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        cache, parts, q = sample
+        oracle.block_twophase(cache, parts, q, None, 1e-6)
+        return cache.shape[1]
+
+
+class MharWorkload(BlockWorkload):
+    """MHAR read: S=4 queries x H=8 heads over N=8 block reps (no phase 2)."""
+
+    def __init__(self, T=131072, d=4096, N=8, S=4, H=8, seed=0):
+        super().__init__(T, d, N, S, seed, name="mhar_block_diagonal_read")
+        self.H = H
+        self.bytes_per_token = N * d * 2 + S * d * 2
+        self.phase1_bytes_per_token = self.bytes_per_token
+        self.launches_per_step = 1
+        self.dominant = "depth_read_kernel (MHAR)"
+        self.profile_tag = f"ncu_mhar_d{d}_H{H}"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} H={self.H} N={self.N} S={self.S} T={self.T}"
+        c["H"] = self.H
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        T, d, N, S, H = self.T, self.d, self.N, self.S, self.H
+        self.cache, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=self.seed,
+                                              device=device)
+        self.cache = self.cache.view(N, T, d)
+        self.queries = inputs.device_normal((S, H, d // H), (16.0 / (d // H)) ** 0.5, g, device=device)
+        self.o = torch.empty((S, T, d), dtype=torch.bfloat16, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.mhar_fwd(self.cache, self.queries, None, 1e-6, out=self.o, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def setup_host(self):
+        import torch
+        self.h_cache = torch.empty(self.cache.shape, dtype=self.cache.dtype, pin_memory=True)
+        self.h_cache.copy_(self.cache)
+        self.h_q = self.queries.cpu().pin_memory()
+        self.h_out = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
+        self.h2d = self.h_cache.numel() * 2 + self.h_q.numel() * 4
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.queries.copy_(self.h_q, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.o, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        import torch
+        it = torch.from_numpy(idx).to(self.cache.device)
+        return (self.cache[:, it, :].float().cpu().numpy().astype(np.float64),
+                self.queries.cpu().numpy().astype(np.float64))
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        src, q = sample
+        oracle.mhar(src, q, None, 1e-6)
+        return src.shape[1]
+
+
+class MsarWorkload(BlockWorkload):
+    """MSAR fused stream expansion + per-stream read + H^pre mixer."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0):
+        super().__init__(T, d, N, 4, seed, name="msar_fused_read")
+        self.ks = (4, 8, 12)
+        self.bytes_per_token = N * d * 2 + d * 2
+        self.phase1_bytes_per_token = self.bytes_per_token
+        self.launches_per_step = 1
+        self.dominant = "msar_kernel"
+        self.profile_tag = f"ncu_msar_d{d}"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} N={self.N} m=4 k=4/8/12 T={self.T}"
+        c.pop("S", None)
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        T, d, N = self.T, self.d, self.N
+        self.cache, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=self.seed,
+                                              device=device)
+        self.cache = self.cache.view(N, T, d)
+        self.queries = inputs.device_normal((4, d), (16.0 / d) ** 0.5, g, device=device)
+        self.conv_w = torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g, device=device)
+                                 for k in self.ks])
+        self.mix_w = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g, device=device)
+        self.out = torch.empty((T, d), dtype=torch.bfloat16, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.msar_expand_fwd(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, None,
+                                self.mix_w, 1e-6, out=self.out, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def setup_host(self):
+        import torch
+        self.h_cache = torch.empty(self.cache.shape, dtype=self.cache.dtype, pin_memory=True)
+        self.h_cache.copy_(self.cache)
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        self.h2d = self.h_cache.numel() * 2
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        # windows of 12 rows ending at each sampled token (the causal receptive field)
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        wins = []
+        for t in idx:
+            lo = max(0, int(t) - 11)
+            wins.append(self.cache[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64))
+        return (wins, self.conv_w.cpu().numpy().astype(np.float64),
+                self.queries.cpu().numpy().astype(np.float64),
+                self.mix_w.cpu().numpy().astype(np.float64))
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        wins, cw, q, mw = sample
+        for w in wins:
+            oracle.msar(w, self.ks, cw, q, None, 1e-6, None, mw, 1e-6)
+        return len(wins)
+
+
+class FullDepthWorkload(BlockWorkload):
+    """Full AttnRes at depth: 64 layers, layer l reads sources 0..l-1."""
+
+    def __init__(self, T=16384, d=4096, L=64, seed=0):
+        super().__init__(T, d, 8, 4, seed, name="full_attnres_depth")
+        self.L = L
+        self.bytes_per_token = sum((l + 1) * d * 2 for l in range(1, L + 1))
+        self.phase1_bytes_per_token = (L + 1) * d * 2           # the deepest layer's read
+        self.launches_per_step = L
+        self.dominant = "depth_read_kernel (Full, layer 64)"
+        self.profile_tag = f"ncu_full_depth_d{d}"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} L={self.L} T={self.T}"
+        c.pop("S", None)
+        c.pop("N", None)
+        c["L"] = self.L
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        T, d, L = self.T, self.d, self.L
+        self.cache, g = inputs.device_sources(L, T, d, lambda i: 1.0 + i / 16.0, seed=self.seed,
+                                              device=device)
+        self.cache = self.cache.view(L, T, d)
+        self.queries = inputs.device_normal((L, d), (16.0 / d) ** 0.5, g, device=device)
+        self.out = torch.empty((T, d), dtype=torch.bfloat16, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        for l in range(1, self.L + 1):
+            if ev is not None and l == self.L:
+                ev[0].record(stream)
+            attnres.attnres_full_fwd(self.cache[:l], self.queries[l - 1], None, 1e-6, out=self.out,
+                                     stream=stream)
+            if ev is not None and l == self.L:
+                ev[1].record(stream)
+
+    def setup_host(self):
+        import torch
+        self.h_cache = torch.empty(self.cache.shape, dtype=self.cache.dtype, pin_memory=True)
+        self.h_cache.copy_(self.cache)
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        self.h2d = self.h_cache.numel() * 2
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        import torch
+        it = torch.from_numpy(idx).to(self.cache.device)
+        return (self.cache[:, it, :].float().cpu().numpy().astype(np.float64),
+                self.queries.cpu().numpy().astype(np.float64))
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        src, q = sample
+        for l in range(1, self.L + 1):
+            oracle.full(src[:l], q[l - 1], None, 1e-6)
+        return src.shape[1]
+
+
+def make_workload(name, T=None):
+    if name == "block":
+        return BlockWorkload(T=T or 32768)
+    if name == "block_d2048":
+        return BlockWorkload(T=T or 8192, d=2048)
+    if name == "mhar":
+        return MharWorkload(T=T or 131072)
+    if name == "msar":
+        return MsarWorkload(T=T or 32768)
+    if name == "full_depth":
+        return FullDepthWorkload(T=T or 16384)
+    raise SystemExit(f"unknown workload {name}")
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no data-path collective)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Max of a scalar over all ranks (timing only)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def run_cuda(args):
+    import torch
+    from depth_wise_attention_gb300 import attnres
+    from depth_wise_attention_gb300.build import build
+
+    world, rank, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    if rank == 0:
+        build()
+    barrier(world)
+    attnres.load()
+
+    wl = make_workload(args.workload, args.T)
+    wl.setup(device)
+    stream = torch.cuda.current_stream(device)
+    torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        wl.step(stream)
+    attnres.attnres_sync_status(stream)
+
+    # ---------------- timed region: K steps, events around the dominant kernel
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        start.record(stream)
+        for k in range(K):
+            wl.step(stream, evs[k])
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+    attnres.attnres_sync_status(stream)
+    elapsed_ms = start.elapsed_time(end)
+    dom_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
+
+    tokens = wl.T * K * world
+    value = tokens / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / K
+    peaks, peaks_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    dom_bytes = wl.dominant_bytes_per_launch()
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    step_gbs = wl.bytes_per_token * wl.T / (ms_per_step / 1e3) / 1e9
+    traffic = profile_traffic(wl.profile_tag)
+
+    # ---------------- end to end: host buffers, copies inside the timed region
+    wl.setup_host()
+    E = max(3, min(K, args.e2e_steps))
+    for _ in range(2):
+        wl.step_e2e(stream)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        wl.step_e2e(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    attnres.attnres_sync_status(stream)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    e2e_value = wl.T * E * world / (e2e_ms / 1e3)
+
+    # ---------------- CPU oracle baseline (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC if args.workload == "block" else f"{wl.name} tokens/s",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": dict(wl.config(), parallelism=f"replicas x{world} (no collective)"),
+        "hbm_gbs_step": step_gbs,
+        "hbm_frac_step": step_gbs / hbm_peak,
+        "roofline": {"kernel": wl.dominant, "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "peak_kind": peaks_kind, "unit": "GB/s",
+                     "frac": achieved / hbm_peak,
+                     "bytes_per_launch": dom_bytes, "ms_per_launch": dom_ms,
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": E,
+                "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h},
+        "gpu_launches": wl.launches_per_step * K,
+        "clocks": clk.summary(),
+        "library": attnres.version(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, seconds):
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    probe = wl.oracle_sample(4, seed=2)
+    t0 = time.perf_counter()
+    wl.run_oracle(probe)
+    per_tok = (time.perf_counter() - t0) / 4
+    n = int(max(8, min(wl.T, seconds / max(per_tok, 1e-6))))
+    sample = wl.oracle_sample(n, seed=1)
+    t0 = time.perf_counter()
+    done = wl.run_oracle(sample)
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} tokens drawn with seed 1 from the same inputs "
+                      f"({dt:.1f} s, single-threaded C oracle, float64)"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the same workload, metric and unit."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    torch.cuda.set_device(0)
+    wl = make_workload(args.workload, args.T)
+    wl.setup(torch.device("cuda", 0))
+    probe = wl.oracle_sample(4, seed=2)
+    t0 = time.perf_counter()
+    wl.run_oracle(probe)
+    per_tok = (time.perf_counter() - t0) / 4
+    budget = args.cpu_seconds * 4
+    per_step = int(max(1, min(wl.T, budget / max(per_tok, 1e-6) / max(1, args.steps + args.warmup))))
+    samples = [wl.oracle_sample(per_step, seed=10 + k) for k in range(args.steps + args.warmup)]
+    for k in range(args.warmup):
+        wl.run_oracle(samples[k])
+    t0 = time.perf_counter()
+    done = 0
+    for k in range(args.steps):
+        done += wl.run_oracle(samples[args.warmup + k])
+    dt = time.perf_counter() - t0
+    value = done / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC if args.workload == "block" else f"{wl.name} tokens/s",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same inputs as the CUDA arm)",
+        "config": dict(wl.config(), parallelism="CPU oracle, rank 0 only"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} tokens per step, seeds 10.., single-threaded"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workload", default="block",
+                    choices=["block", "block_d2048", "mhar", "msar", "full_depth"])
+    ap.add_argument("--T", type=int, default=None, help="override the token count")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+"""Thin ctypes binding of libattnres.so (C ABI in include/attnres.h).
+
+Argument marshalling only: every step of the read runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (torch supplies device memory and the
+current stream); each function has the name of the C entry point it calls and
+raises ``AttnResError`` when the call does not return ATTNRES_OK.  There is no
+fallback: if the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattnres.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "attnres.h")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(5)
+F32, BF16 = 0, 1
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+_SIGS = {
+    "attnres_full_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _f, _vp, _vp],
+    "attnres_block_phase1": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp,
+                             _vp, _vp],
+    "attnres_block_phase2_merge": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp, _f, _vp, _vp],
+    "mhar_fwd": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp,
+                 _vp],
+    "msar_expand_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
+                        _vp, _vp, _f, _vp, _vp],
+    "attnres_status_string": [ctypes.c_int],
+    "attnres_last_cuda_error": [],
+    "attnres_sync_status": [_vp],
+    "attnres_debug_set_wait_timeout_ns": [ctypes.c_uint64],
+    "attnres_debug_set_stall_injection": [ctypes.c_int],
+    "attnres_version": [],
+}
+_RESTYPES = {"attnres_status_string": ctypes.c_char_p, "attnres_last_cuda_error": ctypes.c_char_p,
+             "attnres_version": ctypes.c_char_p, "attnres_debug_set_wait_timeout_ns": None,
+             "attnres_debug_set_stall_injection": None}
+
+
+class AttnResError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = f"{fn}: {status_string(status)}"
+        if status == ERR_CUDA:
+            msg += f" ({last_cuda_error()})"
+        super().__init__(msg)
+
+
+def load(path: str = LIB_PATH):
+    """Load libattnres.so (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m depth_wise_attention_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, args in _SIGS.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = _RESTYPES.get(name, ctypes.c_int)
+        _lib = lib
+    return _lib
+
+
+def header_functions(header: str = HEADER):
+    """Names of the functions declared in include/attnres.h."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", text)) - {"defined"})
+
+
+def status_string(status: int) -> str:
+    return load().attnres_status_string(status).decode()
+
+
+def last_cuda_error() -> str:
+    return load().attnres_last_cuda_error().decode()
+
+
+def version() -> str:
+    return load().attnres_version().decode()
+
+
+def _dt(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _p(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return _vp(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != OK:
+        raise AttnResError(fn, status)
+
+
+def _src_geometry(src):
+    """src [n_src, T, d]: each source contiguous, sources src.stride(0) apart."""
+    n_src, T, d = src.shape
+    if src.stride(2) != 1 or src.stride(1) != d:
+        raise ValueError("each source must be a contiguous [T, d] block")
+    return n_src, T, d, src.stride(0)
+
+
+def attnres_full_fwd(src, query, gain=None, eps=1e-6, out=None, stream=None):
+    """Full AttnRes read of one layer: src [n_src,T,d] -> out [T,d]."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    if out is None:
+        out = torch.empty((T, d), dtype=src.dtype, device=src.device)
+    _check("attnres_full_fwd", load().attnres_full_fwd(
+        _p(src), n_src, stride, T, d, _dt(src), _p(query), _p(gain), eps, _p(out), _stream(stream)))
+    return out
+
+
+def attnres_block_phase1(src, queries, gain=None, eps=1e-6, o=None, lse=None, want_lse=True,
+                         stream=None):
+    """Phase 1: queries [n_q,d] against src [n_src,T,d] -> (o [n_q,T,d], lse [n_q,T])."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    n_q = queries.shape[0]
+    if o is None:
+        o = torch.empty((n_q, T, d), dtype=src.dtype, device=src.device)
+    if lse is None and want_lse:
+        lse = torch.empty((n_q, T), dtype=torch.float32, device=src.device)
+    _check("attnres_block_phase1", load().attnres_block_phase1(
+        _p(src), n_src, stride, T, d, _dt(src), _p(queries), n_q, _p(gain), eps, _p(o), _p(lse),
+        _stream(stream)))
+    return o, lse
+
+
+def attnres_block_phase2_merge(o, lse, partial, query, gain=None, eps=1e-6, out=None, stream=None):
+    """Phase 2: merge partial [T,d] (or None) into (o [T,d], lse [T]) -> out [T,d]."""
+    import torch
+    T, d = o.shape
+    if out is None:
+        out = torch.empty_like(o)
+    _check("attnres_block_phase2_merge", load().attnres_block_phase2_merge(
+        _p(o), _p(lse), _p(partial), T, d, _dt(o), _p(query), _p(gain), eps, _p(out),
+        _stream(stream)))
+    return out
+
+
+def mhar_fwd(src, queries, gain=None, eps=1e-6, out=None, lse=None, want_lse=False, stream=None):
+    """MHAR: queries [n_q,H,d/H] -> out [n_q,T,d] (lse [n_q,H,T])."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    n_q, H, _ = queries.shape
+    if out is None:
+        out = torch.empty((n_q, T, d), dtype=src.dtype, device=src.device)
+    if lse is None and want_lse:
+        lse = torch.empty((n_q, H, T), dtype=torch.float32, device=src.device)
+    _check("mhar_fwd", load().mhar_fwd(
+        _p(src), n_src, stride, T, d, H, _dt(src), _p(queries), n_q, _p(gain), eps, _p(out), _p(lse),
+        _stream(stream)))
+    return (out, lse) if want_lse else out
+
+
+def msar_expand_fwd(src, ksizes, conv_w, queries, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                    mix_eps=1e-6, out=None, stream=None):
+    """MSAR: src [n_src,T,d], ksizes (m-1 ints, host), conv_w packed, queries [m,d],
+    mix_w [m*d,m] -> out [T,d]."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    m = queries.shape[0]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if out is None:
+        out = torch.empty((T, d), dtype=src.dtype, device=src.device)
+    _check("msar_expand_fwd", load().msar_expand_fwd(
+        _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries),
+        _p(gain), eps, _p(mix_gain), _p(mix_w), mix_eps, _p(out), _stream(stream)))
+    return out
+
+
+def attnres_sync_status(stream=None):
+    """Wait for the stream and raise if a kernel recorded a device-side timeout."""
+    _check("attnres_sync_status", load().attnres_sync_status(_stream(stream)))
+
+
+def attnres_debug_set_wait_timeout_ns(ns: int):
+    load().attnres_debug_set_wait_timeout_ns(int(ns))
+
+
+def attnres_debug_set_stall_injection(enable: bool):
+    load().attnres_debug_set_stall_injection(1 if enable else 0)

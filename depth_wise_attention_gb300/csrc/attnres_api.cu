@@ -1,0 +1,416 @@
+// attnres_api.cu -- host side of the C ABI declared in include/attnres.h:
+// argument validation, launch-shape selection and kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attnres.h"
+#include "common.cuh"
+#include "depth_read.cuh"
+#include "dispatch.h"
+#include "msar.h"
+#include "phase2.cuh"
+
+using namespace attnres;
+
+// Device status word: kernels OR DEV_ERR_* bits into it after a wait ran out.
+__device__ int g_attnres_status = 0;
+
+namespace {
+
+thread_local char t_last_err[256] = "";
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_inject_stall{0};
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kStageMaxBytes = 64 * 1024;        // one ring stage
+constexpr size_t kSmemBudget = 200 * 1024;         // stages + aux, per CTA
+
+struct DeviceInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sms = 0;
+    int smem_optin = 0;
+    int *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+attnres_status_t cuda_fail(cudaError_t e, const char *what) {
+    snprintf(t_last_err, sizeof(t_last_err), "%s: %s (%s)", what, cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return ATTNRES_ERR_CUDA;
+}
+
+// Per-device constants: SM count, shared-memory limit, status word address.
+attnres_status_t device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo &d = g_dev[dev];
+    std::call_once(d.once, [&] {
+        d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess)
+            d.err = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (d.err == cudaSuccess)
+            d.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_attnres_status);
+    });
+    if (d.err != cudaSuccess) return cuda_fail(d.err, "device query");
+    *out = &d;
+    return ATTNRES_OK;
+}
+
+WaitCfg wait_cfg(DeviceInfo *d) {
+    WaitCfg w;
+    w.status = d->status;
+    w.timeout_ns = g_timeout_ns.load();
+    w.inject_stall = g_inject_stall.load();
+    return w;
+}
+
+// Kernel attributes are set once per (function, device).
+struct FnCache {
+    std::mutex mu;
+    struct Entry { const void *fn; int dev; size_t smem; int occ; };
+    Entry e[512];
+    int n = 0;
+} g_fn_cache;
+
+attnres_status_t prepare_kernel(const void *fn, size_t smem, int threads, int *occ) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_fn_cache.mu);
+    for (int i = 0; i < g_fn_cache.n; ++i) {
+        auto &c = g_fn_cache.e[i];
+        if (c.fn == fn && c.dev == dev && c.smem >= smem) { *occ = c.occ; return ATTNRES_OK; }
+    }
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    }
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, threads, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (o < 1) return ATTNRES_ERR_UNSUPPORTED;
+    if (g_fn_cache.n < 512) g_fn_cache.e[g_fn_cache.n++] = {fn, dev, smem, o};
+    *occ = o;
+    return ATTNRES_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+size_t esize(attnres_dtype_t dt) { return dt == ATTNRES_BF16 ? 2 : 4; }
+int epv(attnres_dtype_t dt) { return dt == ATTNRES_BF16 ? 8 : 4; }
+
+// [a, a+na) and [b, b+nb) overlap (bytes)
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int pow2ceil(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+// Threads per token row and vectors per thread for a row of nvec vectors.
+void row_shape(int nvec, int *tpr, int *vpt) {
+    int t = pow2ceil((nvec + 1) / 2);
+    if (t < 32) t = 32;
+    if (t > 256) t = 256;
+    *tpr = t;
+    *vpt = pow2ceil((nvec + t - 1) / t);
+}
+
+attnres_status_t check_common(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                              int64_t d, attnres_dtype_t dt, float eps) {
+    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
+    if (n_src < 1 || T < 0 || d < 1 || !(eps >= 0.f) || std::isinf(eps)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && !src) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    if (src_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+    if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(src) || (src_stride * (int64_t)esize(dt)) % 16 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    if (n_src > (int64_t)1 << 30 || d > (int64_t)1 << 20) return ATTNRES_ERR_UNSUPPORTED;
+    return ATTNRES_OK;
+}
+
+// Shared launch path of Full / phase 1 / MHAR.
+attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                   int64_t d, int64_t H, attnres_dtype_t dt, const float *queries,
+                                   int64_t n_q, const float *gain, float eps, void *out, float *lse,
+                                   void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (n_q < 1 || H < 1 || d % H != 0) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!queries || !out)) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t out_bytes = (size_t)n_q * (size_t)T * (size_t)d * es;
+    if (overlap(out, out_bytes, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (lse && overlap(lse, (size_t)n_q * H * T * 4, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (lse && overlap(lse, (size_t)n_q * H * T * 4, out, out_bytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (n_q > 8) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(queries) || (gain && !aligned16(gain)) || (lse && !aligned4(lse)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    if (T == 0) return ATTNRES_OK;
+
+    const int EPV = epv(dt);
+    const int nvec = (int)(d / EPV);
+    int tpr, vpt;
+    row_shape(nvec, &tpr, &vpt);
+    const int nq_pad = pow2ceil((int)n_q);
+    if (vpt > 8 || (int64_t)nq_pad * vpt * EPV > 64) return ATTNRES_ERR_UNSUPPORTED;
+    bool mh = false;
+    int seg = nvec;
+    if (H > 1) {
+        if ((d / H) % EPV != 0) return ATTNRES_ERR_UNSUPPORTED;
+        seg = (int)(nvec / H);
+        if (seg % 32 != 0) return ATTNRES_ERR_UNSUPPORTED;
+        mh = true;
+    }
+    const int tt = 256 / tpr;
+    const size_t row_bytes = (size_t)d * es;
+    int chunk = (int)(kStageMaxBytes / ((size_t)tt * row_bytes));
+    if (chunk < 1) return ATTNRES_ERR_UNSUPPORTED;
+    if (chunk > DR_CMAX) chunk = DR_CMAX;
+    if (chunk > n_src) chunk = (int)n_src;
+    const int nchunks = (int)((n_src + chunk - 1) / chunk);
+    const bool multi = nchunks > 1;
+
+    KernelRef kr;
+    if (!lookup_depth_read(dt == ATTNRES_BF16 ? 1 : 0, nq_pad, vpt, mh, multi, &kr))
+        return ATTNRES_ERR_UNSUPPORTED;
+
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+
+    const uint32_t src_pitch = (uint32_t)(tt * row_bytes);
+    const uint32_t stage_bytes = (uint32_t)(((size_t)chunk * src_pitch + 127) / 128 * 128);
+    size_t budget = kSmemBudget;
+    if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
+    if (budget <= kr.aux_smem) return ATTNRES_ERR_UNSUPPORTED;
+    int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
+    if (nstages > DR_MAX_STAGES) nstages = DR_MAX_STAGES;
+    if (nstages < 2) return ATTNRES_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
+
+    int occ = 0;
+    st = prepare_kernel(kr.fn, smem, DR_THREADS, &occ);
+    if (st != ATTNRES_OK) return st;
+
+    DepthReadArgs a;
+    a.src = static_cast<const unsigned char *>(src);
+    a.src_stride_bytes = src_stride * (int64_t)es;
+    a.n_src = (int)n_src;
+    a.T = T;
+    a.d = (int)d;
+    a.nvec = nvec;
+    a.n_q = (int)n_q;
+    a.H = (int)H;
+    a.seg = seg;
+    a.queries = queries;
+    a.gain = gain;
+    a.eps = eps;
+    a.out = static_cast<unsigned char *>(out);
+    a.out_q_stride_bytes = T * d * (int64_t)es;
+    a.lse = lse;
+    a.tpr = tpr;
+    a.tt = tt;
+    a.chunk = chunk;
+    a.nchunks = nchunks;
+    a.nstages = nstages;
+    a.stage_bytes = stage_bytes;
+    a.src_pitch = src_pitch;
+    a.ntiles = (T + tt - 1) / tt;
+    a.wait = wait_cfg(dev);
+
+    const int64_t max_grid = (int64_t)dev->sms * occ;
+    const int grid = (int)(a.ntiles < max_grid ? a.ntiles : max_grid);
+    void *args[] = {&a};
+    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(DR_THREADS), args, smem,
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "depth_read launch");
+    return ATTNRES_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attnres_status_t attnres_full_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                  int64_t d, attnres_dtype_t dt, const float *query,
+                                  const float *gain, float eps, void *out, void *stream) {
+    return launch_depth_read(src, n_src, src_stride, T, d, 1, dt, query, 1, gain, eps, out, nullptr,
+                             stream);
+}
+
+attnres_status_t attnres_block_phase1(const void *src, int64_t n_src, int64_t src_stride,
+                                      int64_t T, int64_t d, attnres_dtype_t dt,
+                                      const float *queries, int64_t n_q, const float *gain,
+                                      float eps, void *o, float *lse, void *stream) {
+    return launch_depth_read(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, o, lse,
+                             stream);
+}
+
+attnres_status_t mhar_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                          int64_t H, attnres_dtype_t dt, const float *queries, int64_t n_q,
+                          const float *gain, float eps, void *out, float *lse, void *stream) {
+    return launch_depth_read(src, n_src, src_stride, T, d, H, dt, queries, n_q, gain, eps, out, lse,
+                             stream);
+}
+
+attnres_status_t attnres_block_phase2_merge(const void *o, const float *lse, const void *partial,
+                                            int64_t T, int64_t d, attnres_dtype_t dt,
+                                            const float *query, const float *gain, float eps,
+                                            void *out, void *stream) {
+    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
+    if (T < 0 || d < 1 || !(eps >= 0.f) || std::isinf(eps)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!o || !out)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && partial && (!lse || !query)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t nbytes = (size_t)T * (size_t)d * es;
+    if (out != o && overlap(out, nbytes, o, nbytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (partial && overlap(out, nbytes, partial, nbytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(o) || !aligned16(out) || (partial && !aligned16(partial)) ||
+        (query && !aligned16(query)) || (gain && !aligned16(gain)) || (lse && !aligned4(lse)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    if (T == 0) return ATTNRES_OK;
+    if (!partial) {
+        if (out == o) return ATTNRES_OK;
+        cudaError_t e = cudaMemcpyAsync(out, o, nbytes, cudaMemcpyDeviceToDevice,
+                                        static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemcpyAsync");
+    }
+    const int EPV = epv(dt);
+    const int nvec = (int)(d / EPV);
+    int tpr, vpt;
+    row_shape(nvec, &tpr, &vpt);
+    KernelRef kr;
+    if (vpt > 8 || !lookup_phase2(dt == ATTNRES_BF16 ? 1 : 0, vpt, &kr)) return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    attnres_status_t st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    int occ = 0;
+    st = prepare_kernel(kr.fn, 0, P2_THREADS, &occ);
+    if (st != ATTNRES_OK) return st;
+    MergeArgs a;
+    a.o = static_cast<const unsigned char *>(o);
+    a.lse = lse;
+    a.partial = static_cast<const unsigned char *>(partial);
+    a.T = T;
+    a.d = (int)d;
+    a.nvec = nvec;
+    a.query = query;
+    a.gain = gain;
+    a.eps = eps;
+    a.out = static_cast<unsigned char *>(out);
+    a.tpr = tpr;
+    a.tt = P2_THREADS / tpr;
+    a.ntiles = (T + a.tt - 1) / a.tt;
+    const int64_t max_grid = (int64_t)dev->sms * occ;
+    const int grid = (int)(a.ntiles < max_grid ? a.ntiles : max_grid);
+    void *args[] = {&a};
+    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(P2_THREADS), args, 0,
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "phase2 launch");
+    return ATTNRES_OK;
+}
+
+attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                 int64_t d, attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                 const float *conv_w, const float *queries, const float *gain,
+                                 float eps, const float *mix_gain, const float *mix_w, float mix_eps,
+                                 void *out, void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (m < 1 || !(mix_eps >= 0.f) || std::isinf(mix_eps)) return ATTNRES_ERR_INVALID_ARG;
+    if (T == 0) return ATTNRES_OK;
+    if (!ksizes || !conv_w || !queries || !mix_w || !out) return ATTNRES_ERR_INVALID_ARG;
+    for (int64_t r = 0; r + 1 < m; ++r)
+        if (ksizes[r] < 1) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    if (overlap(out, (size_t)T * (size_t)d * es, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (m != 4) return ATTNRES_ERR_UNSUPPORTED;
+    for (int r = 0; r < 3; ++r)
+        if (ksizes[r] > MSAR_KMAX) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(queries) || !aligned16(conv_w) || !aligned16(mix_w) ||
+        (gain && !aligned16(gain)) || (mix_gain && !aligned16(mix_gain)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    if (T == 0) return ATTNRES_OK;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarArgs a;
+    a.src = static_cast<const unsigned char *>(src);
+    a.src_stride_bytes = src_stride * (int64_t)es;
+    a.n_src = (int)n_src;
+    a.T = T;
+    a.d = (int)d;
+    for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
+    a.conv_w = conv_w;
+    a.queries = queries;
+    a.gain = gain;
+    a.eps = eps;
+    a.mix_gain = mix_gain;
+    a.mix_w = mix_w;
+    a.mix_eps = mix_eps;
+    a.out = static_cast<unsigned char *>(out);
+    a.wait = wait_cfg(dev);
+    return launch_msar(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
+}
+
+const char *attnres_status_string(attnres_status_t s) {
+    switch (s) {
+        case ATTNRES_OK: return "ok";
+        case ATTNRES_ERR_INVALID_ARG: return "invalid argument";
+        case ATTNRES_ERR_UNSUPPORTED: return "unsupported shape, alignment or size";
+        case ATTNRES_ERR_CUDA: return "CUDA runtime error";
+        case ATTNRES_ERR_TIMEOUT: return "a device-side wait ran out of time";
+    }
+    return "unknown status";
+}
+
+const char *attnres_last_cuda_error(void) { return t_last_err; }
+
+attnres_status_t attnres_sync_status(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    DeviceInfo *dev = nullptr;
+    attnres_status_t st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    int v = 0;
+    e = cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+        if (v & DEV_ERR_TIMEOUT) return ATTNRES_ERR_TIMEOUT;
+    }
+    return ATTNRES_OK;
+}
+
+void attnres_debug_set_wait_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns ? ns : 2000000000ull);
+}
+
+void attnres_debug_set_stall_injection(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+
+const char *attnres_version(void) { return "attnres 0.1.0 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,26 @@
+// dispatch.h -- host-side lookup of the kernel instantiations compiled in the
+// per-type translation units (kernels_*.cu).  Internal to libattnres.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace attnres {
+
+struct KernelRef {
+    const void *fn = nullptr;   // __global__ function
+    size_t aux_smem = 0;        // shared memory besides the stages (bytes)
+};
+
+// depth_read_kernel<T, nq, vpt, mh, multi>; dt: 0 = f32, 1 = bf16.
+// Returns false if that instantiation is not compiled.
+bool lookup_depth_read(int dt, int nq, int vpt, bool mh, bool multi, KernelRef *out);
+bool lookup_depth_read_f32(int nq, int vpt, bool mh, bool multi, KernelRef *out);
+bool lookup_depth_read_bf16(int nq, int vpt, bool mh, bool multi, KernelRef *out);
+bool lookup_depth_read_bf16_multi(int nq, int vpt, bool mh, KernelRef *out);
+bool lookup_depth_read_f32_multi(int nq, int vpt, bool mh, KernelRef *out);
+
+// phase2_merge_kernel<T, vpt>
+bool lookup_phase2(int dt, int vpt, KernelRef *out);
+
+}  // namespace attnres

@@ -1,0 +1,213 @@
+/*
+ * attnres.h -- C ABI of libattnres.so, the GB300 (sm_103a) implementation of
+ * the Attention Residuals depth-wise softmax read.
+ *
+ * The operation (Full AttnRes; b-lab.team summary of "Attention Residuals",
+ * section 1): for every token, a layer's input is
+ *
+ *     h = sum_i alpha_i v_i,   alpha_i = exp(w . RMSNorm(v_i)) / sum_j exp(w . RMSNorm(v_j)),
+ *     RMSNorm(x) = g * x / sqrt(mean(x^2) + eps),
+ *
+ * over stored source rows v_i (the embedding, earlier layer or block
+ * outputs), with a learned per-layer pseudo-query w.  The weighted sum uses
+ * the raw source values; RMSNorm only enters the score.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every tensor pointer is a DEVICE pointer, row-major and
+ *   contiguous, except that consecutive sources are src_stride elements
+ *   apart.  Host pointers are named as such (only msar_expand_fwd's ksizes).
+ *   The caller owns every buffer; the library allocates nothing, keeps no
+ *   per-call state and is safe to call from several host threads.
+ * Sources.  src holds n_src sources; source i is the [T, d] row block at
+ *   src + i * src_stride (elements).  src_stride >= T * d.
+ * Types.  dt selects the storage type of sources, partial sums and outputs:
+ *   ATTNRES_F32 (float) or ATTNRES_BF16 (bfloat16).  Queries, gains and lse
+ *   are always float.  All arithmetic is float32 (accumulation included);
+ *   bf16 outputs are rounded to nearest-even once, at the store.
+ * Gain.  gain is the RMSNorm gain g[d] (per head slice for MHAR) or NULL for
+ *   all ones.  eps >= 0 is added to the mean square inside the square root.
+ *   A zero key with eps = 0 normalises to zero (score 0).
+ * Streams.  stream is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream).  Every call only enqueues work on it and returns.
+ * Alignment and sizes.  d % 8 == 0; every tensor pointer 16-byte aligned
+ *   (lse: 4-byte); src_stride * sizeof(element) a multiple of 16 bytes.
+ * Errors.  Arguments are validated on the host before anything is launched;
+ *   nothing aborts.  ATTNRES_ERR_INVALID_ARG: a NULL required pointer,
+ *   T < 0, n_src < 1, d < 1, eps < 0 or NaN, src_stride < T*d, a head count
+ *   that does not divide d, or an output that overlaps an input it must not
+ *   alias.  ATTNRES_ERR_UNSUPPORTED: a valid request outside what the
+ *   kernels implement (alignment, d % 8, n_q > 8, size limits listed per
+ *   function).  ATTNRES_ERR_CUDA: a CUDA runtime call failed; the message is
+ *   in attnres_last_cuda_error().  T == 0 is a no-op that returns ATTNRES_OK once
+ *   the scalar arguments are valid; tensor pointers may then be NULL.
+ *   ATTNRES_OK means the work was enqueued.  A device-side wait that ran out
+ *   of time (ATTNRES_ERR_TIMEOUT) is reported by attnres_sync_status().
+ */
+#ifndef ATTNRES_H
+#define ATTNRES_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype_t;
+
+typedef enum {
+    ATTNRES_OK = 0,
+    ATTNRES_ERR_INVALID_ARG = 1,
+    ATTNRES_ERR_UNSUPPORTED = 2,
+    ATTNRES_ERR_CUDA = 3,
+    ATTNRES_ERR_TIMEOUT = 4
+} attnres_status_t;
+
+/*
+ * Full AttnRes read of one layer.
+ * Defined by: b-lab.team summary, section 1 (h_l = sum_{i<l} alpha_{i->l} v_i,
+ * phi(q,k) = exp(q^T RMSNorm(k))); dimensionstp.github.io review, section
+ * 3-2 1).  The layer's sources are v_0..v_{n_src-1}.
+ *   src    [n_src][T][d] (stride src_stride), dtype dt
+ *   query  [d] float, the layer's pseudo-query w_l
+ *   gain   [d] float or NULL
+ *   out    [T][d], dtype dt; must not overlap src
+ * Any n_src >= 1 (sources beyond the on-chip chunk are folded in with an
+ * online softmax).  Limits: d <= 16384 (bf16) / 8192 (f32).
+ */
+attnres_status_t attnres_full_fwd(const void *src, int64_t n_src, int64_t src_stride,
+                                  int64_t T, int64_t d, attnres_dtype_t dt,
+                                  const float *query, const float *gain, float eps,
+                                  void *out, void *stream);
+
+/*
+ * Block AttnRes, phase 1 of the two-phase schedule: all n_q pseudo-queries of
+ * a block read the n_src cached block representations in one pass, so each
+ * cached b_n is read from memory once per block instead of once per layer.
+ * Defined by: b-lab.team summary, section 3 (Inference, Phase 1: parallel
+ * inter-block attention); dimensionstp.github.io review, section 3-2 4).
+ * The softmax state of every (query, token) is returned normalised:
+ *   o_q = sum_i e^{s_qi - m_q} v_i / l_q   and   lse_q = m_q + ln l_q,
+ * so o_0 is already the input of the block's first layer (which reads no
+ * partial sum: summary section 2, tutorial Fig. 4).
+ *   src      [n_src][T][d] cached block representations b_0..b_{n-1}
+ *   queries  [n_q][d] float, 1 <= n_q <= 8
+ *   o        [n_q][T][d], dtype dt; must not overlap src
+ *   lse      [n_q][T] float, or NULL if not needed
+ * Limits: n_q * d <= 16384 after rounding n_q up to 1, 2, 4 or 8.
+ */
+attnres_status_t attnres_block_phase1(const void *src, int64_t n_src, int64_t src_stride,
+                                      int64_t T, int64_t d, attnres_dtype_t dt,
+                                      const float *queries, int64_t n_q,
+                                      const float *gain, float eps,
+                                      void *o, float *lse, void *stream);
+
+/*
+ * Block AttnRes, phase 2: fold one layer's intra-block partial-sum source into
+ * its phase-1 state with the online-softmax merge (exact).
+ * Defined by: b-lab.team summary, section 3 (Phase 2: sequential intra-block
+ * attention + online softmax merge); dimensionstp.github.io review, 3-2 4).
+ *   s_p = w . RMSNorm(p),  M = max(lse, s_p),
+ *   out = (e^{lse-M} o + e^{s_p-M} p) / (e^{lse-M} + e^{s_p-M}).
+ *   o        [T][d] dtype dt (one query's slice of phase-1 o)
+ *   lse      [T] float (the matching slice of phase-1 lse)
+ *   partial  [T][d] dtype dt, the block's current partial sum b^{(n)}_{i-1};
+ *            NULL for the first layer of a block (then out = o)
+ *   query    [d] float, the layer's pseudo-query
+ *   out      [T][d] dtype dt; may be o itself (in place), must not overlap
+ *            partial or partially overlap o
+ */
+attnres_status_t attnres_block_phase2_merge(const void *o, const float *lse,
+                                            const void *partial, int64_t T, int64_t d,
+                                            attnres_dtype_t dt, const float *query,
+                                            const float *gain, float eps, void *out,
+                                            void *stream);
+
+/*
+ * MHAR, the multi-head block-diagonal read: the pseudo-query is reshaped into
+ * H heads of d/H channels; each head has its own softmax over depth and mixes
+ * only its own channel slice.  H = 1 is exactly attnres_block_phase1 (the same
+ * kernel runs).  Defined by: chatpaper.ai "Multi-Head Attention Residuals"
+ * abstract.  Reading taken where the page is silent: the key RMSNorm is per
+ * head, over the head's d/H channels with that slice of the gain.
+ *   src      [n_src][T][d]
+ *   queries  [n_q][H][d/H] float, 1 <= n_q <= 8
+ *   out      [n_q][T][d] dtype dt; must not overlap src
+ *   lse      [n_q][H][T] float or NULL
+ * Limits (H > 1): d/H a multiple of 256 (bf16) / 128 (f32) channels; the
+ * phase-1 limits apply.
+ */
+attnres_status_t mhar_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                          int64_t d, int64_t H, attnres_dtype_t dt, const float *queries,
+                          int64_t n_q, const float *gain, float eps, void *out, float *lse,
+                          void *stream);
+
+/*
+ * MSAR, the fused multi-stream depth read for one target layer: every source
+ * v_i is expanded into m full-width streams (r = 0 identity; r >= 1 a causal
+ * depthwise 1-D convolution along the token axis with kernel size
+ * ksizes[r-1]); each stream reads the depth history with its own pseudo-query
+ * (its weights sum to 1); the m retrieved states Z^(r) are fused by the H^pre
+ * mixer: z = RMSNorm(Flatten(Z)) over m*d, c = sigmoid(z . P), h = sum_r c_r Z^(r).
+ * The expanded streams are never written to memory.
+ * Defined by: onedev.kr "깊이 방향 어텐션을 다중 스트림으로 확장한 MSAR",
+ * sections 무엇과 다른가 (streams, per-stream read, mixer) and 어떻게 쓰나
+ * (fused on-demand expansion).  Readings taken: left zero padding, no conv
+ * bias, u^(r)[t][c] = sum_{j<k} cw[c][j] v[t-j][c]; Flatten is stream-major
+ * (element r*d + c is Z^(r)[c]); plain sigmoid, no bias, no renormalisation.
+ *   src       [n_src][T][d]; token 0 is the start of the causal sequence
+ *   m         number of streams (must be 4)
+ *   ksizes    HOST pointer, m-1 kernel sizes, each 1..16
+ *   conv_w    float, kernels packed one after another, kernel r as [d][k_r]
+ *   queries   [m][d] float
+ *   gain      [d] float or NULL (key RMSNorm gain, shared by the streams)
+ *   mix_gain  [m*d] float or NULL (mixer RMSNorm gain)
+ *   mix_w     [m*d][m] float (the md x m projection P)
+ *   mix_eps   >= 0
+ *   out       [T][d] dtype dt; must not overlap src
+ * Limits: d <= 4096, d a multiple of 256 (bf16) or 128 (f32) channels
+ * divided evenly over a cluster of up to 8 CTAs.
+ */
+attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_stride,
+                                 int64_t T, int64_t d, attnres_dtype_t dt, int64_t m,
+                                 const int32_t *ksizes, const float *conv_w,
+                                 const float *queries, const float *gain, float eps,
+                                 const float *mix_gain, const float *mix_w, float mix_eps,
+                                 void *out, void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *attnres_status_string(attnres_status_t status);
+
+/* Message of the last CUDA error seen by an entry point on this host thread
+ * ("" if none). */
+const char *attnres_last_cuda_error(void);
+
+/*
+ * Waits for all work on stream, then reports (and clears) a device-side
+ * failure recorded by any kernel of this library on the current device since
+ * the last call: ATTNRES_ERR_TIMEOUT if a bounded wait inside a kernel ran
+ * out of time (that kernel's outputs are invalid), ATTNRES_ERR_CUDA if the
+ * synchronisation itself failed, else ATTNRES_OK.
+ */
+attnres_status_t attnres_sync_status(void *stream);
+
+/*
+ * Failure-detection hooks, meant for tests.
+ * attnres_debug_set_wait_timeout_ns: limit of every device-side wait, in
+ *   nanoseconds (default 2e9; 0 restores the default).
+ * attnres_debug_set_stall_injection: when nonzero, kernels that stage data
+ *   with bulk copies issue no copies, so their first wait can only end by
+ *   running out of time; they then record ATTNRES_ERR_TIMEOUT and return
+ *   without touching memory.  Applies to launches made after the call.
+ */
+void attnres_debug_set_wait_timeout_ns(uint64_t ns);
+void attnres_debug_set_stall_injection(int enable);
+
+/* Library version string, e.g. "attnres 0.1.0 sm_103a". */
+const char *attnres_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNRES_H */

@@ -1,0 +1,122 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/attnres.h declares, and rejects bad arguments on the host
+before any CUDA call is made."""
+import ctypes
+
+import pytest
+
+from depth_wise_attention_gb300 import attnres
+from depth_wise_attention_gb300.build import build
+
+OK, INV, UNS = attnres.OK, attnres.ERR_INVALID_ARG, attnres.ERR_UNSUPPORTED
+F32, BF16 = attnres.F32, attnres.BF16
+A = 0x10000           # a fake, 16-byte aligned "device" address (never dereferenced)
+B = 0x40000000        # another one, far away
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return attnres.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = attnres.header_functions()
+    for must in ("attnres_full_fwd", "attnres_block_phase1", "attnres_block_phase2_merge",
+                 "mhar_fwd", "msar_expand_fwd", "attnres_status_string", "attnres_sync_status"):
+        assert must in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for s in range(5):
+        assert attnres.status_string(s)
+    assert attnres.status_string(99) == "unknown status"
+    assert "sm_103a" in attnres.version()
+    assert attnres.last_cuda_error() == ""
+
+
+def full(lib, src=A, n_src=8, stride=None, T=16, d=64, dt=BF16, q=B, g=None, eps=1e-6, out=B + 0x100000):
+    stride = T * d if stride is None else stride
+    return lib.attnres_full_fwd(src, n_src, stride, T, d, dt, q, g, eps, out, None)
+
+
+def phase1(lib, src=A, n_src=8, stride=None, T=16, d=64, dt=BF16, q=B, n_q=4, g=None, eps=1e-6,
+           o=B + 0x100000, lse=B + 0x900000):
+    stride = T * d if stride is None else stride
+    return lib.attnres_block_phase1(src, n_src, stride, T, d, dt, q, n_q, g, eps, o, lse, None)
+
+
+def test_full_validation(lib):
+    assert full(lib, T=0) == OK                      # empty: no-op, no CUDA call
+    assert full(lib, src=None) == INV
+    assert full(lib, q=None) == INV
+    assert full(lib, out=None) == INV
+    assert full(lib, T=-1) == INV
+    assert full(lib, n_src=0) == INV
+    assert full(lib, d=0) == INV
+    assert full(lib, eps=-1.0) == INV
+    assert full(lib, eps=float("nan")) == INV
+    assert full(lib, eps=float("inf")) == INV
+    assert full(lib, stride=16 * 64 - 8) == INV       # sources overlap each other
+    assert full(lib, dt=7) == INV
+    assert full(lib, out=A + 64) == INV               # output overlaps the sources
+    assert full(lib, d=60, stride=16 * 64) == UNS     # d % 8
+    assert full(lib, src=A + 8) == UNS                # misaligned source
+    assert full(lib, out=B + 0x100008) == UNS         # misaligned output
+    assert full(lib, q=B + 4) == UNS                  # misaligned query
+    assert full(lib, g=B + 0x200004) == UNS           # misaligned gain
+    assert full(lib, stride=16 * 64 + 4, dt=BF16) == UNS   # 8-byte source pitch
+    assert full(lib, T=0, src=None, out=None) == OK   # empty: pointers may be NULL
+    assert full(lib, T=0, n_src=0) == INV             # scalars are still validated
+
+
+def test_phase1_and_mhar_validation(lib):
+    assert phase1(lib, T=0) == OK
+    assert phase1(lib, n_q=0) == INV
+    assert phase1(lib, n_q=9) == UNS
+    assert phase1(lib, lse=B + 0x900002) == UNS       # lse must be 4-byte aligned
+    assert phase1(lib, lse=A) == INV                  # lse overlaps the sources
+    assert phase1(lib, o=A + 0x100) == INV
+    # MHAR: H must divide d; head width must suit the kernel
+    mh = lambda H, d=512, T=0: lib.mhar_fwd(A, 8, T * d, T, d, H, BF16, B, 4, None, 1e-6,
+                                            B + 0x100000, None, None)
+    assert mh(3) == INV
+    assert mh(0) == INV
+    assert mh(1) == OK
+    assert lib.mhar_fwd(A, 8, 16 * 512, 16, 512, 8, BF16, B, 4, None, 1e-6, B + 0x100000, None,
+                        None) == UNS                   # 64-channel heads: not a multiple of 256
+
+
+def test_phase2_validation(lib):
+    m = lambda o=A, lse=B, p=B + 0x100000, T=16, d=64, q=B + 0x200000, out=B + 0x300000, eps=1e-6: \
+        lib.attnres_block_phase2_merge(o, lse, p, T, d, BF16, q, None, eps, out, None)
+    assert m(T=0) == OK
+    assert m(o=None) == INV
+    assert m(out=None) == INV
+    assert m(lse=None) == INV
+    assert m(q=None) == INV
+    assert m(o=None, out=None, T=0) == OK
+    assert m(out=B + 0x100000 + 16) == INV           # out overlaps partial
+    assert m(out=A + 16) == INV                      # out partially overlaps o
+    assert m(out=A, T=0) == OK                       # in place is allowed
+    assert m(d=12) == UNS
+    assert m(p=B + 0x100004) == UNS
+
+
+def test_msar_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    bad = (ctypes.c_int32 * 3)(4, 0, 12)
+    big = (ctypes.c_int32 * 3)(4, 8, 17)
+
+    def ms(m=4, k=ks, T=0, d=256, out=B + 0x100000, mix_eps=1e-6):
+        return lib.msar_expand_fwd(A, 8, T * d, T, d, BF16, m, ctypes.cast(k, ctypes.c_void_p),
+                                   B, B + 0x200000, None, 1e-6, None, B + 0x300000, mix_eps, out,
+                                   None)
+    assert ms() == OK
+    assert ms(k=bad, T=4) == INV
+    assert ms(mix_eps=-1.0) == INV
+    assert ms(out=None, T=4) == INV
+    assert ms(m=3, T=4) == UNS
+    assert ms(k=big, T=4) == UNS

@@ -1,0 +1,141 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark times.  Outputs are checked against the oracle on sampled tokens:
+t = 0, t = T-1, t = 1..12 (the causal-convolution edge) and 300 tokens drawn
+with seed 1.  Tokens are independent in every read except MSAR, whose oracle
+is given the 12-row causal window that ends at each sampled token."""
+import numpy as np
+import pytest
+import torch
+
+from _helpers import check_lse, check_out, to_dev, to_host
+from depth_wise_attention_gb300 import attnres, inputs
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+BF16, F32 = torch.bfloat16, torch.float32
+
+
+def sampled_tokens(T, n=300):
+    rng = np.random.default_rng(1)
+    extra = rng.choice(T, size=min(n, T), replace=False)
+    return np.unique(np.concatenate([[0, T - 1], np.arange(1, min(13, T)), extra]))
+
+
+def rows(t, idx):
+    """t [..., T, d] -> float64 numpy rows at token indices idx."""
+    it = torch.from_numpy(idx).to(t.device)
+    return t.index_select(t.dim() - 2, it).float().cpu().numpy().astype(np.float64)
+
+
+def test_full_fp32_T256_d256_L8():
+    x = inputs.full_inputs(8, 256, 256, seed=0, std_step=0.25)
+    out = attnres.attnres_full_fwd(to_dev(x["src"], F32), to_dev(x["query"], F32),
+                                   to_dev(x["gain"], F32), x["eps"])
+    ref = oracle.full(x["src"], x["query"], x["gain"], x["eps"])
+    check_out(out, ref, F32, np.abs(x["src"]).max())
+
+
+@pytest.mark.parametrize("all_partials", [False, True])
+def test_block_two_phase_T8192_d2048(all_partials):
+    """Default: layer 1 reads no partial (summary section 2; tutorial Fig. 4);
+    all_partials=True covers the other reading of 'per-layer partial sums'."""
+    N, S, T, d = 8, 4, 8192, 2048
+    x = inputs.block_inputs(N, S, T, d, seed=0)
+    cache, q, parts = to_dev(x["cache"], BF16), to_dev(x["queries"], F32), to_dev(x["partials"], BF16)
+    o, lse = attnres.attnres_block_phase1(cache, q)
+    first = 0 if all_partials else 1
+    for i in range(first, S):
+        attnres.attnres_block_phase2_merge(o[i], lse[i], parts[i], q[i], out=o[i])
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T)
+    c = x["cache"][:, idx, :].astype(np.float64)
+    p = x["partials"][:, idx, :].astype(np.float64)
+    if all_partials:
+        ref = np.stack([oracle.full(np.concatenate([c, p[i:i + 1]]), x["queries"][i])
+                        for i in range(S)])
+    else:
+        ref = oracle.block_oneshot(c, p, x["queries"])
+    check_out(rows(o, idx), ref, BF16)
+
+
+def _device_block(T, d, N=8, S=4, seed=0):
+    cache, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=seed)
+    cache = cache.view(N, T, d)
+    q = inputs.device_normal((S, d), (16.0 / d) ** 0.5, g)
+    parts = torch.empty((S, T, d), dtype=BF16, device="cuda")
+    for i in range(S):
+        parts[i].copy_(torch.randn((T, d), generator=g, device="cuda"))
+    return cache, q, parts
+
+
+def test_block_two_phase_T32768_d4096_bench_workload():
+    T, d, N, S = 32768, 4096, 8, 4
+    cache, q, parts = _device_block(T, d, N, S)
+    o = torch.empty((S, T, d), dtype=BF16, device="cuda")
+    lse = torch.empty((S, T), dtype=F32, device="cuda")
+    attnres.attnres_block_phase1(cache, q, o=o, lse=lse)
+    idx = sampled_tokens(T)
+    lse_ph1 = lse[:, torch.from_numpy(idx).cuda()].cpu().numpy()
+    for i in range(1, S):
+        attnres.attnres_block_phase2_merge(o[i], lse[i], parts[i], q[i], out=o[i])
+    attnres.attnres_sync_status()
+    c, p = rows(cache, idx), rows(parts, idx)
+    qh = q.cpu().numpy().astype(np.float64)
+    check_out(rows(o, idx), oracle.block_oneshot(c, p, qh), BF16)
+    check_lse(lse_ph1, oracle.block_phase1(c, qh)[1])
+
+
+def test_full_at_depth_T16384_d4096_L64():
+    """Layer l = 1..64 reads sources 0..l-1, one call per layer in order."""
+    T, d, L = 16384, 4096, 64
+    src, g = inputs.device_sources(L, T, d, lambda i: 1.0 + i / 16.0, seed=0)
+    src = src.view(L, T, d)
+    q = inputs.device_normal((L, d), (16.0 / d) ** 0.5, g)
+    out = torch.empty((T, d), dtype=BF16, device="cuda")
+    idx = sampled_tokens(T, n=24)
+    s_h = rows(src, idx)
+    q_h = q.cpu().numpy().astype(np.float64)
+    for l in range(1, L + 1):
+        attnres.attnres_full_fwd(src[:l], q[l - 1], None, 1e-6, out=out)
+        if l in (1, 2, 7, 8, 9, 16, 17, 33, 63, 64):
+            check_out(rows(out, idx), oracle.full(s_h[:l], q_h[l - 1]), BF16, what=f"layer {l}")
+    attnres.attnres_sync_status()
+
+
+def test_mhar_T131072_d4096_H8():
+    T, d, N, S, H = 131072, 4096, 8, 4, 8
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((S, H, d // H), (16.0 / (d // H)) ** 0.5, g)
+    out, lse = attnres.mhar_fwd(src, q, want_lse=True)
+    idx = sampled_tokens(T)
+    ro, rl = oracle.mhar(rows(src, idx), q.cpu().numpy().astype(np.float64), want_lse=True)
+    check_out(rows(out, idx), ro, BF16)
+    check_lse(lse[:, :, torch.from_numpy(idx).cuda()].cpu().numpy(), rl)
+    # H = 1 is AttnRes exactly: the same kernel as phase 1, bit for bit
+    del out, lse
+    q1 = inputs.device_normal((S, 1, d), (16.0 / d) ** 0.5, g)
+    m1 = attnres.mhar_fwd(src, q1)
+    o1, _ = attnres.attnres_block_phase1(src, q1.view(S, d), want_lse=False)
+    assert torch.equal(m1, o1)
+
+
+def test_msar_T32768_d4096():
+    T, d, N = 32768, 4096, 8
+    ks = (4, 8, 12)
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((4, d), (16.0 / d) ** 0.5, g)
+    cw = torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g) for k in ks])
+    mw = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g)
+    out = attnres.msar_expand_fwd(src, ks, cw, q, None, 1e-6, None, mw, 1e-6)
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T, n=150)
+    cw_h, q_h, mw_h = (t.cpu().numpy().astype(np.float64) for t in (cw, q, mw))
+    got = rows(out, idx)
+    ref = np.empty_like(got)
+    for j, t in enumerate(idx):
+        lo = max(0, int(t) - 11)
+        win = src[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
+        ref[j] = oracle.msar(win, ks, cw_h, q_h, None, 1e-6, None, mw_h, 1e-6)[-1]
+    check_out(got, ref, BF16)

@@ -1,0 +1,343 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle on the
+same seeded inputs, at sizes the oracle finishes in seconds that still span
+several tiles (and clusters) plus a ragged tail, and on the edge cases of the
+method.  Tolerances are defined in _helpers.py."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from _helpers import check_lse, check_out, to_dev, to_host
+from depth_wise_attention_gb300 import attnres, inputs
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+
+BF16, F32 = torch.bfloat16, torch.float32
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _sources(rng, n_src, T, d, dtype, step=0.5):
+    src = np.stack([rng.standard_normal((T, d)).astype(np.float32) * (1 + i * step)
+                    for i in range(n_src)])
+    return inputs.bf16_round(src) if dtype == BF16 else src
+
+
+def _queries(rng, n, d, std=None):
+    std = math.sqrt(16.0 / d) if std is None else std
+    return (rng.standard_normal((n, d)) * std).astype(np.float32)
+
+
+# --------------------------------------------------------------- worked example
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("T", [1, 3, 13])
+def test_worked_example_padded(dtype, T):
+    """Tutorial Figs. 2-3, padded to d=8: alpha=[1/4,1/2,1/4], h=[0.5,2,1.5,0..]."""
+    src = np.zeros((3, T, 8), np.float32)
+    src[0, :, 0], src[1, :, 1], src[2, :, 2] = 2.0, 4.0, 6.0
+    w = np.zeros(8, np.float32)
+    w[1] = math.log(2.0) / math.sqrt(8.0)
+    out = attnres.attnres_full_fwd(to_dev(src, dtype), to_dev(w, F32), None, 0.0)
+    want = np.zeros((T, 8))
+    want[:, :3] = [0.5, 2.0, 1.5]
+    assert np.abs(to_host(out) - want).max() <= (1e-6 if dtype == F32 else 0.0)
+
+
+# --------------------------------------------------------------- Full
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("n_src,T,d", [(1, 5, 256), (3, 37, 256), (8, 300, 256), (8, 77, 2048),
+                                       (5, 41, 4096), (8, 19, 8), (2, 9, 24), (7, 33, 1000)])
+def test_full_fwd(dtype, n_src, T, d):
+    rng = _rng(n_src * 1000 + T + d)
+    src = _sources(rng, n_src, T, d, dtype, step=0.25)
+    w = _queries(rng, 1, d)[0]
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    out = attnres.attnres_full_fwd(to_dev(src, dtype), to_dev(w, F32), to_dev(g, F32), 1e-6)
+    ref = oracle.full(src, w, g, 1e-6)
+    check_out(out, ref, dtype, np.abs(src).max())
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("n_src,T,d", [(9, 21, 4096), (13, 40, 2048), (64, 7, 4096), (17, 70, 256),
+                                       (30, 11, 512)])
+def test_full_fwd_many_sources_online_merge(dtype, n_src, T, d):
+    """More sources than one stage holds: chunks merged by the online softmax."""
+    rng = _rng(n_src * 7 + T + d)
+    src = _sources(rng, n_src, T, d, dtype, step=1 / 16)
+    w = _queries(rng, 1, d)[0]
+    out = attnres.attnres_full_fwd(to_dev(src, dtype), to_dev(w, F32), None, 1e-6)
+    check_out(out, oracle.full(src, w, None, 1e-6), dtype, np.abs(src).max())
+
+
+def test_full_fwd_zero_query_is_mean():
+    rng = _rng(3)
+    src = _sources(rng, 6, 50, 512, F32)
+    out = attnres.attnres_full_fwd(to_dev(src, F32), to_dev(np.zeros(512, np.float32), F32))
+    check_out(out, src.mean(axis=0), F32, np.abs(src).max())
+
+
+def test_full_fwd_zero_source_with_zero_eps():
+    src = np.zeros((2, 4, 64), np.float32)
+    src[1, :, 3] = 5.0
+    w = np.zeros(64, np.float32)
+    w[3] = 1.0
+    out = attnres.attnres_full_fwd(to_dev(src, F32), to_dev(w, F32), None, 0.0)
+    check_out(out, oracle.full(src, w, None, 0.0), F32, 5.0)
+
+
+def test_full_fwd_source_stride():
+    """Sources that are not packed back to back (src_stride > T*d)."""
+    rng = _rng(4)
+    n_src, T, d, stride = 6, 33, 512, 33 * 512 + 8 * 100
+    buf = torch.zeros((n_src, stride), dtype=BF16, device="cuda")
+    src = _sources(rng, n_src, T, d, BF16)
+    buf[:, : T * d] = to_dev(src.reshape(n_src, -1), BF16)
+    view = buf[:, : T * d].view(n_src, T, d)
+    assert view.stride(0) == stride
+    w = _queries(rng, 1, d)[0]
+    out = attnres.attnres_full_fwd(view, to_dev(w, F32))
+    check_out(out, oracle.full(src, w, None, 1e-6), BF16)
+
+
+# --------------------------------------------------------------- phase 1 / phase 2
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("n_q", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("T,d", [(70, 2048), (23, 4096)])
+def test_block_phase1(dtype, n_q, T, d):
+    nq_pad = 1 << (n_q - 1).bit_length()
+    if nq_pad * d > 16384:
+        pytest.skip("register budget: n_q (rounded up to a power of two) * d <= 16384")
+    rng = _rng(n_q * 100 + T)
+    src = _sources(rng, 8, T, d, dtype)
+    q = _queries(rng, n_q, d)
+    o, lse = attnres.attnres_block_phase1(to_dev(src, dtype), to_dev(q, F32), None, 1e-6)
+    ro, rl = oracle.block_phase1(src, q, None, 1e-6)
+    check_out(o, ro, dtype, np.abs(src).max(), what="o")
+    check_lse(lse, rl)
+
+
+@pytest.mark.parametrize("n_src", [1, 2, 8, 10, 20])
+def test_block_phase1_source_counts(n_src):
+    rng = _rng(n_src)
+    T, d = 45, 2048
+    src = _sources(rng, n_src, T, d, BF16)
+    q = _queries(rng, 4, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    o, lse = attnres.attnres_block_phase1(to_dev(src, BF16), to_dev(q, F32), to_dev(g, F32), 1e-6)
+    ro, rl = oracle.block_phase1(src, q, g, 1e-6)
+    check_out(o, ro, BF16, what="o")
+    check_lse(lse, rl)
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("T,d", [(1, 64), (99, 2048), (64, 4096), (10, 808)])
+def test_block_phase2_merge(dtype, T, d):
+    rng = _rng(T + d)
+    o = _sources(rng, 1, T, d, dtype)[0]
+    p = _sources(rng, 1, T, d, dtype)[0]
+    lse = (rng.standard_normal(T) * 4).astype(np.float32)
+    q = _queries(rng, 1, d)[0]
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    out = attnres.attnres_block_phase2_merge(to_dev(o, dtype), to_dev(lse, F32), to_dev(p, dtype),
+                                             to_dev(q, F32), to_dev(g, F32), 1e-6)
+    ref = oracle.block_phase2(o, lse, p, q, g, 1e-6)
+    check_out(out, ref, dtype, max(np.abs(o).max(), np.abs(p).max()))
+
+
+def test_block_phase2_in_place_and_without_partial():
+    rng = _rng(11)
+    T, d = 50, 1024
+    o = _sources(rng, 1, T, d, BF16)[0]
+    p = _sources(rng, 1, T, d, BF16)[0]
+    lse = (rng.standard_normal(T) * 4).astype(np.float32)
+    q = _queries(rng, 1, d)[0]
+    od = to_dev(o, BF16)
+    attnres.attnres_block_phase2_merge(od, to_dev(lse, F32), to_dev(p, BF16), to_dev(q, F32), out=od)
+    check_out(od, oracle.block_phase2(o, lse, p, q), BF16)
+    od = to_dev(o, BF16)
+    out = attnres.attnres_block_phase2_merge(od, to_dev(lse, F32), None, to_dev(q, F32))
+    assert torch.equal(out, od)
+
+
+@pytest.mark.parametrize("T,d,N,S", [(150, 2048, 8, 4), (40, 4096, 8, 4), (33, 512, 3, 6)])
+def test_two_phase_block_matches_oneshot(T, d, N, S):
+    """GPU two-phase schedule (phase 1 + S-1 merges) vs the oracle's
+    layer-by-layer one-shot Block read."""
+    x = inputs.block_inputs(N, S, T, d, seed=T)
+    cache, q, parts = x["cache"], x["queries"], x["partials"]
+    cd, qd, pd = to_dev(cache, BF16), to_dev(q, F32), to_dev(parts, BF16)
+    o, lse = attnres.attnres_block_phase1(cd, qd)
+    outs = [o[0]]
+    for i in range(1, S):
+        outs.append(attnres.attnres_block_phase2_merge(o[i], lse[i], pd[i], qd[i]))
+    gpu = torch.stack(outs)
+    ref = oracle.block_oneshot(cache, parts, q)
+    check_out(gpu, ref, BF16)
+
+
+# --------------------------------------------------------------- MHAR
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("H,d,T", [(2, 2048, 31), (4, 2048, 70), (8, 2048, 9), (8, 4096, 37),
+                                   (16, 4096, 12), (4, 1024, 20)])
+def test_mhar(dtype, H, d, T):
+    if dtype == F32 and d // H % 128:
+        pytest.skip("f32 heads need a multiple of 128 channels")
+    if dtype == BF16 and d // H % 256:
+        pytest.skip("bf16 heads need a multiple of 256 channels")
+    rng = _rng(H * 10 + T)
+    src = _sources(rng, 8, T, d, dtype)
+    q = (rng.standard_normal((4, H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    out, lse = attnres.mhar_fwd(to_dev(src, dtype), to_dev(q, F32), to_dev(g, F32), 1e-6,
+                                want_lse=True)
+    ro, rl = oracle.mhar(src, q, g, 1e-6, want_lse=True)
+    check_out(out, ro, dtype, np.abs(src).max())
+    check_lse(lse, rl)
+
+
+def test_mhar_many_sources():
+    rng = _rng(12)
+    T, d, H = 30, 2048, 8
+    src = _sources(rng, 11, T, d, BF16, step=0.2)
+    q = (rng.standard_normal((4, H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
+    out = attnres.mhar_fwd(to_dev(src, BF16), to_dev(q, F32))
+    check_out(out, oracle.mhar(src, q), BF16)
+
+
+def test_mhar_one_head_is_phase1_bitwise():
+    rng = _rng(13)
+    T, d = 57, 4096
+    src = to_dev(_sources(rng, 8, T, d, BF16), BF16)
+    q = to_dev(_queries(rng, 4, d), F32)
+    o, lse = attnres.attnres_block_phase1(src, q)
+    m, ml = attnres.mhar_fwd(src, q.view(4, 1, d), want_lse=True)
+    assert torch.equal(o, m)
+    assert torch.equal(lse, ml.view(4, T))
+
+
+# --------------------------------------------------------------- MSAR
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("n_src,T,d", [(8, 100, 256), (3, 45, 512), (1, 20, 64), (8, 40, 2048),
+                                       (8, 30, 4096), (5, 200, 128)])
+def test_msar(dtype, n_src, T, d):
+    if dtype == F32 and d > 2048:
+        pytest.skip("f32 MSAR supports d <= 2048")
+    x = inputs.msar_inputs(n_src, T, d, seed=T + d, dtype="bf16" if dtype == BF16 else "f32")
+    g = _rng(5).uniform(0.5, 1.5, d).astype(np.float32)
+    mg = _rng(6).uniform(0.5, 1.5, 4 * d).astype(np.float32)
+    out = attnres.msar_expand_fwd(to_dev(x["src"], dtype), x["ksizes"], to_dev(x["conv_w"], F32),
+                                  to_dev(x["queries"], F32), to_dev(g, F32), 1e-6, to_dev(mg, F32),
+                                  to_dev(x["mix_w"], F32), 1e-6)
+    ref = oracle.msar(x["src"], x["ksizes"], x["conv_w"], x["queries"], g, 1e-6, mg, x["mix_w"], 1e-6)
+    check_out(out, ref, dtype, np.abs(x["src"]).max() * 3)
+
+
+@pytest.mark.parametrize("ks", [(1, 2, 3), (16, 5, 9), (12, 8, 4)])
+def test_msar_kernel_sizes(ks):
+    T, d = 60, 512
+    x = inputs.msar_inputs(4, T, d, seed=7, ksizes=ks)
+    out = attnres.msar_expand_fwd(to_dev(x["src"], BF16), x["ksizes"], to_dev(x["conv_w"], F32),
+                                  to_dev(x["queries"], F32), None, 1e-6, None,
+                                  to_dev(x["mix_w"], F32), 1e-6)
+    ref = oracle.msar(x["src"], x["ksizes"], x["conv_w"], x["queries"], None, 1e-6, None,
+                      x["mix_w"], 1e-6)
+    check_out(out, ref, BF16)
+
+
+# --------------------------------------------------------------- hygiene
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary bands around every output must be untouched."""
+    rng = _rng(20)
+    T, d, n_q, pad = 37, 2048, 4, 4096
+    src = to_dev(_sources(rng, 8, T, d, BF16), BF16)
+    q = to_dev(_queries(rng, n_q, d), F32)
+    o_buf = torch.full((pad + n_q * T * d + pad,), 7.0, dtype=BF16, device="cuda")
+    l_buf = torch.full((pad + n_q * T + pad,), 7.0, dtype=F32, device="cuda")
+    o = o_buf[pad: pad + n_q * T * d].view(n_q, T, d)
+    lse = l_buf[pad: pad + n_q * T].view(n_q, T)
+    attnres.attnres_block_phase1(src, q, o=o, lse=lse)
+    h_buf = torch.full((pad + T * d + pad,), 7.0, dtype=BF16, device="cuda")
+    h = h_buf[pad: pad + T * d].view(T, d)
+    attnres.attnres_block_phase2_merge(o[1], lse[1], src[0], q[1], out=h)
+    m_buf = torch.full((pad + T * d + pad,), 7.0, dtype=BF16, device="cuda")
+    x = inputs.msar_inputs(8, T, d, seed=1)
+    attnres.msar_expand_fwd(src, x["ksizes"], to_dev(x["conv_w"], F32), to_dev(x["queries"], F32),
+                            mix_w=to_dev(x["mix_w"], F32), out=m_buf[pad: pad + T * d].view(T, d))
+    torch.cuda.synchronize()
+    for buf in (o_buf, l_buf, h_buf, m_buf):
+        assert torch.all(buf[:pad] == 7.0) and torch.all(buf[-pad:] == 7.0)
+
+
+def test_runs_are_bitwise_deterministic():
+    rng = _rng(21)
+    T, d = 300, 4096
+    src = to_dev(_sources(rng, 8, T, d, BF16), BF16)
+    q = to_dev(_queries(rng, 4, d), F32)
+    a1, l1 = attnres.attnres_block_phase1(src, q)
+    a2, l2 = attnres.attnres_block_phase1(src, q)
+    assert torch.equal(a1, a2) and torch.equal(l1, l2)
+    x = inputs.msar_inputs(8, T, d, seed=2)
+    args = (src, x["ksizes"], to_dev(x["conv_w"], F32), to_dev(x["queries"], F32))
+    kw = dict(mix_w=to_dev(x["mix_w"], F32))
+    assert torch.equal(attnres.msar_expand_fwd(*args, **kw), attnres.msar_expand_fwd(*args, **kw))
+
+
+def test_calls_on_a_side_stream():
+    rng = _rng(22)
+    T, d = 64, 2048
+    src_h = _sources(rng, 8, T, d, BF16)
+    q_h = _queries(rng, 4, d)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        src = to_dev(src_h, BF16)
+        q = to_dev(q_h, F32)
+        o, lse = attnres.attnres_block_phase1(src, q, stream=s)
+    s.synchronize()
+    check_out(o, oracle.block_phase1(src_h, q_h)[0], BF16)
+
+
+def test_empty_sequence_is_a_no_op():
+    src = torch.empty((8, 16, 256), dtype=BF16, device="cuda")[:, :0, :]
+    q = torch.zeros((4, 256), dtype=F32, device="cuda")
+    o, lse = attnres.attnres_block_phase1(src, q)
+    assert o.shape == (4, 0, 256)
+
+
+def test_stall_injection_reports_timeout_and_context_survives():
+    """A kernel whose copies never arrive gives up after the wait limit,
+    records a timeout, and leaves the context usable."""
+    rng = _rng(23)
+    T, d = 64, 2048
+    src_h = _sources(rng, 8, T, d, BF16)
+    q_h = _queries(rng, 4, d)
+    src, q = to_dev(src_h, BF16), to_dev(q_h, F32)
+    attnres.attnres_sync_status()
+    try:
+        attnres.attnres_debug_set_wait_timeout_ns(20_000_000)      # 20 ms
+        attnres.attnres_debug_set_stall_injection(True)
+        attnres.attnres_block_phase1(src, q)
+        with pytest.raises(attnres.AttnResError) as e:
+            attnres.attnres_sync_status()
+        assert e.value.status == attnres.ERR_TIMEOUT
+        x = inputs.msar_inputs(8, T, d, seed=3)
+        attnres.msar_expand_fwd(src, x["ksizes"], to_dev(x["conv_w"], F32),
+                                to_dev(x["queries"], F32), mix_w=to_dev(x["mix_w"], F32))
+        with pytest.raises(attnres.AttnResError) as e:
+            attnres.attnres_sync_status()
+        assert e.value.status == attnres.ERR_TIMEOUT
+    finally:
+        attnres.attnres_debug_set_stall_injection(False)
+        attnres.attnres_debug_set_wait_timeout_ns(0)
+    o, lse = attnres.attnres_block_phase1(src, q)
+    attnres.attnres_sync_status()
+    check_out(o, oracle.block_phase1(src_h, q_h)[0], BF16)
