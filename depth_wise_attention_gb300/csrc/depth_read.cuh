@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(DR_THREADS, 1) depth_read_kernel(const DepthRe
                     float ss = 0.f, dt = 0.f;
                     if (MH) {
                         head = (h * a.tpr + 32 * wr) / a.seg;
-                        lse_writer = (h * a.tpr + 32 * wr) == head * a.seg;
+                        // slots past the row (masked lanes) map to no head
+                        lse_writer = head < a.H && (h * a.tpr + 32 * wr) == head * a.seg;
                         for (int kk = 0; kk < VPT; ++kk)
                             for (int ww = 0; ww < nwr; ++ww)
                                 if ((kk * a.tpr + 32 * ww) / a.seg == head) {
