@@ -170,6 +170,12 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     int tpr, vpt;
     row_shape(nvec, &tpr, &vpt);
     const int nq_pad = pow2ceil((int)n_q);
+    // more queries need more registers per vector: spread the row over more
+    // threads until NQ * VPT * EPV fits the budget of 64 (or no wider row exists)
+    while ((int64_t)nq_pad * vpt * EPV > 64 && tpr < 256 && vpt > 1) {
+        tpr *= 2;
+        vpt = pow2ceil((nvec + tpr - 1) / tpr);
+    }
     if (vpt > 8 || (int64_t)nq_pad * vpt * EPV > 64) return ATTNRES_ERR_UNSUPPORTED;
     bool mh = false;
     int seg = nvec;

@@ -114,6 +114,15 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return *reinterpret_cast<float2 *>(&d);
 }
 
+// d = a * b on two f32 lanes at once.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
 // bf16x2 (one 32-bit word, low half = lower channel) -> two exact floats.
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
@@ -159,6 +168,26 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
                  : "r"(smem_u32(p)));
     return v;
 }
+// 16-byte shared load from a 32-bit shared-window address.
+__device__ __forceinline__ uint4 lds128u(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds32f(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
 
 __device__ __forceinline__ void stg128_cs(void *p, const uint4 &v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -175,32 +204,57 @@ __device__ __forceinline__ uint4 ldg128_stream(const void *p) {
 }
 
 // ----------------------------------------------------- warp reductions
-// Butterfly all-to-some reduction of V values across the 32 lanes of a warp.
-// VP = V rounded up to a multiple of 32, R = VP / 32.  On return lane L holds
-// in v[0..R-1] the warp-wide sums of value indices R*L .. R*L+R-1 (indices
-// >= V are padding).  Each halving step exchanges half of the remaining
-// values with the partner lane, so the warp issues VP/2 + VP/4 + ... shuffles
-// instead of 5 per value.
+// Butterfly all-to-some reduction of N values across the 32 lanes of a warp.
+// Each of the five steps (partner lane = lane ^ 16, 8, 4, 2, 1) exchanges
+// half of the values still held: the lane whose partner bit is set keeps the
+// upper half, the other the lower half, so the warp issues about N shuffles
+// in total instead of 5 per value.  Sizes shrink as n -> ceil(n/2); an odd
+// size pads one zero.  On return lane L holds in v[0..R-1] (R = size after 5
+// halvings) warp-wide sums whose value indices bfly_slot() gives.
+template <int N>
+struct Bfly {
+    static constexpr int N1 = (N + 1) / 2, N2 = (N1 + 1) / 2, N3 = (N2 + 1) / 2, N4 = (N3 + 1) / 2,
+                         N5 = (N4 + 1) / 2;
+    static constexpr int R = N5;
+};
+
 template <int N, int OFF>
-__device__ __forceinline__ void butterfly_step(float *v, int lane) {
+__device__ __forceinline__ void bfly_step(float *v, int lane) {
+    constexpr int H = (N + 1) / 2;
     const bool upper = (lane & OFF) != 0;
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
-        const float lo = v[i], hi = v[i + N / 2];
+    for (int i = 0; i < H; ++i) {
+        const float lo = v[i];
+        const float hi = (i + H < N) ? v[i + H] : 0.f;
         const float send = upper ? lo : hi;
         const float keep = upper ? hi : lo;
         v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
     }
 }
 
-template <int VP>
+template <int N>
 __device__ __forceinline__ void butterfly_reduce(float *v, int lane) {
-    static_assert(VP % 32 == 0, "pad to a multiple of 32");
-    butterfly_step<VP, 16>(v, lane);
-    butterfly_step<VP / 2, 8>(v, lane);
-    butterfly_step<VP / 4, 4>(v, lane);
-    butterfly_step<VP / 8, 2>(v, lane);
-    butterfly_step<VP / 16, 1>(v, lane);
+    using B = Bfly<N>;
+    bfly_step<N, 16>(v, lane);
+    bfly_step<B::N1, 8>(v, lane);
+    bfly_step<B::N2, 4>(v, lane);
+    bfly_step<B::N3, 2>(v, lane);
+    bfly_step<B::N4, 1>(v, lane);
+}
+
+// Value index held by slot j of lane `lane` after butterfly_reduce<N>, or -1
+// if that slot is padding.
+template <int N>
+__host__ __device__ inline int bfly_slot(int lane, int j) {
+    using B = Bfly<N>;
+    const int n[6] = {N, B::N1, B::N2, B::N3, B::N4, B::N5};
+    int pos = j;
+    if (pos >= n[5]) return -1;
+    for (int s = 4; s >= 0; --s) {
+        if (lane & (16 >> s)) pos += n[s + 1];
+        if (pos >= n[s]) return -1;
+    }
+    return pos;
 }
 
 template <int W>
