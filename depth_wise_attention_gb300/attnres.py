@@ -38,11 +38,13 @@ _SIGS = {
     "attnres_sync_status": [_vp],
     "attnres_debug_set_wait_timeout_ns": [ctypes.c_uint64],
     "attnres_debug_set_stall_injection": [ctypes.c_int],
+    "attnres_debug_set_kernel_variant": [ctypes.c_int],
     "attnres_version": [],
 }
 _RESTYPES = {"attnres_status_string": ctypes.c_char_p, "attnres_last_cuda_error": ctypes.c_char_p,
              "attnres_version": ctypes.c_char_p, "attnres_debug_set_wait_timeout_ns": None,
-             "attnres_debug_set_stall_injection": None}
+             "attnres_debug_set_stall_injection": None,
+             "attnres_debug_set_kernel_variant": None}
 
 
 class AttnResError(RuntimeError):
@@ -202,3 +204,8 @@ def attnres_debug_set_wait_timeout_ns(ns: int):
 
 def attnres_debug_set_stall_injection(enable: bool):
     load().attnres_debug_set_stall_injection(1 if enable else 0)
+
+
+def attnres_debug_set_kernel_variant(variant: int):
+    """0: automatic kernel choice; 1: always the general CUDA-core depth read."""
+    load().attnres_debug_set_kernel_variant(int(variant))

@@ -25,6 +25,7 @@ SOURCES = [
     "kernels_f32.cu",
     "kernels_f32_multi.cu",
     "kernels_phase2.cu",
+    "kernels_mma.cu",
     "msar.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

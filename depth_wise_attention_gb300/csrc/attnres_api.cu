@@ -12,6 +12,7 @@
 #include "../../include/attnres.h"
 #include "common.cuh"
 #include "depth_read.cuh"
+#include "depth_read_mma.cuh"
 #include "dispatch.h"
 #include "msar.h"
 #include "phase2.cuh"
@@ -27,6 +28,7 @@ thread_local char t_last_err[256] = "";
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_kernel_variant{0};   // 0 automatic, 1 general (CUDA-core) depth read only
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kStageMaxBytes = 64 * 1024;        // one ring stage
@@ -164,6 +166,57 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     if (!aligned16(out) || !aligned16(queries) || (gain && !aligned16(gain)) || (lse && !aligned4(lse)))
         return ATTNRES_ERR_UNSUPPORTED;
     if (T == 0) return ATTNRES_OK;
+
+    // Tensor-core path: bf16, <= 8 sources, <= 4 queries, d = 1024/2048/4096,
+    // heads that are whole multiples of the per-warp channel slice.
+    if (dt == ATTNRES_BF16 && n_src <= 8 && n_q <= 4 && d % 128 == 0 && 8 % H == 0 &&
+        g_kernel_variant.load() == 0) {
+        const int ks = (int)(d / 128);
+        KernelRef kr;
+        if (lookup_depth_read_mma(pow2ceil((int)n_q), ks, &kr)) {
+            DeviceInfo *dev = nullptr;
+            st = device_info(&dev);
+            if (st != ATTNRES_OK) return st;
+            const uint32_t pitch = (uint32_t)(2 * d + 16);
+            const uint32_t stage_bytes = (8 * pitch + 127) / 128 * 128;
+            size_t budget = kSmemBudget;
+            if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
+            int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
+            if (nstages > DM_MAX_STAGES) nstages = DM_MAX_STAGES;
+            if (nstages >= 2) {
+                const size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
+                int occ = 0;
+                st = prepare_kernel(kr.fn, smem, DM_THREADS, &occ);
+                if (st != ATTNRES_OK) return st;
+                DepthReadMmaArgs m;
+                m.src = static_cast<const unsigned char *>(src);
+                m.src_stride_bytes = src_stride * 2;
+                m.n_src = (int)n_src;
+                m.T = T;
+                m.d = (int)d;
+                m.n_q = (int)n_q;
+                m.H = (int)H;
+                m.wph = (int)(8 / H);
+                m.queries = queries;
+                m.gain = gain;
+                m.eps = eps;
+                m.out = static_cast<unsigned char *>(out);
+                m.out_q_stride_bytes = T * d * 2;
+                m.lse = lse;
+                m.nstages = nstages;
+                m.pitch = pitch;
+                m.stage_bytes = stage_bytes;
+                m.wait = wait_cfg(dev);
+                const int64_t max_grid = (int64_t)dev->sms * occ;
+                const int grid = (int)(T < max_grid ? T : max_grid);
+                void *args[] = {&m};
+                cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(DM_THREADS), args, smem,
+                                                 static_cast<cudaStream_t>(stream));
+                if (e != cudaSuccess) return cuda_fail(e, "depth_read_mma launch");
+                return ATTNRES_OK;
+            }
+        }
+    }
 
     const int EPV = epv(dt);
     const int nvec = (int)(d / EPV);
@@ -416,6 +469,8 @@ void attnres_debug_set_wait_timeout_ns(uint64_t ns) {
 }
 
 void attnres_debug_set_stall_injection(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+
+void attnres_debug_set_kernel_variant(int variant) { g_kernel_variant.store(variant == 1 ? 1 : 0); }
 
 const char *attnres_version(void) { return "attnres 0.1.0 sm_103a"; }
 

@@ -1,0 +1,268 @@
+// depth_read_mma.cuh -- tensor-core variant of the fused depth read (sm_103a).
+//
+// Same operation as depth_read.cuh (Full AttnRes / Block phase 1 / MHAR):
+// per token, s_qi = (w_q * g) . v_i / sqrt(mean(v_i^2) + eps), softmax over
+// the sources i, o_q = sum_i alpha_qi v_i, lse_q.  Used for bf16 sources
+// with at most 8 sources and 4 queries and d a multiple of 128.
+//
+// The per-token work is two small dense contractions, done with warp-level
+// mma.sync.m16n8k16 (bf16 inputs, fp32 accumulation) straight from the
+// shared-memory stage (ldmatrix), so no element is unpacked:
+//   pass 1:  D1 = X Q  and  D2 = X X^T over the warp's channel slice, where
+//            X = [8 sources x 16 channels] (rows 8..15 zero), Q = the queries
+//            split into bf16 hi + lo parts (columns 2q, 2q+1), so
+//            dot_qi = D1[i][2q] + D1[i][2q+1] and sum(v_i^2) = D2[i][i];
+//   pass 2:  O = A X' per 8-channel block, A = [4 queries x (8 sources hi |
+//            8 sources lo)] holding alpha split into bf16 hi + lo parts and
+//            X' = the same 8 source rows stacked twice (ldmatrix .trans).
+// The hi/lo split keeps the queries and the weights to about 16 mantissa
+// bits; products are exact and sums are fp32.
+//
+// Work split: one token per item; warp w owns channels [w*cw, (w+1)*cw)
+// (cw = d/8); its partial dots and sums of squares go to a small shared
+// table, one CTA barrier publishes them, and each warp computes the softmax
+// of its head (all 8 warps for H = 1) redundantly.  Stages, producer and
+// bounded waits are as in depth_read.cuh; source rows in a stage are padded
+// by 16 bytes so ldmatrix row addresses fall in distinct banks.
+#pragma once
+
+#include "common.cuh"
+
+namespace attnres {
+
+constexpr int DM_WARPS = 8;
+constexpr int DM_THREADS = DM_WARPS * 32;
+constexpr int DM_MAX_STAGES = 6;
+
+struct DepthReadMmaArgs {
+    const unsigned char *src;
+    int64_t src_stride_bytes;
+    int n_src;                    // <= 8
+    int64_t T;
+    int d;
+    int n_q;                      // <= NQ
+    int H;                        // heads
+    int wph;                      // warps per head (8 / H)
+    const float *queries;         // [n_q][d]
+    const float *gain;            // [d] or nullptr
+    float eps;
+    unsigned char *out;           // [n_q][T][d] bf16
+    int64_t out_q_stride_bytes;
+    float *lse;                   // [n_q][H][T] or nullptr
+    int nstages;
+    uint32_t pitch;               // bytes between source rows in a stage (2d + 16)
+    uint32_t stage_bytes;
+    WaitCfg wait;
+};
+
+struct DMLayout {
+    static constexpr size_t bar_bytes = 128;
+    // red[2][40 values][8 warps]: dots (q*8+i) then sums of squares (32+i)
+    static constexpr size_t red_floats = 2 * 40 * DM_WARPS;
+    static constexpr size_t aux_bytes = bar_bytes + 4 * red_floats;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D += A B, m16n8k16, bf16 x bf16 -> fp32.  a1 = a3 = 0 (rows 8..15 unused).
+__device__ __forceinline__ void mma_rows8(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                          uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// bf16 hi/lo split of x: hi = rn(x), lo = rn(x - hi).
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = x - hi;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo_ch, float hi_ch) {
+    return f2_to_bf2(lo_ch, hi_ch);
+}
+
+template <int NQ, int KS>
+__global__ void __launch_bounds__(DM_THREADS, 1) depth_read_mma_kernel(const DepthReadMmaArgs a) {
+    static_assert(NQ <= 4, "at most 4 queries (8 MMA columns: hi and lo per query)");
+    using L = DMLayout;
+    constexpr int CW = KS * 16;                 // channels per warp
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.nstages * a.stage_bytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(full + DM_MAX_STAGES);
+    float *red = reinterpret_cast<float *>(smem + (size_t)a.nstages * a.stage_bytes + L::bar_bytes);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, t4 = lane & 3;    // mma groupID / thread-in-group
+
+    if (tid == 0) {
+        for (int s = 0; s < a.nstages; ++s) mbar_init(&full[s], 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    // Source rows n_src..7 of every stage are never loaded but enter the MMAs
+    // (times a zero weight): make them zero, not stale bits that could be NaN.
+    for (int s = 0; s < a.nstages; ++s)
+        for (int i = a.n_src; i < 8; ++i)
+            for (int b = tid * 16; b < a.d * 2; b += DM_THREADS * 16)
+                *reinterpret_cast<uint4 *>(stages + (size_t)s * a.stage_bytes + (size_t)i * a.pitch + b) =
+                    make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    const int gstride = gridDim.x;
+    const int n_items = blockIdx.x < a.T ? (int)((a.T - blockIdx.x + gstride - 1) / gstride) : 0;
+
+    // ------------------------------------------------------------ producer
+    const bool producer = (tid == 0) && !a.wait.inject_stall;
+    uint64_t pol = 0;
+    if (producer) pol = l2_policy_evict_first();
+    int p_stage = 0;
+    int64_t p_tok = blockIdx.x;
+    const uint32_t row_bytes = (uint32_t)a.d * 2;
+    auto issue_next = [&]() {
+        mbar_arrive_expect_tx(&full[p_stage], row_bytes * a.n_src);
+        const unsigned char *g = a.src + p_tok * row_bytes;
+        unsigned char *dst = stages + (size_t)p_stage * a.stage_bytes;
+        for (int i = 0; i < a.n_src; ++i)
+            bulk_g2s(dst + (size_t)i * a.pitch, g + (int64_t)i * a.src_stride_bytes, row_bytes, &full[p_stage], pol);
+        if (++p_stage == a.nstages) p_stage = 0;
+        p_tok += gstride;
+    };
+    int issued = 0;
+    if (producer)
+        for (; issued < n_items && issued < a.nstages; ++issued) issue_next();
+
+    // ------------------------------------------------------------ constants
+    const int cbase = warp * CW;                // first channel of this warp
+    // pass-1 B fragments: query q (gain folded), bf16 hi in column 2q, lo in 2q+1
+    uint32_t bq[KS][2];
+    {
+        const int q = g4 >> 1, part = g4 & 1;
+#pragma unroll
+        for (int s = 0; s < KS; ++s)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = cbase + 16 * s + 8 * h + 2 * t4;
+                float v0 = 0.f, v1 = 0.f;
+                if (q < a.n_q) {
+                    v0 = __ldg(a.queries + (size_t)q * a.d + c);
+                    v1 = __ldg(a.queries + (size_t)q * a.d + c + 1);
+                    if (a.gain) { v0 *= __ldg(a.gain + c); v1 *= __ldg(a.gain + c + 1); }
+                }
+                float h0, l0, h1, l1;
+                split_bf16(v0, h0, l0);
+                split_bf16(v1, h1, l1);
+                bq[s][h] = part == 0 ? pack_bf16(h0, h1) : pack_bf16(l0, l1);
+            }
+    }
+    // head of this warp and the warps that share it
+    const int head = warp / a.wph;
+    const int gw0 = head * a.wph;
+    const float inv_dh = 1.f / (float)(CW * a.wph);
+    // ldmatrix row address of this lane inside a stage: source row lane%8,
+    // channel block (lane/8) of a 32-channel group
+    const uint32_t lrow = (uint32_t)(lane & 7) * a.pitch + (uint32_t)(cbase + 8 * (lane >> 3)) * 2;
+    const uint32_t stage0 = smem_u32(stages);
+
+    int s = 0;
+    uint32_t par = 0;
+    int64_t t = blockIdx.x;
+    for (int it = 0; it < n_items; ++it) {
+        mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
+        const uint32_t sa = stage0 + (uint32_t)s * a.stage_bytes + lrow;
+
+        // ---------------- pass 1: D1 = X Q, D2 = X X^T over the warp's channels
+        float d1[2][4], d2[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { d1[u][e] = 0.f; d2[u][e] = 0.f; }
+#pragma unroll
+        for (int s2 = 0; s2 < KS / 2; ++s2) {
+            uint32_t x0, x1, x2, x3;            // k-step 2*s2: (x0, x1); 2*s2+1: (x2, x3)
+            ldsm_x4(sa + 64 * s2, x0, x1, x2, x3);
+            mma_rows8(d1[0], x0, x1, bq[2 * s2][0], bq[2 * s2][1]);
+            mma_rows8(d2[0], x0, x1, x0, x1);
+            mma_rows8(d1[1], x2, x3, bq[2 * s2 + 1][0], bq[2 * s2 + 1][1]);
+            mma_rows8(d2[1], x2, x3, x2, x3);
+        }
+        const float dot = (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
+        const float q0 = d2[0][0] + d2[1][0];
+        const float q1 = d2[0][1] + d2[1][1];
+        // lane (i = g4, q = t4) holds dot_qi; lane 4i + i/2 holds sum(v_i^2)
+        float *rb = red + (size_t)(it & 1) * 40 * DM_WARPS;
+        rb[(t4 * 8 + g4) * DM_WARPS + warp] = dot;
+        if (t4 == (g4 >> 1)) rb[(32 + g4) * DM_WARPS + warp] = (g4 & 1) ? q1 : q0;
+        __syncthreads();
+        if (producer && it >= 1 && issued < n_items && !*abort_flag) { issue_next(); ++issued; }
+
+        // ---------------- softmax over sources: lane p = q*8 + i
+        const int q = lane >> 3, i = lane & 7;
+        float ss = 0.f, dt = 0.f;
+        for (int w = gw0; w < gw0 + a.wph; ++w) {
+            ss += rb[(32 + i) * DM_WARPS + w];
+            dt += rb[(q * 8 + i) * DM_WARPS + w];
+        }
+        const bool pv = i < a.n_src && q < NQ;
+        const float score = pv ? key_score(dt, ss, inv_dh, a.eps) : -INFINITY;
+        const float cmax = seg_max<8>(score);
+        const float e = pv ? __expf(score - cmax) : 0.f;
+        const float sum = seg_sum<8>(e);
+        const float alpha = pv ? e / sum : 0.f;
+        if (i == 0 && q < a.n_q && warp == gw0 && a.lse != nullptr && !*abort_flag)
+            a.lse[((int64_t)q * a.H + head) * a.T + t] = cmax + __logf(sum);
+
+        // A fragment of pass 2: row q = g4 (< 4), k = sources 2*t4, 2*t4+1 (hi) and +8 (lo)
+        const int srcl = (g4 & 3) * 8 + 2 * t4;
+        const float al0 = __shfl_sync(0xffffffffu, alpha, srcl);
+        const float al1 = __shfl_sync(0xffffffffu, alpha, srcl + 1);
+        uint32_t aa0 = 0u, aa2 = 0u;
+        if (g4 < NQ) {
+            float h0, l0, h1, l1;
+            split_bf16(al0, h0, l0);
+            split_bf16(al1, h1, l1);
+            aa0 = pack_bf16(h0, h1);
+            aa2 = pack_bf16(l0, l1);
+        }
+
+        // ---------------- pass 2: O = A X' per 8-channel block
+        const bool write = !*abort_flag && g4 < a.n_q;
+        unsigned char *ob = a.out + (int64_t)g4 * a.out_q_stride_bytes +
+                            (t * a.d + cbase + 2 * t4) * 2;
+#pragma unroll 4
+        for (int s2 = 0; s2 < KS / 2; ++s2) {
+            uint32_t y[4];
+            ldsm_x4_t(sa + 64 * s2, y[0], y[1], y[2], y[3]);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float o[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_rows8(o, aa0, aa2, y[m], y[m]);
+                if (write)
+                    *reinterpret_cast<uint32_t *>(ob + (32 * s2 + 8 * m) * 2) = f2_to_bf2(o[0], o[1]);
+            }
+        }
+        if (++s == a.nstages) { s = 0; par ^= 1u; }
+        t += gstride;
+    }
+
+    if (producer) {
+        int never = 0;
+        for (int it = issued > a.nstages ? issued - a.nstages : 0; it < issued; ++it)
+            mbar_wait_bounded(&full[it % a.nstages], (uint32_t)(it / a.nstages) & 1, &never, a.wait);
+    }
+}
+
+}  // namespace attnres

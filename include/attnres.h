@@ -203,6 +203,15 @@ attnres_status_t attnres_sync_status(void *stream);
 void attnres_debug_set_wait_timeout_ns(uint64_t ns);
 void attnres_debug_set_stall_injection(int enable);
 
+/*
+ * Kernel selection, meant for tests and measurements: 0 (default) lets the
+ * library pick (tensor-core kernel for bf16 reads with <= 8 sources and <= 4
+ * queries at d = 1024, 2048 or 4096; the general CUDA-core kernel otherwise);
+ * 1 forces the general kernel for Full / phase 1 / MHAR.  Both compute the
+ * same operation.  Applies to calls made afterwards.
+ */
+void attnres_debug_set_kernel_variant(int variant);
+
 /* Library version string, e.g. "attnres 0.1.0 sm_103a". */
 const char *attnres_version(void);
 

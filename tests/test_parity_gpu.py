@@ -341,3 +341,59 @@ def test_stall_injection_reports_timeout_and_context_survives():
     o, lse = attnres.attnres_block_phase1(src, q)
     attnres.attnres_sync_status()
     check_out(o, oracle.block_phase1(src_h, q_h)[0], BF16)
+
+
+# --------------------------------------------------------------- both kernels
+
+@pytest.fixture(params=[0, 1], ids=["auto", "general"])
+def kernel_variant(request):
+    """Runs a test with the automatic kernel choice (tensor-core kernel where it
+    applies) and with the general CUDA-core kernel forced."""
+    attnres.attnres_debug_set_kernel_variant(request.param)
+    yield request.param
+    attnres.attnres_debug_set_kernel_variant(0)
+
+
+@pytest.mark.parametrize("n_src,n_q,T,d", [(8, 4, 37, 4096), (8, 4, 150, 2048), (5, 3, 20, 1024),
+                                           (1, 1, 9, 4096), (2, 2, 33, 2048), (7, 4, 64, 1024),
+                                           (8, 1, 100, 4096)])
+def test_phase1_both_kernels(kernel_variant, n_src, n_q, T, d):
+    rng = _rng(n_src * 31 + n_q * 7 + T + d)
+    src = _sources(rng, n_src, T, d, BF16)
+    q = _queries(rng, n_q, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    o, lse = attnres.attnres_block_phase1(to_dev(src, BF16), to_dev(q, F32), to_dev(g, F32), 1e-6)
+    ro, rl = oracle.block_phase1(src, q, g, 1e-6)
+    check_out(o, ro, BF16, what="o")
+    check_lse(lse, rl)
+
+
+@pytest.mark.parametrize("H,d,T,n_src", [(8, 4096, 21, 8), (4, 4096, 13, 6), (2, 2048, 40, 8),
+                                         (8, 2048, 17, 3), (4, 1024, 25, 8)])
+def test_mhar_both_kernels(kernel_variant, H, d, T, n_src):
+    rng = _rng(H * 13 + d + T)
+    src = _sources(rng, n_src, T, d, BF16)
+    q = (rng.standard_normal((4, H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
+    out, lse = attnres.mhar_fwd(to_dev(src, BF16), to_dev(q, F32), want_lse=True)
+    ro, rl = oracle.mhar(src, q, want_lse=True)
+    check_out(out, ro, BF16)
+    check_lse(lse, rl)
+
+
+def test_kernels_agree_closely():
+    """The two kernels compute the same read; their bf16 outputs may differ by
+    at most one rounding step."""
+    rng = _rng(99)
+    T, d = 200, 4096
+    src = to_dev(_sources(rng, 8, T, d, BF16), BF16)
+    q = to_dev(_queries(rng, 4, d), F32)
+    o1, l1 = attnres.attnres_block_phase1(src, q)
+    attnres.attnres_debug_set_kernel_variant(1)
+    try:
+        o2, l2 = attnres.attnres_block_phase1(src, q)
+    finally:
+        attnres.attnres_debug_set_kernel_variant(0)
+    a, b = to_host(o1), to_host(o2)
+    # one bf16 step of the larger value, plus float32 summation-order noise
+    assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-4 * np.abs(a).max())
+    assert np.abs(to_host(l1) - to_host(l2)).max() < 1e-4
