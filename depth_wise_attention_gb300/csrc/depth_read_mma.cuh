@@ -12,9 +12,12 @@
 //            X = [8 sources x 16 channels] (rows 8..15 zero), Q = the queries
 //            split into bf16 hi + lo parts (columns 2q, 2q+1), so
 //            dot_qi = D1[i][2q] + D1[i][2q+1] and sum(v_i^2) = D2[i][i];
-//   pass 2:  O = A X' per 8-channel block, A = [4 queries x (8 sources hi |
-//            8 sources lo)] holding alpha split into bf16 hi + lo parts and
-//            X' = the same 8 source rows stacked twice (ldmatrix .trans).
+//   pass 2:  O^T = X'^T A per 16-channel block: X'^T = [16 channels x (8
+//            sources | the same 8 sources)] (ldmatrix .trans), A = [(8 sources
+//            hi | 8 sources lo) x 4 queries] holding alpha split into bf16 hi
+//            and lo parts; movmatrix turns the result back into channel pairs
+//            per query, which are staged in the shared-memory rows this warp
+//            has finished reading and leave with one bulk store per query.
 // The hi/lo split keeps the queries and the weights to about 16 mantissa
 // bits; products are exact and sums are fp32.
 //
@@ -57,7 +60,7 @@ struct DepthReadMmaArgs {
 
 struct DMLayout {
     static constexpr size_t bar_bytes = 128;
-    // red[2][40 values][8 warps]: dots (q*8+i) then sums of squares (32+i)
+    // red[2][8 warps][40 values]: dots (q*8+i) then sums of squares (32+i)
     static constexpr size_t red_floats = 2 * 40 * DM_WARPS;
     static constexpr size_t aux_bytes = bar_bytes + 4 * red_floats;
 };
@@ -81,6 +84,38 @@ __device__ __forceinline__ void mma_rows8(float (&c)[4], uint32_t a0, uint32_t a
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// Full m16n8k16 with all four A registers given.
+__device__ __forceinline__ void mma_full(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Transpose an 8x8 matrix of 16-bit elements held one row pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Shared -> global bulk copy (bytes % 16 == 0, both 16-byte aligned).
+__device__ __forceinline__ void bulk_s2g(void *gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // bf16 hi/lo split of x: hi = rn(x), lo = rn(x - hi).
@@ -204,8 +239,22 @@ __global__ void __launch_bounds__(DM_THREADS, 1) depth_read_mma_kernel(const Dep
         const float q1 = d2[0][1] + d2[1][1];
         // lane (i = g4, q = t4) holds dot_qi; lane 4i + i/2 holds sum(v_i^2)
         float *rb = red + (size_t)(it & 1) * 40 * DM_WARPS;
-        rb[(t4 * 8 + g4) * DM_WARPS + warp] = dot;
-        if (t4 == (g4 >> 1)) rb[(32 + g4) * DM_WARPS + warp] = (g4 & 1) ? q1 : q0;
+        rb[warp * 40 + t4 * 8 + g4] = dot;
+        if (t4 == (g4 >> 1)) rb[warp * 40 + 32 + g4] = (g4 & 1) ? q1 : q0;
+        // the previous item's output bulk stores must have read their shared rows
+        // before the barrier that lets the producer refill that stage
+        if (lane < a.n_q && it >= 1) bulk_wait_read0();
+        if (a.n_src < a.n_q && it >= 1) {
+            // Rows n_src..n_q-1 of the previous stage held outputs but are never
+            // reloaded: restore their zeros (this warp's channel slice) once the
+            // bulk stores have read them.
+            __syncwarp();
+            const int sp = s == 0 ? a.nstages - 1 : s - 1;
+            for (int row = a.n_src; row < a.n_q; ++row)
+                for (int b = lane * 16; b < CW * 2; b += 32 * 16)
+                    *reinterpret_cast<uint4 *>(stages + (size_t)sp * a.stage_bytes + (size_t)row * a.pitch +
+                                               (size_t)cbase * 2 + b) = make_uint4(0u, 0u, 0u, 0u);
+        }
         __syncthreads();
         if (producer && it >= 1 && issued < n_items && !*abort_flag) { issue_next(); ++issued; }
 
@@ -213,8 +262,8 @@ __global__ void __launch_bounds__(DM_THREADS, 1) depth_read_mma_kernel(const Dep
         const int q = lane >> 3, i = lane & 7;
         float ss = 0.f, dt = 0.f;
         for (int w = gw0; w < gw0 + a.wph; ++w) {
-            ss += rb[(32 + i) * DM_WARPS + w];
-            dt += rb[(q * 8 + i) * DM_WARPS + w];
+            ss += rb[w * 40 + 32 + i];
+            dt += rb[w * 40 + q * 8 + i];
         }
         const bool pv = i < a.n_src && q < NQ;
         const float score = pv ? key_score(dt, ss, inv_dh, a.eps) : -INFINITY;
@@ -225,39 +274,60 @@ __global__ void __launch_bounds__(DM_THREADS, 1) depth_read_mma_kernel(const Dep
         if (i == 0 && q < a.n_q && warp == gw0 && a.lse != nullptr && !*abort_flag)
             a.lse[((int64_t)q * a.H + head) * a.T + t] = cmax + __logf(sum);
 
-        // A fragment of pass 2: row q = g4 (< 4), k = sources 2*t4, 2*t4+1 (hi) and +8 (lo)
+        // B fragment of pass 2: k = sources 2*t4, 2*t4+1 (hi) and +8 (lo), column q = g4 (< 4)
         const int srcl = (g4 & 3) * 8 + 2 * t4;
         const float al0 = __shfl_sync(0xffffffffu, alpha, srcl);
         const float al1 = __shfl_sync(0xffffffffu, alpha, srcl + 1);
-        uint32_t aa0 = 0u, aa2 = 0u;
+        uint32_t bb0 = 0u, bb1 = 0u;
         if (g4 < NQ) {
             float h0, l0, h1, l1;
             split_bf16(al0, h0, l0);
             split_bf16(al1, h1, l1);
-            aa0 = pack_bf16(h0, h1);
-            aa2 = pack_bf16(l0, l1);
+            bb0 = pack_bf16(h0, h1);
+            bb1 = pack_bf16(l0, l1);
         }
 
-        // ---------------- pass 2: O = A X' per 8-channel block
-        const bool write = !*abort_flag && g4 < a.n_q;
-        unsigned char *ob = a.out + (int64_t)g4 * a.out_q_stride_bytes +
-                            (t * a.d + cbase + 2 * t4) * 2;
+        // ---------------- pass 2: O^T = X'^T A per 16-channel block
+        // After movmatrix lane (q = g4, t4) holds channels 2*t4, 2*t4+1 of the
+        // block's two 8-channel halves; it stages them in stage row q (q < 4),
+        // at the channels this warp has already consumed.
+        const uint32_t orow = stage0 + (uint32_t)s * a.stage_bytes + (uint32_t)(g4 & 3) * a.pitch +
+                              (uint32_t)(cbase + 2 * t4) * 2;
+        const bool keep = g4 < NQ;
 #pragma unroll 4
         for (int s2 = 0; s2 < KS / 2; ++s2) {
             uint32_t y[4];
             ldsm_x4_t(sa + 64 * s2, y[0], y[1], y[2], y[3]);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
+            for (int h = 0; h < 2; ++h) {
                 float o[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_rows8(o, aa0, aa2, y[m], y[m]);
-                if (write)
-                    *reinterpret_cast<uint32_t *>(ob + (32 * s2 + 8 * m) * 2) = f2_to_bf2(o[0], o[1]);
+                mma_full(o, y[2 * h], y[2 * h + 1], y[2 * h], y[2 * h + 1], bb0, bb1);
+                const uint32_t lo8 = movmatrix_t(f2_to_bf2(o[0], o[1]));   // channels +0..7
+                const uint32_t hi8 = movmatrix_t(f2_to_bf2(o[2], o[3]));   // channels +8..15
+                if (keep) {
+                    sts32(orow + (uint32_t)(32 * s2 + 16 * h) * 2, lo8);
+                    sts32(orow + (uint32_t)(32 * s2 + 16 * h + 8) * 2, hi8);
+                }
             }
+        }
+        // one bulk store per query row of this warp's channel slice
+        fence_proxy_async_smem();
+        __syncwarp();
+        // (bulk-copy groups belong to the issuing thread: lane q issues, commits
+        // and later waits for the store of query q)
+        if (lane < a.n_q) {
+            if (!*abort_flag)
+                bulk_s2g(a.out + (int64_t)lane * a.out_q_stride_bytes + (t * a.d + cbase) * 2,
+                         stage0 + (uint32_t)s * a.stage_bytes + (uint32_t)lane * a.pitch + (uint32_t)cbase * 2,
+                         (uint32_t)CW * 2);
+            bulk_commit();
         }
         if (++s == a.nstages) { s = 0; par ^= 1u; }
         t += gstride;
     }
 
+    // outputs must be written before the CTA exits
+    if (lane < a.n_q) bulk_wait0();
     if (producer) {
         int never = 0;
         for (int it = issued > a.nstages ? issued - a.nstages : 0; it < issued; ++it)
