@@ -132,20 +132,19 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
     uint64_t pol = 0;
     if (producer) pol = l2_policy_evict_first();
     int64_t next_row = rho0;                              // next row to load
+    int p_slot = 0;                                       // its ring slot: (next_row - rho0) % ring
     auto issue_row = [&](int64_t rho) {
-        const int s = (int)(rho % ring);
-        mbar_arrive_expect_tx(&bars[s], (uint32_t)slot_bytes);
+        mbar_arrive_expect_tx(&bars[p_slot], (uint32_t)slot_bytes);
         const unsigned char *g = a.src + (rho * d + (int64_t)rank * ch) * ES;
-        unsigned char *dst = ringbuf + (size_t)s * slot_bytes;
+        unsigned char *dst = ringbuf + (size_t)p_slot * slot_bytes;
         for (int i = 0; i < nsrc; ++i)
             bulk_g2s(dst + (size_t)i * row_bytes, g + (int64_t)i * a.src_stride_bytes, (uint32_t)row_bytes,
-                     &bars[s], pol);
+                     &bars[p_slot], pol);
+        if (++p_slot == ring) p_slot = 0;
     };
     const int64_t prolog_end = min(te, tb + 1 + MSAR_LA);
     if (producer)
         for (; next_row < prolog_end; ++next_row) issue_row(next_row);
-    auto row_parity = [&](int64_t rho) { return (uint32_t)((rho - rho0) / ring) & 1u; };
-    auto slot_ptr = [&](int64_t rho) { return ringbuf + (size_t)(rho % ring) * slot_bytes; };
 
     float2 zprev[MSAR_M];
     float mixp[5];
@@ -154,6 +153,9 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
 #pragma unroll
     for (int o = 0; o < 5; ++o) mixp[o] = 0.f;
 
+    // ring slot and mbarrier phase parity of the current token's row
+    int cur_slot = (int)(tb - rho0);
+    uint32_t cur_par = 0;
     for (int64_t n = 0; n <= ntok; ++n) {
         const int64_t t = tb + n;
         const bool is_tok = n < ntok;
@@ -164,30 +166,38 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
         for (int q = 0; q < MSAR_NS; ++q) v[q] = 0.f;
         if (is_tok) {
             if (n == 0) {
-                for (int64_t rho = rho0; rho <= t; ++rho)
-                    mbar_wait_bounded(&bars[rho % ring], row_parity(rho), abort_flag, a.wait);
+                // rows rho0..t occupy slots 0..t-rho0 for the first time
+                for (int sl = 0; sl <= cur_slot; ++sl) mbar_wait_bounded(&bars[sl], 0u, abort_flag, a.wait);
             } else {
-                mbar_wait_bounded(&bars[t % ring], row_parity(t), abort_flag, a.wait);
+                mbar_wait_bounded(&bars[cur_slot], cur_par, abort_flag, a.wait);
             }
-            const unsigned char *cur = slot_ptr(t);
 #pragma unroll
             for (int i = 0; i < MSAR_SMAX; ++i) {
-                x[i] = make_float2(0.f, 0.f);
-                if (i < nsrc) x[i] = P2::ld(cur + (size_t)i * row_bytes + (size_t)cl * ES);
 #pragma unroll
                 for (int r = 0; r < MSAR_M - 1; ++r) u[i][r] = make_float2(0.f, 0.f);
             }
-            // causal depthwise convolutions of the three expanded streams
+            // causal depthwise convolutions: each history row t-j is read once
+            // and applied to every stream whose kernel reaches back that far
+            for (int j = 0; j <= hist; ++j) {
+                if (t - j < 0) break;
+                int sl = cur_slot - j;
+                if (sl < 0) sl += ring;
+                const unsigned char *row = ringbuf + (size_t)sl * slot_bytes + (size_t)cl * ES;
+                float2 xs[MSAR_SMAX];
 #pragma unroll
-            for (int r = 0; r < MSAR_M - 1; ++r) {
-                for (int j = 0; j < a.k[r]; ++j) {
-                    const int64_t rho = t - j;
-                    if (rho < 0) break;
-                    const float2 w = *reinterpret_cast<const float2 *>(wconv + (size_t)(koff[r] + j) * ch + cl);
-                    const unsigned char *row = slot_ptr(rho) + (size_t)cl * ES;
+                for (int i = 0; i < MSAR_SMAX; ++i)
+                    xs[i] = i < nsrc ? P2::ld(row + (size_t)i * row_bytes) : make_float2(0.f, 0.f);
+                if (j == 0) {
 #pragma unroll
-                    for (int i = 0; i < MSAR_SMAX; ++i)
-                        if (i < nsrc) u[i][r] = ffma2(w, P2::ld(row + (size_t)i * row_bytes), u[i][r]);
+                    for (int i = 0; i < MSAR_SMAX; ++i) x[i] = xs[i];
+                }
+#pragma unroll
+                for (int r = 0; r < MSAR_M - 1; ++r) {
+                    if (j < a.k[r]) {
+                        const float2 w = *reinterpret_cast<const float2 *>(wconv + (size_t)(koff[r] + j) * ch + cl);
+#pragma unroll
+                        for (int i = 0; i < MSAR_SMAX; ++i) u[i][r] = ffma2(w, xs[i], u[i][r]);
+                    }
                 }
             }
             // per (source, stream): sum of squares and the stream-query dot
@@ -201,6 +211,7 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
                     v[(i * MSAR_M + r) * 2 + 1] = dot2(u[i][r - 1], wq[r]);
                 }
             }
+            if (++cur_slot == ring) { cur_slot = 0; cur_par ^= 1u; }
         }
         // ---- reduce over the CTA: butterfly in each warp, then across warps
         butterfly_reduce<MSAR_NS>(v, lane);
@@ -295,7 +306,7 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
         int never = 0;
         const int64_t lo = next_row - ring > rho0 ? next_row - ring : rho0;
         for (int64_t rho = lo; rho < next_row; ++rho)
-            mbar_wait_bounded(&bars[rho % ring], row_parity(rho), &never, a.wait);
+            mbar_wait_bounded(&bars[(rho - rho0) % ring], (uint32_t)((rho - rho0) / ring) & 1u, &never, a.wait);
     }
 }
 
