@@ -31,16 +31,20 @@ if ROOT not in sys.path:
 
 METRIC = "Block AttnRes fwd tokens/s (d=4096,N=8,S=4); achieved HBM GB/s vs GB300 peak"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["depth_wise_attention_gb300/csrc/depth_read.cuh",
-                  "depth_wise_attention_gb300/csrc/common.cuh",
-                  "depth_wise_attention_gb300/csrc/phase2.cuh",
-                  "depth_wise_attention_gb300/csrc/msar.cu",
-                  "depth_wise_attention_gb300/csrc/attnres_api.cu"]
+# Source files that define each profiled kernel; a committed ncu summary is
+# only used while these files are unchanged.
+CSRC = "depth_wise_attention_gb300/csrc/"
+KERNEL_SOURCES = {
+    "depth_read_mma": [CSRC + "depth_read_mma.cuh", CSRC + "common.cuh", CSRC + "kernels_mma.cu"],
+    "depth_read": [CSRC + "depth_read.cuh", CSRC + "common.cuh"],
+    "phase2": [CSRC + "phase2.cuh", CSRC + "common.cuh", CSRC + "kernels_phase2.cu"],
+    "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
+}
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -54,7 +58,7 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def profile_traffic(kernel_tag: str):
+def profile_traffic(kernel_tag: str, kernel: str):
     """dram bytes per launch of `kernel_tag` from the committed ncu summary, if
     it was taken on the current kernel sources (else None)."""
     path = os.path.join(PROFILE_DIR, f"{kernel_tag}.txt")
@@ -66,7 +70,7 @@ def profile_traffic(kernel_tag: str):
             if "=" in line and not line.startswith("#"):
                 k, v = line.split("=", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_sources_sha") != kernel_sources_sha():
+    if vals.get("kernel_sources_sha") != kernel_sources_sha(kernel):
         return None
     try:
         return float(vals["traffic_bytes_per_launch_full_size"])
@@ -144,7 +148,8 @@ class BlockWorkload:
         self.merge_bytes_per_token = 3 * d * b + 4
         self.bytes_per_token = self.phase1_bytes_per_token + (S - 1) * self.merge_bytes_per_token
         self.launches_per_step = 1 + (S - 1)
-        self.dominant = "depth_read_kernel (phase 1)"
+        self.dominant = "depth_read_mma_kernel (phase 1)"
+        self.dominant_src = "depth_read_mma"
         self.profile_tag = f"ncu_phase1_block_d{d}"
 
     def config(self):
@@ -230,7 +235,8 @@ class MharWorkload(BlockWorkload):
         self.bytes_per_token = N * d * 2 + S * d * 2
         self.phase1_bytes_per_token = self.bytes_per_token
         self.launches_per_step = 1
-        self.dominant = "depth_read_kernel (MHAR)"
+        self.dominant = "depth_read_mma_kernel (MHAR)"
+        self.dominant_src = "depth_read_mma"
         self.profile_tag = f"ncu_mhar_d{d}_H{H}"
 
     def config(self):
@@ -297,6 +303,7 @@ class MsarWorkload(BlockWorkload):
         self.phase1_bytes_per_token = self.bytes_per_token
         self.launches_per_step = 1
         self.dominant = "msar_kernel"
+        self.dominant_src = "msar"
         self.profile_tag = f"ncu_msar_d{d}"
 
     def config(self):
@@ -370,6 +377,7 @@ class FullDepthWorkload(BlockWorkload):
         self.phase1_bytes_per_token = (L + 1) * d * 2           # the deepest layer's read
         self.launches_per_step = L
         self.dominant = "depth_read_kernel (Full, layer 64)"
+        self.dominant_src = "depth_read"
         self.profile_tag = f"ncu_full_depth_d{d}"
 
     def config(self):
@@ -534,7 +542,7 @@ def run_cuda(args):
     dom_bytes = wl.dominant_bytes_per_launch()
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     step_gbs = wl.bytes_per_token * wl.T / (ms_per_step / 1e3) / 1e9
-    traffic = profile_traffic(wl.profile_tag)
+    traffic = profile_traffic(wl.profile_tag, wl.dominant_src)
 
     # ---------------- end to end: host buffers, copies inside the timed region
     wl.setup_host()
