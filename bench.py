@@ -490,6 +490,11 @@ def max_over_ranks(x: float, world: int, device) -> float:
 # arms
 # --------------------------------------------------------------------------
 
+def aggregate(tokens_per_rank: int, steps: int, world: int, elapsed_ms_max: float):
+    """Whole-job throughput: all ranks' tokens over the slowest rank's time."""
+    return tokens_per_rank * steps * world / (elapsed_ms_max / 1e3)
+
+
 def run_cuda(args):
     import torch
     from depth_wise_attention_gb300 import attnres
@@ -534,8 +539,7 @@ def run_cuda(args):
     dom_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
 
-    tokens = wl.T * K * world
-    value = tokens / (elapsed_ms / 1e3)
+    value = aggregate(wl.T, K, world, elapsed_ms)
     ms_per_step = elapsed_ms / K
     peaks, peaks_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
