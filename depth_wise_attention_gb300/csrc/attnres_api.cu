@@ -169,11 +169,12 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
 
     // Tensor-core path: bf16, <= 8 sources, <= 4 queries, d = 1024/2048/4096,
     // heads that are whole multiples of the per-warp channel slice.
-    if (dt == ATTNRES_BF16 && n_src <= 8 && n_q <= 4 && d % 128 == 0 && 8 % H == 0 &&
+    if (dt == ATTNRES_BF16 && n_src <= 8 && n_q <= 4 && (d == 1024 || d == 2048 || d == 4096) &&
         g_kernel_variant.load() == 0) {
-        const int ks = (int)(d / 128);
+        const int nw = d == 1024 ? 8 : 16;
+        const int ks = (int)(d / (16 * nw));
         KernelRef kr;
-        if (lookup_depth_read_mma(pow2ceil((int)n_q), ks, &kr)) {
+        if (nw % H == 0 && lookup_depth_read_mma(pow2ceil((int)n_q), ks, nw, &kr)) {
             DeviceInfo *dev = nullptr;
             st = device_info(&dev);
             if (st != ATTNRES_OK) return st;
@@ -186,7 +187,7 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
             if (nstages >= 2) {
                 const size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
                 int occ = 0;
-                st = prepare_kernel(kr.fn, smem, DM_THREADS, &occ);
+                st = prepare_kernel(kr.fn, smem, nw * 32, &occ);
                 if (st != ATTNRES_OK) return st;
                 DepthReadMmaArgs m;
                 m.src = static_cast<const unsigned char *>(src);
@@ -196,7 +197,7 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
                 m.d = (int)d;
                 m.n_q = (int)n_q;
                 m.H = (int)H;
-                m.wph = (int)(8 / H);
+                m.wph = (int)(nw / H);
                 m.queries = queries;
                 m.gain = gain;
                 m.eps = eps;
@@ -210,7 +211,7 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
                 const int64_t max_grid = (int64_t)dev->sms * occ;
                 const int grid = (int)(T < max_grid ? T : max_grid);
                 void *args[] = {&m};
-                cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(DM_THREADS), args, smem,
+                cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(nw * 32), args, smem,
                                                  static_cast<cudaStream_t>(stream));
                 if (e != cudaSuccess) return cuda_fail(e, "depth_read_mma launch");
                 return ATTNRES_OK;

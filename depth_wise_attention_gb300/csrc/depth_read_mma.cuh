@@ -21,10 +21,10 @@
 // The hi/lo split keeps the queries and the weights to about 16 mantissa
 // bits; products are exact and sums are fp32.
 //
-// Work split: one token per item; warp w owns channels [w*cw, (w+1)*cw)
-// (cw = d/8); its partial dots and sums of squares go to a small shared
+// Work split: one token per item; warp w of NW owns channels [w*cw, (w+1)*cw)
+// (cw = d/NW); its partial dots and sums of squares go to a small shared
 // table, one CTA barrier publishes them, and each warp computes the softmax
-// of its head (all 8 warps for H = 1) redundantly.  Stages, producer and
+// of its head (all NW warps for H = 1) redundantly.  Stages, producer and
 // bounded waits are as in depth_read.cuh; source rows in a stage are padded
 // by 16 bytes so ldmatrix row addresses fall in distinct banks.
 #pragma once
@@ -33,8 +33,7 @@
 
 namespace attnres {
 
-constexpr int DM_WARPS = 8;
-constexpr int DM_THREADS = DM_WARPS * 32;
+constexpr int DM_MAX_WARPS = 16;
 constexpr int DM_MAX_STAGES = 6;
 
 struct DepthReadMmaArgs {
@@ -45,7 +44,7 @@ struct DepthReadMmaArgs {
     int d;
     int n_q;                      // <= NQ
     int H;                        // heads
-    int wph;                      // warps per head (8 / H)
+    int wph;                      // warps per head (NW / H)
     const float *queries;         // [n_q][d]
     const float *gain;            // [d] or nullptr
     float eps;
@@ -60,8 +59,8 @@ struct DepthReadMmaArgs {
 
 struct DMLayout {
     static constexpr size_t bar_bytes = 128;
-    // red[2][8 warps][40 values]: dots (q*8+i) then sums of squares (32+i)
-    static constexpr size_t red_floats = 2 * 40 * DM_WARPS;
+    // red[2][NW warps][40 values]: dots (q*8+i) then sums of squares (32+i)
+    static constexpr size_t red_floats = 2 * 40 * DM_MAX_WARPS;
     static constexpr size_t aux_bytes = bar_bytes + 4 * red_floats;
 };
 
@@ -127,8 +126,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo_ch, float hi_ch) {
     return f2_to_bf2(lo_ch, hi_ch);
 }
 
-template <int NQ, int KS>
-__global__ void __launch_bounds__(DM_THREADS, 1) depth_read_mma_kernel(const DepthReadMmaArgs a) {
+template <int NQ, int KS, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthReadMmaArgs a) {
     static_assert(NQ <= 4, "at most 4 queries (8 MMA columns: hi and lo per query)");
     using L = DMLayout;
     constexpr int CW = KS * 16;                 // channels per warp
@@ -152,7 +151,7 @@ __global__ void __launch_bounds__(DM_THREADS, 1) depth_read_mma_kernel(const Dep
     // (times a zero weight): make them zero, not stale bits that could be NaN.
     for (int s = 0; s < a.nstages; ++s)
         for (int i = a.n_src; i < 8; ++i)
-            for (int b = tid * 16; b < a.d * 2; b += DM_THREADS * 16)
+            for (int b = tid * 16; b < a.d * 2; b += NW * 32 * 16)
                 *reinterpret_cast<uint4 *>(stages + (size_t)s * a.stage_bytes + (size_t)i * a.pitch + b) =
                     make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
@@ -238,7 +237,7 @@ __global__ void __launch_bounds__(DM_THREADS, 1) depth_read_mma_kernel(const Dep
         const float q0 = d2[0][0] + d2[1][0];
         const float q1 = d2[0][1] + d2[1][1];
         // lane (i = g4, q = t4) holds dot_qi; lane 4i + i/2 holds sum(v_i^2)
-        float *rb = red + (size_t)(it & 1) * 40 * DM_WARPS;
+        float *rb = red + (size_t)(it & 1) * 40 * NW;
         rb[warp * 40 + t4 * 8 + g4] = dot;
         if (t4 == (g4 >> 1)) rb[warp * 40 + 32 + g4] = (g4 & 1) ? q1 : q0;
         // the previous item's output bulk stores must have read their shared rows

@@ -20,8 +20,8 @@ bool lookup_depth_read_bf16(int nq, int vpt, bool mh, bool multi, KernelRef *out
 bool lookup_depth_read_bf16_multi(int nq, int vpt, bool mh, KernelRef *out);
 bool lookup_depth_read_f32_multi(int nq, int vpt, bool mh, KernelRef *out);
 
-// depth_read_mma_kernel<nq, ks> (bf16 only; ks = d / 128 k-steps per warp)
-bool lookup_depth_read_mma(int nq, int ks, KernelRef *out);
+// depth_read_mma_kernel<nq, ks, nw> (bf16 only; nw warps of 16*ks channels, d = 16*ks*nw)
+bool lookup_depth_read_mma(int nq, int ks, int nw, KernelRef *out);
 
 // phase2_merge_kernel<T, vpt>
 bool lookup_phase2(int dt, int vpt, KernelRef *out);
