@@ -59,8 +59,11 @@ struct DepthReadMmaArgs {
 
 struct DMLayout {
     static constexpr size_t bar_bytes = 128;
-    // red[2][NW warps][40 values]: dots (q*8+i) then sums of squares (32+i)
-    static constexpr size_t red_floats = 2 * 40 * DM_MAX_WARPS;
+    // red[2][40 values][RS]: for each value (dots q*8+i, then sums of squares
+    // 32+i) the partial of every warp; row stride RS = 20 floats keeps the
+    // 16-float rows 16-byte aligned and the writes at most 4-way conflicting
+    static constexpr int RS = 20;
+    static constexpr size_t red_floats = 2 * 40 * RS;
     static constexpr size_t aux_bytes = bar_bytes + 4 * red_floats;
 };
 
@@ -98,6 +101,14 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
+}
+// Store four 8x8 matrices of 16-bit elements transposed: lane 8j + r gives
+// the shared address of stored row r of matrix j (= column r of the fragment).
+__device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                          uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
 }
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -237,9 +248,10 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
         const float q0 = d2[0][0] + d2[1][0];
         const float q1 = d2[0][1] + d2[1][1];
         // lane (i = g4, q = t4) holds dot_qi; lane 4i + i/2 holds sum(v_i^2)
-        float *rb = red + (size_t)(it & 1) * 40 * NW;
-        rb[warp * 40 + t4 * 8 + g4] = dot;
-        if (t4 == (g4 >> 1)) rb[warp * 40 + 32 + g4] = (g4 & 1) ? q1 : q0;
+        constexpr int RS = L::RS;
+        float *rb = red + (size_t)(it & 1) * 40 * RS;
+        rb[(t4 * 8 + g4) * RS + warp] = dot;
+        if (t4 == (g4 >> 1)) rb[(32 + g4) * RS + warp] = (g4 & 1) ? q1 : q0;
         // the previous item's output bulk stores must have read their shared rows
         // before the barrier that lets the producer refill that stage
         if (lane < a.n_q && it >= 1) bulk_wait_read0();
@@ -260,9 +272,19 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
         // ---------------- softmax over sources: lane p = q*8 + i
         const int q = lane >> 3, i = lane & 7;
         float ss = 0.f, dt = 0.f;
-        for (int w = gw0; w < gw0 + a.wph; ++w) {
-            ss += rb[w * 40 + 32 + i];
-            dt += rb[w * 40 + q * 8 + i];
+        {
+            const float *ps = rb + (32 + i) * RS + gw0;
+            const float *pd = rb + (q * 8 + i) * RS + gw0;
+            if (a.wph % 4 == 0) {
+                for (int w = 0; w < a.wph; w += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(ps + w);
+                    const float4 y = *reinterpret_cast<const float4 *>(pd + w);
+                    ss += (x.x + x.y) + (x.z + x.w);
+                    dt += (y.x + y.y) + (y.z + y.w);
+                }
+            } else {
+                for (int w = 0; w < a.wph; ++w) { ss += ps[w]; dt += pd[w]; }
+            }
         }
         const bool pv = i < a.n_src && q < NQ;
         const float score = pv ? key_score(dt, ss, inv_dh, a.eps) : -INFINITY;
@@ -287,27 +309,21 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
         }
 
         // ---------------- pass 2: O^T = X'^T A per 16-channel block
-        // After movmatrix lane (q = g4, t4) holds channels 2*t4, 2*t4+1 of the
-        // block's two 8-channel halves; it stages them in stage row q (q < 4),
-        // at the channels this warp has already consumed.
-        const uint32_t orow = stage0 + (uint32_t)s * a.stage_bytes + (uint32_t)(g4 & 3) * a.pitch +
-                              (uint32_t)(cbase + 2 * t4) * 2;
-        const bool keep = g4 < NQ;
+        // The result tiles are [channels x queries]; stmatrix .trans writes them
+        // back as query rows of 8 channels into stage rows 0..7 at the channels
+        // this warp has already consumed (queries 4..7 are zero columns, so rows
+        // 4..7 only ever receive zeros there).
+        const uint32_t orow = stage0 + (uint32_t)s * a.stage_bytes + (uint32_t)(lane & 7) * a.pitch +
+                              (uint32_t)(cbase + 8 * (lane >> 3)) * 2;
 #pragma unroll 4
         for (int s2 = 0; s2 < KS / 2; ++s2) {
             uint32_t y[4];
             ldsm_x4_t(sa + 64 * s2, y[0], y[1], y[2], y[3]);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float o[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_full(o, y[2 * h], y[2 * h + 1], y[2 * h], y[2 * h + 1], bb0, bb1);
-                const uint32_t lo8 = movmatrix_t(f2_to_bf2(o[0], o[1]));   // channels +0..7
-                const uint32_t hi8 = movmatrix_t(f2_to_bf2(o[2], o[3]));   // channels +8..15
-                if (keep) {
-                    sts32(orow + (uint32_t)(32 * s2 + 16 * h) * 2, lo8);
-                    sts32(orow + (uint32_t)(32 * s2 + 16 * h + 8) * 2, hi8);
-                }
-            }
+            float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_full(o0, y[0], y[1], y[0], y[1], bb0, bb1);
+            mma_full(o1, y[2], y[3], y[2], y[3], bb0, bb1);
+            stsm_x4_t(orow + 64 * s2, f2_to_bf2(o0[0], o0[1]), f2_to_bf2(o0[2], o0[3]),
+                      f2_to_bf2(o1[0], o1[1]), f2_to_bf2(o1[2], o1[3]));
         }
         // one bulk store per query row of this warp's channel slice
         fence_proxy_async_smem();
