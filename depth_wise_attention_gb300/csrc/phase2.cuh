@@ -62,23 +62,36 @@ __global__ void __launch_bounds__(P2_THREADS) phase2_merge_kernel(const MergeArg
         }
     }
 
-    int buf = 0;
-    for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, buf ^= 1) {
+    // Software pipeline over this CTA's tiles: the loads of tile n+1 are in
+    // flight while tile n is reduced, merged and stored.
+    uint4 ov[VPT], pv[VPT];
+    float lv = 0.f;
+    auto load_tile = [&](int64_t tile, uint4 (&o_)[VPT], uint4 (&p_)[VPT], float &l_) {
         const int64_t t = tile * a.tt + r;
-        const bool row_ok = t < a.T;
-        uint4 ov[VPT], pv[VPT];
-        float2 ss = make_float2(0.f, 0.f), dt = make_float2(0.f, 0.f);
+        const bool ok = tile < a.ntiles && t < a.T;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            if (row_ok && vok[k]) {
+            if (ok && vok[k]) {
                 const int64_t off = (t * a.d + (int64_t)vid[k] * EPV) * E::BYTES;
-                ov[k] = ldg128_stream(a.o + off);
-                pv[k] = ldg128_stream(a.partial + off);
+                o_[k] = ldg128_stream(a.o + off);
+                p_[k] = ldg128_stream(a.partial + off);
             } else {
-                ov[k] = make_uint4(0, 0, 0, 0);
-                pv[k] = make_uint4(0, 0, 0, 0);
+                o_[k] = make_uint4(0, 0, 0, 0);
+                p_[k] = make_uint4(0, 0, 0, 0);
             }
         }
+        l_ = ok ? __ldg(a.lse + t) : 0.f;
+    };
+    int64_t tile = blockIdx.x;
+    load_tile(tile, ov, pv, lv);
+    int buf = 0;
+    for (; tile < a.ntiles; tile += gridDim.x, buf ^= 1) {
+        const int64_t t = tile * a.tt + r;
+        const bool row_ok = t < a.T;
+        uint4 on[VPT], pn[VPT];
+        float ln;
+        load_tile(tile + gridDim.x, on, pn, ln);
+        float2 ss = make_float2(0.f, 0.f), dt = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             float2 x[NP];
@@ -104,9 +117,8 @@ __global__ void __launch_bounds__(P2_THREADS) phase2_merge_kernel(const MergeArg
         }
         if (row_ok) {
             const float sp = key_score(tdt, tss, inv_d, a.eps);
-            const float l = __ldg(a.lse + t);
-            const float M = fmaxf(l, sp);
-            const float ea = __expf(l - M), eb = __expf(sp - M);
+            const float M = fmaxf(lv, sp);
+            const float ea = __expf(lv - M), eb = __expf(sp - M);
             const float inv = 1.f / (ea + eb);
             const float2 ca = make_float2(ea * inv, ea * inv), cb = make_float2(eb * inv, eb * inv);
 #pragma unroll
@@ -116,15 +128,14 @@ __global__ void __launch_bounds__(P2_THREADS) phase2_merge_kernel(const MergeArg
                     E::unpack(ov[k], xo);
                     E::unpack(pv[k], xp);
 #pragma unroll
-                    for (int p = 0; p < NP; ++p) {
-                        y[p].x = xo[p].x * ca.x;
-                        y[p].y = xo[p].y * ca.y;
-                        y[p] = ffma2(xp[p], cb, y[p]);
-                    }
+                    for (int p = 0; p < NP; ++p) y[p] = ffma2(xp[p], cb, fmul2(xo[p], ca));
                     stg128_cs(a.out + (t * a.d + (int64_t)vid[k] * EPV) * E::BYTES, E::pack(y));
                 }
             }
         }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) { ov[k] = on[k]; pv[k] = pn[k]; }
+        lv = ln;
         // red[buf] is rewritten two tiles later, after the next __syncthreads
     }
 }
