@@ -54,7 +54,9 @@ template <> struct Pair2<float> {
 
 __device__ __forceinline__ float dot2(float2 a, float2 b) { return fmaf(a.x, b.x, a.y * b.y); }
 
-template <typename Tin>
+// KA, KB, KC > 0 fix the three kernel sizes at compile time (fully unrolled,
+// branch-free convolution); 0 means they are read from the arguments.
+template <typename Tin, int KA, int KB, int KC>
 __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const int ring, const int ktot) {
     using P2 = Pair2<Tin>;
     constexpr int ES = sizeof(Tin);
@@ -69,7 +71,10 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
     const int nsrc = a.n_src;
     const int d = a.d;
     const size_t row_bytes = (size_t)ch * ES;            // one source row of the slice
-    const size_t slot_bytes = row_bytes * nsrc;          // one ring slot (all sources)
+    // one ring slot holds MSAR_SMAX source rows; rows of absent sources (and
+    // rows before the start of the sequence) stay zero
+    const size_t slot_bytes = row_bytes * MSAR_SMAX;
+    constexpr bool FIXED = KA > 0;
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ringbuf = smem;
@@ -79,24 +84,30 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
     uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + 2 * 8 * MSAR_NX);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 32);
 
+    const int kk[3] = {FIXED ? KA : a.k[0], FIXED ? KB : a.k[1], FIXED ? KC : a.k[2]};
     int koff[3];
     koff[0] = 0;
-    koff[1] = a.k[0];
-    koff[2] = a.k[0] + a.k[1];
-    const int kmax = max(a.k[0], max(a.k[1], a.k[2]));
+    koff[1] = kk[0];
+    koff[2] = kk[0] + kk[1];
+    const int kmax = max(kk[0], max(kk[1], kk[2]));
     const int hist = kmax - 1;
+    constexpr int HIST_C = FIXED ? (KA > KB ? (KA > KC ? KA : KC) : (KB > KC ? KB : KC)) - 1 : 0;
+
+    // zero the whole ring once (absent sources, rows before token 0)
+    for (size_t b = (size_t)tid * 16; b < (size_t)ring * slot_bytes; b += (size_t)blockDim.x * 16)
+        *reinterpret_cast<uint4 *>(ringbuf + b) = make_uint4(0u, 0u, 0u, 0u);
 
     // conv weights of this CTA's channel slice, layout [koff_r + j][c]
     {
         int64_t goff[3];
         goff[0] = 0;
-        goff[1] = (int64_t)d * a.k[0];
-        goff[2] = (int64_t)d * (a.k[0] + a.k[1]);
+        goff[1] = (int64_t)d * kk[0];
+        goff[2] = (int64_t)d * (kk[0] + kk[1]);
         for (int idx = tid; idx < ktot * ch; idx += blockDim.x) {
             const int jj = idx / ch, c = idx - jj * ch;
             const int r = jj >= koff[2] ? 2 : (jj >= koff[1] ? 1 : 0);
             const int j = jj - koff[r];
-            wconv[idx] = __ldg(a.conv_w + goff[r] + (int64_t)(rank * ch + c) * a.k[r] + j);
+            wconv[idx] = __ldg(a.conv_w + goff[r] + (int64_t)(rank * ch + c) * kk[r] + j);
         }
     }
     if (tid == 0) {
@@ -118,11 +129,14 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
         for (int o = 0; o < 4; ++o)
             pm[r][o] = make_float2(__ldg(a.mix_w + k0 * 4 + o) * g0, __ldg(a.mix_w + (k0 + 1) * 4 + o) * g1);
     }
+    // generic-proxy zero fill must be ordered before the bulk copies into the ring
+    fence_proxy_async_shared();
     // every CTA of the cluster is running (and its barriers initialised)
     // before any distributed-shared-memory access
     cluster.sync();
 
     const int64_t cid = blockIdx.x / K;
+    (void)HIST_C;
     const int64_t tb = cid * a.tokens_per_cluster;
     const int64_t te = min(a.T, tb + a.tokens_per_cluster);
     const int64_t ntok = te > tb ? te - tb : 0;
@@ -134,7 +148,7 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
     int64_t next_row = rho0;                              // next row to load
     int p_slot = 0;                                       // its ring slot: (next_row - rho0) % ring
     auto issue_row = [&](int64_t rho) {
-        mbar_arrive_expect_tx(&bars[p_slot], (uint32_t)slot_bytes);
+        mbar_arrive_expect_tx(&bars[p_slot], (uint32_t)(row_bytes * nsrc));
         const unsigned char *g = a.src + (rho * d + (int64_t)rank * ch) * ES;
         unsigned char *dst = ringbuf + (size_t)p_slot * slot_bytes;
         for (int i = 0; i < nsrc; ++i)
@@ -178,27 +192,32 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
             }
             // causal depthwise convolutions: each history row t-j is read once
             // and applied to every stream whose kernel reaches back that far
-            for (int j = 0; j <= hist; ++j) {
-                if (t - j < 0) break;
+            // (rows before token 0 and absent sources are zero in the ring)
+            auto conv_row = [&](int j) {
                 int sl = cur_slot - j;
                 if (sl < 0) sl += ring;
                 const unsigned char *row = ringbuf + (size_t)sl * slot_bytes + (size_t)cl * ES;
                 float2 xs[MSAR_SMAX];
 #pragma unroll
-                for (int i = 0; i < MSAR_SMAX; ++i)
-                    xs[i] = i < nsrc ? P2::ld(row + (size_t)i * row_bytes) : make_float2(0.f, 0.f);
+                for (int i = 0; i < MSAR_SMAX; ++i) xs[i] = P2::ld(row + (size_t)i * row_bytes);
                 if (j == 0) {
 #pragma unroll
                     for (int i = 0; i < MSAR_SMAX; ++i) x[i] = xs[i];
                 }
 #pragma unroll
                 for (int r = 0; r < MSAR_M - 1; ++r) {
-                    if (j < a.k[r]) {
+                    if (j < kk[r]) {
                         const float2 w = *reinterpret_cast<const float2 *>(wconv + (size_t)(koff[r] + j) * ch + cl);
 #pragma unroll
                         for (int i = 0; i < MSAR_SMAX; ++i) u[i][r] = ffma2(w, xs[i], u[i][r]);
                     }
                 }
+            };
+            if (FIXED) {
+#pragma unroll
+                for (int j = 0; j <= HIST_C; ++j) conv_row(j);
+            } else {
+                for (int j = 0; j <= hist; ++j) conv_row(j);
             }
             // per (source, stream): sum of squares and the stream-query dot
 #pragma unroll
@@ -326,10 +345,13 @@ attnres_status_t launch_msar(int dt, MsarArgs a, int sms, void *stream, char *er
     const int kmax = a.k[0] > a.k[1] ? (a.k[0] > a.k[2] ? a.k[0] : a.k[2]) : (a.k[1] > a.k[2] ? a.k[1] : a.k[2]);
     const int ring = kmax + MSAR_LA;
     const int ktot = a.k[0] + a.k[1] + a.k[2];
-    const size_t smem = (size_t)ring * a.n_src * ch * es + (size_t)ktot * ch * 4 +
+    const size_t smem = (size_t)ring * MSAR_SMAX * ch * es + (size_t)ktot * ch * 4 +
                         (size_t)(8 * MSAR_NX + 2 * 8 * MSAR_NX) * 4 + 32 * 8 + 16;
-    const void *fn = dt == 1 ? reinterpret_cast<const void *>(&msar_kernel<__nv_bfloat16>)
-                             : reinterpret_cast<const void *>(&msar_kernel<float>);
+    const bool k4812 = a.k[0] == 4 && a.k[1] == 8 && a.k[2] == 12;
+    const void *fn = dt == 1 ? (k4812 ? reinterpret_cast<const void *>(&msar_kernel<__nv_bfloat16, 4, 8, 12>)
+                                      : reinterpret_cast<const void *>(&msar_kernel<__nv_bfloat16, 0, 0, 0>))
+                             : (k4812 ? reinterpret_cast<const void *>(&msar_kernel<float, 4, 8, 12>)
+                                      : reinterpret_cast<const void *>(&msar_kernel<float, 0, 0, 0>));
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
