@@ -32,7 +32,7 @@ std::atomic<int> g_kernel_variant{0};   // 0 automatic, 1 general (CUDA-core) de
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kStageMaxBytes = 64 * 1024;        // one ring stage
-constexpr size_t kSmemBudget = 200 * 1024;         // stages + aux, per CTA
+constexpr size_t kSmemBudget = 227 * 1024;         // stages + aux, per CTA (sm_103a opt-in limit)
 
 struct DeviceInfo {
     std::once_flag once;
@@ -171,15 +171,21 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     // heads that are whole multiples of the per-warp channel slice.
     if (dt == ATTNRES_BF16 && n_src <= 8 && n_q <= 4 && (d == 1024 || d == 2048 || d == 4096) &&
         g_kernel_variant.load() == 0) {
+        // d = 4096: one token per item (16 warps x 256 channels); d <= 2048:
+        // two tokens per item (16 warps x d/16 channels), which fills all 16 MMA rows
+        const bool two = d <= 2048;
         const int nw = d == 1024 ? 8 : 16;
         const int ks = (int)(d / (16 * nw));
+        const int rows = two ? 16 : 8;
         KernelRef kr;
-        if (nw % H == 0 && lookup_depth_read_mma(pow2ceil((int)n_q), ks, nw, &kr)) {
+        const bool found = two ? lookup_depth_read_mma2(pow2ceil((int)n_q), ks, nw, &kr)
+                               : lookup_depth_read_mma(pow2ceil((int)n_q), ks, nw, &kr);
+        if (nw % H == 0 && found) {
             DeviceInfo *dev = nullptr;
             st = device_info(&dev);
             if (st != ATTNRES_OK) return st;
             const uint32_t pitch = (uint32_t)(2 * d + 16);
-            const uint32_t stage_bytes = (8 * pitch + 127) / 128 * 128;
+            const uint32_t stage_bytes = (rows * pitch + 127) / 128 * 128;
             size_t budget = kSmemBudget;
             if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
             int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
@@ -208,8 +214,9 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
                 m.pitch = pitch;
                 m.stage_bytes = stage_bytes;
                 m.wait = wait_cfg(dev);
+                const int64_t items = two ? (T + 1) / 2 : T;
                 const int64_t max_grid = (int64_t)dev->sms * occ;
-                const int grid = (int)(T < max_grid ? T : max_grid);
+                const int grid = (int)(items < max_grid ? items : max_grid);
                 void *args[] = {&m};
                 cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(nw * 32), args, smem,
                                                  static_cast<cudaStream_t>(stream));

@@ -8,10 +8,11 @@
 // The per-token work is two small dense contractions, done with warp-level
 // mma.sync.m16n8k16 (bf16 inputs, fp32 accumulation) straight from the
 // shared-memory stage (ldmatrix), so no element is unpacked:
-//   pass 1:  D1 = X Q  and  D2 = X X^T over the warp's channel slice, where
-//            X = [8 sources x 16 channels] (rows 8..15 zero), Q = the queries
-//            split into bf16 hi + lo parts (columns 2q, 2q+1), so
-//            dot_qi = D1[i][2q] + D1[i][2q+1] and sum(v_i^2) = D2[i][i];
+//   pass 1:  D1 = X Q over the warp's channel slice, where X = [8 sources x
+//            16 channels] (rows 8..15 zero), Q = the queries split into bf16
+//            hi + lo parts (columns 2q, 2q+1), so dot_qi = D1[i][2q] +
+//            D1[i][2q+1]; sum(v_i^2) is accumulated with packed FMAs on the
+//            same ldmatrix fragments;
 //   pass 2:  O^T = X'^T A per 16-channel block: X'^T = [16 channels x (8
 //            sources | the same 8 sources)] (ldmatrix .trans), A = [(8 sources
 //            hi | 8 sources lo) x 4 queries] holding alpha split into bf16 hi
@@ -59,11 +60,12 @@ struct DepthReadMmaArgs {
 
 struct DMLayout {
     static constexpr size_t bar_bytes = 128;
-    // red[2][40 values][RS]: for each value (dots q*8+i, then sums of squares
-    // 32+i) the partial of every warp; row stride RS = 20 floats keeps the
-    // 16-float rows 16-byte aligned and the writes at most 4-way conflicting
+    // red[2][40 values per token][RS]: for each value (dots q*8+i, then sums
+    // of squares 32+i) the partial of every warp; row stride RS = 20 floats
+    // keeps the 16-float rows 16-byte aligned and the writes at most 4-way
+    // conflicting; two tokens per item use 80 values
     static constexpr int RS = 20;
-    static constexpr size_t red_floats = 2 * 40 * RS;
+    static constexpr size_t red_floats = 2 * 80 * RS;
     static constexpr size_t aux_bytes = bar_bytes + 4 * red_floats;
 };
 
@@ -171,18 +173,21 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
     const int n_items = blockIdx.x < a.T ? (int)((a.T - blockIdx.x + gstride - 1) / gstride) : 0;
 
     // ------------------------------------------------------------ producer
-    const bool producer = (tid == 0) && !a.wait.inject_stall;
+    // warp 0 produces (lane 0 arms the stage's mbarrier and issues the copies;
+    // measured faster than one copy per lane here)
+    const bool producer = (warp == 0) && !a.wait.inject_stall;
     uint64_t pol = 0;
     if (producer) pol = l2_policy_evict_first();
     int p_stage = 0;
     int64_t p_tok = blockIdx.x;
     const uint32_t row_bytes = (uint32_t)a.d * 2;
     auto issue_next = [&]() {
-        mbar_arrive_expect_tx(&full[p_stage], row_bytes * a.n_src);
-        const unsigned char *g = a.src + p_tok * row_bytes;
-        unsigned char *dst = stages + (size_t)p_stage * a.stage_bytes;
-        for (int i = 0; i < a.n_src; ++i)
-            bulk_g2s(dst + (size_t)i * a.pitch, g + (int64_t)i * a.src_stride_bytes, row_bytes, &full[p_stage], pol);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[p_stage], row_bytes * a.n_src);
+            for (int i = 0; i < a.n_src; ++i)
+                bulk_g2s(stages + (size_t)p_stage * a.stage_bytes + (size_t)i * a.pitch,
+                         a.src + p_tok * row_bytes + (int64_t)i * a.src_stride_bytes, row_bytes, &full[p_stage], pol);
+        }
         if (++p_stage == a.nstages) p_stage = 0;
         p_tok += gstride;
     };
@@ -229,29 +234,36 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
         mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
         const uint32_t sa = stage0 + (uint32_t)s * a.stage_bytes + lrow;
 
-        // ---------------- pass 1: D1 = X Q, D2 = X X^T over the warp's channels
-        float d1[2][4], d2[2][4];
+        // ---------------- pass 1: D1 = X Q on the tensor cores; sum(v_i^2) with
+        // packed FMAs on the same fragments (lane (g4, t4) holds 8 elements of
+        // source g4 per two k-steps)
+        float d1[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) { d1[u][e] = 0.f; d2[u][e] = 0.f; }
+            for (int e = 0; e < 4; ++e) d1[u][e] = 0.f;
+        float2 sq = make_float2(0.f, 0.f);
 #pragma unroll
         for (int s2 = 0; s2 < KS / 2; ++s2) {
             uint32_t x0, x1, x2, x3;            // k-step 2*s2: (x0, x1); 2*s2+1: (x2, x3)
             ldsm_x4(sa + 64 * s2, x0, x1, x2, x3);
             mma_rows8(d1[0], x0, x1, bq[2 * s2][0], bq[2 * s2][1]);
-            mma_rows8(d2[0], x0, x1, x0, x1);
             mma_rows8(d1[1], x2, x3, bq[2 * s2 + 1][0], bq[2 * s2 + 1][1]);
-            mma_rows8(d2[1], x2, x3, x2, x3);
+            const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
+            sq = ffma2(f0, f0, sq);
+            sq = ffma2(f1, f1, sq);
+            sq = ffma2(f2, f2, sq);
+            sq = ffma2(f3, f3, sq);
         }
         const float dot = (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
-        const float q0 = d2[0][0] + d2[1][0];
-        const float q1 = d2[0][1] + d2[1][1];
-        // lane (i = g4, q = t4) holds dot_qi; lane 4i + i/2 holds sum(v_i^2)
+        float ssq = sq.x + sq.y;
+        ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
+        ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+        // lane (i = g4, q = t4) holds dot_qi; lanes 4i.. hold sum(v_i^2)
         constexpr int RS = L::RS;
         float *rb = red + (size_t)(it & 1) * 40 * RS;
         rb[(t4 * 8 + g4) * RS + warp] = dot;
-        if (t4 == (g4 >> 1)) rb[(32 + g4) * RS + warp] = (g4 & 1) ? q1 : q0;
+        if (t4 == 0) rb[(32 + g4) * RS + warp] = ssq;
         // the previous item's output bulk stores must have read their shared rows
         // before the barrier that lets the producer refill that stage
         if (lane < a.n_q && it >= 1) bulk_wait_read0();
@@ -267,7 +279,10 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
                                                (size_t)cbase * 2 + b) = make_uint4(0u, 0u, 0u, 0u);
         }
         __syncthreads();
-        if (producer && it >= 1 && issued < n_items && !*abort_flag) { issue_next(); ++issued; }
+        if (producer && it >= 1 && issued < n_items) {
+            // one decision for the whole producer warp (issue_next synchronises it)
+            if (__shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0)) { issue_next(); ++issued; }
+        }
 
         // ---------------- softmax over sources: lane p = q*8 + i
         const int q = lane >> 3, i = lane & 7;
@@ -343,7 +358,253 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
 
     // outputs must be written before the CTA exits
     if (lane < a.n_q) bulk_wait0();
-    if (producer) {
+    if (producer && lane == 0) {
+        int never = 0;
+        for (int it = issued > a.nstages ? issued - a.nstages : 0; it < issued; ++it)
+            mbar_wait_bounded(&full[it % a.nstages], (uint32_t)(it / a.nstages) & 1, &never, a.wait);
+    }
+}
+
+
+// Two tokens per item (d <= 2048, where two tokens' 8 source rows fit one
+// 64 KB stage).  Pass 1 uses all 16 MMA rows (token 0's sources in rows 0..7,
+// token 1's in rows 8..15); the two tokens' softmaxes run as independent
+// chains; the per-item barrier, softmax latency and bulk stores are paid
+// once per two tokens.  Stage row tok*8 + i holds source i of token tok.
+template <int NQ, int KS, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) depth_read_mma2_kernel(const DepthReadMmaArgs a) {
+    static_assert(NQ <= 4, "at most 4 queries (8 MMA columns: hi and lo per query)");
+    using L = DMLayout;
+    constexpr int CW = KS * 16;                 // channels per warp
+    constexpr int RS = L::RS;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.nstages * a.stage_bytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(full + DM_MAX_STAGES);
+    float *red = reinterpret_cast<float *>(smem + (size_t)a.nstages * a.stage_bytes + L::bar_bytes);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, t4 = lane & 3;
+
+    if (tid == 0) {
+        for (int s = 0; s < a.nstages; ++s) mbar_init(&full[s], 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    // rows of absent sources (both tokens) stay zero
+    for (int s = 0; s < a.nstages; ++s)
+        for (int tk = 0; tk < 2; ++tk)
+            for (int i = a.n_src; i < 8; ++i)
+                for (int b = tid * 16; b < a.d * 2; b += NW * 32 * 16)
+                    *reinterpret_cast<uint4 *>(stages + (size_t)s * a.stage_bytes +
+                                               (size_t)(tk * 8 + i) * a.pitch + b) = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    const int64_t npairs = (a.T + 1) / 2;
+    const int gstride = gridDim.x;
+    const int n_items = blockIdx.x < npairs ? (int)((npairs - blockIdx.x + gstride - 1) / gstride) : 0;
+
+    // ------------------------------------------------------------ producer
+    // warp 0 produces: lane 0 arms the mbarrier, lane tk*8 + i copies source i of token tk
+    const bool producer = (warp == 0) && !a.wait.inject_stall;
+    uint64_t pol = 0;
+    if (producer) pol = l2_policy_evict_first();
+    int p_stage = 0;
+    int64_t p_pair = blockIdx.x;
+    const uint32_t row_bytes = (uint32_t)a.d * 2;
+    auto issue_next = [&]() {
+        const int64_t t0 = 2 * p_pair;
+        const int ntok = t0 + 1 < a.T ? 2 : 1;
+        if (lane == 0) mbar_arrive_expect_tx(&full[p_stage], row_bytes * a.n_src * ntok);
+        __syncwarp();
+        const int tk = lane >> 3, i = lane & 7;
+        if (lane < 16 && tk < ntok && i < a.n_src) {
+            const unsigned char *g = a.src + (t0 + tk) * row_bytes + (int64_t)i * a.src_stride_bytes;
+            bulk_g2s(stages + (size_t)p_stage * a.stage_bytes + (size_t)(tk * 8 + i) * a.pitch, g, row_bytes,
+                     &full[p_stage], pol);
+        }
+        if (++p_stage == a.nstages) p_stage = 0;
+        p_pair += gstride;
+    };
+    int issued = 0;
+    if (producer)
+        for (; issued < n_items && issued < a.nstages; ++issued) issue_next();
+
+    // ------------------------------------------------------------ constants
+    const int cbase = warp * CW;
+    uint32_t bq[KS][2];
+    {
+        const int q = g4 >> 1, part = g4 & 1;
+#pragma unroll
+        for (int s = 0; s < KS; ++s)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = cbase + 16 * s + 8 * h + 2 * t4;
+                float v0 = 0.f, v1 = 0.f;
+                if (q < a.n_q) {
+                    v0 = __ldg(a.queries + (size_t)q * a.d + c);
+                    v1 = __ldg(a.queries + (size_t)q * a.d + c + 1);
+                    if (a.gain) { v0 *= __ldg(a.gain + c); v1 *= __ldg(a.gain + c + 1); }
+                }
+                float h0, l0, h1, l1;
+                split_bf16(v0, h0, l0);
+                split_bf16(v1, h1, l1);
+                bq[s][h] = part == 0 ? pack_bf16(h0, h1) : pack_bf16(l0, l1);
+            }
+    }
+    const int head = warp / a.wph;
+    const int gw0 = head * a.wph;
+    const float inv_dh = 1.f / (float)(CW * a.wph);
+    // ldmatrix (both directions): matrix j = lane/8 is token j&1, channels
+    // +8*(j>>1) of the 16-channel step; row = source lane%8
+    const uint32_t lrow = (uint32_t)(((lane >> 3) & 1) * 8 + (lane & 7)) * a.pitch +
+                          (uint32_t)(cbase + 8 * (lane >> 4)) * 2;
+    // stmatrix: matrix j = lane/8 is token j>>1, channels +8*(j&1); row = query lane%8
+    const uint32_t orow = (uint32_t)((lane >> 4) * 8 + (lane & 7)) * a.pitch +
+                          (uint32_t)(cbase + 8 * ((lane >> 3) & 1)) * 2;
+    const uint32_t stage0 = smem_u32(stages);
+
+    int s = 0;
+    uint32_t par = 0;
+    int64_t pair = blockIdx.x;
+    for (int it = 0; it < n_items; ++it) {
+        const int64_t t0 = 2 * pair;
+        const bool has1 = t0 + 1 < a.T;
+        mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
+        const uint32_t sbase = stage0 + (uint32_t)s * a.stage_bytes;
+
+        // ---------------- pass 1: D1 = X Q (16 rows) on the tensor cores; sums
+        // of squares with packed FMAs on the fragments (lane (g4, t4) holds 4
+        // elements of source g4 of each token per k-step)
+        float d1[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d1[u][e] = 0.f;
+        float2 sq0 = make_float2(0.f, 0.f), sq1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            uint32_t x0, x1, x2, x3;       // (tok0, ch 0-7), (tok1, ch 0-7), (tok0, ch 8-15), (tok1, ch 8-15)
+            ldsm_x4(sbase + lrow + 32 * k, x0, x1, x2, x3);
+            mma_full(d1[k & 1], x0, x1, x2, x3, bq[k][0], bq[k][1]);
+            const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
+            sq0 = ffma2(f0, f0, sq0);
+            sq0 = ffma2(f2, f2, sq0);
+            sq1 = ffma2(f1, f1, sq1);
+            sq1 = ffma2(f3, f3, sq1);
+        }
+        // lane (i = g4, q = t4): dots of token 0 in c0+c1, token 1 in c2+c3
+        const float dot0 = (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
+        const float dot1 = (d1[0][2] + d1[1][2]) + (d1[0][3] + d1[1][3]);
+        float s0 = sq0.x + sq0.y, s1 = sq1.x + sq1.y;
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        float *rb = red + (size_t)(it & 1) * 80 * RS;
+        rb[(t4 * 8 + g4) * RS + warp] = dot0;
+        rb[(40 + t4 * 8 + g4) * RS + warp] = dot1;
+        if (t4 == 0) {
+            rb[(32 + g4) * RS + warp] = s0;
+            rb[(72 + g4) * RS + warp] = s1;
+        }
+        if (lane < 8 && it >= 1) bulk_wait_read0();
+        if (a.n_src < a.n_q && it >= 1) {
+            __syncwarp();
+            const int sp = s == 0 ? a.nstages - 1 : s - 1;
+            for (int tk = 0; tk < 2; ++tk)
+                for (int row = a.n_src; row < a.n_q; ++row)
+                    for (int b = lane * 16; b < CW * 2; b += 32 * 16)
+                        *reinterpret_cast<uint4 *>(stages + (size_t)sp * a.stage_bytes +
+                                                   (size_t)(tk * 8 + row) * a.pitch + (size_t)cbase * 2 + b) =
+                            make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncthreads();
+        if (producer && it >= 1 && issued < n_items) {
+            // one decision for the whole producer warp (issue_next synchronises it)
+            if (__shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0)) { issue_next(); ++issued; }
+        }
+
+        // ---------------- softmax over sources for both tokens: lane p = q*8 + i
+        const int q = lane >> 3, i = lane & 7;
+        float ss0 = 0.f, dt0 = 0.f, ss1 = 0.f, dt1 = 0.f;
+        {
+            const float *ps0 = rb + (32 + i) * RS + gw0, *pd0 = rb + (q * 8 + i) * RS + gw0;
+            const float *ps1 = ps0 + 40 * RS, *pd1 = pd0 + 40 * RS;
+            if (a.wph % 4 == 0) {
+                for (int w = 0; w < a.wph; w += 4) {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(ps0 + w);
+                    const float4 y0 = *reinterpret_cast<const float4 *>(pd0 + w);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(ps1 + w);
+                    const float4 y1 = *reinterpret_cast<const float4 *>(pd1 + w);
+                    ss0 += (x0.x + x0.y) + (x0.z + x0.w);
+                    dt0 += (y0.x + y0.y) + (y0.z + y0.w);
+                    ss1 += (x1.x + x1.y) + (x1.z + x1.w);
+                    dt1 += (y1.x + y1.y) + (y1.z + y1.w);
+                }
+            } else {
+                for (int w = 0; w < a.wph; ++w) { ss0 += ps0[w]; dt0 += pd0[w]; ss1 += ps1[w]; dt1 += pd1[w]; }
+            }
+        }
+        const bool pv = i < a.n_src && q < NQ;
+        const float sc0 = pv ? key_score(dt0, ss0, inv_dh, a.eps) : -INFINITY;
+        const float sc1 = pv ? key_score(dt1, ss1, inv_dh, a.eps) : -INFINITY;
+        const float m0 = seg_max<8>(sc0), m1 = seg_max<8>(sc1);
+        const float e0 = pv ? __expf(sc0 - m0) : 0.f, e1 = pv ? __expf(sc1 - m1) : 0.f;
+        const float l0 = seg_sum<8>(e0), l1 = seg_sum<8>(e1);
+        const float al_0 = pv ? e0 / l0 : 0.f, al_1 = pv ? e1 / l1 : 0.f;
+        if (i == 0 && q < a.n_q && warp == gw0 && a.lse != nullptr && !*abort_flag) {
+            a.lse[((int64_t)q * a.H + head) * a.T + t0] = m0 + __logf(l0);
+            if (has1) a.lse[((int64_t)q * a.H + head) * a.T + t0 + 1] = m1 + __logf(l1);
+        }
+        // pass-2 B fragments of both tokens
+        const int srcl = (g4 & 3) * 8 + 2 * t4;
+        uint32_t bb[2][2] = {{0u, 0u}, {0u, 0u}};
+        {
+            const float a00 = __shfl_sync(0xffffffffu, al_0, srcl), a01 = __shfl_sync(0xffffffffu, al_0, srcl + 1);
+            const float a10 = __shfl_sync(0xffffffffu, al_1, srcl), a11 = __shfl_sync(0xffffffffu, al_1, srcl + 1);
+            if (g4 < NQ) {
+                float h0, lo0, h1, lo1;
+                split_bf16(a00, h0, lo0);
+                split_bf16(a01, h1, lo1);
+                bb[0][0] = pack_bf16(h0, h1);
+                bb[0][1] = pack_bf16(lo0, lo1);
+                split_bf16(a10, h0, lo0);
+                split_bf16(a11, h1, lo1);
+                bb[1][0] = pack_bf16(h0, h1);
+                bb[1][1] = pack_bf16(lo0, lo1);
+            }
+        }
+
+        // ---------------- pass 2 for both tokens, outputs staged by stmatrix
+#pragma unroll 4
+        for (int k = 0; k < KS; ++k) {
+            uint32_t y0, y1, y2, y3;       // .trans: (tok0, ch 0-7), (tok1, ch 0-7), (tok0, ch 8-15), (tok1, ch 8-15)
+            ldsm_x4_t(sbase + lrow + 32 * k, y0, y1, y2, y3);
+            float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_full(o0, y0, y2, y0, y2, bb[0][0], bb[0][1]);
+            mma_full(o1, y1, y3, y1, y3, bb[1][0], bb[1][1]);
+            stsm_x4_t(sbase + orow + 32 * k, f2_to_bf2(o0[0], o0[1]), f2_to_bf2(o0[2], o0[3]),
+                      f2_to_bf2(o1[0], o1[1]), f2_to_bf2(o1[2], o1[3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        // lanes 0..3: token 0, query lane; lanes 4..7: token 1, query lane-4
+        if (lane < 8) {
+            const int tk = lane >> 2, qq = lane & 3;
+            if (qq < a.n_q && (tk == 0 || has1) && !*abort_flag)
+                bulk_s2g(a.out + (int64_t)qq * a.out_q_stride_bytes + ((t0 + tk) * a.d + cbase) * 2,
+                         sbase + (uint32_t)(tk * 8 + qq) * a.pitch + (uint32_t)cbase * 2, (uint32_t)CW * 2);
+            bulk_commit();
+        }
+        if (++s == a.nstages) { s = 0; par ^= 1u; }
+        pair += gstride;
+    }
+
+    if (lane < 8) bulk_wait0();
+    if (producer && lane == 0) {
         int never = 0;
         for (int it = issued > a.nstages ? issued - a.nstages : 0; it < issued; ++it)
             mbar_wait_bounded(&full[it % a.nstages], (uint32_t)(it / a.nstages) & 1, &never, a.wait);

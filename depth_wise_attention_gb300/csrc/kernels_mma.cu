@@ -12,13 +12,30 @@ static KernelRef dm_ref() {
     return r;
 }
 
+template <int NQ, int KS, int NW>
+static KernelRef dm2_ref() {
+    KernelRef r;
+    r.fn = reinterpret_cast<const void *>(&depth_read_mma2_kernel<NQ, KS, NW>);
+    r.aux_smem = DMLayout::aux_bytes;
+    return r;
+}
+
+bool lookup_depth_read_mma2(int nq, int ks, int nw, KernelRef *out) {
+#define ATTNRES_DM2_CASE(NQ, KS, NW) \
+    if (nq == NQ && ks == KS && nw == NW) { *out = dm2_ref<NQ, KS, NW>(); return true; }
+    // d = 1024: 8 warps x 128 channels; d = 2048: 16 warps x 128 channels
+    ATTNRES_DM2_CASE(1, 8, 8) ATTNRES_DM2_CASE(1, 8, 16)
+    ATTNRES_DM2_CASE(2, 8, 8) ATTNRES_DM2_CASE(2, 8, 16)
+    ATTNRES_DM2_CASE(4, 8, 8) ATTNRES_DM2_CASE(4, 8, 16)
+#undef ATTNRES_DM2_CASE
+    return false;
+}
+
 bool lookup_depth_read_mma(int nq, int ks, int nw, KernelRef *out) {
 #define ATTNRES_DM_CASE(NQ, KS, NW) \
     if (nq == NQ && ks == KS && nw == NW) { *out = dm_ref<NQ, KS, NW>(); return true; }
-    // d = 1024: 8 warps x 128 channels; d = 2048, 4096: 16 warps x 128 / 256 channels
-    ATTNRES_DM_CASE(1, 8, 8) ATTNRES_DM_CASE(1, 8, 16) ATTNRES_DM_CASE(1, 16, 16)
-    ATTNRES_DM_CASE(2, 8, 8) ATTNRES_DM_CASE(2, 8, 16) ATTNRES_DM_CASE(2, 16, 16)
-    ATTNRES_DM_CASE(4, 8, 8) ATTNRES_DM_CASE(4, 8, 16) ATTNRES_DM_CASE(4, 16, 16)
+    // d = 4096: 16 warps x 256 channels (d <= 2048 use the two-token kernel)
+    ATTNRES_DM_CASE(1, 16, 16) ATTNRES_DM_CASE(2, 16, 16) ATTNRES_DM_CASE(4, 16, 16)
 #undef ATTNRES_DM_CASE
     return false;
 }
