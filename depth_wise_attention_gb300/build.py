@@ -26,6 +26,7 @@ SOURCES = [
     "kernels_f32_multi.cu",
     "kernels_phase2.cu",
     "kernels_mma.cu",
+    "kernels_mma_multi.cu",
     "msar.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

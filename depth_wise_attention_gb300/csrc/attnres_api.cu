@@ -28,7 +28,8 @@ thread_local char t_last_err[256] = "";
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
-std::atomic<int> g_kernel_variant{0};   // 0 automatic, 1 general (CUDA-core) depth read only
+std::atomic<int> g_kernel_variant{0};   // 0 automatic, 1 general (CUDA-core) depth read only,
+                                        // 2 tensor-core depth reads wherever they apply
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kStageMaxBytes = 64 * 1024;        // one ring stage
@@ -167,19 +168,30 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
         return ATTNRES_ERR_UNSUPPORTED;
     if (T == 0) return ATTNRES_OK;
 
-    // Tensor-core path: bf16, <= 8 sources, <= 4 queries, d = 1024/2048/4096,
-    // heads that are whole multiples of the per-warp channel slice.
-    if (dt == ATTNRES_BF16 && n_src <= 8 && n_q <= 4 && (d == 1024 || d == 2048 || d == 4096) &&
-        g_kernel_variant.load() == 0) {
-        // d = 4096: one token per item (16 warps x 256 channels); d <= 2048:
-        // two tokens per item (16 warps x d/16 channels), which fills all 16 MMA rows
-        const bool two = d <= 2048;
+    // Tensor-core path: bf16, <= 4 queries, d = 1024/2048/4096, heads that are
+    // whole multiples of the per-warp channel slice.  <= 8 sources: d = 4096
+    // one token per item (16 warps x 256 channels), d <= 2048 two tokens per
+    // item (16 warps x d/16 channels), which fills all 16 MMA rows.
+    // > 8 sources: one token per item, its sources in chunks of 8 folded in by
+    // an online softmax.  An item costs about the same whatever its rows, so
+    // the chunked kernel only beats the general kernel's 4-source chunks (two
+    // CTAs per SM) when its chunks are nearly full and numerous: measured at
+    // d = 4096 from 24 sources on with a last chunk of 5..8 rows (up to 7%
+    // faster at 64 sources; slower at d = 2048, so only d = 4096 is built).
+    const int kv = g_kernel_variant.load();
+    const bool chunked = n_src > 8;
+    const bool chunked_wins = n_src >= 24 && (n_src % 8 == 0 || n_src % 8 >= 5);
+    if (dt == ATTNRES_BF16 && n_q <= 4 && (d == 1024 || d == 2048 || d == 4096) && kv != 1 &&
+        (!chunked || (d == 4096 && (chunked_wins || kv == 2)))) {
+        const bool two = !chunked && d <= 2048;
         const int nw = d == 1024 ? 8 : 16;
         const int ks = (int)(d / (16 * nw));
         const int rows = two ? 16 : 8;
+        const int nq2 = pow2ceil((int)n_q);
         KernelRef kr;
-        const bool found = two ? lookup_depth_read_mma2(pow2ceil((int)n_q), ks, nw, &kr)
-                               : lookup_depth_read_mma(pow2ceil((int)n_q), ks, nw, &kr);
+        const bool found = chunked ? lookup_depth_read_mma_multi(nq2, ks, nw, &kr)
+                           : two   ? lookup_depth_read_mma2(nq2, ks, nw, &kr)
+                                   : lookup_depth_read_mma(nq2, ks, nw, &kr);
         if (nw % H == 0 && found) {
             DeviceInfo *dev = nullptr;
             st = device_info(&dev);
@@ -217,11 +229,15 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
                 const int64_t items = two ? (T + 1) / 2 : T;
                 const int64_t max_grid = (int64_t)dev->sms * occ;
                 const int grid = (int)(items < max_grid ? items : max_grid);
-                void *args[] = {&m};
-                cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(nw * 32), args, smem,
-                                                 static_cast<cudaStream_t>(stream));
-                if (e != cudaSuccess) return cuda_fail(e, "depth_read_mma launch");
-                return ATTNRES_OK;
+                // the chunked kernel counts a CTA's (token, chunk) items in an int
+                const int64_t per_cta = (items + grid - 1) / grid * (chunked ? (n_src + 7) / 8 : 1);
+                if (per_cta <= (int64_t)INT32_MAX) {
+                    void *args[] = {&m};
+                    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(nw * 32), args, smem,
+                                                     static_cast<cudaStream_t>(stream));
+                    if (e != cudaSuccess) return cuda_fail(e, "depth_read_mma launch");
+                    return ATTNRES_OK;
+                }
             }
         }
     }
@@ -489,7 +505,9 @@ void attnres_debug_set_wait_timeout_ns(uint64_t ns) {
 
 void attnres_debug_set_stall_injection(int enable) { g_inject_stall.store(enable ? 1 : 0); }
 
-void attnres_debug_set_kernel_variant(int variant) { g_kernel_variant.store(variant == 1 ? 1 : 0); }
+void attnres_debug_set_kernel_variant(int variant) {
+    g_kernel_variant.store(variant == 1 || variant == 2 ? variant : 0);
+}
 
 const char *attnres_version(void) { return "attnres 0.1.0 sm_103a"; }
 

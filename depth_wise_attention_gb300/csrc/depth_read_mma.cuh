@@ -139,6 +139,148 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo_ch, float hi_ch) {
     return f2_to_bf2(lo_ch, hi_ch);
 }
 
+// Pass-1 B fragments of a warp's channel slice [cbase, cbase + 16*KS): query
+// q = g4/2 with the gain folded in, its bf16 hi part in column 2q and its lo
+// part in column 2q+1 (columns of absent queries are zero).
+template <int KS>
+__device__ __forceinline__ void dm_query_fragments(const DepthReadMmaArgs &a, int cbase, int g4, int t4,
+                                                   uint32_t (&bq)[KS][2]) {
+    const int q = g4 >> 1, part = g4 & 1;
+#pragma unroll
+    for (int s = 0; s < KS; ++s)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = cbase + 16 * s + 8 * h + 2 * t4;
+            float v0 = 0.f, v1 = 0.f;
+            if (q < a.n_q) {
+                v0 = __ldg(a.queries + (size_t)q * a.d + c);
+                v1 = __ldg(a.queries + (size_t)q * a.d + c + 1);
+                if (a.gain) { v0 *= __ldg(a.gain + c); v1 *= __ldg(a.gain + c + 1); }
+            }
+            float h0, l0, h1, l1;
+            split_bf16(v0, h0, l0);
+            split_bf16(v1, h1, l1);
+            bq[s][h] = part == 0 ? pack_bf16(h0, h1) : pack_bf16(l0, l1);
+        }
+}
+
+// Pass 1 over 8 source rows of a warp's channel slice: D1 = X Q on the tensor
+// cores (X = [8 sources x 16 channels], rows 8..15 zero) and sum(v_i^2) with
+// packed FMAs on the same ldmatrix fragments.  sa is this lane's ldmatrix row
+// address (source lane%8, channel block lane/8 of a 32-channel group).  On
+// return lane (i = g4, q = t4) holds dot_qi and lanes 4i.. hold sum(v_i^2).
+template <int KS>
+__device__ __forceinline__ void dm_pass1_rows8(uint32_t sa, const uint32_t (&bq)[KS][2], float &dot,
+                                               float &ssq) {
+    float d1[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d1[u][e] = 0.f;
+    float2 sq = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int s2 = 0; s2 < KS / 2; ++s2) {
+        uint32_t x0, x1, x2, x3;            // k-step 2*s2: (x0, x1); 2*s2+1: (x2, x3)
+        ldsm_x4(sa + 64 * s2, x0, x1, x2, x3);
+        mma_rows8(d1[0], x0, x1, bq[2 * s2][0], bq[2 * s2][1]);
+        mma_rows8(d1[1], x2, x3, bq[2 * s2 + 1][0], bq[2 * s2 + 1][1]);
+        const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
+        sq = ffma2(f0, f0, sq);
+        sq = ffma2(f1, f1, sq);
+        sq = ffma2(f2, f2, sq);
+        sq = ffma2(f3, f3, sq);
+    }
+    dot = (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
+    ssq = sq.x + sq.y;
+    ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
+    ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+}
+
+// At most 2 queries: two k-steps per MMA.  A = [8 sources x k-step a; the
+// same 8 sources x k-step b] (rows 0..7, 8..15); B column c holds query c/4,
+// k-step (c/2)&1 and bf16 part c&1 (hi, lo).  Output rows of k-step a only
+// meet its columns in lanes with t4 even (c0 + c1), rows of k-step b in lanes
+// with t4 odd (c2 + c3): half the MMAs of dm_pass1_rows8, half the B registers.
+template <int KS>
+__device__ __forceinline__ void dm_query_fragments_packed(const DepthReadMmaArgs &a, int cbase, int g4, int t4,
+                                                          uint32_t (&bq)[KS / 2][2]) {
+    const int q = g4 >> 2, kb = (g4 >> 1) & 1, part = g4 & 1;
+#pragma unroll
+    for (int s2 = 0; s2 < KS / 2; ++s2)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = cbase + 32 * s2 + 16 * kb + 8 * h + 2 * t4;
+            float v0 = 0.f, v1 = 0.f;
+            if (q < a.n_q) {
+                v0 = __ldg(a.queries + (size_t)q * a.d + c);
+                v1 = __ldg(a.queries + (size_t)q * a.d + c + 1);
+                if (a.gain) { v0 *= __ldg(a.gain + c); v1 *= __ldg(a.gain + c + 1); }
+            }
+            float h0, l0, h1, l1;
+            split_bf16(v0, h0, l0);
+            split_bf16(v1, h1, l1);
+            bq[s2][h] = part == 0 ? pack_bf16(h0, h1) : pack_bf16(l0, l1);
+        }
+}
+
+// Pass 1 with dm_query_fragments_packed.  On return lanes (i = g4, t4 = 2q,
+// 2q+1) hold dot_qi and lanes 4i.. hold sum(v_i^2).
+template <int KS>
+__device__ __forceinline__ void dm_pass1_rows8_packed(uint32_t sa, const uint32_t (&bq)[KS / 2][2], int t4,
+                                                      float &dot, float &ssq) {
+    float d1[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d1[u][e] = 0.f;
+    float2 sq = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int s2 = 0; s2 < KS / 2; ++s2) {
+        uint32_t x0, x1, x2, x3;            // k-step a: (x0, x1); k-step b: (x2, x3)
+        ldsm_x4(sa + 64 * s2, x0, x1, x2, x3);
+        mma_full(d1[s2 & 1], x0, x2, x1, x3, bq[s2][0], bq[s2][1]);
+        const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
+        sq = ffma2(f0, f0, sq);
+        sq = ffma2(f1, f1, sq);
+        sq = ffma2(f2, f2, sq);
+        sq = ffma2(f3, f3, sq);
+    }
+    const float part = (t4 & 1) ? (d1[0][2] + d1[1][2]) + (d1[0][3] + d1[1][3])
+                                : (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
+    dot = part + __shfl_xor_sync(0xffffffffu, part, 1);
+    ssq = sq.x + sq.y;
+    ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
+    ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+}
+
+// Sum over the wph warps of a head (starting at gw0) of the partial sum of
+// squares of source i and the partial dot of (query q, source i), from the
+// value-major table rb[value][warp] (row stride RS).
+__device__ __forceinline__ void dm_head_partials(const float *rb, int RS, int gw0, int wph, int q, int i,
+                                                 float &ss, float &dt) {
+    ss = 0.f;
+    dt = 0.f;
+    const float *ps = rb + (32 + i) * RS + gw0;
+    const float *pd = rb + (q * 8 + i) * RS + gw0;
+    if (wph % 4 == 0) {
+        for (int w = 0; w < wph; w += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(ps + w);
+            const float4 y = *reinterpret_cast<const float4 *>(pd + w);
+            ss += (x.x + x.y) + (x.z + x.w);
+            dt += (y.x + y.y) + (y.z + y.w);
+        }
+    } else {
+        for (int w = 0; w < wph; ++w) { ss += ps[w]; dt += pd[w]; }
+    }
+}
+
+// Scale an m16n8 accumulator fragment column-wise: elements 0, 2 belong to
+// column 2*t4, elements 1, 3 to column 2*t4+1.
+__device__ __forceinline__ void dm_rescale(float (&c)[4], float2 f) {
+    const float2 a = fmul2(make_float2(c[0], c[1]), f), b = fmul2(make_float2(c[2], c[3]), f);
+    c[0] = a.x; c[1] = a.y; c[2] = b.x; c[3] = b.y;
+}
+
 template <int NQ, int KS, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthReadMmaArgs a) {
     static_assert(NQ <= 4, "at most 4 queries (8 MMA columns: hi and lo per query)");
@@ -197,27 +339,10 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
 
     // ------------------------------------------------------------ constants
     const int cbase = warp * CW;                // first channel of this warp
-    // pass-1 B fragments: query q (gain folded), bf16 hi in column 2q, lo in 2q+1
-    uint32_t bq[KS][2];
-    {
-        const int q = g4 >> 1, part = g4 & 1;
-#pragma unroll
-        for (int s = 0; s < KS; ++s)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = cbase + 16 * s + 8 * h + 2 * t4;
-                float v0 = 0.f, v1 = 0.f;
-                if (q < a.n_q) {
-                    v0 = __ldg(a.queries + (size_t)q * a.d + c);
-                    v1 = __ldg(a.queries + (size_t)q * a.d + c + 1);
-                    if (a.gain) { v0 *= __ldg(a.gain + c); v1 *= __ldg(a.gain + c + 1); }
-                }
-                float h0, l0, h1, l1;
-                split_bf16(v0, h0, l0);
-                split_bf16(v1, h1, l1);
-                bq[s][h] = part == 0 ? pack_bf16(h0, h1) : pack_bf16(l0, l1);
-            }
-    }
+    constexpr bool PACK = NQ <= 2;
+    uint32_t bq[PACK ? KS / 2 : KS][2];
+    if constexpr (PACK) dm_query_fragments_packed<KS>(a, cbase, g4, t4, bq);
+    else dm_query_fragments<KS>(a, cbase, g4, t4, bq);
     // head of this warp and the warps that share it
     const int head = warp / a.wph;
     const int gw0 = head * a.wph;
@@ -234,35 +359,14 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
         mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
         const uint32_t sa = stage0 + (uint32_t)s * a.stage_bytes + lrow;
 
-        // ---------------- pass 1: D1 = X Q on the tensor cores; sum(v_i^2) with
-        // packed FMAs on the same fragments (lane (g4, t4) holds 8 elements of
-        // source g4 per two k-steps)
-        float d1[2][4];
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) d1[u][e] = 0.f;
-        float2 sq = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int s2 = 0; s2 < KS / 2; ++s2) {
-            uint32_t x0, x1, x2, x3;            // k-step 2*s2: (x0, x1); 2*s2+1: (x2, x3)
-            ldsm_x4(sa + 64 * s2, x0, x1, x2, x3);
-            mma_rows8(d1[0], x0, x1, bq[2 * s2][0], bq[2 * s2][1]);
-            mma_rows8(d1[1], x2, x3, bq[2 * s2 + 1][0], bq[2 * s2 + 1][1]);
-            const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
-            sq = ffma2(f0, f0, sq);
-            sq = ffma2(f1, f1, sq);
-            sq = ffma2(f2, f2, sq);
-            sq = ffma2(f3, f3, sq);
-        }
-        const float dot = (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
-        float ssq = sq.x + sq.y;
-        ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
-        ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
-        // lane (i = g4, q = t4) holds dot_qi; lanes 4i.. hold sum(v_i^2)
+        // ---------------- pass 1: D1 = X Q on the tensor cores, sum(v_i^2) alongside
+        float dot, ssq;
+        int dq = t4;                         // query of this lane's dot
+        if constexpr (PACK) { dm_pass1_rows8_packed<KS>(sa, bq, t4, dot, ssq); dq = t4 >> 1; }
+        else dm_pass1_rows8<KS>(sa, bq, dot, ssq);
         constexpr int RS = L::RS;
         float *rb = red + (size_t)(it & 1) * 40 * RS;
-        rb[(t4 * 8 + g4) * RS + warp] = dot;
+        if (!PACK || (t4 & 1) == 0) rb[(dq * 8 + g4) * RS + warp] = dot;
         if (t4 == 0) rb[(32 + g4) * RS + warp] = ssq;
         // the previous item's output bulk stores must have read their shared rows
         // before the barrier that lets the producer refill that stage
@@ -286,21 +390,8 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
 
         // ---------------- softmax over sources: lane p = q*8 + i
         const int q = lane >> 3, i = lane & 7;
-        float ss = 0.f, dt = 0.f;
-        {
-            const float *ps = rb + (32 + i) * RS + gw0;
-            const float *pd = rb + (q * 8 + i) * RS + gw0;
-            if (a.wph % 4 == 0) {
-                for (int w = 0; w < a.wph; w += 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(ps + w);
-                    const float4 y = *reinterpret_cast<const float4 *>(pd + w);
-                    ss += (x.x + x.y) + (x.z + x.w);
-                    dt += (y.x + y.y) + (y.z + y.w);
-                }
-            } else {
-                for (int w = 0; w < a.wph; ++w) { ss += ps[w]; dt += pd[w]; }
-            }
-        }
+        float ss, dt;
+        dm_head_partials(rb, RS, gw0, a.wph, q, i, ss, dt);
         const bool pv = i < a.n_src && q < NQ;
         const float score = pv ? key_score(dt, ss, inv_dh, a.eps) : -INFINITY;
         const float cmax = seg_max<8>(score);
@@ -435,25 +526,7 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma2_kernel(const Depth
     // ------------------------------------------------------------ constants
     const int cbase = warp * CW;
     uint32_t bq[KS][2];
-    {
-        const int q = g4 >> 1, part = g4 & 1;
-#pragma unroll
-        for (int s = 0; s < KS; ++s)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = cbase + 16 * s + 8 * h + 2 * t4;
-                float v0 = 0.f, v1 = 0.f;
-                if (q < a.n_q) {
-                    v0 = __ldg(a.queries + (size_t)q * a.d + c);
-                    v1 = __ldg(a.queries + (size_t)q * a.d + c + 1);
-                    if (a.gain) { v0 *= __ldg(a.gain + c); v1 *= __ldg(a.gain + c + 1); }
-                }
-                float h0, l0, h1, l1;
-                split_bf16(v0, h0, l0);
-                split_bf16(v1, h1, l1);
-                bq[s][h] = part == 0 ? pack_bf16(h0, h1) : pack_bf16(l0, l1);
-            }
-    }
+    dm_query_fragments<KS>(a, cbase, g4, t4, bq);
     const int head = warp / a.wph;
     const int gw0 = head * a.wph;
     const float inv_dh = 1.f / (float)(CW * a.wph);
@@ -604,6 +677,233 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma2_kernel(const Depth
     }
 
     if (lane < 8) bulk_wait0();
+    if (producer && lane == 0) {
+        int never = 0;
+        for (int it = issued > a.nstages ? issued - a.nstages : 0; it < issued; ++it)
+            mbar_wait_bounded(&full[it % a.nstages], (uint32_t)(it / a.nstages) & 1, &never, a.wait);
+    }
+}
+
+// More than 8 sources, one token per item: the token's sources arrive in
+// chunks of 8 rows (one stage each) and are folded in by an online softmax.
+// Per query the running maximum m and normaliser l live in the softmax lanes
+// (lane q*8 + i); the output accumulators O^T stay in the MMA fragments across
+// the chunks, each chunk first scaling them by e^{m_old - m_new} and then
+// adding X'^T E with E = e^{s - m_new} (at most 1, split into bf16 hi and lo
+// like alpha in the one-chunk kernel).  After the token's last chunk the
+// fragments are divided by l, staged by stmatrix and stored in bulk as there.
+// A partial last chunk (n_src % 8 rows) leaves rows of its stage unfilled:
+// the warps that consumed that stage just before zero those rows (their
+// channel slice) so that they enter the MMAs as zeros, not as another
+// token's values.
+template <int NQ, int KS, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_multi_kernel(const DepthReadMmaArgs a) {
+    static_assert(NQ <= 4, "at most 4 queries (8 MMA columns: hi and lo per query)");
+    using L = DMLayout;
+    constexpr int CW = KS * 16;                 // channels per warp
+    constexpr int RS = L::RS;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.nstages * a.stage_bytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(full + DM_MAX_STAGES);
+    float *red = reinterpret_cast<float *>(smem + (size_t)a.nstages * a.stage_bytes + L::bar_bytes);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, t4 = lane & 3;
+
+    if (tid == 0) {
+        for (int s = 0; s < a.nstages; ++s) mbar_init(&full[s], 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    // every row of every stage starts zero (the copies overwrite them later:
+    // order these generic writes before the async-proxy writes)
+    for (int s = 0; s < a.nstages; ++s)
+        for (int i = 0; i < 8; ++i)
+            for (int b = tid * 16; b < a.d * 2; b += NW * 32 * 16)
+                *reinterpret_cast<uint4 *>(stages + (size_t)s * a.stage_bytes + (size_t)i * a.pitch + b) =
+                    make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    const int nch = (a.n_src + 7) >> 3;         // chunks per token
+    const int rlast = a.n_src - 8 * (nch - 1);  // rows of the last chunk (1..8)
+    const int gstride = gridDim.x;
+    const int n_tok = blockIdx.x < a.T ? (int)((a.T - blockIdx.x + gstride - 1) / gstride) : 0;
+    const int n_items = n_tok * nch;            // the host keeps this within int
+
+    // ------------------------------------------------------------ producer
+    const bool producer = (warp == 0) && !a.wait.inject_stall;
+    uint64_t pol = 0;
+    if (producer) pol = l2_policy_evict_first();
+    int p_stage = 0, p_j = 0;
+    int64_t p_tok = blockIdx.x;
+    const uint32_t row_bytes = (uint32_t)a.d * 2;
+    auto issue_next = [&]() {
+        if (lane == 0) {
+            const int rows = p_j == nch - 1 ? rlast : 8;
+            mbar_arrive_expect_tx(&full[p_stage], row_bytes * rows);
+            const unsigned char *g = a.src + p_tok * row_bytes + (int64_t)(8 * p_j) * a.src_stride_bytes;
+            for (int i = 0; i < rows; ++i)
+                bulk_g2s(stages + (size_t)p_stage * a.stage_bytes + (size_t)i * a.pitch,
+                         g + (int64_t)i * a.src_stride_bytes, row_bytes, &full[p_stage], pol);
+        }
+        if (++p_stage == a.nstages) p_stage = 0;
+        if (++p_j == nch) { p_j = 0; p_tok += gstride; }
+    };
+    int issued = 0;
+    if (producer)
+        for (; issued < n_items && issued < a.nstages; ++issued) issue_next();
+
+    // ------------------------------------------------------------ constants
+    const int cbase = warp * CW;
+    constexpr bool PACK = NQ <= 2;
+    uint32_t bq[PACK ? KS / 2 : KS][2];
+    if constexpr (PACK) dm_query_fragments_packed<KS>(a, cbase, g4, t4, bq);
+    else dm_query_fragments<KS>(a, cbase, g4, t4, bq);
+    const int head = warp / a.wph;
+    const int gw0 = head * a.wph;
+    const float inv_dh = 1.f / (float)(CW * a.wph);
+    const uint32_t lrow = (uint32_t)(lane & 7) * a.pitch + (uint32_t)(cbase + 8 * (lane >> 3)) * 2;
+    const uint32_t stage0 = smem_u32(stages);
+
+    float acc[KS][4];
+#pragma unroll
+    for (int k = 0; k < KS; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[k][e] = 0.f;
+    // softmax lane p = q*8 + i: running max / normaliser of query q
+    const int q = lane >> 3, i = lane & 7;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    int s = 0, j = 0;
+    uint32_t par = 0;
+    int64_t t = blockIdx.x;
+    // chunk index of the copy that refills the stage consumed at item it:
+    // item it + nstages
+    int jn = a.nstages % nch;
+    for (int it = 0; it < n_items; ++it) {
+        mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
+        const uint32_t sa = stage0 + (uint32_t)s * a.stage_bytes + lrow;
+        const int rows = j == nch - 1 ? rlast : 8;
+        const bool last = j == nch - 1;
+
+        // ---------------- pass 1 (as in the one-chunk kernel)
+        float dot, ssq;
+        int dq = t4;
+        if constexpr (PACK) { dm_pass1_rows8_packed<KS>(sa, bq, t4, dot, ssq); dq = t4 >> 1; }
+        else dm_pass1_rows8<KS>(sa, bq, dot, ssq);
+        float *rb = red + (size_t)(it & 1) * 40 * RS;
+        if (!PACK || (t4 & 1) == 0) rb[(dq * 8 + g4) * RS + warp] = dot;
+        if (t4 == 0) rb[(32 + g4) * RS + warp] = ssq;
+        if (it >= 1) {
+            // the stage consumed at it-1 is refilled after the barrier below with
+            // item it-1+nstages: its output rows (if it held a token's last chunk)
+            // must have been read by the bulk stores, and rows that the refill
+            // leaves empty must be zero
+            if (lane < a.n_q) bulk_wait_read0();
+            const int jp = jn == 0 ? nch - 1 : jn - 1;
+            if (jp == nch - 1 && rlast < 8 && it - 1 + a.nstages < n_items) {
+                __syncwarp();
+                const int sp = s == 0 ? a.nstages - 1 : s - 1;
+                for (int row = rlast; row < 8; ++row)
+                    for (int b = lane * 16; b < CW * 2; b += 32 * 16)
+                        *reinterpret_cast<uint4 *>(stages + (size_t)sp * a.stage_bytes + (size_t)row * a.pitch +
+                                                   (size_t)cbase * 2 + b) = make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+            }
+        }
+        __syncthreads();
+        if (producer && it >= 1 && issued < n_items) {
+            if (__shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0)) { issue_next(); ++issued; }
+        }
+
+        // ---------------- online softmax over this chunk's sources
+        float ss, dt;
+        dm_head_partials(rb, RS, gw0, a.wph, q, i, ss, dt);
+        const bool pv = i < rows && q < NQ;
+        const float score = pv ? key_score(dt, ss, inv_dh, a.eps) : -INFINITY;
+        const float m_new = fmaxf(m_run, seg_max<8>(score));
+        const float corr = __expf(m_run - m_new);   // 0 on the token's first chunk
+        const float e = pv ? __expf(score - m_new) : 0.f;
+        l_run = l_run * corr + seg_sum<8>(e);
+        m_run = m_new;
+        if (last && i == 0 && q < a.n_q && warp == gw0 && a.lse != nullptr && !*abort_flag)
+            a.lse[((int64_t)q * a.H + head) * a.T + t] = m_run + __logf(l_run);
+
+        // pass-2 B fragment (sources 2*t4, 2*t4+1 of column q = g4), and the
+        // per-column factors of this lane's accumulators (columns 2*t4, 2*t4+1;
+        // columns 4..7 are always zero)
+        const int srcl = (g4 & 3) * 8 + 2 * t4;
+        const float e0 = __shfl_sync(0xffffffffu, e, srcl);
+        const float e1 = __shfl_sync(0xffffffffu, e, srcl + 1);
+        uint32_t bb0 = 0u, bb1 = 0u;
+        if (g4 < NQ) {
+            float h0, l0, h1, l1;
+            split_bf16(e0, h0, l0);
+            split_bf16(e1, h1, l1);
+            bb0 = pack_bf16(h0, h1);
+            bb1 = pack_bf16(l0, l1);
+        }
+        const int cl0 = ((2 * t4) & 3) * 8, cl1 = ((2 * t4 + 1) & 3) * 8;
+        const float2 cf = make_float2(__shfl_sync(0xffffffffu, corr, cl0), __shfl_sync(0xffffffffu, corr, cl1));
+
+        // ---------------- pass 2: rescale, accumulate
+        if (!last) {
+#pragma unroll
+            for (int s2 = 0; s2 < KS / 2; ++s2) {
+                uint32_t y[4];
+                ldsm_x4_t(sa + 64 * s2, y[0], y[1], y[2], y[3]);
+                dm_rescale(acc[2 * s2], cf);
+                dm_rescale(acc[2 * s2 + 1], cf);
+                mma_full(acc[2 * s2], y[0], y[1], y[0], y[1], bb0, bb1);
+                mma_full(acc[2 * s2 + 1], y[2], y[3], y[2], y[3], bb0, bb1);
+            }
+        } else {
+            // last chunk: normalise, stage the outputs by stmatrix, clear the
+            // accumulators and the running state for the next token
+            const float inv_l = 1.f / l_run;
+            const float2 fin = make_float2(__shfl_sync(0xffffffffu, inv_l, cl0),
+                                           __shfl_sync(0xffffffffu, inv_l, cl1));
+            const uint32_t orow = stage0 + (uint32_t)s * a.stage_bytes + (uint32_t)(lane & 7) * a.pitch +
+                                  (uint32_t)(cbase + 8 * (lane >> 3)) * 2;
+#pragma unroll
+            for (int s2 = 0; s2 < KS / 2; ++s2) {
+                uint32_t y[4];
+                ldsm_x4_t(sa + 64 * s2, y[0], y[1], y[2], y[3]);
+                dm_rescale(acc[2 * s2], cf);
+                dm_rescale(acc[2 * s2 + 1], cf);
+                mma_full(acc[2 * s2], y[0], y[1], y[0], y[1], bb0, bb1);
+                mma_full(acc[2 * s2 + 1], y[2], y[3], y[2], y[3], bb0, bb1);
+                dm_rescale(acc[2 * s2], fin);
+                dm_rescale(acc[2 * s2 + 1], fin);
+                stsm_x4_t(orow + 64 * s2, f2_to_bf2(acc[2 * s2][0], acc[2 * s2][1]),
+                          f2_to_bf2(acc[2 * s2][2], acc[2 * s2][3]),
+                          f2_to_bf2(acc[2 * s2 + 1][0], acc[2 * s2 + 1][1]),
+                          f2_to_bf2(acc[2 * s2 + 1][2], acc[2 * s2 + 1][3]));
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) { acc[2 * s2][e2] = 0.f; acc[2 * s2 + 1][e2] = 0.f; }
+            }
+            m_run = -INFINITY;
+            l_run = 0.f;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane < a.n_q) {
+                if (!*abort_flag)
+                    bulk_s2g(a.out + (int64_t)lane * a.out_q_stride_bytes + (t * a.d + cbase) * 2,
+                             stage0 + (uint32_t)s * a.stage_bytes + (uint32_t)lane * a.pitch + (uint32_t)cbase * 2,
+                             (uint32_t)CW * 2);
+                bulk_commit();
+            }
+        }
+        if (++s == a.nstages) { s = 0; par ^= 1u; }
+        if (++j == nch) { j = 0; t += gstride; }
+        if (++jn == nch) jn = 0;
+    }
+
+    if (lane < a.n_q) bulk_wait0();
     if (producer && lane == 0) {
         int never = 0;
         for (int it = issued > a.nstages ? issued - a.nstages : 0; it < issued; ++it)

@@ -24,6 +24,8 @@ bool lookup_depth_read_f32_multi(int nq, int vpt, bool mh, KernelRef *out);
 bool lookup_depth_read_mma(int nq, int ks, int nw, KernelRef *out);
 // depth_read_mma2_kernel<nq, ks, nw>: two tokens per item (d = 1024, 2048)
 bool lookup_depth_read_mma2(int nq, int ks, int nw, KernelRef *out);
+// depth_read_mma_multi_kernel<nq, ks, nw>: > 8 sources in chunks of 8 (online softmax)
+bool lookup_depth_read_mma_multi(int nq, int ks, int nw, KernelRef *out);
 
 // phase2_merge_kernel<T, vpt>
 bool lookup_phase2(int dt, int vpt, KernelRef *out);

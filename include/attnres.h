@@ -205,10 +205,13 @@ void attnres_debug_set_stall_injection(int enable);
 
 /*
  * Kernel selection, meant for tests and measurements: 0 (default) lets the
- * library pick (tensor-core kernel for bf16 reads with <= 8 sources and <= 4
- * queries at d = 1024, 2048 or 4096; the general CUDA-core kernel otherwise);
- * 1 forces the general kernel for Full / phase 1 / MHAR.  Both compute the
- * same operation.  Applies to calls made afterwards.
+ * library pick (tensor-core kernels for bf16 reads with <= 4 queries at
+ * d = 1024, 2048 or 4096 and <= 8 sources, and at d = 4096 for more sources
+ * where the chunked tensor-core kernel was measured faster; the general
+ * CUDA-core kernel otherwise); 1 forces the general kernel for Full / phase 1
+ * / MHAR; 2 takes the tensor-core kernels wherever they apply (the chunked
+ * one for any source count > 8 at d = 4096).  All compute the same
+ * operation.  Applies to calls made afterwards; other values act as 0.
  */
 void attnres_debug_set_kernel_variant(int variant);
 

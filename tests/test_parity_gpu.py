@@ -380,6 +380,47 @@ def test_mhar_both_kernels(kernel_variant, H, d, T, n_src):
     check_lse(lse, rl)
 
 
+@pytest.fixture(params=[0, 1, 2], ids=["auto", "general", "tensor"])
+def kernel_variant3(request):
+    """kernel_variant plus 2: the tensor-core kernels wherever they apply (the
+    chunked one for every source count > 8 at d = 4096)."""
+    attnres.attnres_debug_set_kernel_variant(request.param)
+    yield request.param
+    attnres.attnres_debug_set_kernel_variant(0)
+
+
+@pytest.mark.parametrize("n_src,n_q,H,T,d", [(9, 1, 1, 700, 4096), (16, 4, 1, 50, 4096), (12, 3, 1, 170, 4096),
+                                             (23, 2, 1, 400, 4096), (64, 1, 1, 160, 4096), (31, 1, 1, 300, 4096),
+                                             (11, 4, 8, 40, 4096), (20, 4, 4, 33, 4096), (17, 1, 1, 1, 4096),
+                                             (13, 2, 2, 90, 2048)])
+def test_chunked_read_both_kernels(kernel_variant3, n_src, n_q, H, T, d):
+    """More than 8 sources: chunks of 8 folded in by the online softmax; full
+    and partial last chunks, several tokens per CTA, heads, a single token."""
+    rng = _rng(n_src * 17 + n_q + H * 5 + T + d)
+    src = _sources(rng, n_src, T, d, BF16, step=1 / 16)
+    q = (rng.standard_normal((n_q, H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    out, lse = attnres.mhar_fwd(to_dev(src, BF16), to_dev(q, F32), to_dev(g, F32), 1e-6, want_lse=True)
+    ro, rl = oracle.mhar(src, q, g, 1e-6, want_lse=True)
+    check_out(out, ro, BF16, np.abs(src).max())
+    check_lse(lse, rl)
+
+
+def test_chunked_read_keeps_non_finite_tokens_apart(kernel_variant3):
+    """Tokens whose first chunk holds infinities get non-finite outputs; the
+    rows that a partial last chunk leaves unloaded must not carry them into
+    other tokens' reads."""
+    rng = _rng(77)
+    n_src, T, d = 9, 400, 4096
+    src = _sources(rng, n_src, T, d, BF16, step=1 / 16)
+    bad = np.arange(0, T, 5)
+    src[1:8, bad, :] = np.inf
+    w = _queries(rng, 1, d)[0]
+    out = to_host(attnres.attnres_full_fwd(to_dev(src, BF16), to_dev(w, F32), None, 1e-6))
+    good = np.setdiff1d(np.arange(T), bad)
+    check_out(out[good], oracle.full(np.ascontiguousarray(src[:, good]), w, None, 1e-6), BF16)
+
+
 def test_kernels_agree_closely():
     """The two kernels compute the same read; their bf16 outputs may differ by
     at most one rounding step."""
