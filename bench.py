@@ -306,6 +306,13 @@ class MsarWorkload(BlockWorkload):
         self.dominant = "msar_kernel"
         self.dominant_src = "msar"
         self.profile_tag = f"ncu_msar_d{d}"
+        # The read is bound by fp32 arithmetic, not HBM: its roofline is the
+        # CUDA-core FMA rate.  Multiply-adds per token: the causal convolutions
+        # (N sources x d channels x (4+8+12) taps), per (source, stream) the
+        # sum of squares and the query dot (N x 4 x 2 x d), the weighted sums
+        # (4 x N x d), the mixer's sum of squares (4d), projection (4d x 4) and
+        # the output sum (4 x d).
+        self.fma_per_token = N * d * sum(self.ks) + N * 4 * 2 * d + 4 * N * d + 4 * d + 4 * d * 4 + 4 * d
 
     def config(self):
         c = super().config()
@@ -574,6 +581,22 @@ def run_cuda(args):
 
     if rank != 0:
         return
+    roofline = {"kernel": wl.dominant, "bound": "hbm", "achieved": achieved,
+                "peak": hbm_peak, "peak_kind": peaks_kind, "unit": "GB/s",
+                "frac": achieved / hbm_peak,
+                "bytes_per_launch": dom_bytes, "ms_per_launch": dom_ms,
+                "traffic": traffic}
+    fma = getattr(wl, "fma_per_token", None)
+    if fma:
+        # fp32 CUDA-core peak from the unit counts and the clock: 152 SMs x
+        # 128 fp32 lanes x 2 flops per FMA x the maximum SM clock (2070 MHz)
+        alu_peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        tflops = 2.0 * fma * wl.T / (dom_ms / 1e3) / 1e12
+        roofline = {"kernel": wl.dominant, "bound": "alu", "achieved": tflops, "peak": alu_peak,
+                    "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                    "unit": "TFLOP/s", "frac": tflops / alu_peak,
+                    "flops_per_launch": 2.0 * fma * wl.T, "ms_per_launch": dom_ms,
+                    "hbm_gbs": achieved, "traffic": traffic}
     line = {
         "metric": METRIC if args.workload == "block" else f"{wl.name} tokens/s",
         "value": value,
@@ -590,11 +613,7 @@ def run_cuda(args):
         "config": dict(wl.config(), parallelism=f"replicas x{world} (no collective)"),
         "hbm_gbs_step": step_gbs,
         "hbm_frac_step": step_gbs / hbm_peak,
-        "roofline": {"kernel": wl.dominant, "bound": "hbm", "achieved": achieved,
-                     "peak": hbm_peak, "peak_kind": peaks_kind, "unit": "GB/s",
-                     "frac": achieved / hbm_peak,
-                     "bytes_per_launch": dom_bytes, "ms_per_launch": dom_ms,
-                     "traffic": traffic},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": E,
                 "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h},
