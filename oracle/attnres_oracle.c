@@ -225,6 +225,27 @@ int oracle_block_phase2(const double *o, const double *lse, const double *partia
     return 0;
 }
 
+/* Intra-block partial-sum update fused with the next layer's merge.
+ * [Summary §2 Block AttnRes]: the current block's source for layer i >= 2 is
+ * the partial sum b_{i-1}^(n) of the block's layer outputs so far;
+ * [Tutorial Fig. 4]: once a layer's output f is produced, only the current
+ * partial sum changes, to the old partial plus f (the embedding and the
+ * completed block sums stay as they are).  [Summary §3 Inference, Phase 2]:
+ * the merge of the next layer then scores that new partial.
+ *   p_out = p + f            (p == NULL: the block's first output, p_out = f)
+ *   out   = phase-2 merge of (o, lse) with p_out      (oracle_block_phase2)
+ * p, f, p_out, o, out [T][d]; lse [T]. */
+int oracle_block_phase2_update(const double *p, const double *f, const double *o,
+                               const double *lse, int64_t T, int64_t d, const double *query,
+                               const double *gain, double eps, double *p_out, double *out)
+{
+    if (!f || !o || !lse || !query || !p_out || !out || T < 0 || d < 1 || eps < 0) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < d; ++c)
+            p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];
+    return oracle_block_phase2(o, lse, p_out, T, d, query, gain, eps, out);
+}
+
 /* ---------------------------------------------------------------------- */
 /* MHAR                                                                    */
 /* ---------------------------------------------------------------------- */
@@ -258,6 +279,39 @@ int oracle_mhar(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t 
                 if (lse) lse[(q * H + hd) * T + t] = l;
             }
     free(rows); free(h);
+    return 0;
+}
+
+/* MHAR inside the two-phase Block schedule.  Phase 1 is oracle_mhar over
+ * the cached block representations (it keeps lse per head); phase 2 folds in
+ * the layer's partial sum head by head, each head with its own slice of the
+ * query, the gain and the RMSNorm ([MHAR abstract]: every head has its own
+ * softmax over the sources, the read is block-diagonal), by the merge of
+ * [Summary §3 Inference, Phase 2]:
+ *   s_h = w_h . RMSNorm_h(p_h),  M = max(lse_h, s_h),
+ *   out_h = (e^{lse_h - M} o_h + e^{s_h - M} p_h) / (e^{lse_h - M} + e^{s_h - M}).
+ * o, partial, out [T][d]; lse [H][T]; query [H][d/H]; partial == NULL copies o. */
+int oracle_mhar_phase2(const double *o, const double *lse, const double *partial,
+                       int64_t T, int64_t d, int64_t H, const double *query,
+                       const double *gain, double eps, double *out)
+{
+    if (!o || !lse || !query || !out || T < 0 || d < 1 || H < 1 || d % H || eps < 0) return -1;
+    const int64_t dh = d / H;
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)dh);
+    if (!tmp) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t hd = 0; hd < H; ++hd) {
+            const double *oh = o + t * d + hd * dh;
+            double *outh = out + t * d + hd * dh;
+            if (!partial) { for (int64_t c = 0; c < dh; ++c) outh[c] = oh[c]; continue; }
+            const double *ph = partial + t * d + hd * dh;
+            const double l = lse[hd * T + t];
+            double sp = score(query + hd * dh, ph, gain ? gain + hd * dh : NULL, dh, eps, tmp);
+            double M = l > sp ? l : sp;
+            double a = exp(l - M), b = exp(sp - M);
+            for (int64_t c = 0; c < dh; ++c) outh[c] = (a * oh[c] + b * ph[c]) / (a + b);
+        }
+    free(tmp);
     return 0;
 }
 

@@ -50,6 +50,9 @@ def _load():
         lib.oracle_block_phase1.argtypes = [_D, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double,
                                             _D, _D]
         lib.oracle_block_phase2.argtypes = [_D, _D, _D, _I64, _I64, _D, _D, ctypes.c_double, _D]
+        lib.oracle_block_phase2_update.argtypes = [_D, _D, _D, _D, _I64, _I64, _D, _D,
+                                                   ctypes.c_double, _D, _D]
+        lib.oracle_mhar_phase2.argtypes = [_D, _D, _D, _I64, _I64, _I64, _D, _D, ctypes.c_double, _D]
         lib.oracle_mhar.argtypes = [_D, _I64, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double,
                                     _D, _D]
         lib.oracle_msar_conv.argtypes = [_D, _I64, _I64, _I64, _D, _D]
@@ -57,7 +60,8 @@ def _load():
                                     _D, _D, _D, ctypes.c_double, _D, _D, ctypes.c_double, _D,
                                     _D, _D]
         for f in ("oracle_full", "oracle_weighted_sum", "oracle_block_oneshot",
-                  "oracle_block_phase1", "oracle_block_phase2", "oracle_mhar",
+                  "oracle_block_phase1", "oracle_block_phase2", "oracle_block_phase2_update",
+                  "oracle_mhar_phase2", "oracle_mhar",
                   "oracle_msar_conv", "oracle_msar"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -137,6 +141,32 @@ def block_phase2(o, lse, partial, query, gain=None, eps=1e-6):
     out = np.empty((T, d))
     _check(_load().oracle_block_phase2(_p(o), _p(lse), _p(partial), T, d, _p(query), _p(gain),
                                        float(eps), _p(out)), "oracle_block_phase2")
+    return out
+
+
+def block_phase2_update(p, f, o, lse, query, gain=None, eps=1e-6):
+    """Partial-sum update fused with the next layer's merge: p [T,d] or None,
+    f [T,d], o [T,d], lse [T] -> (p + f, merged out)."""
+    f, o, lse, query, gain = _f64(f), _f64(o), _f64(lse), _f64(query), _f64(gain)
+    p = _f64(p) if p is not None else None
+    T, d = o.shape
+    p_out = np.empty((T, d))
+    out = np.empty((T, d))
+    _check(_load().oracle_block_phase2_update(_p(p), _p(f), _p(o), _p(lse), T, d, _p(query), _p(gain),
+                                              float(eps), _p(p_out), _p(out)), "oracle_block_phase2_update")
+    return p_out, out
+
+
+def mhar_phase2(o, lse, partial, query, gain=None, eps=1e-6):
+    """Per-head phase-2 merge: o [T,d], lse [H,T], partial [T,d] or None,
+    query [H,d/H] -> out [T,d]."""
+    o, lse, query, gain = _f64(o), _f64(lse), _f64(query), _f64(gain)
+    partial = _f64(partial) if partial is not None else None
+    T, d = o.shape
+    H = query.shape[0]
+    out = np.empty((T, d))
+    _check(_load().oracle_mhar_phase2(_p(o), _p(lse), _p(partial), T, d, H, _p(query), _p(gain),
+                                      float(eps), _p(out)), "oracle_mhar_phase2")
     return out
 
 

@@ -250,6 +250,58 @@ def test_phase2_without_partial_is_identity():
     assert np.array_equal(out, o)
 
 
+def test_fused_update_chain_equals_oneshot_block():
+    """Summary section 2: layer i >= 2 of a block reads the partial sum of the
+    block's outputs so far; Tutorial Fig. 4: each new output only changes the
+    current partial.  Chaining the fused update-and-merge over a block gives the
+    one-shot Block read with the cumulative partials, and the last partial is
+    the block's sum of outputs."""
+    rng = np.random.default_rng(21)
+    N, S, T, d = 4, 5, 5, 24
+    cache = _rand(rng, N, T, d) * (1 + np.arange(N))[:, None, None]
+    f = _rand(rng, S, T, d)                       # outputs f_1..f_S of the block's layers
+    q = _rand(rng, S, d, scale=2.0)
+    g = rng.uniform(0.5, 1.5, d)
+    partials = np.zeros((S, T, d))
+    partials[1:] = np.cumsum(f[:-1], axis=0)       # layer i reads f_1 + ... + f_{i-1}
+    ref = oracle.block_oneshot(cache, partials, q, g, eps=1e-6)
+    o, lse = oracle.block_phase1(cache, q, g, eps=1e-6)
+    p = None
+    for i in range(1, S):
+        p, out = oracle.block_phase2_update(p, f[i - 1], o[i], lse[i], q[i], g, eps=1e-6)
+        assert np.allclose(out, ref[i], atol=1e-13, rtol=0)
+    p, _ = oracle.block_phase2_update(p, f[S - 1], o[0], lse[0], q[0], g, eps=1e-6)
+    assert np.allclose(p, f.sum(axis=0), atol=1e-13, rtol=0)
+
+
+def test_fused_update_tutorial_fig4_state():
+    """Tutorial Fig. 4: the block keeps e, f1+f2 and the current f3; after f4
+    the current sum is f3+f4 and the next layer reads e, f1+f2, f3+f4 (a Full
+    read over those three sources)."""
+    e = np.array([2.0, 0, 0, 0])
+    f1 = np.array([0, 4.0, 0, 0])
+    f2 = np.array([0, 0, 6.0, 0])
+    f3 = np.array([0, 0, 0, 8.0])
+    f4 = np.array([1.0, -2.0, 0.5, 3.0])
+    w = np.array([0.3, 1.2, -0.7, 0.4])
+    cache = np.stack([e, f1 + f2])[:, None, :]
+    o, lse = oracle.block_phase1(cache, w[None, :], None, eps=0.0)
+    p, out = oracle.block_phase2_update(f3[None, :], f4[None, :], o[0], lse[0], w, None, eps=0.0)
+    assert np.array_equal(p[0], f3 + f4)
+    ref = oracle.full(np.stack([e, f1 + f2, f3 + f4])[:, None, :], w, None, eps=0.0)
+    assert np.allclose(out, ref, atol=1e-14, rtol=0)
+
+
+def test_fused_update_without_old_partial_starts_the_sum():
+    rng = np.random.default_rng(22)
+    T, d = 3, 16
+    f, o = _rand(rng, T, d), _rand(rng, T, d)
+    lse, q = _rand(rng, T), _rand(rng, d)
+    p, out = oracle.block_phase2_update(None, f, o, lse, q, eps=1e-6)
+    assert np.array_equal(p, f)
+    assert np.allclose(out, oracle.block_phase2(o, lse, f, q, eps=1e-6), atol=0, rtol=0)
+
+
 # --------------------------------------------------------------------------
 # MHAR
 # --------------------------------------------------------------------------
@@ -290,6 +342,34 @@ def test_mhar_read_is_block_diagonal():
     changed = np.abs(pert - base).max(axis=(0, 1)) > 0
     assert np.all(changed[dh:2 * dh])
     assert not np.any(changed[:dh]) and not np.any(changed[2 * dh:])
+
+
+def test_mhar_two_phase_equals_oneshot():
+    """MHAR inside the two-phase schedule: phase 1 over the cached reps keeps
+    lse per head; the per-head merge of the partial gives the one-shot MHAR
+    read over the reps plus the partial."""
+    rng = np.random.default_rng(23)
+    H, dh, N, T = 4, 8, 5, 6
+    d = H * dh
+    cache = _rand(rng, N, T, d) * (1 + np.arange(N))[:, None, None]
+    p = _rand(rng, T, d, scale=2.0)
+    q = _rand(rng, 1, H, dh, scale=2.0)
+    g = rng.uniform(0.5, 1.5, d)
+    o, lse = oracle.mhar(cache, q, g, eps=1e-6, want_lse=True)
+    two = oracle.mhar_phase2(o[0], lse[0], p, q[0], g, eps=1e-6)
+    one = oracle.mhar(np.concatenate([cache, p[None]]), q, g, eps=1e-6)[0]
+    assert np.allclose(two, one, atol=1e-13, rtol=0)
+
+
+def test_mhar_phase2_one_head_is_block_phase2():
+    rng = np.random.default_rng(24)
+    T, d = 4, 24
+    o, p = _rand(rng, T, d), _rand(rng, T, d)
+    lse, q = _rand(rng, T), _rand(rng, d)
+    g = rng.uniform(0.5, 1.5, d)
+    a = oracle.mhar_phase2(o, lse[None], p, q[None], g, eps=1e-6)
+    b = oracle.block_phase2(o, lse, p, q, g, eps=1e-6)
+    assert np.allclose(a, b, atol=1e-15, rtol=0)
 
 
 # --------------------------------------------------------------------------

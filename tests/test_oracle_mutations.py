@@ -23,9 +23,15 @@ MUTANTS = {
          "for (int64_t i = 1; i < n_src; ++i) acc += a[i] * rows[i][c];")],
     "gain_ignored": [("double gc = g ? g[c] : 1.0;", "double gc = 1.0;")],
     "lse_drops_max": [("return m + log(l);", "return log(l);")],
-    "merge_sign": [("b = exp(sp - M);", "b = exp(M - sp);")],
+    "merge_sign": [("double a = exp(lse[t] - M), b = exp(sp - M);", "double a = exp(lse[t] - M), b = exp(M - sp);")],
+    "mhar_phase2_merge_sign": [("double a = exp(l - M), b = exp(sp - M);", "double a = exp(l - M), b = exp(M - sp);")],
     "first_layer_reads_partial": [("if (li >= 1) { rows[N]", "if (li >= 0) { rows[N]")],
     "mhar_query_transposed": [("queries + (q * H + hd) * dh", "queries + (hd * n_q + q) * dh")],
+    "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
+                                  "p_out[t * d + c] = f[t * d + c];")],
+    "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
+    "mhar_phase2_gain_not_sliced": [("double sp = score(query + hd * dh, ph, gain ? gain + hd * dh : NULL, dh, eps, tmp);",
+                                     "double sp = score(query + hd * dh, ph, gain, dh, eps, tmp);")],
     "conv_kernel_reversed": [("acc += cw[c * k + j] * v[(t - j) * d + c];",
                               "acc += cw[c * k + (k - 1 - j)] * v[(t - j) * d + c];")],
     "conv_anticausal": [("if (t - j >= 0) acc += cw[c * k + j] * v[(t - j) * d + c];",
