@@ -10,7 +10,7 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|msar|full_depth|
-block_d2048) are for profiling and the design notes.
+block_d2048|block_fused) are for profiling and the design notes.
 """
 from __future__ import annotations
 
@@ -225,6 +225,69 @@ class BlockWorkload:
         cache, parts, q = sample
         oracle.block_twophase(cache, parts, q, None, 1e-6)
         return cache.shape[1]
+
+
+class BlockFusedWorkload(BlockWorkload):
+    """Block AttnRes two-phase forward of one block with the intra-block
+    partial sum maintained on the way: phase 1, then each layer i >= 2 adds the
+    previous layer's output f_{i-1} to the partial and merges it in one fused
+    call (the first call starts the partial from f_1).  The layer outputs are
+    synthetic inputs [S, T, d] ~ N(0, 1)."""
+
+    def __init__(self, T=32768, d=4096, N=8, S=4, seed=0):
+        super().__init__(T, d, N, S, seed, name="block_attnres_two_phase_fused_update")
+        b = 2
+        first = 4 * d * b + 4          # read f, o, lse; write partial, out
+        later = 5 * d * b + 4          # read partial, f, o, lse; write partial, out
+        self.merge_bytes_per_token = later
+        self.bytes_per_token = self.phase1_bytes_per_token + first + (S - 2) * later
+
+    def setup(self, device):
+        import torch
+        super().setup(device)
+        self.f = self.partials                       # f_1..f_S, one per layer
+        self.p = torch.empty((self.T, self.d), dtype=torch.bfloat16, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.attnres_block_phase1(self.cache, self.queries, None, 1e-6, o=self.o, lse=self.lse,
+                                     stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for i in range(1, self.S):
+            attnres.attnres_block_phase2_update_merge(self.p if i > 1 else None, self.f[i - 1], self.o[i],
+                                                      self.lse[i], self.queries[i], None, 1e-6,
+                                                      partial_out=self.p, out=self.o[i], stream=stream)
+
+    def setup_host(self):
+        super().setup_host()
+        self.h_parts = torch_pinned_like(self.f[:self.S - 1])
+        self.h2d = (self.h_cache.numel() + self.h_parts.numel()) * 2 + self.h_q.numel() * 4
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.f[:self.S - 1].copy_(self.h_parts, non_blocking=True)
+        self.queries.copy_(self.h_q, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.o, non_blocking=True)
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        cache, f, q = sample
+        o, lse = oracle.block_phase1(cache, q, None, 1e-6)
+        p = None
+        for i in range(1, self.S):
+            p, _ = oracle.block_phase2_update(p, f[i - 1], o[i], lse[i], q[i], None, 1e-6)
+        return cache.shape[1]
+
+
+def torch_pinned_like(t):
+    import torch
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
 
 
 class MharWorkload(BlockWorkload):
@@ -454,6 +517,8 @@ def make_workload(name, T=None):
         return MharWorkload(T=T or 131072)
     if name == "msar":
         return MsarWorkload(T=T or 32768)
+    if name == "block_fused":
+        return BlockFusedWorkload(T=T or 32768)
     if name == "full_depth":
         return FullDepthWorkload(T=T or 16384)
     raise SystemExit(f"unknown workload {name}")
@@ -688,7 +753,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "mhar", "msar", "full_depth"])
+                    choices=["block", "block_d2048", "block_fused", "mhar", "msar", "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

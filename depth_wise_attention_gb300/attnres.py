@@ -29,6 +29,9 @@ _SIGS = {
     "attnres_block_phase1": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp,
                              _vp, _vp],
     "attnres_block_phase2_merge": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp, _f, _vp, _vp],
+    "attnres_block_phase2_update_merge": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp,
+                                          _f, _vp, _vp],
+    "mhar_phase2_merge": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _f, _vp, _vp],
     "mhar_fwd": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp,
                  _vp],
     "msar_expand_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
@@ -160,6 +163,40 @@ def attnres_block_phase2_merge(o, lse, partial, query, gain=None, eps=1e-6, out=
         _p(o), _p(lse), _p(partial), T, d, _dt(o), _p(query), _p(gain), eps, _p(out),
         _stream(stream)))
     return out
+
+
+def attnres_block_phase2_update_merge(partial, f, o, lse, query, gain=None, eps=1e-6, partial_out=None,
+                                      out=None, stream=None):
+    """Fused update and merge: partial [T,d] or None, f [T,d] -> (partial + f, merged out).
+    partial_out may be partial or f (in place); out may be o."""
+    import torch
+    T, d = o.shape
+    if partial_out is None:
+        partial_out = torch.empty_like(f)
+    if out is None:
+        out = torch.empty_like(o)
+    _check("attnres_block_phase2_update_merge", load().attnres_block_phase2_update_merge(
+        _p(partial), _p(f), _p(partial_out), _p(o), _p(lse), T, d, _dt(o), _p(query), _p(gain), eps,
+        _p(out), _stream(stream)))
+    return partial_out, out
+
+
+def mhar_phase2_merge(o, lse, partial, query, gain=None, eps=1e-6, f=None, partial_out=None, out=None,
+                      stream=None):
+    """Per-head phase-2 merge: o [T,d], lse [H,T], partial [T,d] or None, query [H,d/H].
+    With f, the partial is first updated (returned as partial_out).  Returns out, or
+    (partial_out, out) when f is given."""
+    import torch
+    T, d = o.shape
+    H = query.shape[0]
+    if f is not None and partial_out is None:
+        partial_out = torch.empty_like(f)
+    if out is None:
+        out = torch.empty_like(o)
+    _check("mhar_phase2_merge", load().mhar_phase2_merge(
+        _p(o), _p(lse), _p(partial), _p(f), _p(partial_out), T, d, H, _dt(o), _p(query), _p(gain), eps,
+        _p(out), _stream(stream)))
+    return (partial_out, out) if f is not None else out
 
 
 def mhar_fwd(src, queries, gain=None, eps=1e-6, out=None, lse=None, want_lse=False, stream=None):

@@ -25,6 +25,7 @@ SOURCES = [
     "kernels_f32.cu",
     "kernels_f32_multi.cu",
     "kernels_phase2.cu",
+    "kernels_phase2_mh.cu",
     "kernels_mma.cu",
     "kernels_mma_multi.cu",
     "msar.cu",

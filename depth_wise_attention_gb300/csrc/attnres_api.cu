@@ -339,6 +339,93 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     return ATTNRES_OK;
 }
 
+// Shared launch path of the phase-2 merges (one head or H heads, with or
+// without the fused partial-sum update).  upd: partial_out = partial + f, and
+// the merge scores it; otherwise the merge scores partial (NULL: out = o).
+attnres_status_t launch_phase2(const void *o, const float *lse, const void *partial, const void *f,
+                               void *partial_out, bool upd, int64_t T, int64_t d, int64_t H,
+                               attnres_dtype_t dt, const float *query, const float *gain, float eps,
+                               void *out, void *stream) {
+    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
+    if (T < 0 || d < 1 || H < 1 || d % H != 0 || !(eps >= 0.f) || std::isinf(eps)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!o || !out)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && upd && (!f || !partial_out)) return ATTNRES_ERR_INVALID_ARG;
+    const bool merges = upd || partial;
+    if (T > 0 && merges && (!lse || !query)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t nbytes = (size_t)T * (size_t)d * es;
+    const size_t lbytes = (size_t)H * (size_t)T * 4;
+    // out may be o itself but may overlap no other tensor; the updated partial
+    // may be partial or f itself but may overlap nothing else
+    if (out != o && overlap(out, nbytes, o, nbytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (partial && overlap(out, nbytes, partial, nbytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (upd) {
+        if (overlap(out, nbytes, f, nbytes) || overlap(out, nbytes, partial_out, nbytes) ||
+            overlap(partial_out, nbytes, o, nbytes))
+            return ATTNRES_ERR_INVALID_ARG;
+        if (partial_out != partial && partial && overlap(partial_out, nbytes, partial, nbytes))
+            return ATTNRES_ERR_INVALID_ARG;
+        if (partial_out != f && overlap(partial_out, nbytes, f, nbytes)) return ATTNRES_ERR_INVALID_ARG;
+    }
+    if (merges && lse && (overlap(lse, lbytes, out, nbytes) || (upd && overlap(lse, lbytes, partial_out, nbytes))))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(o) || !aligned16(out) || (partial && !aligned16(partial)) || (f && !aligned16(f)) ||
+        (partial_out && !aligned16(partial_out)) || (query && !aligned16(query)) ||
+        (gain && !aligned16(gain)) || (lse && !aligned4(lse)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    const int EPV = epv(dt);
+    const int nvec = (int)(d / EPV);
+    int seg = nvec;
+    if (H > 1) {
+        // a head is whole 16-byte vectors, and either whole warps of them or a
+        // power-of-two group inside a warp
+        if ((d / H) % EPV != 0) return ATTNRES_ERR_UNSUPPORTED;
+        seg = (int)(nvec / H);
+        if (seg % 32 != 0 && (seg > 32 || (seg & (seg - 1)) != 0)) return ATTNRES_ERR_UNSUPPORTED;
+    }
+    if (T == 0) return ATTNRES_OK;
+    if (!merges) {
+        if (out == o) return ATTNRES_OK;
+        cudaError_t e = cudaMemcpyAsync(out, o, nbytes, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemcpyAsync");
+    }
+    int tpr, vpt;
+    row_shape(nvec, &tpr, &vpt);
+    KernelRef kr;
+    if (vpt > 8 || !lookup_phase2(dt == ATTNRES_BF16 ? 1 : 0, vpt, upd, H > 1, &kr)) return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    attnres_status_t st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    int occ = 0;
+    st = prepare_kernel(kr.fn, 0, P2_THREADS, &occ);
+    if (st != ATTNRES_OK) return st;
+    MergeArgs a;
+    a.o = static_cast<const unsigned char *>(o);
+    a.lse = lse;
+    a.partial = static_cast<const unsigned char *>(partial);
+    a.f = static_cast<const unsigned char *>(f);
+    a.partial_out = static_cast<unsigned char *>(partial_out);
+    a.T = T;
+    a.d = (int)d;
+    a.nvec = nvec;
+    a.seg = seg;
+    a.query = query;
+    a.gain = gain;
+    a.eps = eps;
+    a.out = static_cast<unsigned char *>(out);
+    a.tpr = tpr;
+    a.tt = P2_THREADS / tpr;
+    a.ntiles = (T + a.tt - 1) / a.tt;
+    const int64_t max_grid = (int64_t)dev->sms * occ;
+    const int grid = (int)(a.ntiles < max_grid ? a.ntiles : max_grid);
+    void *args[] = {&a};
+    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(P2_THREADS), args, 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "phase2 launch");
+    return ATTNRES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -369,59 +456,21 @@ attnres_status_t attnres_block_phase2_merge(const void *o, const float *lse, con
                                             int64_t T, int64_t d, attnres_dtype_t dt,
                                             const float *query, const float *gain, float eps,
                                             void *out, void *stream) {
-    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
-    if (T < 0 || d < 1 || !(eps >= 0.f) || std::isinf(eps)) return ATTNRES_ERR_INVALID_ARG;
-    if (T > 0 && (!o || !out)) return ATTNRES_ERR_INVALID_ARG;
-    if (T > 0 && partial && (!lse || !query)) return ATTNRES_ERR_INVALID_ARG;
-    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
-    const size_t es = esize(dt);
-    const size_t nbytes = (size_t)T * (size_t)d * es;
-    if (out != o && overlap(out, nbytes, o, nbytes)) return ATTNRES_ERR_INVALID_ARG;
-    if (partial && overlap(out, nbytes, partial, nbytes)) return ATTNRES_ERR_INVALID_ARG;
-    if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
-    if (!aligned16(o) || !aligned16(out) || (partial && !aligned16(partial)) ||
-        (query && !aligned16(query)) || (gain && !aligned16(gain)) || (lse && !aligned4(lse)))
-        return ATTNRES_ERR_UNSUPPORTED;
-    if (T == 0) return ATTNRES_OK;
-    if (!partial) {
-        if (out == o) return ATTNRES_OK;
-        cudaError_t e = cudaMemcpyAsync(out, o, nbytes, cudaMemcpyDeviceToDevice,
-                                        static_cast<cudaStream_t>(stream));
-        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemcpyAsync");
-    }
-    const int EPV = epv(dt);
-    const int nvec = (int)(d / EPV);
-    int tpr, vpt;
-    row_shape(nvec, &tpr, &vpt);
-    KernelRef kr;
-    if (vpt > 8 || !lookup_phase2(dt == ATTNRES_BF16 ? 1 : 0, vpt, &kr)) return ATTNRES_ERR_UNSUPPORTED;
-    DeviceInfo *dev = nullptr;
-    attnres_status_t st = device_info(&dev);
-    if (st != ATTNRES_OK) return st;
-    int occ = 0;
-    st = prepare_kernel(kr.fn, 0, P2_THREADS, &occ);
-    if (st != ATTNRES_OK) return st;
-    MergeArgs a;
-    a.o = static_cast<const unsigned char *>(o);
-    a.lse = lse;
-    a.partial = static_cast<const unsigned char *>(partial);
-    a.T = T;
-    a.d = (int)d;
-    a.nvec = nvec;
-    a.query = query;
-    a.gain = gain;
-    a.eps = eps;
-    a.out = static_cast<unsigned char *>(out);
-    a.tpr = tpr;
-    a.tt = P2_THREADS / tpr;
-    a.ntiles = (T + a.tt - 1) / a.tt;
-    const int64_t max_grid = (int64_t)dev->sms * occ;
-    const int grid = (int)(a.ntiles < max_grid ? a.ntiles : max_grid);
-    void *args[] = {&a};
-    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(P2_THREADS), args, 0,
-                                     static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "phase2 launch");
-    return ATTNRES_OK;
+    return launch_phase2(o, lse, partial, nullptr, nullptr, false, T, d, 1, dt, query, gain, eps, out, stream);
+}
+
+attnres_status_t attnres_block_phase2_update_merge(const void *partial, const void *f, void *partial_out,
+                                                   const void *o, const float *lse, int64_t T, int64_t d,
+                                                   attnres_dtype_t dt, const float *query, const float *gain,
+                                                   float eps, void *out, void *stream) {
+    return launch_phase2(o, lse, partial, f, partial_out, true, T, d, 1, dt, query, gain, eps, out, stream);
+}
+
+attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *partial, const void *f,
+                                   void *partial_out, int64_t T, int64_t d, int64_t H, attnres_dtype_t dt,
+                                   const float *query, const float *gain, float eps, void *out, void *stream) {
+    return launch_phase2(o, lse, partial, f, partial_out, f != nullptr, T, d, H, dt, query, gain, eps, out,
+                         stream);
 }
 
 attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,

@@ -27,7 +27,8 @@ bool lookup_depth_read_mma2(int nq, int ks, int nw, KernelRef *out);
 // depth_read_mma_multi_kernel<nq, ks, nw>: > 8 sources in chunks of 8 (online softmax)
 bool lookup_depth_read_mma_multi(int nq, int ks, int nw, KernelRef *out);
 
-// phase2_merge_kernel<T, vpt>
-bool lookup_phase2(int dt, int vpt, KernelRef *out);
+// phase2_merge_kernel<T, vpt, upd, mh>: upd = fused partial-sum update, mh = per-head merge
+bool lookup_phase2(int dt, int vpt, bool upd, bool mh, KernelRef *out);
+bool lookup_phase2_mh(int dt, int vpt, bool upd, KernelRef *out);
 
 }  // namespace attnres

@@ -124,6 +124,38 @@ attnres_status_t attnres_block_phase2_merge(const void *o, const float *lse,
                                             void *stream);
 
 /*
+ * Block AttnRes, phase 2 fused with the intra-block partial-sum update: the
+ * previous layer's output f joins the block's current partial sum, and the
+ * next layer's merge scores the updated partial, in one pass (the partial is
+ * read once instead of once by an update and again by the merge).
+ * Defined by: b-lab.team summary, section 2 (the source of layer i >= 2 is
+ * the partial sum b^{(n)}_{i-1} of the block's outputs so far) and section 3
+ * (Phase 2, whose kernel fusion cuts I/O); ai-systems-engineering.com
+ * tutorial, Fig. 4 (after a layer's output is produced only the current
+ * partial sum changes, to the old partial plus that output).
+ *   partial_out = partial + f       (partial NULL: partial_out = f),
+ *   out = phase-2 merge of (o, lse) with partial_out, as
+ *         attnres_block_phase2_merge.
+ * The merge scores and mixes partial + f in fp32 (the exact sum of the two
+ * stored inputs up to fp32 rounding); partial_out receives that sum rounded
+ * once to dt, the value later layers and the next block read.
+ *   partial      [T][d] dtype dt or NULL (the block's first output)
+ *   f            [T][d] dtype dt, the previous layer's output
+ *   partial_out  [T][d] dtype dt; may be partial or f itself, must not
+ *                otherwise overlap them, o, out or lse
+ *   o, lse       the next layer's phase-1 state ([T][d] dtype dt, [T] float)
+ *   query        [d] float, the next layer's pseudo-query
+ *   out          [T][d] dtype dt; may be o itself, must not overlap partial,
+ *                f or partial_out
+ */
+attnres_status_t attnres_block_phase2_update_merge(const void *partial, const void *f,
+                                                   void *partial_out, const void *o,
+                                                   const float *lse, int64_t T, int64_t d,
+                                                   attnres_dtype_t dt, const float *query,
+                                                   const float *gain, float eps, void *out,
+                                                   void *stream);
+
+/*
  * MHAR, the multi-head block-diagonal read: the pseudo-query is reshaped into
  * H heads of d/H channels; each head has its own softmax over depth and mixes
  * only its own channel slice.  H = 1 is exactly attnres_block_phase1 (the same
@@ -141,6 +173,35 @@ attnres_status_t mhar_fwd(const void *src, int64_t n_src, int64_t src_stride, in
                           int64_t d, int64_t H, attnres_dtype_t dt, const float *queries,
                           int64_t n_q, const float *gain, float eps, void *out, float *lse,
                           void *stream);
+
+/*
+ * MHAR inside the two-phase Block schedule, phase 2: mhar_fwd over the cached
+ * block representations is phase 1 (its lse [n_q][H][T] keeps the state per
+ * head); this folds one layer's partial sum into it head by head: head h
+ * scores its slice of the partial with its slice of the query, the gain and
+ * the RMSNorm, and merges only its own channels,
+ *   s_h = w_h . RMSNorm_h(p_h),  M = max(lse_h, s_h),
+ *   out_h = (e^{lse_h-M} o_h + e^{s_h-M} p_h) / (e^{lse_h-M} + e^{s_h-M}).
+ * H = 1 is attnres_block_phase2_merge.  With f non-NULL the partial is first
+ * updated as in attnres_block_phase2_update_merge (partial_out = partial + f)
+ * and the merge scores the update.
+ * Defined by: chatpaper.ai "Multi-Head Attention Residuals" abstract (per-head
+ * softmax, block-diagonal read) with the b-lab.team summary, section 3
+ * (Phase 2 merge).
+ *   o        [T][d] dtype dt (one query's slice of the MHAR output)
+ *   lse      [H][T] float (the matching slice of the MHAR lse)
+ *   partial  [T][d] dtype dt or NULL (no update: out = o; update: p = 0)
+ *   f, partial_out  NULL, or as attnres_block_phase2_update_merge
+ *   query    [H][d/H] float
+ *   out      [T][d] dtype dt; may be o itself
+ * Limits (H > 1): a head is a whole number of 16-byte vectors (d/H a multiple
+ * of 8 bf16 or 4 f32 channels), and the vectors per head are a multiple of 32
+ * or a power of two below 32.
+ */
+attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *partial,
+                                   const void *f, void *partial_out, int64_t T, int64_t d,
+                                   int64_t H, attnres_dtype_t dt, const float *query,
+                                   const float *gain, float eps, void *out, void *stream);
 
 /*
  * MSAR, the fused multi-stream depth read for one target layer: every source

@@ -105,6 +105,40 @@ def test_phase2_validation(lib):
     assert m(p=B + 0x100004) == UNS
 
 
+def test_phase2_update_and_mhar_phase2_validation(lib):
+    P, F, PO, O, L, Q, OUT = A, A + 0x100000, A + 0x200000, B, B + 0x100000, B + 0x200000, B + 0x300000
+
+    def up(p=P, f=F, po=PO, o=O, lse=L, T=16, d=64, q=Q, out=OUT, eps=1e-6):
+        return lib.attnres_block_phase2_update_merge(p, f, po, o, lse, T, d, BF16, q, None, eps, out, None)
+    assert up(T=0) == OK
+    assert up(f=None) == INV                          # the update needs f
+    assert up(po=None) == INV                         # ... and somewhere to put p + f
+    assert up(lse=None) == INV
+    assert up(q=None) == INV
+    assert up(po=P, T=0) == OK                        # update in place of the partial
+    assert up(po=F, T=0) == OK                        # ... or of f
+    assert up(po=P + 16) == INV                       # partially overlapping the partial
+    assert up(po=O) == INV                            # the updated partial may not overlap o
+    assert up(out=F) == INV                           # out may not overlap f
+    assert up(out=PO + 16) == INV                     # ... or the updated partial
+    assert up(out=O, T=0) == OK                       # merge in place of o
+    assert up(f=F + 8) == UNS                         # misaligned f
+    assert up(d=12) == UNS
+
+    def mh(H=8, d=4096, T=16, p=P, f=None, po=None, lse=L):
+        return lib.mhar_phase2_merge(O, lse, p, f, po, T, d, H, BF16, Q, None, 1e-6, OUT, None)
+    assert mh(T=0) == OK
+    assert mh(H=3, T=0) == INV                        # H must divide d
+    assert mh(H=0, T=0) == INV
+    assert mh(lse=None) == INV
+    assert mh(f=F, po=None) == INV                    # an update needs partial_out
+    assert mh(H=1, T=0) == OK
+    assert mh(H=8, d=4096, T=0) == OK                 # 64 vectors per head
+    assert mh(H=16, d=2048, T=0) == OK                # 16 vectors per head (inside a warp)
+    assert mh(H=6, d=6 * 40, T=0) == UNS              # 5 vectors per head
+    assert mh(H=3, d=3 * 384, T=0) == UNS             # 48 vectors per head
+
+
 def test_msar_validation(lib):
     ks = (ctypes.c_int32 * 3)(4, 8, 12)
     bad = (ctypes.c_int32 * 3)(4, 0, 12)

@@ -166,6 +166,76 @@ def test_block_phase2_in_place_and_without_partial():
     assert torch.equal(out, od)
 
 
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("T,d", [(1, 64), (99, 2048), (64, 4096), (10, 808), (700, 256)])
+@pytest.mark.parametrize("with_old", [True, False])
+def test_block_phase2_update_merge(dtype, T, d, with_old):
+    """The fused partial-sum update and merge: p' = p + f (rounded to the
+    storage type) and the next layer's merge of p'."""
+    rng = _rng(T + d + with_old)
+    o = _sources(rng, 1, T, d, dtype)[0]
+    p = _sources(rng, 1, T, d, dtype)[0] if with_old else None
+    f = _sources(rng, 1, T, d, dtype, step=0)[0]
+    lse = (rng.standard_normal(T) * 4).astype(np.float32)
+    q = _queries(rng, 1, d)[0]
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    pd = to_dev(p, dtype) if with_old else None
+    p_new, out = attnres.attnres_block_phase2_update_merge(pd, to_dev(f, dtype), to_dev(o, dtype),
+                                                           to_dev(lse, F32), to_dev(q, F32), to_dev(g, F32),
+                                                           1e-6)
+    ref_p, ref = oracle.block_phase2_update(p, f, o, lse, q, g, 1e-6)
+    check_out(p_new, ref_p, dtype, np.abs(ref_p).max(), what="partial")
+    check_out(out, ref, dtype, max(np.abs(o).max(), np.abs(ref_p).max()))
+
+
+def test_block_phase2_update_merge_in_place():
+    rng = _rng(31)
+    T, d = 300, 4096
+    o = _sources(rng, 1, T, d, BF16)[0]
+    p = _sources(rng, 1, T, d, BF16)[0]
+    f = _sources(rng, 1, T, d, BF16)[0]
+    lse = (rng.standard_normal(T) * 4).astype(np.float32)
+    q = _queries(rng, 1, d)[0]
+    ref_p, ref = oracle.block_phase2_update(p, f, o, lse, q)
+    for target in ("partial", "f"):
+        od, pd, fd = to_dev(o, BF16), to_dev(p, BF16), to_dev(f, BF16)
+        po = pd if target == "partial" else fd
+        attnres.attnres_block_phase2_update_merge(pd, fd, od, to_dev(lse, F32), to_dev(q, F32),
+                                                  partial_out=po, out=od)
+        check_out(po, ref_p, BF16, what="partial")
+        check_out(od, ref, BF16)
+
+
+@pytest.mark.parametrize("T,d,N,S", [(150, 2048, 8, 4), (40, 4096, 8, 4), (33, 512, 3, 6)])
+def test_block_chain_with_fused_updates_matches_oneshot(T, d, N, S):
+    """A whole block on the GPU: phase 1, then each layer i >= 2 updates the
+    partial with the previous layer's output and merges it in one call; every
+    layer's input equals the one-shot Block read with the cumulative partials,
+    and the last partial is the block's sum of outputs."""
+    rng = _rng(T * 3 + d + N + S)
+    cache = _sources(rng, N, T, d, BF16)
+    f = _sources(rng, S, T, d, BF16, step=0)
+    q = _queries(rng, S, d)
+    qd = to_dev(q, F32)
+    o, lse = attnres.attnres_block_phase1(to_dev(cache, BF16), qd)
+    fd = to_dev(f, BF16)
+    p = None
+    p_stored = np.zeros((T, d))                   # the partial as stored (bf16)
+    outs = [to_host(o[0])]
+    partials = np.zeros((S, T, d))
+    for i in range(1, S):
+        p, out = attnres.attnres_block_phase2_update_merge(p, fd[i - 1], o[i], lse[i], qd[i])
+        # layer i merges the stored partial plus f_{i-1}, summed exactly; the
+        # stored partial is that sum rounded to bf16
+        partials[i] = p_stored + f[i - 1]
+        p_stored = inputs.bf16_round(partials[i].astype(np.float32)).astype(np.float64)
+        outs.append(to_host(out))
+    ref = oracle.block_oneshot(cache, partials, q, None, 1e-6)
+    for i in range(S):
+        check_out(outs[i], ref[i], BF16, what=f"layer {i + 1}")
+    check_out(p, p_stored, BF16, what="partial")
+
+
 @pytest.mark.parametrize("T,d,N,S", [(150, 2048, 8, 4), (40, 4096, 8, 4), (33, 512, 3, 6)])
 def test_two_phase_block_matches_oneshot(T, d, N, S):
     """GPU two-phase schedule (phase 1 + S-1 merges) vs the oracle's
@@ -210,6 +280,56 @@ def test_mhar_many_sources():
     q = (rng.standard_normal((4, H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
     out = attnres.mhar_fwd(to_dev(src, BF16), to_dev(q, F32))
     check_out(out, oracle.mhar(src, q), BF16)
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("H,d,T", [(8, 4096, 40), (16, 2048, 33), (4, 1024, 70), (2, 512, 9), (8, 512, 21),
+                                   (1, 2048, 17)])
+def test_mhar_phase2_merge(dtype, H, d, T):
+    """MHAR phase 2: per-head merge of the partial into the per-head phase-1
+    state (heads of whole warps, of a power-of-two group inside a warp, H = 1)."""
+    rng = _rng(H * 7 + d + T)
+    o = _sources(rng, 1, T, d, dtype)[0]
+    p = _sources(rng, 1, T, d, dtype)[0]
+    lse = (rng.standard_normal((H, T)) * 4).astype(np.float32)
+    q = (rng.standard_normal((H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    out = attnres.mhar_phase2_merge(to_dev(o, dtype), to_dev(lse, F32), to_dev(p, dtype), to_dev(q, F32),
+                                    to_dev(g, F32), 1e-6)
+    check_out(out, oracle.mhar_phase2(o, lse, p, q, g, 1e-6), dtype, max(np.abs(o).max(), np.abs(p).max()))
+
+
+def test_mhar_two_phase_matches_oneshot_and_fused_update():
+    """MHAR inside the two-phase schedule on the GPU: mhar_fwd over the cached
+    reps (phase 1, lse per head), then the per-head merge of a partial equals the
+    one-shot MHAR read over the reps plus the partial; with f the partial is
+    updated first."""
+    rng = _rng(41)
+    H, d, T, N = 8, 4096, 90, 8
+    cache = _sources(rng, N, T, d, BF16)
+    p = _sources(rng, 1, T, d, BF16)[0]
+    f = _sources(rng, 1, T, d, BF16, step=0)[0]
+    q = (rng.standard_normal((1, H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
+    qd = to_dev(q, F32)
+    o, lse = attnres.mhar_fwd(to_dev(cache, BF16), qd, want_lse=True)
+    out = attnres.mhar_phase2_merge(o[0], lse[0], to_dev(p, BF16), qd[0])
+    check_out(out, oracle.mhar(np.concatenate([cache, p[None]]), q)[0], BF16)
+    p_new, out2 = attnres.mhar_phase2_merge(o[0], lse[0], to_dev(p, BF16), qd[0], f=to_dev(f, BF16))
+    pf = p.astype(np.float64) + f
+    check_out(p_new, pf, BF16, what="partial")
+    check_out(out2, oracle.mhar(np.concatenate([cache, pf[None]]), q)[0], BF16)
+
+
+def test_mhar_phase2_one_head_equals_block_phase2_bitwise():
+    rng = _rng(42)
+    T, d = 77, 4096
+    o = to_dev(_sources(rng, 1, T, d, BF16)[0], BF16)
+    p = to_dev(_sources(rng, 1, T, d, BF16)[0], BF16)
+    lse = to_dev((rng.standard_normal(T) * 4).astype(np.float32), F32)
+    q = to_dev(_queries(rng, 1, d)[0], F32)
+    a = attnres.attnres_block_phase2_merge(o, lse, p, q)
+    b = attnres.mhar_phase2_merge(o, lse.view(1, T), p, q.view(1, d))
+    assert torch.equal(a, b)
 
 
 def test_mhar_one_head_is_phase1_bitwise():
