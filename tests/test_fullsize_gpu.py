@@ -85,6 +85,32 @@ def test_block_two_phase_T32768_d4096_bench_workload():
     check_lse(lse_ph1, oracle.block_phase1(c, qh)[1])
 
 
+def test_block_fused_update_T32768_d4096_bench_workload():
+    """The bench's fused schedule: phase 1, then layers 2..4 each add the
+    previous layer's output to the partial and merge it in one call.  Layer i
+    merges the stored partial plus f_{i-1} summed exactly; the stored partial is
+    that sum rounded to bf16."""
+    T, d, N, S = 32768, 4096, 8, 4
+    cache, q, f = _device_block(T, d, N, S)
+    o = torch.empty((S, T, d), dtype=BF16, device="cuda")
+    lse = torch.empty((S, T), dtype=F32, device="cuda")
+    p = torch.empty((T, d), dtype=BF16, device="cuda")
+    attnres.attnres_block_phase1(cache, q, o=o, lse=lse)
+    idx = sampled_tokens(T)
+    c, fh = rows(cache, idx), rows(f, idx)
+    stored = np.zeros_like(fh[0])
+    partials = np.zeros_like(fh)
+    for i in range(1, S):
+        attnres.attnres_block_phase2_update_merge(p if i > 1 else None, f[i - 1], o[i], lse[i], q[i],
+                                                  partial_out=p, out=o[i])
+        partials[i] = stored + fh[i - 1]
+        stored = inputs.bf16_round(partials[i].astype(np.float32)).astype(np.float64)
+    attnres.attnres_sync_status()
+    qh = q.cpu().numpy().astype(np.float64)
+    check_out(rows(o, idx), oracle.block_oneshot(c, partials, qh), BF16)
+    check_out(rows(p, idx), stored, BF16, what="partial")
+
+
 def test_full_at_depth_T16384_d4096_L64():
     """Layer l = 1..64 reads sources 0..l-1, one call per layer in order."""
     T, d, L = 16384, 4096, 64
@@ -97,7 +123,7 @@ def test_full_at_depth_T16384_d4096_L64():
     q_h = q.cpu().numpy().astype(np.float64)
     for l in range(1, L + 1):
         attnres.attnres_full_fwd(src[:l], q[l - 1], None, 1e-6, out=out)
-        if l in (1, 2, 7, 8, 9, 16, 17, 33, 63, 64):
+        if l in (1, 2, 7, 8, 9, 16, 17, 24, 29, 33, 45, 63, 64):
             check_out(rows(out, idx), oracle.full(s_h[:l], q_h[l - 1]), BF16, what=f"layer {l}")
     attnres.attnres_sync_status()
 
@@ -118,6 +144,28 @@ def test_mhar_T131072_d4096_H8():
     m1 = attnres.mhar_fwd(src, q1)
     o1, _ = attnres.attnres_block_phase1(src, q1.view(S, d), want_lse=False)
     assert torch.equal(m1, o1)
+
+
+def test_mhar_two_phase_T131072_d4096_H8():
+    """MHAR inside the two-phase schedule at the MHAR size: mhar_fwd (phase 1,
+    lse per head) and the per-head merge of a partial per query equal the
+    one-shot MHAR read over the reps plus the partial."""
+    T, d, N, S, H = 131072, 4096, 8, 4, 8
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((S, H, d // H), (16.0 / (d // H)) ** 0.5, g)
+    part = torch.randn((T, d), generator=g, device="cuda").to(BF16)
+    out, lse = attnres.mhar_fwd(src, q, want_lse=True)
+    for i in range(1, S):
+        attnres.mhar_phase2_merge(out[i], lse[i], part, q[i], out=out[i])
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T)
+    s_h, p_h = rows(src, idx), rows(part, idx)
+    q_h = q.cpu().numpy().astype(np.float64)
+    got = rows(out, idx)
+    check_out(got[0], oracle.mhar(s_h, q_h[:1])[0], BF16, what="layer 1")
+    ref = oracle.mhar(np.concatenate([s_h, p_h[None]]), q_h[1:])
+    check_out(got[1:], ref, BF16)
 
 
 def test_msar_T32768_d4096():
