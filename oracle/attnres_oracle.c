@@ -247,6 +247,110 @@ int oracle_block_phase2_update(const double *p, const double *f, const double *o
 }
 
 /* ---------------------------------------------------------------------- */
+/* Backward of the read                                                     */
+/* ---------------------------------------------------------------------- */
+
+/* Gradients of the depth read of n_q queries over n_src sources (Full
+ * AttnRes: n_q = 1; a Block layer: its sources [b_0..b_{n-1}, partial]; Block
+ * phase 1: the block's S queries) for a loss whose gradient with respect to
+ * every output h_q[t] is dout[q][t] (the backward of [Summary §1]; the
+ * forward is read_one, so alpha is recomputed from the sources).  The chain
+ * rule is taken step by step, per token:
+ *   forward  r_i = sqrt(mean(v_i^2) + eps),  k_i = g * v_i / r_i,
+ *            s_qi = w_q . k_i,  alpha_q = softmax_i(s_q),  h_q = sum_i alpha_qi v_i
+ *   dalpha_qi = dout_q . v_i
+ *   ds_qi     = alpha_qi (dalpha_qi - sum_j alpha_qj dalpha_qj)      (softmax)
+ *   dv_i     += sum_q alpha_qi dout_q                               (value path)
+ *   dk_i      = sum_q ds_qi w_q;   dw_q += sum_i ds_qi k_i
+ *   dg[c]    += sum_i dk_i[c] v_i[c] / r_i
+ *   dv_i[c]  += g[c] dk_i[c] / r_i - v_i[c] (sum_c' g[c'] dk_i[c'] v_i[c']) / (d r_i^3)
+ * (the last line is the derivative of g * v / r; a zero source with eps = 0
+ * has k = 0 and passes nothing back through its score).
+ * src, dsrc [n_src][T][d]; queries, dq [n_q][d]; dout [n_q][T][d]; dg [d]
+ * (the gain's gradient even when gain is NULL, i.e. 1); dq and dg are sums
+ * over the tokens. */
+int oracle_read_bwd(const double *src, int64_t n_src, int64_t T, int64_t d,
+                    const double *queries, int64_t n_q, const double *gain, double eps,
+                    const double *dout, double *dsrc, double *dq, double *dg)
+{
+    if (!src || !queries || !dout || !dsrc || !dq || !dg || n_src < 1 || n_q < 1 || T < 0 || d < 1 ||
+        eps < 0)
+        return -1;
+    double *r = (double *)malloc(sizeof(double) * (size_t)n_src);
+    double *k = (double *)malloc(sizeof(double) * (size_t)(n_src * d));
+    double *s = (double *)malloc(sizeof(double) * (size_t)n_src);
+    double *a = (double *)malloc(sizeof(double) * (size_t)(n_q * n_src));
+    double *ds = (double *)malloc(sizeof(double) * (size_t)(n_q * n_src));
+    double *dk = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!r || !k || !s || !a || !ds || !dk) {
+        free(r); free(k); free(s); free(a); free(ds); free(dk);
+        return -1;
+    }
+    for (int64_t i = 0; i < n_src * T * d; ++i) dsrc[i] = 0.0;
+    for (int64_t i = 0; i < n_q * d; ++i) dq[i] = 0.0;
+    for (int64_t c = 0; c < d; ++c) dg[c] = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        /* forward: normalised keys, scores, weights */
+        for (int64_t i = 0; i < n_src; ++i) {
+            const double *v = src + (i * T + t) * d;
+            double ms = 0.0;
+            for (int64_t c = 0; c < d; ++c) ms += v[c] * v[c];
+            r[i] = sqrt(ms / (double)d + eps);
+            for (int64_t c = 0; c < d; ++c)
+                k[i * d + c] = r[i] > 0.0 ? (gain ? gain[c] : 1.0) * v[c] / r[i] : 0.0;
+        }
+        for (int64_t q = 0; q < n_q; ++q) {
+            for (int64_t i = 0; i < n_src; ++i) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc += queries[q * d + c] * k[i * d + c];
+                s[i] = acc;
+            }
+            softmax(s, n_src, a + q * n_src);
+            /* softmax backward */
+            const double *dh = dout + (q * T + t) * d;
+            double mean = 0.0;
+            for (int64_t i = 0; i < n_src; ++i) {
+                const double *v = src + (i * T + t) * d;
+                double dal = 0.0;
+                for (int64_t c = 0; c < d; ++c) dal += dh[c] * v[c];
+                ds[q * n_src + i] = dal;                     /* dalpha, for now */
+                mean += a[q * n_src + i] * dal;
+            }
+            for (int64_t i = 0; i < n_src; ++i)
+                ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] - mean);
+            /* value path and the query's gradient */
+            for (int64_t i = 0; i < n_src; ++i) {
+                double *dv = dsrc + (i * T + t) * d;
+                for (int64_t c = 0; c < d; ++c) {
+                    dv[c] += a[q * n_src + i] * dh[c];
+                    dq[q * d + c] += ds[q * n_src + i] * k[i * d + c];
+                }
+            }
+        }
+        /* score path through the normalised key of every source */
+        for (int64_t i = 0; i < n_src; ++i) {
+            if (r[i] <= 0.0) continue;
+            const double *v = src + (i * T + t) * d;
+            double *dv = dsrc + (i * T + t) * d;
+            for (int64_t c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int64_t q = 0; q < n_q; ++q) acc += ds[q * n_src + i] * queries[q * d + c];
+                dk[c] = acc;
+            }
+            double gdkv = 0.0;
+            for (int64_t c = 0; c < d; ++c) gdkv += (gain ? gain[c] : 1.0) * dk[c] * v[c];
+            for (int64_t c = 0; c < d; ++c) {
+                const double gc = gain ? gain[c] : 1.0;
+                dg[c] += dk[c] * v[c] / r[i];
+                dv[c] += gc * dk[c] / r[i] - v[c] * gdkv / ((double)d * r[i] * r[i] * r[i]);
+            }
+        }
+    }
+    free(r); free(k); free(s); free(a); free(ds); free(dk);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* MHAR                                                                    */
 /* ---------------------------------------------------------------------- */
 

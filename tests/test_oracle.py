@@ -302,6 +302,69 @@ def test_fused_update_without_old_partial_starts_the_sum():
     assert np.allclose(out, oracle.block_phase2(o, lse, f, q, eps=1e-6), atol=0, rtol=0)
 
 
+def _fd_grads(src, q, g, dout, eps, h=1e-6):
+    """Central finite differences of L = sum(dout * h_out) through the forward
+    oracle (Block phase 1 reads every query against every source)."""
+    def loss(s_, q_, g_):
+        o, _ = oracle.block_phase1(s_, q_, g_, eps)
+        return float((o * dout).sum())
+    out = []
+    for x, put in ((src, lambda v: (v, q, g)), (q, lambda v: (src, v, g)), (g, lambda v: (src, q, v))):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            a, b = x.copy(), x.copy()
+            a[idx] += h
+            b[idx] -= h
+            fd[idx] = (loss(*put(a)) - loss(*put(b))) / (2 * h)
+        out.append(fd)
+    return out
+
+
+@pytest.mark.parametrize("n_src,n_q,eps,with_gain", [(3, 1, 1e-6, False), (5, 3, 1e-6, True), (2, 2, 0.1, True),
+                                                     (4, 1, 0.0, True)])
+def test_read_bwd_matches_finite_differences(n_src, n_q, eps, with_gain):
+    """The backward of the read against central differences of the (pinned)
+    forward oracle, for the sources, the queries and the gain."""
+    rng = np.random.default_rng(31 + n_src * 3 + n_q)
+    T, d = 2, 8
+    src = _rand(rng, n_src, T, d) * (1 + np.arange(n_src))[:, None, None]
+    q = _rand(rng, n_q, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d) if with_gain else np.ones(d)
+    dout = _rand(rng, n_q, T, d)
+    dsrc, dq, dg = oracle.read_bwd(src, q, dout, g if with_gain else None, eps)
+    fs, fq, fg = _fd_grads(src, q, g, dout, eps)
+    for got, ref in ((dsrc, fs), (dq, fq), (dg, fg)):
+        assert np.abs(got - ref).max() <= 1e-6 * max(1.0, np.abs(ref).max())
+
+
+def test_read_bwd_single_source_passes_the_gradient_straight_through():
+    """One source: alpha = 1 whatever the score, so the source gets the sum of
+    the output gradients and the query and the gain get nothing."""
+    rng = np.random.default_rng(32)
+    src = _rand(rng, 1, 4, 16)
+    q, dout = _rand(rng, 3, 16), _rand(rng, 3, 4, 16)
+    dsrc, dq, dg = oracle.read_bwd(src, q, dout, rng.uniform(0.5, 1.5, 16), 1e-6)
+    assert np.allclose(dsrc[0], dout.sum(axis=0), atol=1e-14)
+    assert np.abs(dq).max() == 0.0 and np.abs(dg).max() == 0.0
+
+
+def test_read_bwd_score_path_is_orthogonal_to_the_source_at_zero_eps():
+    """At eps = 0 a score does not change when its source is scaled, so the
+    score path's gradient of source i (its gradient minus the value path's
+    sum_q alpha_qi dout_q) is orthogonal to v_i."""
+    rng = np.random.default_rng(33)
+    n_src, T, d = 4, 3, 12
+    src = _rand(rng, n_src, T, d) * (1 + np.arange(n_src))[:, None, None]
+    q, dout = _rand(rng, 2, d, scale=2.0), _rand(rng, 2, T, d)
+    dsrc, _, _ = oracle.read_bwd(src, q, dout, None, 0.0)
+    _, alpha = oracle.full(src, q[0], None, eps=0.0, want_alpha=True)
+    _, alpha1 = oracle.full(src, q[1], None, eps=0.0, want_alpha=True)
+    value = (alpha.T[:, :, None] * dout[0][None]) + (alpha1.T[:, :, None] * dout[1][None])
+    score_part = dsrc - value
+    assert np.abs((score_part * src).sum(axis=2)).max() < 1e-12
+    assert np.abs(score_part).max() > 1e-3
+
+
 # --------------------------------------------------------------------------
 # MHAR
 # --------------------------------------------------------------------------

@@ -27,6 +27,11 @@ MUTANTS = {
     "mhar_phase2_merge_sign": [("double a = exp(l - M), b = exp(sp - M);", "double a = exp(l - M), b = exp(M - sp);")],
     "first_layer_reads_partial": [("if (li >= 1) { rows[N]", "if (li >= 0) { rows[N]")],
     "mhar_query_transposed": [("queries + (q * H + hd) * dh", "queries + (hd * n_q + q) * dh")],
+    "bwd_softmax_mean_dropped": [("ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] - mean);",
+                                  "ds[q * n_src + i] = a[q * n_src + i] * ds[q * n_src + i];")],
+    "bwd_rms_term_sign": [("dv[c] += gc * dk[c] / r[i] - v[c] * gdkv", "dv[c] += gc * dk[c] / r[i] + v[c] * gdkv")],
+    "bwd_gain_grad_not_normalised": [("dg[c] += dk[c] * v[c] / r[i];", "dg[c] += dk[c] * v[c];")],
+    "bwd_value_path_first_query_weights": [("dv[c] += a[q * n_src + i] * dh[c];", "dv[c] += a[i] * dh[c];")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
