@@ -10,7 +10,7 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|msar|full_depth|
-block_d2048|block_fused) are for profiling and the design notes.
+block_d2048|block_fused|read_bwd) are for profiling and the design notes.
 """
 from __future__ import annotations
 
@@ -40,6 +40,7 @@ KERNEL_SOURCES = {
     "depth_read": [CSRC + "depth_read.cuh", CSRC + "common.cuh"],
     "phase2": [CSRC + "phase2.cuh", CSRC + "common.cuh", CSRC + "kernels_phase2.cu"],
     "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
+    "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
 }
 
 
@@ -290,6 +291,85 @@ def torch_pinned_like(t):
     return h
 
 
+class ReadBwdWorkload(BlockWorkload):
+    """Backward of one Block layer's read in training: the layer's query over
+    its 9 sources (the N=8 block reps and the partial sum), bf16, d=4096: the
+    sources', the query's and the gain's gradients for a given output
+    gradient.  Sources as the Block workload; output gradient ~ N(0, 1)."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0):
+        super().__init__(T, d, N, 4, seed, name="attnres_read_backward")
+        b = 2
+        n_src = N + 1
+        # read the sources and the output gradient, write the sources' gradients
+        self.bytes_per_token = (2 * n_src + 1) * d * b
+        self.phase1_bytes_per_token = self.bytes_per_token
+        self.launches_per_step = 2            # streaming kernel + the workspace reduction
+        self.dominant = "read_bwd_kernel"
+        self.dominant_src = "read_bwd"
+        self.profile_tag = f"ncu_read_bwd_d{d}"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} n_src={self.N + 1} n_q=1 T={self.T}"
+        c.pop("S", None)
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres, inputs
+        T, d, N = self.T, self.d, self.N
+        self.src, g = inputs.device_sources(N + 1, T, d, lambda n: 1.0 + n / 2.0 if n < N else 1.0,
+                                            seed=self.seed, device=device)
+        self.src = self.src.view(N + 1, T, d)
+        self.queries = inputs.device_normal((1, d), (16.0 / d) ** 0.5, g, device=device)
+        self.gain = torch.ones((d,), dtype=torch.float32, device=device)
+        self.dout = torch.randn((1, T, d), generator=g, device=device).to(torch.bfloat16)
+        self.dsrc = torch.empty_like(self.src)
+        self.dq = torch.empty((1, d), dtype=torch.float32, device=device)
+        self.dg = torch.empty((d,), dtype=torch.float32, device=device)
+        nb = attnres.attnres_read_bwd_workspace_size(N + 1, T, d, 1, torch.bfloat16)
+        self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+        self.cache = self.src                   # for oracle_sample
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.attnres_read_bwd(self.src, self.queries, self.dout, self.gain, 1e-6, dsrc=self.dsrc,
+                                 dqueries=self.dq, dgain=self.dg, workspace=self.ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def setup_host(self):
+        self.h_src = torch_pinned_like(self.src)
+        self.h_dout = torch_pinned_like(self.dout)
+        self.h_out = torch_pinned_like(self.dsrc)
+        self.h2d = (self.h_src.numel() + self.h_dout.numel()) * 2
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.src.copy_(self.h_src, non_blocking=True)
+        self.dout.copy_(self.h_dout, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.dsrc, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        import torch
+        it = torch.from_numpy(idx).to(self.src.device)
+        src = self.src[:, it, :].float().cpu().numpy().astype(np.float64)
+        dout = self.dout[:, it, :].float().cpu().numpy().astype(np.float64)
+        return src, self.queries.cpu().numpy().astype(np.float64), dout
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        src, q, dout = sample
+        oracle.read_bwd(src, q, dout, None, 1e-6)
+        return src.shape[1]
+
+
 class MharWorkload(BlockWorkload):
     """MHAR read: S=4 queries x H=8 heads over N=8 block reps (no phase 2)."""
 
@@ -517,6 +597,8 @@ def make_workload(name, T=None):
         return MharWorkload(T=T or 131072)
     if name == "msar":
         return MsarWorkload(T=T or 32768)
+    if name == "read_bwd":
+        return ReadBwdWorkload(T=T or 32768)
     if name == "block_fused":
         return BlockFusedWorkload(T=T or 32768)
     if name == "full_depth":
@@ -753,7 +835,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "block_fused", "mhar", "msar", "full_depth"])
+                    choices=["block", "block_d2048", "block_fused", "read_bwd", "mhar", "msar", "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

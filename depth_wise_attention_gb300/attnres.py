@@ -32,6 +32,9 @@ _SIGS = {
     "attnres_block_phase2_update_merge": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp,
                                           _f, _vp, _vp],
     "mhar_phase2_merge": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _f, _vp, _vp],
+    "attnres_read_bwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _i64,
+                         ctypes.c_int, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "attnres_read_bwd_workspace_size": [_i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
     "mhar_fwd": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp,
                  _vp],
     "msar_expand_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
@@ -197,6 +200,40 @@ def mhar_phase2_merge(o, lse, partial, query, gain=None, eps=1e-6, f=None, parti
         _p(o), _p(lse), _p(partial), _p(f), _p(partial_out), T, d, H, _dt(o), _p(query), _p(gain), eps,
         _p(out), _stream(stream)))
     return (partial_out, out) if f is not None else out
+
+
+def attnres_read_bwd_workspace_size(n_src, T, d, n_q, dtype):
+    import torch
+    n = ctypes.c_size_t(0)
+    dt = BF16 if dtype == torch.bfloat16 else F32
+    _check("attnres_read_bwd_workspace_size",
+           load().attnres_read_bwd_workspace_size(n_src, T, d, n_q, dt, ctypes.byref(n)))
+    return n.value
+
+
+def attnres_read_bwd(src, queries, dout, gain=None, eps=1e-6, dsrc=None, accumulate=False, dqueries=None,
+                     dgain=None, want_dgain=True, workspace=None, stream=None):
+    """Backward of the read of queries [n_q,d] over src [n_src,T,d] for output
+    gradients dout [n_q,T,d] -> (dsrc, dqueries, dgain).  The workspace is
+    allocated here unless given (the library itself allocates nothing)."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    n_q = queries.shape[0]
+    if dsrc is None:
+        dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=src.device)
+    _, _, _, dstride = _src_geometry(dsrc)
+    if dqueries is None:
+        dqueries = torch.empty((n_q, d), dtype=torch.float32, device=src.device)
+    if dgain is None and want_dgain:
+        dgain = torch.empty((d,), dtype=torch.float32, device=src.device)
+    if workspace is None:
+        nbytes = attnres_read_bwd_workspace_size(n_src, T, d, n_q, src.dtype)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=src.device)
+    _check("attnres_read_bwd", load().attnres_read_bwd(
+        _p(src), n_src, stride, T, d, _dt(src), _p(queries), n_q, _p(gain), eps, _p(dout), _p(dsrc), dstride,
+        1 if accumulate else 0, _p(dqueries), _p(dgain), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return dsrc, dqueries, dgain
 
 
 def mhar_fwd(src, queries, gain=None, eps=1e-6, out=None, lse=None, want_lse=False, stream=None):

@@ -28,6 +28,7 @@ SOURCES = [
     "kernels_phase2_mh.cu",
     "kernels_mma.cu",
     "kernels_mma_multi.cu",
+    "kernels_bwd.cu",
     "msar.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -16,6 +16,7 @@
 #include "dispatch.h"
 #include "msar.h"
 #include "phase2.cuh"
+#include "read_bwd.cuh"
 
 using namespace attnres;
 
@@ -426,6 +427,125 @@ attnres_status_t launch_phase2(const void *o, const float *lse, const void *part
     return ATTNRES_OK;
 }
 
+// Backward of the read: tile shape, workspace size and launch.
+struct ReadBwdShape {
+    int tpr, vpt, tt, ns;
+};
+
+attnres_status_t read_bwd_shape(int64_t n_src, int64_t d, int64_t n_q, attnres_dtype_t dt, ReadBwdShape *sh) {
+    const int nvec = (int)(d / epv(dt));
+    row_shape(nvec, &sh->tpr, &sh->vpt);
+    sh->tt = RB_THREADS / sh->tpr;
+    // a tile holds n_src + n_q rows of tt tokens and two stages must fit:
+    // spread a token over more threads (fewer tokens per tile) until they do
+    const size_t rows = (size_t)(n_src + n_q) * (size_t)d * esize(dt);
+    while (2 * rows * (size_t)sh->tt + 8 * 1024 > kSmemBudget && sh->tpr < RB_THREADS && sh->vpt > 1) {
+        sh->tpr *= 2;
+        sh->vpt = pow2ceil((nvec + sh->tpr - 1) / sh->tpr);
+        sh->tt = RB_THREADS / sh->tpr;
+    }
+    sh->ns = n_src <= 8 ? 8 : 16;
+    if (n_q > 2 || sh->vpt > 4 || (sh->ns == 16 && n_q > 1) || n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    return ATTNRES_OK;
+}
+
+// Per-(CTA, row) partials of U: one CTA per SM at most.
+size_t read_bwd_ws_bytes(int sms, const ReadBwdShape &sh, int64_t n_q, int64_t d) {
+    return (size_t)sms * (size_t)sh.tt * (size_t)n_q * (size_t)d * sizeof(float);
+}
+
+attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                 attnres_dtype_t dt, const float *queries, int64_t n_q, const float *gain,
+                                 float eps, const void *dout, void *dsrc, int64_t dsrc_stride, int accumulate,
+                                 float *dq, float *dgain, void *ws, size_t ws_bytes, void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (n_q < 1 || (accumulate != 0 && accumulate != 1)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!queries || !dout || !dsrc || !dq || !ws)) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t dsrc_bytes = ((size_t)(n_src - 1) * (size_t)dsrc_stride + (size_t)T * (size_t)d) * es;
+    const size_t dout_bytes = (size_t)n_q * (size_t)T * (size_t)d * es;
+    const size_t dq_bytes = (size_t)n_q * (size_t)d * sizeof(float);
+    if (overlap(dsrc, dsrc_bytes, src, src_bytes) || overlap(dsrc, dsrc_bytes, dout, dout_bytes) ||
+        overlap(ws, ws_bytes, src, src_bytes) || overlap(ws, ws_bytes, dsrc, dsrc_bytes) ||
+        overlap(ws, ws_bytes, dout, dout_bytes) || overlap(dq, dq_bytes, ws, ws_bytes) ||
+        (dgain && (overlap(dgain, (size_t)d * 4, ws, ws_bytes) || overlap(dgain, (size_t)d * 4, dq, dq_bytes))))
+        return ATTNRES_ERR_INVALID_ARG;
+    ReadBwdShape sh;
+    st = read_bwd_shape(n_src, d, n_q, dt, &sh);
+    if (st != ATTNRES_OK) return st;
+    if (!aligned16(dout) || !aligned16(dsrc) || (dsrc_stride * (int64_t)es) % 16 != 0 || !aligned16(queries) ||
+        (gain && !aligned16(gain)) || !aligned4(dq) || (dgain && !aligned4(dgain)) || !aligned16(ws))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    if (T == 0) {
+        // no tokens: the parameter gradients are zero, the sources have none
+        cudaError_t e = dq ? cudaMemsetAsync(dq, 0, dq_bytes, static_cast<cudaStream_t>(stream)) : cudaSuccess;
+        if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (ws_bytes < read_bwd_ws_bytes(dev->sms, sh, n_q, d)) return ATTNRES_ERR_INVALID_ARG;
+    KernelRef kr;
+    if (!lookup_read_bwd(dt == ATTNRES_BF16 ? 1 : 0, (int)n_q, sh.ns, sh.vpt, &kr)) return ATTNRES_ERR_UNSUPPORTED;
+    const uint32_t row_pitch = (uint32_t)((size_t)sh.tt * (size_t)d * es);
+    const uint32_t stage_bytes = (uint32_t)(((size_t)(n_src + n_q) * row_pitch + 127) / 128 * 128);
+    size_t budget = kSmemBudget;
+    if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
+    if (budget <= kr.aux_smem) return ATTNRES_ERR_UNSUPPORTED;
+    int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
+    if (nstages > RB_MAX_STAGES) nstages = RB_MAX_STAGES;
+    if (nstages < 2) return ATTNRES_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
+    int occ = 0;
+    st = prepare_kernel(kr.fn, smem, RB_THREADS, &occ);
+    if (st != ATTNRES_OK) return st;
+    ReadBwdArgs a;
+    a.src = static_cast<const unsigned char *>(src);
+    a.src_stride_bytes = src_stride * (int64_t)es;
+    a.n_src = (int)n_src;
+    a.T = T;
+    a.d = (int)d;
+    a.nvec = (int)(d / epv(dt));
+    a.n_q = (int)n_q;
+    a.queries = queries;
+    a.gain = gain;
+    a.eps = eps;
+    a.dout = static_cast<const unsigned char *>(dout);
+    a.dsrc = static_cast<unsigned char *>(dsrc);
+    a.dsrc_stride_bytes = dsrc_stride * (int64_t)es;
+    a.accumulate = accumulate;
+    a.ws = static_cast<float *>(ws);
+    a.tpr = sh.tpr;
+    a.tt = sh.tt;
+    a.nstages = nstages;
+    a.stage_bytes = stage_bytes;
+    a.row_pitch = row_pitch;
+    a.ntiles = (T + sh.tt - 1) / sh.tt;
+    a.wait = wait_cfg(dev);
+    const int grid = (int)(a.ntiles < dev->sms ? a.ntiles : dev->sms);
+    void *args[] = {&a};
+    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(RB_THREADS), args, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "read_bwd launch");
+    ReadBwdFinishArgs f;
+    f.ws = a.ws;
+    f.nparts = grid * sh.tt;
+    f.n_q = (int)n_q;
+    f.d = (int)d;
+    f.queries = queries;
+    f.gain = gain;
+    f.dq = dq;
+    f.dgain = dgain;
+    void *fargs[] = {&f};
+    const int fgrid = (int)((d + 255) / 256);
+    e = cudaLaunchKernel(read_bwd_finish_fn(), dim3(fgrid), dim3(256), fargs, 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "read_bwd finish launch");
+    return ATTNRES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -471,6 +591,30 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
                                    const float *query, const float *gain, float eps, void *out, void *stream) {
     return launch_phase2(o, lse, partial, f, partial_out, f != nullptr, T, d, H, dt, query, gain, eps, out,
                          stream);
+}
+
+attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t n_q,
+                                                attnres_dtype_t dt, size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || n_src < 1 || T < 0 || d < 1 || n_q < 1)
+        return ATTNRES_ERR_INVALID_ARG;
+    if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    ReadBwdShape sh;
+    attnres_status_t st = read_bwd_shape(n_src, d, n_q, dt, &sh);
+    if (st != ATTNRES_OK) return st;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    *bytes = read_bwd_ws_bytes(dev->sms, sh, n_q, d);
+    return ATTNRES_OK;
+}
+
+attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                  attnres_dtype_t dt, const float *queries, int64_t n_q, const float *gain,
+                                  float eps, const void *dout, void *dsrc, int64_t dsrc_stride, int accumulate,
+                                  float *dqueries, float *dgain, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    return launch_read_bwd(src, n_src, src_stride, T, d, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+                           accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
 }
 
 attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,

@@ -27,6 +27,11 @@ bool lookup_depth_read_mma2(int nq, int ks, int nw, KernelRef *out);
 // depth_read_mma_multi_kernel<nq, ks, nw>: > 8 sources in chunks of 8 (online softmax)
 bool lookup_depth_read_mma_multi(int nq, int ks, int nw, KernelRef *out);
 
+// read_bwd_kernel<T, nq, ns, vpt> (nq queries, at most ns sources) and the
+// workspace reduction kernel that finishes dq and dgain
+bool lookup_read_bwd(int dt, int nq, int ns, int vpt, KernelRef *out);
+const void *read_bwd_finish_fn();
+
 // phase2_merge_kernel<T, vpt, upd, mh>: upd = fused partial-sum update, mh = per-head merge
 bool lookup_phase2(int dt, int vpt, bool upd, bool mh, KernelRef *out);
 bool lookup_phase2_mh(int dt, int vpt, bool upd, KernelRef *out);

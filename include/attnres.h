@@ -204,6 +204,53 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
                                    const float *gain, float eps, void *out, void *stream);
 
 /*
+ * Backward of the depth read (Full AttnRes: n_q = 1; a Block layer: its
+ * sources [b_0..b_{n-1}, partial]; the queries of a block read together):
+ * given the gradients dout of the outputs h_q = sum_i alpha_qi v_i, returns
+ * the gradients of the sources, the pseudo-queries and the RMSNorm gain.
+ * The weights alpha are recomputed from the sources (nothing is saved by the
+ * forward).  Defined by the read of the b-lab.team summary, section 1
+ * (h = sum_i alpha_i v_i, alpha = softmax of w . RMSNorm(v_i)), differentiated
+ * term by term:
+ *   ds_qi = alpha_qi (dout_q . v_i - sum_j alpha_qj dout_q . v_j)
+ *   dv_i  = sum_q alpha_qi dout_q + sum_q ds_qi (w_q * g) / r_i
+ *           - v_i sum_q ds_qi ((w_q * g) . v_i) / (d r_i^3)
+ *   dw_q  = g * sum_{t,i} ds_qi v_i / r_i,   dgain = sum_{t,i,q} ds_qi w_q * v_i / r_i
+ * with r_i = sqrt(mean(v_i^2) + eps) (a zero source with eps = 0 passes
+ * nothing back through its score).
+ *   src        [n_src][T][d], sources src_stride elements apart
+ *   queries    [n_q][d] float, n_q = 1 or 2;  gain [d] float or NULL
+ *   dout       [n_q][T][d] dtype dt
+ *   dsrc       [n_src][T][d] dtype dt, sources dsrc_stride (>= T*d) elements
+ *              apart; overwritten, or added to when accumulate = 1 (so the
+ *              gradients of several reads of the same sources can be summed)
+ *   dqueries   [n_q][d] float, overwritten
+ *   dgain      [d] float or NULL, overwritten
+ *   workspace  device scratch of at least the size attnres_read_bwd_workspace_size
+ *              reports (16-byte aligned), owned by the caller; the sums over
+ *              the tokens go through it and are reduced in a fixed order, so
+ *              results are bitwise reproducible
+ * No output may overlap an input or the workspace.  T = 0 zeroes dqueries and
+ * dgain.  Limits: n_src <= 8 with 2 queries, <= 16 with 1; the n_src + n_q
+ * rows of a token tile must fit two shared-memory stages (for d = 4096 bf16,
+ * n_src + n_q <= 13).
+ */
+attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                  int64_t d, attnres_dtype_t dt, const float *queries, int64_t n_q,
+                                  const float *gain, float eps, const void *dout, void *dsrc,
+                                  int64_t dsrc_stride, int accumulate, float *dqueries,
+                                  float *dgain, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
+ * Workspace bytes attnres_read_bwd needs for these sizes on the current
+ * device (an upper bound: one partial row of d floats per query for every
+ * token row a CTA holds, one CTA per SM).  No device work is done.
+ */
+attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t n_q,
+                                                attnres_dtype_t dt, size_t *bytes);
+
+/*
  * MSAR, the fused multi-stream depth read for one target layer: every source
  * v_i is expanded into m full-width streams (r = 0 identity; r >= 1 a causal
  * depthwise 1-D convolution along the token axis with kernel size

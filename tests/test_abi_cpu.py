@@ -139,6 +139,35 @@ def test_phase2_update_and_mhar_phase2_validation(lib):
     assert mh(H=3, d=3 * 384, T=0) == UNS             # 48 vectors per head
 
 
+def test_read_bwd_validation(lib):
+    SRC, Q, DO, DS, DQ, DG, WS = A, B, B + 0x100000, A + 0x1000000, B + 0x200000, B + 0x300000, B + 0x400000
+
+    def bw(src=SRC, n_src=9, T=16, d=64, q=Q, n_q=1, dout=DO, dsrc=DS, dstride=None, acc=0, dq=DQ, dg=DG,
+           ws=WS, wsb=1 << 20, eps=1e-6):
+        dstride = T * d if dstride is None else dstride
+        return lib.attnres_read_bwd(src, n_src, T * d, T, d, BF16, q, n_q, None, eps, dout, dsrc, dstride, acc,
+                                    dq, dg, ws, wsb, None)
+    assert bw(n_q=0) == INV
+    assert bw(acc=2) == INV
+    assert bw(dout=None) == INV
+    assert bw(dsrc=None) == INV
+    assert bw(dq=None) == INV
+    assert bw(ws=None) == INV
+    assert bw(dstride=16 * 64 - 8) == INV              # gradient rows of two sources overlap
+    assert bw(dsrc=SRC + 64) == INV                    # overlaps the sources
+    assert bw(ws=DO + 32) == INV                       # workspace overlaps dout
+    assert bw(dq=WS + 64) == INV                       # dq overlaps the workspace
+    assert bw(n_q=3) == UNS                            # at most two queries
+    assert bw(n_src=17) == UNS
+    assert bw(n_src=9, n_q=2) == UNS                   # two queries: at most 8 sources
+    assert bw(dout=DO + 8) == UNS                      # misaligned
+    assert bw(dg=None, T=0) != INV                     # dgain is optional
+    n = ctypes.c_size_t(0)
+    assert lib.attnres_read_bwd_workspace_size(9, 16, 64, 1, BF16, None) == INV
+    assert lib.attnres_read_bwd_workspace_size(9, 16, 60, 1, BF16, ctypes.byref(n)) == UNS
+    assert lib.attnres_read_bwd_workspace_size(9, 16, 64, 3, BF16, ctypes.byref(n)) == UNS
+
+
 def test_msar_validation(lib):
     ks = (ctypes.c_int32 * 3)(4, 8, 12)
     bad = (ctypes.c_int32 * 3)(4, 0, 12)

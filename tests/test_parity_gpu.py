@@ -343,6 +343,65 @@ def test_mhar_one_head_is_phase1_bitwise():
     assert torch.equal(lse, ml.view(4, T))
 
 
+# --------------------------------------------------------------- backward
+
+def _check_grads(got, ref, dtype, what):
+    dsrc, dq, dg = got
+    rs, rq, rg = ref
+    check_out(dsrc, rs, dtype, what=f"{what} dsrc")
+    # parameter gradients are fp32 sums over the tokens
+    for name, g_, r_ in (("dq", dq, rq), ("dgain", dg, rg)):
+        if g_ is not None:
+            check_out(g_, r_, F32, np.abs(r_).max(), strict=False, what=f"{what} {name}")
+
+
+@pytest.mark.parametrize("n_src,n_q,T,d,dtype,with_gain", [
+    (1, 1, 5, 64, F32, False), (3, 1, 37, 256, F32, True), (9, 1, 70, 4096, BF16, True),
+    (8, 2, 40, 2048, BF16, False), (16, 1, 20, 1024, BF16, True), (5, 2, 300, 512, F32, True),
+    (12, 1, 3, 4096, BF16, False), (4, 1, 333, 1000, F32, True), (7, 2, 90, 1024, BF16, True)])
+def test_read_bwd(n_src, n_q, T, d, dtype, with_gain):
+    """Backward of the read against the oracle's chain rule: the sources', the
+    queries' and the gain's gradients."""
+    rng = _rng(n_src * 5 + n_q + T + d)
+    src = _sources(rng, n_src, T, d, dtype, step=0.25)
+    q = _queries(rng, n_q, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gain else None
+    dout = _sources(rng, n_q, T, d, dtype, step=0)
+    got = attnres.attnres_read_bwd(to_dev(src, dtype), to_dev(q, F32), to_dev(dout, dtype),
+                                   to_dev(g, F32) if with_gain else None, 1e-6)
+    _check_grads(got, oracle.read_bwd(src, q, dout, g, 1e-6), dtype, f"n_src={n_src}")
+
+
+def test_read_bwd_accumulates_and_is_deterministic():
+    rng = _rng(51)
+    n_src, T, d = 9, 200, 4096
+    src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.25), BF16)
+    q = to_dev(_queries(rng, 1, d), F32)
+    dout = to_dev(_sources(rng, 1, T, d, BF16, step=0), BF16)
+    g = to_dev(rng.uniform(0.5, 1.5, d).astype(np.float32), F32)
+    a = attnres.attnres_read_bwd(src, q, dout, g)
+    b = attnres.attnres_read_bwd(src, q, dout, g)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    base = to_dev(_sources(rng, n_src, T, d, BF16), BF16)
+    acc = base.clone()
+    attnres.attnres_read_bwd(src, q, dout, g, dsrc=acc, accumulate=True)
+    ref = to_host(base) + to_host(a[0])
+    check_out(acc, ref, BF16, what="accumulated dsrc")
+
+
+def test_read_bwd_empty_sequence_zeroes_parameter_gradients():
+    d = 256
+    src = torch.empty((3, 0, d), dtype=F32, device="cuda")
+    q = to_dev(_queries(_rng(52), 1, d), F32)
+    dq = torch.full((1, d), 7.0, device="cuda")
+    dg = torch.full((d,), 7.0, device="cuda")
+    attnres.attnres_read_bwd(src, q, torch.empty((1, 0, d), dtype=F32, device="cuda"), None, 1e-6,
+                             dqueries=dq, dgain=dg)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dq) == 0 and torch.count_nonzero(dg) == 0
+
+
 # --------------------------------------------------------------- MSAR
 
 @pytest.mark.parametrize("dtype", [F32, BF16])
