@@ -34,6 +34,8 @@ _SIGS = {
     "mhar_phase2_merge": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _f, _vp, _vp],
     "attnres_read_bwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _i64,
                          ctypes.c_int, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "attnres_read_bwd_noalloc": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _i64,
+                                 ctypes.c_int, _vp, _vp, _vp],
     "attnres_read_bwd_workspace_size": [_i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
     "mhar_fwd": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp,
                  _vp],
@@ -233,6 +235,25 @@ def attnres_read_bwd(src, queries, dout, gain=None, eps=1e-6, dsrc=None, accumul
         _p(src), n_src, stride, T, d, _dt(src), _p(queries), n_q, _p(gain), eps, _p(dout), _p(dsrc), dstride,
         1 if accumulate else 0, _p(dqueries), _p(dgain), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+    return dsrc, dqueries, dgain
+
+
+def attnres_read_bwd_noalloc(src, queries, dout, gain=None, eps=1e-6, dsrc=None, accumulate=False,
+                             dqueries=None, dgain=None, want_dgain=True, stream=None):
+    """attnres_read_bwd with the library's built-in scratch instead of a workspace."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    n_q = queries.shape[0]
+    if dsrc is None:
+        dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=src.device)
+    _, _, _, dstride = _src_geometry(dsrc)
+    if dqueries is None:
+        dqueries = torch.empty((n_q, d), dtype=torch.float32, device=src.device)
+    if dgain is None and want_dgain:
+        dgain = torch.empty((d,), dtype=torch.float32, device=src.device)
+    _check("attnres_read_bwd_noalloc", load().attnres_read_bwd_noalloc(
+        _p(src), n_src, stride, T, d, _dt(src), _p(queries), n_q, _p(gain), eps, _p(dout), _p(dsrc), dstride,
+        1 if accumulate else 0, _p(dqueries), _p(dgain), _stream(stream)))
     return dsrc, dqueries, dgain
 
 

@@ -546,6 +546,32 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
     return ATTNRES_OK;
 }
 
+// Scratch of the no-allocation backward: a fixed device array in the
+// library's own image (8 MB: every one-query backward and two-query ones up
+// to d of about 6.7 K on 152 SMs; one backward at a time per device may use
+// it), its address looked up once per device.
+constexpr size_t kBwdScratchFloats = (size_t)2 << 20;
+static __device__ __align__(256) float g_bwd_scratch[kBwdScratchFloats];
+
+struct ScratchInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void *ptr = nullptr;
+};
+ScratchInfo g_scratch[kMaxDevices];
+
+attnres_status_t bwd_scratch(void **ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return ATTNRES_ERR_UNSUPPORTED;
+    ScratchInfo &si = g_scratch[dev];
+    std::call_once(si.once, [&] { si.err = cudaGetSymbolAddress(&si.ptr, g_bwd_scratch); });
+    if (si.err != cudaSuccess) return cuda_fail(si.err, "cudaGetSymbolAddress");
+    *ptr = si.ptr;
+    return ATTNRES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -615,6 +641,24 @@ attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_st
                                   void *stream) {
     return launch_read_bwd(src, n_src, src_stride, T, d, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
                            accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
+}
+
+attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                          int64_t d, attnres_dtype_t dt, const float *queries, int64_t n_q,
+                                          const float *gain, float eps, const void *dout, void *dsrc,
+                                          int64_t dsrc_stride, int accumulate, float *dqueries, float *dgain,
+                                          void *stream) {
+    size_t need = 0;
+    if (T > 0) {
+        attnres_status_t st = attnres_read_bwd_workspace_size(n_src, T, d, n_q, dt, &need);
+        if (st != ATTNRES_OK) return st;
+        if (need > kBwdScratchFloats * sizeof(float)) return ATTNRES_ERR_UNSUPPORTED;
+    }
+    void *ws = nullptr;
+    attnres_status_t st = bwd_scratch(&ws);
+    if (st != ATTNRES_OK) return st;
+    return launch_read_bwd(src, n_src, src_stride, T, d, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+                           accumulate, dqueries, dgain, ws, kBwdScratchFloats * sizeof(float), stream);
 }
 
 attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,

@@ -251,6 +251,24 @@ attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64
                                                 attnres_dtype_t dt, size_t *bytes);
 
 /*
+ * attnres_read_bwd without a caller workspace: the same backward, with the
+ * sums over the tokens reduced through a fixed 8 MB scratch array that the
+ * library's image holds in device memory (its address is looked up once per
+ * device); nothing is allocated.  The pages have no counterpart: this entry
+ * point exists for callers that cannot hand out device memory (for instance
+ * inside a captured CUDA graph).  Calls that would need more scratch than the
+ * array holds return ATTNRES_ERR_UNSUPPORTED; all other arguments, limits and
+ * errors are those of attnres_read_bwd.  The array is shared: calls on one
+ * device must be ordered (one stream, or streams that wait for each other).
+ */
+attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_t src_stride,
+                                          int64_t T, int64_t d, attnres_dtype_t dt,
+                                          const float *queries, int64_t n_q, const float *gain,
+                                          float eps, const void *dout, void *dsrc,
+                                          int64_t dsrc_stride, int accumulate, float *dqueries,
+                                          float *dgain, void *stream);
+
+/*
  * MSAR, the fused multi-stream depth read for one target layer: every source
  * v_i is expanded into m full-width streams (r = 0 identity; r >= 1 a causal
  * depthwise 1-D convolution along the token axis with kernel size
