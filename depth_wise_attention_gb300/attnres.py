@@ -41,6 +41,8 @@ _SIGS = {
                  _vp],
     "msar_expand_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
                         _vp, _vp, _f, _vp, _vp],
+    "msar_expand_fwd_chunk": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
+                              _vp, _vp, _f, _vp, _vp],
     "attnres_status_string": [ctypes.c_int],
     "attnres_last_cuda_error": [],
     "attnres_sync_status": [_vp],
@@ -305,3 +307,20 @@ def attnres_debug_set_kernel_variant(variant: int):
     """0: automatic kernel choice; 1: always the general CUDA-core depth read;
     2: the tensor-core depth reads wherever they apply."""
     load().attnres_debug_set_kernel_variant(int(variant))
+
+
+def msar_expand_fwd_chunk(src, t_prev, ksizes, conv_w, queries, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                          mix_eps=1e-6, out=None, stream=None):
+    """MSAR for one chunk: src [n_src, t_prev + T, d] (t_prev history rows first)
+    -> out [T, d] for the last T rows."""
+    import torch
+    n_src, rows, d, stride = _src_geometry(src)
+    T = rows - t_prev
+    m = queries.shape[0]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if out is None:
+        out = torch.empty((T, d), dtype=src.dtype, device=src.device)
+    _check("msar_expand_fwd_chunk", load().msar_expand_fwd_chunk(
+        _p(src), n_src, stride, t_prev, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries),
+        _p(gain), eps, _p(mix_gain), _p(mix_w), mix_eps, _p(out), _stream(stream)))
+    return out

@@ -572,6 +572,54 @@ attnres_status_t bwd_scratch(void **ptr) {
     return ATTNRES_OK;
 }
 
+// Shared launch path of the MSAR read: src holds t_prev history rows and
+// then the T rows whose outputs are written.
+attnres_status_t launch_msar_read(const void *src, int64_t n_src, int64_t src_stride, int64_t t_prev, int64_t T,
+                                  int64_t d, attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                  const float *conv_w, const float *queries, const float *gain, float eps,
+                                  const float *mix_gain, const float *mix_w, float mix_eps, void *out,
+                                  void *stream) {
+    if (T < 0 || t_prev > INT64_MAX - T) return ATTNRES_ERR_INVALID_ARG;
+    const int64_t rows = t_prev + T;                      // source rows per source
+    attnres_status_t st = check_common(src, n_src, src_stride, rows, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (m < 1 || !(mix_eps >= 0.f) || std::isinf(mix_eps)) return ATTNRES_ERR_INVALID_ARG;
+    if (T == 0) return ATTNRES_OK;
+    if (!ksizes || !conv_w || !queries || !mix_w || !out) return ATTNRES_ERR_INVALID_ARG;
+    for (int64_t r = 0; r + 1 < m; ++r)
+        if (ksizes[r] < 1) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)rows * (size_t)d) * es;
+    if (overlap(out, (size_t)T * (size_t)d * es, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
+    if (m != 4) return ATTNRES_ERR_UNSUPPORTED;
+    for (int r = 0; r < 3; ++r)
+        if (ksizes[r] > MSAR_KMAX) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(queries) || !aligned16(conv_w) || !aligned16(mix_w) ||
+        (gain && !aligned16(gain)) || (mix_gain && !aligned16(mix_gain)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarArgs a;
+    a.src = static_cast<const unsigned char *>(src);
+    a.src_stride_bytes = src_stride * (int64_t)es;
+    a.n_src = (int)n_src;
+    a.T = T;
+    a.t_prev = t_prev;
+    a.d = (int)d;
+    for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
+    a.conv_w = conv_w;
+    a.queries = queries;
+    a.gain = gain;
+    a.eps = eps;
+    a.mix_gain = mix_gain;
+    a.mix_w = mix_w;
+    a.mix_eps = mix_eps;
+    a.out = static_cast<unsigned char *>(out);
+    a.wait = wait_cfg(dev);
+    return launch_msar(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
+}
+
 }  // namespace
 
 extern "C" {
@@ -666,43 +714,18 @@ attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_str
                                  const float *conv_w, const float *queries, const float *gain,
                                  float eps, const float *mix_gain, const float *mix_w, float mix_eps,
                                  void *out, void *stream) {
-    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
-    if (st != ATTNRES_OK) return st;
-    if (m < 1 || !(mix_eps >= 0.f) || std::isinf(mix_eps)) return ATTNRES_ERR_INVALID_ARG;
-    if (T == 0) return ATTNRES_OK;
-    if (!ksizes || !conv_w || !queries || !mix_w || !out) return ATTNRES_ERR_INVALID_ARG;
-    for (int64_t r = 0; r + 1 < m; ++r)
-        if (ksizes[r] < 1) return ATTNRES_ERR_INVALID_ARG;
-    const size_t es = esize(dt);
-    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
-    if (overlap(out, (size_t)T * (size_t)d * es, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
-    if (m != 4) return ATTNRES_ERR_UNSUPPORTED;
-    for (int r = 0; r < 3; ++r)
-        if (ksizes[r] > MSAR_KMAX) return ATTNRES_ERR_UNSUPPORTED;
-    if (!aligned16(out) || !aligned16(queries) || !aligned16(conv_w) || !aligned16(mix_w) ||
-        (gain && !aligned16(gain)) || (mix_gain && !aligned16(mix_gain)))
-        return ATTNRES_ERR_UNSUPPORTED;
-    if (T == 0) return ATTNRES_OK;
-    DeviceInfo *dev = nullptr;
-    st = device_info(&dev);
-    if (st != ATTNRES_OK) return st;
-    MsarArgs a;
-    a.src = static_cast<const unsigned char *>(src);
-    a.src_stride_bytes = src_stride * (int64_t)es;
-    a.n_src = (int)n_src;
-    a.T = T;
-    a.d = (int)d;
-    for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
-    a.conv_w = conv_w;
-    a.queries = queries;
-    a.gain = gain;
-    a.eps = eps;
-    a.mix_gain = mix_gain;
-    a.mix_w = mix_w;
-    a.mix_eps = mix_eps;
-    a.out = static_cast<unsigned char *>(out);
-    a.wait = wait_cfg(dev);
-    return launch_msar(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
+    return launch_msar_read(src, n_src, src_stride, 0, T, d, dt, m, ksizes, conv_w, queries, gain, eps,
+                            mix_gain, mix_w, mix_eps, out, stream);
+}
+
+attnres_status_t msar_expand_fwd_chunk(const void *src, int64_t n_src, int64_t src_stride, int64_t T_prev,
+                                       int64_t T, int64_t d, attnres_dtype_t dt, int64_t m,
+                                       const int32_t *ksizes, const float *conv_w, const float *queries,
+                                       const float *gain, float eps, const float *mix_gain,
+                                       const float *mix_w, float mix_eps, void *out, void *stream) {
+    if (T_prev < 0) return ATTNRES_ERR_INVALID_ARG;
+    return launch_msar_read(src, n_src, src_stride, T_prev, T, d, dt, m, ksizes, conv_w, queries, gain, eps,
+                            mix_gain, mix_w, mix_eps, out, stream);
 }
 
 const char *attnres_status_string(attnres_status_t s) {

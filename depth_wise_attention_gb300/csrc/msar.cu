@@ -140,7 +140,10 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
     const int64_t tb = cid * a.tokens_per_cluster;
     const int64_t te = min(a.T, tb + a.tokens_per_cluster);
     const int64_t ntok = te > tb ? te - tb : 0;
-    const int64_t rho0 = tb - hist > 0 ? tb - hist : 0;   // first row this cluster loads
+    // source rows of this cluster's first and past-last output tokens (a
+    // chunk of a longer sequence starts t_prev history rows into src)
+    const int64_t rb = tb + a.t_prev, re = te + a.t_prev;
+    const int64_t rho0 = rb - hist > 0 ? rb - hist : 0;   // first row this cluster loads
 
     const bool producer = (tid == 0) && !a.wait.inject_stall;
     uint64_t pol = 0;
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
                      &bars[p_slot], pol);
         if (++p_slot == ring) p_slot = 0;
     };
-    const int64_t prolog_end = min(te, tb + 1 + MSAR_LA);
+    const int64_t prolog_end = min(re, rb + 1 + MSAR_LA);
     if (producer)
         for (; next_row < prolog_end; ++next_row) issue_row(next_row);
 
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
     for (int o = 0; o < 5; ++o) mixp[o] = 0.f;
 
     // ring slot and mbarrier phase parity of the current token's row
-    int cur_slot = (int)(tb - rho0);
+    int cur_slot = (int)(rb - rho0);
     uint32_t cur_par = 0;
     for (int64_t n = 0; n <= ntok; ++n) {
         const int64_t t = tb + n;
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
         }
         __syncthreads();
         // every thread has finished reading row t - hist: reuse its slot
-        if (producer && next_row < te && !*abort_flag) issue_row(next_row++);
+        if (producer && next_row < re && !*abort_flag) issue_row(next_row++);
         const int par = (int)(n & 1);
         for (int j = tid; j < MSAR_NX; j += blockDim.x) {
             float s = 0.f;

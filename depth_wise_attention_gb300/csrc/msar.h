@@ -19,7 +19,8 @@ struct MsarArgs {
     const unsigned char *src;
     int64_t src_stride_bytes;
     int n_src;
-    int64_t T;
+    int64_t T;                 // output tokens
+    int64_t t_prev;            // history rows before the first output token: token t is src row t + t_prev
     int d;
     int k[3];                  // conv kernel sizes of streams 1..3
     const float *conv_w;       // packed [d][k_1] [d][k_2] [d][k_3]

@@ -301,6 +301,30 @@ attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_str
                                  const float *mix_gain, const float *mix_w, float mix_eps,
                                  void *out, void *stream);
 
+/*
+ * MSAR for one chunk of a longer sequence (chunked prefill): src holds, per
+ * source, T_prev rows that earlier chunks already processed followed by the
+ * T rows of this chunk; out receives the T outputs of this chunk.  The
+ * causal convolutions read back into the T_prev history rows; rows before
+ * the start of src count as zero, so T_prev = max kernel size - 1 (or every
+ * earlier token) gives exactly the outputs msar_expand_fwd would give for
+ * these tokens over the whole sequence.  T_prev = 0 is msar_expand_fwd.
+ * Defined by: onedev.kr MSAR page, sections 무엇과 다른가 and 어떻게 쓰나 (the
+ * causal stream expansion, fused on demand), with chunked prefill of long
+ * contexts from the dimensionstp.github.io review, sections 3-2 5) and 4-3.
+ *   src     [n_src] x [T_prev + T][d], sources src_stride (>= (T_prev+T)*d)
+ *           elements apart
+ *   out     [T][d] dtype dt; must not overlap src
+ * All other arguments, limits and errors are those of msar_expand_fwd;
+ * T_prev < 0 is ATTNRES_ERR_INVALID_ARG.
+ */
+attnres_status_t msar_expand_fwd_chunk(const void *src, int64_t n_src, int64_t src_stride,
+                                       int64_t T_prev, int64_t T, int64_t d, attnres_dtype_t dt,
+                                       int64_t m, const int32_t *ksizes, const float *conv_w,
+                                       const float *queries, const float *gain, float eps,
+                                       const float *mix_gain, const float *mix_w, float mix_eps,
+                                       void *out, void *stream);
+
 /* Static description of a status code (never NULL). */
 const char *attnres_status_string(attnres_status_t status);
 

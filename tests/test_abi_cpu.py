@@ -183,3 +183,11 @@ def test_msar_validation(lib):
     assert ms(out=None, T=4) == INV
     assert ms(m=3, T=4) == UNS
     assert ms(k=big, T=4) == UNS
+
+    def mc(t_prev=2, T=0, d=256, stride=None):
+        stride = (t_prev + T) * d if stride is None else stride
+        return lib.msar_expand_fwd_chunk(A, 8, stride, t_prev, T, d, BF16, 4, ctypes.cast(ks, ctypes.c_void_p),
+                                         B, B + 0x200000, None, 1e-6, None, B + 0x300000, 1e-6, B + 0x100000, None)
+    assert mc() == OK
+    assert mc(t_prev=-1) == INV
+    assert mc(t_prev=3, T=4, stride=4 * 256) == INV    # sources hold fewer than t_prev + T rows

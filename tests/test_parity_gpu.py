@@ -343,6 +343,46 @@ def test_mhar_one_head_is_phase1_bitwise():
     assert torch.equal(lse, ml.view(4, T))
 
 
+def _msar_setup(rng, n_src, T, d, ks, dtype):
+    src = _sources(rng, n_src, T, d, dtype)
+    m = 4
+    q = _queries(rng, m, d)
+    cw = np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel() for k in ks])
+    mw = (rng.standard_normal((m * d, m)) / math.sqrt(m * d)).astype(np.float32)
+    return src, q, cw, mw
+
+
+@pytest.mark.parametrize("t_prev,T,d,dtype", [(11, 40, 2048, BF16), (3, 17, 512, F32), (0, 25, 256, BF16),
+                                              (30, 9, 4096, BF16)])
+def test_msar_chunk_matches_full_sequence(t_prev, T, d, dtype):
+    """A chunk of T tokens after t_prev history rows gives the full-sequence
+    read's outputs for those tokens (rows before the history count as zero)."""
+    rng = _rng(t_prev * 3 + T + d)
+    ks = (4, 8, 12)
+    src, q, cw, mw = _msar_setup(rng, 8, t_prev + T, d, ks, dtype)
+    out = attnres.msar_expand_fwd_chunk(to_dev(src, dtype), t_prev, ks, to_dev(cw, F32), to_dev(q, F32),
+                                        mix_w=to_dev(mw, F32))
+    ref = oracle.msar(src, ks, cw, q, None, 1e-6, None, mw, 1e-6)[t_prev:]
+    check_out(out, ref, dtype, np.abs(src).max())
+
+
+def test_msar_chunked_prefill_equals_one_call_bitwise():
+    """Prefill a sequence in chunks, each with the previous 11 rows as history:
+    every chunk's outputs equal the one-call read's rows bit for bit, and a
+    chunk with no history equals msar_expand_fwd."""
+    rng = _rng(61)
+    T, d, ks = 300, 2048, (4, 8, 12)
+    src, q, cw, mw = _msar_setup(rng, 8, T, d, ks, BF16)
+    sd, qd, cwd, mwd = to_dev(src, BF16), to_dev(q, F32), to_dev(cw, F32), to_dev(mw, F32)
+    whole = attnres.msar_expand_fwd(sd, ks, cwd, qd, mix_w=mwd)
+    first = attnres.msar_expand_fwd_chunk(sd[:, :64].contiguous(), 0, ks, cwd, qd, mix_w=mwd)
+    assert torch.equal(first, whole[:64])
+    for c0, c1 in ((64, 128), (128, 250), (250, 300)):
+        h = min(11, c0)
+        part = attnres.msar_expand_fwd_chunk(sd[:, c0 - h:c1].contiguous(), h, ks, cwd, qd, mix_w=mwd)
+        assert torch.equal(part, whole[c0:c1]), (c0, c1)
+
+
 # --------------------------------------------------------------- backward
 
 def _check_grads(got, ref, dtype, what):
