@@ -10,7 +10,7 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|msar|full_depth|
-block_d2048|block_fused|read_bwd) are for profiling and the design notes.
+block_d2048|block_fused|read_bwd|decode) are for profiling and the design notes.
 """
 from __future__ import annotations
 
@@ -41,6 +41,7 @@ KERNEL_SOURCES = {
     "phase2": [CSRC + "phase2.cuh", CSRC + "common.cuh", CSRC + "kernels_phase2.cu"],
     "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
+    "depth_read_decode": [CSRC + "depth_read_decode.cuh", CSRC + "common.cuh", CSRC + "kernels_decode.cu"],
 }
 
 
@@ -370,6 +371,78 @@ class ReadBwdWorkload(BlockWorkload):
         return src.shape[1]
 
 
+class DecodeWorkload(BlockWorkload):
+    """Decode-shaped Block AttnRes two-phase forward: a block (phase 1 + 3
+    merges) over T=16 tokens, bf16, d=4096, N=8, S=4.  Each step reads its own
+    set of inputs; the sets rotate through more than L2 holds, so every step
+    starts from HBM.  A step's four launches are captured once per input set in
+    a CUDA graph and replayed (decode latency is launch-bound otherwise).  The
+    metric is tokens/s; ms_per_step is the latency of one block."""
+
+    def __init__(self, T=16, d=4096, N=8, S=4, seed=0, sets=160):
+        super().__init__(T, d, N, S, seed, name="block_attnres_two_phase_decode")
+        self.sets = sets
+        self.k = 0
+        self.dominant = "decode step (graph: depth_read_decode_kernel + 3 merges)"
+        self.dominant_src = "depth_read_decode"
+        self.profile_tag = f"ncu_decode_d{d}_T{T}"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} N={self.N} S={self.S} T={self.T}"
+        c["l2"] = f"{self.sets} rotating input sets ({self.sets * self.bytes_per_token * self.T / 1e6:.0f} MB > L2)"
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        T, d, N, S = self.T, self.d, self.N, self.S
+        caches, g = inputs.device_sources(N * self.sets, T, d, lambda n: 1.0 + (n % N) / 2.0, seed=self.seed,
+                                          device=device)
+        self.caches = caches.view(self.sets, N, T, d)
+        self.queries = inputs.device_normal((S, d), (16.0 / d) ** 0.5, g, device=device)
+        self.parts = torch.randn((self.sets, S, T, d), generator=g, device=device).to(torch.bfloat16)
+        self.os = torch.empty((self.sets, S, T, d), dtype=torch.bfloat16, device=device)
+        self.lses = torch.empty((self.sets, S, T), dtype=torch.float32, device=device)
+        self.cache, self.partials, self.o, self.lse = self.caches[0], self.parts[0], self.os[0], self.lses[0]
+        # one graph per input set, captured after a warm-up run of each path
+        cap = torch.cuda.Stream(device)
+        with torch.cuda.stream(cap):
+            self._launch(0, cap)
+        torch.cuda.synchronize(device)
+        self.graphs = []
+        for j in range(self.sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                self._launch(j, cap)
+            self.graphs.append(g)
+        torch.cuda.synchronize(device)
+
+    def _launch(self, j, stream):
+        from depth_wise_attention_gb300 import attnres
+        cache, parts, o, lse = self.caches[j], self.parts[j], self.os[j], self.lses[j]
+        attnres.attnres_block_phase1(cache, self.queries, None, 1e-6, o=o, lse=lse, stream=stream)
+        for i in range(1, self.S):
+            attnres.attnres_block_phase2_merge(o[i], lse[i], parts[i], self.queries[i], None, 1e-6, out=o[i],
+                                               stream=stream)
+
+    def dominant_bytes_per_launch(self):
+        return self.T * self.bytes_per_token
+
+    def step(self, stream, ev=None):
+        j = self.k % self.sets
+        self.k += 1
+        if ev is not None:
+            ev[0].record(stream)
+        self.graphs[j].replay()
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step_e2e(self, stream):
+        self.k = 0
+        super().step_e2e(stream)
+
+
 class MharWorkload(BlockWorkload):
     """MHAR read: S=4 queries x H=8 heads over N=8 block reps (no phase 2)."""
 
@@ -597,6 +670,8 @@ def make_workload(name, T=None):
         return MharWorkload(T=T or 131072)
     if name == "msar":
         return MsarWorkload(T=T or 32768)
+    if name == "decode":
+        return DecodeWorkload(T=T or 16)
     if name == "read_bwd":
         return ReadBwdWorkload(T=T or 32768)
     if name == "block_fused":
@@ -835,7 +910,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "block_fused", "read_bwd", "mhar", "msar", "full_depth"])
+                    choices=["block", "block_d2048", "block_fused", "read_bwd", "decode", "mhar", "msar",
+                             "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -305,7 +305,8 @@ def attnres_debug_set_stall_injection(enable: bool):
 
 def attnres_debug_set_kernel_variant(variant: int):
     """0: automatic kernel choice; 1: always the general CUDA-core depth read;
-    2: the tensor-core depth reads wherever they apply."""
+    2: the tensor-core depth reads wherever they apply; 3: the few-token kernel
+    (a token per cluster of CTAs) wherever it applies."""
     load().attnres_debug_set_kernel_variant(int(variant))
 
 

@@ -12,6 +12,7 @@
 #include "../../include/attnres.h"
 #include "common.cuh"
 #include "depth_read.cuh"
+#include "depth_read_decode.cuh"
 #include "depth_read_mma.cuh"
 #include "dispatch.h"
 #include "msar.h"
@@ -30,7 +31,8 @@ thread_local char t_last_err[256] = "";
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_kernel_variant{0};   // 0 automatic, 1 general (CUDA-core) depth read only,
-                                        // 2 tensor-core depth reads wherever they apply
+                                        // 2 tensor-core depth reads wherever they apply,
+                                        // 3 the few-token kernel wherever it applies
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kStageMaxBytes = 64 * 1024;        // one ring stage
@@ -149,6 +151,21 @@ attnres_status_t check_common(const void *src, int64_t n_src, int64_t src_stride
     return ATTNRES_OK;
 }
 
+// Calls with at most this many tokens take the few-token kernel: a token per
+// cluster of CTAs beats the streaming kernels' one CTA per token there.
+constexpr int64_t kDecodeMaxT = 64;
+
+// Few-token kernel shape: the largest cluster (<= 8 CTAs) whose CTAs each get
+// a whole number of warps of 16-byte vectors, one vector per thread.
+bool decode_shape(int nvec, int *cs, int *vpc) {
+    for (int c = DEC_MAX_CS; c >= 1; c >>= 1) {
+        if (nvec % c) continue;
+        const int v = nvec / c;
+        if (v % 32 == 0 && v <= DEC_MAX_THREADS) { *cs = c; *vpc = v; return true; }
+    }
+    return false;
+}
+
 // Shared launch path of Full / phase 1 / MHAR.
 attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
                                    int64_t d, int64_t H, attnres_dtype_t dt, const float *queries,
@@ -168,6 +185,48 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     if (!aligned16(out) || !aligned16(queries) || (gain && !aligned16(gain)) || (lse && !aligned4(lse)))
         return ATTNRES_ERR_UNSUPPORTED;
     if (T == 0) return ATTNRES_OK;
+
+    // Few tokens (decode-shaped calls): one token per cluster of CTAs.
+    const int kvd = g_kernel_variant.load();
+    if (H == 1 && n_q <= 4 && (kvd == 3 || (kvd == 0 && T <= kDecodeMaxT))) {
+        int cs = 0, vpc = 0;
+        const int ns = n_src <= 8 ? 8 : 16;
+        KernelRef kr;
+        if (n_src <= 16 && decode_shape((int)(d / epv(dt)), &cs, &vpc) &&
+            lookup_depth_read_decode(dt == ATTNRES_BF16 ? 1 : 0, pow2ceil((int)n_q), ns, &kr)) {
+            DecodeArgs a;
+            a.src = static_cast<const unsigned char *>(src);
+            a.src_stride_bytes = src_stride * (int64_t)es;
+            a.n_src = (int)n_src;
+            a.T = T;
+            a.d = (int)d;
+            a.n_q = (int)n_q;
+            a.queries = queries;
+            a.gain = gain;
+            a.eps = eps;
+            a.out = static_cast<unsigned char *>(out);
+            a.out_q_stride_bytes = T * d * (int64_t)es;
+            a.lse = lse;
+            a.cs = cs;
+            a.vpc = vpc;
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            cfg.gridDim = dim3((unsigned)(T * cs));
+            cfg.blockDim = dim3((unsigned)vpc);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = static_cast<cudaStream_t>(stream);
+            void *args[] = {&a};
+            cudaError_t e = cudaLaunchKernelExC(&cfg, kr.fn, args);
+            if (e != cudaSuccess) return cuda_fail(e, "depth_read_decode launch");
+            return ATTNRES_OK;
+        }
+    }
 
     // Tensor-core path: bf16, <= 4 queries, d = 1024/2048/4096, heads that are
     // whole multiples of the per-warp channel slice.  <= 8 sources: d = 4096
@@ -766,7 +825,7 @@ void attnres_debug_set_wait_timeout_ns(uint64_t ns) {
 void attnres_debug_set_stall_injection(int enable) { g_inject_stall.store(enable ? 1 : 0); }
 
 void attnres_debug_set_kernel_variant(int variant) {
-    g_kernel_variant.store(variant == 1 || variant == 2 ? variant : 0);
+    g_kernel_variant.store(variant >= 1 && variant <= 3 ? variant : 0);
 }
 
 const char *attnres_version(void) { return "attnres 0.1.0 sm_103a"; }

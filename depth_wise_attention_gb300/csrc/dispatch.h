@@ -27,6 +27,9 @@ bool lookup_depth_read_mma2(int nq, int ks, int nw, KernelRef *out);
 // depth_read_mma_multi_kernel<nq, ks, nw>: > 8 sources in chunks of 8 (online softmax)
 bool lookup_depth_read_mma_multi(int nq, int ks, int nw, KernelRef *out);
 
+// depth_read_decode_kernel<T, nq, ns>: one token per cluster of CTAs (few tokens)
+bool lookup_depth_read_decode(int dt, int nq, int ns, KernelRef *out);
+
 // read_bwd_kernel<T, nq, ns, vpt> (nq queries, at most ns sources) and the
 // workspace reduction kernel that finishes dq and dgain
 bool lookup_read_bwd(int dt, int nq, int ns, int vpt, KernelRef *out);

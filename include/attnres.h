@@ -355,13 +355,16 @@ void attnres_debug_set_stall_injection(int enable);
 
 /*
  * Kernel selection, meant for tests and measurements: 0 (default) lets the
- * library pick (tensor-core kernels for bf16 reads with <= 4 queries at
- * d = 1024, 2048 or 4096 and <= 8 sources, and at d = 4096 for more sources
- * where the chunked tensor-core kernel was measured faster; the general
- * CUDA-core kernel otherwise); 1 forces the general kernel for Full / phase 1
- * / MHAR; 2 takes the tensor-core kernels wherever they apply (the chunked
- * one for any source count > 8 at d = 4096).  All compute the same
- * operation.  Applies to calls made afterwards; other values act as 0.
+ * library pick (for one head and at most 64 tokens the few-token kernel, a
+ * token per cluster of CTAs, when it applies; else tensor-core kernels for
+ * bf16 reads with <= 4 queries at d = 1024, 2048 or 4096 and <= 8 sources,
+ * and at d = 4096 for more sources where the chunked tensor-core kernel was
+ * measured faster; the general CUDA-core kernel otherwise); 1 forces the
+ * general kernel for Full / phase 1 / MHAR; 2 takes the tensor-core kernels
+ * wherever they apply (the chunked one for any source count > 8 at d = 4096);
+ * 3 takes the few-token kernel wherever it applies (one head, <= 16 sources
+ * with <= 2 queries or <= 8 with 4, any number of tokens).  All compute the
+ * same operation.  Applies to calls made afterwards; other values act as 0.
  */
 void attnres_debug_set_kernel_variant(int variant);
 

@@ -534,9 +534,10 @@ def test_empty_sequence_is_a_no_op():
 
 def test_stall_injection_reports_timeout_and_context_survives():
     """A kernel whose copies never arrive gives up after the wait limit,
-    records a timeout, and leaves the context usable."""
+    records a timeout, and leaves the context usable (T above the few-token
+    kernel's range, which loads without copies and waits)."""
     rng = _rng(23)
-    T, d = 64, 2048
+    T, d = 200, 2048
     src_h = _sources(rng, 8, T, d, BF16)
     q_h = _queries(rng, 4, d)
     src, q = to_dev(src_h, BF16), to_dev(q_h, F32)
@@ -564,10 +565,11 @@ def test_stall_injection_reports_timeout_and_context_survives():
 
 # --------------------------------------------------------------- both kernels
 
-@pytest.fixture(params=[0, 1], ids=["auto", "general"])
+@pytest.fixture(params=[0, 1, 2, 3], ids=["auto", "general", "tensor", "decode"])
 def kernel_variant(request):
-    """Runs a test with the automatic kernel choice (tensor-core kernel where it
-    applies) and with the general CUDA-core kernel forced."""
+    """Runs a test with the automatic kernel choice, with the general CUDA-core
+    kernel forced, with the tensor-core kernels wherever they apply and with the
+    few-token (cluster per token) kernel wherever it applies."""
     attnres.attnres_debug_set_kernel_variant(request.param)
     yield request.param
     attnres.attnres_debug_set_kernel_variant(0)
@@ -599,7 +601,7 @@ def test_mhar_both_kernels(kernel_variant, H, d, T, n_src):
     check_lse(lse, rl)
 
 
-@pytest.fixture(params=[0, 1, 2], ids=["auto", "general", "tensor"])
+@pytest.fixture(params=[0, 1, 2, 3], ids=["auto", "general", "tensor", "decode"])
 def kernel_variant3(request):
     """kernel_variant plus 2: the tensor-core kernels wherever they apply (the
     chunked one for every source count > 8 at d = 4096)."""
@@ -638,6 +640,25 @@ def test_chunked_read_keeps_non_finite_tokens_apart(kernel_variant3):
     out = to_host(attnres.attnres_full_fwd(to_dev(src, BF16), to_dev(w, F32), None, 1e-6))
     good = np.setdiff1d(np.arange(T), bad)
     check_out(out[good], oracle.full(np.ascontiguousarray(src[:, good]), w, None, 1e-6), BF16)
+
+
+@pytest.mark.parametrize("n_src,n_q,T,d,dtype", [(8, 4, 1, 4096, BF16), (16, 1, 3, 4096, BF16), (16, 2, 64, 2048, BF16),
+                                                 (5, 3, 9, 1024, F32), (1, 1, 2, 256, BF16), (8, 1, 500, 4096, BF16),
+                                                 (12, 1, 7, 512, F32)])
+def test_decode_kernel(n_src, n_q, T, d, dtype):
+    """The few-token kernel (a token per cluster of CTAs), forced for any T."""
+    rng = _rng(n_src * 11 + n_q + T + d)
+    src = _sources(rng, n_src, T, d, dtype, step=0.25)
+    q = _queries(rng, n_q, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    attnres.attnres_debug_set_kernel_variant(3)
+    try:
+        o, lse = attnres.attnres_block_phase1(to_dev(src, dtype), to_dev(q, F32), to_dev(g, F32), 1e-6)
+    finally:
+        attnres.attnres_debug_set_kernel_variant(0)
+    ro, rl = oracle.block_phase1(src, q, g, 1e-6)
+    check_out(o, ro, dtype, np.abs(src).max(), what="o")
+    check_lse(lse, rl)
 
 
 def test_kernels_agree_closely():
