@@ -83,6 +83,24 @@ __global__ void __launch_bounds__(P2_THREADS, VPT <= 2 ? (UPD || MH ? 2 : 3) : 1
         }
     }
 
+    // MH, heads of whole warps: for each of this thread's heads j and vector
+    // slot k2, the warps [wlo, whi) of the row whose slot-k2 vectors lie in
+    // head hk[j] (every bound a multiple of 32 vectors, so exact)
+    int wlo[NR][NR], whi[NR][NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j)
+#pragma unroll
+        for (int k2 = 0; k2 < NR; ++k2) {
+            if (MH) {
+                const int lo = (hk[j] * a.seg - k2 * a.tpr) / 32, hi = ((hk[j] + 1) * a.seg - k2 * a.tpr) / 32;
+                wlo[j][k2] = lo < 0 ? 0 : (lo > nwr ? nwr : lo);
+                whi[j][k2] = hi < 0 ? 0 : (hi > nwr ? nwr : hi);
+            } else {
+                wlo[j][k2] = 0;
+                whi[j][k2] = nwr;
+            }
+        }
+
     // Software pipeline over this CTA's tiles: the loads of tile n+1 are in
     // flight while tile n is reduced, merged and stored.
     uint4 ov[VPT], pv[VPT], fv[UPD ? VPT : 1];
@@ -178,12 +196,12 @@ __global__ void __launch_bounds__(P2_THREADS, VPT <= 2 ? (UPD || MH ? 2 : 3) : 1
                 tss[j] = 0.f;
                 tdt[j] = 0.f;
                 // every (vector slot, warp) of this row whose head is head j's
+#pragma unroll
                 for (int k2 = 0; k2 < NR; ++k2)
-                    for (int w = 0; w < nwr; ++w)
-                        if (!MH || (k2 * a.tpr + 32 * w) / a.seg == hk[j]) {
-                            tss[j] += red[buf][r * nwr + w][k2][0];
-                            tdt[j] += red[buf][r * nwr + w][k2][1];
-                        }
+                    for (int w = wlo[j][k2]; w < whi[j][k2]; ++w) {
+                        tss[j] += red[buf][r * nwr + w][k2][0];
+                        tdt[j] += red[buf][r * nwr + w][k2][1];
+                    }
             }
         } else {
 #pragma unroll
