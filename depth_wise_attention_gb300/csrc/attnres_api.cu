@@ -229,9 +229,10 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     }
 
     // Tensor-core path: bf16, <= 4 queries, d = 1024/2048/4096, heads that are
-    // whole multiples of the per-warp channel slice.  <= 8 sources: d = 4096
-    // one token per item (16 warps x 256 channels), d <= 2048 two tokens per
-    // item (16 warps x d/16 channels), which fills all 16 MMA rows.
+    // whole multiples of the per-warp channel slice.  <= 8 sources: one token
+    // per item with 256 channels per warp at d = 4096 (16 warps) and d = 2048
+    // (8 warps, two CTAs per SM); d = 1024 two tokens per item (8 warps x 128
+    // channels), which fills all 16 MMA rows.
     // > 8 sources: one token per item, its sources in chunks of 8 folded in by
     // an online softmax.  An item costs about the same whatever its rows, so
     // the chunked kernel only beats the general kernel's 4-source chunks (two
@@ -243,8 +244,8 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     const bool chunked_wins = n_src >= 24 && (n_src % 8 == 0 || n_src % 8 >= 5);
     if (dt == ATTNRES_BF16 && n_q <= 4 && (d == 1024 || d == 2048 || d == 4096) && kv != 1 &&
         (!chunked || (d == 4096 && (chunked_wins || kv == 2)))) {
-        const bool two = !chunked && d <= 2048;
-        const int nw = d == 1024 ? 8 : 16;
+        const bool two = !chunked && d <= 1024;
+        const int nw = d <= 2048 ? 8 : 16;
         const int ks = (int)(d / (16 * nw));
         const int rows = two ? 16 : 8;
         const int nq2 = pow2ceil((int)n_q);
@@ -262,6 +263,9 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
             if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
             int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
             if (nstages > DM_MAX_STAGES) nstages = DM_MAX_STAGES;
+            // d = 2048: three stages, so that two CTAs share an SM (measured
+            // 10-16% faster than one CTA with more stages or two tokens per item)
+            if (d == 2048 && !chunked && nstages > 3) nstages = 3;
             if (nstages >= 2) {
                 const size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
                 int occ = 0;

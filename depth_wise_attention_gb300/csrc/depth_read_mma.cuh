@@ -281,8 +281,11 @@ __device__ __forceinline__ void dm_rescale(float (&c)[4], float2 f) {
     c[0] = a.x; c[1] = a.y; c[2] = b.x; c[3] = b.y;
 }
 
+// With 8 warps (d = 2048) two CTAs share an SM (three 32 KB stages each, at
+// most 128 registers a thread), so one CTA's per-token chain hides behind the
+// other's; with 16 warps (d = 4096) the stages need the whole SM.
 template <int NQ, int KS, int NW>
-__global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthReadMmaArgs a) {
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) depth_read_mma_kernel(const DepthReadMmaArgs a) {
     static_assert(NQ <= 4, "at most 4 queries (8 MMA columns: hi and lo per query)");
     using L = DMLayout;
     constexpr int CW = KS * 16;                 // channels per warp
@@ -457,8 +460,8 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_kernel(const DepthR
 }
 
 
-// Two tokens per item (d <= 2048, where two tokens' 8 source rows fit one
-// 64 KB stage).  Pass 1 uses all 16 MMA rows (token 0's sources in rows 0..7,
+// Two tokens per item (d = 1024, where two tokens' 8 source rows fit one
+// 33 KB stage).  Pass 1 uses all 16 MMA rows (token 0's sources in rows 0..7,
 // token 1's in rows 8..15); the two tokens' softmaxes run as independent
 // chains; the per-item barrier, softmax latency and bulk stores are paid
 // once per two tokens.  Stage row tok*8 + i holds source i of token tok.
