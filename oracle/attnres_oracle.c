@@ -419,6 +419,54 @@ int oracle_mhar_phase2(const double *o, const double *lse, const double *partial
     return 0;
 }
 
+/* Backward of oracle_mhar.  [MHAR abstract]: each head is its own read over
+ * its slice of the channels (the read is block-diagonal), so the gradient of
+ * head h depends only on that slice of the sources, of the output gradient,
+ * of the query and of the gain.  Every head's slice is gathered into
+ * contiguous arrays, differentiated by oracle_read_bwd with d/H channels, and
+ * the gradients are scattered back into their slices.
+ * src[n_src][T][d], queries[n_q][H][d/H], dout[n_q][T][d]; outputs
+ * dsrc[n_src][T][d], dq[n_q][H][d/H], dg[d]. */
+int oracle_mhar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t H,
+                    const double *queries, int64_t n_q, const double *gain, double eps,
+                    const double *dout, double *dsrc, double *dq, double *dg)
+{
+    if (!src || !queries || !dout || !dsrc || !dq || !dg || n_src < 1 || n_q < 1 || T < 0 || d < 1 ||
+        H < 1 || d % H || eps < 0)
+        return -1;
+    const int64_t dh = d / H;
+    double *s_h = (double *)malloc(sizeof(double) * (size_t)(n_src * T * dh + 1));
+    double *w_h = (double *)malloc(sizeof(double) * (size_t)(n_q * dh));
+    double *g_h = (double *)malloc(sizeof(double) * (size_t)dh);
+    double *do_h = (double *)malloc(sizeof(double) * (size_t)(n_q * T * dh + 1));
+    double *ds_h = (double *)malloc(sizeof(double) * (size_t)(n_src * T * dh + 1));
+    double *dq_h = (double *)malloc(sizeof(double) * (size_t)(n_q * dh));
+    double *dg_h = (double *)malloc(sizeof(double) * (size_t)dh);
+    int rc = (s_h && w_h && g_h && do_h && ds_h && dq_h && dg_h) ? 0 : -1;
+    for (int64_t hd = 0; hd < H && rc == 0; ++hd) {
+        const int64_t c0 = hd * dh;
+        for (int64_t i = 0; i < n_src; ++i)
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t c = 0; c < dh; ++c) s_h[(i * T + t) * dh + c] = src[(i * T + t) * d + c0 + c];
+        for (int64_t q = 0; q < n_q; ++q) {
+            for (int64_t c = 0; c < dh; ++c) w_h[q * dh + c] = queries[q * d + c0 + c];
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t c = 0; c < dh; ++c) do_h[(q * T + t) * dh + c] = dout[(q * T + t) * d + c0 + c];
+        }
+        for (int64_t c = 0; c < dh; ++c) g_h[c] = gain ? gain[c0 + c] : 1.0;
+        rc = oracle_read_bwd(s_h, n_src, T, dh, w_h, n_q, g_h, eps, do_h, ds_h, dq_h, dg_h);
+        if (rc) break;
+        for (int64_t i = 0; i < n_src; ++i)
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t c = 0; c < dh; ++c) dsrc[(i * T + t) * d + c0 + c] = ds_h[(i * T + t) * dh + c];
+        for (int64_t q = 0; q < n_q; ++q)
+            for (int64_t c = 0; c < dh; ++c) dq[q * d + c0 + c] = dq_h[q * dh + c];
+        for (int64_t c = 0; c < dh; ++c) dg[c0 + c] = dg_h[c];
+    }
+    free(s_h); free(w_h); free(g_h); free(do_h); free(ds_h); free(dq_h); free(dg_h);
+    return rc;
+}
+
 /* ---------------------------------------------------------------------- */
 /* MSAR                                                                    */
 /* ---------------------------------------------------------------------- */

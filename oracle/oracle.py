@@ -54,6 +54,8 @@ def _load():
                                                    ctypes.c_double, _D, _D]
         lib.oracle_mhar_phase2.argtypes = [_D, _D, _D, _I64, _I64, _I64, _D, _D, ctypes.c_double, _D]
         lib.oracle_read_bwd.argtypes = [_D, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double, _D, _D, _D, _D]
+        lib.oracle_mhar_bwd.argtypes = [_D, _I64, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double, _D, _D, _D,
+                                        _D]
         lib.oracle_mhar.argtypes = [_D, _I64, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double,
                                     _D, _D]
         lib.oracle_msar_conv.argtypes = [_D, _I64, _I64, _I64, _D, _D]
@@ -62,7 +64,7 @@ def _load():
                                     _D, _D]
         for f in ("oracle_full", "oracle_weighted_sum", "oracle_block_oneshot",
                   "oracle_block_phase1", "oracle_block_phase2", "oracle_block_phase2_update",
-                  "oracle_mhar_phase2", "oracle_read_bwd", "oracle_mhar",
+                  "oracle_mhar_phase2", "oracle_read_bwd", "oracle_mhar_bwd", "oracle_mhar",
                   "oracle_msar_conv", "oracle_msar"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -195,6 +197,22 @@ def read_bwd(src, queries, dout, gain=None, eps=1e-6):
     dg = np.empty(d)
     _check(_load().oracle_read_bwd(_p(src), n_src, T, d, _p(queries), n_q, _p(gain), float(eps), _p(dout),
                                    _p(dsrc), _p(dq), _p(dg)), "oracle_read_bwd")
+    return dsrc, dq, dg
+
+
+def mhar_bwd(src, queries, dout, gain=None, eps=1e-6):
+    """Backward of the MHAR read of queries [n_q,H,d/H] over src [n_src,T,d]
+    for output gradients dout [n_q,T,d] -> (dsrc [n_src,T,d],
+    dq [n_q,H,d/H], dgain [d])."""
+    src, queries, dout, gain = _f64(src), _f64(queries), _f64(dout), _f64(gain)
+    n_src, T, d = src.shape
+    n_q, H, dh = queries.shape
+    assert H * dh == d
+    dsrc = np.empty((n_src, T, d))
+    dq = np.empty((n_q, H, dh))
+    dg = np.empty(d)
+    _check(_load().oracle_mhar_bwd(_p(src), n_src, T, d, H, _p(queries), n_q, _p(gain), float(eps), _p(dout),
+                                   _p(dsrc), _p(dq), _p(dg)), "oracle_mhar_bwd")
     return dsrc, dq, dg
 
 

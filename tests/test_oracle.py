@@ -365,6 +365,69 @@ def test_read_bwd_score_path_is_orthogonal_to_the_source_at_zero_eps():
     assert np.abs(score_part).max() > 1e-3
 
 
+def _fd_grads_mhar(src, q, g, dout, eps, h=1e-6):
+    """Central finite differences of L = sum(dout * out) through the MHAR
+    forward oracle; q is [n_q, H, d/H]."""
+    def loss(s_, q_, g_):
+        return float((oracle.mhar(s_, q_, g_, eps) * dout).sum())
+    out = []
+    for x, put in ((src, lambda v: (v, q, g)), (q, lambda v: (src, v, g)), (g, lambda v: (src, q, v))):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            a, b = x.copy(), x.copy()
+            a[idx] += h
+            b[idx] -= h
+            fd[idx] = (loss(*put(a)) - loss(*put(b))) / (2 * h)
+        out.append(fd)
+    return out
+
+
+@pytest.mark.parametrize("n_src,n_q,H,eps", [(3, 1, 2, 1e-6), (4, 2, 4, 0.05), (2, 3, 3, 0.0)])
+def test_mhar_bwd_matches_finite_differences(n_src, n_q, H, eps):
+    """The MHAR backward against central differences of the (pinned) MHAR
+    forward oracle: per-head RMSNorm, softmax and slice of the gain."""
+    rng = np.random.default_rng(41 + n_src + 7 * H)
+    T, dh = 2, 4
+    d = H * dh
+    src = _rand(rng, n_src, T, d) * (1 + np.arange(n_src))[:, None, None]
+    q = _rand(rng, n_q, H, dh, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d)
+    dout = _rand(rng, n_q, T, d)
+    dsrc, dq, dg = oracle.mhar_bwd(src, q, dout, g, eps)
+    fs, fq, fg = _fd_grads_mhar(src, q, g, dout, eps)
+    for got, ref in ((dsrc, fs), (dq, fq), (dg, fg)):
+        assert np.abs(got - ref).max() <= 1e-6 * max(1.0, np.abs(ref).max())
+
+
+def test_mhar_bwd_one_head_is_the_read_backward():
+    """H = 1 recovers the single-head read ([MHAR abstract]), so its backward
+    is the read's backward."""
+    rng = np.random.default_rng(43)
+    src, q, dout = _rand(rng, 5, 3, 16), _rand(rng, 2, 16), _rand(rng, 2, 3, 16)
+    g = rng.uniform(0.5, 1.5, 16)
+    a = oracle.mhar_bwd(src, q[:, None, :], dout, g, 1e-6)
+    b = oracle.read_bwd(src, q, dout, g, 1e-6)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1][:, 0], b[1]) and np.array_equal(a[2], b[2])
+
+
+def test_mhar_bwd_is_block_diagonal():
+    """An output gradient on head h's slice alone gives gradients on that
+    slice alone: the other slices of the sources, the queries and the gain get
+    exactly zero."""
+    rng = np.random.default_rng(44)
+    n_src, T, H, dh = 4, 3, 4, 6
+    d = H * dh
+    src, q = _rand(rng, n_src, T, d), _rand(rng, 2, H, dh)
+    dout = np.zeros((2, T, d))
+    dout[:, :, 2 * dh:3 * dh] = _rand(rng, 2, T, dh)
+    dsrc, dq, dg = oracle.mhar_bwd(src, q, dout, rng.uniform(0.5, 1.5, d), 1e-6)
+    off = np.ones(d, dtype=bool)
+    off[2 * dh:3 * dh] = False
+    assert np.abs(dsrc[:, :, off]).max() == 0.0 and np.abs(dg[off]).max() == 0.0
+    assert np.abs(np.delete(dq, 2, axis=1)).max() == 0.0
+    assert np.abs(dsrc[:, :, ~off]).max() > 1e-3 and np.abs(dq[:, 2]).max() > 1e-3
+
+
 # --------------------------------------------------------------------------
 # MHAR
 # --------------------------------------------------------------------------

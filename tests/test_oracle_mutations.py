@@ -32,6 +32,11 @@ MUTANTS = {
     "bwd_rms_term_sign": [("dv[c] += gc * dk[c] / r[i] - v[c] * gdkv", "dv[c] += gc * dk[c] / r[i] + v[c] * gdkv")],
     "bwd_gain_grad_not_normalised": [("dg[c] += dk[c] * v[c] / r[i];", "dg[c] += dk[c] * v[c];")],
     "bwd_value_path_first_query_weights": [("dv[c] += a[q * n_src + i] * dh[c];", "dv[c] += a[i] * dh[c];")],
+    "mhar_bwd_gain_not_sliced": [("for (int64_t c = 0; c < dh; ++c) g_h[c] = gain ? gain[c0 + c] : 1.0;",
+                                  "for (int64_t c = 0; c < dh; ++c) g_h[c] = gain ? gain[c] : 1.0;")],
+    "mhar_bwd_dout_of_first_head": [("do_h[(q * T + t) * dh + c] = dout[(q * T + t) * d + c0 + c];",
+                                     "do_h[(q * T + t) * dh + c] = dout[(q * T + t) * d + c];")],
+    "mhar_bwd_query_grad_unsliced": [("dq[q * d + c0 + c] = dq_h[q * dh + c];", "dq[q * d + c] = dq_h[q * dh + c];")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
