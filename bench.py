@@ -10,7 +10,7 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|msar|full_depth|
-block_d2048|block_fused|read_bwd|decode) are for profiling and the design notes.
+block_d2048|block_fused|read_bwd|mhar_bwd|decode) are for profiling and the design notes.
 """
 from __future__ import annotations
 
@@ -41,6 +41,7 @@ KERNEL_SOURCES = {
     "phase2": [CSRC + "phase2.cuh", CSRC + "common.cuh", CSRC + "kernels_phase2.cu"],
     "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
+    "read_bwd_mh": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu", CSRC + "kernels_bwd_mh.cu"],
     "depth_read_decode": [CSRC + "depth_read_decode.cuh", CSRC + "common.cuh", CSRC + "kernels_decode.cu"],
 }
 
@@ -420,6 +421,64 @@ class ReadBwdWorkload(BlockWorkload):
         return src.shape[1]
 
 
+class MharBwdWorkload(ReadBwdWorkload):
+    """Backward of the MHAR read at the MHAR workload's sizes: 4 queries of
+    H=8 heads over N=8 sources, bf16, d=4096: the sources', the queries' and
+    the gain's gradients for a given output gradient.  The kernel takes the
+    queries in two passes of two (the second adds into the source
+    gradients); the algorithmic bytes are one pass's: read the sources and
+    the 4 output gradients, write the sources' gradients."""
+
+    def __init__(self, T=131072, d=4096, N=8, H=8, n_q=4, seed=0):
+        BlockWorkload.__init__(self, T, d, N, 4, seed, name="mhar_read_backward")
+        b = 2
+        self.H, self.n_q = H, n_q
+        self.bytes_per_token = (2 * N + n_q) * d * b
+        self.phase1_bytes_per_token = self.bytes_per_token
+        self.launches_per_step = 2 * ((n_q + 1) // 2)   # per pass: streaming kernel + reduction
+        self.dominant = "mhar read backward (read_bwd_kernel per-head passes + reductions)"
+        self.dominant_src = "read_bwd_mh"
+        self.profile_tag = f"ncu_mhar_bwd_d{d}_H{H}"
+
+    def config(self):
+        c = BlockWorkload.config(self)
+        c["workload"] = f"{self.name} bf16 d={self.d} H={self.H} n_src={self.N} n_q={self.n_q} T={self.T}"
+        c.pop("S", None)
+        c["H"], c["n_q"] = self.H, self.n_q
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres, inputs
+        T, d, N, H, n_q = self.T, self.d, self.N, self.H, self.n_q
+        self.src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=self.seed, device=device)
+        self.src = self.src.view(N, T, d)
+        self.queries = inputs.device_normal((n_q, H, d // H), (16.0 / (d // H)) ** 0.5, g, device=device)
+        self.gain = torch.ones((d,), dtype=torch.float32, device=device)
+        self.dout = torch.randn((n_q, T, d), generator=g, device=device).to(torch.bfloat16)
+        self.dsrc = torch.empty_like(self.src)
+        self.dq = torch.empty((n_q, H, d // H), dtype=torch.float32, device=device)
+        self.dg = torch.empty((d,), dtype=torch.float32, device=device)
+        nb = attnres.mhar_read_bwd_workspace_size(N, T, d, H, n_q, torch.bfloat16)
+        self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+        self.cache = self.src
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.mhar_read_bwd(self.src, self.queries, self.dout, self.gain, 1e-6, dsrc=self.dsrc,
+                              dqueries=self.dq, dgain=self.dg, workspace=self.ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        src, q, dout = sample
+        oracle.mhar_bwd(src, q, dout, None, 1e-6)
+        return src.shape[1]
+
+
 class DecodeWorkload(BlockWorkload):
     """Decode-shaped Block AttnRes two-phase forward: a block (phase 1 + 3
     merges) over T=16 tokens, bf16, d=4096, N=8, S=4.  Each step reads its own
@@ -723,6 +782,8 @@ def make_workload(name, T=None):
         return DecodeWorkload(T=T or 16)
     if name == "read_bwd":
         return ReadBwdWorkload(T=T or 32768)
+    if name == "mhar_bwd":
+        return MharBwdWorkload(T=T or 131072)
     if name == "block_fused":
         return BlockFusedWorkload(T=T or 32768)
     if name == "full_depth":
@@ -971,7 +1032,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "block_fused", "read_bwd", "decode", "mhar", "msar",
+                    choices=["block", "block_d2048", "block_fused", "read_bwd", "mhar_bwd", "decode", "mhar", "msar",
                              "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)

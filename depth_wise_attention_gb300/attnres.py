@@ -37,6 +37,9 @@ _SIGS = {
     "attnres_read_bwd_noalloc": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _i64,
                                  ctypes.c_int, _vp, _vp, _vp],
     "attnres_read_bwd_workspace_size": [_i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+    "mhar_read_bwd": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _i64,
+                      ctypes.c_int, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "mhar_read_bwd_workspace_size": [_i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
     "mhar_fwd": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp,
                  _vp],
     "msar_expand_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
@@ -256,6 +259,42 @@ def attnres_read_bwd_noalloc(src, queries, dout, gain=None, eps=1e-6, dsrc=None,
     _check("attnres_read_bwd_noalloc", load().attnres_read_bwd_noalloc(
         _p(src), n_src, stride, T, d, _dt(src), _p(queries), n_q, _p(gain), eps, _p(dout), _p(dsrc), dstride,
         1 if accumulate else 0, _p(dqueries), _p(dgain), _stream(stream)))
+    return dsrc, dqueries, dgain
+
+
+def mhar_read_bwd_workspace_size(n_src, T, d, H, n_q, dtype):
+    import torch
+    n = ctypes.c_size_t(0)
+    dt = BF16 if dtype == torch.bfloat16 else F32
+    _check("mhar_read_bwd_workspace_size",
+           load().mhar_read_bwd_workspace_size(n_src, T, d, H, n_q, dt, ctypes.byref(n)))
+    return n.value
+
+
+def mhar_read_bwd(src, queries, dout, gain=None, eps=1e-6, dsrc=None, accumulate=False, dqueries=None,
+                  dgain=None, want_dgain=True, workspace=None, stream=None):
+    """Backward of the MHAR read of queries [n_q,H,d/H] over src [n_src,T,d]
+    for output gradients dout [n_q,T,d] -> (dsrc, dqueries [n_q,H,d/H],
+    dgain).  The workspace is allocated here unless given."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    n_q, H, dh = queries.shape
+    if H * dh != d:
+        raise ValueError("queries must be [n_q, H, d/H]")
+    if dsrc is None:
+        dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=src.device)
+    _, _, _, dstride = _src_geometry(dsrc)
+    if dqueries is None:
+        dqueries = torch.empty((n_q, H, dh), dtype=torch.float32, device=src.device)
+    if dgain is None and want_dgain:
+        dgain = torch.empty((d,), dtype=torch.float32, device=src.device)
+    if workspace is None:
+        nbytes = mhar_read_bwd_workspace_size(n_src, T, d, H, n_q, src.dtype)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=src.device)
+    _check("mhar_read_bwd", load().mhar_read_bwd(
+        _p(src), n_src, stride, T, d, H, _dt(src), _p(queries), n_q, _p(gain), eps, _p(dout), _p(dsrc), dstride,
+        1 if accumulate else 0, _p(dqueries), _p(dgain), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return dsrc, dqueries, dgain
 
 

@@ -29,6 +29,7 @@ SOURCES = [
     "kernels_mma.cu",
     "kernels_mma_multi.cu",
     "kernels_bwd.cu",
+    "kernels_bwd_mh.cu",
     "kernels_decode.cu",
     "msar.cu",
 ]

@@ -493,37 +493,59 @@ attnres_status_t launch_phase2(const void *o, const float *lse, const void *part
 // Backward of the read: tile shape, workspace size and launch.
 struct ReadBwdShape {
     int tpr, vpt, tt, ns;
+    int nqc;        // queries per kernel pass (more queries take several passes)
+    bool mh;        // per-head mode (H > 1)
+    int hg;         // reduction groups per warp in per-head mode
+    int vph;        // 16-byte vectors per head
 };
 
-attnres_status_t read_bwd_shape(int64_t n_src, int64_t d, int64_t n_q, attnres_dtype_t dt, ReadBwdShape *sh) {
+attnres_status_t read_bwd_shape(int64_t n_src, int64_t d, int64_t n_q, int64_t H, attnres_dtype_t dt,
+                                ReadBwdShape *sh) {
     const int nvec = (int)(d / epv(dt));
+    sh->ns = n_src <= 8 ? 8 : 16;
+    if (n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    sh->nqc = sh->ns == 16 ? 1 : 2;
+    if (n_q < sh->nqc) sh->nqc = (int)n_q;
     row_shape(nvec, &sh->tpr, &sh->vpt);
     sh->tt = RB_THREADS / sh->tpr;
-    // a tile holds n_src + n_q rows of tt tokens and two stages must fit:
+    // a tile holds n_src + nqc rows of tt tokens and two stages must fit:
     // spread a token over more threads (fewer tokens per tile) until they do
-    const size_t rows = (size_t)(n_src + n_q) * (size_t)d * esize(dt);
+    const size_t rows = (size_t)(n_src + sh->nqc) * (size_t)d * esize(dt);
     while (2 * rows * (size_t)sh->tt + 8 * 1024 > kSmemBudget && sh->tpr < RB_THREADS && sh->vpt > 1) {
         sh->tpr *= 2;
         sh->vpt = pow2ceil((nvec + sh->tpr - 1) / sh->tpr);
         sh->tt = RB_THREADS / sh->tpr;
     }
-    sh->ns = n_src <= 8 ? 8 : 16;
-    if (n_q > 2 || sh->vpt > 4 || (sh->ns == 16 && n_q > 1) || n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    if (sh->vpt > 4) return ATTNRES_ERR_UNSUPPORTED;
+    sh->mh = H > 1;
+    sh->hg = 1;
+    sh->vph = nvec;
+    if (sh->mh) {
+        // heads of whole runs of 32 vectors; one group per warp when a head
+        // holds whole warps' worth of vectors, else one group per run
+        if ((d / H) % epv(dt) != 0) return ATTNRES_ERR_UNSUPPORTED;
+        sh->vph = nvec / (int)H;
+        if (sh->vph % (32 * sh->vpt) == 0) sh->hg = 1;
+        else if (sh->vph % 32 == 0) sh->hg = sh->vpt;
+        else return ATTNRES_ERR_UNSUPPORTED;
+    }
     return ATTNRES_OK;
 }
 
-// Per-(CTA, row) partials of U: one CTA per SM at most.
-size_t read_bwd_ws_bytes(int sms, const ReadBwdShape &sh, int64_t n_q, int64_t d) {
-    return (size_t)sms * (size_t)sh.tt * (size_t)n_q * (size_t)d * sizeof(float);
+// Per-(CTA, row) partials of U for one pass of queries: one CTA per SM at most.
+size_t read_bwd_ws_bytes(int sms, const ReadBwdShape &sh, int64_t d) {
+    return (size_t)sms * (size_t)sh.tt * (size_t)sh.nqc * (size_t)d * sizeof(float);
 }
 
 attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
-                                 attnres_dtype_t dt, const float *queries, int64_t n_q, const float *gain,
-                                 float eps, const void *dout, void *dsrc, int64_t dsrc_stride, int accumulate,
-                                 float *dq, float *dgain, void *ws, size_t ws_bytes, void *stream) {
+                                 int64_t H, attnres_dtype_t dt, const float *queries, int64_t n_q,
+                                 const float *gain, float eps, const void *dout, void *dsrc, int64_t dsrc_stride,
+                                 int accumulate, float *dq, float *dgain, void *ws, size_t ws_bytes,
+                                 void *stream) {
     attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
     if (st != ATTNRES_OK) return st;
     if (n_q < 1 || (accumulate != 0 && accumulate != 1)) return ATTNRES_ERR_INVALID_ARG;
+    if (H < 1 || d % H != 0) return ATTNRES_ERR_INVALID_ARG;
     if (T > 0 && (!queries || !dout || !dsrc || !dq || !ws)) return ATTNRES_ERR_INVALID_ARG;
     if (dsrc_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
     const size_t es = esize(dt);
@@ -537,7 +559,7 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         (dgain && (overlap(dgain, (size_t)d * 4, ws, ws_bytes) || overlap(dgain, (size_t)d * 4, dq, dq_bytes))))
         return ATTNRES_ERR_INVALID_ARG;
     ReadBwdShape sh;
-    st = read_bwd_shape(n_src, d, n_q, dt, &sh);
+    st = read_bwd_shape(n_src, d, n_q, H, dt, &sh);
     if (st != ATTNRES_OK) return st;
     if (!aligned16(dout) || !aligned16(dsrc) || (dsrc_stride * (int64_t)es) % 16 != 0 || !aligned16(queries) ||
         (gain && !aligned16(gain)) || !aligned4(dq) || (dgain && !aligned4(dgain)) || !aligned16(ws))
@@ -551,21 +573,31 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
     }
-    if (ws_bytes < read_bwd_ws_bytes(dev->sms, sh, n_q, d)) return ATTNRES_ERR_INVALID_ARG;
-    KernelRef kr;
-    if (!lookup_read_bwd(dt == ATTNRES_BF16 ? 1 : 0, (int)n_q, sh.ns, sh.vpt, &kr)) return ATTNRES_ERR_UNSUPPORTED;
+    if (ws_bytes < read_bwd_ws_bytes(dev->sms, sh, d)) return ATTNRES_ERR_INVALID_ARG;
+    // kernels of every pass (a last pass may take fewer queries)
+    KernelRef kr[2];
+    const int nq_last = (int)(n_q - (n_q - 1) / sh.nqc * sh.nqc);
+    for (int v = 0; v < 2; ++v) {
+        const int nq = v == 0 ? sh.nqc : nq_last;
+        const bool ok = sh.mh ? lookup_read_bwd_mh(dt == ATTNRES_BF16 ? 1 : 0, nq, sh.ns, sh.vpt, sh.hg, &kr[v])
+                              : lookup_read_bwd(dt == ATTNRES_BF16 ? 1 : 0, nq, sh.ns, sh.vpt, &kr[v]);
+        if (!ok) return ATTNRES_ERR_UNSUPPORTED;
+    }
     const uint32_t row_pitch = (uint32_t)((size_t)sh.tt * (size_t)d * es);
-    const uint32_t stage_bytes = (uint32_t)(((size_t)(n_src + n_q) * row_pitch + 127) / 128 * 128);
+    const uint32_t stage_bytes = (uint32_t)(((size_t)(n_src + sh.nqc) * row_pitch + 127) / 128 * 128);
     size_t budget = kSmemBudget;
     if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
-    if (budget <= kr.aux_smem) return ATTNRES_ERR_UNSUPPORTED;
-    int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
+    size_t aux = kr[0].aux_smem > kr[1].aux_smem ? kr[0].aux_smem : kr[1].aux_smem;
+    if (budget <= aux) return ATTNRES_ERR_UNSUPPORTED;
+    int nstages = (int)((budget - aux) / stage_bytes);
     if (nstages > RB_MAX_STAGES) nstages = RB_MAX_STAGES;
     if (nstages < 2) return ATTNRES_ERR_UNSUPPORTED;
-    const size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
-    int occ = 0;
-    st = prepare_kernel(kr.fn, smem, RB_THREADS, &occ);
-    if (st != ATTNRES_OK) return st;
+    const size_t smem = (size_t)nstages * stage_bytes + aux;
+    for (int v = 0; v < 2; ++v) {
+        int occ = 0;
+        st = prepare_kernel(kr[v].fn, smem, RB_THREADS, &occ);
+        if (st != ATTNRES_OK) return st;
+    }
     ReadBwdArgs a;
     a.src = static_cast<const unsigned char *>(src);
     a.src_stride_bytes = src_stride * (int64_t)es;
@@ -573,14 +605,10 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
     a.T = T;
     a.d = (int)d;
     a.nvec = (int)(d / epv(dt));
-    a.n_q = (int)n_q;
-    a.queries = queries;
     a.gain = gain;
     a.eps = eps;
-    a.dout = static_cast<const unsigned char *>(dout);
     a.dsrc = static_cast<unsigned char *>(dsrc);
     a.dsrc_stride_bytes = dsrc_stride * (int64_t)es;
-    a.accumulate = accumulate;
     a.ws = static_cast<float *>(ws);
     a.tpr = sh.tpr;
     a.tt = sh.tt;
@@ -588,24 +616,38 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
     a.stage_bytes = stage_bytes;
     a.row_pitch = row_pitch;
     a.ntiles = (T + sh.tt - 1) / sh.tt;
+    a.vph = sh.vph;
+    a.nheads = (int)H;
+    a.inv_dh = 1.f / (float)(d / H);
     a.wait = wait_cfg(dev);
     const int grid = (int)(a.ntiles < dev->sms ? a.ntiles : dev->sms);
-    void *args[] = {&a};
-    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(RB_THREADS), args, smem, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "read_bwd launch");
-    ReadBwdFinishArgs f;
-    f.ws = a.ws;
-    f.nparts = grid * sh.tt;
-    f.n_q = (int)n_q;
-    f.d = (int)d;
-    f.queries = queries;
-    f.gain = gain;
-    f.dq = dq;
-    f.dgain = dgain;
-    void *fargs[] = {&f};
-    const int fgrid = (int)((d + 255) / 256);
-    e = cudaLaunchKernel(read_bwd_finish_fn(), dim3(fgrid), dim3(256), fargs, 0, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "read_bwd finish launch");
+    // queries in passes of nqc: the source gradients and dgain add up over
+    // the passes (each query's terms are independent of the others')
+    for (int64_t q0 = 0; q0 < n_q; q0 += sh.nqc) {
+        const int nq = (int)(n_q - q0 < sh.nqc ? n_q - q0 : sh.nqc);
+        a.n_q = nq;
+        a.queries = queries + q0 * d;
+        a.dout = static_cast<const unsigned char *>(dout) + (size_t)q0 * (size_t)T * (size_t)d * es;
+        a.accumulate = q0 == 0 ? accumulate : 1;
+        void *args[] = {&a};
+        const void *fn = kr[nq == sh.nqc ? 0 : 1].fn;
+        cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(RB_THREADS), args, smem, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "read_bwd launch");
+        ReadBwdFinishArgs f;
+        f.ws = a.ws;
+        f.nparts = grid * sh.tt;
+        f.n_q = nq;
+        f.d = (int)d;
+        f.queries = a.queries;
+        f.gain = gain;
+        f.dq = dq + q0 * d;
+        f.dgain = dgain;
+        f.accumulate_dgain = q0 > 0 ? 1 : 0;
+        void *fargs[] = {&f};
+        const int fgrid = (int)((d + 255) / 256);
+        e = cudaLaunchKernel(read_bwd_finish_fn(), dim3(fgrid), dim3(256), fargs, 0, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "read_bwd finish launch");
+    }
     return ATTNRES_OK;
 }
 
@@ -730,19 +772,25 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
                          stream);
 }
 
-attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t n_q,
-                                                attnres_dtype_t dt, size_t *bytes) {
-    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || n_src < 1 || T < 0 || d < 1 || n_q < 1)
+static attnres_status_t read_bwd_workspace(int64_t n_src, int64_t T, int64_t d, int64_t H, int64_t n_q,
+                                           attnres_dtype_t dt, size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || n_src < 1 || T < 0 || d < 1 || n_q < 1 || H < 1 ||
+        d % H != 0)
         return ATTNRES_ERR_INVALID_ARG;
     if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
     ReadBwdShape sh;
-    attnres_status_t st = read_bwd_shape(n_src, d, n_q, dt, &sh);
+    attnres_status_t st = read_bwd_shape(n_src, d, n_q, H, dt, &sh);
     if (st != ATTNRES_OK) return st;
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != ATTNRES_OK) return st;
-    *bytes = read_bwd_ws_bytes(dev->sms, sh, n_q, d);
+    *bytes = read_bwd_ws_bytes(dev->sms, sh, d);
     return ATTNRES_OK;
+}
+
+attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t n_q,
+                                                attnres_dtype_t dt, size_t *bytes) {
+    return read_bwd_workspace(n_src, T, d, 1, n_q, dt, bytes);
 }
 
 attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
@@ -750,7 +798,7 @@ attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_st
                                   float eps, const void *dout, void *dsrc, int64_t dsrc_stride, int accumulate,
                                   float *dqueries, float *dgain, void *workspace, size_t workspace_bytes,
                                   void *stream) {
-    return launch_read_bwd(src, n_src, src_stride, T, d, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+    return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
                            accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
 }
 
@@ -768,8 +816,22 @@ attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_
     void *ws = nullptr;
     attnres_status_t st = bwd_scratch(&ws);
     if (st != ATTNRES_OK) return st;
-    return launch_read_bwd(src, n_src, src_stride, T, d, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+    return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
                            accumulate, dqueries, dgain, ws, kBwdScratchFloats * sizeof(float), stream);
+}
+
+attnres_status_t mhar_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t H, int64_t n_q,
+                                             attnres_dtype_t dt, size_t *bytes) {
+    return read_bwd_workspace(n_src, T, d, H, n_q, dt, bytes);
+}
+
+attnres_status_t mhar_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                               int64_t H, attnres_dtype_t dt, const float *queries, int64_t n_q,
+                               const float *gain, float eps, const void *dout, void *dsrc, int64_t dsrc_stride,
+                               int accumulate, float *dqueries, float *dgain, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    return launch_read_bwd(src, n_src, src_stride, T, d, H, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+                           accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
 }
 
 attnres_status_t msar_expand_fwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,

@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(256) read_bwd_finish_kernel(const ReadBwdFinis
             a.dq[(size_t)q * a.d + c] = g * u;
             dgc = fmaf(__ldg(a.queries + (size_t)q * a.d + c), u, dgc);
         }
-        if (a.dgain) a.dgain[c] = dgc;
+        if (a.dgain) a.dgain[c] = a.accumulate_dgain ? a.dgain[c] + dgc : dgc;
     }
 }
 

@@ -22,6 +22,14 @@
 // re-reads the stage, writes dv and accumulates U in registers.  Each CTA row
 // writes its U to the caller's workspace, and read_bwd_finish_kernel reduces
 // the workspace in a fixed order (deterministic) into dq and dgain.
+//
+// Per-head mode (MH, the backward of the MHAR read): every quantity above is
+// taken per head over the head's slice of channels (d becomes d/H in c_i).
+// Each warp then owns VPT runs of 32 consecutive vectors, so a run never
+// straddles a head when a head is a multiple of 32 vectors: with HG == 1 a
+// warp's VPT runs lie in one head and its values are reduced together; with
+// HG == VPT each run is its own group.  The coefficient lanes of a group sum
+// the table entries of all groups of its head.
 #pragma once
 
 #include "common.cuh"
@@ -53,16 +61,21 @@ struct ReadBwdArgs {
     uint32_t stage_bytes;
     uint32_t row_pitch;             // bytes of one tensor's tile rows in a stage (tt * d * esize)
     int64_t ntiles;
+    int vph;                        // 16-byte vectors per head (nvec for one head)
+    int nheads;
+    float inv_dh;                   // 1 / channels per head
     WaitCfg wait;
 };
 
-template <int NQ, int NS>
+template <int NQ, int NS, int HG = 1>
 struct RBLayout {
-    static constexpr int V = NS * (1 + 2 * NQ);             // values reduced per token row
-    static constexpr int R = Bfly<V>::R;
+    static constexpr int V = NS * (1 + 2 * NQ);             // values reduced per token row and group
+    static constexpr int R = Bfly<HG * V>::R;
     static constexpr size_t bar_bytes = 128;
-    static constexpr size_t red_floats = 2 * (RB_THREADS / 32) * V;   // [2][row][value][warp in row]
-    static constexpr size_t coef_floats = (RB_THREADS / 32) * NS * (2 * NQ + 1);  // per warp: alpha, b, c
+    // [2][row][value][group in row]
+    static constexpr size_t red_floats = 2 * (RB_THREADS / 32) * HG * V;
+    // per warp and group: alpha, b, c
+    static constexpr size_t coef_floats = (RB_THREADS / 32) * HG * NS * (2 * NQ + 1);
     static constexpr size_t aux_bytes = bar_bytes + 4 * (red_floats + coef_floats);
     // value index: sum of squares of source i, then (w_q*g).v_i, then dout_q.v_i
     __host__ __device__ static constexpr int iss(int i) { return i; }
@@ -70,14 +83,15 @@ struct RBLayout {
     __host__ __device__ static constexpr int isd(int q, int i) { return NS + NQ * NS + q * NS + i; }
 };
 
-template <typename Tin, int NQ, int NS, int VPT>
+template <typename Tin, int NQ, int NS, int VPT, bool MH = false, int HG = 1>
 __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdArgs a) {
     using E = Elem<Tin>;
-    using L = RBLayout<NQ, NS>;
+    using L = RBLayout<NQ, NS, HG>;
     constexpr int EPV = E::EPV;
     constexpr int NP = EPV / 2;
     constexpr int V = L::V, R = L::R;
     static_assert(NQ * NS <= 32, "one lane per (query, source) pair");
+    static_assert(HG == 1 || (MH && HG == VPT), "groups per warp: one, or one per run in per-head mode");
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *stages = smem;
@@ -128,14 +142,15 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
     // ------------------------------------------------------------ constants
     const int r = tid / a.tpr, tr = tid - r * a.tpr;
     const int wr = tr >> 5, nwr = a.tpr >> 5;
-    const float inv_d = 1.f / (float)a.d;
+    const int ngr = nwr * HG;     // reduction groups per token row
+    const float inv_d = a.inv_dh;
     int vid[VPT];
     bool vok[VPT];
     float2 wg[NQ][VPT][NP];       // w_q * g on this thread's channels
     float2 U[NQ][VPT][NP];        // sum over tokens of sum_i b_qi v_i
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-        vid[k] = k * a.tpr + tr;
+        vid[k] = MH ? (wr * VPT + k) * 32 + lane : k * a.tpr + tr;
         vok[k] = vid[k] < a.nvec;
 #pragma unroll
         for (int q = 0; q < NQ; ++q)
@@ -151,11 +166,29 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
                 U[q][k][p] = make_float2(0.f, 0.f);
             }
     }
-    int slot_idx[R];
+    // table offset of each value this lane holds after the butterfly: value
+    // jj of local group g goes to [jj][wr * HG + g] of the row's table
+    int slot_off[R];
 #pragma unroll
-    for (int j = 0; j < R; ++j) slot_idx[j] = bfly_slot<V>(lane, j);
-    float *cw = coef + (size_t)warp * NS * (2 * NQ + 1);   // [i][alpha_q..., b_q..., c]
+    for (int j = 0; j < R; ++j) {
+        const int idx = bfly_slot<HG * V>(lane, j);
+        const int g = idx / V, jj = idx - g * V;
+        slot_off[j] = idx >= 0 ? jj * ngr + wr * HG + g : -1;
+    }
     constexpr int CS = 2 * NQ + 1;
+    float *cw = coef + (size_t)warp * HG * NS * CS;   // [group][i][alpha_q..., b_q..., c]
+    // the table groups that make up the head of each of this warp's groups
+    int g_first[HG], g_count;
+    {
+        const int cv = 32 * VPT / HG;                  // vectors per group
+        g_count = MH ? a.vph / cv : nwr;
+#pragma unroll
+        for (int g = 0; g < HG; ++g) {
+            int h = MH ? (wr * HG + g) * cv / a.vph : 0;
+            if (h >= a.nheads) h = a.nheads - 1;       // a group past the row: computed, never used
+            g_first[g] = h * g_count;
+        }
+    }
 
     int s = 0;
     uint32_t par = 0;
@@ -181,55 +214,66 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
                     for (int p = 0; p < NP; ++p) dl[q][k][p] = make_float2(0.f, 0.f);
                 }
             }
-        float v[V];
+        float v[HG * V];
 #pragma unroll
         for (int i = 0; i < NS; ++i) {
-            float2 ss = make_float2(0.f, 0.f), sw[NQ], sd[NQ];
+            float2 ss[HG], sw[HG][NQ], sd[HG][NQ];
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) { sw[q] = make_float2(0.f, 0.f); sd[q] = make_float2(0.f, 0.f); }
+            for (int g = 0; g < HG; ++g) {
+                ss[g] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) { sw[g][q] = make_float2(0.f, 0.f); sd[g][q] = make_float2(0.f, 0.f); }
+            }
             if (i < a.n_src) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
                     if (!vok[k]) continue;
+                    constexpr int one = HG == 1 ? 1 : 0;
+                    const int g = one ? 0 : k;
                     float2 x[NP];
                     E::unpack(*reinterpret_cast<const uint4 *>(sb + (size_t)i * a.row_pitch + (size_t)vid[k] * 16), x);
 #pragma unroll
                     for (int p = 0; p < NP; ++p) {
-                        ss = ffma2(x[p], x[p], ss);
+                        ss[g] = ffma2(x[p], x[p], ss[g]);
 #pragma unroll
                         for (int q = 0; q < NQ; ++q) {
-                            sw[q] = ffma2(x[p], wg[q][k][p], sw[q]);
-                            sd[q] = ffma2(x[p], dl[q][k][p], sd[q]);
+                            sw[g][q] = ffma2(x[p], wg[q][k][p], sw[g][q]);
+                            sd[g][q] = ffma2(x[p], dl[q][k][p], sd[g][q]);
                         }
                     }
                 }
             }
-            v[L::iss(i)] = ss.x + ss.y;
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                v[L::isw(q, i)] = sw[q].x + sw[q].y;
-                v[L::isd(q, i)] = sd[q].x + sd[q].y;
+            for (int g = 0; g < HG; ++g) {
+                v[g * V + L::iss(i)] = ss[g].x + ss[g].y;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    v[g * V + L::isw(q, i)] = sw[g][q].x + sw[g][q].y;
+                    v[g * V + L::isd(q, i)] = sd[g][q].x + sd[g][q].y;
+                }
             }
         }
-        butterfly_reduce<V>(v, lane);
-        float *rrow = red + (size_t)(it & 1) * (RB_THREADS / 32) * V + (size_t)r * nwr * V;
+        butterfly_reduce<HG * V>(v, lane);
+        float *rrow = red + (size_t)(it & 1) * (RB_THREADS / 32) * HG * V + (size_t)r * ngr * V;
 #pragma unroll
         for (int j = 0; j < R; ++j)
-            if (slot_idx[j] >= 0) rrow[slot_idx[j] * nwr + wr] = v[j];
+            if (slot_off[j] >= 0) rrow[slot_off[j]] = v[j];
         __syncthreads();
         // every warp has finished item it-1: refill its stage for item it-1+nstages
         if (producer && it >= 1 && issued < n_items && !*abort_flag) { issue_next(); ++issued; }
 
-        // ---------------- per-token coefficients: lane (q, i) = q*NS + i
-        {
+        // ---------------- per-token coefficients: lane (q, i) = q*NS + i, for
+        // each group of this warp (its head's table groups summed)
+#pragma unroll
+        for (int g = 0; g < HG; ++g) {
             const int q = lane / NS, i = lane - q * NS;
             const bool pv = q < NQ && q < a.n_q && i < a.n_src;
             float ss = 0.f, sw = 0.f, sd = 0.f;
             if (q < NQ) {
-                for (int w = 0; w < nwr; ++w) {
-                    ss += rrow[L::iss(i) * nwr + w];
-                    sw += rrow[L::isw(q, i) * nwr + w];
-                    sd += rrow[L::isd(q, i) * nwr + w];
+                for (int w = g_first[g]; w < g_first[g] + g_count; ++w) {
+                    ss += rrow[L::iss(i) * ngr + w];
+                    sw += rrow[L::isw(q, i) * ngr + w];
+                    sd += rrow[L::isd(q, i) * ngr + w];
                 }
             }
             const float ms = fmaf(ss, inv_d, a.eps);
@@ -246,9 +290,10 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
             float cpart = -ds * sw * rinv * rinv * rinv * inv_d;
             if (NQ == 2) cpart += __shfl_xor_sync(0xffffffffu, cpart, NS);
             if (q < NQ) {
-                cw[i * CS + q] = alpha;
-                cw[i * CS + NQ + q] = b;
-                if (q == 0) cw[i * CS + 2 * NQ] = cpart;
+                float *cg = cw + g * NS * CS;
+                cg[i * CS + q] = alpha;
+                cg[i * CS + NQ + q] = b;
+                if (q == 0) cg[i * CS + 2 * NQ] = cpart;
             }
         }
         __syncwarp();
@@ -258,14 +303,21 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
 #pragma unroll
         for (int i = 0; i < NS; ++i) {
             if (i >= a.n_src || !row_ok) break;
-            float al[NQ], bq[NQ];
+            float alg[HG][NQ], bqg[HG][NQ], cig[HG];
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) { al[q] = cw[i * CS + q]; bq[q] = cw[i * CS + NQ + q]; }
-            const float ci = cw[i * CS + 2 * NQ];
-            const float2 c2 = make_float2(ci, ci);
+            for (int g = 0; g < HG; ++g) {
+                const float *cg = cw + g * NS * CS;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) { alg[g][q] = cg[i * CS + q]; bqg[g][q] = cg[i * CS + NQ + q]; }
+                cig[g] = cg[i * CS + 2 * NQ];
+            }
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 if (!vok[k]) continue;
+                constexpr int one = HG == 1 ? 1 : 0;
+                const int g = one ? 0 : k;
+                const float *al = alg[g], *bq = bqg[g];
+                const float2 c2 = make_float2(cig[g], cig[g]);
                 float2 x[NP], y[NP];
                 E::unpack(*reinterpret_cast<const uint4 *>(sb + (size_t)i * a.row_pitch + (size_t)vid[k] * 16), x);
 #pragma unroll
@@ -326,6 +378,7 @@ struct ReadBwdFinishArgs {
     const float *gain;
     float *dq;                      // [n_q][d]
     float *dgain;                   // [d] or nullptr
+    int accumulate_dgain;           // 1: dgain += (a later group of queries)
 };
 
 }  // namespace attnres

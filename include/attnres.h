@@ -219,7 +219,7 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  * with r_i = sqrt(mean(v_i^2) + eps) (a zero source with eps = 0 passes
  * nothing back through its score).
  *   src        [n_src][T][d], sources src_stride elements apart
- *   queries    [n_q][d] float, n_q = 1 or 2;  gain [d] float or NULL
+ *   queries    [n_q][d] float, n_q >= 1;  gain [d] float or NULL
  *   dout       [n_q][T][d] dtype dt
  *   dsrc       [n_src][T][d] dtype dt, sources dsrc_stride (>= T*d) elements
  *              apart; overwritten, or added to when accumulate = 1 (so the
@@ -231,9 +231,11 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  *              the tokens go through it and are reduced in a fixed order, so
  *              results are bitwise reproducible
  * No output may overlap an input or the workspace.  T = 0 zeroes dqueries and
- * dgain.  Limits: n_src <= 8 with 2 queries, <= 16 with 1; the n_src + n_q
- * rows of a token tile must fit two shared-memory stages (for d = 4096 bf16,
- * n_src + n_q <= 13).
+ * dgain.  The queries are taken in passes of 2 (of 1 with more than 8
+ * sources) over the sources; later passes add into dsrc and dgain, so with
+ * more than one pass a bf16 dsrc is rounded once per pass.  Limits:
+ * n_src <= 16; the n_src + (queries of a pass) rows of a token tile must fit
+ * two shared-memory stages (for d = 4096 bf16, n_src + 2 <= 13).
  */
 attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
                                   int64_t d, attnres_dtype_t dt, const float *queries, int64_t n_q,
@@ -244,8 +246,8 @@ attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_st
 
 /*
  * Workspace bytes attnres_read_bwd needs for these sizes on the current
- * device (an upper bound: one partial row of d floats per query for every
- * token row a CTA holds, one CTA per SM).  No device work is done.
+ * device (an upper bound: one partial row of d floats per query of a pass for
+ * every token row a CTA holds, one CTA per SM).  No device work is done.
  */
 attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t n_q,
                                                 attnres_dtype_t dt, size_t *bytes);
@@ -267,6 +269,34 @@ attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_
                                           float eps, const void *dout, void *dsrc,
                                           int64_t dsrc_stride, int accumulate, float *dqueries,
                                           float *dgain, void *stream);
+
+/*
+ * Backward of the MHAR read (mhar_fwd): H heads of d/H channels, each head its
+ * own read over its slice, so the gradient of head h is attnres_read_bwd's
+ * formula on that slice of the sources, output gradients, queries and gain,
+ * with d replaced by d/H in the RMS term.  Defined by the chatpaper.ai page
+ * "Multi-Head Attention Residuals", abstract (per-head softmax, block-diagonal
+ * read, H = 1 is the single-head read; its fused routing kernels serve
+ * training, i.e. this backward), with the per-head RMSNorm reading of mhar_fwd.
+ *   queries   [n_q][H][d/H] float (the layout mhar_fwd takes)
+ *   dqueries  [n_q][H][d/H] float, overwritten
+ * Every other argument, the passes over the queries, the workspace and the
+ * errors are those of attnres_read_bwd (workspace from
+ * mhar_read_bwd_workspace_size).  H = 1 is attnres_read_bwd.  Limits besides
+ * attnres_read_bwd's: a head holds a multiple of 32 16-byte vectors (d/H a
+ * multiple of 256 channels for bf16, 128 for f32), else
+ * ATTNRES_ERR_UNSUPPORTED; d % H != 0 is ATTNRES_ERR_INVALID_ARG.
+ */
+attnres_status_t mhar_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                               int64_t d, int64_t H, attnres_dtype_t dt, const float *queries,
+                               int64_t n_q, const float *gain, float eps, const void *dout,
+                               void *dsrc, int64_t dsrc_stride, int accumulate, float *dqueries,
+                               float *dgain, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* Workspace bytes mhar_read_bwd needs (as attnres_read_bwd_workspace_size). */
+attnres_status_t mhar_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t H,
+                                             int64_t n_q, attnres_dtype_t dt, size_t *bytes);
 
 /*
  * MSAR, the fused multi-stream depth read for one target layer: every source

@@ -157,15 +157,32 @@ def test_read_bwd_validation(lib):
     assert bw(dsrc=SRC + 64) == INV                    # overlaps the sources
     assert bw(ws=DO + 32) == INV                       # workspace overlaps dout
     assert bw(dq=WS + 64) == INV                       # dq overlaps the workspace
-    assert bw(n_q=3) == UNS                            # at most two queries
     assert bw(n_src=17) == UNS
-    assert bw(n_src=9, n_q=2) == UNS                   # two queries: at most 8 sources
     assert bw(dout=DO + 8) == UNS                      # misaligned
     assert bw(dg=None, T=0) != INV                     # dgain is optional
     n = ctypes.c_size_t(0)
     assert lib.attnres_read_bwd_workspace_size(9, 16, 64, 1, BF16, None) == INV
     assert lib.attnres_read_bwd_workspace_size(9, 16, 60, 1, BF16, ctypes.byref(n)) == UNS
-    assert lib.attnres_read_bwd_workspace_size(9, 16, 64, 3, BF16, ctypes.byref(n)) == UNS
+    assert lib.attnres_read_bwd_workspace_size(17, 16, 64, 1, BF16, ctypes.byref(n)) == UNS
+    # more queries than one pass takes are accepted (passes of 2, or of 1 above 8 sources)
+    for n_src, n_q in ((9, 3), (8, 5)):
+        assert lib.attnres_read_bwd_workspace_size(n_src, 16, 64, n_q, BF16, ctypes.byref(n)) not in (INV, UNS)
+
+
+def test_mhar_read_bwd_validation(lib):
+    SRC, Q, DO, DS, DQ, DG, WS = A, B, B + 0x1000000, A + 0x2000000, B + 0x2000000, B + 0x2100000, B + 0x2200000
+
+    def bw(H=8, d=4096, n_src=8, T=16, n_q=2, dt=BF16, dq=DQ, ws=WS):
+        return lib.mhar_read_bwd(SRC, n_src, T * d, T, d, H, dt, Q, n_q, None, 1e-6, DO, DS, T * d, 0, dq, DG,
+                                 ws, 1 << 20, None)
+    assert bw(H=0) == INV
+    assert bw(H=3) == INV                              # H must divide d
+    assert bw(dq=None) == INV
+    assert bw(H=32) == UNS                             # 16 vectors per head: not a multiple of 32
+    assert bw(H=3, d=768, T=0) not in (INV, UNS)       # 32 vectors per head: accepted
+    n = ctypes.c_size_t(0)
+    assert lib.mhar_read_bwd_workspace_size(8, 16, 4096, 3, 2, BF16, ctypes.byref(n)) == INV
+    assert lib.mhar_read_bwd_workspace_size(8, 16, 4096, 32, 2, BF16, ctypes.byref(n)) == UNS
 
 
 def test_msar_validation(lib):

@@ -168,6 +168,30 @@ def test_mhar_two_phase_T131072_d4096_H8():
     check_out(got[1:], ref, BF16)
 
 
+def test_mhar_read_bwd_T131072_d4096_H8_bench_workload():
+    """The MHAR backward at the MHAR size (4 queries, two passes): source
+    gradients on sampled tokens against the oracle; the query and gain
+    gradients (sums over all tokens) equal the sums of the two halves'."""
+    T, d, N, S, H = 131072, 4096, 8, 4, 8
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((S, H, d // H), (16.0 / (d // H)) ** 0.5, g)
+    gain = torch.ones((d,), dtype=F32, device="cuda")
+    dout = torch.randn((S, T, d), generator=g, device="cuda").to(BF16)
+    dsrc, dq, dg = attnres.mhar_read_bwd(src, q, dout, gain)
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T)
+    ref = oracle.mhar_bwd(rows(src, idx), q.cpu().numpy().astype(np.float64), rows(dout, idx), None, 1e-6)
+    check_out(rows(dsrc, idx), ref[0], BF16, what="dsrc")
+    del dsrc
+    h = T // 2
+    parts = [attnres.mhar_read_bwd(src[:, a:b].contiguous(), q, dout[:, a:b].contiguous(), gain, dsrc=None)[1:]
+             for a, b in ((0, h), (h, T))]
+    for name, whole, (x, y) in (("dq", dq, (parts[0][0], parts[1][0])), ("dgain", dg, (parts[0][1], parts[1][1]))):
+        w, s_ = to_host(whole), to_host(x) + to_host(y)
+        assert np.abs(w - s_).max() <= 1e-4 * np.abs(w).max(), name
+
+
 def test_msar_T32768_d4096():
     T, d, N = 32768, 4096, 8
     ks = (4, 8, 12)

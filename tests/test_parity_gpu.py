@@ -442,6 +442,77 @@ def test_read_bwd_empty_sequence_zeroes_parameter_gradients():
     assert torch.count_nonzero(dq) == 0 and torch.count_nonzero(dg) == 0
 
 
+@pytest.mark.parametrize("n_src,n_q,T,d,dtype", [(8, 3, 45, 2048, BF16), (5, 5, 30, 512, F32),
+                                                  (9, 3, 25, 1024, BF16), (16, 2, 12, 2048, BF16)])
+def test_read_bwd_more_queries_than_one_pass(n_src, n_q, T, d, dtype):
+    """Queries beyond one pass (2, or 1 above 8 sources) take further passes
+    whose source and gain gradients add up."""
+    rng = _rng(n_src * 7 + n_q + T)
+    src = _sources(rng, n_src, T, d, dtype, step=0.25)
+    q = _queries(rng, n_q, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    dout = _sources(rng, n_q, T, d, dtype, step=0)
+    got = attnres.attnres_read_bwd(to_dev(src, dtype), to_dev(q, F32), to_dev(dout, dtype), to_dev(g, F32), 1e-6)
+    _check_grads(got, oracle.read_bwd(src, q, dout, g, 1e-6), dtype, f"n_q={n_q}")
+
+
+@pytest.mark.parametrize("n_src,n_q,T,d,H,dtype,with_gain", [
+    (8, 2, 64, 4096, 8, BF16, True),        # the MHAR workload's heads: one warp per head
+    (8, 1, 50, 4096, 16, BF16, True),       # 32 vectors per head: one group per run of a warp
+    (4, 4, 33, 2048, 4, BF16, False),       # two token rows per CTA, two passes of queries
+    (3, 1, 41, 1024, 2, F32, True),         # a head spans two warps
+    (9, 1, 30, 4096, 8, BF16, True),        # more than 8 sources
+    (16, 2, 20, 2048, 2, BF16, False),      # 16 sources, passes of one query
+    (6, 3, 77, 1536, 3, F32, True),         # warps past the row's last head
+    (2, 1, 130, 512, 2, F32, True)])
+def test_mhar_read_bwd(n_src, n_q, T, d, H, dtype, with_gain):
+    """Backward of the MHAR read against the oracle's per-head chain rule."""
+    rng = _rng(n_src * 11 + n_q + T + d + H)
+    src = _sources(rng, n_src, T, d, dtype, step=0.25)
+    q = _queries(rng, n_q, d).reshape(n_q, H, d // H)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gain else None
+    dout = _sources(rng, n_q, T, d, dtype, step=0)
+    got = attnres.mhar_read_bwd(to_dev(src, dtype), to_dev(q, F32), to_dev(dout, dtype),
+                                to_dev(g, F32) if with_gain else None, 1e-6)
+    _check_grads(got, oracle.mhar_bwd(src, q, dout, g, 1e-6), dtype, f"H={H}")
+
+
+def test_mhar_read_bwd_one_head_is_the_read_backward_bitwise():
+    rng = _rng(71)
+    n_src, T, d = 8, 90, 2048
+    src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.25), BF16)
+    q = to_dev(_queries(rng, 2, d), F32)
+    dout = to_dev(_sources(rng, 2, T, d, BF16, step=0), BF16)
+    a = attnres.attnres_read_bwd(src, q, dout, None)
+    b = attnres.mhar_read_bwd(src, q.view(2, 1, d), dout, None)
+    for x, y in zip(a, b):
+        assert torch.equal(x.reshape(-1), y.reshape(-1))
+
+
+def test_mhar_read_bwd_is_block_diagonal_and_deterministic():
+    """An output gradient on one head's slice leaves every other slice of the
+    source, query and gain gradients exactly zero; two runs agree bitwise."""
+    rng = _rng(72)
+    n_src, T, d, H = 8, 100, 4096, 8
+    dh = d // H
+    src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.25), BF16)
+    q = to_dev(_queries(rng, 2, d).reshape(2, H, dh), F32)
+    g = to_dev(rng.uniform(0.5, 1.5, d).astype(np.float32), F32)
+    do = np.zeros((2, T, d), dtype=np.float32)
+    do[:, :, 5 * dh:6 * dh] = rng.standard_normal((2, T, dh))
+    dout = to_dev(do, BF16)
+    a = attnres.mhar_read_bwd(src, q, dout, g)
+    b = attnres.mhar_read_bwd(src, q, dout, g)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    dsrc, dq, dg = a
+    off = torch.ones(d, dtype=torch.bool, device="cuda")
+    off[5 * dh:6 * dh] = False
+    assert torch.count_nonzero(dsrc[:, :, off]) == 0 and torch.count_nonzero(dg[off]) == 0
+    assert torch.count_nonzero(dq[:, [h for h in range(H) if h != 5]]) == 0
+    assert torch.count_nonzero(dsrc[:, :, ~off]) > 0
+
+
 # --------------------------------------------------------------- MSAR
 
 @pytest.mark.parametrize("dtype", [F32, BF16])
