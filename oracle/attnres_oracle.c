@@ -491,6 +491,46 @@ int oracle_msar_conv(const double *v, int64_t T, int64_t d, int64_t k,
     return 0;
 }
 
+/* H^pre mixer of one token, [MSAR §무엇과 다른가]: z = RMSNorm(Flatten(Z))
+ * over m*d (stream-major: element r*d + c is Z^(r)[c]); c = sigmoid(z^T P)
+ * with P [m*d][m]; h = sum_r c_r Z^(r).  Z[m][d] -> out[d]; zf[m*d] and
+ * logit[m] are scratch; mixc (may be NULL) receives c. */
+static void msar_mix(const double *Z, int64_t m, int64_t d, const double *mix_gain,
+                     const double *mix_w, double mix_eps, double *zf, double *logit,
+                     double *out, double *mixc)
+{
+    rmsnorm(Z, mix_gain, m * d, mix_eps, zf);
+    for (int64_t o = 0; o < m; ++o) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < m * d; ++k) acc += zf[k] * mix_w[k * m + o];
+        logit[o] = 1.0 / (1.0 + exp(-acc));
+        if (mixc) mixc[o] = logit[o];
+    }
+    for (int64_t c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int64_t r = 0; r < m; ++r) acc += logit[r] * Z[r * d + c];
+        out[c] = acc;
+    }
+}
+
+/* The m streams of one source, [MSAR §무엇과 다른가]: u[r][T][d] with u[0] = v
+ * and u[r] the causal conv of v with kernel r (conv_w packed as above). */
+static int msar_expand(const double *v, int64_t T, int64_t d, int64_t m, const int32_t *ksizes,
+                       const double *conv_w, double *u)
+{
+    size_t per = (size_t)T * (size_t)d;
+    int64_t off = 0;
+    for (int64_t r = 0; r < m; ++r) {
+        double *ur = u + (size_t)r * per;
+        if (r == 0) memcpy(ur, v, sizeof(double) * per);
+        else {
+            if (oracle_msar_conv(v, T, d, ksizes[r - 1], conv_w + off, ur)) return -1;
+            off += d * (int64_t)ksizes[r - 1];
+        }
+    }
+    return 0;
+}
+
 /* MSAR read for one target layer, [MSAR §무엇과 다른가]:
  *   1. every source v_i is expanded into m full-width streams u_i^(r);
  *   2. each stream r reads the depth history with its own pseudo-query
@@ -538,18 +578,7 @@ int oracle_msar(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t 
                 if (read_one(rows, n_src, d, queries + r * d, gain, eps, Z + r * d, a, NULL)) goto fail;
                 if (alpha) for (int64_t i = 0; i < n_src; ++i) alpha[(t * m + r) * n_src + i] = a[i];
             }
-            rmsnorm(Z, mix_gain, m * d, mix_eps, zf);
-            for (int64_t o = 0; o < m; ++o) {
-                double acc = 0.0;
-                for (int64_t k = 0; k < m * d; ++k) acc += zf[k] * mix_w[k * m + o];
-                logit[o] = 1.0 / (1.0 + exp(-acc));
-                if (mixc) mixc[t * m + o] = logit[o];
-            }
-            for (int64_t c = 0; c < d; ++c) {
-                double acc = 0.0;
-                for (int64_t r = 0; r < m; ++r) acc += logit[r] * Z[r * d + c];
-                out[t * d + c] = acc;
-            }
+            msar_mix(Z, m, d, mix_gain, mix_w, mix_eps, zf, logit, out + t * d, mixc ? mixc + t * m : NULL);
         }
     }
     free(u); free(Z); free(zf); free(rows); free(a); free(logit);
@@ -557,4 +586,85 @@ int oracle_msar(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t 
 fail:
     free(u); free(Z); free(zf); free(rows); free(a); free(logit);
     return -1;
+}
+
+/* MSAR inside the two-phase Block schedule, phase 1.  [MSAR §어떻게 쓰나]:
+ * AttnRes's two-phase computation carries over to MSAR unchanged: every
+ * target query of the block is read against the completed sources in one
+ * batch, and each layer later merges its own partial-sum contribution by the
+ * online softmax.  Reading taken: the streams of a source belong to the
+ * source (the page writes them v_i^(r), with no layer index), so one set of
+ * conv kernels serves every layer of the block and each cached source is
+ * expanded once.  For every layer s and stream r this keeps the read's state
+ * over the cached sources, as phase 1 of [Summary §3 Inference]:
+ *   o_s^(r)   = sum_i softmax_i(w_s^(r)T RMSNorm(u_i^(r))) u_i^(r)
+ *   lse_s^(r) = log sum_i exp(w_s^(r)T RMSNorm(u_i^(r))).
+ * src[n_src][T][d]; queries[S][m][d]; o[S][m][T][d]; lse[S][m][T]. */
+int oracle_msar_phase1(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                       const int32_t *ksizes, const double *conv_w, const double *queries,
+                       int64_t S, const double *gain, double eps, double *o, double *lse)
+{
+    if (!src || !ksizes || !conv_w || !queries || !o || !lse || n_src < 1 || T < 0 || d < 1 ||
+        m < 1 || S < 1 || eps < 0) return -1;
+    size_t per = (size_t)T * (size_t)d;
+    /* u[i][r][T][d]: the streams of every source, expanded once */
+    double *u = (double *)malloc(sizeof(double) * (size_t)n_src * (size_t)m * per + 1);
+    const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_src);
+    int rc = (u && rows) ? 0 : -1;
+    for (int64_t i = 0; i < n_src && rc == 0; ++i)
+        rc = msar_expand(src + (size_t)i * per, T, d, m, ksizes, conv_w, u + (size_t)i * (size_t)m * per);
+    for (int64_t sl = 0; sl < S && rc == 0; ++sl)
+        for (int64_t r = 0; r < m && rc == 0; ++r)
+            for (int64_t t = 0; t < T && rc == 0; ++t) {
+                for (int64_t i = 0; i < n_src; ++i)
+                    rows[i] = u + ((size_t)i * (size_t)m + (size_t)r) * per + (size_t)t * (size_t)d;
+                rc = read_one(rows, n_src, d, queries + (sl * m + r) * d, gain, eps,
+                              o + (((size_t)sl * (size_t)m + (size_t)r) * (size_t)T + (size_t)t) * (size_t)d,
+                              NULL, lse + (sl * m + r) * T + t);
+            }
+    free(u); free(rows);
+    return rc;
+}
+
+/* MSAR two-phase, phase 2 for one layer.  The layer's partial sum p is its
+ * one more source ([Summary §2 Block AttnRes]); it is expanded into m streams
+ * with the same kernels, causally over p's own history ([MSAR §무엇과 다른가]).
+ * Each stream's score s_p^(r) = w^(r)T RMSNorm(u_p^(r)) is merged into that
+ * stream's phase-1 state by the merge of [Summary §3 Inference, Phase 2]:
+ *   M = max(lse^(r), s_p^(r)),
+ *   Z^(r) = (e^{lse^(r)-M} o^(r) + e^{s_p^(r)-M} u_p^(r)) / (e^{lse^(r)-M} + e^{s_p^(r)-M}),
+ * and the merged states go through the H^pre mixer (msar_mix).  partial ==
+ * NULL (the block's first layer) takes Z^(r) = o^(r).
+ * o[m][T][d]; lse[m][T]; partial[T][d] or NULL; query[m][d]; out[T][d]. */
+int oracle_msar_phase2(const double *o, const double *lse, const double *partial, int64_t T,
+                       int64_t d, int64_t m, const int32_t *ksizes, const double *conv_w,
+                       const double *query, const double *gain, double eps,
+                       const double *mix_gain, const double *mix_w, double mix_eps, double *out)
+{
+    if (!o || !lse || !ksizes || !conv_w || !query || !mix_w || !out || T < 0 || d < 1 || m < 1 ||
+        eps < 0 || mix_eps < 0) return -1;
+    size_t per = (size_t)T * (size_t)d;
+    double *up = partial ? (double *)malloc(sizeof(double) * (size_t)m * per + 1) : NULL;
+    double *Z = (double *)malloc(sizeof(double) * (size_t)m * (size_t)d + 1);
+    double *zf = (double *)malloc(sizeof(double) * (size_t)m * (size_t)d + 1);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)m);
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+    int rc = (Z && zf && logit && tmp && (!partial || up)) ? 0 : -1;
+    if (rc == 0 && partial) rc = msar_expand(partial, T, d, m, ksizes, conv_w, up);
+    for (int64_t t = 0; t < T && rc == 0; ++t) {
+        for (int64_t r = 0; r < m; ++r) {
+            const double *orow = o + ((size_t)r * (size_t)T + (size_t)t) * (size_t)d;
+            double *zr = Z + r * d;
+            if (!partial) { for (int64_t c = 0; c < d; ++c) zr[c] = orow[c]; continue; }
+            const double *prow = up + (size_t)r * per + (size_t)t * (size_t)d;
+            const double l = lse[r * T + t];
+            double sp = score(query + r * d, prow, gain, d, eps, tmp);
+            double M = l > sp ? l : sp;
+            double a = exp(l - M), b = exp(sp - M);
+            for (int64_t c = 0; c < d; ++c) zr[c] = (a * orow[c] + b * prow[c]) / (a + b);
+        }
+        msar_mix(Z, m, d, mix_gain, mix_w, mix_eps, zf, logit, out + t * d, NULL);
+    }
+    free(up); free(Z); free(zf); free(logit); free(tmp);
+    return rc;
 }

@@ -62,10 +62,15 @@ def _load():
         lib.oracle_msar.argtypes = [_D, _I64, _I64, _I64, _I64, ctypes.POINTER(ctypes.c_int32),
                                     _D, _D, _D, ctypes.c_double, _D, _D, ctypes.c_double, _D,
                                     _D, _D]
+        _K = ctypes.POINTER(ctypes.c_int32)
+        lib.oracle_msar_phase1.argtypes = [_D, _I64, _I64, _I64, _I64, _K, _D, _D, _I64, _D, ctypes.c_double,
+                                           _D, _D]
+        lib.oracle_msar_phase2.argtypes = [_D, _D, _D, _I64, _I64, _I64, _K, _D, _D, _D, ctypes.c_double, _D, _D,
+                                           ctypes.c_double, _D]
         for f in ("oracle_full", "oracle_weighted_sum", "oracle_block_oneshot",
                   "oracle_block_phase1", "oracle_block_phase2", "oracle_block_phase2_update",
                   "oracle_mhar_phase2", "oracle_read_bwd", "oracle_mhar_bwd", "oracle_mhar",
-                  "oracle_msar_conv", "oracle_msar"):
+                  "oracle_msar_conv", "oracle_msar", "oracle_msar_phase1", "oracle_msar_phase2"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -260,3 +265,36 @@ def msar(src, ksizes, conv_w, queries, gain=None, eps=1e-6, mix_gain=None, mix_w
                                _p(queries), _p(gain), float(eps), _p(mix_gain), _p(mix_w),
                                float(mix_eps), _p(out), _p(alpha), _p(mixc)), "oracle_msar")
     return (out, alpha, mixc) if want_debug else out
+
+
+def msar_phase1(src, ksizes, conv_w, queries, gain=None, eps=1e-6):
+    """MSAR two-phase, phase 1.  src [n_src,T,d]; queries [S,m,d] (every layer
+    of the block, one query per stream) -> o [S,m,T,d], lse [S,m,T]."""
+    src, conv_w, queries, gain = _f64(src), _f64(conv_w), _f64(queries), _f64(gain)
+    n_src, T, d = src.shape
+    S, m, _ = queries.shape
+    ks = np.ascontiguousarray(ksizes, dtype=np.int32)
+    assert ks.shape == (m - 1,) and conv_w.size == d * int(ks.sum())
+    o = np.empty((S, m, T, d))
+    lse = np.empty((S, m, T))
+    _check(_load().oracle_msar_phase1(_p(src), n_src, T, d, m, ks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                      _p(conv_w), _p(queries), S, _p(gain), float(eps), _p(o), _p(lse)),
+           "oracle_msar_phase1")
+    return o, lse
+
+
+def msar_phase2(o, lse, partial, ksizes, conv_w, query, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                mix_eps=1e-6):
+    """MSAR two-phase, phase 2 of one layer.  o [m,T,d], lse [m,T], partial
+    [T,d] or None, query [m,d], mix_w [m*d,m] -> out [T,d]."""
+    o, lse, partial, conv_w = _f64(o), _f64(lse), _f64(partial), _f64(conv_w)
+    query, gain, mix_gain, mix_w = _f64(query), _f64(gain), _f64(mix_gain), _f64(mix_w)
+    m, T, d = o.shape
+    ks = np.ascontiguousarray(ksizes, dtype=np.int32)
+    assert ks.shape == (m - 1,) and conv_w.size == d * int(ks.sum()) and mix_w.shape == (m * d, m)
+    out = np.empty((T, d))
+    _check(_load().oracle_msar_phase2(_p(o), _p(lse), _p(partial), T, d, m,
+                                      ks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _p(conv_w), _p(query),
+                                      _p(gain), float(eps), _p(mix_gain), _p(mix_w), float(mix_eps), _p(out)),
+           "oracle_msar_phase2")
+    return out

@@ -605,6 +605,77 @@ def test_msar_window_read_equals_full_sequence():
         assert np.allclose(win[-1], base[t], atol=1e-14)
 
 
+def _msar_block_inputs(rng, N, S, T, d, ks=(4, 8, 12)):
+    cached = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
+    parts = _rand(rng, S, T, d)
+    q = _rand(rng, S, 4, d, scale=2.0)
+    cw = _rand(rng, d * sum(ks), scale=0.4)
+    P = _rand(rng, 4 * d, 4, scale=0.2)
+    g = rng.uniform(0.5, 1.5, d)
+    mg = rng.uniform(0.5, 1.5, 4 * d)
+    return cached, parts, q, cw, P, g, mg
+
+
+@pytest.mark.parametrize("N,S,eps", [(5, 3, 1e-6), (1, 2, 0.1), (3, 1, 0.0)])
+def test_msar_two_phase_equals_one_shot(N, S, eps):
+    """[MSAR §어떻게 쓰나]: two-phase MSAR (phase 1 over the cached sources for
+    every layer of the block, then each layer's partial merged per stream)
+    equals the one-shot MSAR read of [b_0..b_{N-1}, p_s] with that layer's
+    queries; the block's first layer (no partial) equals the read of the
+    cached sources alone."""
+    rng = np.random.default_rng(61 + N + S)
+    T, d = 14, 8
+    ks = (4, 8, 12)
+    cached, parts, q, cw, P, g, mg = _msar_block_inputs(rng, N, S, T, d, ks)
+    o, lse = oracle.msar_phase1(cached, ks, cw, q, g, eps)
+    for s_ in range(S):
+        got = oracle.msar_phase2(o[s_], lse[s_], parts[s_], ks, cw, q[s_], g, eps, mg, P, 1e-6)
+        ref = oracle.msar(np.concatenate([cached, parts[s_][None]]), ks, cw, q[s_], g, eps, mg, P, 1e-6)
+        assert np.abs(got - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max()), s_
+        first = oracle.msar_phase2(o[s_], lse[s_], None, ks, cw, q[s_], g, eps, mg, P, 1e-6)
+        ref0 = oracle.msar(cached, ks, cw, q[s_], g, eps, mg, P, 1e-6)
+        assert np.abs(first - ref0).max() <= 1e-12 * max(1.0, np.abs(ref0).max()), s_
+
+
+def test_msar_phase1_single_source_state():
+    """One cached source: every stream's weight is 1, so o_s^(r) is the
+    stream itself (the source, or its causal conv, pinned against
+    np.convolve) and lse_s^(r) is that stream's score."""
+    rng = np.random.default_rng(62)
+    T, d, ks = 9, 8, (2, 3, 5)
+    src = _rand(rng, 1, T, d)
+    q = _rand(rng, 2, 4, d, scale=2.0)
+    cw = _rand(rng, d * sum(ks), scale=0.5)
+    o, lse = oracle.msar_phase1(src, ks, cw, q, None, 0.0)
+    streams = [src[0]]
+    off = 0
+    for k in ks:
+        streams.append(oracle.msar_conv(src[0], cw[off:off + d * k].reshape(d, k)))
+        off += d * k
+    for s_ in range(2):
+        for r in range(4):
+            u = streams[r]
+            assert np.allclose(o[s_, r], u, atol=1e-14)
+            rms = np.sqrt(np.mean(u * u, axis=1))
+            assert np.allclose(lse[s_, r], (u @ q[s_, r]) / rms, atol=1e-12)
+
+
+def test_msar_phase2_is_causal_in_the_partial():
+    """The partial's streams are causal convolutions of the partial: changing
+    p at t' > t leaves out[t] unchanged, and at t - 11 <= t' <= t changes it."""
+    rng = np.random.default_rng(63)
+    N, S, T, d = 3, 1, 30, 8
+    cached, parts, q, cw, P, g, mg = _msar_block_inputs(rng, N, S, T, d)
+    o, lse = oracle.msar_phase1(cached, (4, 8, 12), cw, q, g, 1e-6)
+    base = oracle.msar_phase2(o[0], lse[0], parts[0], (4, 8, 12), cw, q[0], g, 1e-6, mg, P, 1e-6)
+    t = 20
+    for tp, should_change in ((t + 1, False), (t - 12, False), (t - 11, True), (t, True)):
+        p2 = parts[0].copy()
+        p2[tp] += 3.0
+        h = oracle.msar_phase2(o[0], lse[0], p2, (4, 8, 12), cw, q[0], g, 1e-6, mg, P, 1e-6)
+        assert (np.abs(h[t] - base[t]).max() > 0) == should_change, tp
+
+
 # --------------------------------------------------------------------------
 # brute force: C oracle vs the NumPy twin on tiny shapes
 # --------------------------------------------------------------------------

@@ -24,7 +24,8 @@ MUTANTS = {
     "gain_ignored": [("double gc = g ? g[c] : 1.0;", "double gc = 1.0;")],
     "lse_drops_max": [("return m + log(l);", "return log(l);")],
     "merge_sign": [("double a = exp(lse[t] - M), b = exp(sp - M);", "double a = exp(lse[t] - M), b = exp(M - sp);")],
-    "mhar_phase2_merge_sign": [("double a = exp(l - M), b = exp(sp - M);", "double a = exp(l - M), b = exp(M - sp);")],
+    "mhar_phase2_merge_sign": [("double a = exp(l - M), b = exp(sp - M);\n            for (int64_t c = 0; c < dh; ++c)",
+                                "double a = exp(l - M), b = exp(M - sp);\n            for (int64_t c = 0; c < dh; ++c)")],
     "first_layer_reads_partial": [("if (li >= 1) { rows[N]", "if (li >= 0) { rows[N]")],
     "mhar_query_transposed": [("queries + (q * H + hd) * dh", "queries + (hd * n_q + q) * dh")],
     "bwd_softmax_mean_dropped": [("ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] - mean);",
@@ -37,6 +38,13 @@ MUTANTS = {
     "mhar_bwd_dout_of_first_head": [("do_h[(q * T + t) * dh + c] = dout[(q * T + t) * d + c0 + c];",
                                      "do_h[(q * T + t) * dh + c] = dout[(q * T + t) * d + c];")],
     "mhar_bwd_query_grad_unsliced": [("dq[q * d + c0 + c] = dq_h[q * dh + c];", "dq[q * d + c] = dq_h[q * dh + c];")],
+    "msar_phase1_layer_stream_transposed": [("queries + (sl * m + r) * d, gain, eps,",
+                                             "queries + (r * S + sl) * d, gain, eps,")],
+    "msar_phase2_merge_sign": [("double a = exp(l - M), b = exp(sp - M);\n            for (int64_t c = 0; c < d; ++c) zr[c]",
+                                "double a = exp(l - M), b = exp(M - sp);\n            for (int64_t c = 0; c < d; ++c) zr[c]")],
+    "msar_phase2_partial_identity_streams": [("if (rc == 0 && partial) rc = msar_expand(partial, T, d, m, ksizes, conv_w, up);",
+                                              "if (rc == 0 && partial) rc = msar_expand(partial, T, d, 1, ksizes, conv_w, up);\n    for (int64_t r = 1; r < m && up; ++r) memcpy(up + (size_t)r * per, partial, sizeof(double) * per);")],
+    "msar_phase2_lse_of_stream_zero": [("const double l = lse[r * T + t];", "const double l = lse[t];")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
