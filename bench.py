@@ -10,7 +10,8 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|msar|full_depth|
-block_d2048|block_fused|read_bwd|mhar_bwd|decode) are for profiling and the design notes.
+block_d2048|block_fused|read_bwd|mhar_bwd|msar_block|decode) are for profiling and the
+design notes.
 """
 from __future__ import annotations
 
@@ -41,6 +42,7 @@ KERNEL_SOURCES = {
     "phase2": [CSRC + "phase2.cuh", CSRC + "common.cuh", CSRC + "kernels_phase2.cu"],
     "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
+    "msar_phase1": [CSRC + "msar_phase1.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "read_bwd_mh": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu", CSRC + "kernels_bwd_mh.cu"],
     "depth_read_decode": [CSRC + "depth_read_decode.cuh", CSRC + "common.cuh", CSRC + "kernels_decode.cu"],
 }
@@ -699,6 +701,103 @@ class MsarWorkload(BlockWorkload):
         return len(wins)
 
 
+class MsarBlockWorkload(MsarWorkload):
+    """MSAR inside the two-phase Block schedule: one block of S=4 layers over
+    N=8 cached sources, bf16, d=4096.  One step = phase 1 (every source
+    expanded once, read by the 4 x 4 stream queries of the block's layers)
+    + 4 phase-2 calls (layers 2..4 merge their partial sums; layer 1 mixes
+    the phase-1 state alone).  The dominant kernel is phase 1; its roofline is
+    the CUDA-core FMA rate."""
+
+    def __init__(self, T=32768, d=4096, N=8, S=4, seed=0):
+        MsarWorkload.__init__(self, T, d, N, seed)
+        self.name = "msar_two_phase_block"
+        self.S = S
+        b = 2
+        # phase 1: read the cached sources, write o (S x 4 streams) and lse
+        self.phase1_bytes_per_token = N * d * b + S * 4 * d * b + S * 4 * 4
+        # phase 2 per layer: read o and lse (and the partial for layers 2..S), write h
+        self.bytes_per_token = (self.phase1_bytes_per_token + S * (4 * d * b + 4 * 4 + d * b)
+                                + (S - 1) * d * b)
+        self.launches_per_step = 1 + S
+        self.dominant = "msar_phase1_kernel"
+        self.dominant_src = "msar_phase1"
+        self.profile_tag = f"ncu_msar_phase1_d{d}"
+        # phase 1 multiply-adds per token: the convolutions of the N sources,
+        # per (source, stream) the sum of squares and one query dot per layer,
+        # and per (layer, stream) the weighted sum over the sources
+        self.fma_per_token = N * d * sum(self.ks) + N * 4 * d + S * N * 4 * d + S * 4 * N * d
+
+    def config(self):
+        c = MsarWorkload.config(self)
+        c["workload"] = f"{self.name} bf16 d={self.d} N={self.N} S={self.S} m=4 k=4/8/12 T={self.T}"
+        c["S"] = self.S
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        MsarWorkload.setup(self, device)
+        T, d, S = self.T, self.d, self.S
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed + 1)
+        self.queries = inputs.device_normal((S, 4, d), (16.0 / d) ** 0.5, g, device=device)
+        self.parts = torch.randn((S, T, d), generator=g, device=device).to(torch.bfloat16)
+        self.o = torch.empty((S, 4, T, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((S, 4, T), dtype=torch.float32, device=device)
+        self.outs = torch.empty((S, T, d), dtype=torch.bfloat16, device=device)
+        self.out = self.outs
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.msar_block_phase1(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, o=self.o,
+                                  lse=self.lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for s_ in range(self.S):
+            attnres.msar_block_phase2(self.o[s_], self.lse[s_], self.parts[s_] if s_ > 0 else None, self.ks,
+                                      self.conv_w, self.queries[s_], None, 1e-6, None, self.mix_w, 1e-6,
+                                      out=self.outs[s_], stream=stream)
+
+    def setup_host(self):
+        import torch
+        MsarWorkload.setup_host(self)
+        self.h_parts = torch.empty((self.S - 1,) + tuple(self.parts.shape[1:]), dtype=self.parts.dtype,
+                                   pin_memory=True)
+        self.h_parts.copy_(self.parts[1:])
+        self.h2d += self.h_parts.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.parts[1:].copy_(self.h_parts, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.outs, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        wins = []
+        for t in idx:
+            lo = max(0, int(t) - 11)
+            wins.append((self.cache[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64),
+                         self.parts[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)))
+        return (wins, self.conv_w.cpu().numpy().astype(np.float64),
+                self.queries.cpu().numpy().astype(np.float64),
+                self.mix_w.cpu().numpy().astype(np.float64))
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        wins, cw, q, mw = sample
+        for cached, parts in wins:
+            o, lse = oracle.msar_phase1(cached, self.ks, cw, q, None, 1e-6)
+            for s_ in range(self.S):
+                oracle.msar_phase2(o[s_], lse[s_], parts[s_] if s_ > 0 else None, self.ks, cw, q[s_], None,
+                                   1e-6, None, mw, 1e-6)
+        return len(wins)
+
+
 class FullDepthWorkload(BlockWorkload):
     """Full AttnRes at depth: 64 layers, layer l reads sources 0..l-1."""
 
@@ -784,6 +883,8 @@ def make_workload(name, T=None):
         return ReadBwdWorkload(T=T or 32768)
     if name == "mhar_bwd":
         return MharBwdWorkload(T=T or 131072)
+    if name == "msar_block":
+        return MsarBlockWorkload(T=T or 32768)
     if name == "block_fused":
         return BlockFusedWorkload(T=T or 32768)
     if name == "full_depth":
@@ -1032,7 +1133,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "block_fused", "read_bwd", "mhar_bwd", "decode", "mhar", "msar",
+                    choices=["block", "block_d2048", "block_fused", "read_bwd", "mhar_bwd", "decode", "mhar", "msar", "msar_block",
                              "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)

@@ -44,6 +44,10 @@ _SIGS = {
                  _vp],
     "msar_expand_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
                         _vp, _vp, _f, _vp, _vp],
+    "msar_block_phase1": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _i64, _vp, _f, _vp,
+                          _vp, _vp],
+    "msar_block_phase2": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
+                          _vp, _vp],
     "msar_expand_fwd_chunk": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
                               _vp, _vp, _f, _vp, _vp],
     "attnres_status_string": [ctypes.c_int],
@@ -363,4 +367,36 @@ def msar_expand_fwd_chunk(src, t_prev, ksizes, conv_w, queries, gain=None, eps=1
     _check("msar_expand_fwd_chunk", load().msar_expand_fwd_chunk(
         _p(src), n_src, stride, t_prev, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries),
         _p(gain), eps, _p(mix_gain), _p(mix_w), mix_eps, _p(out), _stream(stream)))
+    return out
+
+
+def msar_block_phase1(src, ksizes, conv_w, queries, gain=None, eps=1e-6, o=None, lse=None, stream=None):
+    """MSAR two-phase, phase 1: queries [S, m, d] of a block's layers over the
+    cached sources src [n_src, T, d] -> (o [S, m, T, d], lse [S, m, T])."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    S, m, _ = queries.shape
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if o is None:
+        o = torch.empty((S, m, T, d), dtype=src.dtype, device=src.device)
+    if lse is None:
+        lse = torch.empty((S, m, T), dtype=torch.float32, device=src.device)
+    _check("msar_block_phase1", load().msar_block_phase1(
+        _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries), S, _p(gain),
+        eps, _p(o), _p(lse), _stream(stream)))
+    return o, lse
+
+
+def msar_block_phase2(o, lse, partial, ksizes, conv_w, query, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                      mix_eps=1e-6, out=None, stream=None):
+    """MSAR two-phase, phase 2 of one layer: o [m, T, d], lse [m, T], partial
+    [T, d] or None, query [m, d] -> out [T, d]."""
+    import torch
+    m, T, d = o.shape
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if out is None:
+        out = torch.empty((T, d), dtype=o.dtype, device=o.device)
+    _check("msar_block_phase2", load().msar_block_phase2(
+        _p(o), _p(lse), _p(partial), T, d, _dt(o), m, ctypes.cast(ks, _vp), _p(conv_w), _p(query), _p(gain), eps,
+        _p(mix_gain), _p(mix_w), mix_eps, _p(out), _stream(stream)))
     return out

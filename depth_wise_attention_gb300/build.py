@@ -32,6 +32,8 @@ SOURCES = [
     "kernels_bwd_mh.cu",
     "kernels_decode.cu",
     "msar.cu",
+    "msar_phase1.cu",
+    "msar_phase2.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

@@ -725,6 +725,111 @@ attnres_status_t launch_msar_read(const void *src, int64_t n_src, int64_t src_st
     return launch_msar(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
 }
 
+// MSAR in the two-phase Block schedule.  Kernel sizes as the one-shot read.
+attnres_status_t check_msar_kernels(int64_t m, const int32_t *ksizes) {
+    if (m < 1) return ATTNRES_ERR_INVALID_ARG;
+    if (!ksizes) return ATTNRES_ERR_INVALID_ARG;
+    for (int64_t r = 0; r + 1 < m; ++r)
+        if (ksizes[r] < 1) return ATTNRES_ERR_INVALID_ARG;
+    if (m != 4) return ATTNRES_ERR_UNSUPPORTED;
+    for (int r = 0; r < 3; ++r)
+        if (ksizes[r] > MSAR_KMAX) return ATTNRES_ERR_UNSUPPORTED;
+    return ATTNRES_OK;
+}
+
+attnres_status_t launch_msar_phase1_host(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                         attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                         const float *conv_w, const float *queries, int64_t S, const float *gain,
+                                         float eps, void *o, float *lse, void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (S < 1) return ATTNRES_ERR_INVALID_ARG;
+    if (T == 0) return ATTNRES_OK;
+    if (!conv_w || !queries || !o || !lse) return ATTNRES_ERR_INVALID_ARG;
+    st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t o_bytes = (size_t)S * 4 * (size_t)T * (size_t)d * es;
+    const size_t lse_bytes = (size_t)S * 4 * (size_t)T * sizeof(float);
+    if (overlap(o, o_bytes, src, src_bytes) || overlap(lse, lse_bytes, src, src_bytes) ||
+        overlap(lse, lse_bytes, o, o_bytes))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (n_src > MSAR_SMAX) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(o) || !aligned4(lse) || !aligned16(queries) || !aligned16(conv_w) || (gain && !aligned16(gain)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    // layers in groups of up to MSAR_P1_MAXL (each group expands the sources again)
+    for (int64_t l0 = 0; l0 < S; l0 += MSAR_P1_MAXL) {
+        MsarP1Args a;
+        a.src = static_cast<const unsigned char *>(src);
+        a.src_stride_bytes = src_stride * (int64_t)es;
+        a.n_src = (int)n_src;
+        a.T = T;
+        a.d = (int)d;
+        for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
+        a.conv_w = conv_w;
+        a.queries = queries + l0 * 4 * d;
+        a.n_layers = (int)(S - l0 < MSAR_P1_MAXL ? S - l0 : MSAR_P1_MAXL);
+        a.gain = gain;
+        a.eps = eps;
+        a.o = static_cast<unsigned char *>(o) + (size_t)l0 * 4 * (size_t)T * (size_t)d * es;
+        a.lse = lse + l0 * 4 * T;
+        a.wait = wait_cfg(dev);
+        st = launch_msar_phase1(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
+        if (st != ATTNRES_OK) return st;
+    }
+    return ATTNRES_OK;
+}
+
+attnres_status_t launch_msar_phase2_host(const void *o, const float *lse, const void *partial, int64_t T, int64_t d,
+                                         attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                         const float *conv_w, const float *query, const float *gain, float eps,
+                                         const float *mix_gain, const float *mix_w, float mix_eps, void *out,
+                                         void *stream) {
+    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
+    if (T < 0 || d < 1 || !(eps >= 0.f) || std::isinf(eps) || !(mix_eps >= 0.f) || std::isinf(mix_eps))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / (4 * T)) return ATTNRES_ERR_INVALID_ARG;
+    if (T == 0) return ATTNRES_OK;
+    if (!o || !lse || !conv_w || !query || !mix_w || !out) return ATTNRES_ERR_INVALID_ARG;
+    attnres_status_t st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    const size_t es = esize(dt);
+    const size_t row_bytes = (size_t)T * (size_t)d * es;
+    if (overlap(out, row_bytes, o, 4 * row_bytes) || overlap(out, row_bytes, lse, (size_t)4 * T * 4) ||
+        (partial && overlap(out, row_bytes, partial, row_bytes)))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (d % 8 != 0 || d > ((int64_t)1 << 20)) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(o) || !aligned4(lse) || (partial && !aligned16(partial)) || !aligned16(out) ||
+        !aligned16(query) || !aligned16(conv_w) || !aligned16(mix_w) || (gain && !aligned16(gain)) ||
+        (mix_gain && !aligned16(mix_gain)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarP2Args a;
+    a.o = static_cast<const unsigned char *>(o);
+    a.lse = lse;
+    a.partial = static_cast<const unsigned char *>(partial);
+    a.T = T;
+    a.d = (int)d;
+    for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
+    a.conv_w = conv_w;
+    a.query = query;
+    a.gain = gain;
+    a.eps = eps;
+    a.mix_gain = mix_gain;
+    a.mix_w = mix_w;
+    a.mix_eps = mix_eps;
+    a.out = static_cast<unsigned char *>(out);
+    a.wait = wait_cfg(dev);
+    a.tt = 0;
+    return launch_msar_phase2(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
+}
+
 }  // namespace
 
 extern "C" {
@@ -851,6 +956,22 @@ attnres_status_t msar_expand_fwd_chunk(const void *src, int64_t n_src, int64_t s
     if (T_prev < 0) return ATTNRES_ERR_INVALID_ARG;
     return launch_msar_read(src, n_src, src_stride, T_prev, T, d, dt, m, ksizes, conv_w, queries, gain, eps,
                             mix_gain, mix_w, mix_eps, out, stream);
+}
+
+attnres_status_t msar_block_phase1(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                   attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                   const float *queries, int64_t S, const float *gain, float eps, void *o,
+                                   float *lse, void *stream) {
+    return launch_msar_phase1_host(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, S, gain, eps, o,
+                                   lse, stream);
+}
+
+attnres_status_t msar_block_phase2(const void *o, const float *lse, const void *partial, int64_t T, int64_t d,
+                                   attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                   const float *query, const float *gain, float eps, const float *mix_gain,
+                                   const float *mix_w, float mix_eps, void *out, void *stream) {
+    return launch_msar_phase2_host(o, lse, partial, T, d, dt, m, ksizes, conv_w, query, gain, eps, mix_gain, mix_w,
+                                   mix_eps, out, stream);
 }
 
 const char *attnres_status_string(attnres_status_t s) {

@@ -34,26 +34,6 @@ constexpr int MSAR_LA = 4;                              // rows prefetched ahead
 constexpr int MSAR_NS = MSAR_SMAX * MSAR_M * 2;         // score sums per token (64)
 constexpr int MSAR_NX = MSAR_NS + 5;                    // + mixer sums (ssZ, 4 dots)
 
-template <typename Tin> struct Pair2;
-template <> struct Pair2<__nv_bfloat16> {
-    __device__ static __forceinline__ float2 ld(const unsigned char *p) {
-        return bf2_to_f2(*reinterpret_cast<const uint32_t *>(p));
-    }
-    __device__ static __forceinline__ void st(unsigned char *p, float2 v) {
-        *reinterpret_cast<uint32_t *>(p) = f2_to_bf2(v.x, v.y);
-    }
-};
-template <> struct Pair2<float> {
-    __device__ static __forceinline__ float2 ld(const unsigned char *p) {
-        return *reinterpret_cast<const float2 *>(p);
-    }
-    __device__ static __forceinline__ void st(unsigned char *p, float2 v) {
-        *reinterpret_cast<float2 *>(p) = v;
-    }
-};
-
-__device__ __forceinline__ float dot2(float2 a, float2 b) { return fmaf(a.x, b.x, a.y * b.y); }
-
 // KA, KB, KC > 0 fix the three kernel sizes at compile time (fully unrolled,
 // branch-free convolution); 0 means they are read from the arguments.
 template <typename Tin, int KA, int KB, int KC>

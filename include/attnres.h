@@ -355,6 +355,55 @@ attnres_status_t msar_expand_fwd_chunk(const void *src, int64_t n_src, int64_t s
                                        const float *mix_gain, const float *mix_w, float mix_eps,
                                        void *out, void *stream);
 
+/*
+ * MSAR inside the two-phase Block schedule, phase 1: the queries of S layers
+ * of a block read the completed (cached) sources in one pass.  Every source
+ * is expanded once into its m streams (as msar_expand_fwd) and, for every
+ * layer s and stream r, the read's state over the sources is kept:
+ *   o_s^(r)   = sum_i softmax_i(w_s^(r) . RMSNorm(u_i^(r))) u_i^(r)
+ *   lse_s^(r) = log sum_i exp(w_s^(r) . RMSNorm(u_i^(r)))
+ * Defined by: onedev.kr "깊이 방향 어텐션을 다중 스트림으로 확장한 MSAR",
+ * section 어떻게 쓰나 (AttnRes's caching and two-phase computation carry over:
+ * a block's target queries are batched against the completed sources, and
+ * each layer then merges its own partial sum with the online softmax), with
+ * the phase-1 state of the b-lab.team summary, section 3 (Inference).
+ * Reading taken: the streams of a source are the source's own (the page
+ * writes them v_i^(r), with no layer index), so one conv_w serves every
+ * layer and the partials.
+ *   src       [n_src][T][d], n_src <= 8
+ *   queries   [S][m][d] float (m = 4 streams per layer)
+ *   o         [S][m][T][d] dtype dt;  lse [S][m][T] float
+ * Other arguments and limits as msar_expand_fwd.  More than 4 layers are
+ * read in groups of 4 (each group expands the sources again).
+ */
+attnres_status_t msar_block_phase1(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                   int64_t d, attnres_dtype_t dt, int64_t m,
+                                   const int32_t *ksizes, const float *conv_w,
+                                   const float *queries, int64_t S, const float *gain, float eps,
+                                   void *o, float *lse, void *stream);
+
+/*
+ * MSAR two-phase, phase 2 of one layer: the layer's partial sum is its one
+ * more source.  It is expanded into its m streams with the same kernels
+ * (causally over the partial's own history, token 0 first); each stream's
+ * score s_p^(r) = w^(r) . RMSNorm(u_p^(r)) is merged into that stream's
+ * phase-1 state by the online-softmax merge (b-lab.team summary, section 3,
+ * Phase 2):  Z^(r) = (e^{lse-M} o^(r) + e^{s_p-M} u_p^(r)) / (e^{lse-M} + e^{s_p-M});
+ * the merged Z go through the H^pre mixer as in msar_expand_fwd.  partial ==
+ * NULL (the block's first layer) mixes Z^(r) = o^(r).
+ *   o         [m][T][d] dtype dt (layer s of msar_block_phase1's o)
+ *   lse       [m][T] float
+ *   partial   [T][d] dtype dt, or NULL
+ *   query     [m][d] float (the layer's stream queries)
+ *   out       [T][d] dtype dt; must not overlap o, lse or partial
+ * Other arguments and limits as msar_expand_fwd.
+ */
+attnres_status_t msar_block_phase2(const void *o, const float *lse, const void *partial, int64_t T,
+                                   int64_t d, attnres_dtype_t dt, int64_t m,
+                                   const int32_t *ksizes, const float *conv_w, const float *query,
+                                   const float *gain, float eps, const float *mix_gain,
+                                   const float *mix_w, float mix_eps, void *out, void *stream);
+
 /* Static description of a status code (never NULL). */
 const char *attnres_status_string(attnres_status_t status);
 

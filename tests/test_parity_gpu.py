@@ -543,6 +543,74 @@ def test_msar_kernel_sizes(ks):
     check_out(out, ref, BF16)
 
 
+def _msar_block(rng, N, S, T, d, dtype, ks=(4, 8, 12)):
+    """Cached sources, S layers' stream queries and partial sums, conv and
+    mixer weights for the two-phase MSAR tests."""
+    cached = _sources(rng, N, T, d, dtype)
+    parts = _sources(rng, S, T, d, dtype, step=0)
+    q = _queries(rng, S * 4, d).reshape(S, 4, d)
+    cw = np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel() for k in ks])
+    mw = (rng.standard_normal((4 * d, 4)) / math.sqrt(4 * d)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    mg = rng.uniform(0.5, 1.5, 4 * d).astype(np.float32)
+    return cached, parts, q, cw, mw, g, mg
+
+
+@pytest.mark.parametrize("dtype,N,S,T,d", [(BF16, 8, 4, 60, 4096), (BF16, 3, 2, 45, 512), (F32, 5, 1, 33, 256),
+                                           (BF16, 1, 3, 20, 2048), (F32, 8, 4, 70, 1024), (BF16, 6, 6, 25, 512)])
+def test_msar_block_phase1(dtype, N, S, T, d):
+    """Phase 1 against the oracle: every layer's per-stream state (o, lse)
+    over the cached sources; six layers take two groups."""
+    rng = _rng(N * 13 + S + T + d)
+    ks = (4, 8, 12)
+    cached, _, q, cw, _, g, _ = _msar_block(rng, N, S, T, d, dtype, ks)
+    o, lse = attnres.msar_block_phase1(to_dev(cached, dtype), ks, to_dev(cw, F32), to_dev(q, F32), to_dev(g, F32),
+                                       1e-6)
+    ro, rl = oracle.msar_phase1(cached, ks, cw, q, g, 1e-6)
+    check_out(o, ro, dtype, np.abs(cached).max() * 3, what="o")
+    check_lse(lse, rl)
+
+
+@pytest.mark.parametrize("dtype,T,d,with_partial", [(BF16, 50, 4096, True), (BF16, 50, 4096, False),
+                                                    (F32, 40, 512, True), (BF16, 130, 1024, True),
+                                                    (F32, 17, 256, False)])
+def test_msar_block_phase2(dtype, T, d, with_partial):
+    """Phase 2 against the oracle on the same phase-1 state (the oracle's,
+    rounded to the working dtype): the partial's streams, the per-stream
+    merge and the mixer; no partial mixes the state alone."""
+    rng = _rng(T + d + with_partial)
+    ks = (4, 8, 12)
+    cached, parts, q, cw, mw, g, mg = _msar_block(rng, 4, 1, T, d, dtype, ks)
+    o, lse = oracle.msar_phase1(cached, ks, cw, q, g, 1e-6)
+    o1 = inputs.bf16_round(o[0].astype(np.float32)) if dtype == BF16 else o[0].astype(np.float32)
+    p = parts[0] if with_partial else None
+    out = attnres.msar_block_phase2(to_dev(o1, dtype), to_dev(lse[0].astype(np.float32), F32),
+                                    to_dev(p, dtype) if with_partial else None, ks, to_dev(cw, F32),
+                                    to_dev(q[0], F32), to_dev(g, F32), 1e-6, to_dev(mg, F32), to_dev(mw, F32), 1e-6)
+    ref = oracle.msar_phase2(o1.astype(np.float64), lse[0].astype(np.float32).astype(np.float64), p, ks, cw, q[0], g,
+                             1e-6, mg, mw, 1e-6)
+    check_out(out, ref, dtype, np.abs(cached).max() * 3)
+
+
+@pytest.mark.parametrize("dtype,N,S,T,d", [(BF16, 8, 4, 64, 4096), (F32, 3, 2, 40, 512), (BF16, 5, 3, 150, 1024)])
+def test_msar_block_two_phase_equals_one_shot(dtype, N, S, T, d):
+    """The GPU two-phase chain (phase 1 for the block, phase 2 per layer)
+    against the oracle's one-shot MSAR read of [cached, partial_s] (layer 1:
+    the cached sources alone)."""
+    rng = _rng(N * 7 + S * 3 + T)
+    ks = (4, 8, 12)
+    cached, parts, q, cw, mw, g, mg = _msar_block(rng, N, S, T, d, dtype, ks)
+    cwd, qd, gd, mgd, mwd = (to_dev(x, F32) for x in (cw, q, g, mg, mw))
+    o, lse = attnres.msar_block_phase1(to_dev(cached, dtype), ks, cwd, qd, gd, 1e-6)
+    for s_ in range(S):
+        p = parts[s_] if s_ > 0 else None
+        out = attnres.msar_block_phase2(o[s_], lse[s_], to_dev(p, dtype) if p is not None else None, ks, cwd,
+                                        qd[s_], gd, 1e-6, mgd, mwd, 1e-6)
+        srcs = cached if p is None else np.concatenate([cached, p[None]])
+        ref = oracle.msar(srcs, ks, cw, q[s_], g, 1e-6, mg, mw, 1e-6)
+        check_out(out, ref, dtype, np.abs(srcs).max() * 3, what=f"layer {s_ + 1}")
+
+
 # --------------------------------------------------------------- hygiene
 
 def test_outputs_stay_inside_their_buffers():
