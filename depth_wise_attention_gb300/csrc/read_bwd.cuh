@@ -36,6 +36,12 @@
 
 namespace attnres {
 
+// Bulk prefetch of global memory into L2 (no shared memory, no completion).
+// src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
 constexpr int RB_THREADS = 256;
 constexpr int RB_MAX_STAGES = 4;
 
@@ -132,6 +138,10 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
         for (int q = 0; q < a.n_q; ++q)
             bulk_g2s(dst + (size_t)(a.n_src + q) * a.row_pitch, a.dout + (q * a.T * a.d) * E::BYTES + off, bytes,
                      &full[p_stage], pol);
+        // a pass that adds into dsrc reads the tile's gradient rows back in
+        // pass B: have them in L2 by then
+        if (a.accumulate)
+            for (int i = 0; i < a.n_src; ++i) bulk_prefetch_l2(a.dsrc + (int64_t)i * a.dsrc_stride_bytes + off, bytes);
         if (++p_stage == a.nstages) p_stage = 0;
         p_tile += gstride;
     };
@@ -303,6 +313,17 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
 #pragma unroll
         for (int i = 0; i < NS; ++i) {
             if (i >= a.n_src || !row_ok) break;
+            // the values to add to (accumulate), loaded before the gradient is
+            // formed (with 4 vectors a thread, where registers are short, at use)
+            constexpr bool EARLY = VPT <= 2;
+            uint4 zraw[VPT];
+            if (EARLY && a.accumulate) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k)
+                    if (vok[k])
+                        zraw[k] = *reinterpret_cast<const uint4 *>(a.dsrc + (int64_t)i * a.dsrc_stride_bytes +
+                                                                  (t * a.d + (int64_t)vid[k] * EPV) * E::BYTES);
+            }
             float alg[HG][NQ], bqg[HG][NQ], cig[HG];
 #pragma unroll
             for (int g = 0; g < HG; ++g) {
@@ -335,7 +356,7 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
                                         (t * a.d + (int64_t)vid[k] * EPV) * E::BYTES;
                     if (a.accumulate) {
                         float2 z[NP];
-                        E::unpack(*reinterpret_cast<const uint4 *>(gp), z);
+                        E::unpack(EARLY ? zraw[k] : *reinterpret_cast<const uint4 *>(gp), z);
 #pragma unroll
                         for (int p = 0; p < NP; ++p) y[p] = make_float2(y[p].x + z[p].x, y[p].y + z[p].y);
                     }

@@ -208,3 +208,34 @@ def test_msar_validation(lib):
     assert mc() == OK
     assert mc(t_prev=-1) == INV
     assert mc(t_prev=3, T=4, stride=4 * 256) == INV    # sources hold fewer than t_prev + T rows
+
+
+def test_msar_two_phase_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    bad = (ctypes.c_int32 * 3)(4, 0, 12)
+    kp = lambda k: ctypes.cast(k, ctypes.c_void_p)
+    T, d = 16, 256
+
+    def p1(src=A, n_src=8, m=4, k=ks, S=4, o=B + 0x1000000, lse=B + 0x3000000, T=T):
+        return lib.msar_block_phase1(src, n_src, T * d, T, d, BF16, m, kp(k), B, B + 0x200000, S, None, 1e-6,
+                                     o, lse, None)
+    assert p1(T=0) == OK
+    assert p1(S=0) == INV
+    assert p1(o=None) == INV
+    assert p1(k=bad) == INV
+    assert p1(o=A + 64) == INV                  # overlaps the sources
+    assert p1(m=3) == UNS
+    assert p1(n_src=9) == UNS
+    assert p1(o=B + 0x1000008) == UNS           # misaligned
+
+    def p2(o=A, lse=B + 0x3000000, part=A + 0x2000000, m=4, k=ks, out=B + 0x1000000, mix_eps=1e-6, T=T):
+        return lib.msar_block_phase2(o, lse, part, T, d, BF16, m, kp(k), B, B + 0x200000, None, 1e-6, None,
+                                     B + 0x300000, mix_eps, out, None)
+    assert p2(T=0) == OK
+    assert p2(o=None) == INV
+    assert p2(out=None) == INV
+    assert p2(mix_eps=-1.0) == INV
+    assert p2(k=bad) == INV
+    assert p2(out=A + 64) == INV                # overlaps the state
+    assert p2(m=3) == UNS
+    assert p2(part=A + 0x2000008) == UNS        # misaligned partial
