@@ -268,10 +268,13 @@ int oracle_block_phase2_update(const double *p, const double *f, const double *o
  * has k = 0 and passes nothing back through its score).
  * src, dsrc [n_src][T][d]; queries, dq [n_q][d]; dout [n_q][T][d]; dg [d]
  * (the gain's gradient even when gain is NULL, i.e. 1); dq and dg are sums
- * over the tokens. */
-int oracle_read_bwd(const double *src, int64_t n_src, int64_t T, int64_t d,
-                    const double *queries, int64_t n_q, const double *gain, double eps,
-                    const double *dout, double *dsrc, double *dq, double *dg)
+ * over the tokens.
+ * dlse [n_q][T] (may be NULL): the gradient of each query's log-sum-exp,
+ * lse_q = log sum_i exp(s_qi) (the phase-1 state of [Summary §3 Inference]);
+ * d lse_q / d s_qi = alpha_qi, so it adds alpha_qi dlse_q to ds_qi. */
+int oracle_read_bwd_lse(const double *src, int64_t n_src, int64_t T, int64_t d,
+                        const double *queries, int64_t n_q, const double *gain, double eps,
+                        const double *dout, const double *dlse, double *dsrc, double *dq, double *dg)
 {
     if (!src || !queries || !dout || !dsrc || !dq || !dg || n_src < 1 || n_q < 1 || T < 0 || d < 1 ||
         eps < 0)
@@ -317,7 +320,7 @@ int oracle_read_bwd(const double *src, int64_t n_src, int64_t T, int64_t d,
                 mean += a[q * n_src + i] * dal;
             }
             for (int64_t i = 0; i < n_src; ++i)
-                ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] - mean);
+                ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] - mean + (dlse ? dlse[q * T + t] : 0.0));
             /* value path and the query's gradient */
             for (int64_t i = 0; i < n_src; ++i) {
                 double *dv = dsrc + (i * T + t) * d;
@@ -347,6 +350,74 @@ int oracle_read_bwd(const double *src, int64_t n_src, int64_t T, int64_t d,
         }
     }
     free(r); free(k); free(s); free(a); free(ds); free(dk);
+    return 0;
+}
+
+/* The read's backward without a log-sum-exp gradient. */
+int oracle_read_bwd(const double *src, int64_t n_src, int64_t T, int64_t d,
+                    const double *queries, int64_t n_q, const double *gain, double eps,
+                    const double *dout, double *dsrc, double *dq, double *dg)
+{
+    return oracle_read_bwd_lse(src, n_src, T, d, queries, n_q, gain, eps, dout, NULL, dsrc, dq, dg);
+}
+
+/* Backward of the phase-2 merge (oracle_block_phase2) for an output gradient
+ * dh [T][d].  Per token, with the forward
+ *   r_p = sqrt(mean(p^2) + eps),  s_p = w . (g * p) / r_p,  M = max(lse, s_p),
+ *   a = e^{lse-M} / (e^{lse-M} + e^{s_p-M}),  b = 1 - a,  h = a o + b p,
+ * the chain rule gives
+ *   d_o          = a dh
+ *   dlse         = a b (dh . (o - p))          (da/dlse = a b, dh/da = o - p)
+ *   ds_p         = -dlse                       (da/ds_p = -a b)
+ *   d_partial    = b dh + ds_p d s_p/d p,  d s_p/d p = g*w / r_p - p (w . (g*p)) / (d r_p^3)
+ *   dquery      += ds_p g * p / r_p,  dgain += ds_p w * p / r_p.
+ * A zero partial with eps = 0 has no score path (s_p = 0 and nothing passes
+ * back through it).  partial == NULL (the block's first layer, out = o):
+ * d_o = dh, dlse = 0, and the partial, query and gain get nothing.
+ * o, partial, dh, d_o, d_partial [T][d]; lse, dlse [T]; query, dquery, dgain [d]. */
+int oracle_block_phase2_bwd(const double *o, const double *lse, const double *partial,
+                            int64_t T, int64_t d, const double *query, const double *gain,
+                            double eps, const double *dh, double *d_o, double *dlse,
+                            double *d_partial, double *dquery, double *dgain)
+{
+    if (!o || !lse || !query || !dh || !d_o || !dlse || !dquery || !dgain || T < 0 || d < 1 || eps < 0)
+        return -1;
+    if (partial && !d_partial) return -1;
+    for (int64_t c = 0; c < d; ++c) { dquery[c] = 0.0; dgain[c] = 0.0; }
+    for (int64_t t = 0; t < T; ++t) {
+        const double *ot = o + t * d, *ht = dh + t * d;
+        if (!partial) {
+            for (int64_t c = 0; c < d; ++c) d_o[t * d + c] = ht[c];
+            dlse[t] = 0.0;
+            continue;
+        }
+        const double *pt = partial + t * d;
+        double ms = 0.0, wgp = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            ms += pt[c] * pt[c];
+            wgp += query[c] * (gain ? gain[c] : 1.0) * pt[c];
+        }
+        const double r = sqrt(ms / (double)d + eps);
+        const double sp = r > 0.0 ? wgp / r : 0.0;
+        const double M = lse[t] > sp ? lse[t] : sp;
+        const double ea = exp(lse[t] - M), eb = exp(sp - M);
+        const double a = ea / (ea + eb), b = eb / (ea + eb);
+        double hdiff = 0.0;
+        for (int64_t c = 0; c < d; ++c) hdiff += ht[c] * (ot[c] - pt[c]);
+        dlse[t] = a * b * hdiff;
+        const double dsp = -dlse[t];
+        for (int64_t c = 0; c < d; ++c) {
+            const double gc = gain ? gain[c] : 1.0;
+            d_o[t * d + c] = a * ht[c];
+            double dp = b * ht[c];
+            if (r > 0.0) {
+                dp += dsp * (gc * query[c] / r - pt[c] * wgp / ((double)d * r * r * r));
+                dquery[c] += dsp * gc * pt[c] / r;
+                dgain[c] += dsp * query[c] * pt[c] / r;
+            }
+            d_partial[t * d + c] = dp;
+        }
+    }
     return 0;
 }
 

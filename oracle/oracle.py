@@ -54,6 +54,10 @@ def _load():
                                                    ctypes.c_double, _D, _D]
         lib.oracle_mhar_phase2.argtypes = [_D, _D, _D, _I64, _I64, _I64, _D, _D, ctypes.c_double, _D]
         lib.oracle_read_bwd.argtypes = [_D, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double, _D, _D, _D, _D]
+        lib.oracle_read_bwd_lse.argtypes = [_D, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double, _D, _D, _D, _D,
+                                            _D]
+        lib.oracle_block_phase2_bwd.argtypes = [_D, _D, _D, _I64, _I64, _D, _D, ctypes.c_double, _D, _D, _D, _D,
+                                                _D, _D]
         lib.oracle_mhar_bwd.argtypes = [_D, _I64, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double, _D, _D, _D,
                                         _D]
         lib.oracle_mhar.argtypes = [_D, _I64, _I64, _I64, _I64, _D, _I64, _D, ctypes.c_double,
@@ -69,7 +73,8 @@ def _load():
                                            ctypes.c_double, _D]
         for f in ("oracle_full", "oracle_weighted_sum", "oracle_block_oneshot",
                   "oracle_block_phase1", "oracle_block_phase2", "oracle_block_phase2_update",
-                  "oracle_mhar_phase2", "oracle_read_bwd", "oracle_mhar_bwd", "oracle_mhar",
+                  "oracle_mhar_phase2", "oracle_read_bwd", "oracle_read_bwd_lse", "oracle_block_phase2_bwd",
+                  "oracle_mhar_bwd", "oracle_mhar",
                   "oracle_msar_conv", "oracle_msar", "oracle_msar_phase1", "oracle_msar_phase2"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -203,6 +208,38 @@ def read_bwd(src, queries, dout, gain=None, eps=1e-6):
     _check(_load().oracle_read_bwd(_p(src), n_src, T, d, _p(queries), n_q, _p(gain), float(eps), _p(dout),
                                    _p(dsrc), _p(dq), _p(dg)), "oracle_read_bwd")
     return dsrc, dq, dg
+
+
+def block_phase1_bwd(src, queries, d_o, dlse, gain=None, eps=1e-6):
+    """Backward of Block phase 1 (the read's outputs o [n_q,T,d] and its
+    log-sum-exp lse [n_q,T]) for gradients d_o and dlse (None: zero) ->
+    (dsrc [n_src,T,d], dq [n_q,d], dgain [d])."""
+    src, queries, d_o, dlse, gain = _f64(src), _f64(queries), _f64(d_o), _f64(dlse), _f64(gain)
+    n_src, T, d = src.shape
+    n_q = queries.shape[0]
+    dsrc = np.empty((n_src, T, d))
+    dq = np.empty((n_q, d))
+    dg = np.empty(d)
+    _check(_load().oracle_read_bwd_lse(_p(src), n_src, T, d, _p(queries), n_q, _p(gain), float(eps), _p(d_o),
+                                       _p(dlse), _p(dsrc), _p(dq), _p(dg)), "oracle_read_bwd_lse")
+    return dsrc, dq, dg
+
+
+def block_phase2_bwd(o, lse, partial, query, dh, gain=None, eps=1e-6):
+    """Backward of the phase-2 merge: o, partial (or None), dh [T,d]; lse [T];
+    query [d] -> (d_o [T,d], dlse [T], d_partial [T,d] or None, dquery [d],
+    dgain [d])."""
+    o, lse, partial, query, dh, gain = _f64(o), _f64(lse), _f64(partial), _f64(query), _f64(dh), _f64(gain)
+    T, d = o.shape
+    d_o = np.empty((T, d))
+    dlse = np.empty(T)
+    dp = np.empty((T, d)) if partial is not None else None
+    dq = np.empty(d)
+    dg = np.empty(d)
+    _check(_load().oracle_block_phase2_bwd(_p(o), _p(lse), _p(partial), T, d, _p(query), _p(gain), float(eps),
+                                           _p(dh), _p(d_o), _p(dlse), _p(dp), _p(dq), _p(dg)),
+           "oracle_block_phase2_bwd")
+    return d_o, dlse, dp, dq, dg
 
 
 def mhar_bwd(src, queries, dout, gain=None, eps=1e-6):

@@ -365,6 +365,103 @@ def test_read_bwd_score_path_is_orthogonal_to_the_source_at_zero_eps():
     assert np.abs(score_part).max() > 1e-3
 
 
+def _fd(loss, args, h=1e-6):
+    """Central differences of loss(*args) with respect to every array in args
+    (None entries skipped)."""
+    out = []
+    for n, x in enumerate(args):
+        if x is None:
+            out.append(None)
+            continue
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            a, b = [list(args), list(args)]
+            xa, xb = x.copy(), x.copy()
+            xa[idx] += h
+            xb[idx] -= h
+            a[n], b[n] = xa, xb
+            fd[idx] = (loss(*a) - loss(*b)) / (2 * h)
+        out.append(fd)
+    return out
+
+
+@pytest.mark.parametrize("eps,with_gain", [(1e-6, True), (0.1, False), (0.0, True)])
+def test_block_phase1_bwd_matches_finite_differences(eps, with_gain):
+    """Block phase 1's backward for gradients of both its outputs, o and lse,
+    against central differences of the (pinned) phase-1 oracle."""
+    rng = np.random.default_rng(71)
+    n_src, n_q, T, d = 4, 3, 2, 8
+    src = _rand(rng, n_src, T, d) * (1 + np.arange(n_src))[:, None, None]
+    q = _rand(rng, n_q, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d) if with_gain else np.ones(d)
+    d_o, dl = _rand(rng, n_q, T, d), _rand(rng, n_q, T)
+
+    def loss(s_, q_, g_):
+        o, lse = oracle.block_phase1(s_, q_, g_, eps)
+        return float((o * d_o).sum() + (lse * dl).sum())
+    got = oracle.block_phase1_bwd(src, q, d_o, dl, g if with_gain else None, eps)
+    ref = _fd(loss, (src, q, g))
+    for x, y in zip(got, ref):
+        assert np.abs(x - y).max() <= 1e-6 * max(1.0, np.abs(y).max())
+
+
+def test_block_phase1_bwd_without_lse_gradient_is_the_read_backward():
+    rng = np.random.default_rng(72)
+    src, q, d_o = _rand(rng, 5, 3, 16), _rand(rng, 2, 16), _rand(rng, 2, 3, 16)
+    a = oracle.block_phase1_bwd(src, q, d_o, None, None, 1e-6)
+    b = oracle.read_bwd(src, q, d_o, None, 1e-6)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+@pytest.mark.parametrize("eps,with_gain", [(1e-6, True), (0.1, False), (0.0, True)])
+def test_block_phase2_bwd_matches_finite_differences(eps, with_gain):
+    """The merge's backward against central differences of the (pinned)
+    phase-2 oracle, for o, lse, the partial, the query and the gain."""
+    rng = np.random.default_rng(73)
+    T, d = 3, 8
+    o, p, dh = _rand(rng, T, d), _rand(rng, T, d, scale=2.0), _rand(rng, T, d)
+    lse, q = _rand(rng, T), _rand(rng, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d) if with_gain else np.ones(d)
+
+    def loss(o_, l_, p_, q_, g_):
+        return float((oracle.block_phase2(o_, l_, p_, q_, g_, eps=eps) * dh).sum())
+    d_o, dl, dp, dq, dg = oracle.block_phase2_bwd(o, lse, p, q, dh, g if with_gain else None, eps)
+    ref = _fd(loss, (o, lse, p, q, g))
+    for x, y in zip((d_o, dl, dp, dq, dg), ref):
+        assert np.abs(x - y).max() <= 1e-6 * max(1.0, np.abs(y).max())
+
+
+def test_block_phase2_bwd_without_partial_passes_the_gradient_to_o():
+    rng = np.random.default_rng(74)
+    o, dh, lse, q = _rand(rng, 4, 8), _rand(rng, 4, 8), _rand(rng, 4), _rand(rng, 8)
+    d_o, dl, dp, dq, dg = oracle.block_phase2_bwd(o, lse, None, q, dh)
+    assert np.array_equal(d_o, dh) and not dl.any() and dp is None and not dq.any() and not dg.any()
+
+
+@pytest.mark.parametrize("N,eps", [(4, 1e-6), (1, 0.05), (6, 0.0)])
+def test_two_phase_backward_equals_one_shot_backward(N, eps):
+    """The two-phase schedule computes the one-shot read of [b_0..b_{N-1}, p]
+    ([Summary §3 Inference]), so its backward -- the merge's backward, then
+    phase 1's backward for the merge's d_o and dlse -- gives the one-shot
+    read's gradients: the cached sources', the partial's, the query's and the
+    gain's."""
+    rng = np.random.default_rng(75 + N)
+    T, d = 3, 12
+    cached = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
+    p, dh = _rand(rng, T, d, scale=1.5), _rand(rng, T, d)
+    q = _rand(rng, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d)
+    o, lse = oracle.block_phase1(cached, q[None], g, eps)
+    d_o, dl, dp, dq2, dg2 = oracle.block_phase2_bwd(o[0], lse[0], p, q, dh, g, eps)
+    ds1, dq1, dg1 = oracle.block_phase1_bwd(cached, q[None], d_o[None], dl[None], g, eps)
+    ref_s, ref_q, ref_g = oracle.read_bwd(np.concatenate([cached, p[None]]), q[None], dh[None], g, eps)
+    tol = lambda y: 1e-12 * max(1.0, np.abs(y).max())
+    assert np.abs(ds1 - ref_s[:N]).max() <= tol(ref_s)
+    assert np.abs(dp - ref_s[N]).max() <= tol(ref_s)
+    assert np.abs(dq1[0] + dq2 - ref_q[0]).max() <= tol(ref_q)
+    assert np.abs(dg1 + dg2 - ref_g).max() <= tol(ref_g)
+
+
 def _fd_grads_mhar(src, q, g, dout, eps, h=1e-6):
     """Central finite differences of L = sum(dout * out) through the MHAR
     forward oracle; q is [n_q, H, d/H]."""

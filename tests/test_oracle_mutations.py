@@ -28,8 +28,12 @@ MUTANTS = {
                                 "double a = exp(l - M), b = exp(M - sp);\n            for (int64_t c = 0; c < dh; ++c)")],
     "first_layer_reads_partial": [("if (li >= 1) { rows[N]", "if (li >= 0) { rows[N]")],
     "mhar_query_transposed": [("queries + (q * H + hd) * dh", "queries + (hd * n_q + q) * dh")],
-    "bwd_softmax_mean_dropped": [("ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] - mean);",
-                                  "ds[q * n_src + i] = a[q * n_src + i] * ds[q * n_src + i];")],
+    "bwd_softmax_mean_dropped": [("ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] - mean + (dlse",
+                                  "ds[q * n_src + i] = a[q * n_src + i] * (ds[q * n_src + i] + (dlse")],
+    "bwd_lse_gradient_sign": [("- mean + (dlse ? dlse[q * T + t] : 0.0));", "- mean - (dlse ? dlse[q * T + t] : 0.0));")],
+    "merge_bwd_dlse_without_b": [("dlse[t] = a * b * hdiff;", "dlse[t] = a * hdiff;")],
+    "merge_bwd_value_path_weight": [("double dp = b * ht[c];", "double dp = a * ht[c];")],
+    "merge_bwd_rms_term_sign": [("dp += dsp * (gc * query[c] / r - pt[c] * wgp", "dp += dsp * (gc * query[c] / r + pt[c] * wgp")],
     "bwd_rms_term_sign": [("dv[c] += gc * dk[c] / r[i] - v[c] * gdkv", "dv[c] += gc * dk[c] / r[i] + v[c] * gdkv")],
     "bwd_gain_grad_not_normalised": [("dg[c] += dk[c] * v[c] / r[i];", "dg[c] += dk[c] * v[c];")],
     "bwd_value_path_first_query_weights": [("dv[c] += a[q * n_src + i] * dh[c];", "dv[c] += a[i] * dh[c];")],
