@@ -10,7 +10,7 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|msar|full_depth|
-block_d2048|block_fused|read_bwd|mhar_bwd|msar_block|decode) are for profiling and the
+block_d2048|block_fused|block_bwd|read_bwd|mhar_bwd|msar_block|decode) are for profiling and the
 design notes.
 """
 from __future__ import annotations
@@ -422,6 +422,108 @@ class ReadBwdWorkload(BlockWorkload):
         src, q, dout = sample
         oracle.read_bwd(src, q, dout, None, 1e-6)
         return src.shape[1]
+
+
+class BlockBwdWorkload(BlockWorkload):
+    """Backward of the headline Block step (bf16, d=4096, N=8, S=4): the
+    merge backward of each layer (layers 2..4 with their partials, layer 1
+    without, which passes its gradient straight to o), then phase 1's backward
+    for the four layers' o and lse gradients (two passes of two queries).
+    Algorithmic bytes per token: the merge backward reads o, p and dh and
+    writes d_o and d_partial (3 layers), layer 1 copies dh to d_o, and phase
+    1's backward reads the 8 sources and the 4 d_o rows and writes the 8
+    source gradients once."""
+
+    def __init__(self, T=32768, d=4096, N=8, S=4, seed=0):
+        super().__init__(T, d, N, S, seed, name="block_attnres_two_phase_backward")
+        b = 2
+        self.phase1_bytes_per_token = (2 * N + S) * d * b + S * 4
+        self.merge_bwd_bytes_per_token = 5 * d * b + 2 * 4
+        self.bytes_per_token = self.phase1_bytes_per_token + (S - 1) * self.merge_bwd_bytes_per_token + 2 * d * b
+        self.launches_per_step = (S - 1) * 2 + 1 + 2 * ((S + 1) // 2)
+        self.dominant = "phase-1 backward (read_bwd_kernel passes + reductions)"
+        self.dominant_src = "read_bwd"
+        self.profile_tag = f"ncu_block_bwd_phase1_d{d}"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} N={self.N} S={self.S} T={self.T}"
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres
+        super().setup(device)
+        T, d, N, S = self.T, self.d, self.N, self.S
+        attnres.attnres_block_phase1(self.cache, self.queries, None, 1e-6, o=self.o, lse=self.lse)
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed + 7)
+        self.dh = torch.randn((S, T, d), generator=g, device=device).to(torch.bfloat16)
+        self.d_o = torch.empty_like(self.o)
+        self.d_lse = torch.empty_like(self.lse)
+        self.d_parts = torch.empty_like(self.partials)
+        self.dsrc = torch.empty_like(self.cache)
+        self.dq2 = torch.empty((S, d), dtype=torch.float32, device=device)
+        self.dg2 = torch.empty((S, d), dtype=torch.float32, device=device)
+        self.dq1 = torch.empty((S, d), dtype=torch.float32, device=device)
+        self.dg1 = torch.empty((d,), dtype=torch.float32, device=device)
+        nb = attnres.attnres_block_phase2_bwd_workspace_size(T, d, torch.bfloat16)
+        self.ws2 = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+        nb = attnres.attnres_read_bwd_workspace_size(N, T, d, S, torch.bfloat16)
+        self.ws1 = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        for s_ in range(self.S):
+            attnres.attnres_block_phase2_bwd(self.o[s_], self.lse[s_], self.partials[s_] if s_ > 0 else None,
+                                             self.queries[s_], self.dh[s_], None, 1e-6, d_o=self.d_o[s_],
+                                             d_lse=self.d_lse[s_], d_partial=self.d_parts[s_],
+                                             dquery=self.dq2[s_], dgain=self.dg2[s_], workspace=self.ws2,
+                                             stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.attnres_block_phase1_bwd(self.cache, self.queries, self.d_o, self.d_lse, None, 1e-6,
+                                         dsrc=self.dsrc, dqueries=self.dq1, dgain=self.dg1, workspace=self.ws1,
+                                         stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def setup_host(self):
+        import torch
+        self.h_cache = torch_pinned_like(self.cache)
+        self.h_parts = torch_pinned_like(self.partials)
+        self.h_dh = torch_pinned_like(self.dh)
+        self.h_out = torch_pinned_like(self.dsrc)
+        self.h2d = (self.h_cache.numel() + self.h_parts.numel() + self.h_dh.numel()) * 2
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.partials.copy_(self.h_parts, non_blocking=True)
+        self.dh.copy_(self.h_dh, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.dsrc, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        import torch
+        it = torch.from_numpy(idx).to(self.cache.device)
+        c = self.cache[:, it, :].float().cpu().numpy().astype(np.float64)
+        p = self.partials[:, it, :].float().cpu().numpy().astype(np.float64)
+        h = self.dh[:, it, :].float().cpu().numpy().astype(np.float64)
+        return c, p, h, self.queries.cpu().numpy().astype(np.float64)
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        c, p, h, q = sample
+        o, lse = oracle.block_phase1(c, q, None, 1e-6)
+        d_o, d_lse = np.empty_like(o), np.empty_like(lse)
+        for s_ in range(self.S):
+            r = oracle.block_phase2_bwd(o[s_], lse[s_], p[s_] if s_ > 0 else None, q[s_], h[s_], None, 1e-6)
+            d_o[s_], d_lse[s_] = r[0], r[1]
+        oracle.block_phase1_bwd(c, q, d_o, d_lse, None, 1e-6)
+        return c.shape[1]
 
 
 class MharBwdWorkload(ReadBwdWorkload):
@@ -882,6 +984,8 @@ def make_workload(name, T=None):
         return DecodeWorkload(T=T or 16)
     if name == "read_bwd":
         return ReadBwdWorkload(T=T or 32768)
+    if name == "block_bwd":
+        return BlockBwdWorkload(T=T or 32768)
     if name == "mhar_bwd":
         return MharBwdWorkload(T=T or 131072)
     if name == "msar_block":
@@ -1134,7 +1238,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "block_fused", "read_bwd", "mhar_bwd", "decode", "mhar", "msar", "msar_block",
+                    choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "decode", "mhar", "msar", "msar_block",
                              "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)

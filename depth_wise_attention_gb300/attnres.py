@@ -37,6 +37,11 @@ _SIGS = {
     "attnres_read_bwd_noalloc": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _i64,
                                  ctypes.c_int, _vp, _vp, _vp],
     "attnres_read_bwd_workspace_size": [_i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+    "attnres_block_phase1_bwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _vp,
+                                 _i64, ctypes.c_int, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "attnres_block_phase2_bwd": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp, _f, _vp, _vp, _vp, _vp,
+                                 ctypes.c_int, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "attnres_block_phase2_bwd_workspace_size": [_i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
     "mhar_read_bwd": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _f, _vp, _vp, _i64,
                       ctypes.c_int, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "mhar_read_bwd_workspace_size": [_i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
@@ -264,6 +269,66 @@ def attnres_read_bwd_noalloc(src, queries, dout, gain=None, eps=1e-6, dsrc=None,
         _p(src), n_src, stride, T, d, _dt(src), _p(queries), n_q, _p(gain), eps, _p(dout), _p(dsrc), dstride,
         1 if accumulate else 0, _p(dqueries), _p(dgain), _stream(stream)))
     return dsrc, dqueries, dgain
+
+
+def attnres_block_phase1_bwd(src, queries, d_o, d_lse=None, gain=None, eps=1e-6, dsrc=None, accumulate=False,
+                             dqueries=None, dgain=None, want_dgain=True, workspace=None, stream=None):
+    """Backward of Block phase 1 for gradients of its outputs o [n_q,T,d] and
+    lse [n_q,T] (None: zero) -> (dsrc, dqueries, dgain)."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    n_q = queries.shape[0]
+    if dsrc is None:
+        dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=src.device)
+    _, _, _, dstride = _src_geometry(dsrc)
+    if dqueries is None:
+        dqueries = torch.empty((n_q, d), dtype=torch.float32, device=src.device)
+    if dgain is None and want_dgain:
+        dgain = torch.empty((d,), dtype=torch.float32, device=src.device)
+    if workspace is None:
+        nbytes = attnres_read_bwd_workspace_size(n_src, T, d, n_q, src.dtype)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=src.device)
+    _check("attnres_block_phase1_bwd", load().attnres_block_phase1_bwd(
+        _p(src), n_src, stride, T, d, _dt(src), _p(queries), n_q, _p(gain), eps, _p(d_o), _p(d_lse), _p(dsrc),
+        dstride, 1 if accumulate else 0, _p(dqueries), _p(dgain), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dsrc, dqueries, dgain
+
+
+def attnres_block_phase2_bwd_workspace_size(T, d, dtype):
+    import torch
+    n = ctypes.c_size_t(0)
+    dt = BF16 if dtype == torch.bfloat16 else F32
+    _check("attnres_block_phase2_bwd_workspace_size",
+           load().attnres_block_phase2_bwd_workspace_size(T, d, dt, ctypes.byref(n)))
+    return n.value
+
+
+def attnres_block_phase2_bwd(o, lse, partial, query, dh, gain=None, eps=1e-6, d_o=None, d_lse=None,
+                             d_partial=None, accumulate=False, dquery=None, dgain=None, want_dgain=True,
+                             workspace=None, stream=None):
+    """Backward of the phase-2 merge: o, partial (or None), dh [T,d]; lse [T]
+    -> (d_o, d_lse, d_partial (None without a partial), dquery, dgain)."""
+    import torch
+    T, d = o.shape
+    if d_o is None:
+        d_o = torch.empty_like(o)
+    if d_lse is None:
+        d_lse = torch.empty((T,), dtype=torch.float32, device=o.device)
+    if partial is not None and d_partial is None:
+        d_partial = torch.empty_like(partial)
+    if dquery is None:
+        dquery = torch.empty((d,), dtype=torch.float32, device=o.device)
+    if dgain is None and want_dgain:
+        dgain = torch.empty((d,), dtype=torch.float32, device=o.device)
+    if workspace is None:
+        nbytes = attnres_block_phase2_bwd_workspace_size(T, d, o.dtype)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=o.device)
+    _check("attnres_block_phase2_bwd", load().attnres_block_phase2_bwd(
+        _p(o), _p(lse), _p(partial), T, d, _dt(o), _p(query), _p(gain), eps, _p(dh), _p(d_o), _p(d_lse),
+        _p(d_partial), 1 if accumulate else 0, _p(dquery), _p(dgain), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return d_o, d_lse, (d_partial if partial is not None else None), dquery, dgain
 
 
 def mhar_read_bwd_workspace_size(n_src, T, d, H, n_q, dtype):

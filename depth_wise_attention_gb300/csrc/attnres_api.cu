@@ -17,6 +17,7 @@
 #include "dispatch.h"
 #include "msar.h"
 #include "phase2.cuh"
+#include "merge_bwd.cuh"
 #include "read_bwd.cuh"
 
 using namespace attnres;
@@ -539,9 +540,9 @@ size_t read_bwd_ws_bytes(int sms, const ReadBwdShape &sh, int64_t d) {
 
 attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
                                  int64_t H, attnres_dtype_t dt, const float *queries, int64_t n_q,
-                                 const float *gain, float eps, const void *dout, void *dsrc, int64_t dsrc_stride,
-                                 int accumulate, float *dq, float *dgain, void *ws, size_t ws_bytes,
-                                 void *stream) {
+                                 const float *gain, float eps, const void *dout, const float *dlse, void *dsrc,
+                                 int64_t dsrc_stride, int accumulate, float *dq, float *dgain, void *ws,
+                                 size_t ws_bytes, void *stream) {
     attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
     if (st != ATTNRES_OK) return st;
     if (n_q < 1 || (accumulate != 0 && accumulate != 1)) return ATTNRES_ERR_INVALID_ARG;
@@ -558,11 +559,14 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         overlap(ws, ws_bytes, dout, dout_bytes) || overlap(dq, dq_bytes, ws, ws_bytes) ||
         (dgain && (overlap(dgain, (size_t)d * 4, ws, ws_bytes) || overlap(dgain, (size_t)d * 4, dq, dq_bytes))))
         return ATTNRES_ERR_INVALID_ARG;
+    if (dlse && (H != 1 || overlap(dsrc, dsrc_bytes, dlse, (size_t)n_q * (size_t)T * 4)))
+        return ATTNRES_ERR_INVALID_ARG;
     ReadBwdShape sh;
     st = read_bwd_shape(n_src, d, n_q, H, dt, &sh);
     if (st != ATTNRES_OK) return st;
     if (!aligned16(dout) || !aligned16(dsrc) || (dsrc_stride * (int64_t)es) % 16 != 0 || !aligned16(queries) ||
-        (gain && !aligned16(gain)) || !aligned4(dq) || (dgain && !aligned4(dgain)) || !aligned16(ws))
+        (gain && !aligned16(gain)) || !aligned4(dq) || (dgain && !aligned4(dgain)) || !aligned16(ws) ||
+        (dlse && !aligned4(dlse)))
         return ATTNRES_ERR_UNSUPPORTED;
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
@@ -628,6 +632,7 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         a.n_q = nq;
         a.queries = queries + q0 * d;
         a.dout = static_cast<const unsigned char *>(dout) + (size_t)q0 * (size_t)T * (size_t)d * es;
+        a.dlse = dlse ? dlse + q0 * T : nullptr;
         a.accumulate = q0 == 0 ? accumulate : 1;
         void *args[] = {&a};
         const void *fn = kr[nq == sh.nqc ? 0 : 1].fn;
@@ -648,6 +653,115 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         e = cudaLaunchKernel(read_bwd_finish_fn(), dim3(fgrid), dim3(256), fargs, 0, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "read_bwd finish launch");
     }
+    return ATTNRES_OK;
+}
+
+// Backward of the phase-2 merge: tile shape, workspace and launch.
+struct MergeBwdShape {
+    int tpr, vpt, tt;
+    int grid;
+};
+
+attnres_status_t merge_bwd_shape(int64_t T, int64_t d, attnres_dtype_t dt, const DeviceInfo *dev,
+                                 MergeBwdShape *sh) {
+    row_shape((int)(d / epv(dt)), &sh->tpr, &sh->vpt);
+    if (sh->vpt > 4) return ATTNRES_ERR_UNSUPPORTED;
+    sh->tt = MB_THREADS / sh->tpr;
+    const int64_t ntiles = (T + sh->tt - 1) / sh->tt;
+    const int64_t occ = sh->vpt <= 2 ? 2 : 1;
+    const int64_t g = (int64_t)dev->sms * occ;
+    sh->grid = (int)(ntiles < g ? (ntiles > 0 ? ntiles : 1) : g);
+    return ATTNRES_OK;
+}
+
+size_t merge_bwd_ws_bytes(const MergeBwdShape &sh, int64_t d) {
+    return (size_t)sh.grid * (size_t)sh.tt * (size_t)d * sizeof(float);
+}
+
+attnres_status_t launch_merge_bwd(const void *o, const float *lse, const void *partial, int64_t T, int64_t d,
+                                  attnres_dtype_t dt, const float *query, const float *gain, float eps,
+                                  const void *dh, void *d_o, float *d_lse, void *d_partial, int accumulate,
+                                  float *dquery, float *dgain, void *ws, size_t ws_bytes, void *stream) {
+    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
+    if (T < 0 || d < 1 || !(eps >= 0.f) || std::isinf(eps) || (accumulate != 0 && accumulate != 1))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!o || !lse || !query || !dh || !d_o || !d_lse || !dquery)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && partial && (!d_partial || !ws)) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t rb = (size_t)T * (size_t)d * es;
+    const size_t lb = (size_t)T * 4;
+    const void *ins[4] = {o, partial, dh, lse};
+    const size_t insz[4] = {rb, rb, rb, lb};
+    void *outs[3] = {d_o, d_partial, d_lse};
+    const size_t outsz[3] = {rb, rb, lb};
+    for (int i = 0; i < 3; ++i) {
+        if (!outs[i]) continue;
+        for (int j = 0; j < 4; ++j)
+            if (ins[j] && overlap(outs[i], outsz[i], ins[j], insz[j])) return ATTNRES_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 3; ++j)
+            if (outs[j] && overlap(outs[i], outsz[i], outs[j], outsz[j])) return ATTNRES_ERR_INVALID_ARG;
+        if (ws && overlap(outs[i], outsz[i], ws, ws_bytes)) return ATTNRES_ERR_INVALID_ARG;
+    }
+    if (dgain && overlap(dgain, (size_t)d * 4, dquery, (size_t)d * 4)) return ATTNRES_ERR_INVALID_ARG;
+    if (d % 8 != 0 || d > ((int64_t)1 << 20)) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(o) || (partial && !aligned16(partial)) || !aligned16(dh) || !aligned16(d_o) ||
+        (d_partial && !aligned16(d_partial)) || !aligned4(lse) || !aligned4(d_lse) || !aligned16(query) ||
+        (gain && !aligned16(gain)) || !aligned4(dquery) || (dgain && !aligned4(dgain)) || (ws && !aligned16(ws)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    attnres_status_t st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0 || !partial) {
+        // no tokens, or no partial (out = o): d_o = dh, dlse = 0, no parameter gradient
+        cudaError_t e = cudaMemsetAsync(dquery, 0, (size_t)d * 4, s);
+        if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, s);
+        if (e == cudaSuccess && T > 0) e = cudaMemcpyAsync(d_o, dh, rb, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess && T > 0) e = cudaMemsetAsync(d_lse, 0, lb, s);
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "merge backward without a partial");
+    }
+    MergeBwdShape sh;
+    st = merge_bwd_shape(T, d, dt, dev, &sh);
+    if (st != ATTNRES_OK) return st;
+    if (ws_bytes < merge_bwd_ws_bytes(sh, d)) return ATTNRES_ERR_INVALID_ARG;
+    KernelRef kr;
+    if (!lookup_merge_bwd(dt == ATTNRES_BF16 ? 1 : 0, sh.vpt, &kr)) return ATTNRES_ERR_UNSUPPORTED;
+    MergeBwdArgs a;
+    a.o = static_cast<const unsigned char *>(o);
+    a.lse = lse;
+    a.partial = static_cast<const unsigned char *>(partial);
+    a.dh = static_cast<const unsigned char *>(dh);
+    a.T = T;
+    a.d = (int)d;
+    a.nvec = (int)(d / epv(dt));
+    a.query = query;
+    a.gain = gain;
+    a.eps = eps;
+    a.d_o = static_cast<unsigned char *>(d_o);
+    a.d_lse = d_lse;
+    a.d_partial = static_cast<unsigned char *>(d_partial);
+    a.accumulate = accumulate;
+    a.ws = static_cast<float *>(ws);
+    a.tpr = sh.tpr;
+    a.tt = sh.tt;
+    a.ntiles = (T + sh.tt - 1) / sh.tt;
+    void *args[] = {&a};
+    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(sh.grid), dim3(MB_THREADS), args, 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge backward launch");
+    ReadBwdFinishArgs f;
+    f.ws = a.ws;
+    f.nparts = sh.grid * sh.tt;
+    f.n_q = 1;
+    f.d = (int)d;
+    f.queries = query;
+    f.gain = gain;
+    f.dq = dquery;
+    f.dgain = dgain;
+    f.accumulate_dgain = 0;
+    void *fargs[] = {&f};
+    e = cudaLaunchKernel(read_bwd_finish_fn(), dim3((unsigned)((d + 255) / 256)), dim3(256), fargs, 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge backward finish launch");
     return ATTNRES_OK;
 }
 
@@ -903,7 +1017,8 @@ attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_st
                                   float eps, const void *dout, void *dsrc, int64_t dsrc_stride, int accumulate,
                                   float *dqueries, float *dgain, void *workspace, size_t workspace_bytes,
                                   void *stream) {
-    return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+    return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, nullptr, dsrc,
+                           dsrc_stride,
                            accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
 }
 
@@ -921,8 +1036,41 @@ attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_
     void *ws = nullptr;
     attnres_status_t st = bwd_scratch(&ws);
     if (st != ATTNRES_OK) return st;
-    return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+    return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, nullptr, dsrc,
+                           dsrc_stride,
                            accumulate, dqueries, dgain, ws, kBwdScratchFloats * sizeof(float), stream);
+}
+
+attnres_status_t attnres_block_phase1_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                          int64_t d, attnres_dtype_t dt, const float *queries, int64_t n_q,
+                                          const float *gain, float eps, const void *d_o, const float *d_lse,
+                                          void *dsrc, int64_t dsrc_stride, int accumulate, float *dqueries,
+                                          float *dgain, void *workspace, size_t workspace_bytes, void *stream) {
+    return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, d_o, d_lse, dsrc,
+                           dsrc_stride, accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
+}
+
+attnres_status_t attnres_block_phase2_bwd_workspace_size(int64_t T, int64_t d, attnres_dtype_t dt,
+                                                        size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || T < 0 || d < 1) return ATTNRES_ERR_INVALID_ARG;
+    if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    attnres_status_t st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MergeBwdShape sh;
+    st = merge_bwd_shape(T, d, dt, dev, &sh);
+    if (st != ATTNRES_OK) return st;
+    *bytes = merge_bwd_ws_bytes(sh, d);
+    return ATTNRES_OK;
+}
+
+attnres_status_t attnres_block_phase2_bwd(const void *o, const float *lse, const void *partial, int64_t T,
+                                          int64_t d, attnres_dtype_t dt, const float *query, const float *gain,
+                                          float eps, const void *dh, void *d_o, float *d_lse, void *d_partial,
+                                          int accumulate, float *dquery, float *dgain, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    return launch_merge_bwd(o, lse, partial, T, d, dt, query, gain, eps, dh, d_o, d_lse, d_partial, accumulate,
+                            dquery, dgain, workspace, workspace_bytes, stream);
 }
 
 attnres_status_t mhar_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t H, int64_t n_q,
@@ -935,7 +1083,8 @@ attnres_status_t mhar_read_bwd(const void *src, int64_t n_src, int64_t src_strid
                                const float *gain, float eps, const void *dout, void *dsrc, int64_t dsrc_stride,
                                int accumulate, float *dqueries, float *dgain, void *workspace,
                                size_t workspace_bytes, void *stream) {
-    return launch_read_bwd(src, n_src, src_stride, T, d, H, dt, queries, n_q, gain, eps, dout, dsrc, dsrc_stride,
+    return launch_read_bwd(src, n_src, src_stride, T, d, H, dt, queries, n_q, gain, eps, dout, nullptr, dsrc,
+                           dsrc_stride,
                            accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
 }
 

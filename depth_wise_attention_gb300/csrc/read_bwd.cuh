@@ -9,7 +9,9 @@
 //     c_i   = - sum_q ds_qi ((w_q*g) . v_i) / (d r_i^3)
 //     dv_i  = sum_q alpha_qi dout_q + sum_q b_qi (w_q*g) + c_i v_i
 //     U_q  += sum_i b_qi v_i           (summed over the tokens)
-// and after all tokens dq_q = g * U_q, dgain = sum_q w_q * U_q.
+// and after all tokens dq_q = g * U_q, dgain = sum_q w_q * U_q.  A gradient of
+// the read's log-sum-exp (Block phase 1's lse output) adds alpha_qi dlse_q to
+// ds_qi, since d lse_q / d s_qi = alpha_qi.
 //
 // Structure: the forward's streaming layout.  One persistent CTA per SM;
 // thread 0 streams each tile's n_src source rows and n_q gradient rows into
@@ -57,6 +59,7 @@ struct ReadBwdArgs {
     const float *gain;              // [d] or nullptr
     float eps;
     const unsigned char *dout;      // [n_q][T][d]
+    const float *dlse;              // [n_q][T] gradient of each query's log-sum-exp, or nullptr
     unsigned char *dsrc;            // [n_src] x (dsrc_stride_bytes apart) [T][d]
     int64_t dsrc_stride_bytes;
     int accumulate;                 // 1: dsrc += gradient
@@ -295,7 +298,8 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
             const float esum = seg_sum<NS>(e);
             const float alpha = pv ? e / esum : 0.f;
             const float mean = seg_sum<NS>(alpha * sd);
-            const float ds = alpha * (sd - mean);
+            const float dl = (a.dlse != nullptr && pv && row_ok) ? __ldg(a.dlse + (int64_t)q * a.T + t) : 0.f;
+            const float ds = alpha * (sd - mean + dl);
             const float b = ds * rinv;
             float cpart = -ds * sw * rinv * rinv * rinv * inv_d;
             if (NQ == 2) cpart += __shfl_xor_sync(0xffffffffu, cpart, NS);

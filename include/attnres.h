@@ -271,6 +271,58 @@ attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_
                                           float *dgain, void *stream);
 
 /*
+ * Backward of Block phase 1 (attnres_block_phase1), whose outputs are the
+ * reads o_q and their log-sum-exp lse_q = log sum_i exp(s_qi): the gradients
+ * d_o of o and d_lse of lse (the phase-1 state's gradients, as the phase-2
+ * merge's backward returns them) give the sources', the queries' and the
+ * gain's gradients.  Since d lse_q / d s_qi = alpha_qi, the lse gradient adds
+ * alpha_qi d_lse_q to ds_qi of attnres_read_bwd's formula.  Defined by the
+ * b-lab.team summary, section 3 (Inference): phase 1 keeps (o, lse) per query.
+ *   d_o     [n_q][T][d] dtype dt;  d_lse [n_q][T] float, or NULL (zero)
+ * Every other argument, the workspace (attnres_read_bwd_workspace_size) and
+ * the limits are attnres_read_bwd's.
+ */
+attnres_status_t attnres_block_phase1_bwd(const void *src, int64_t n_src, int64_t src_stride,
+                                          int64_t T, int64_t d, attnres_dtype_t dt,
+                                          const float *queries, int64_t n_q, const float *gain,
+                                          float eps, const void *d_o, const float *d_lse, void *dsrc,
+                                          int64_t dsrc_stride, int accumulate, float *dqueries,
+                                          float *dgain, void *workspace, size_t workspace_bytes,
+                                          void *stream);
+
+/*
+ * Backward of the phase-2 merge (attnres_block_phase2_merge) for an output
+ * gradient dh.  Per token, with r_p = sqrt(mean(p^2) + eps),
+ * s_p = (w * g) . p / r_p, a = e^{lse-M} / (e^{lse-M} + e^{s_p-M}), b = 1 - a:
+ *   d_o       = a dh
+ *   d_lse     = a b (dh . (o - p))
+ *   d_partial = b dh - d_lse ((w * g) / r_p - p ((w * g) . p) / (d r_p^3))
+ *   dquery    = -g * sum_t d_lse p / r_p,   dgain = -w * sum_t d_lse p / r_p
+ * (a zero partial with eps = 0 passes nothing back through its score).
+ * Defined by the merge of the b-lab.team summary, section 3 (Inference,
+ * Phase 2), differentiated term by term.  partial == NULL (out = o): d_o = dh,
+ * d_lse = 0, dquery = dgain = 0, d_partial untouched.
+ *   o, partial, dh, d_o, d_partial  [T][d] dtype dt;  lse, d_lse [T] float
+ *   query, dquery, dgain            [d] float (dgain may be NULL)
+ *   accumulate  1: d_partial += its gradient (the partial sums several layers'
+ *               outputs, so their gradients add up); 0: overwritten
+ *   workspace   device scratch of attnres_block_phase2_bwd_workspace_size
+ *               bytes (16-byte aligned); sums over the tokens go through it
+ *               and are reduced in a fixed order (bitwise reproducible)
+ * No output may overlap an input, another output or the workspace.
+ */
+attnres_status_t attnres_block_phase2_bwd(const void *o, const float *lse, const void *partial,
+                                          int64_t T, int64_t d, attnres_dtype_t dt,
+                                          const float *query, const float *gain, float eps,
+                                          const void *dh, void *d_o, float *d_lse, void *d_partial,
+                                          int accumulate, float *dquery, float *dgain,
+                                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes attnres_block_phase2_bwd needs (no device work). */
+attnres_status_t attnres_block_phase2_bwd_workspace_size(int64_t T, int64_t d, attnres_dtype_t dt,
+                                                        size_t *bytes);
+
+/*
  * Backward of the MHAR read (mhar_fwd): H heads of d/H channels, each head its
  * own read over its slice, so the gradient of head h is attnres_read_bwd's
  * formula on that slice of the sources, output gradients, queries and gain,

@@ -239,3 +239,33 @@ def test_msar_two_phase_validation(lib):
     assert p2(out=A + 64) == INV                # overlaps the state
     assert p2(m=3) == UNS
     assert p2(part=A + 0x2000008) == UNS        # misaligned partial
+
+
+def test_two_phase_backward_validation(lib):
+    T, d = 16, 256
+    O, L, P, DH, DO, DL, DP, DQ, DG, WS = (A, B, A + 0x100000, A + 0x200000, B + 0x100000, B + 0x300000,
+                                           B + 0x200000, B + 0x400000, B + 0x500000, B + 0x600000)
+
+    def p2(o=O, lse=L, part=P, dh=DH, do=DO, dl=DL, dp=DP, acc=0, dq=DQ, dg=DG, ws=WS, T=T, d=d, eps=1e-6):
+        return lib.attnres_block_phase2_bwd(o, lse, part, T, d, BF16, B + 0x700000, None, eps, dh, do, dl, dp, acc,
+                                            dq, dg, ws, 1 << 20, None)
+    assert p2(T=0) not in (INV, UNS)
+    assert p2(o=None) == INV
+    assert p2(dh=None) == INV
+    assert p2(dp=None) == INV                     # a partial needs its gradient buffer
+    assert p2(acc=2) == INV
+    assert p2(eps=-1.0) == INV
+    assert p2(do=DH + 64) == INV                  # d_o overlaps dh
+    assert p2(dp=DO + 64) == INV                  # outputs overlap
+    assert p2(d=60) == UNS
+    assert p2(do=DO + 8) == UNS                   # misaligned
+    n = ctypes.c_size_t(0)
+    assert lib.attnres_block_phase2_bwd_workspace_size(T, d, BF16, None) == INV
+    assert lib.attnres_block_phase2_bwd_workspace_size(T, 60, BF16, ctypes.byref(n)) == UNS
+
+    def p1(dl=DL, dsrc=A + 0x1000000):
+        return lib.attnres_block_phase1_bwd(A, 8, T * d, T, d, BF16, B, 4, None, 1e-6, DH, dl, dsrc, T * d, 0,
+                                            DQ, DG, WS, 1 << 20, None)
+    assert p1(dsrc=None) == INV
+    assert p1(dl=A + 0x1000000 + 64) == INV       # d_lse overlaps dsrc
+    assert p1(dl=DL + 2) == UNS                   # misaligned d_lse

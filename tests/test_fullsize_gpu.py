@@ -248,3 +248,36 @@ def test_msar_two_phase_T32768_d4096_bench_workload():
         # elementwise bound of one rounding; the bf16 tolerance on the
         # output's scale (2e-2 of max |ref|) is the bar here.
         check_out(got, ref, BF16, strict=False, what=f"layer {s_ + 1}")
+
+
+def test_block_two_phase_backward_T32768_d4096():
+    """The backward of the headline Block step at full size: each layer's
+    merge backward (layers 2..4 with their partials, layer 1 without), then
+    phase 1's backward for all four layers' d_o and d_lse.  Sampled tokens'
+    source and partial gradients against the oracle's backward of the
+    one-shot reads."""
+    T, d, N, S = 32768, 4096, 8, 4
+    cache, q, parts = _device_block(T, d, N, S)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    dh = torch.randn((S, T, d), generator=g, device="cuda").to(BF16)
+    o, lse = attnres.attnres_block_phase1(cache, q)
+    d_o, d_lse = torch.empty_like(o), torch.empty_like(lse)
+    dparts = []
+    for s_ in range(S):
+        r = attnres.attnres_block_phase2_bwd(o[s_], lse[s_], parts[s_] if s_ > 0 else None, q[s_], dh[s_],
+                                             d_o=d_o[s_], d_lse=d_lse[s_])
+        dparts.append(r[2])
+    dsrc, _, _ = attnres.attnres_block_phase1_bwd(cache, q, d_o, d_lse)
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T)
+    c, p, h = rows(cache, idx), rows(parts, idx), rows(dh, idx)
+    qh = q.cpu().numpy().astype(np.float64)
+    ref_cached = np.zeros_like(c)
+    for s_ in range(S):
+        srcs = c if s_ == 0 else np.concatenate([c, p[s_][None]])
+        rs, _, _ = oracle.read_bwd(srcs, qh[s_][None], h[s_][None], None, 1e-6)
+        ref_cached += rs[:N]
+        if s_ > 0:
+            check_out(rows(dparts[s_], idx), rs[N], BF16, strict=False, what=f"layer {s_ + 1} d_partial")
+    check_out(rows(dsrc, idx), ref_cached, BF16, strict=False, what="cached sources' gradient")

@@ -442,6 +442,104 @@ def test_read_bwd_empty_sequence_zeroes_parameter_gradients():
     assert torch.count_nonzero(dq) == 0 and torch.count_nonzero(dg) == 0
 
 
+@pytest.mark.parametrize("n_src,n_q,T,d,dtype,with_lse", [
+    (8, 4, 64, 4096, BF16, True), (8, 4, 40, 2048, BF16, False), (3, 2, 37, 256, F32, True),
+    (9, 1, 50, 4096, BF16, True), (5, 3, 130, 1000, F32, True)])
+def test_block_phase1_bwd(n_src, n_q, T, d, dtype, with_lse):
+    """Block phase 1's backward (gradients of its o and lse outputs) against
+    the oracle; without d_lse it is the read's backward."""
+    rng = _rng(n_src * 3 + n_q * 5 + T + d)
+    src = _sources(rng, n_src, T, d, dtype, step=0.25)
+    q = _queries(rng, n_q, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    d_o = _sources(rng, n_q, T, d, dtype, step=0)
+    dl = rng.standard_normal((n_q, T)).astype(np.float32) if with_lse else None
+    got = attnres.attnres_block_phase1_bwd(to_dev(src, dtype), to_dev(q, F32), to_dev(d_o, dtype),
+                                           to_dev(dl, F32) if with_lse else None, to_dev(g, F32), 1e-6)
+    _check_grads(got, oracle.block_phase1_bwd(src, q, d_o, dl, g, 1e-6), dtype, f"n_q={n_q}")
+
+
+@pytest.mark.parametrize("T,d,dtype,with_gain,with_partial", [
+    (100, 4096, BF16, True, True), (37, 2048, BF16, False, True), (50, 256, F32, True, True),
+    (333, 1000, F32, True, True), (20, 512, BF16, True, False), (1, 64, F32, False, True)])
+def test_block_phase2_bwd(T, d, dtype, with_gain, with_partial):
+    """The merge's backward against the oracle: d_o, d_lse, d_partial, the
+    query's and the gain's gradients (no partial: d_o = dh, the rest zero)."""
+    rng = _rng(T + d + with_gain)
+    o = _sources(rng, 1, T, d, dtype)[0]
+    p = _sources(rng, 1, T, d, dtype, step=0)[0] * 1.5 if with_partial else None
+    if dtype == BF16 and p is not None:
+        p = inputs.bf16_round(p)
+    dh = _sources(rng, 1, T, d, dtype, step=0)[0]
+    lse = (rng.standard_normal(T) * 3).astype(np.float32)
+    q = _queries(rng, 1, d)[0]
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gain else None
+    got = attnres.attnres_block_phase2_bwd(to_dev(o, dtype), to_dev(lse, F32),
+                                           to_dev(p, dtype) if with_partial else None, to_dev(q, F32),
+                                           to_dev(dh, dtype), to_dev(g, F32) if with_gain else None, 1e-6)
+    ref = oracle.block_phase2_bwd(o, lse, p, q, dh, g, 1e-6)
+    check_out(got[0], ref[0], dtype, what="d_o")
+    check_out(got[1], ref[1], F32, np.abs(ref[1]).max() + 1e-30, strict=False, what="d_lse")
+    if with_partial:
+        check_out(got[2], ref[2], dtype, what="d_partial")
+    else:
+        assert got[2] is None
+    for name, x, y in (("dquery", got[3], ref[3]), ("dgain", got[4], ref[4])):
+        check_out(x, y, F32, np.abs(y).max() + 1e-30, strict=False, what=name)
+
+
+def test_block_phase2_bwd_accumulates_and_is_deterministic():
+    rng = _rng(81)
+    T, d = 300, 4096
+    o, p, dh = (to_dev(_sources(rng, 1, T, d, BF16, step=0)[0], BF16) for _ in range(3))
+    lse = to_dev((rng.standard_normal(T) * 3).astype(np.float32), F32)
+    q = to_dev(_queries(rng, 1, d)[0], F32)
+    a = attnres.attnres_block_phase2_bwd(o, lse, p, q, dh)
+    b = attnres.attnres_block_phase2_bwd(o, lse, p, q, dh)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    base = to_dev(_sources(rng, 1, T, d, BF16)[0], BF16)
+    acc = base.clone()
+    attnres.attnres_block_phase2_bwd(o, lse, p, q, dh, d_partial=acc, accumulate=True)
+    check_out(acc, to_host(base) + to_host(a[2]), BF16, what="accumulated d_partial")
+
+
+@pytest.mark.parametrize("dtype,N,S,T,d", [(BF16, 8, 4, 64, 4096), (F32, 3, 2, 45, 512), (BF16, 5, 3, 100, 1024)])
+def test_block_two_phase_backward_equals_one_shot(dtype, N, S, T, d):
+    """The GPU backward of a block's two-phase forward -- each layer's merge
+    backward, then phase 1's backward for all layers' d_o and d_lse -- against
+    the oracle's backward of the one-shot reads (layer 1 reads the cached
+    sources alone, layer s >= 2 also its partial)."""
+    rng = _rng(N * 11 + S + T)
+    cached = _sources(rng, N, T, d, dtype, step=0.25)
+    parts = _sources(rng, S, T, d, dtype, step=0)
+    q = _queries(rng, S, d)
+    dh = _sources(rng, S, T, d, dtype, step=0)
+    cd, qd = to_dev(cached, dtype), to_dev(q, F32)
+    o, lse = attnres.attnres_block_phase1(cd, qd)
+    d_o = torch.empty_like(o)
+    d_lse = torch.empty_like(lse)
+    dpart, dq2 = [None] * S, np.zeros((S, d))
+    for s_ in range(S):
+        r = attnres.attnres_block_phase2_bwd(o[s_], lse[s_], to_dev(parts[s_], dtype) if s_ > 0 else None, qd[s_],
+                                             to_dev(dh[s_], dtype), d_o=d_o[s_], d_lse=d_lse[s_])
+        dpart[s_], dq2[s_] = r[2], to_host(r[3])
+    dsrc, dq1, _ = attnres.attnres_block_phase1_bwd(cd, qd, d_o, d_lse)
+    ref_cached = np.zeros((N, T, d))
+    for s_ in range(S):
+        srcs = cached if s_ == 0 else np.concatenate([cached, parts[s_][None]])
+        rs, rq, _ = oracle.read_bwd(srcs, q[s_][None], dh[s_][None], None, 1e-6)
+        ref_cached += rs[:N]
+        if s_ > 0:
+            check_out(dpart[s_], rs[N], dtype, np.abs(rs[N]).max() * 4 + 1e-30, strict=False,
+                      what=f"layer {s_ + 1} d_partial")
+        # the chain's intermediates (o, d_o) are stored in the source dtype,
+        # so its parameter gradients carry that rounding
+        gq = to_host(dq1)[s_] + dq2[s_]
+        check_out(gq, rq[0], dtype, np.abs(rq[0]).max() + 1e-30, strict=False, what=f"layer {s_ + 1} dq")
+    check_out(dsrc, ref_cached, dtype, what="cached sources' gradient")
+
+
 @pytest.mark.parametrize("n_src,n_q,T,d,dtype", [(8, 3, 45, 2048, BF16), (5, 5, 30, 512, F32),
                                                   (9, 3, 25, 1024, BF16), (16, 2, 12, 2048, BF16)])
 def test_read_bwd_more_queries_than_one_pass(n_src, n_q, T, d, dtype):
