@@ -44,6 +44,7 @@ KERNEL_SOURCES = {
     "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
     "msar_phase1": [CSRC + "msar_phase1.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "msar_phase2": [CSRC + "msar_phase2.cu", CSRC + "msar.h", CSRC + "common.cuh"],
+    "merge_bwd": [CSRC + "merge_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_merge_bwd.cu"],
     "read_bwd_mh": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu", CSRC + "kernels_bwd_mh.cu"],
     "depth_read_decode": [CSRC + "depth_read_decode.cuh", CSRC + "common.cuh", CSRC + "kernels_decode.cu"],
 }
