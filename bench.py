@@ -9,9 +9,9 @@ reads no partial).  Inputs are synthetic, seeded, resident in HBM and larger
 than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
-same workload instead.  Other workloads (--workload mhar|msar|full_depth|
-block_d2048|block_fused|block_bwd|read_bwd|mhar_bwd|msar_block|decode) are for profiling and the
-design notes.
+same workload instead.  Other workloads (--workload mhar|mhar_block|msar|
+msar_block|msar_chunked|full_depth|block_d2048|block_fused|block_bwd|read_bwd|
+mhar_bwd|decode) are for profiling and the design notes.
 """
 from __future__ import annotations
 
@@ -724,6 +724,72 @@ class MharWorkload(BlockWorkload):
         return src.shape[1]
 
 
+class MharBlockWorkload(MharWorkload):
+    """MHAR inside the two-phase Block schedule at the MHAR size: phase 1 is
+    the MHAR read of the S=4 queries x H=8 heads over the N=8 cached reps
+    with each head's lse; layers 2..4 then merge their partial sums head by
+    head (mhar_phase2_merge, in place)."""
+
+    def __init__(self, T=131072, d=4096, N=8, S=4, H=8, seed=0):
+        super().__init__(T, d, N, S, H, seed)
+        self.name = "mhar_two_phase_block"
+        b = 2
+        self.phase1_bytes_per_token = N * d * b + S * d * b + S * H * 4
+        self.bytes_per_token = self.phase1_bytes_per_token + (S - 1) * (3 * d * b + H * 4)
+        self.launches_per_step = 1 + (S - 1)
+        self.dominant = "depth_read_mma_kernel (MHAR phase 1 with per-head lse)"
+        self.profile_tag = f"ncu_mhar_two_phase_d{d}_H{H}"
+
+    def setup(self, device):
+        import torch
+        super().setup(device)
+        T, d, S, H = self.T, self.d, self.S, self.H
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed + 11)
+        self.lse = torch.empty((S, H, T), dtype=torch.float32, device=device)
+        self.partials = torch.randn((S, T, d), generator=g, device=device).to(torch.bfloat16)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.mhar_fwd(self.cache, self.queries, None, 1e-6, out=self.o, lse=self.lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for i in range(1, self.S):
+            attnres.mhar_phase2_merge(self.o[i], self.lse[i], self.partials[i], self.queries[i], None, 1e-6,
+                                      out=self.o[i], stream=stream)
+
+    def setup_host(self):
+        super().setup_host()
+        self.h_parts = torch_pinned_like(self.partials[1:])
+        self.h2d += self.h_parts.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.partials[1:].copy_(self.h_parts, non_blocking=True)
+        self.queries.copy_(self.h_q, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.o, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        import torch
+        it = torch.from_numpy(idx).to(self.cache.device)
+        return (self.cache[:, it, :].float().cpu().numpy().astype(np.float64),
+                self.partials[:, it, :].float().cpu().numpy().astype(np.float64),
+                self.queries.cpu().numpy().astype(np.float64))
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        src, parts, q = sample
+        o, lse = oracle.mhar(src, q, None, 1e-6, want_lse=True)
+        for i in range(1, self.S):
+            oracle.mhar_phase2(o[i], lse[i], parts[i], q[i], None, 1e-6)
+        return src.shape[1]
+
+
 class MsarWorkload(BlockWorkload):
     """MSAR fused stream expansion + per-stream read + H^pre mixer."""
 
@@ -902,6 +968,39 @@ class MsarBlockWorkload(MsarWorkload):
         return len(wins)
 
 
+class MsarChunkedWorkload(MsarWorkload):
+    """Chunked prefill of the MSAR read: the T=32768 tokens in chunks of
+    4096, each call given the 11 rows before its chunk as the causal history
+    (msar_expand_fwd_chunk on strided views of the sources, nothing copied).
+    Same outputs as the one-call read, bit for bit."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0, chunk=4096):
+        super().__init__(T, d, N, seed)
+        self.name = "msar_chunked_prefill"
+        self.chunk = chunk
+        self.launches_per_step = (T + chunk - 1) // chunk
+        self.dominant = "msar_kernel (all chunks)"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} N={self.N} m=4 k=4/8/12 T={self.T} chunk={self.chunk}"
+        c["chunk"] = self.chunk
+        return c
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        hist = max(self.ks) - 1
+        if ev is not None:
+            ev[0].record(stream)
+        for c0 in range(0, self.T, self.chunk):
+            c1 = min(self.T, c0 + self.chunk)
+            h = min(hist, c0)
+            attnres.msar_expand_fwd_chunk(self.cache[:, c0 - h:c1], h, self.ks, self.conv_w, self.queries, None,
+                                          1e-6, None, self.mix_w, 1e-6, out=self.out[c0:c1], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+
 class FullDepthWorkload(BlockWorkload):
     """Full AttnRes at depth: 64 layers, layer l reads sources 0..l-1."""
 
@@ -987,6 +1086,10 @@ def make_workload(name, T=None):
         return ReadBwdWorkload(T=T or 32768)
     if name == "block_bwd":
         return BlockBwdWorkload(T=T or 32768)
+    if name == "mhar_block":
+        return MharBlockWorkload(T=T or 131072)
+    if name == "msar_chunked":
+        return MsarChunkedWorkload(T=T or 32768)
     if name == "mhar_bwd":
         return MharBwdWorkload(T=T or 131072)
     if name == "msar_block":
@@ -1239,7 +1342,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "decode", "mhar", "msar", "msar_block",
+                    choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
+                             "msar_chunked", "decode", "mhar", "msar", "msar_block",
                              "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
