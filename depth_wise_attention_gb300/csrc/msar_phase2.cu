@@ -94,7 +94,10 @@ __global__ void __launch_bounds__(MP2_THREADS, 1) msar_phase2_kernel(const MsarP
         slice = rem / ngroups;
         group = rem - slice * ngroups;
     };
-    const bool producer = tid == 0 && !a.wait.inject_stall;
+    // warp 0 produces: lane 0 arms the stage's mbarrier, then the warp's lanes
+    // share the item's row copies (one lane issuing ~40 copies would hold
+    // warp 0 back and every warp would wait for it at the next barrier)
+    const bool producer = warp == 0 && !a.wait.inject_stall;
     uint64_t pol = 0;
     if (producer) pol = l2_policy_evict_first();
     auto issue = [&](int i) {
@@ -107,15 +110,21 @@ __global__ void __launch_bounds__(MP2_THREADS, 1) msar_phase2_kernel(const MsarP
         const int nrows = (pass == 0 ? 0 : 4 * n) + (has_p ? n : 0);
         uint64_t *bar = &bars[i % MP2_NST];
         unsigned char *st = stages + (size_t)(i % MP2_NST) * SH::STAGE;
-        mbar_arrive_expect_tx(bar, rb * (uint32_t)nrows);
-        if (pass != 0)
-            for (int r = 0; r < 4; ++r)
-                for (int k = 0; k < n; ++k)
-                    bulk_g2s(st + (size_t)(r * G + k) * MP2_SW * ES, a.o + (((int64_t)r * T + tb + k) * d + c0) * ES,
-                             rb, bar, pol);
-        if (has_p)
-            for (int k = 0; k < n; ++k)
-                bulk_g2s(st + (size_t)(4 * G + k) * MP2_SW * ES, a.partial + ((tb + k) * d + c0) * ES, rb, bar, pol);
+        if (lane == 0) mbar_arrive_expect_tx(bar, rb * (uint32_t)nrows);
+        __syncwarp();
+        // copy j < 4n: state row (stream j / n, token j % n); then the partial's rows
+        const int nstate = pass == 0 ? 0 : 4 * n;
+        for (int j = lane; j < nrows; j += 32) {
+            if (j < nstate) {
+                const int r = j / n, k = j - r * n;
+                bulk_g2s(st + (size_t)(r * G + k) * MP2_SW * ES, a.o + (((int64_t)r * T + tb + k) * d + c0) * ES,
+                         rb, bar, pol);
+            } else {
+                const int k = j - nstate;
+                bulk_g2s(st + (size_t)(4 * G + k) * MP2_SW * ES, a.partial + ((tb + k) * d + c0) * ES, rb, bar,
+                         pol);
+            }
+        }
     };
     int issued = 0;
     if (producer)
@@ -320,11 +329,14 @@ __global__ void __launch_bounds__(MP2_THREADS, 1) msar_phase2_kernel(const MsarP
             }
         }
         __syncthreads();                         // every thread is done with stage i
-        if (producer && issued < nitems && !*abort_flag) issue(issued++);
+        if (producer) {
+            // one decision for the whole producer warp
+            if (__shfl_sync(0xffffffffu, (issued < nitems && !*abort_flag) ? 1 : 0, 0)) issue(issued++);
+        }
     }
 
     // Drain (only matters after an abort): copies must land before exit.
-    if (producer) {
+    if (producer && lane == 0) {
         int never = 0;
         for (int i = issued > MP2_NST ? issued - MP2_NST : 0; i < issued; ++i)
             mbar_wait_bounded(&bars[i % MP2_NST], (uint32_t)(i / MP2_NST) & 1u, &never, a.wait);
