@@ -30,6 +30,7 @@ SOURCES = [
     "kernels_mma_multi.cu",
     "kernels_bwd.cu",
     "kernels_bwd_mh.cu",
+    "kernels_bwd_qg.cu",
     "kernels_merge_bwd.cu",
     "kernels_decode.cu",
     "msar.cu",

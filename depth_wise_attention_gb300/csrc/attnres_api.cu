@@ -500,13 +500,10 @@ struct ReadBwdShape {
     int vph;        // 16-byte vectors per head
 };
 
-attnres_status_t read_bwd_shape(int64_t n_src, int64_t d, int64_t n_q, int64_t H, attnres_dtype_t dt,
-                                ReadBwdShape *sh) {
+attnres_status_t read_bwd_shape_for(int64_t n_src, int64_t d, int nqc, int64_t H, attnres_dtype_t dt,
+                                    ReadBwdShape *sh) {
     const int nvec = (int)(d / epv(dt));
-    sh->ns = n_src <= 8 ? 8 : 16;
-    if (n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
-    sh->nqc = sh->ns == 16 ? 1 : 2;
-    if (n_q < sh->nqc) sh->nqc = (int)n_q;
+    sh->nqc = nqc;
     row_shape(nvec, &sh->tpr, &sh->vpt);
     sh->tt = RB_THREADS / sh->tpr;
     // a tile holds n_src + nqc rows of tt tokens and two stages must fit:
@@ -533,6 +530,25 @@ attnres_status_t read_bwd_shape(int64_t n_src, int64_t d, int64_t n_q, int64_t H
     return ATTNRES_OK;
 }
 
+// max_nqc: at most this many queries per launch (0: no limit beyond the kernels')
+attnres_status_t read_bwd_shape(int64_t n_src, int64_t d, int64_t n_q, int64_t H, attnres_dtype_t dt,
+                                ReadBwdShape *sh, int max_nqc = 0) {
+    if (n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    sh->ns = n_src <= 8 ? 8 : 16;
+    // queries per launch: up to 4 (two groups of two over the same staged
+    // sources) with at most 8 sources where that kernel exists, else 2 (1
+    // with more than 8 sources)
+    const int base = sh->ns == 16 ? 1 : 2;
+    if (sh->ns == 8 && n_q > 2 && (max_nqc == 0 || max_nqc > 2)) {
+        const int want = n_q < 4 ? (int)n_q : 4;
+        KernelRef kr;
+        if (read_bwd_shape_for(n_src, d, want, H, dt, sh) == ATTNRES_OK &&
+            lookup_read_bwd_qg(dt == ATTNRES_BF16 ? 1 : 0, sh->vpt, sh->mh, sh->hg, &kr))
+            return ATTNRES_OK;
+    }
+    return read_bwd_shape_for(n_src, d, n_q < base ? (int)n_q : base, H, dt, sh);
+}
+
 // Per-(CTA, row) partials of U for one pass of queries: one CTA per SM at most.
 size_t read_bwd_ws_bytes(int sms, const ReadBwdShape &sh, int64_t d) {
     return (size_t)sms * (size_t)sh.tt * (size_t)sh.nqc * (size_t)d * sizeof(float);
@@ -542,7 +558,7 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
                                  int64_t H, attnres_dtype_t dt, const float *queries, int64_t n_q,
                                  const float *gain, float eps, const void *dout, const float *dlse, void *dsrc,
                                  int64_t dsrc_stride, int accumulate, float *dq, float *dgain, void *ws,
-                                 size_t ws_bytes, void *stream) {
+                                 size_t ws_bytes, void *stream, int max_nqc = 0) {
     attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
     if (st != ATTNRES_OK) return st;
     if (n_q < 1 || (accumulate != 0 && accumulate != 1)) return ATTNRES_ERR_INVALID_ARG;
@@ -562,7 +578,7 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
     if (dlse && (H != 1 || overlap(dsrc, dsrc_bytes, dlse, (size_t)n_q * (size_t)T * 4)))
         return ATTNRES_ERR_INVALID_ARG;
     ReadBwdShape sh;
-    st = read_bwd_shape(n_src, d, n_q, H, dt, &sh);
+    st = read_bwd_shape(n_src, d, n_q, H, dt, &sh, max_nqc);
     if (st != ATTNRES_OK) return st;
     if (!aligned16(dout) || !aligned16(dsrc) || (dsrc_stride * (int64_t)es) % 16 != 0 || !aligned16(queries) ||
         (gain && !aligned16(gain)) || !aligned4(dq) || (dgain && !aligned4(dgain)) || !aligned16(ws) ||
@@ -578,13 +594,16 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
     }
     if (ws_bytes < read_bwd_ws_bytes(dev->sms, sh, d)) return ATTNRES_ERR_INVALID_ARG;
-    // kernels of every pass (a last pass may take fewer queries)
+    // kernels of every pass (a last pass may take fewer queries): up to 2
+    // queries one group, 3 or 4 two groups of two
     KernelRef kr[2];
     const int nq_last = (int)(n_q - (n_q - 1) / sh.nqc * sh.nqc);
     for (int v = 0; v < 2; ++v) {
         const int nq = v == 0 ? sh.nqc : nq_last;
-        const bool ok = sh.mh ? lookup_read_bwd_mh(dt == ATTNRES_BF16 ? 1 : 0, nq, sh.ns, sh.vpt, sh.hg, &kr[v])
-                              : lookup_read_bwd(dt == ATTNRES_BF16 ? 1 : 0, nq, sh.ns, sh.vpt, &kr[v]);
+        const int dti = dt == ATTNRES_BF16 ? 1 : 0;
+        const bool ok = nq > 2 ? lookup_read_bwd_qg(dti, sh.vpt, sh.mh, sh.hg, &kr[v])
+                        : sh.mh ? lookup_read_bwd_mh(dti, nq, sh.ns, sh.vpt, sh.hg, &kr[v])
+                                : lookup_read_bwd(dti, nq, sh.ns, sh.vpt, &kr[v]);
         if (!ok) return ATTNRES_ERR_UNSUPPORTED;
     }
     const uint32_t row_pitch = (uint32_t)((size_t)sh.tt * (size_t)d * es);
@@ -1027,18 +1046,29 @@ attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_
                                           const float *gain, float eps, const void *dout, void *dsrc,
                                           int64_t dsrc_stride, int accumulate, float *dqueries, float *dgain,
                                           void *stream) {
-    size_t need = 0;
+    // queries per pass: as many as the kernels take, unless their workspace
+    // outgrows the scratch array (then passes of two)
+    int max_nqc = 0;
     if (T > 0) {
+        size_t need = 0;
         attnres_status_t st = attnres_read_bwd_workspace_size(n_src, T, d, n_q, dt, &need);
         if (st != ATTNRES_OK) return st;
-        if (need > kBwdScratchFloats * sizeof(float)) return ATTNRES_ERR_UNSUPPORTED;
+        if (need > kBwdScratchFloats * sizeof(float)) {
+            ReadBwdShape sh;
+            DeviceInfo *dev = nullptr;
+            st = read_bwd_shape(n_src, d, n_q, 1, dt, &sh, 2);
+            if (st == ATTNRES_OK) st = device_info(&dev);
+            if (st != ATTNRES_OK) return st;
+            if (read_bwd_ws_bytes(dev->sms, sh, d) > kBwdScratchFloats * sizeof(float)) return ATTNRES_ERR_UNSUPPORTED;
+            max_nqc = 2;
+        }
     }
     void *ws = nullptr;
     attnres_status_t st = bwd_scratch(&ws);
     if (st != ATTNRES_OK) return st;
     return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, nullptr, dsrc,
-                           dsrc_stride,
-                           accumulate, dqueries, dgain, ws, kBwdScratchFloats * sizeof(float), stream);
+                           dsrc_stride, accumulate, dqueries, dgain, ws, kBwdScratchFloats * sizeof(float), stream,
+                           max_nqc);
 }
 
 attnres_status_t attnres_block_phase1_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,

@@ -33,6 +33,8 @@ bool lookup_depth_read_decode(int dt, int nq, int ns, KernelRef *out);
 // read_bwd_kernel<T, nq, ns, vpt> (nq queries, at most ns sources) and the
 // workspace reduction kernel that finishes dq and dgain
 bool lookup_read_bwd(int dt, int nq, int ns, int vpt, KernelRef *out);
+// read_bwd_kernel with two query groups of two (up to 4 queries, <= 8 sources) per launch
+bool lookup_read_bwd_qg(int dt, int vpt, bool mh, int hg, KernelRef *out);
 // merge_bwd_kernel<T, vpt>: backward of the Block phase-2 merge
 bool lookup_merge_bwd(int dt, int vpt, KernelRef *out);
 // read_bwd_kernel in per-head mode (MHAR backward), hg reduction groups per warp

@@ -32,6 +32,12 @@
 // warp's VPT runs lie in one head and its values are reduced together; with
 // HG == VPT each run is its own group.  The coefficient lanes of a group sum
 // the table entries of all groups of its head.
+//
+// Query groups (QG): with QG == 2 one launch takes up to 2 * NQ queries.  The
+// stage holds every query's gradient rows; each tile runs passes A and B
+// once per group of NQ queries on the same staged sources, so the sources
+// are read from memory once, and the second group adds into the dsrc rows
+// the first group of the same tile has just written (L2-resident).
 #pragma once
 
 #include "common.cuh"
@@ -92,7 +98,7 @@ struct RBLayout {
     __host__ __device__ static constexpr int isd(int q, int i) { return NS + NQ * NS + q * NS + i; }
 };
 
-template <typename Tin, int NQ, int NS, int VPT, bool MH = false, int HG = 1>
+template <typename Tin, int NQ, int NS, int VPT, bool MH = false, int HG = 1, int QG = 1>
 __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdArgs a) {
     using E = Elem<Tin>;
     using L = RBLayout<NQ, NS, HG>;
@@ -159,25 +165,29 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
     const float inv_d = a.inv_dh;
     int vid[VPT];
     bool vok[VPT];
-    float2 wg[NQ][VPT][NP];       // w_q * g on this thread's channels
-    float2 U[NQ][VPT][NP];        // sum over tokens of sum_i b_qi v_i
+    float2 wg[QG][NQ][VPT][NP];   // w_q * g on this thread's channels, per query group
+    float2 U[QG][NQ][VPT][NP];    // sum over tokens of sum_i b_qi v_i
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         vid[k] = MH ? (wr * VPT + k) * 32 + lane : k * a.tpr + tr;
         vok[k] = vid[k] < a.nvec;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)
+        for (int qg = 0; qg < QG; ++qg)
 #pragma unroll
-            for (int p = 0; p < NP; ++p) {
-                float2 w = make_float2(0.f, 0.f);
-                if (q < a.n_q && vok[k]) {
-                    const int c = vid[k] * EPV + 2 * p;
-                    w = make_float2(__ldg(a.queries + (size_t)q * a.d + c), __ldg(a.queries + (size_t)q * a.d + c + 1));
-                    if (a.gain) { w.x *= __ldg(a.gain + c); w.y *= __ldg(a.gain + c + 1); }
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    const int qq = qg * NQ + q;
+                    float2 w = make_float2(0.f, 0.f);
+                    if (qq < a.n_q && vok[k]) {
+                        const int c = vid[k] * EPV + 2 * p;
+                        w = make_float2(__ldg(a.queries + (size_t)qq * a.d + c),
+                                        __ldg(a.queries + (size_t)qq * a.d + c + 1));
+                        if (a.gain) { w.x *= __ldg(a.gain + c); w.y *= __ldg(a.gain + c + 1); }
+                    }
+                    wg[qg][q][k][p] = w;
+                    U[qg][q][k][p] = make_float2(0.f, 0.f);
                 }
-                wg[q][k][p] = w;
-                U[q][k][p] = make_float2(0.f, 0.f);
-            }
     }
     // table offset of each value this lane holds after the butterfly: value
     // jj of local group g goes to [jj][wr * HG + g] of the row's table
@@ -211,6 +221,11 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
         const bool row_ok = t < a.T;
         mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
         const unsigned char *sb = stages + (size_t)s * a.stage_bytes + (size_t)r * a.d * E::BYTES;
+#pragma unroll
+        for (int qg = 0; qg < QG; ++qg) {
+        const int q0 = qg * NQ;             // first query of this group
+        // the second group adds into the rows the first one has written
+        const bool acc = qg > 0 || a.accumulate;
 
         // ---------------- pass A: sum(v^2), (w*g).v, dout.v per source
         float2 dl[NQ][VPT][NP];   // this token's output gradients on my channels
@@ -218,8 +233,8 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
         for (int q = 0; q < NQ; ++q)
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                if (q < a.n_q && vok[k]) {
-                    E::unpack(*reinterpret_cast<const uint4 *>(sb + (size_t)(a.n_src + q) * a.row_pitch +
+                if (q0 + q < a.n_q && vok[k]) {
+                    E::unpack(*reinterpret_cast<const uint4 *>(sb + (size_t)(a.n_src + q0 + q) * a.row_pitch +
                                                                (size_t)vid[k] * 16),
                               dl[q][k]);
                 } else {
@@ -250,7 +265,7 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
                         ss[g] = ffma2(x[p], x[p], ss[g]);
 #pragma unroll
                         for (int q = 0; q < NQ; ++q) {
-                            sw[g][q] = ffma2(x[p], wg[q][k][p], sw[g][q]);
+                            sw[g][q] = ffma2(x[p], wg[qg][q][k][p], sw[g][q]);
                             sd[g][q] = ffma2(x[p], dl[q][k][p], sd[g][q]);
                         }
                     }
@@ -267,20 +282,20 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
             }
         }
         butterfly_reduce<HG * V>(v, lane);
-        float *rrow = red + (size_t)(it & 1) * (RB_THREADS / 32) * HG * V + (size_t)r * ngr * V;
+        float *rrow = red + (size_t)((it * QG + qg) & 1) * (RB_THREADS / 32) * HG * V + (size_t)r * ngr * V;
 #pragma unroll
         for (int j = 0; j < R; ++j)
             if (slot_off[j] >= 0) rrow[slot_off[j]] = v[j];
         __syncthreads();
         // every warp has finished item it-1: refill its stage for item it-1+nstages
-        if (producer && it >= 1 && issued < n_items && !*abort_flag) { issue_next(); ++issued; }
+        if (qg == 0 && producer && it >= 1 && issued < n_items && !*abort_flag) { issue_next(); ++issued; }
 
         // ---------------- per-token coefficients: lane (q, i) = q*NS + i, for
         // each group of this warp (its head's table groups summed)
 #pragma unroll
         for (int g = 0; g < HG; ++g) {
             const int q = lane / NS, i = lane - q * NS;
-            const bool pv = q < NQ && q < a.n_q && i < a.n_src;
+            const bool pv = q < NQ && q0 + q < a.n_q && i < a.n_src;
             float ss = 0.f, sw = 0.f, sd = 0.f;
             if (q < NQ) {
                 for (int w = g_first[g]; w < g_first[g] + g_count; ++w) {
@@ -298,7 +313,7 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
             const float esum = seg_sum<NS>(e);
             const float alpha = pv ? e / esum : 0.f;
             const float mean = seg_sum<NS>(alpha * sd);
-            const float dl = (a.dlse != nullptr && pv && row_ok) ? __ldg(a.dlse + (int64_t)q * a.T + t) : 0.f;
+            const float dl = (a.dlse != nullptr && pv && row_ok) ? __ldg(a.dlse + (int64_t)(q0 + q) * a.T + t) : 0.f;
             const float ds = alpha * (sd - mean + dl);
             const float b = ds * rinv;
             float cpart = -ds * sw * rinv * rinv * rinv * inv_d;
@@ -321,7 +336,7 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
             // formed (with 4 vectors a thread, where registers are short, at use)
             constexpr bool EARLY = VPT <= 2;
             uint4 zraw[VPT];
-            if (EARLY && a.accumulate) {
+            if (EARLY && acc) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k)
                     if (vok[k])
@@ -351,23 +366,26 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
 #pragma unroll
                     for (int q = 0; q < NQ; ++q) {
                         y[p] = ffma2(make_float2(al[q], al[q]), dl[q][k][p], y[p]);
-                        y[p] = ffma2(make_float2(bq[q], bq[q]), wg[q][k][p], y[p]);
-                        U[q][k][p] = ffma2(make_float2(bq[q], bq[q]), x[p], U[q][k][p]);
+                        y[p] = ffma2(make_float2(bq[q], bq[q]), wg[qg][q][k][p], y[p]);
+                        U[qg][q][k][p] = ffma2(make_float2(bq[q], bq[q]), x[p], U[qg][q][k][p]);
                     }
                 }
                 if (!*abort_flag) {
                     unsigned char *gp = a.dsrc + (int64_t)i * a.dsrc_stride_bytes +
                                         (t * a.d + (int64_t)vid[k] * EPV) * E::BYTES;
-                    if (a.accumulate) {
+                    if (acc) {
                         float2 z[NP];
                         E::unpack(EARLY ? zraw[k] : *reinterpret_cast<const uint4 *>(gp), z);
 #pragma unroll
                         for (int p = 0; p < NP; ++p) y[p] = make_float2(y[p].x + z[p].x, y[p].y + z[p].y);
                     }
-                    stg128_cs(gp, E::pack(y));
+                    // the first of two groups keeps its rows in L2 for the second
+                    if (QG > 1 && qg == 0) *reinterpret_cast<uint4 *>(gp) = E::pack(y);
+                    else stg128_cs(gp, E::pack(y));
                 }
             }
         }
+        }  // query groups
         if (++s == a.nstages) { s = 0; par ^= 1u; }
         tile += gstride;
     }
@@ -376,13 +394,16 @@ __global__ void __launch_bounds__(RB_THREADS, 1) read_bwd_kernel(const ReadBwdAr
     if (!*abort_flag) {
         float *wrow = a.ws + ((size_t)blockIdx.x * a.tt + r) * (size_t)a.n_q * a.d;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)
+        for (int qg = 0; qg < QG; ++qg)
 #pragma unroll
-            for (int k = 0; k < VPT; ++k)
-                if (q < a.n_q && vok[k])
+            for (int q = 0; q < NQ; ++q)
 #pragma unroll
-                    for (int p = 0; p < NP; ++p)
-                        *reinterpret_cast<float2 *>(wrow + (size_t)q * a.d + vid[k] * EPV + 2 * p) = U[q][k][p];
+                for (int k = 0; k < VPT; ++k)
+                    if (qg * NQ + q < a.n_q && vok[k])
+#pragma unroll
+                        for (int p = 0; p < NP; ++p)
+                            *reinterpret_cast<float2 *>(wrow + (size_t)(qg * NQ + q) * a.d + vid[k] * EPV + 2 * p) =
+                                U[qg][q][k][p];
     }
     if (producer) {
         int never = 0;

@@ -39,3 +39,24 @@ def test_noalloc_backward_rejects_sizes_beyond_its_scratch():
         pytest.skip("this device's largest backward fits the built-in scratch")
     with pytest.raises(attnres.AttnResError):
         attnres.attnres_read_bwd_noalloc(src, q, dout)
+
+
+def test_noalloc_backward_with_four_queries_at_d4096():
+    """Four queries at d = 4096 would need a 10 MB workspace in one pass; the
+    no-allocation backward then takes passes of two within its 8 MB scratch,
+    and its gradients agree with the oracle."""
+    import numpy as np
+    from _helpers import check_out, to_host
+    from oracle import oracle
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    n_src, n_q, T, d = 8, 4, 40, 4096
+    src = (torch.randn((n_src, T, d), generator=g, device="cuda") *
+           (1 + 0.25 * torch.arange(n_src, device="cuda"))[:, None, None]).to(torch.bfloat16)
+    q = torch.randn((n_q, d), generator=g, device="cuda") * (16.0 / d) ** 0.5
+    dout = torch.randn((n_q, T, d), generator=g, device="cuda").to(torch.bfloat16)
+    dsrc, dq, dg = attnres.attnres_read_bwd_noalloc(src, q, dout)
+    ref = oracle.read_bwd(to_host(src).astype(np.float64), to_host(q).astype(np.float64),
+                          to_host(dout).astype(np.float64), None, 1e-6)
+    check_out(dsrc, ref[0], torch.bfloat16, what="dsrc")
+    check_out(dq, ref[1], torch.float32, np.abs(ref[1]).max(), strict=False, what="dq")
