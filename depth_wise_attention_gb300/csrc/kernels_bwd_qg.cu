@@ -17,11 +17,11 @@ static KernelRef rbq_ref() {
 #define ATTNRES_RBQ_CASE(T, VPT, MH, HG) \
     if (vpt == VPT && mh == MH && hg == HG) { *out = rbq_ref<T, VPT, MH, HG>(); return true; }
 
-// bf16 with 4 vectors a thread keeps one query group (two groups spill)
+// bf16 with 4 vectors a thread, or with one reduction group per run of a
+// warp, keeps one query group per launch (two groups spill registers there)
 static bool rbq_lookup_bf16(int vpt, bool mh, int hg, KernelRef *out) {
     ATTNRES_RBQ_CASE(__nv_bfloat16, 1, false, 1) ATTNRES_RBQ_CASE(__nv_bfloat16, 2, false, 1)
     ATTNRES_RBQ_CASE(__nv_bfloat16, 1, true, 1) ATTNRES_RBQ_CASE(__nv_bfloat16, 2, true, 1)
-    ATTNRES_RBQ_CASE(__nv_bfloat16, 2, true, 2)
     return false;
 }
 
