@@ -659,6 +659,41 @@ fail:
     return -1;
 }
 
+/* MSAR read with each source's own conv kernels: source i is expanded with
+ * the kernels packed at conv_w + i * conv_src_stride (as oracle_msar's
+ * conv_w for that source; the streams of a source are the source's own,
+ * [MSAR §무엇과 다른가] v_i^(r)); the per-stream reads and the mixer are
+ * oracle_msar's.  conv_src_stride = 0 is oracle_msar. */
+int oracle_msar_ps(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                   const int32_t *ksizes, const double *conv_w, int64_t conv_src_stride,
+                   const double *queries, const double *gain, double eps, const double *mix_gain,
+                   const double *mix_w, double mix_eps, double *out)
+{
+    if (!src || !ksizes || !conv_w || !queries || !mix_w || !out || n_src < 1 || T < 0 || d < 1 ||
+        m < 1 || eps < 0 || mix_eps < 0 || conv_src_stride < 0) return -1;
+    size_t per = (size_t)T * (size_t)d;
+    /* u[i][r][T][d] */
+    double *u = (double *)malloc(sizeof(double) * (size_t)n_src * (size_t)m * per + 1);
+    double *Z = (double *)malloc(sizeof(double) * (size_t)m * (size_t)d + 1);
+    double *zf = (double *)malloc(sizeof(double) * (size_t)m * (size_t)d + 1);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)m);
+    const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_src);
+    int rc = (u && Z && zf && logit && rows) ? 0 : -1;
+    for (int64_t i = 0; i < n_src && rc == 0; ++i)
+        rc = msar_expand(src + (size_t)i * per, T, d, m, ksizes, conv_w + i * conv_src_stride,
+                         u + (size_t)i * (size_t)m * per);
+    for (int64_t t = 0; t < T && rc == 0; ++t) {
+        for (int64_t r = 0; r < m && rc == 0; ++r) {
+            for (int64_t i = 0; i < n_src; ++i)
+                rows[i] = u + ((size_t)i * (size_t)m + (size_t)r) * per + (size_t)t * (size_t)d;
+            rc = read_one(rows, n_src, d, queries + r * d, gain, eps, Z + r * d, NULL, NULL);
+        }
+        if (rc == 0) msar_mix(Z, m, d, mix_gain, mix_w, mix_eps, zf, logit, out + t * d, NULL);
+    }
+    free(u); free(Z); free(zf); free(logit); free(rows);
+    return rc;
+}
+
 /* MSAR inside the two-phase Block schedule, phase 1.  [MSAR §어떻게 쓰나]:
  * AttnRes's two-phase computation carries over to MSAR unchanged: every
  * target query of the block is read against the completed sources in one

@@ -702,6 +702,58 @@ def test_msar_window_read_equals_full_sequence():
         assert np.allclose(win[-1], base[t], atol=1e-14)
 
 
+def test_msar_per_source_with_equal_kernels_is_msar():
+    """Every source given the same kernels is the shared-kernel read."""
+    rng = np.random.default_rng(81)
+    N, T, d, ks = 4, 15, 8, (4, 8, 12)
+    src, q = _rand(rng, N, T, d), _rand(rng, 4, d, scale=2.0)
+    cw, P = _rand(rng, d * sum(ks), scale=0.4), _rand(rng, 4 * d, 4, scale=0.2)
+    a = oracle.msar_ps(src, ks, np.stack([cw] * N), q, None, 1e-6, None, P, 1e-6)
+    b = oracle.msar(src, ks, cw, q, None, 1e-6, None, P, 1e-6)
+    assert np.allclose(a, b, atol=1e-13, rtol=0)
+
+
+def test_msar_per_source_delay_kernels_are_delayed_sources():
+    """Source i's kernels all delta taps at delay j_i: its conv streams are
+    the source delayed by j_i rows (zero before the sequence).  With stream
+    queries that see only stream 1 and a zero mixer, the read of stream 1 is
+    the Full read of the delayed sources, which the output is twice of."""
+    rng = np.random.default_rng(82)
+    N, T, d, ks = 3, 12, 8, (4, 4, 4)
+    src = _rand(rng, N, T, d)
+    delays = (0, 2, 3)
+    cw = np.zeros((N, d * sum(ks)))
+    for i, j in enumerate(delays):
+        for r in range(3):
+            k = np.zeros((d, 4))
+            k[:, j] = 1.0
+            cw[i, d * 4 * r: d * 4 * (r + 1)] = k.ravel()
+    w = _rand(rng, d, scale=2.0)
+    q = np.stack([w] * 4)
+    out = oracle.msar_ps(src, ks, cw, q, None, 1e-6, None, np.zeros((4 * d, 4)), 1e-6)
+    delayed = np.zeros_like(src)
+    for i, j in enumerate(delays):
+        delayed[i, j:] = src[i, :T - j]
+    # streams 1..3 each read the delayed sources; stream 0 reads the sources
+    ref = 0.5 * oracle.full(src, w, None, eps=1e-6) + 1.5 * oracle.full(delayed, w, None, eps=1e-6)
+    assert np.allclose(out, ref, atol=1e-12)
+
+
+def test_msar_per_source_permutation_equivariant():
+    """Permuting the sources together with their kernels leaves the read
+    unchanged (each stream's softmax is over a set of sources)."""
+    rng = np.random.default_rng(83)
+    N, T, d, ks = 5, 14, 8, (4, 8, 12)
+    src, q = _rand(rng, N, T, d), _rand(rng, 4, d, scale=2.0)
+    cw, P = _rand(rng, N, d * sum(ks), scale=0.4), _rand(rng, 4 * d, 4, scale=0.2)
+    perm = np.array([3, 0, 4, 1, 2])
+    a = oracle.msar_ps(src, ks, cw, q, None, 1e-6, None, P, 1e-6)
+    b = oracle.msar_ps(src[perm], ks, cw[perm], q, None, 1e-6, None, P, 1e-6)
+    assert np.allclose(a, b, atol=1e-12, rtol=0)
+    c = oracle.msar_ps(src[perm], ks, cw, q, None, 1e-6, None, P, 1e-6)
+    assert np.abs(a - c).max() > 1e-3        # kernels must travel with their sources
+
+
 def _msar_block_inputs(rng, N, S, T, d, ks=(4, 8, 12)):
     cached = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
     parts = _rand(rng, S, T, d)

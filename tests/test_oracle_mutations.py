@@ -49,6 +49,7 @@ MUTANTS = {
     "msar_phase2_partial_identity_streams": [("if (rc == 0 && partial) rc = msar_expand(partial, T, d, m, ksizes, conv_w, up);",
                                               "if (rc == 0 && partial) rc = msar_expand(partial, T, d, 1, ksizes, conv_w, up);\n    for (int64_t r = 1; r < m && up; ++r) memcpy(up + (size_t)r * per, partial, sizeof(double) * per);")],
     "msar_phase2_lse_of_stream_zero": [("const double l = lse[r * T + t];", "const double l = lse[t];")],
+    "msar_ps_first_source_kernels": [("conv_w + i * conv_src_stride,", "conv_w,")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
