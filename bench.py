@@ -10,7 +10,7 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|mhar_block|msar|
-msar_block|msar_chunked|full_depth|block_d2048|block_fused|block_bwd|read_bwd|
+msar_block|msar_chunked|msar_ps|full_depth|block_d2048|block_fused|block_bwd|read_bwd|
 mhar_bwd|decode) are for profiling and the design notes.
 """
 from __future__ import annotations
@@ -968,6 +968,42 @@ class MsarBlockWorkload(MsarWorkload):
         return len(wins)
 
 
+class MsarPerSourceWorkload(MsarWorkload):
+    """The MSAR read with each of the N=8 sources' own conv kernels
+    (msar_expand_fwd_ps): kernels ~ N(0, 1/k) per source, read through L2."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0):
+        super().__init__(T, d, N, seed)
+        self.name = "msar_per_source_kernels"
+        self.dominant = "msar_kernel (per-source kernels)"
+        self.profile_tag = f"ncu_msar_per_source_d{d}"
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        super().setup(device)
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed + 5)
+        self.conv_w = torch.stack([torch.cat([inputs.device_normal((self.d * k,), (1.0 / k) ** 0.5, g, device=device)
+                                              for k in self.ks]) for _ in range(self.N)])
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.msar_expand_fwd_ps(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, None, self.mix_w,
+                                   1e-6, out=self.out, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        wins, cw, q, mw = sample
+        for w in wins:
+            oracle.msar_ps(w, self.ks, cw, q, None, 1e-6, None, mw, 1e-6)
+        return len(wins)
+
+
 class MsarChunkedWorkload(MsarWorkload):
     """Chunked prefill of the MSAR read: the T=32768 tokens in chunks of
     4096, each call given the 11 rows before its chunk as the causal history
@@ -1088,6 +1124,8 @@ def make_workload(name, T=None):
         return BlockBwdWorkload(T=T or 32768)
     if name == "mhar_block":
         return MharBlockWorkload(T=T or 131072)
+    if name == "msar_ps":
+        return MsarPerSourceWorkload(T=T or 32768)
     if name == "msar_chunked":
         return MsarChunkedWorkload(T=T or 32768)
     if name == "mhar_bwd":
@@ -1343,7 +1381,7 @@ def main():
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="block",
                     choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
-                             "msar_chunked", "decode", "mhar", "msar", "msar_block",
+                             "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block",
                              "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)

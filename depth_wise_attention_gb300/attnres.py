@@ -49,6 +49,8 @@ _SIGS = {
                  _vp],
     "msar_expand_fwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f,
                         _vp, _vp, _f, _vp, _vp],
+    "msar_expand_fwd_ps": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _i64, _vp, _vp, _f, _vp,
+                           _vp, _f, _vp, _vp],
     "msar_block_phase1": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _i64, _vp, _f, _vp,
                           _vp, _vp],
     "msar_block_phase2": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
@@ -464,4 +466,20 @@ def msar_block_phase2(o, lse, partial, ksizes, conv_w, query, gain=None, eps=1e-
     _check("msar_block_phase2", load().msar_block_phase2(
         _p(o), _p(lse), _p(partial), T, d, _dt(o), m, ctypes.cast(ks, _vp), _p(conv_w), _p(query), _p(gain), eps,
         _p(mix_gain), _p(mix_w), mix_eps, _p(out), _stream(stream)))
+    return out
+
+
+def msar_expand_fwd_ps(src, ksizes, conv_w, queries, gain=None, eps=1e-6, mix_gain=None, mix_w=None, mix_eps=1e-6,
+                       out=None, stream=None):
+    """MSAR with each source's own conv kernels: conv_w [n_src, d*sum(k)] (or
+    any [n_src, stride >= d*sum(k)] float tensor) -> out [T, d]."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    m = queries.shape[0]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if out is None:
+        out = torch.empty((T, d), dtype=src.dtype, device=src.device)
+    _check("msar_expand_fwd_ps", load().msar_expand_fwd_ps(
+        _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), conv_w.stride(0), _p(queries),
+        _p(gain), eps, _p(mix_gain), _p(mix_w), mix_eps, _p(out), _stream(stream)))
     return out

@@ -816,7 +816,7 @@ attnres_status_t launch_msar_read(const void *src, int64_t n_src, int64_t src_st
                                   int64_t d, attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
                                   const float *conv_w, const float *queries, const float *gain, float eps,
                                   const float *mix_gain, const float *mix_w, float mix_eps, void *out,
-                                  void *stream) {
+                                  void *stream, int64_t conv_src_stride = 0) {
     if (T < 0 || t_prev > INT64_MAX - T) return ATTNRES_ERR_INVALID_ARG;
     const int64_t rows = t_prev + T;                      // source rows per source
     attnres_status_t st = check_common(src, n_src, src_stride, rows, d, dt, eps);
@@ -826,12 +826,20 @@ attnres_status_t launch_msar_read(const void *src, int64_t n_src, int64_t src_st
     if (!ksizes || !conv_w || !queries || !mix_w || !out) return ATTNRES_ERR_INVALID_ARG;
     for (int64_t r = 0; r + 1 < m; ++r)
         if (ksizes[r] < 1) return ATTNRES_ERR_INVALID_ARG;
+    if (conv_src_stride != 0) {
+        // each source's kernels must not overlap the next source's
+        int64_t ktot = 0;
+        for (int64_t r = 0; r + 1 < m; ++r) ktot += ksizes[r];
+        if (conv_src_stride < 0 || (n_src > 1 && conv_src_stride < d * ktot)) return ATTNRES_ERR_INVALID_ARG;
+    }
     const size_t es = esize(dt);
     const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)rows * (size_t)d) * es;
     if (overlap(out, (size_t)T * (size_t)d * es, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
     if (m != 4) return ATTNRES_ERR_UNSUPPORTED;
     for (int r = 0; r < 3; ++r)
         if (ksizes[r] > MSAR_KMAX) return ATTNRES_ERR_UNSUPPORTED;
+    // per-source kernels start 16-byte aligned (they are read with 16-byte loads)
+    if (conv_src_stride != 0 && n_src > 1 && conv_src_stride % 4 != 0) return ATTNRES_ERR_UNSUPPORTED;
     if (!aligned16(out) || !aligned16(queries) || !aligned16(conv_w) || !aligned16(mix_w) ||
         (gain && !aligned16(gain)) || (mix_gain && !aligned16(mix_gain)))
         return ATTNRES_ERR_UNSUPPORTED;
@@ -847,6 +855,7 @@ attnres_status_t launch_msar_read(const void *src, int64_t n_src, int64_t src_st
     a.d = (int)d;
     for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
     a.conv_w = conv_w;
+    a.conv_src_stride = conv_src_stride;
     a.queries = queries;
     a.gain = gain;
     a.eps = eps;
@@ -1135,6 +1144,16 @@ attnres_status_t msar_expand_fwd_chunk(const void *src, int64_t n_src, int64_t s
     if (T_prev < 0) return ATTNRES_ERR_INVALID_ARG;
     return launch_msar_read(src, n_src, src_stride, T_prev, T, d, dt, m, ksizes, conv_w, queries, gain, eps,
                             mix_gain, mix_w, mix_eps, out, stream);
+}
+
+attnres_status_t msar_expand_fwd_ps(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                    attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                    int64_t conv_src_stride, const float *queries, const float *gain, float eps,
+                                    const float *mix_gain, const float *mix_w, float mix_eps, void *out,
+                                    void *stream) {
+    if (conv_src_stride <= 0) return ATTNRES_ERR_INVALID_ARG;
+    return launch_msar_read(src, n_src, src_stride, 0, T, d, dt, m, ksizes, conv_w, queries, gain, eps, mix_gain,
+                            mix_w, mix_eps, out, stream, conv_src_stride);
 }
 
 attnres_status_t msar_block_phase1(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,

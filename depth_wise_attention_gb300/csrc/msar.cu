@@ -22,6 +22,12 @@
 // peer's buffer and one cluster barrier per token publishes them.  The mixer
 // sums of token t travel with the score sums of token t+1, so each token
 // costs one cluster barrier.
+//
+// Per-source kernels (PS): each source has its own conv kernels, packed
+// conv_src_stride floats apart.  The 8 sources' kernels of a CTA's slice
+// (393 KB at 512 channels) do not fit in shared memory, so each thread reads
+// its two channels' taps of every source through L2 (the whole set, 3 MB at
+// d = 4096, stays resident) as the convolution needs them.
 #include <cooperative_groups.h>
 
 #include "msar.h"
@@ -36,7 +42,7 @@ constexpr int MSAR_NX = MSAR_NS + 5;                    // + mixer sums (ssZ, 4 
 
 // KA, KB, KC > 0 fix the three kernel sizes at compile time (fully unrolled,
 // branch-free convolution); 0 means they are read from the arguments.
-template <typename Tin, int KA, int KB, int KC>
+template <typename Tin, int KA, int KB, int KC, bool PS = false>
 __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const int ring, const int ktot) {
     using P2 = Pair2<Tin>;
     constexpr int ES = sizeof(Tin);
@@ -78,11 +84,12 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
         *reinterpret_cast<uint4 *>(ringbuf + b) = make_uint4(0u, 0u, 0u, 0u);
 
     // conv weights of this CTA's channel slice, layout [koff_r + j][c]
-    {
-        int64_t goff[3];
-        goff[0] = 0;
-        goff[1] = (int64_t)d * kk[0];
-        goff[2] = (int64_t)d * (kk[0] + kk[1]);
+    // (per-source kernels are read from global memory instead)
+    int64_t goff[3];
+    goff[0] = 0;
+    goff[1] = (int64_t)d * kk[0];
+    goff[2] = (int64_t)d * (kk[0] + kk[1]);
+    if (!PS) {
         for (int idx = tid; idx < ktot * ch; idx += blockDim.x) {
             const int jj = idx / ch, c = idx - jj * ch;
             const int r = jj >= koff[2] ? 2 : (jj >= koff[1] ? 1 : 0);
@@ -196,7 +203,55 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
                     }
                 }
             };
-            if (FIXED) {
+            // Per-source kernels: source by source, the source's three
+            // kernels on my two channels are loaded once per token (channels
+            // cg0 and cg0 + 1 hold 2 k_r consecutive floats of the [d][k_r]
+            // layout: 16-byte loads when k_r is a multiple of 4), then applied
+            // to that source's rows of the window.
+            auto conv_source = [&](int i) {
+                const float *wb = a.conv_w + (int64_t)i * a.conv_src_stride;
+                constexpr int KW = FIXED ? HIST_C + 1 : MSAR_KMAX;
+                float2 w[MSAR_M - 1][KW];
+#pragma unroll
+                for (int r = 0; r < MSAR_M - 1; ++r) {
+                    const float *wr = wb + goff[r] + (int64_t)cg0 * kk[r];
+                    if (FIXED && (kk[r] % 4) == 0) {
+#pragma unroll
+                        for (int j4 = 0; j4 < KW; j4 += 4) {
+                            if (j4 < kk[r]) {
+                                const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wr + j4));
+                                const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wr + kk[r] + j4));
+                                w[r][j4 + 0] = make_float2(w0.x, w1.x);
+                                w[r][j4 + 1] = make_float2(w0.y, w1.y);
+                                w[r][j4 + 2] = make_float2(w0.z, w1.z);
+                                w[r][j4 + 3] = make_float2(w0.w, w1.w);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < KW; ++j)
+                            w[r][j] = j < kk[r] ? make_float2(__ldg(wr + j), __ldg(wr + kk[r] + j)) : make_float2(0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < KW; ++j) {
+                    if (j > hist) break;
+                    int sl = cur_slot - j;
+                    if (sl < 0) sl += ring;
+                    const float2 xs = P2::ld(ringbuf + (size_t)sl * slot_bytes + (size_t)cl * ES + (size_t)i * row_bytes);
+                    if (j == 0) x[i] = xs;
+#pragma unroll
+                    for (int r = 0; r < MSAR_M - 1; ++r)
+                        if (j < kk[r]) u[i][r] = ffma2(w[r][j], xs, u[i][r]);
+                }
+            };
+            if (PS) {
+#pragma unroll
+                for (int i = 0; i < MSAR_SMAX; ++i) {
+                    if (i < nsrc) conv_source(i);
+                    else x[i] = make_float2(0.f, 0.f);
+                }
+            } else if (FIXED) {
 #pragma unroll
                 for (int j = 0; j <= HIST_C; ++j) conv_row(j);
             } else {
@@ -312,6 +367,12 @@ __global__ void __launch_bounds__(256, 1) msar_kernel(const MsarArgs a, const in
     }
 }
 
+template <typename Tin, bool PS>
+static const void *msar_fn(bool k4812) {
+    return k4812 ? reinterpret_cast<const void *>(&msar_kernel<Tin, 4, 8, 12, PS>)
+                 : reinterpret_cast<const void *>(&msar_kernel<Tin, 0, 0, 0, PS>);
+}
+
 attnres_status_t launch_msar(int dt, MsarArgs a, int sms, void *stream, char *err, size_t errlen) {
     const int es = dt == 1 ? 2 : 4;
     const int max_ch = dt == 1 ? 512 : 256;       // ring of 16+ rows x 8 sources fits
@@ -328,13 +389,14 @@ attnres_status_t launch_msar(int dt, MsarArgs a, int sms, void *stream, char *er
     const int kmax = a.k[0] > a.k[1] ? (a.k[0] > a.k[2] ? a.k[0] : a.k[2]) : (a.k[1] > a.k[2] ? a.k[1] : a.k[2]);
     const int ring = kmax + MSAR_LA;
     const int ktot = a.k[0] + a.k[1] + a.k[2];
-    const size_t smem = (size_t)ring * MSAR_SMAX * ch * es + (size_t)ktot * ch * 4 +
+    const bool ps = a.conv_src_stride != 0;
+    // per-source kernels stay in global memory: no shared-memory copy
+    const int ktot_smem = ps ? 0 : ktot;
+    const size_t smem = (size_t)ring * MSAR_SMAX * ch * es + (size_t)ktot_smem * ch * 4 +
                         (size_t)(8 * MSAR_NX + 2 * 8 * MSAR_NX) * 4 + 32 * 8 + 16;
     const bool k4812 = a.k[0] == 4 && a.k[1] == 8 && a.k[2] == 12;
-    const void *fn = dt == 1 ? (k4812 ? reinterpret_cast<const void *>(&msar_kernel<__nv_bfloat16, 4, 8, 12>)
-                                      : reinterpret_cast<const void *>(&msar_kernel<__nv_bfloat16, 0, 0, 0>))
-                             : (k4812 ? reinterpret_cast<const void *>(&msar_kernel<float, 4, 8, 12>)
-                                      : reinterpret_cast<const void *>(&msar_kernel<float, 0, 0, 0>));
+    const void *fn = dt == 1 ? (ps ? msar_fn<__nv_bfloat16, true>(k4812) : msar_fn<__nv_bfloat16, false>(k4812))
+                             : (ps ? msar_fn<float, true>(k4812) : msar_fn<float, false>(k4812));
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -375,7 +437,7 @@ attnres_status_t launch_msar(int dt, MsarArgs a, int sms, void *stream, char *er
     a.nclusters = (int)nclusters;
     a.tokens_per_cluster = (a.T + nclusters - 1) / nclusters;
     cfg.gridDim = dim3((unsigned)(nclusters * K));
-    e = cudaLaunchKernelEx(&cfg, (void (*)(const MsarArgs, int, int))fn, a, ring, ktot);
+    e = cudaLaunchKernelEx(&cfg, (void (*)(const MsarArgs, int, int))fn, a, ring, ktot_smem);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "msar launch: %s", cudaGetErrorString(e));
         return ATTNRES_ERR_CUDA;

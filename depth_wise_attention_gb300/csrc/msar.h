@@ -24,6 +24,7 @@ struct MsarArgs {
     int d;
     int k[3];                  // conv kernel sizes of streams 1..3
     const float *conv_w;       // packed [d][k_1] [d][k_2] [d][k_3]
+    int64_t conv_src_stride;   // floats between sources' packed kernels; 0: all sources share conv_w
     const float *queries;      // [4][d]
     const float *gain;         // [d] or nullptr
     float eps;

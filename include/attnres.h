@@ -408,6 +408,27 @@ attnres_status_t msar_expand_fwd_chunk(const void *src, int64_t n_src, int64_t s
                                        void *out, void *stream);
 
 /*
+ * msar_expand_fwd with each source's own conv kernels: source i is expanded
+ * with the kernels packed (as msar_expand_fwd's conv_w) at
+ * conv_w + i * conv_src_stride floats.  Defined by the MSAR page, section
+ * 무엇과 다른가 (the streams v_i^(r) of each source), read here with per-source
+ * kernels; msar_expand_fwd is the reading in which all sources share them.
+ *   conv_src_stride  > 0 floats; at least d * (k_1 + k_2 + k_3) with more than
+ *                    one source (else ATTNRES_ERR_INVALID_ARG), and then a
+ *                    multiple of 4 (16-byte aligned kernels; else
+ *                    ATTNRES_ERR_UNSUPPORTED)
+ * Every other argument and limit as msar_expand_fwd.  The kernels of 8
+ * sources do not fit in shared memory, so they are read through L2 as the
+ * convolution needs them: slower than the shared-kernel read.
+ */
+attnres_status_t msar_expand_fwd_ps(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                    int64_t d, attnres_dtype_t dt, int64_t m,
+                                    const int32_t *ksizes, const float *conv_w,
+                                    int64_t conv_src_stride, const float *queries,
+                                    const float *gain, float eps, const float *mix_gain,
+                                    const float *mix_w, float mix_eps, void *out, void *stream);
+
+/*
  * MSAR inside the two-phase Block schedule, phase 1: the queries of S layers
  * of a block read the completed (cached) sources in one pass.  Every source
  * is expanded once into its m streams (as msar_expand_fwd) and, for every

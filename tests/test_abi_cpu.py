@@ -269,3 +269,18 @@ def test_two_phase_backward_validation(lib):
     assert p1(dsrc=None) == INV
     assert p1(dl=A + 0x1000000 + 64) == INV       # d_lse overlaps dsrc
     assert p1(dl=DL + 2) == UNS                   # misaligned d_lse
+
+
+def test_msar_per_source_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    T, d = 16, 256
+
+    def ps(stride, n_src=8, T=T):
+        return lib.msar_expand_fwd_ps(A, n_src, T * d, T, d, BF16, 4, ctypes.cast(ks, ctypes.c_void_p), B, stride,
+                                      B + 0x400000, None, 1e-6, None, B + 0x500000, 1e-6, B + 0x600000, None)
+    assert ps(0) == INV                           # the per-source entry needs a stride
+    assert ps(-1) == INV
+    assert ps(d * 24 - 1) == INV                  # sources' kernels would overlap
+    assert ps(d * 24, T=0) == OK
+    assert ps(1, n_src=1, T=0) == OK              # one source: any positive stride
+    assert ps(d * 24 + 2) == UNS                  # kernels not 16-byte aligned

@@ -709,6 +709,36 @@ def test_msar_block_two_phase_equals_one_shot(dtype, N, S, T, d):
         check_out(out, ref, dtype, np.abs(srcs).max() * 3, what=f"layer {s_ + 1}")
 
 
+@pytest.mark.parametrize("dtype,n_src,T,d,ks", [(BF16, 8, 60, 4096, (4, 8, 12)), (F32, 3, 45, 512, (4, 8, 12)),
+                                                 (BF16, 8, 100, 256, (1, 2, 3)), (BF16, 5, 30, 1024, (16, 5, 9)),
+                                                 (F32, 1, 20, 128, (4, 8, 12))])
+def test_msar_per_source_kernels(dtype, n_src, T, d, ks):
+    """MSAR with each source's own conv kernels against the oracle."""
+    rng = _rng(n_src * 3 + T + d)
+    src = _sources(rng, n_src, T, d, dtype)
+    q = _queries(rng, 4, d)
+    cw = np.stack([np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel()
+                                   for k in ks]) for _ in range(n_src)])
+    mw = (rng.standard_normal((4 * d, 4)) / math.sqrt(4 * d)).astype(np.float32)
+    out = attnres.msar_expand_fwd_ps(to_dev(src, dtype), ks, to_dev(cw, F32), to_dev(q, F32), mix_w=to_dev(mw, F32))
+    ref = oracle.msar_ps(src, ks, cw, q, None, 1e-6, None, mw, 1e-6)
+    check_out(out, ref, dtype, np.abs(src).max() * 3)
+
+
+def test_msar_per_source_equal_kernels_equal_the_shared_read_bitwise():
+    """Per-source kernels that are all the same give the shared-kernel read
+    bit for bit (the same products summed in the same order)."""
+    rng = _rng(91)
+    n_src, T, d, ks = 8, 70, 2048, (4, 8, 12)
+    src = to_dev(_sources(rng, n_src, T, d, BF16), BF16)
+    q = to_dev(_queries(rng, 4, d), F32)
+    cw = np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel() for k in ks])
+    mw = to_dev((rng.standard_normal((4 * d, 4)) / math.sqrt(4 * d)).astype(np.float32), F32)
+    shared = attnres.msar_expand_fwd(src, ks, to_dev(cw, F32), q, mix_w=mw)
+    per = attnres.msar_expand_fwd_ps(src, ks, to_dev(np.stack([cw] * n_src), F32), q, mix_w=mw)
+    assert torch.equal(shared, per)
+
+
 # --------------------------------------------------------------- hygiene
 
 def test_outputs_stay_inside_their_buffers():
