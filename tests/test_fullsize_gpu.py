@@ -281,3 +281,61 @@ def test_block_two_phase_backward_T32768_d4096():
         if s_ > 0:
             check_out(rows(dparts[s_], idx), rs[N], BF16, strict=False, what=f"layer {s_ + 1} d_partial")
     check_out(rows(dsrc, idx), ref_cached, BF16, strict=False, what="cached sources' gradient")
+
+
+def test_msar_per_source_and_chunked_T32768_d4096():
+    """MSAR at the MSAR size with each source's own kernels (sampled tokens
+    against the oracle on causal windows), and the chunked prefill of the
+    shared-kernel read (8 chunks of 4096 with 11 history rows) equal to the
+    one-call read bit for bit."""
+    T, d, N = 32768, 4096, 8
+    ks = (4, 8, 12)
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((4, d), (16.0 / d) ** 0.5, g)
+    mw = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g)
+    cw = torch.stack([torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g) for k in ks]) for _ in range(N)])
+    out = attnres.msar_expand_fwd_ps(src, ks, cw, q, None, 1e-6, None, mw, 1e-6)
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T, n=60)
+    cw_h, q_h, mw_h = (t.cpu().numpy().astype(np.float64) for t in (cw, q, mw))
+    got = rows(out, idx)
+    ref = np.empty_like(got)
+    for j, t in enumerate(idx):
+        lo = max(0, int(t) - 11)
+        win = src[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
+        ref[j] = oracle.msar_ps(win, ks, cw_h, q_h, None, 1e-6, None, mw_h, 1e-6)[-1]
+    check_out(got, ref, BF16, what="per-source kernels")
+    del out
+    shared_cw = cw[0].contiguous()
+    whole = attnres.msar_expand_fwd(src, ks, shared_cw, q, None, 1e-6, None, mw, 1e-6)
+    chunked = torch.empty_like(whole)
+    for c0 in range(0, T, 4096):
+        h = min(11, c0)
+        attnres.msar_expand_fwd_chunk(src[:, c0 - h:c0 + 4096], h, ks, shared_cw, q, None, 1e-6, None, mw, 1e-6,
+                                      out=chunked[c0:c0 + 4096])
+    assert torch.equal(whole, chunked)
+
+
+def test_read_bwd_T32768_d4096_bench_workload():
+    """The backward of a Block layer's read at the bench size (9 sources, 1
+    query): sampled source gradients against the oracle; the query and gain
+    gradients equal the sums of the two halves' runs."""
+    T, d, N = 32768, 4096, 8
+    src, g = inputs.device_sources(N + 1, T, d, lambda n: 1.0 + n / 2.0 if n < N else 1.0, seed=0)
+    src = src.view(N + 1, T, d)
+    q = inputs.device_normal((1, d), (16.0 / d) ** 0.5, g)
+    gain = torch.ones((d,), dtype=F32, device="cuda")
+    dout = torch.randn((1, T, d), generator=g, device="cuda").to(BF16)
+    dsrc, dq, dg = attnres.attnres_read_bwd(src, q, dout, gain)
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T)
+    ref = oracle.read_bwd(rows(src, idx), q.cpu().numpy().astype(np.float64), rows(dout, idx), None, 1e-6)
+    check_out(rows(dsrc, idx), ref[0], BF16, what="dsrc")
+    del dsrc
+    h = T // 2
+    parts = [attnres.attnres_read_bwd(src[:, a:b].contiguous(), q, dout[:, a:b].contiguous(), gain)[1:]
+             for a, b in ((0, h), (h, T))]
+    for name, whole, (x, y) in (("dq", dq, (parts[0][0], parts[1][0])), ("dgain", dg, (parts[0][1], parts[1][1]))):
+        w, s_ = to_host(whole), to_host(x) + to_host(y)
+        assert np.abs(w - s_).max() <= 1e-4 * np.abs(w).max(), name
