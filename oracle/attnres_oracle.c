@@ -694,6 +694,131 @@ int oracle_msar_ps(const double *src, int64_t n_src, int64_t T, int64_t d, int64
     return rc;
 }
 
+/* Backward of the MSAR read (oracle_msar) for an output gradient dh[T][d].
+ * The forward is taken apart as in oracle_msar: streams u_i^(r), per-stream
+ * reads Z^(r) (read_one), and the H^pre mixer.  Chain rule, per token:
+ *   mixer   dc_r   = dh . Z^(r);  dl_o = dc_o c_o (1 - c_o)     (c = sigmoid(l))
+ *           dzn    = sum_o dl_o P[:, o];  dP[:, o] += dl_o zn;  dmix_gain += dzn * zf / nu
+ *           dzf    = mg * dzn / nu - zf (sum_k mg_k dzn_k zf_k) / (m d nu^3)   (RMSNorm over m d)
+ *           dZ^(r) = c_r dh + dzf[r d .. (r+1) d)
+ *   reads   each stream r is a read of the sources u_i^(r) with query w_r:
+ *           oracle_read_bwd gives du_i^(r), dw_r and stream r's share of dgain
+ *   streams dv_i[t] += du_i^(0)[t];  for r >= 1, u^(r)[t][c] = sum_j cw_r[c][j] v[t-j][c]:
+ *           dv_i[t-j][c] += cw_r[c][j] du_i^(r)[t][c],  dcw_r[c][j] += du_i^(r)[t][c] v_i[t-j][c]
+ * Outputs: dsrc[n_src][T][d], dconv_w (packed as conv_w), dq[m][d], dg[d],
+ * dmix_gain[m*d], dmix_w[m*d][m]. */
+int oracle_msar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                    const int32_t *ksizes, const double *conv_w, const double *queries,
+                    const double *gain, double eps, const double *mix_gain, const double *mix_w,
+                    double mix_eps, const double *dh, double *dsrc, double *dconv_w, double *dq,
+                    double *dg, double *dmix_gain, double *dmix_w)
+{
+    if (!src || !ksizes || !conv_w || !queries || !mix_w || !dh || !dsrc || !dconv_w || !dq || !dg ||
+        !dmix_gain || !dmix_w || n_src < 1 || T < 0 || d < 1 || m < 1 || eps < 0 || mix_eps < 0)
+        return -1;
+    const size_t per = (size_t)T * (size_t)d, md = (size_t)m * (size_t)d;
+    int64_t ktot = 0;
+    for (int64_t r = 0; r + 1 < m; ++r) ktot += ksizes[r];
+    double *u = (double *)malloc(sizeof(double) * (size_t)m * (size_t)n_src * per + 1);    /* [r][i][T][d] */
+    double *Z = (double *)malloc(sizeof(double) * md * (size_t)T + 1);                     /* [r][T][d] */
+    double *dZ = (double *)malloc(sizeof(double) * md * (size_t)T + 1);                    /* [r][T][d] */
+    double *du = (double *)malloc(sizeof(double) * (size_t)n_src * per + 1);               /* [i][T][d] */
+    double *dqr = (double *)malloc(sizeof(double) * (size_t)d);
+    double *dgr = (double *)malloc(sizeof(double) * (size_t)d);
+    double *zf = (double *)malloc(sizeof(double) * md + 1);
+    double *zn = (double *)malloc(sizeof(double) * md + 1);
+    double *dzn = (double *)malloc(sizeof(double) * md + 1);
+    double *c = (double *)malloc(sizeof(double) * (size_t)m);
+    double *dl = (double *)malloc(sizeof(double) * (size_t)m);
+    const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_src);
+    int rc = (u && Z && dZ && du && dqr && dgr && zf && zn && dzn && c && dl && rows) ? 0 : -1;
+    for (size_t k = 0; rc == 0 && k < (size_t)n_src * per; ++k) dsrc[k] = 0.0;
+    for (int64_t k = 0; rc == 0 && k < d * ktot; ++k) dconv_w[k] = 0.0;
+    for (size_t k = 0; rc == 0 && k < md; ++k) { dmix_gain[k] = 0.0; for (int64_t o = 0; o < m; ++o) dmix_w[k * m + o] = 0.0; }
+    for (int64_t k = 0; rc == 0 && k < d; ++k) dg[k] = 0.0;
+    /* forward: streams and per-stream reads */
+    for (int64_t r = 0, off = 0; r < m && rc == 0; ++r) {
+        for (int64_t i = 0; i < n_src && rc == 0; ++i) {
+            const double *v = src + (size_t)i * per;
+            double *ur = u + ((size_t)r * (size_t)n_src + (size_t)i) * per;
+            if (r == 0) memcpy(ur, v, sizeof(double) * per);
+            else rc = oracle_msar_conv(v, T, d, ksizes[r - 1], conv_w + off, ur);
+        }
+        if (r >= 1) off += d * (int64_t)ksizes[r - 1];
+        for (int64_t t = 0; t < T && rc == 0; ++t) {
+            for (int64_t i = 0; i < n_src; ++i) rows[i] = u + ((size_t)r * (size_t)n_src + (size_t)i) * per + (size_t)t * (size_t)d;
+            rc = read_one(rows, n_src, d, queries + r * d, gain, eps, Z + (size_t)r * per + (size_t)t * (size_t)d, NULL, NULL);
+        }
+    }
+    /* mixer backward, per token */
+    for (int64_t t = 0; t < T && rc == 0; ++t) {
+        const double *ht = dh + t * d;
+        for (int64_t r = 0; r < m; ++r)
+            for (int64_t k = 0; k < d; ++k) zf[r * d + k] = Z[(size_t)r * per + (size_t)t * (size_t)d + k];
+        double ms = 0.0;
+        for (size_t k = 0; k < md; ++k) ms += zf[k] * zf[k];
+        const double nu = sqrt(ms / (double)md + mix_eps);
+        for (size_t k = 0; k < md; ++k) zn[k] = nu > 0.0 ? (mix_gain ? mix_gain[k] : 1.0) * zf[k] / nu : 0.0;
+        for (int64_t o = 0; o < m; ++o) {
+            double acc = 0.0;
+            for (size_t k = 0; k < md; ++k) acc += zn[k] * mix_w[k * m + o];
+            c[o] = 1.0 / (1.0 + exp(-acc));
+            double dc = 0.0;
+            for (int64_t k = 0; k < d; ++k) dc += ht[k] * zf[o * d + k];
+            dl[o] = dc * c[o] * (1.0 - c[o]);
+        }
+        double s = 0.0;
+        for (size_t k = 0; k < md; ++k) {
+            double acc = 0.0;
+            for (int64_t o = 0; o < m; ++o) {
+                acc += dl[o] * mix_w[k * m + o];
+                dmix_w[k * m + o] += dl[o] * zn[k];
+            }
+            dzn[k] = acc;
+            if (nu > 0.0) dmix_gain[k] += acc * zf[k] / nu;
+            s += (mix_gain ? mix_gain[k] : 1.0) * acc * zf[k];
+        }
+        for (int64_t r = 0; r < m; ++r)
+            for (int64_t k = 0; k < d; ++k) {
+                const size_t kk = (size_t)r * (size_t)d + (size_t)k;
+                double dzf = 0.0;
+                if (nu > 0.0)
+                    dzf = (mix_gain ? mix_gain[kk] : 1.0) * dzn[kk] / nu - zf[kk] * s / ((double)md * nu * nu * nu);
+                dZ[(size_t)r * per + (size_t)t * (size_t)d + k] = c[r] * ht[k] + dzf;
+            }
+    }
+    /* per-stream read backward, then back through the streams */
+    for (int64_t r = 0, off = 0; r < m && rc == 0; ++r) {
+        rc = oracle_read_bwd(u + (size_t)r * (size_t)n_src * per, n_src, T, d, queries + r * d, 1, gain, eps,
+                             dZ + (size_t)r * per, du, dqr, dgr);
+        if (rc) break;
+        for (int64_t k = 0; k < d; ++k) { dq[r * d + k] = dqr[k]; dg[k] += dgr[k]; }
+        if (r == 0) {
+            for (size_t k = 0; k < (size_t)n_src * per; ++k) dsrc[k] += du[k];
+            continue;
+        }
+        const int64_t kr = ksizes[r - 1];
+        const double *cw = conv_w + off;
+        double *dcw = dconv_w + off;
+        for (int64_t i = 0; i < n_src; ++i) {
+            const double *v = src + (size_t)i * per;
+            const double *dui = du + (size_t)i * per;
+            double *dv = dsrc + (size_t)i * per;
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t k = 0; k < d; ++k)
+                    for (int64_t j = 0; j < kr; ++j)
+                        if (t - j >= 0) {
+                            dv[(t - j) * d + k] += cw[k * kr + j] * dui[t * d + k];
+                            dcw[k * kr + j] += dui[t * d + k] * v[(t - j) * d + k];
+                        }
+        }
+        off += d * kr;
+    }
+    free(u); free(Z); free(dZ); free(du); free(dqr); free(dgr); free(zf); free(zn); free(dzn); free(c); free(dl);
+    free(rows);
+    return rc;
+}
+
 /* MSAR inside the two-phase Block schedule, phase 1.  [MSAR §어떻게 쓰나]:
  * AttnRes's two-phase computation carries over to MSAR unchanged: every
  * target query of the block is read against the completed sources in one

@@ -754,6 +754,42 @@ def test_msar_per_source_permutation_equivariant():
     assert np.abs(a - c).max() > 1e-3        # kernels must travel with their sources
 
 
+@pytest.mark.parametrize("N,T,d,ks,eps", [(3, 7, 4, (2, 3, 4), 1e-6), (2, 5, 6, (1, 4, 2), 0.05)])
+def test_msar_bwd_matches_finite_differences(N, T, d, ks, eps):
+    """Every gradient of the MSAR read (sources, conv kernels, stream
+    queries, gain, mixer gain, mixer projection) against central differences
+    of the (pinned) MSAR forward oracle."""
+    rng = np.random.default_rng(91 + N + T)
+    src = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
+    cw = _rand(rng, d * sum(ks), scale=0.6)
+    q = _rand(rng, 4, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d)
+    mg = rng.uniform(0.5, 1.5, 4 * d)
+    P = _rand(rng, 4 * d, 4, scale=0.5)
+    dh = _rand(rng, T, d)
+
+    def loss(s_, cw_, q_, g_, mg_, P_):
+        return float((oracle.msar(s_, ks, cw_, q_, g_, eps, mg_, P_, 1e-6) * dh).sum())
+    got = oracle.msar_bwd(src, ks, cw, q, dh, g, eps, mg, P, 1e-6)
+    ref = _fd(loss, (src, cw, q, g, mg, P))
+    for name, x, y in zip(("dsrc", "dconv_w", "dq", "dgain", "dmix_gain", "dmix_w"), got, ref):
+        assert np.abs(x - y).max() <= 2e-6 * max(1.0, np.abs(y).max()), name
+
+
+def test_msar_bwd_identity_stream_only_is_read_backward():
+    """Zero conv kernels make streams 1..3 zero (their reads give zero and
+    send nothing back); with a zero mixer projection c_r = 1/2 and the mixer
+    passes dh/2 to each stream's read minus its RMSNorm term, which a zero
+    projection also zeroes (dzn = 0): stream 0's read then gets dh / 2, so the
+    sources' gradient is the read backward of dh / 2."""
+    rng = np.random.default_rng(92)
+    N, T, d, ks = 3, 6, 8, (4, 8, 12)
+    src, q, dh = _rand(rng, N, T, d), _rand(rng, 4, d, scale=1.5), _rand(rng, T, d)
+    got = oracle.msar_bwd(src, ks, np.zeros(d * sum(ks)), q, dh, None, 1e-6, None, np.zeros((4 * d, 4)), 1e-6)
+    ref = oracle.read_bwd(src, q[:1], 0.5 * dh[None], None, 1e-6)
+    assert np.allclose(got[0], ref[0], atol=1e-12) and np.allclose(got[2][0], ref[1][0], atol=1e-12)
+
+
 def _msar_block_inputs(rng, N, S, T, d, ks=(4, 8, 12)):
     cached = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
     parts = _rand(rng, S, T, d)

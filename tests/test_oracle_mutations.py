@@ -50,6 +50,12 @@ MUTANTS = {
                                               "if (rc == 0 && partial) rc = msar_expand(partial, T, d, 1, ksizes, conv_w, up);\n    for (int64_t r = 1; r < m && up; ++r) memcpy(up + (size_t)r * per, partial, sizeof(double) * per);")],
     "msar_phase2_lse_of_stream_zero": [("const double l = lse[r * T + t];", "const double l = lse[t];")],
     "msar_ps_first_source_kernels": [("conv_w + i * conv_src_stride,", "conv_w,")],
+    "msar_bwd_sigmoid_derivative": [("dl[o] = dc * c[o] * (1.0 - c[o]);", "dl[o] = dc * c[o];")],
+    "msar_bwd_mixer_rms_sign": [("/ nu - zf[kk] * s / ((double)md * nu * nu * nu);", "/ nu + zf[kk] * s / ((double)md * nu * nu * nu);")],
+    "msar_bwd_conv_transpose_unshifted": [("dv[(t - j) * d + k] += cw[k * kr + j] * dui[t * d + k];",
+                                           "dv[t * d + k] += cw[k * kr + j] * dui[t * d + k];")],
+    "msar_bwd_kernel_grad_unshifted": [("dcw[k * kr + j] += dui[t * d + k] * v[(t - j) * d + k];",
+                                        "dcw[k * kr + j] += dui[t * d + k] * v[t * d + k];")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
