@@ -10,8 +10,8 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|mhar_block|msar|
-msar_block|msar_chunked|msar_ps|full_depth|block_d2048|block_fused|block_bwd|read_bwd|
-mhar_bwd|decode) are for profiling and the design notes.
+msar_block|msar_chunked|msar_ps|msar_bwd|full_depth|block_d2048|block_fused|block_bwd|
+read_bwd|mhar_bwd|decode) are for profiling and the design notes.
 """
 from __future__ import annotations
 
@@ -47,6 +47,8 @@ KERNEL_SOURCES = {
     "merge_bwd": [CSRC + "merge_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_merge_bwd.cu"],
     "read_bwd_mh": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu", CSRC + "kernels_bwd_mh.cu"],
     "depth_read_decode": [CSRC + "depth_read_decode.cuh", CSRC + "common.cuh", CSRC + "kernels_decode.cu"],
+    "msar_bwd": [CSRC + "msar_bwd.cu", CSRC + "msar_bwd.h", CSRC + "msar.h", CSRC + "common.cuh",
+                 CSRC + "read_bwd.cuh", CSRC + "kernels_bwd.cu", CSRC + "depth_read_mma.cuh", CSRC + "kernels_mma.cu"],
 }
 
 
@@ -871,6 +873,89 @@ class MsarWorkload(BlockWorkload):
         return len(wins)
 
 
+class MsarBwdWorkload(MsarWorkload):
+    """Backward of the MSAR read at the MSAR workload's sizes (N=8 sources,
+    bf16, d=4096, k=4/8/12, T=32768) for a dense output gradient dh ~ N(0, 1):
+    the sources', conv kernels', stream queries', gain's and mixer's
+    gradients.  One step is the whole chain (streams, 4 stream reads, mixer
+    backward and its sums, 4 read backwards, the convolutions' transpose and
+    the fixed-order sums).  Its roofline is the CUDA-core FMA rate of the
+    arithmetic the backward cannot avoid, per token: the convolutions once
+    forward and twice back (N d k_tot x 3), the 4 stream reads (N d x 3 each:
+    sum of squares, query dot, weighted sum), their backward (N d x 7 each:
+    the read again, dh . v, U, dsrc), and the mixer (4d x 16)."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0):
+        super().__init__(T, d, N, seed)
+        self.name = "msar_read_backward"
+        b = 2
+        # read the sources and dh, write the sources' gradients
+        self.bytes_per_token = (2 * N + 1) * d * b
+        self.phase1_bytes_per_token = self.bytes_per_token
+        self.launches_per_step = 1 + 4 + 2 + 2 + 4 * 2 + 1 + 2
+        self.dominant = "msar backward (whole chain)"
+        self.dominant_src = "msar_bwd"
+        self.profile_tag = f"ncu_msar_bwd_d{d}"
+        self.fma_per_token = N * d * sum(self.ks) * 3 + 4 * N * d * 3 + 4 * N * d * 7 + 4 * d * 16
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres
+        super().setup(device)
+        T, d, N = self.T, self.d, self.N
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed + 7)
+        self.dh = torch.randn((T, d), generator=g, device=device).to(torch.bfloat16)
+        self.dsrc = torch.empty_like(self.cache)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.grads = (torch.empty_like(self.conv_w), torch.empty((4, d), **f32), torch.empty((d,), **f32),
+                      torch.empty((4 * d,), **f32), torch.empty((4 * d, 4), **f32))
+        nb = attnres.msar_expand_bwd_workspace_size(N, T, d, torch.bfloat16, self.ks)
+        self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.msar_expand_bwd(self.cache, self.ks, self.conv_w, self.queries, self.dh, None, 1e-6, None,
+                                self.mix_w, 1e-6, dsrc=self.dsrc, grads=self.grads, workspace=self.ws,
+                                stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def setup_host(self):
+        self.h_cache = torch_pinned_like(self.cache)
+        self.h_dh = torch_pinned_like(self.dh)
+        self.h_out = torch_pinned_like(self.dsrc)
+        self.h2d = (self.h_cache.numel() + self.h_dh.numel()) * 2
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.dh.copy_(self.h_dh, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.dsrc, non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        # per sampled token t: the 12-row causal window ending at t and dh on row t alone
+        wins, cw, q, mw = super().oracle_sample(n_tokens, seed)
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        dhs = []
+        for w, t in zip(wins, idx):
+            dw = np.zeros(w.shape[1:])
+            dw[-1] = self.dh[int(t)].float().cpu().numpy()
+            dhs.append(dw)
+        return wins, dhs, cw, q, mw
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        wins, dhs, cw, q, mw = sample
+        for w, dw in zip(wins, dhs):
+            oracle.msar_bwd(w, self.ks, cw, q, dw, None, 1e-6, None, mw, 1e-6)
+        return len(wins)
+
+
 class MsarBlockWorkload(MsarWorkload):
     """MSAR inside the two-phase Block schedule: one block of S=4 layers over
     N=8 cached sources, bf16, d=4096.  One step = phase 1 (every source
@@ -1132,6 +1217,8 @@ def make_workload(name, T=None):
         return MharBwdWorkload(T=T or 131072)
     if name == "msar_block":
         return MsarBlockWorkload(T=T or 32768)
+    if name == "msar_bwd":
+        return MsarBwdWorkload(T=T or 32768)
     if name == "block_fused":
         return BlockFusedWorkload(T=T or 32768)
     if name == "full_depth":
@@ -1382,7 +1469,7 @@ def main():
     ap.add_argument("--workload", default="block",
                     choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
                              "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block",
-                             "full_depth"])
+                             "msar_bwd", "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

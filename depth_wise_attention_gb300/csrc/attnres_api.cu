@@ -16,6 +16,7 @@
 #include "depth_read_mma.cuh"
 #include "dispatch.h"
 #include "msar.h"
+#include "msar_bwd.h"
 #include "phase2.cuh"
 #include "merge_bwd.cuh"
 #include "read_bwd.cuh"
@@ -972,6 +973,171 @@ attnres_status_t launch_msar_phase2_host(const void *o, const float *lse, const 
     return launch_msar_phase2(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
 }
 
+// MSAR backward: chunking and workspace layout.  Each region starts on a
+// 256-byte boundary of the workspace.
+struct MsarBwdPlan {
+    int64_t tc, chunks;
+    ReadBwdShape rb;
+    size_t rb_bytes;
+    size_t off_u, off_z, off_dz, off_du, off_rb, off_dg, off_e, off_mp, off_a, off_cp, total;
+};
+
+attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt, const int32_t *ksizes,
+                               const DeviceInfo *dev, MsarBwdPlan *p) {
+    if (d != 1024 && d != 2048 && d != 4096) return ATTNRES_ERR_UNSUPPORTED;
+    if (n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    attnres_status_t st = read_bwd_shape(n_src, d, 1, 1, dt, &p->rb);
+    if (st != ATTNRES_OK) return st;
+    p->rb_bytes = read_bwd_ws_bytes(dev->sms, p->rb, d);
+    // token chunks of the conv kernels: about 8 CTAs of 256 channels per SM
+    // over all chunks, at least 32 tokens per chunk
+    const int64_t per_chunk = n_src * ((d + 255) / 256);
+    int64_t want = (8 * (int64_t)dev->sms + per_chunk - 1) / per_chunk;
+    if (want < 1) want = 1;
+    p->tc = (T + want - 1) / want;
+    if (p->tc < 32) p->tc = 32;
+    p->chunks = T > 0 ? (T + p->tc - 1) / p->tc : 0;
+    const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
+    const size_t es = esize(dt);
+    const size_t row = (size_t)T * (size_t)d * es;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    p->off_u = take(3 * (size_t)n_src * row);
+    p->off_z = take(4 * row);
+    p->off_dz = take(4 * row);
+    p->off_du = take(4 * (size_t)n_src * row);
+    p->off_rb = take(p->rb_bytes);
+    p->off_dg = take(4 * (size_t)d * 4);
+    p->off_e = take((size_t)T * 4 * 4);
+    p->off_mp = take((size_t)p->chunks * 16 * (size_t)d * 4);
+    p->off_a = take(16 * (size_t)d * 4);
+    p->off_cp = take((size_t)p->chunks * (size_t)n_src * (size_t)ktot * (size_t)d * 4);
+    p->total = off;
+    return ATTNRES_OK;
+}
+
+// Backward of the MSAR read (msar_expand_fwd), as a chain of steps in the
+// caller's workspace: the streams, the per-stream reads Z^(r), the mixer's
+// backward, the per-stream read backward, and the causal convolutions'
+// transpose.
+attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                 attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                 const float *queries, const float *gain, float eps, const float *mix_gain,
+                                 const float *mix_w, float mix_eps, const void *dh, void *dsrc,
+                                 int64_t dsrc_stride, float *dconv_w, float *dqueries, float *dgain,
+                                 float *dmix_gain, float *dmix_w, void *ws, size_t ws_bytes, void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (!(mix_eps >= 0.f) || std::isinf(mix_eps)) return ATTNRES_ERR_INVALID_ARG;
+    st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    if (!conv_w || !queries || !mix_w || !dconv_w || !dqueries || !dmix_w) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!dh || !dsrc || !ws)) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+    const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t dsrc_bytes = ((size_t)(n_src - 1) * (size_t)dsrc_stride + (size_t)T * (size_t)d) * es;
+    const size_t row_bytes = (size_t)T * (size_t)d * es;
+    const size_t md = 4 * (size_t)d;
+    if (T > 0 && (overlap(dsrc, dsrc_bytes, src, src_bytes) || overlap(dsrc, dsrc_bytes, dh, row_bytes) ||
+                  overlap(ws, ws_bytes, src, src_bytes) || overlap(ws, ws_bytes, dsrc, dsrc_bytes) ||
+                  overlap(ws, ws_bytes, dh, row_bytes)))
+        return ATTNRES_ERR_INVALID_ARG;
+    // the parameter gradients: disjoint from one another and from the workspace
+    const void *pg[5] = {dconv_w, dqueries, dgain, dmix_gain, dmix_w};
+    const size_t pn[5] = {(size_t)ktot * (size_t)d * 4, md * 4, (size_t)d * 4, md * 4, md * 16};
+    for (int x = 0; x < 5; ++x) {
+        if (!pg[x]) continue;
+        if (T > 0 && overlap(pg[x], pn[x], ws, ws_bytes)) return ATTNRES_ERR_INVALID_ARG;
+        for (int y = x + 1; y < 5; ++y)
+            if (pg[y] && overlap(pg[x], pn[x], pg[y], pn[y])) return ATTNRES_ERR_INVALID_ARG;
+    }
+    if ((d != 1024 && d != 2048 && d != 4096) || n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(conv_w) || !aligned16(queries) || !aligned16(mix_w) || (gain && !aligned16(gain)) ||
+        (mix_gain && !aligned16(mix_gain)) || !aligned16(dmix_w) || !aligned4(dconv_w) || !aligned4(dqueries) ||
+        (dgain && !aligned4(dgain)) || (dmix_gain && !aligned4(dmix_gain)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    if (T > 0 && (!aligned16(dh) || !aligned16(dsrc) || (dsrc_stride * (int64_t)es) % 16 != 0 || !aligned16(ws)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarBwdPlan p;
+    st = msar_bwd_plan(n_src, T, d, dt, ksizes, dev, &p);
+    if (st != ATTNRES_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // no tokens: every parameter gradient is zero
+        cudaError_t e = cudaSuccess;
+        for (int x = 0; x < 5 && e == cudaSuccess; ++x)
+            if (pg[x]) e = cudaMemsetAsync(const_cast<void *>(pg[x]), 0, pn[x], s);
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    MsarBwdArgs a;
+    a.src = static_cast<const unsigned char *>(src);
+    a.src_stride_bytes = src_stride * (int64_t)es;
+    a.n_src = (int)n_src;
+    a.T = T;
+    a.d = (int)d;
+    for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
+    a.ktot = (int)ktot;
+    a.conv_w = conv_w;
+    a.tc = p.tc;
+    a.u = w + p.off_u;
+    a.z = w + p.off_z;
+    a.dz = w + p.off_dz;
+    a.dh = static_cast<const unsigned char *>(dh);
+    a.mix_gain = mix_gain;
+    a.mix_w = mix_w;
+    a.mix_eps = mix_eps;
+    a.mix_e = reinterpret_cast<float *>(w + p.off_e);
+    a.mix_parts = reinterpret_cast<float *>(w + p.off_mp);
+    a.du = w + p.off_du;
+    a.dsrc = static_cast<unsigned char *>(dsrc);
+    a.dsrc_stride_bytes = dsrc_stride * (int64_t)es;
+    a.conv_parts = reinterpret_cast<float *>(w + p.off_cp);
+    a.dmix_w = dmix_w;
+    a.dmix_gain = dmix_gain;
+    const int dti = dt == ATTNRES_BF16 ? 1 : 0;
+    const int64_t per_stream = n_src * T * d;          // elements of one stream's sources
+    cudaError_t e = msar_bwd_streams(dti, a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "msar backward streams launch");
+    // Z^(r): stream 0 reads the sources themselves, stream r >= 1 the conv streams
+    for (int64_t r = 0; r < 4; ++r) {
+        const void *sr = r == 0 ? src : static_cast<const void *>(a.u + (size_t)(r - 1) * per_stream * es);
+        st = launch_depth_read(sr, n_src, r == 0 ? src_stride : T * d, T, d, 1, dt, queries + r * d, 1, gain, eps,
+                               a.z + (size_t)r * row_bytes, nullptr, stream);
+        if (st != ATTNRES_OK) return st;
+    }
+    e = msar_bwd_mix(dti, a, dev->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "msar backward mixer launch");
+    float *A = reinterpret_cast<float *>(w + p.off_a);
+    e = msar_bwd_sum(a.mix_parts, p.chunks, 16 * (int64_t)d, A, 0, stream);
+    if (e == cudaSuccess) e = msar_bwd_mix_finish(a, A, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "msar backward mixer sums launch");
+    // the per-stream read backward: du^(r), dw_r and stream r's share of dgain
+    float *dg = reinterpret_cast<float *>(w + p.off_dg);
+    for (int64_t r = 0; r < 4; ++r) {
+        const void *sr = r == 0 ? src : static_cast<const void *>(a.u + (size_t)(r - 1) * per_stream * es);
+        st = launch_read_bwd(sr, n_src, r == 0 ? src_stride : T * d, T, d, 1, dt, queries + r * d, 1, gain, eps,
+                             a.dz + (size_t)r * row_bytes, nullptr, a.du + (size_t)r * per_stream * es, T * d, 0,
+                             dqueries + r * d, dg + r * d, w + p.off_rb, p.rb_bytes, stream);
+        if (st != ATTNRES_OK) return st;
+    }
+    e = msar_bwd_conv(dti, a, stream);
+    if (e == cudaSuccess) e = msar_bwd_sum(a.conv_parts, p.chunks * n_src, ktot * d, dconv_w, 0, stream);
+    if (e == cudaSuccess && dgain) e = msar_bwd_sum(dg, 4, d, dgain, 0, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "msar backward conv launch");
+    return ATTNRES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1170,6 +1336,35 @@ attnres_status_t msar_block_phase2(const void *o, const float *lse, const void *
                                    const float *mix_w, float mix_eps, void *out, void *stream) {
     return launch_msar_phase2_host(o, lse, partial, T, d, dt, m, ksizes, conv_w, query, gain, eps, mix_gain, mix_w,
                                    mix_eps, out, stream);
+}
+
+attnres_status_t msar_expand_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt, int64_t m,
+                                               const int32_t *ksizes, size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || n_src < 1 || T < 0 || d < 1)
+        return ATTNRES_ERR_INVALID_ARG;
+    attnres_status_t st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarBwdPlan p;
+    st = msar_bwd_plan(n_src, T, d, dt, ksizes, dev, &p);
+    if (st != ATTNRES_OK) return st;
+    *bytes = p.total;
+    return ATTNRES_OK;
+}
+
+attnres_status_t msar_expand_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                 attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                 const float *queries, const float *gain, float eps, const float *mix_gain,
+                                 const float *mix_w, float mix_eps, const void *dh, void *dsrc,
+                                 int64_t dsrc_stride, float *dconv_w, float *dqueries, float *dgain,
+                                 float *dmix_gain, float *dmix_w, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+    return launch_msar_bwd(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, gain, eps, mix_gain,
+                           mix_w, mix_eps, dh, dsrc, dsrc_stride, dconv_w, dqueries, dgain, dmix_gain, dmix_w,
+                           workspace, workspace_bytes, stream);
 }
 
 const char *attnres_status_string(attnres_status_t s) {

@@ -477,6 +477,52 @@ attnres_status_t msar_block_phase2(const void *o, const float *lse, const void *
                                    const float *gain, float eps, const float *mix_gain,
                                    const float *mix_w, float mix_eps, void *out, void *stream);
 
+/*
+ * Backward of msar_expand_fwd for an output gradient dh: the gradients of the
+ * sources, the conv kernels, the stream queries, the key gain and the mixer's
+ * gain and projection.  Defined by the chain rule through the three steps of
+ * the MSAR page, section 무엇과 다른가 (onedev.kr "깊이 방향 어텐션을 다중
+ * 스트림으로 확장한 MSAR"): the H^pre mixer (sigmoid of the RMSNorm'd flat
+ * Z times P), each stream's depth read (the backward of attnres_read_bwd,
+ * one query per stream), and the causal depthwise convolutions, whose
+ * transpose sends du^(r)[t] back to the rows t-j it read.  Readings as
+ * msar_expand_fwd.
+ *   src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, gain, eps,
+ *   mix_gain, mix_w, mix_eps   as msar_expand_fwd (the forward's inputs)
+ *   dh         [T][d] dtype dt
+ *   dsrc       [n_src] x [T][d] dtype dt, dsrc_stride (>= T*d) elements
+ *              apart; overwritten; must not overlap src or dh
+ *   dconv_w    float, packed as conv_w; overwritten
+ *   dqueries   [m][d] float; overwritten
+ *   dgain      [d] float or NULL (the gain's gradient, summed over the
+ *              streams; with gain NULL it is the gradient at an all-ones gain)
+ *   dmix_gain  [m*d] float or NULL (same convention); dmix_w [m*d][m] float
+ *   workspace  device scratch of msar_expand_bwd_workspace_size bytes (it
+ *              holds the conv streams, the per-stream reads and their
+ *              gradients: about (7 n_src + 8) T d elements of dtype dt);
+ *              must not overlap any other argument
+ * The parameter gradients are sums over the tokens taken in a fixed order
+ * (same inputs, same bits).  The streams, the per-stream reads and their
+ * gradients are held in dtype dt.  T = 0 zeroes the parameter gradients.
+ * Limits: m = 4, kernel sizes 1..16, d = 1024, 2048 or 4096, n_src <= 16,
+ * else ATTNRES_ERR_UNSUPPORTED; pointers 16-byte aligned except the float
+ * gradients dconv_w, dqueries, dgain, dmix_gain (4-byte).  A NULL required
+ * pointer, a short workspace or overlapping outputs is
+ * ATTNRES_ERR_INVALID_ARG.
+ */
+attnres_status_t msar_expand_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                 int64_t d, attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                 const float *conv_w, const float *queries, const float *gain,
+                                 float eps, const float *mix_gain, const float *mix_w, float mix_eps,
+                                 const void *dh, void *dsrc, int64_t dsrc_stride, float *dconv_w,
+                                 float *dqueries, float *dgain, float *dmix_gain, float *dmix_w,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes msar_expand_bwd needs for these sizes on the current device. */
+attnres_status_t msar_expand_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d,
+                                               attnres_dtype_t dt, int64_t m,
+                                               const int32_t *ksizes, size_t *bytes);
+
 /* Static description of a status code (never NULL). */
 const char *attnres_status_string(attnres_status_t status);
 

@@ -284,3 +284,38 @@ def test_msar_per_source_validation(lib):
     assert ps(d * 24, T=0) == OK
     assert ps(1, n_src=1, T=0) == OK              # one source: any positive stride
     assert ps(d * 24 + 2) == UNS                  # kernels not 16-byte aligned
+
+
+def test_msar_backward_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    bad = (ctypes.c_int32 * 3)(4, 0, 12)
+    kp = lambda k: ctypes.cast(k, ctypes.c_void_p)
+    T, d = 16, 1024
+    DH, DS, DCW, DQ, DG, DMG, DMW, WS = (B + 0x1000000, B + 0x2000000, B + 0x3000000, B + 0x3100000,
+                                         B + 0x3200000, B + 0x3300000, B + 0x3400000, B + 0x4000000)
+
+    def mb(n_src=8, T=T, d=d, m=4, k=ks, dh=DH, ds=DS, dstride=None, dcw=DCW, dq=DQ, dg=DG, dmg=DMG, dmw=DMW,
+           ws=WS, mix_eps=1e-6):
+        dstride = T * d if dstride is None else dstride
+        return lib.msar_expand_bwd(A, n_src, T * d, T, d, BF16, m, kp(k), B, B + 0x200000, None, 1e-6, None,
+                                   B + 0x300000, mix_eps, dh, ds, dstride, dcw, dq, dg, dmg, dmw, ws, 1 << 30, None)
+    assert mb(k=bad) == INV
+    assert mb(mix_eps=-1.0) == INV
+    assert mb(dh=None) == INV
+    assert mb(ds=None) == INV
+    assert mb(dq=None) == INV
+    assert mb(dmw=None) == INV
+    assert mb(ws=None) == INV
+    assert mb(dstride=T * d - 1) == INV
+    assert mb(ds=A + 64) == INV                   # dsrc overlaps the sources
+    assert mb(ws=DH - 64) == INV                  # workspace overlaps dh
+    assert mb(dg=DQ + 64) == INV                  # parameter gradients overlap
+    assert mb(m=3) == UNS
+    assert mb(d=256) == UNS                       # mixer kernels exist for d = 1024, 2048, 4096
+    assert mb(n_src=17) == UNS
+    assert mb(dmw=DMW + 4) == UNS                 # misaligned projection gradient
+    assert mb(dh=DH + 8) == UNS
+    n = ctypes.c_size_t(0)
+    assert lib.msar_expand_bwd_workspace_size(8, T, d, BF16, 4, kp(ks), None) == INV
+    assert lib.msar_expand_bwd_workspace_size(8, T, d, BF16, 4, kp(bad), ctypes.byref(n)) == INV
+    assert lib.msar_expand_bwd_workspace_size(8, T, d, BF16, 3, kp(ks), ctypes.byref(n)) == UNS

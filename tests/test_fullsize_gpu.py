@@ -339,3 +339,46 @@ def test_read_bwd_T32768_d4096_bench_workload():
     for name, whole, (x, y) in (("dq", dq, (parts[0][0], parts[1][0])), ("dgain", dg, (parts[0][1], parts[1][1]))):
         w, s_ = to_host(whole), to_host(x) + to_host(y)
         assert np.abs(w - s_).max() <= 1e-4 * np.abs(w).max(), name
+
+
+def test_msar_bwd_T32768_d4096():
+    """Backward of the MSAR read at the MSAR size.  Every gradient is linear
+    in dh and the read of token t sees source rows t-11..t only, so with dh
+    nonzero on a few clusters of 4 tokens each gradient is the sum of the
+    oracle's backward over the clusters' 15-row causal windows, and dsrc is
+    exactly zero outside them.  Clusters at the start, across a boundary of
+    the conv kernels' token chunks, in the middle and at the end.  Then a
+    dense dh: two calls agree bit for bit."""
+    T, d, N = 32768, 4096, 8
+    ks = (4, 8, 12)
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((4, d), (16.0 / d) ** 0.5, g)
+    cw = torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g) for k in ks])
+    mw = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g)
+    starts = [0, 3275, 17001, T - 4]
+    dh = torch.zeros((T, d), dtype=BF16, device="cuda")
+    for c in starts:
+        dh[c:c + 4] = torch.randn((4, d), generator=g, device="cuda").to(BF16)
+    got = attnres.msar_expand_bwd(src, ks, cw, q, dh, None, 1e-6, None, mw, 1e-6)
+    attnres.attnres_sync_status()
+    cw_h, q_h, mw_h = (t.cpu().numpy().astype(np.float64) for t in (cw, q, mw))
+    ref_par = None
+    inside = torch.zeros(T, dtype=torch.bool, device="cuda")
+    for c in starts:
+        lo = max(0, c - 11)
+        win = src[:, lo:c + 4, :].float().cpu().numpy().astype(np.float64)
+        dwin = dh[lo:c + 4].float().cpu().numpy().astype(np.float64)
+        r = oracle.msar_bwd(win, ks, cw_h, q_h, dwin, None, 1e-6, None, mw_h, 1e-6)
+        check_out(got[0][:, lo:c + 4], r[0], BF16, strict=False, what=f"dsrc rows {lo}..{c + 3}")
+        inside[lo:c + 4] = True
+        ref_par = list(r[1:]) if ref_par is None else [a + b for a, b in zip(ref_par, r[1:])]
+    assert torch.count_nonzero(got[0][:, ~inside]) == 0
+    for name, g_, r_ in zip(("dconv_w", "dqueries", "dgain", "dmix_gain", "dmix_w"), got[1:], ref_par):
+        check_out(g_, np.asarray(r_).reshape(tuple(g_.shape)), BF16, strict=False, what=name)
+    del got
+    dense = torch.randn((T, d), generator=g, device="cuda").to(BF16)
+    a = attnres.msar_expand_bwd(src, ks, cw, q, dense, None, 1e-6, None, mw, 1e-6)
+    b = attnres.msar_expand_bwd(src, ks, cw, q, dense, None, 1e-6, None, mw, 1e-6)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)

@@ -739,6 +739,88 @@ def test_msar_per_source_equal_kernels_equal_the_shared_read_bitwise():
     assert torch.equal(shared, per)
 
 
+# --------------------------------------------------------------- MSAR backward
+
+def _msar_bwd_case(rng, n_src, T, d, dtype, ks, with_gains):
+    src = _sources(rng, n_src, T, d, dtype)
+    q = _queries(rng, 4, d)
+    cw = np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel() for k in ks])
+    mw = (rng.standard_normal((4 * d, 4)) / math.sqrt(4 * d)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gains else None
+    mg = rng.uniform(0.5, 1.5, 4 * d).astype(np.float32) if with_gains else None
+    dh = _sources(rng, 1, T, d, dtype, step=0)[0]
+    return src, q, cw, mw, g, mg, dh
+
+
+def _msar_bwd_gpu(case, ks, dtype):
+    src, q, cw, mw, g, mg, dh = case
+    dev = lambda x: to_dev(x, F32) if x is not None else None
+    return attnres.msar_expand_bwd(to_dev(src, dtype), ks, dev(cw), dev(q), to_dev(dh, dtype), dev(g), 1e-6,
+                                   dev(mg), dev(mw), 1e-6)
+
+
+_MSAR_GRADS = ("dsrc", "dconv_w", "dqueries", "dgain", "dmix_gain", "dmix_w")
+
+
+def _check_msar_grads(got, ref, dtype, what):
+    """Every gradient within the dtype's bar of its own largest value: the
+    streams, the per-stream reads and their gradients are held in dtype
+    between the steps, so with bf16 the parameter gradients carry bf16
+    roundings too."""
+    for name, g_, r_ in zip(_MSAR_GRADS, got, ref):
+        r_ = np.asarray(r_).reshape(tuple(g_.shape))
+        check_out(g_, r_, dtype, np.abs(r_).max(), strict=False, what=f"{what} {name}")
+
+
+@pytest.mark.parametrize("dtype,n_src,T,d,ks,with_gains", [
+    (BF16, 8, 70, 4096, (4, 8, 12), True), (BF16, 3, 45, 2048, (4, 8, 12), False),
+    (F32, 5, 300, 1024, (4, 8, 12), True), (BF16, 1, 33, 1024, (4, 8, 12), True),
+    (BF16, 16, 20, 2048, (4, 8, 12), False), (BF16, 4, 130, 1024, (16, 5, 9), True),
+    (F32, 2, 64, 1024, (1, 2, 3), True), (BF16, 9, 1, 4096, (4, 8, 12), True)])
+def test_msar_bwd(dtype, n_src, T, d, ks, with_gains):
+    """Backward of the MSAR read against the oracle's chain rule: the
+    sources', conv kernels', stream queries', gain's and mixer's gradients
+    (T = 300 at d = 1024 spans ten token chunks of the conv kernels)."""
+    rng = _rng(n_src * 7 + T + d + sum(ks))
+    case = _msar_bwd_case(rng, n_src, T, d, dtype, ks, with_gains)
+    got = _msar_bwd_gpu(case, ks, dtype)
+    src, q, cw, mw, g, mg, dh = case
+    ref = oracle.msar_bwd(src, ks, cw, q, dh, g, 1e-6, mg, mw, 1e-6)
+    _check_msar_grads(got, ref, dtype, f"n_src={n_src} T={T} d={d}")
+
+
+def test_msar_bwd_is_deterministic_and_linear_in_dh():
+    """Same inputs, same bits; and the backward of dh1 + dh2 is the sum of the
+    two backwards (every gradient is linear in dh)."""
+    rng = _rng(93)
+    ks, T, d = (4, 8, 12), 150, 2048
+    src, q, cw, mw, g, mg, dh = _msar_bwd_case(rng, 8, T, d, F32, ks, True)
+    a = _msar_bwd_gpu((src, q, cw, mw, g, mg, dh), ks, F32)
+    b = _msar_bwd_gpu((src, q, cw, mw, g, mg, dh), ks, F32)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    dh1 = dh.copy()
+    dh1[T // 2:] = 0
+    dh2 = dh - dh1
+    a1 = _msar_bwd_gpu((src, q, cw, mw, g, mg, dh1), ks, F32)
+    a2 = _msar_bwd_gpu((src, q, cw, mw, g, mg, dh2), ks, F32)
+    for name, x, y1, y2 in zip(_MSAR_GRADS, a, a1, a2):
+        ref = to_host(y1) + to_host(y2)
+        check_out(x, ref, F32, np.abs(ref).max(), strict=False, what=f"linearity {name}")
+
+
+def test_msar_bwd_empty_sequence_zeroes_parameter_gradients():
+    d, ks = 1024, (4, 8, 12)
+    src = torch.empty((3, 0, d), dtype=BF16, device="cuda")
+    x = inputs.msar_inputs(3, 1, d, seed=3)
+    got = attnres.msar_expand_bwd(src, ks, to_dev(x["conv_w"], F32), to_dev(x["queries"], F32),
+                                  torch.empty((0, d), dtype=BF16, device="cuda"), mix_w=to_dev(x["mix_w"], F32))
+    torch.cuda.synchronize()
+    assert got[0].numel() == 0
+    for t in got[1:]:
+        assert torch.count_nonzero(t) == 0
+
+
 # --------------------------------------------------------------- hygiene
 
 def test_outputs_stay_inside_their_buffers():
