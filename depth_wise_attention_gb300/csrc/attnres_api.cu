@@ -976,10 +976,11 @@ attnres_status_t launch_msar_phase2_host(const void *o, const float *lse, const 
 // MSAR backward: chunking and workspace layout.  Each region starts on a
 // 256-byte boundary of the workspace.
 struct MsarBwdPlan {
-    int64_t tc, chunks;
+    int64_t tc, chunks, tc_s, tc_m;
+    int nsl;
     ReadBwdShape rb;
     size_t rb_bytes;
-    size_t off_u, off_z, off_dz, off_du, off_rb, off_dg, off_e, off_mp, off_a, off_cp, total;
+    size_t off_u, off_z, off_dz, off_du, off_rb, off_dg, off_part, off_e, off_mp, off_a, off_cp, total;
 };
 
 attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt, const int32_t *ksizes,
@@ -989,14 +990,16 @@ attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtyp
     attnres_status_t st = read_bwd_shape(n_src, d, 1, 1, dt, &p->rb);
     if (st != ATTNRES_OK) return st;
     p->rb_bytes = read_bwd_ws_bytes(dev->sms, p->rb, d);
-    // token chunks of the conv kernels: about 8 CTAs of 256 channels per SM
-    // over all chunks, at least 32 tokens per chunk
-    const int64_t per_chunk = n_src * ((d + 255) / 256);
-    int64_t want = (8 * (int64_t)dev->sms + per_chunk - 1) / per_chunk;
-    if (want < 1) want = 1;
-    p->tc = (T + want - 1) / want;
+    // token chunks: the conv backward and A's partials in at most 64 chunks
+    // of at least 32 tokens; the streams kernel in chunks of T/128 (at least
+    // 32); the mixer 128 tokens per CTA over d/1024 channel slices
+    p->tc = (T + 63) / 64;
     if (p->tc < 32) p->tc = 32;
     p->chunks = T > 0 ? (T + p->tc - 1) / p->tc : 0;
+    p->tc_s = (T + 127) / 128;
+    if (p->tc_s < 32) p->tc_s = 32;
+    p->tc_m = 128;
+    p->nsl = (int)(d / 1024);
     const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
     const size_t es = esize(dt);
     const size_t row = (size_t)T * (size_t)d * es;
@@ -1012,6 +1015,7 @@ attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtyp
     p->off_du = take(4 * (size_t)n_src * row);
     p->off_rb = take(p->rb_bytes);
     p->off_dg = take(4 * (size_t)d * 4);
+    p->off_part = take((size_t)T * (size_t)p->nsl * 9 * 4);
     p->off_e = take((size_t)T * 4 * 4);
     p->off_mp = take((size_t)p->chunks * 16 * (size_t)d * 4);
     p->off_a = take(16 * (size_t)d * 4);
@@ -1090,6 +1094,10 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     a.ktot = (int)ktot;
     a.conv_w = conv_w;
     a.tc = p.tc;
+    a.tc_s = p.tc_s;
+    a.tc_m = p.tc_m;
+    a.nsl = p.nsl;
+    a.mix_part = reinterpret_cast<float *>(w + p.off_part);
     a.u = w + p.off_u;
     a.z = w + p.off_z;
     a.dz = w + p.off_dz;
@@ -1116,7 +1124,7 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
                                a.z + (size_t)r * row_bytes, nullptr, stream);
         if (st != ATTNRES_OK) return st;
     }
-    e = msar_bwd_mix(dti, a, dev->sms, stream);
+    e = msar_bwd_mix(dti, a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "msar backward mixer launch");
     float *A = reinterpret_cast<float *>(w + p.off_a);
     e = msar_bwd_sum(a.mix_parts, p.chunks, 16 * (int64_t)d, A, 0, stream);
@@ -1132,7 +1140,7 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
         if (st != ATTNRES_OK) return st;
     }
     e = msar_bwd_conv(dti, a, stream);
-    if (e == cudaSuccess) e = msar_bwd_sum(a.conv_parts, p.chunks * n_src, ktot * d, dconv_w, 0, stream);
+    if (e == cudaSuccess) e = msar_bwd_conv_sum(a, p.chunks * n_src, dconv_w, stream);
     if (e == cudaSuccess && dgain) e = msar_bwd_sum(dg, 4, d, dgain, 0, stream);
     if (e != cudaSuccess) return cuda_fail(e, "msar backward conv launch");
     return ATTNRES_OK;

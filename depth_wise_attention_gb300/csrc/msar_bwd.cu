@@ -5,10 +5,14 @@
 //   1. msar_streams_kernel   the conv streams u_i^(r), r = 1..3, of every source
 //   2. the depth read        Z^(r) = read of the sources u_i^(r) with query w_r
 //                            (the forward read kernels, one call per stream)
-//   3. msar_mix_bwd_kernel   the H^pre mixer's backward: dZ^(r), and per token
-//                            e_t[o] = dl_t[o] / nu_t; msar_mix_acc_kernel then
-//                            sums A[k][o] = sum_t zf_t[k] e_t[o], from which
-//                            dmix_w = mg * A and dmix_gain = sum_o P[:, o] A[:, o]
+//   3. msar_mix_stats_kernel per token and channel slice, the mixer's partial
+//                            sums (sum zf^2, the 4 projection dots, the 4
+//                            dh . Z^(r));
+//      msar_mix_dz_kernel    from their totals the mixer's backward: dZ^(r),
+//                            and per token e_t[o] = dl_t[o] / nu_t;
+//      msar_mix_acc_kernel   A[k][o] = sum_t zf_t[k] e_t[o] in per-chunk
+//                            partials, from which dmix_w = mg * A and
+//                            dmix_gain = sum_o P[:, o] A[:, o]
 //   4. the read backward     du_i^(r), dw_r and the gain's share per stream
 //                            (read_bwd_kernel, one call per stream)
 //   5. msar_conv_bwd_kernel  back through the causal convolutions:
@@ -16,6 +20,11 @@
 //                            and per-CTA partials of dcw_r[j] = sum du_i^(r)[t] v_i[t - j]
 //   6. msar_sum_kernel       the partials summed in a fixed order (deterministic)
 // The streams and their gradients are stored in the source dtype.
+//
+// The two convolution kernels walk the tokens of a chunk one row at a time
+// with register windows of the rows they need again; the rows reach shared
+// memory in batches through asynchronous 16-byte copies issued several
+// batches ahead, so that each SM keeps tens of KB of loads in flight.
 #include <stdio.h>
 
 #include "msar.h"
@@ -23,180 +32,304 @@
 
 namespace attnres {
 
+// ---------------------------------------------------------------- helpers
+// 16-byte asynchronous global -> shared copy; valid == false writes zeros and
+// reads nothing (src must still be a mapped address).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename Tin> __device__ __forceinline__ float ld1(const unsigned char *p);
+template <> __device__ __forceinline__ float ld1<float>(const unsigned char *p) {
+    return *reinterpret_cast<const float *>(p);
+}
+template <> __device__ __forceinline__ float ld1<__nv_bfloat16>(const unsigned char *p) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+template <typename Tin> __device__ __forceinline__ void st1(unsigned char *p, float v);
+template <> __device__ __forceinline__ void st1<float>(unsigned char *p, float v) {
+    *reinterpret_cast<float *>(p) = v;
+}
+template <> __device__ __forceinline__ void st1<__nv_bfloat16>(unsigned char *p, float v) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
+}
+
+// Compile-time kernel sizes: KA, KB, KC > 0 fix them (fully unrolled,
+// branch-free taps); 0 reads them from the arguments with windows of
+// MSAR_KMAX rows.
+template <int KA, int KB, int KC> struct ConvShape {
+    static constexpr bool FIXED = KA > 0;
+    static constexpr int K0 = FIXED ? KA : MSAR_KMAX, K1 = FIXED ? KB : MSAR_KMAX, K2 = FIXED ? KC : MSAR_KMAX;
+    static constexpr int KT = K0 + K1 + K2;
+    static constexpr int KM = K0 > K1 ? (K0 > K2 ? K0 : K2) : (K1 > K2 ? K1 : K2);
+    __host__ __device__ static constexpr int k(int r) { return r == 0 ? K0 : r == 1 ? K1 : K2; }
+    __host__ __device__ static constexpr int off(int r) { return r == 0 ? 0 : r == 1 ? K0 : K0 + K1; }
+};
+
 // ---------------------------------------------------------------- step 1
-// One thread per (source, channel pair) walks a chunk of tokens with a
-// register window of its source's last KW rows; the three kernels of its two
-// channels sit in registers.  Writes U[r-1][i][t][c..c+1] for r = 1..3.
-template <typename Tin, int KW>
-__global__ void __launch_bounds__(256) msar_streams_kernel(const MsarBwdArgs a) {
+// CTA = (slice of ST_CB channels, source i, chunk of tc_s tokens); a thread
+// owns two adjacent channels with their three kernels in registers and a
+// window of the source's last KM rows.  Rows t0 - (KM-1) .. t1-1 arrive in
+// batches of ST_RB rows into a ring of ST_NS stages.
+constexpr int ST_THREADS = 256;
+constexpr int ST_CB = 2 * ST_THREADS;
+constexpr int ST_RB = 8;
+constexpr int ST_NS = 4;
+
+template <typename Tin, int KA, int KB, int KC>
+__global__ void __launch_bounds__(ST_THREADS) msar_streams_kernel(const MsarBwdArgs a) {
     using P2 = Pair2<Tin>;
+    using CS = ConvShape<KA, KB, KC>;
     constexpr int ES = sizeof(Tin);
-    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
+    constexpr int H = CS::KM - 1;
+    constexpr int ROWB = ST_CB * ES;
+    constexpr int CPR = ROWB / 16;
+    constexpr int CPS = ST_RB * CPR;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const int cb = blockIdx.x * ST_CB;
+    const int c = cb + 2 * tid;
     const int i = blockIdx.y;
-    const int64_t t0 = (int64_t)blockIdx.z * a.tc;
-    if (c >= a.d) return;
-    const int64_t t1 = t0 + a.tc < a.T ? t0 + a.tc : a.T;
-    float2 w[3][KW];
-    int64_t off = 0;
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
-#pragma unroll
-        for (int j = 0; j < KW; ++j)
-            w[r][j] = j < a.k[r] ? make_float2(__ldg(a.conv_w + off + (int64_t)c * a.k[r] + j),
-                                               __ldg(a.conv_w + off + (int64_t)(c + 1) * a.k[r] + j))
-                                 : make_float2(0.f, 0.f);
-        off += (int64_t)a.d * a.k[r];
-    }
+    const int64_t t0 = (int64_t)blockIdx.z * a.tc_s;
+    const int64_t t1 = t0 + a.tc_s < a.T ? t0 + a.tc_s : a.T;
+    const int64_t nrows = t1 - t0 + H;
+    const int nb = (int)((nrows + ST_RB - 1) / ST_RB);
     const unsigned char *v = a.src + (int64_t)i * a.src_stride_bytes;
-    float2 win[KW];                  // win[j] = v[t - j]
-#pragma unroll
-    for (int j = 0; j < KW; ++j) {
-        const int64_t tr = t0 - 1 - j;
-        win[j] = (j < KW - 1 && tr >= 0) ? P2::ld(v + (tr * a.d + c) * ES) : make_float2(0.f, 0.f);
-    }
-    for (int64_t t = t0; t < t1; ++t) {
-#pragma unroll
-        for (int j = KW - 1; j > 0; --j) win[j] = win[j - 1];
-        win[0] = P2::ld(v + (t * a.d + c) * ES);
+    const uint32_t sbase = smem_u32(smem);
+
+    float2 w[CS::KT];
+    {
+        int64_t off = 0;
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
-            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < KW; ++j)
-                if (j < a.k[r]) acc = ffma2(w[r][j], win[j], acc);
-            P2::st(a.u + ((((int64_t)r * a.n_src + i) * a.T + t) * a.d + c) * ES, acc);
+            for (int j = 0; j < CS::k(r); ++j)
+                w[CS::off(r) + j] = (CS::FIXED || j < a.k[r])
+                                        ? make_float2(__ldg(a.conv_w + off + (int64_t)c * a.k[r] + j),
+                                                      __ldg(a.conv_w + off + (int64_t)(c + 1) * a.k[r] + j))
+                                        : make_float2(0.f, 0.f);
+            off += (int64_t)a.d * a.k[r];
+        }
+    }
+    auto issue = [&](int b) {
+        if (b < nb) {
+            const uint32_t st = sbase + (uint32_t)((b % ST_NS) * ST_RB * ROWB);
+            for (int q = tid; q < CPS; q += ST_THREADS) {
+                const int rr = q / CPR, cc = q - rr * CPR;
+                const int64_t row = t0 - H + (int64_t)b * ST_RB + rr;
+                const bool ok = row >= 0 && row < t1;
+                cp_async16(st + rr * ROWB + cc * 16, v + ((ok ? row : 0) * a.d + cb) * ES + cc * 16, ok);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int b = 0; b < ST_NS - 1; ++b) issue(b);
+
+    float2 win[CS::KM];              // win[j] = v[row - j]
+#pragma unroll
+    for (int j = 0; j < CS::KM; ++j) win[j] = make_float2(0.f, 0.f);
+    // output pointers of the three streams at token t0, one row apart per step
+    const int64_t rowb = (int64_t)a.d * ES;
+    unsigned char *up[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) up[r] = a.u + (((int64_t)r * a.n_src + i) * a.T + t0) * rowb + (int64_t)c * ES;
+    for (int b = 0; b < nb; ++b) {
+        cp_async_wait<ST_NS - 2>();
+        __syncthreads();
+        issue(b + ST_NS - 1);
+        const unsigned char *stage = smem + (b % ST_NS) * ST_RB * ROWB + 2 * tid * ES;
+#pragma unroll
+        for (int rr = 0; rr < ST_RB; ++rr) {
+            const int64_t row = t0 - H + (int64_t)b * ST_RB + rr;
+#pragma unroll
+            for (int j = CS::KM - 1; j > 0; --j) win[j] = win[j - 1];
+            win[0] = P2::ld(stage + rr * ROWB);
+            if (row >= t0 && row < t1) {
+#pragma unroll
+                for (int r = 0; r < 3; ++r) {
+                    // even and odd taps in two independent chains
+                    float2 ae = make_float2(0.f, 0.f), ao = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < CS::k(r); ++j)
+                        if (CS::FIXED || j < a.k[r]) {
+                            if (j & 1) ao = ffma2(w[CS::off(r) + j], win[j], ao);
+                            else ae = ffma2(w[CS::off(r) + j], win[j], ae);
+                        }
+                    P2::st(up[r], make_float2(ae.x + ao.x, ae.y + ao.y));
+                    up[r] += rowb;
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------- step 3
+// Mixer backward, tiled by channel slices of MX_CS channels (of every stream)
+// so that a CTA keeps its slice of g * P in shared memory and reuses it over
+// a chunk of tokens.  A warp takes one token at a time; a lane owns 8
+// adjacent channels per 256-channel step.  gP is stored transposed by the
+// channel's position within its 8 ([r][c % 8][c / 8]) so that the lanes'
+// reads of one position are consecutive.
+constexpr int MX_CS = 1024;
+constexpr int MX_THREADS = 256;
+constexpr size_t MX_SMEM = (size_t)4 * MX_CS * sizeof(float4);
+
+__device__ __forceinline__ int gp_index(int r, int c) { return r * MX_CS + (c & 7) * (MX_CS / 8) + (c >> 3); }
+
+__device__ __forceinline__ void stage_gp(const MsarBwdArgs &a, float4 *gp, int c0) {
+    for (int q = threadIdx.x; q < 4 * MX_CS; q += blockDim.x) {
+        const int r = q / MX_CS, cc = q - r * MX_CS;
+        const int64_t k = (int64_t)r * a.d + c0 + cc;
+        float4 p = __ldg(reinterpret_cast<const float4 *>(a.mix_w) + k);
+        const float g = a.mix_gain ? __ldg(a.mix_gain + k) : 1.f;
+        p.x *= g; p.y *= g; p.z *= g; p.w *= g;
+        gp[gp_index(r, cc)] = p;
+    }
+    __syncthreads();
+}
+
+// 8 channels of one row as floats
+template <typename Tin> __device__ __forceinline__ void load8(const unsigned char *p, float (&x)[8]);
+template <> __device__ __forceinline__ void load8<__nv_bfloat16>(const unsigned char *p, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = bf2_to_f2(w[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+template <> __device__ __forceinline__ void load8<float>(const unsigned char *p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 16);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <typename Tin> __device__ __forceinline__ void store8(unsigned char *p, const float (&x)[8]);
+template <> __device__ __forceinline__ void store8<__nv_bfloat16>(unsigned char *p, const float (&x)[8]) {
+    *reinterpret_cast<uint4 *>(p) =
+        make_uint4(f2_to_bf2(x[0], x[1]), f2_to_bf2(x[2], x[3]), f2_to_bf2(x[4], x[5]), f2_to_bf2(x[6], x[7]));
+}
+template <> __device__ __forceinline__ void store8<float>(unsigned char *p, const float (&x)[8]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4 *>(p + 16) = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+// Per (token, slice): s[0] = sum zf^2, s[1+o] = sum g zf P[:, o], s[5+r] = dh . Z^(r)
+// over the slice's channels -> mix_part[t][slice][9].
+template <typename Tin>
+__global__ void __launch_bounds__(MX_THREADS) msar_mix_stats_kernel(const MsarBwdArgs a) {
+    constexpr int ES = sizeof(Tin);
+    extern __shared__ __align__(16) float4 gp[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sl = blockIdx.x, c0 = sl * MX_CS;
+    stage_gp(a, gp, c0);
+    const int64_t t0 = (int64_t)blockIdx.y * a.tc_m;
+    const int64_t t1 = t0 + a.tc_m < a.T ? t0 + a.tc_m : a.T;
+    for (int64_t t = t0 + warp; t < t1; t += MX_THREADS / 32) {
+        float s[9];
+#pragma unroll
+        for (int q = 0; q < 9; ++q) s[q] = 0.f;
+#pragma unroll 1
+        for (int it = 0; it < MX_CS / 256; ++it) {
+            const int cl = it * 256 + lane * 8;
+            float dh[8], z[4][8];
+            load8<Tin>(a.dh + (t * a.d + c0 + cl) * ES, dh);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) load8<Tin>(a.z + (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES, z[r]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 p = gp[gp_index(r, cl + e)];
+                    s[0] = fmaf(z[r][e], z[r][e], s[0]);
+                    s[1] = fmaf(z[r][e], p.x, s[1]);
+                    s[2] = fmaf(z[r][e], p.y, s[2]);
+                    s[3] = fmaf(z[r][e], p.z, s[3]);
+                    s[4] = fmaf(z[r][e], p.w, s[4]);
+                    s[5 + r] = fmaf(dh[e], z[r][e], s[5 + r]);
+                }
+        }
+#pragma unroll
+        for (int q = 0; q < 9; ++q) s[q] = seg_sum<32>(s[q]);
+        if (lane == 0) {
+            float *dst = a.mix_part + (t * a.nsl + sl) * 9;
+#pragma unroll
+            for (int q = 0; q < 9; ++q) dst[q] = s[q];
         }
     }
 }
 
-// ---------------------------------------------------------------- step 3
-// One token per CTA iteration; thread tid of NT owns channels
-// [tid*CPT, tid*CPT + CPT) of every stream (d = NT * CPT, CPT a multiple of
-// the 16-byte vector).  Two block reductions per token: (sum zf^2, the 4
-// projection dots, the 4 dh.Z^(r)), then sum mg dzn zf.  P is read through
-// L1/L2 (4d x 4 floats).
-template <typename Tin, int NT, int CPT>
-__global__ void __launch_bounds__(NT) msar_mix_bwd_kernel(const MsarBwdArgs a) {
-    using E = Elem<Tin>;
-    constexpr int EPV = E::EPV, NV = CPT / EPV, NP = EPV / 2, NW = NT / 32;
-    static_assert(CPT % EPV == 0, "whole vectors per thread");
-    __shared__ float red[NW][10];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = a.d;
-    const int64_t md = 4 * (int64_t)d;
-    const int c0 = tid * CPT;
-    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-        float zf[4][CPT], dh[CPT];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                float2 x[NP];
-                E::unpack(*reinterpret_cast<const uint4 *>(a.z + (((int64_t)r * a.T + t) * d + c0 + v * EPV) * E::BYTES), x);
-#pragma unroll
-                for (int p = 0; p < NP; ++p) { zf[r][v * EPV + 2 * p] = x[p].x; zf[r][v * EPV + 2 * p + 1] = x[p].y; }
-            }
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            float2 x[NP];
-            E::unpack(*reinterpret_cast<const uint4 *>(a.dh + (t * d + c0 + v * EPV) * E::BYTES), x);
-#pragma unroll
-            for (int p = 0; p < NP; ++p) { dh[v * EPV + 2 * p] = x[p].x; dh[v * EPV + 2 * p + 1] = x[p].y; }
-        }
-        // round 1: sum zf^2, sum mg zf P[:, o], dh . Z^(r)
-        float s[9];
-#pragma unroll
-        for (int q = 0; q < 9; ++q) s[q] = 0.f;
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) {
-                const int64_t kk = (int64_t)r * d + c0 + k;
-                const float z = zf[r][k];
-                const float g = a.mix_gain ? __ldg(a.mix_gain + kk) : 1.f;
-                const float4 pw = __ldg(reinterpret_cast<const float4 *>(a.mix_w + kk * 4));
-                s[0] = fmaf(z, z, s[0]);
-                const float gz = g * z;
-                s[1] = fmaf(gz, pw.x, s[1]);
-                s[2] = fmaf(gz, pw.y, s[2]);
-                s[3] = fmaf(gz, pw.z, s[3]);
-                s[4] = fmaf(gz, pw.w, s[4]);
-                s[5 + r] = fmaf(dh[k], z, s[5 + r]);
-            }
-#pragma unroll
-        for (int q = 0; q < 9; ++q) s[q] = seg_sum<32>(s[q]);
-        if (lane == 0)
-#pragma unroll
-            for (int q = 0; q < 9; ++q) red[warp][q] = s[q];
-        __syncthreads();
+// From the per-slice sums of token t (added in slice order): nu, c, dl, and
+//   dZ^(r) = c_r dh + (sum_o dl_o gP[:, o]) / nu - zf (sum_o dl_o s_o) / (m d nu^3)
+// (sum_k g_k dzn_k zf_k = sum_o dl_o sum_k g_k zf_k P[k][o] = sum_o dl_o s_o).
+template <typename Tin>
+__global__ void __launch_bounds__(MX_THREADS) msar_mix_dz_kernel(const MsarBwdArgs a) {
+    constexpr int ES = sizeof(Tin);
+    extern __shared__ __align__(16) float4 gp[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sl = blockIdx.x, c0 = sl * MX_CS;
+    const float inv_md = 1.f / (4.f * (float)a.d);
+    stage_gp(a, gp, c0);
+    const int64_t t0 = (int64_t)blockIdx.y * a.tc_m;
+    const int64_t t1 = t0 + a.tc_m < a.T ? t0 + a.tc_m : a.T;
+    for (int64_t t = t0 + warp; t < t1; t += MX_THREADS / 32) {
         float tot[9];
 #pragma unroll
-        for (int q = 0; q < 9; ++q) {
-            tot[q] = 0.f;
-            for (int w = 0; w < NW; ++w) tot[q] += red[w][q];
-        }
-        __syncthreads();
-        const float ms = fmaf(tot[0], 1.f / (float)md, a.mix_eps);
+        for (int q = 0; q < 9; ++q) tot[q] = 0.f;
+        for (int k = 0; k < a.nsl; ++k)
+#pragma unroll
+            for (int q = 0; q < 9; ++q) tot[q] += __ldg(a.mix_part + (t * a.nsl + k) * 9 + q);
+        const float ms = fmaf(tot[0], inv_md, a.mix_eps);
         const float inv = ms > 0.f ? rsqrtf(ms) : 0.f;              // 1 / nu
         float cr[4], dl[4];
+        float s2 = 0.f;
 #pragma unroll
         for (int o = 0; o < 4; ++o) {
             cr[o] = 1.f / (1.f + __expf(-tot[1 + o] * inv));
             dl[o] = tot[5 + o] * cr[o] * (1.f - cr[o]);
+            s2 = fmaf(dl[o], tot[1 + o], s2);
         }
-        // dzn_k = sum_o dl_o P[k][o] (formed again below rather than held);
-        // round 2: sum mg dzn zf
-        auto dzn_at = [&](int64_t kk) {
-            const float4 pw = __ldg(reinterpret_cast<const float4 *>(a.mix_w + kk * 4));
-            return dl[0] * pw.x + dl[1] * pw.y + dl[2] * pw.z + dl[3] * pw.w;
-        };
-        float s2 = 0.f;
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) {
-                const int64_t kk = (int64_t)r * d + c0 + k;
-                const float g = a.mix_gain ? __ldg(a.mix_gain + kk) : 1.f;
-                s2 = fmaf(g * dzn_at(kk), zf[r][k], s2);
-            }
-        if (tid == 0)
+        const float k3 = s2 * inv * inv * inv * inv_md;
+        if (sl == 0 && lane == 0)
             *reinterpret_cast<float4 *>(a.mix_e + t * 4) = make_float4(dl[0] * inv, dl[1] * inv, dl[2] * inv, dl[3] * inv);
-        s2 = seg_sum<32>(s2);
-        if (lane == 0) red[warp][9] = s2;
-        __syncthreads();
-        float ts2 = 0.f;
-        for (int w = 0; w < NW; ++w) ts2 += red[w][9];
-        __syncthreads();
-        const float k3 = ts2 * inv * inv * inv / (float)md;
-        // dZ^(r) = c_r dh + mg dzn / nu - zf s / (m d nu^3)
+#pragma unroll 1
+        for (int it = 0; it < MX_CS / 256; ++it) {
+            const int cl = it * 256 + lane * 8;
+            float dh[8];
+            load8<Tin>(a.dh + (t * a.d + c0 + cl) * ES, dh);
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < 4; ++r) {
+                const int64_t off = (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES;
+                float z[8], y[8];
+                load8<Tin>(a.z + off, z);
 #pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                float2 y[NP];
-#pragma unroll
-                for (int p = 0; p < NP; ++p) {
-                    float yy[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k = v * EPV + 2 * p + e;
-                        const int64_t kk = (int64_t)r * d + c0 + k;
-                        const float g = a.mix_gain ? __ldg(a.mix_gain + kk) : 1.f;
-                        yy[e] = cr[r] * dh[k] + g * dzn_at(kk) * inv - zf[r][k] * k3;
-                    }
-                    y[p] = make_float2(yy[0], yy[1]);
+                for (int e = 0; e < 8; ++e) {
+                    const float4 p = gp[gp_index(r, cl + e)];
+                    const float gdzn = dl[0] * p.x + dl[1] * p.y + dl[2] * p.z + dl[3] * p.w;
+                    y[e] = cr[r] * dh[e] + gdzn * inv - z[e] * k3;
                 }
-                *reinterpret_cast<uint4 *>(a.dz + (((int64_t)r * a.T + t) * d + c0 + v * EPV) * E::BYTES) = E::pack(y);
+                store8<Tin>(a.dz + off, y);
             }
+        }
     }
 }
 
-// A[k][o] = sum_t zf_t[k] e_t[o] over a chunk of tokens: one thread per
-// element k of the flattened m d vector; per-chunk partials in mix_parts.
+// A[k][o] = sum_t zf_t[k] e_t[o] over a chunk of tokens: one thread per two
+// elements k of the flattened m d vector, eight tokens' loads at a time;
+// per-chunk partials in mix_parts.
 template <typename Tin>
 __global__ void __launch_bounds__(256) msar_mix_acc_kernel(const MsarBwdArgs a) {
     using P2 = Pair2<Tin>;
     constexpr int ES = sizeof(Tin);
+    constexpr int U = 8;
     const int64_t md = 4 * (int64_t)a.d;
     const int64_t k2 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 2;   // elements k2, k2 + 1
     if (k2 >= md) return;
@@ -204,14 +337,24 @@ __global__ void __launch_bounds__(256) msar_mix_acc_kernel(const MsarBwdArgs a) 
     const int64_t c = k2 - (int64_t)r * a.d;
     const int64_t t0 = (int64_t)blockIdx.y * a.tc;
     const int64_t t1 = t0 + a.tc < a.T ? t0 + a.tc : a.T;
+    const unsigned char *zr = a.z + ((int64_t)r * a.T * a.d + c) * ES;
     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t t = t0; t < t1; ++t) {
-        const float2 z = P2::ld(a.z + (((int64_t)r * a.T + t) * a.d + c) * ES);
-        const float4 e = __ldg(reinterpret_cast<const float4 *>(a.mix_e + t * 4));
-        acc0.x = fmaf(z.x, e.x, acc0.x); acc0.y = fmaf(z.x, e.y, acc0.y);
-        acc0.z = fmaf(z.x, e.z, acc0.z); acc0.w = fmaf(z.x, e.w, acc0.w);
-        acc1.x = fmaf(z.y, e.x, acc1.x); acc1.y = fmaf(z.y, e.y, acc1.y);
-        acc1.z = fmaf(z.y, e.z, acc1.z); acc1.w = fmaf(z.y, e.w, acc1.w);
+    for (int64_t t = t0; t < t1; t += U) {
+        float2 z[U];
+        float4 e[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool ok = t + u < t1;
+            z[u] = ok ? P2::ld(zr + (t + u) * a.d * ES) : make_float2(0.f, 0.f);
+            e[u] = ok ? __ldg(reinterpret_cast<const float4 *>(a.mix_e) + (t + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            acc0.x = fmaf(z[u].x, e[u].x, acc0.x); acc0.y = fmaf(z[u].x, e[u].y, acc0.y);
+            acc0.z = fmaf(z[u].x, e[u].z, acc0.z); acc0.w = fmaf(z[u].x, e[u].w, acc0.w);
+            acc1.x = fmaf(z[u].y, e[u].x, acc1.x); acc1.y = fmaf(z[u].y, e[u].y, acc1.y);
+            acc1.z = fmaf(z[u].y, e[u].z, acc1.z); acc1.w = fmaf(z[u].y, e[u].w, acc1.w);
+        }
     }
     float *wp = a.mix_parts + (size_t)blockIdx.y * (size_t)(md * 4);
     *reinterpret_cast<float4 *>(wp + k2 * 4) = acc0;
@@ -231,104 +374,187 @@ __global__ void __launch_bounds__(256) msar_mix_finish_kernel(const MsarBwdArgs 
 }
 
 // ---------------------------------------------------------------- step 5
-// One thread per (source, channel) walks a chunk of tokens downwards with a
-// register window of the three conv streams' gradients ahead
-// (dw_r[j] = du^(r)[t + j]) and of the source's rows behind (vw[j] = v[t - j]):
-//   dv[t]      = du^(0)[t] + sum_r sum_j cw_r[j] du^(r)[t + j]
-//   dcw_r[j]  += du^(r)[t] v[t - j]
-// The kernel-gradient partials of the thread's channel go to
-// conv_parts[(chunk * n_src + i)][ktot][d], packed like conv_w.  KA, KB, KC > 0
-// fix the kernel sizes at compile time; 0 reads them from the arguments
-// (windows of MSAR_KMAX rows).
-template <typename Tin> __device__ __forceinline__ float ld1(const unsigned char *p);
-template <> __device__ __forceinline__ float ld1<float>(const unsigned char *p) {
-    return *reinterpret_cast<const float *>(p);
-}
-template <> __device__ __forceinline__ float ld1<__nv_bfloat16>(const unsigned char *p) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
-}
-template <typename Tin> __device__ __forceinline__ void st1(unsigned char *p, float v);
-template <> __device__ __forceinline__ void st1<float>(unsigned char *p, float v) {
-    *reinterpret_cast<float *>(p) = v;
-}
-template <> __device__ __forceinline__ void st1<__nv_bfloat16>(unsigned char *p, float v) {
-    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
-}
+// CTA = (slice of CB_CH channels, source i, chunk [t0, t1) of tc tokens),
+// walked downwards one token at a time from t1 - 1 + (KM-1): the first KM-1
+// steps (t >= t1) only warm up the windows.  Warp-specialised, two adjacent
+// channels per thread:
+//   * the first CB_HALF threads scatter each new row of the conv streams'
+//     gradients into a window of pending outputs, pend[j] = dv[t - j]:
+//         pend[j] += cw_r[j] du^(r)[t]     (r = 1..3, j < k_r)
+//     after which dv[t] = pend[0] + du^(0)[t] is complete (every
+//     du^(r)[t + j] has arrived) and is written;
+//   * the other CB_HALF threads keep a window of the source's rows behind
+//     (vw[j] = v[t - j]) and the sums dcw_r[j] += du^(r)[t] v[t - j] for the
+//     chunk's own tokens.
+// Each step's five rows (du^(1..3)[t], du^(0)[t], v[t - (KM-1)]) arrive in
+// batches of RB steps into a ring of CB_NS stages, copied by all threads.
+// The kernel-gradient partials go to conv_parts[(chunk * n_src + i)][ktot][d]
+// with tap (r, j) at row koff_r + j and the channels contiguous (coalesced);
+// msar_conv_sum_kernel adds them up and packs them like conv_w.
+constexpr int CB_CH = 256;
+constexpr int CB_HALF = CB_CH / 2;
+constexpr int CB_THREADS = 2 * CB_HALF;
+constexpr int CB_NS = 4;
+constexpr int CB_NROW = 5;
+template <typename Tin> struct ConvBwdStage {
+    static constexpr int RB = sizeof(Tin) == 2 ? 8 : 4;            // steps per stage
+    static constexpr int ROWB = CB_CH * (int)sizeof(Tin);
+    static constexpr int BYTES = RB * CB_NROW * ROWB;              // 20 KB either way
+};
 
 template <typename Tin, int KA, int KB, int KC>
-__global__ void __launch_bounds__(256) msar_conv_bwd_kernel(const MsarBwdArgs a) {
-    constexpr bool FIXED = KA > 0;
-    constexpr int K0 = FIXED ? KA : MSAR_KMAX, K1 = FIXED ? KB : MSAR_KMAX, K2 = FIXED ? KC : MSAR_KMAX;
-    constexpr int KT = K0 + K1 + K2;
-    constexpr int KM = K0 > K1 ? (K0 > K2 ? K0 : K2) : (K1 > K2 ? K1 : K2);
+__global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kernel(const MsarBwdArgs a) {
+    using P2 = Pair2<Tin>;
+    using CS = ConvShape<KA, KB, KC>;
+    using SG = ConvBwdStage<Tin>;
     constexpr int ES = sizeof(Tin);
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    constexpr int H = CS::KM - 1;
+    constexpr int RB = SG::RB, ROWB = SG::ROWB;
+    constexpr int CPR = ROWB / 16;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const int lt = tid & (CB_HALF - 1);
+    const int cb = blockIdx.x * CB_CH;
+    const int c = cb + 2 * lt;
     const int i = blockIdx.y;
     const int64_t t0 = (int64_t)blockIdx.z * a.tc;
-    if (c >= a.d) return;
     const int64_t t1 = t0 + a.tc < a.T ? t0 + a.tc : a.T;
-    auto has = [&](int r, int j) { return FIXED || j < a.k[r]; };
-    float w[KT], g[KT], dw[KT], vw[KM];
-    {
+    const int64_t nsteps = t1 - t0 + H;           // step s is token t1 - 1 + H - s
+    const int nb = (int)((nsteps + RB - 1) / RB);
+    const int64_t rowb = (int64_t)a.d * ES;
+    const int64_t ttop = t1 - 1 + H;
+    const unsigned char *v = a.src + (int64_t)i * a.src_stride_bytes;
+    const uint32_t sbase = smem_u32(smem);
+    auto has = [&](int r, int j) { return CS::FIXED || j < a.k[r]; };
+    // stage layout [RB steps][5 rows][CB_CH channels]; rows outside the
+    // sequence (or du^(0) beyond the chunk) are zero-filled.  A stage holds
+    // RB x CPR = CB_THREADS (step, 16-byte chunk) pairs: each thread copies
+    // the five rows of its pair.
+    static_assert(RB * CPR == CB_THREADS, "one (step, chunk) pair per thread");
+    const int my_sb = tid / CPR, my_cc = tid - my_sb * CPR;
+    const int64_t coff = (int64_t)cb * ES + my_cc * 16;
+    const unsigned char *du_i = a.du + (int64_t)i * a.T * rowb + coff;     // du^(0) of source i
+    const int64_t sstride = (int64_t)a.n_src * a.T * rowb;                  // du^(r) -> du^(r+1)
+    const unsigned char *v_c = v + coff;
+    auto issue = [&](int b) {
+        const int64_t s = (int64_t)b * RB + my_sb;
+        const int64_t t = ttop - s;
+        const bool live = b < nb && s < nsteps;
+        const int64_t trow = t * rowb;
+        const uint32_t dst = sbase + (uint32_t)((b % CB_NS) * SG::BYTES + my_sb * CB_NROW * ROWB + my_cc * 16);
+        const bool okr = live && t < a.T;
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+            cp_async16(dst + r * ROWB, du_i + (r + 1) * sstride + (okr ? trow : 0), okr);
+        const bool ok0 = live && t < t1;
+        cp_async16(dst + 3 * ROWB, du_i + (ok0 ? trow : 0), ok0);
+        const bool okv = live && t - H >= 0;
+        cp_async16(dst + 4 * ROWB, v_c + (okv ? trow - H * rowb : 0), okv);
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int b = 0; b < CB_NS - 1; ++b) issue(b);
+
+    if (tid < CB_HALF) {
+        // ---- dv: the kernels and the window of pending outputs
+        float2 w[CS::KT], pend[CS::KM];
         int64_t off = 0;
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
 #pragma unroll
-            for (int j = 0; j < (r == 0 ? K0 : r == 1 ? K1 : K2); ++j) {
-                w[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j] = has(r, j) ? __ldg(a.conv_w + off + (int64_t)c * a.k[r] + j) : 0.f;
-                g[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j] = 0.f;
-            }
+            for (int j = 0; j < CS::k(r); ++j)
+                w[CS::off(r) + j] = has(r, j) ? make_float2(__ldg(a.conv_w + off + (int64_t)c * a.k[r] + j),
+                                                            __ldg(a.conv_w + off + (int64_t)(c + 1) * a.k[r] + j))
+                                              : make_float2(0.f, 0.f);
             off += (int64_t)a.d * a.k[r];
         }
-    }
-    const unsigned char *v = a.src + (int64_t)i * a.src_stride_bytes;
-    auto du_at = [&](int r, int64_t t) {          // du^(r+1)[t] of source i (zero past the end)
-        return t < a.T ? ld1<Tin>(a.du + ((((int64_t)(r + 1) * a.n_src + i) * a.T + t) * a.d + c) * ES) : 0.f;
-    };
-    // each step first moves the windows down one row; before the first step
-    // (t = t1 - 1) they hold dw_r[j] = du^(r)[t1 + j] and vw[j] = v[t1 - j]
 #pragma unroll
-    for (int r = 0; r < 3; ++r)
+        for (int j = 0; j < CS::KM; ++j) pend[j] = make_float2(0.f, 0.f);
+        unsigned char *dp = a.dsrc + (int64_t)i * a.dsrc_stride_bytes + (t1 - 1) * rowb + (int64_t)c * ES;
+        for (int b = 0; b < nb; ++b) {
+            cp_async_wait<CB_NS - 2>();
+            named_bar_sync(1, CB_THREADS);
+            issue(b + CB_NS - 1);
+            const unsigned char *stage = smem + (b % CB_NS) * SG::BYTES + 2 * lt * ES;
 #pragma unroll
-        for (int j = 0; j < (r == 0 ? K0 : r == 1 ? K1 : K2); ++j) dw[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j] = has(r, j) ? du_at(r, t1 + j) : 0.f;
+            for (int sb = 0; sb < RB; ++sb) {
+                const int64_t s = (int64_t)b * RB + sb;
+                if (s >= nsteps) break;
 #pragma unroll
-    for (int j = 0; j < KM; ++j) {
-        const int64_t tr = t1 - j;
-        vw[j] = (j >= 1 && tr >= 0) ? ld1<Tin>(v + (tr * a.d + c) * ES) : 0.f;
-    }
-    for (int64_t t = t1 - 1; t >= t0; --t) {
-        // windows move down one row: dw_r[j] = du^(r)[t + j], vw[j] = v[t - j]
+                for (int r = 0; r < 3; ++r) {
+                    const float2 dn = P2::ld(stage + (sb * CB_NROW + r) * ROWB);      // du^(r)[t]
+#pragma unroll
+                    for (int j = 0; j < CS::k(r); ++j)
+                        if (has(r, j)) pend[j] = ffma2(w[CS::off(r) + j], dn, pend[j]);
+                }
+                if (s >= H) {                                   // t < t1: dv[t] is complete
+                    const float2 d0 = P2::ld(stage + (sb * CB_NROW + 3) * ROWB);      // du^(0)[t]
+                    P2::st(dp, make_float2(d0.x + pend[0].x, d0.y + pend[0].y));
+                    dp -= rowb;
+                }
+#pragma unroll
+                for (int j = 0; j < CS::KM - 1; ++j) pend[j] = pend[j + 1];
+                pend[CS::KM - 1] = make_float2(0.f, 0.f);
+            }
+        }
+    } else {
+        // ---- dcw: the window of the source's rows behind and the sums
+        float2 g[CS::KT], vw[CS::KM];
+#pragma unroll
+        for (int j = 0; j < CS::KT; ++j) g[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < CS::KM; ++j) vw[j] = make_float2(0.f, 0.f);
+        for (int b = 0; b < nb; ++b) {
+            cp_async_wait<CB_NS - 2>();
+            named_bar_sync(1, CB_THREADS);
+            issue(b + CB_NS - 1);
+            const unsigned char *stage = smem + (b % CB_NS) * SG::BYTES + 2 * lt * ES;
+#pragma unroll
+            for (int sb = 0; sb < RB; ++sb) {
+                const int64_t s = (int64_t)b * RB + sb;
+                if (s >= nsteps) break;
+                // vw[j] = v[t - j]: the newest row is v[t - H]
+#pragma unroll
+                for (int j = 0; j < CS::KM - 1; ++j) vw[j] = vw[j + 1];
+                vw[CS::KM - 1] = P2::ld(stage + (sb * CB_NROW + 4) * ROWB);
+                if (s >= H) {
+#pragma unroll
+                    for (int r = 0; r < 3; ++r) {
+                        const float2 dn = P2::ld(stage + (sb * CB_NROW + r) * ROWB);  // du^(r)[t]
+#pragma unroll
+                        for (int j = 0; j < CS::k(r); ++j)
+                            if (has(r, j)) g[CS::off(r) + j] = ffma2(dn, vw[j], g[CS::off(r) + j]);
+                    }
+                }
+            }
+        }
+        float *gp = a.conv_parts + ((size_t)blockIdx.z * a.n_src + i) * (size_t)a.ktot * a.d + c;
+        int koff = 0;
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
 #pragma unroll
-            for (int j = (r == 0 ? K0 : r == 1 ? K1 : K2) - 1; j > 0; --j) dw[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j] = dw[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j - 1];
-            dw[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1)] = du_at(r, t);
+            for (int j = 0; j < CS::k(r); ++j)
+                if (has(r, j)) *reinterpret_cast<float2 *>(gp + (int64_t)(koff + j) * a.d) = g[CS::off(r) + j];
+            koff += a.k[r];
         }
-#pragma unroll
-        for (int j = 0; j < KM - 1; ++j) vw[j] = vw[j + 1];
-        {
-            const int64_t tr = t - (KM - 1);
-            vw[KM - 1] = tr >= 0 ? ld1<Tin>(v + (tr * a.d + c) * ES) : 0.f;
-        }
-        float acc = ld1<Tin>(a.du + (((int64_t)i * a.T + t) * a.d + c) * ES);     // du^(0)[t]
-#pragma unroll
-        for (int r = 0; r < 3; ++r)
-#pragma unroll
-            for (int j = 0; j < (r == 0 ? K0 : r == 1 ? K1 : K2); ++j)
-                if (has(r, j)) {
-                    acc = fmaf(w[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j], dw[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j], acc);
-                    g[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j] = fmaf(dw[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1)], vw[j], g[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j]);
-                }
-        st1<Tin>(a.dsrc + (int64_t)i * a.dsrc_stride_bytes + (t * a.d + c) * ES, acc);
     }
-    float *gp = a.conv_parts + ((size_t)blockIdx.z * a.n_src + i) * (size_t)a.ktot * a.d;
-    int koff = 0;
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
-#pragma unroll
-        for (int j = 0; j < (r == 0 ? K0 : r == 1 ? K1 : K2); ++j)
-            if (has(r, j)) gp[(int64_t)koff * a.d + (int64_t)c * a.k[r] + j] = g[(r == 0 ? 0 : r == 1 ? K0 : K0 + K1) + j];
-        koff += a.k[r];
+    cp_async_wait<0>();
+}
+
+// dconv_w from the conv partials: element e = (koff_r + j) * d + c of every
+// partial, summed over the partials in order, lands at koff_r * d + c * k_r + j
+// (conv_w's packing).
+__global__ void __launch_bounds__(256) msar_conv_sum_kernel(const float *parts, int64_t nparts, int d, int k0, int k1,
+                                                            int k2, float *out) {
+    const int ktot = k0 + k1 + k2;
+    const int64_t n = (int64_t)ktot * d;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int64_t p = 0; p < nparts; ++p) s += parts[p * n + e];
+        const int jg = (int)(e / d), c = (int)(e - (int64_t)jg * d);
+        const int kr = jg < k0 ? k0 : jg < k0 + k1 ? k1 : k2;
+        const int koff = jg < k0 ? 0 : jg < k0 + k1 ? k0 : k0 + k1;
+        out[(int64_t)koff * d + (int64_t)c * kr + (jg - koff)] = s;
     }
 }
 
@@ -344,44 +570,43 @@ __global__ void __launch_bounds__(256) msar_sum_kernel(const float *parts, int64
 }
 
 // ---------------------------------------------------------------- launchers
-template <typename Tin>
-static cudaError_t launch_streams_t(const MsarBwdArgs &a, cudaStream_t s) {
-    const dim3 grid((unsigned)((a.d / 2 + 255) / 256), (unsigned)a.n_src, (unsigned)((a.T + a.tc - 1) / a.tc));
-    msar_streams_kernel<Tin, MSAR_KMAX><<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
+static bool k4812(const MsarBwdArgs &a) { return a.k[0] == 4 && a.k[1] == 8 && a.k[2] == 12; }
+
+template <typename F> static cudaError_t set_smem(F fn, size_t bytes) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <typename Tin>
-static cudaError_t launch_conv_bwd_t(const MsarBwdArgs &a, cudaStream_t s) {
-    const dim3 grid((unsigned)((a.d + 255) / 256), (unsigned)a.n_src, (unsigned)((a.T + a.tc - 1) / a.tc));
-    if (a.k[0] == 4 && a.k[1] == 8 && a.k[2] == 12)
-        msar_conv_bwd_kernel<Tin, 4, 8, 12><<<grid, 256, 0, s>>>(a);
-    else
-        msar_conv_bwd_kernel<Tin, 0, 0, 0><<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <typename Tin, int NT>
-static cudaError_t launch_mix_bwd_nt(const MsarBwdArgs &a, int sms, cudaStream_t s) {
-    auto fn = msar_mix_bwd_kernel<Tin, NT, 8>;
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, NT, 0);
+template <typename Tin, int KA, int KB, int KC>
+static cudaError_t launch_streams_k(const MsarBwdArgs &a, cudaStream_t s) {
+    auto fn = msar_streams_kernel<Tin, KA, KB, KC>;
+    const size_t smem = (size_t)ST_NS * ST_RB * ST_CB * sizeof(Tin);
+    cudaError_t e = set_smem(fn, smem);
     if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int64_t slots = (int64_t)sms * occ;
-    fn<<<(unsigned)(a.T < slots ? a.T : slots), NT, 0, s>>>(a);
+    const dim3 grid((unsigned)(a.d / ST_CB), (unsigned)a.n_src, (unsigned)((a.T + a.tc_s - 1) / a.tc_s));
+    fn<<<grid, ST_THREADS, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tin, int KA, int KB, int KC>
+static cudaError_t launch_conv_bwd_k(const MsarBwdArgs &a, cudaStream_t s) {
+    auto fn = msar_conv_bwd_kernel<Tin, KA, KB, KC>;
+    const size_t smem = (size_t)CB_NS * ConvBwdStage<Tin>::BYTES;
+    cudaError_t e = set_smem(fn, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)(a.d / CB_CH), (unsigned)a.n_src, (unsigned)((a.T + a.tc - 1) / a.tc));
+    fn<<<grid, CB_THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 template <typename Tin>
-static cudaError_t launch_mix_bwd_t(const MsarBwdArgs &a, int sms, cudaStream_t s) {
-    cudaError_t e;
-    switch (a.d) {
-        case 1024: e = launch_mix_bwd_nt<Tin, 128>(a, sms, s); break;
-        case 2048: e = launch_mix_bwd_nt<Tin, 256>(a, sms, s); break;
-        case 4096: e = launch_mix_bwd_nt<Tin, 512>(a, sms, s); break;
-        default: return cudaErrorInvalidValue;
-    }
+static cudaError_t launch_mix_t(const MsarBwdArgs &a, cudaStream_t s) {
+    const dim3 grid((unsigned)a.nsl, (unsigned)((a.T + a.tc_m - 1) / a.tc_m));
+    cudaError_t e = set_smem(msar_mix_stats_kernel<Tin>, MX_SMEM);
+    if (e == cudaSuccess) e = set_smem(msar_mix_dz_kernel<Tin>, MX_SMEM);
+    if (e != cudaSuccess) return e;
+    msar_mix_stats_kernel<Tin><<<grid, MX_THREADS, MX_SMEM, s>>>(a);
+    msar_mix_dz_kernel<Tin><<<grid, MX_THREADS, MX_SMEM, s>>>(a);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const dim3 agrid((unsigned)((2 * (int64_t)a.d + 255) / 256), (unsigned)((a.T + a.tc - 1) / a.tc));
     msar_mix_acc_kernel<Tin><<<agrid, 256, 0, s>>>(a);
@@ -390,17 +615,32 @@ static cudaError_t launch_mix_bwd_t(const MsarBwdArgs &a, int sms, cudaStream_t 
 
 cudaError_t msar_bwd_streams(int dt, const MsarBwdArgs &a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return dt == 1 ? launch_streams_t<__nv_bfloat16>(a, s) : launch_streams_t<float>(a, s);
+    if (a.d % ST_CB != 0) return cudaErrorInvalidValue;
+    if (dt == 1)
+        return k4812(a) ? launch_streams_k<__nv_bfloat16, 4, 8, 12>(a, s) : launch_streams_k<__nv_bfloat16, 0, 0, 0>(a, s);
+    return k4812(a) ? launch_streams_k<float, 4, 8, 12>(a, s) : launch_streams_k<float, 0, 0, 0>(a, s);
 }
 
-cudaError_t msar_bwd_mix(int dt, const MsarBwdArgs &a, int sms, void *stream) {
+cudaError_t msar_bwd_mix(int dt, const MsarBwdArgs &a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return dt == 1 ? launch_mix_bwd_t<__nv_bfloat16>(a, sms, s) : launch_mix_bwd_t<float>(a, sms, s);
+    if (a.d % MX_CS != 0 || a.nsl != a.d / MX_CS) return cudaErrorInvalidValue;
+    return dt == 1 ? launch_mix_t<__nv_bfloat16>(a, s) : launch_mix_t<float>(a, s);
 }
 
 cudaError_t msar_bwd_conv(int dt, const MsarBwdArgs &a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return dt == 1 ? launch_conv_bwd_t<__nv_bfloat16>(a, s) : launch_conv_bwd_t<float>(a, s);
+    if (a.d % CB_CH != 0) return cudaErrorInvalidValue;
+    if (dt == 1)
+        return k4812(a) ? launch_conv_bwd_k<__nv_bfloat16, 4, 8, 12>(a, s) : launch_conv_bwd_k<__nv_bfloat16, 0, 0, 0>(a, s);
+    return k4812(a) ? launch_conv_bwd_k<float, 4, 8, 12>(a, s) : launch_conv_bwd_k<float, 0, 0, 0>(a, s);
+}
+
+cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, int64_t nparts, float *dconv_w, void *stream) {
+    const int64_t n = (int64_t)a.ktot * a.d;
+    const int64_t blocks = (n + 255) / 256;
+    msar_conv_sum_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        a.conv_parts, nparts, a.d, a.k[0], a.k[1], a.k[2], dconv_w);
+    return cudaGetLastError();
 }
 
 cudaError_t msar_bwd_mix_finish(const MsarBwdArgs &a, const float *A, void *stream) {

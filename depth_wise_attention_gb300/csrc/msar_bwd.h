@@ -17,7 +17,10 @@ struct MsarBwdArgs {
     int k[3];                       // kernel sizes of streams 1..3
     int ktot;                       // k[0] + k[1] + k[2]
     const float *conv_w;            // packed [d][k_1] [d][k_2] [d][k_3]
-    int64_t tc;                     // tokens per chunk (streams, conv backward, mixer sums)
+    int64_t tc;                     // tokens per chunk of the conv backward and of A's partials
+    int64_t tc_s;                   // tokens per chunk of the streams kernel
+    int64_t tc_m;                   // tokens per CTA of the mixer kernels
+    int nsl;                        // channel slices of the mixer (d / 1024)
     unsigned char *u;               // [3][n_src][T][d] the conv streams (source dtype)
     unsigned char *z;               // [4][T][d] the per-stream reads
     unsigned char *dz;              // [4][T][d] their gradients
@@ -25,23 +28,26 @@ struct MsarBwdArgs {
     const float *mix_gain;          // [4d] or nullptr
     const float *mix_w;             // [4d][4]
     float mix_eps;
+    float *mix_part;                // [T][nsl][9] the mixer's per-slice sums
     float *mix_e;                   // [T][4] dl_t / nu_t
     float *mix_parts;               // [chunks][4d][4] partial sums of A
     unsigned char *du;              // [4][n_src][T][d] the streams' gradients (source dtype)
     unsigned char *dsrc;            // [n_src] gradients, dsrc_stride_bytes apart
     int64_t dsrc_stride_bytes;
-    float *conv_parts;              // [chunks][n_src][ktot][d] partial sums of dconv_w
+    float *conv_parts;              // [chunks][n_src][ktot][d] partial sums of dconv_w (tap-major)
     float *dmix_w;                  // [4d][4]
     float *dmix_gain;               // [4d] or nullptr
 };
 
 cudaError_t msar_bwd_streams(int dt, const MsarBwdArgs &a, void *stream);
-// mixer backward (dz, mix_e) and the per-chunk partials of A; d is 1024,
-// 2048 or 4096 (cudaErrorInvalidValue otherwise)
-cudaError_t msar_bwd_mix(int dt, const MsarBwdArgs &a, int sms, void *stream);
+// mixer backward (dz, mix_e) and the per-chunk partials of A; d a multiple
+// of 1024 with nsl = d / 1024 (cudaErrorInvalidValue otherwise)
+cudaError_t msar_bwd_mix(int dt, const MsarBwdArgs &a, void *stream);
 // dmix_w and dmix_gain from A
 cudaError_t msar_bwd_mix_finish(const MsarBwdArgs &a, const float *A, void *stream);
 cudaError_t msar_bwd_conv(int dt, const MsarBwdArgs &a, void *stream);
+// dconv_w (packed like conv_w) = the nparts conv partials summed in order
+cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, int64_t nparts, float *dconv_w, void *stream);
 // out[e] = (accumulate ? out[e] : 0) + sum_p parts[p][e] in order of p
 cudaError_t msar_bwd_sum(const float *parts, int64_t nparts, int64_t n, float *out, int accumulate, void *stream);
 
