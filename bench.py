@@ -892,7 +892,7 @@ class MsarBwdWorkload(MsarWorkload):
         # read the sources and dh, write the sources' gradients
         self.bytes_per_token = (2 * N + 1) * d * b
         self.phase1_bytes_per_token = self.bytes_per_token
-        self.launches_per_step = 1 + 4 + 2 + 2 + 4 * 2 + 1 + 2
+        self.launches_per_step = 1 + 4 + 3 + 2 + 4 * 2 + 1 + 2
         self.dominant = "msar backward (whole chain)"
         self.dominant_src = "msar_bwd"
         self.profile_tag = f"ncu_msar_bwd_d{d}"

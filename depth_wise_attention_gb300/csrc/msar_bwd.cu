@@ -322,43 +322,55 @@ __global__ void __launch_bounds__(MX_THREADS) msar_mix_dz_kernel(const MsarBwdAr
     }
 }
 
-// A[k][o] = sum_t zf_t[k] e_t[o] over a chunk of tokens: one thread per two
-// elements k of the flattened m d vector, eight tokens' loads at a time;
-// per-chunk partials in mix_parts.
+// A[k][o] = sum_t zf_t[k] e_t[o] over a chunk of tokens: one thread per 8
+// adjacent elements k of the flattened m d vector (one 16-byte load per
+// token), four tokens' loads at a time; per-chunk partials in mix_parts.
 template <typename Tin>
 __global__ void __launch_bounds__(256) msar_mix_acc_kernel(const MsarBwdArgs a) {
-    using P2 = Pair2<Tin>;
     constexpr int ES = sizeof(Tin);
-    constexpr int U = 8;
+    constexpr int U = 4;
     const int64_t md = 4 * (int64_t)a.d;
-    const int64_t k2 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 2;   // elements k2, k2 + 1
-    if (k2 >= md) return;
-    const int r = (int)(k2 / a.d);
-    const int64_t c = k2 - (int64_t)r * a.d;
+    const int64_t k8 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;   // elements k8 .. k8 + 7
+    if (k8 >= md) return;
+    const int r = (int)(k8 / a.d);
+    const int64_t c = k8 - (int64_t)r * a.d;
     const int64_t t0 = (int64_t)blockIdx.y * a.tc;
     const int64_t t1 = t0 + a.tc < a.T ? t0 + a.tc : a.T;
-    const unsigned char *zr = a.z + ((int64_t)r * a.T * a.d + c) * ES;
-    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t rowb = (int64_t)a.d * ES;
+    const unsigned char *zr = a.z + (int64_t)r * a.T * rowb + c * ES;
+    float acc[8][4];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int o = 0; o < 4; ++o) acc[e][o] = 0.f;
     for (int64_t t = t0; t < t1; t += U) {
-        float2 z[U];
-        float4 e[U];
+        float z[U][8];
+        float4 ev[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool ok = t + u < t1;
-            z[u] = ok ? P2::ld(zr + (t + u) * a.d * ES) : make_float2(0.f, 0.f);
-            e[u] = ok ? __ldg(reinterpret_cast<const float4 *>(a.mix_e) + (t + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ok) {
+                load8<Tin>(zr + (t + u) * rowb, z[u]);
+                ev[u] = __ldg(reinterpret_cast<const float4 *>(a.mix_e) + (t + u));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) z[u][e] = 0.f;
+                ev[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            acc0.x = fmaf(z[u].x, e[u].x, acc0.x); acc0.y = fmaf(z[u].x, e[u].y, acc0.y);
-            acc0.z = fmaf(z[u].x, e[u].z, acc0.z); acc0.w = fmaf(z[u].x, e[u].w, acc0.w);
-            acc1.x = fmaf(z[u].y, e[u].x, acc1.x); acc1.y = fmaf(z[u].y, e[u].y, acc1.y);
-            acc1.z = fmaf(z[u].y, e[u].z, acc1.z); acc1.w = fmaf(z[u].y, e[u].w, acc1.w);
-        }
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                acc[e][0] = fmaf(z[u][e], ev[u].x, acc[e][0]);
+                acc[e][1] = fmaf(z[u][e], ev[u].y, acc[e][1]);
+                acc[e][2] = fmaf(z[u][e], ev[u].z, acc[e][2]);
+                acc[e][3] = fmaf(z[u][e], ev[u].w, acc[e][3]);
+            }
     }
-    float *wp = a.mix_parts + (size_t)blockIdx.y * (size_t)(md * 4);
-    *reinterpret_cast<float4 *>(wp + k2 * 4) = acc0;
-    *reinterpret_cast<float4 *>(wp + (k2 + 1) * 4) = acc1;
+    float4 *wp = reinterpret_cast<float4 *>(a.mix_parts + (size_t)blockIdx.y * (size_t)(md * 4)) + k8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) wp[e] = make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
 }
 
 // dmix_w[k][o] = mg_k A[k][o];  dmix_gain[k] = sum_o P[k][o] A[k][o]
@@ -608,7 +620,7 @@ static cudaError_t launch_mix_t(const MsarBwdArgs &a, cudaStream_t s) {
     msar_mix_dz_kernel<Tin><<<grid, MX_THREADS, MX_SMEM, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const dim3 agrid((unsigned)((2 * (int64_t)a.d + 255) / 256), (unsigned)((a.T + a.tc - 1) / a.tc));
+    const dim3 agrid((unsigned)((4 * (int64_t)a.d / 8 + 255) / 256), (unsigned)((a.T + a.tc - 1) / a.tc));
     msar_mix_acc_kernel<Tin><<<agrid, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
