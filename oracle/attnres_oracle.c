@@ -707,14 +707,19 @@ int oracle_msar_ps(const double *src, int64_t n_src, int64_t T, int64_t d, int64
  *           dv_i[t-j][c] += cw_r[c][j] du_i^(r)[t][c],  dcw_r[c][j] += du_i^(r)[t][c] v_i[t-j][c]
  * Outputs: dsrc[n_src][T][d], dconv_w (packed as conv_w), dq[m][d], dg[d],
  * dmix_gain[m*d], dmix_w[m*d][m]. */
-int oracle_msar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
-                    const int32_t *ksizes, const double *conv_w, const double *queries,
-                    const double *gain, double eps, const double *mix_gain, const double *mix_w,
-                    double mix_eps, const double *dh, double *dsrc, double *dconv_w, double *dq,
-                    double *dg, double *dmix_gain, double *dmix_w)
+/* Shared by the two entry points below: conv_src_stride = 0 gives every
+ * source the kernels at conv_w and sums dconv_w over the sources; > 0 gives
+ * source i the kernels at conv_w + i * conv_src_stride and its own gradient at
+ * dconv_w + i * conv_src_stride (the per-source reading of oracle_msar_ps). */
+static int msar_bwd_impl(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                         const int32_t *ksizes, const double *conv_w, int64_t conv_src_stride,
+                         const double *queries, const double *gain, double eps, const double *mix_gain,
+                         const double *mix_w, double mix_eps, const double *dh, double *dsrc, double *dconv_w,
+                         double *dq, double *dg, double *dmix_gain, double *dmix_w)
 {
     if (!src || !ksizes || !conv_w || !queries || !mix_w || !dh || !dsrc || !dconv_w || !dq || !dg ||
-        !dmix_gain || !dmix_w || n_src < 1 || T < 0 || d < 1 || m < 1 || eps < 0 || mix_eps < 0)
+        !dmix_gain || !dmix_w || n_src < 1 || T < 0 || d < 1 || m < 1 || eps < 0 || mix_eps < 0 ||
+        conv_src_stride < 0)
         return -1;
     const size_t per = (size_t)T * (size_t)d, md = (size_t)m * (size_t)d;
     int64_t ktot = 0;
@@ -733,7 +738,8 @@ int oracle_msar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int6
     const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_src);
     int rc = (u && Z && dZ && du && dqr && dgr && zf && zn && dzn && c && dl && rows) ? 0 : -1;
     for (size_t k = 0; rc == 0 && k < (size_t)n_src * per; ++k) dsrc[k] = 0.0;
-    for (int64_t k = 0; rc == 0 && k < d * ktot; ++k) dconv_w[k] = 0.0;
+    for (int64_t i = 0; rc == 0 && i < (conv_src_stride ? n_src : 1); ++i)
+        for (int64_t k = 0; k < d * ktot; ++k) dconv_w[i * conv_src_stride + k] = 0.0;
     for (size_t k = 0; rc == 0 && k < md; ++k) { dmix_gain[k] = 0.0; for (int64_t o = 0; o < m; ++o) dmix_w[k * m + o] = 0.0; }
     for (int64_t k = 0; rc == 0 && k < d; ++k) dg[k] = 0.0;
     /* forward: streams and per-stream reads */
@@ -742,7 +748,7 @@ int oracle_msar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int6
             const double *v = src + (size_t)i * per;
             double *ur = u + ((size_t)r * (size_t)n_src + (size_t)i) * per;
             if (r == 0) memcpy(ur, v, sizeof(double) * per);
-            else rc = oracle_msar_conv(v, T, d, ksizes[r - 1], conv_w + off, ur);
+            else rc = oracle_msar_conv(v, T, d, ksizes[r - 1], conv_w + i * conv_src_stride + off, ur);
         }
         if (r >= 1) off += d * (int64_t)ksizes[r - 1];
         for (int64_t t = 0; t < T && rc == 0; ++t) {
@@ -798,9 +804,9 @@ int oracle_msar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int6
             continue;
         }
         const int64_t kr = ksizes[r - 1];
-        const double *cw = conv_w + off;
-        double *dcw = dconv_w + off;
         for (int64_t i = 0; i < n_src; ++i) {
+            const double *cw = conv_w + i * conv_src_stride + off;
+            double *dcw = dconv_w + i * conv_src_stride + off;
             const double *v = src + (size_t)i * per;
             const double *dui = du + (size_t)i * per;
             double *dv = dsrc + (size_t)i * per;
@@ -817,6 +823,32 @@ int oracle_msar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int6
     free(u); free(Z); free(dZ); free(du); free(dqr); free(dgr); free(zf); free(zn); free(dzn); free(c); free(dl);
     free(rows);
     return rc;
+}
+
+int oracle_msar_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                    const int32_t *ksizes, const double *conv_w, const double *queries,
+                    const double *gain, double eps, const double *mix_gain, const double *mix_w,
+                    double mix_eps, const double *dh, double *dsrc, double *dconv_w, double *dq,
+                    double *dg, double *dmix_gain, double *dmix_w)
+{
+    return msar_bwd_impl(src, n_src, T, d, m, ksizes, conv_w, 0, queries, gain, eps, mix_gain, mix_w, mix_eps,
+                         dh, dsrc, dconv_w, dq, dg, dmix_gain, dmix_w);
+}
+
+/* Backward of oracle_msar_ps (each source's own kernels, conv_src_stride > 0
+ * floats apart): the chain rule of oracle_msar_bwd with source i's streams
+ * taken through its own kernels, and dconv_w written per source at the same
+ * stride (the floats between one source's kernels and the next are left
+ * untouched).  [MSAR 무엇과 다른가], the streams v_i^(r) of each source. */
+int oracle_msar_ps_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                       const int32_t *ksizes, const double *conv_w, int64_t conv_src_stride,
+                       const double *queries, const double *gain, double eps, const double *mix_gain,
+                       const double *mix_w, double mix_eps, const double *dh, double *dsrc, double *dconv_w,
+                       double *dq, double *dg, double *dmix_gain, double *dmix_w)
+{
+    if (conv_src_stride < 1) return -1;
+    return msar_bwd_impl(src, n_src, T, d, m, ksizes, conv_w, conv_src_stride, queries, gain, eps, mix_gain,
+                         mix_w, mix_eps, dh, dsrc, dconv_w, dq, dg, dmix_gain, dmix_w);
 }
 
 /* MSAR inside the two-phase Block schedule, phase 1.  [MSAR §어떻게 쓰나]:

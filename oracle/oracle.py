@@ -71,6 +71,8 @@ def _load():
                                         ctypes.c_double, _D, _D, _D, _D, _D, _D, _D]
         lib.oracle_msar_ps.argtypes = [_D, _I64, _I64, _I64, _I64, _K, _D, _I64, _D, _D, ctypes.c_double, _D, _D,
                                        ctypes.c_double, _D]
+        lib.oracle_msar_ps_bwd.argtypes = [_D, _I64, _I64, _I64, _I64, _K, _D, _I64, _D, _D, ctypes.c_double, _D,
+                                           _D, ctypes.c_double, _D, _D, _D, _D, _D, _D, _D]
         lib.oracle_msar_phase1.argtypes = [_D, _I64, _I64, _I64, _I64, _K, _D, _D, _I64, _D, ctypes.c_double,
                                            _D, _D]
         lib.oracle_msar_phase2.argtypes = [_D, _D, _D, _I64, _I64, _I64, _K, _D, _D, _D, ctypes.c_double, _D, _D,
@@ -79,7 +81,8 @@ def _load():
                   "oracle_block_phase1", "oracle_block_phase2", "oracle_block_phase2_update",
                   "oracle_mhar_phase2", "oracle_read_bwd", "oracle_read_bwd_lse", "oracle_block_phase2_bwd",
                   "oracle_mhar_bwd", "oracle_mhar",
-                  "oracle_msar_conv", "oracle_msar", "oracle_msar_bwd", "oracle_msar_ps", "oracle_msar_phase1", "oracle_msar_phase2"):
+                  "oracle_msar_conv", "oracle_msar", "oracle_msar_bwd", "oracle_msar_ps", "oracle_msar_ps_bwd", "oracle_msar_phase1",
+                  "oracle_msar_phase2"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -355,6 +358,29 @@ def msar_ps(src, ksizes, conv_w, queries, gain=None, eps=1e-6, mix_gain=None, mi
                                   _p(conv_w), conv_w.shape[1], _p(queries), _p(gain), float(eps), _p(mix_gain),
                                   _p(mix_w), float(mix_eps), _p(out)), "oracle_msar_ps")
     return out
+
+
+def msar_ps_bwd(src, ksizes, conv_w, queries, dh, gain=None, eps=1e-6, mix_gain=None, mix_w=None, mix_eps=1e-6):
+    """Backward of msar_ps for dh [T,d] -> (dsrc [n_src,T,d], dconv_w [n_src,
+    d*sum(k)] (each source's own), dq [m,d], dgain [d], dmix_gain [m*d],
+    dmix_w [m*d,m])."""
+    src, conv_w, queries, dh = _f64(src), _f64(conv_w), _f64(queries), _f64(dh)
+    gain, mix_gain, mix_w = _f64(gain), _f64(mix_gain), _f64(mix_w)
+    n_src, T, d = src.shape
+    m = queries.shape[0]
+    ks = np.ascontiguousarray(ksizes, dtype=np.int32)
+    assert ks.shape == (m - 1,) and conv_w.shape == (n_src, d * int(ks.sum())) and mix_w.shape == (m * d, m)
+    dsrc = np.empty((n_src, T, d))
+    dcw = np.empty(conv_w.shape)
+    dq = np.empty((m, d))
+    dg = np.empty(d)
+    dmg = np.empty(m * d)
+    dmw = np.empty((m * d, m))
+    _check(_load().oracle_msar_ps_bwd(_p(src), n_src, T, d, m, ks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                      _p(conv_w), conv_w.shape[1], _p(queries), _p(gain), float(eps), _p(mix_gain),
+                                      _p(mix_w), float(mix_eps), _p(dh), _p(dsrc), _p(dcw), _p(dq), _p(dg), _p(dmg),
+                                      _p(dmw)), "oracle_msar_ps_bwd")
+    return dsrc, dcw, dq, dg, dmg, dmw
 
 
 def msar_bwd(src, ksizes, conv_w, queries, dh, gain=None, eps=1e-6, mix_gain=None, mix_w=None, mix_eps=1e-6):

@@ -790,6 +790,43 @@ def test_msar_bwd_identity_stream_only_is_read_backward():
     assert np.allclose(got[0], ref[0], atol=1e-12) and np.allclose(got[2][0], ref[1][0], atol=1e-12)
 
 
+@pytest.mark.parametrize("N,T,d,ks", [(3, 7, 4, (2, 3, 4)), (2, 6, 4, (1, 4, 2))])
+def test_msar_ps_bwd_matches_finite_differences(N, T, d, ks):
+    """Every gradient of the MSAR read with per-source kernels, each source's
+    kernel gradient on its own, against central differences of the (pinned)
+    per-source forward oracle."""
+    rng = np.random.default_rng(95 + N + T)
+    src = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
+    cw = _rand(rng, N, d * sum(ks), scale=0.6)
+    q = _rand(rng, 4, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d)
+    mg = rng.uniform(0.5, 1.5, 4 * d)
+    P = _rand(rng, 4 * d, 4, scale=0.5)
+    dh = _rand(rng, T, d)
+
+    def loss(s_, cw_, q_, g_, mg_, P_):
+        return float((oracle.msar_ps(s_, ks, cw_, q_, g_, 1e-6, mg_, P_, 1e-6) * dh).sum())
+    got = oracle.msar_ps_bwd(src, ks, cw, q, dh, g, 1e-6, mg, P, 1e-6)
+    ref = _fd(loss, (src, cw, q, g, mg, P))
+    for name, x, y in zip(("dsrc", "dconv_w", "dq", "dgain", "dmix_gain", "dmix_w"), got, ref):
+        assert np.abs(x - y).max() <= 2e-6 * max(1.0, np.abs(y).max()), name
+
+
+def test_msar_ps_bwd_equal_kernels_is_the_shared_backward():
+    """Per-source kernels that are all equal: every gradient but the kernels'
+    is the shared-kernel backward's, and the sources' kernel gradients add up
+    to the shared kernel's (the shared kernel is used by every source)."""
+    rng = np.random.default_rng(96)
+    N, T, d, ks = 4, 9, 6, (4, 8, 12)
+    src, q, dh = _rand(rng, N, T, d), _rand(rng, 4, d, scale=1.5), _rand(rng, T, d)
+    cw, P = _rand(rng, d * sum(ks), scale=0.4), _rand(rng, 4 * d, 4, scale=0.3)
+    shared = oracle.msar_bwd(src, ks, cw, q, dh, None, 1e-6, None, P, 1e-6)
+    per = oracle.msar_ps_bwd(src, ks, np.stack([cw] * N), q, dh, None, 1e-6, None, P, 1e-6)
+    for k in (0, 2, 3, 4, 5):
+        assert np.allclose(per[k], shared[k], atol=1e-12, rtol=0), k
+    assert np.allclose(per[1].sum(axis=0), shared[1], atol=1e-12, rtol=0)
+
+
 def _msar_block_inputs(rng, N, S, T, d, ks=(4, 8, 12)):
     cached = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
     parts = _rand(rng, S, T, d)

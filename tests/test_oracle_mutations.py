@@ -56,6 +56,10 @@ MUTANTS = {
                                            "dv[t * d + k] += cw[k * kr + j] * dui[t * d + k];")],
     "msar_bwd_kernel_grad_unshifted": [("dcw[k * kr + j] += dui[t * d + k] * v[(t - j) * d + k];",
                                         "dcw[k * kr + j] += dui[t * d + k] * v[t * d + k];")],
+    "msar_ps_bwd_shared_kernel_in_transpose": [("const double *cw = conv_w + i * conv_src_stride + off;",
+                                                "const double *cw = conv_w + off;")],
+    "msar_ps_bwd_kernel_grad_not_per_source": [("double *dcw = dconv_w + i * conv_src_stride + off;",
+                                                "double *dcw = dconv_w + off;")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
