@@ -10,7 +10,7 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|mhar_block|msar|
-msar_block|msar_chunked|msar_ps|msar_bwd|full_depth|block_d2048|block_fused|block_bwd|
+msar_block|msar_chunked|msar_ps|msar_bwd|msar_bwd_ps|full_depth|block_d2048|block_fused|block_bwd|
 read_bwd|mhar_bwd|decode) are for profiling and the design notes.
 """
 from __future__ import annotations
@@ -956,6 +956,48 @@ class MsarBwdWorkload(MsarWorkload):
         return len(wins)
 
 
+class MsarBwdPerSourceWorkload(MsarBwdWorkload):
+    """The MSAR backward with each of the N=8 sources' own conv kernels
+    (msar_expand_bwd_ps): kernels ~ N(0, 1/k) per source, each source's
+    kernel gradient on its own."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0):
+        super().__init__(T, d, N, seed)
+        self.name = "msar_read_backward_per_source_kernels"
+        self.profile_tag = f"ncu_msar_bwd_per_source_d{d}"
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import inputs
+        super().setup(device)
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed + 5)
+        self.conv_w = torch.stack([torch.cat([inputs.device_normal((self.d * k,), (1.0 / k) ** 0.5, g, device=device)
+                                              for k in self.ks]) for _ in range(self.N)])
+        self.grads = (torch.empty_like(self.conv_w),) + self.grads[1:]
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.msar_expand_bwd_ps(self.cache, self.ks, self.conv_w, self.queries, self.dh, None, 1e-6, None,
+                                   self.mix_w, 1e-6, dsrc=self.dsrc, grads=self.grads, workspace=self.ws,
+                                   stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        wins, dhs, _, q, mw = super().oracle_sample(n_tokens, seed)
+        return wins, dhs, self.conv_w.cpu().numpy().astype(np.float64), q, mw
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        wins, dhs, cw, q, mw = sample
+        for w, dw in zip(wins, dhs):
+            oracle.msar_ps_bwd(w, self.ks, cw, q, dw, None, 1e-6, None, mw, 1e-6)
+        return len(wins)
+
+
 class MsarBlockWorkload(MsarWorkload):
     """MSAR inside the two-phase Block schedule: one block of S=4 layers over
     N=8 cached sources, bf16, d=4096.  One step = phase 1 (every source
@@ -1219,6 +1261,8 @@ def make_workload(name, T=None):
         return MsarBlockWorkload(T=T or 32768)
     if name == "msar_bwd":
         return MsarBwdWorkload(T=T or 32768)
+    if name == "msar_bwd_ps":
+        return MsarBwdPerSourceWorkload(T=T or 32768)
     if name == "block_fused":
         return BlockFusedWorkload(T=T or 32768)
     if name == "full_depth":
@@ -1469,7 +1513,7 @@ def main():
     ap.add_argument("--workload", default="block",
                     choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
                              "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block",
-                             "msar_bwd", "full_depth"])
+                             "msar_bwd", "msar_bwd_ps", "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

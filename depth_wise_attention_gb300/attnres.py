@@ -60,6 +60,8 @@ _SIGS = {
     "msar_expand_bwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
                         _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "msar_expand_bwd_workspace_size": [_i64, _i64, _i64, ctypes.c_int, _i64, _vp, ctypes.POINTER(ctypes.c_size_t)],
+    "msar_expand_bwd_ps": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _i64, _vp, _vp, _f, _vp, _vp,
+                           _f, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "attnres_status_string": [ctypes.c_int],
     "attnres_last_cuda_error": [],
     "attnres_sync_status": [_vp],
@@ -527,4 +529,37 @@ def msar_expand_bwd(src, ksizes, conv_w, queries, dh, gain=None, eps=1e-6, mix_g
         _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries), _p(gain), eps,
         _p(mix_gain), _p(mix_w), mix_eps, _p(dh), _p(dsrc), dstride, _p(dconv_w), _p(dqueries), _p(dgain),
         _p(dmix_gain), _p(dmix_w), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dsrc, dconv_w, dqueries, dgain, dmix_gain, dmix_w
+
+
+def msar_expand_bwd_ps(src, ksizes, conv_w, queries, dh, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                       mix_eps=1e-6, dsrc=None, want_dgain=True, want_dmix_gain=True, grads=None, workspace=None,
+                       stream=None):
+    """Backward of msar_expand_fwd_ps: conv_w [n_src, stride >= d*sum(k)] ->
+    (dsrc, dconv_w [n_src, stride] (each source's own; the padding past
+    d*sum(k) is zero), dqueries, dgain, dmix_gain, dmix_w)."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    m = queries.shape[0]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    dev = src.device
+    if dsrc is None:
+        dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=dev)
+    _, _, _, dstride = _src_geometry(dsrc)
+    if grads is not None:
+        dconv_w, dqueries, dgain, dmix_gain, dmix_w = grads
+    else:
+        dconv_w = torch.zeros(conv_w.shape, dtype=torch.float32, device=dev)
+        dqueries = torch.empty((m, d), dtype=torch.float32, device=dev)
+        dgain = torch.empty((d,), dtype=torch.float32, device=dev) if want_dgain else None
+        dmix_gain = torch.empty((m * d,), dtype=torch.float32, device=dev) if want_dmix_gain else None
+        dmix_w = torch.empty((m * d, m), dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = msar_expand_bwd_workspace_size(n_src, T, d, src.dtype, ksizes)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=dev)
+    _check("msar_expand_bwd_ps", load().msar_expand_bwd_ps(
+        _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), conv_w.stride(0), _p(queries),
+        _p(gain), eps, _p(mix_gain), _p(mix_w), mix_eps, _p(dh), _p(dsrc), dstride, _p(dconv_w), _p(dqueries),
+        _p(dgain), _p(dmix_gain), _p(dmix_w), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return dsrc, dconv_w, dqueries, dgain, dmix_gain, dmix_w

@@ -1033,7 +1033,8 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
                                  const float *queries, const float *gain, float eps, const float *mix_gain,
                                  const float *mix_w, float mix_eps, const void *dh, void *dsrc,
                                  int64_t dsrc_stride, float *dconv_w, float *dqueries, float *dgain,
-                                 float *dmix_gain, float *dmix_w, void *ws, size_t ws_bytes, void *stream) {
+                                 float *dmix_gain, float *dmix_w, void *ws, size_t ws_bytes, void *stream,
+                                 int64_t conv_src_stride = 0) {
     attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
     if (st != ATTNRES_OK) return st;
     if (!(mix_eps >= 0.f) || std::isinf(mix_eps)) return ATTNRES_ERR_INVALID_ARG;
@@ -1043,6 +1044,11 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     if (T > 0 && (!dh || !dsrc || !ws)) return ATTNRES_ERR_INVALID_ARG;
     if (dsrc_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
     const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
+    // per-source kernels: each source's set must not overlap the next one's
+    if (conv_src_stride < 0 || (conv_src_stride > 0 && n_src > 1 && conv_src_stride < d * ktot))
+        return ATTNRES_ERR_INVALID_ARG;
+    const int64_t n_sets = conv_src_stride > 0 ? n_src : 1;              // kernel sets (and gradients)
+    const size_t cw_bytes = ((size_t)(n_sets - 1) * (size_t)conv_src_stride + (size_t)ktot * (size_t)d) * 4;
     const size_t es = esize(dt);
     const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
     const size_t dsrc_bytes = ((size_t)(n_src - 1) * (size_t)dsrc_stride + (size_t)T * (size_t)d) * es;
@@ -1054,7 +1060,7 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
         return ATTNRES_ERR_INVALID_ARG;
     // the parameter gradients: disjoint from one another and from the workspace
     const void *pg[5] = {dconv_w, dqueries, dgain, dmix_gain, dmix_w};
-    const size_t pn[5] = {(size_t)ktot * (size_t)d * 4, md * 4, (size_t)d * 4, md * 4, md * 16};
+    const size_t pn[5] = {cw_bytes, md * 4, (size_t)d * 4, md * 4, md * 16};
     for (int x = 0; x < 5; ++x) {
         if (!pg[x]) continue;
         if (T > 0 && overlap(pg[x], pn[x], ws, ws_bytes)) return ATTNRES_ERR_INVALID_ARG;
@@ -1062,6 +1068,7 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
             if (pg[y] && overlap(pg[x], pn[x], pg[y], pn[y])) return ATTNRES_ERR_INVALID_ARG;
     }
     if ((d != 1024 && d != 2048 && d != 4096) || n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    if (conv_src_stride > 0 && n_src > 1 && conv_src_stride % 4 != 0) return ATTNRES_ERR_UNSUPPORTED;
     if (!aligned16(conv_w) || !aligned16(queries) || !aligned16(mix_w) || (gain && !aligned16(gain)) ||
         (mix_gain && !aligned16(mix_gain)) || !aligned16(dmix_w) || !aligned4(dconv_w) || !aligned4(dqueries) ||
         (dgain && !aligned4(dgain)) || (dmix_gain && !aligned4(dmix_gain)))
@@ -1078,8 +1085,10 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     if (T == 0) {
         // no tokens: every parameter gradient is zero
         cudaError_t e = cudaSuccess;
-        for (int x = 0; x < 5 && e == cudaSuccess; ++x)
+        for (int x = 1; x < 5 && e == cudaSuccess; ++x)
             if (pg[x]) e = cudaMemsetAsync(const_cast<void *>(pg[x]), 0, pn[x], s);
+        for (int64_t k = 0; k < n_sets && e == cudaSuccess; ++k)
+            e = cudaMemsetAsync(dconv_w + k * conv_src_stride, 0, (size_t)ktot * (size_t)d * 4, s);
         return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
     }
     if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
@@ -1093,6 +1102,7 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
     a.ktot = (int)ktot;
     a.conv_w = conv_w;
+    a.conv_src_stride = conv_src_stride;
     a.tc = p.tc;
     a.tc_s = p.tc_s;
     a.tc_m = p.tc_m;
@@ -1140,7 +1150,15 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
         if (st != ATTNRES_OK) return st;
     }
     e = msar_bwd_conv(dti, a, stream);
-    if (e == cudaSuccess) e = msar_bwd_conv_sum(a, p.chunks * n_src, dconv_w, stream);
+    if (conv_src_stride == 0) {
+        // one kernel set: every (chunk, source) partial adds into it
+        if (e == cudaSuccess) e = msar_bwd_conv_sum(a, a.conv_parts, p.chunks * n_src, ktot * d, dconv_w, stream);
+    } else {
+        // source i's gradient: its partials of every chunk
+        for (int64_t i = 0; i < n_src && e == cudaSuccess; ++i)
+            e = msar_bwd_conv_sum(a, a.conv_parts + i * ktot * d, p.chunks, n_src * ktot * d,
+                                  dconv_w + i * conv_src_stride, stream);
+    }
     if (e == cudaSuccess && dgain) e = msar_bwd_sum(dg, 4, d, dgain, 0, stream);
     if (e != cudaSuccess) return cuda_fail(e, "msar backward conv launch");
     return ATTNRES_OK;
@@ -1361,6 +1379,19 @@ attnres_status_t msar_expand_bwd_workspace_size(int64_t n_src, int64_t T, int64_
     if (st != ATTNRES_OK) return st;
     *bytes = p.total;
     return ATTNRES_OK;
+}
+
+attnres_status_t msar_expand_bwd_ps(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                    attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                    int64_t conv_src_stride, const float *queries, const float *gain, float eps,
+                                    const float *mix_gain, const float *mix_w, float mix_eps, const void *dh,
+                                    void *dsrc, int64_t dsrc_stride, float *dconv_w, float *dqueries, float *dgain,
+                                    float *dmix_gain, float *dmix_w, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (conv_src_stride <= 0) return ATTNRES_ERR_INVALID_ARG;
+    return launch_msar_bwd(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, gain, eps, mix_gain,
+                           mix_w, mix_eps, dh, dsrc, dsrc_stride, dconv_w, dqueries, dgain, dmix_gain, dmix_w,
+                           workspace, workspace_bytes, stream, conv_src_stride);
 }
 
 attnres_status_t msar_expand_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,

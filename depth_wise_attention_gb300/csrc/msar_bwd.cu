@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(ST_THREADS) msar_streams_kernel(const MsarBwdA
     const int nb = (int)((nrows + ST_RB - 1) / ST_RB);
     const unsigned char *v = a.src + (int64_t)i * a.src_stride_bytes;
     const uint32_t sbase = smem_u32(smem);
+    const float *cw = a.conv_w + (int64_t)i * a.conv_src_stride;      // this source's kernels
 
     float2 w[CS::KT];
     {
@@ -110,8 +111,8 @@ __global__ void __launch_bounds__(ST_THREADS) msar_streams_kernel(const MsarBwdA
 #pragma unroll
             for (int j = 0; j < CS::k(r); ++j)
                 w[CS::off(r) + j] = (CS::FIXED || j < a.k[r])
-                                        ? make_float2(__ldg(a.conv_w + off + (int64_t)c * a.k[r] + j),
-                                                      __ldg(a.conv_w + off + (int64_t)(c + 1) * a.k[r] + j))
+                                        ? make_float2(__ldg(cw + off + (int64_t)c * a.k[r] + j),
+                                                      __ldg(cw + off + (int64_t)(c + 1) * a.k[r] + j))
                                         : make_float2(0.f, 0.f);
             off += (int64_t)a.d * a.k[r];
         }
@@ -469,14 +470,15 @@ __global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kern
 
     if (tid < CB_HALF) {
         // ---- dv: the kernels and the window of pending outputs
+        const float *cw = a.conv_w + (int64_t)i * a.conv_src_stride;  // this source's kernels
         float2 w[CS::KT], pend[CS::KM];
         int64_t off = 0;
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
 #pragma unroll
             for (int j = 0; j < CS::k(r); ++j)
-                w[CS::off(r) + j] = has(r, j) ? make_float2(__ldg(a.conv_w + off + (int64_t)c * a.k[r] + j),
-                                                            __ldg(a.conv_w + off + (int64_t)(c + 1) * a.k[r] + j))
+                w[CS::off(r) + j] = has(r, j) ? make_float2(__ldg(cw + off + (int64_t)c * a.k[r] + j),
+                                                            __ldg(cw + off + (int64_t)(c + 1) * a.k[r] + j))
                                               : make_float2(0.f, 0.f);
             off += (int64_t)a.d * a.k[r];
         }
@@ -553,16 +555,16 @@ __global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kern
     cp_async_wait<0>();
 }
 
-// dconv_w from the conv partials: element e = (koff_r + j) * d + c of every
-// partial, summed over the partials in order, lands at koff_r * d + c * k_r + j
-// (conv_w's packing).
-__global__ void __launch_bounds__(256) msar_conv_sum_kernel(const float *parts, int64_t nparts, int d, int k0, int k1,
-                                                            int k2, float *out) {
+// dconv_w from the conv partials (pstride floats apart): element
+// e = (koff_r + j) * d + c of every partial, summed over the partials in
+// order, lands at koff_r * d + c * k_r + j (conv_w's packing).
+__global__ void __launch_bounds__(256) msar_conv_sum_kernel(const float *parts, int64_t nparts, int64_t pstride, int d,
+                                                            int k0, int k1, int k2, float *out) {
     const int ktot = k0 + k1 + k2;
     const int64_t n = (int64_t)ktot * d;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
         float s = 0.f;
-        for (int64_t p = 0; p < nparts; ++p) s += parts[p * n + e];
+        for (int64_t p = 0; p < nparts; ++p) s += parts[p * pstride + e];
         const int jg = (int)(e / d), c = (int)(e - (int64_t)jg * d);
         const int kr = jg < k0 ? k0 : jg < k0 + k1 ? k1 : k2;
         const int koff = jg < k0 ? 0 : jg < k0 + k1 ? k0 : k0 + k1;
@@ -647,11 +649,12 @@ cudaError_t msar_bwd_conv(int dt, const MsarBwdArgs &a, void *stream) {
     return k4812(a) ? launch_conv_bwd_k<float, 4, 8, 12>(a, s) : launch_conv_bwd_k<float, 0, 0, 0>(a, s);
 }
 
-cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, int64_t nparts, float *dconv_w, void *stream) {
+cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, const float *parts, int64_t nparts, int64_t part_stride,
+                              float *dconv_w, void *stream) {
     const int64_t n = (int64_t)a.ktot * a.d;
     const int64_t blocks = (n + 255) / 256;
     msar_conv_sum_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        a.conv_parts, nparts, a.d, a.k[0], a.k[1], a.k[2], dconv_w);
+        parts, nparts, part_stride, a.d, a.k[0], a.k[1], a.k[2], dconv_w);
     return cudaGetLastError();
 }
 

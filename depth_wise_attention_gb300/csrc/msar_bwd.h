@@ -16,7 +16,8 @@ struct MsarBwdArgs {
     int d;
     int k[3];                       // kernel sizes of streams 1..3
     int ktot;                       // k[0] + k[1] + k[2]
-    const float *conv_w;            // packed [d][k_1] [d][k_2] [d][k_3]
+    const float *conv_w;            // packed [d][k_1] [d][k_2] [d][k_3] (per source: conv_src_stride apart)
+    int64_t conv_src_stride;        // floats between sources' kernels; 0 = one set shared by all
     int64_t tc;                     // tokens per chunk of the conv backward and of A's partials
     int64_t tc_s;                   // tokens per chunk of the streams kernel
     int64_t tc_m;                   // tokens per CTA of the mixer kernels
@@ -46,8 +47,10 @@ cudaError_t msar_bwd_mix(int dt, const MsarBwdArgs &a, void *stream);
 // dmix_w and dmix_gain from A
 cudaError_t msar_bwd_mix_finish(const MsarBwdArgs &a, const float *A, void *stream);
 cudaError_t msar_bwd_conv(int dt, const MsarBwdArgs &a, void *stream);
-// dconv_w (packed like conv_w) = the nparts conv partials summed in order
-cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, int64_t nparts, float *dconv_w, void *stream);
+// dconv_w (packed like conv_w) = the nparts conv partials at parts,
+// parts + part_stride, ... (floats) summed in order
+cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, const float *parts, int64_t nparts, int64_t part_stride,
+                              float *dconv_w, void *stream);
 // out[e] = (accumulate ? out[e] : 0) + sum_p parts[p][e] in order of p
 cudaError_t msar_bwd_sum(const float *parts, int64_t nparts, int64_t n, float *out, int accumulate, void *stream);
 

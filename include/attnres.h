@@ -518,7 +518,32 @@ attnres_status_t msar_expand_bwd(const void *src, int64_t n_src, int64_t src_str
                                  float *dqueries, float *dgain, float *dmix_gain, float *dmix_w,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
-/* Workspace bytes msar_expand_bwd needs for these sizes on the current device. */
+/*
+ * msar_expand_bwd for msar_expand_fwd_ps (each source's own conv kernels):
+ * source i's kernels are read at conv_w + i * conv_src_stride and its kernel
+ * gradient is written at dconv_w + i * conv_src_stride (packed as its
+ * kernels; the floats between one source's set and the next are not
+ * written).  Defined by the same chain rule as msar_expand_bwd, with source
+ * i's streams taken through its own kernels (MSAR page, section 무엇과 다른가,
+ * the streams v_i^(r) of each source).
+ *   conv_src_stride  > 0 floats; at least d * (k_1 + k_2 + k_3) with more than
+ *                    one source (else ATTNRES_ERR_INVALID_ARG), and then a
+ *                    multiple of 4 (else ATTNRES_ERR_UNSUPPORTED)
+ *   dconv_w          float, n_src sets conv_src_stride apart; overwritten
+ * Every other argument, the workspace (msar_expand_bwd_workspace_size) and the
+ * limits are msar_expand_bwd's.
+ */
+attnres_status_t msar_expand_bwd_ps(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                    int64_t d, attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                    const float *conv_w, int64_t conv_src_stride, const float *queries,
+                                    const float *gain, float eps, const float *mix_gain,
+                                    const float *mix_w, float mix_eps, const void *dh, void *dsrc,
+                                    int64_t dsrc_stride, float *dconv_w, float *dqueries, float *dgain,
+                                    float *dmix_gain, float *dmix_w, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/* Workspace bytes msar_expand_bwd (and msar_expand_bwd_ps) needs for these
+ * sizes on the current device. */
 attnres_status_t msar_expand_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d,
                                                attnres_dtype_t dt, int64_t m,
                                                const int32_t *ksizes, size_t *bytes);

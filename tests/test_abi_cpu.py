@@ -319,3 +319,20 @@ def test_msar_backward_validation(lib):
     assert lib.msar_expand_bwd_workspace_size(8, T, d, BF16, 4, kp(ks), None) == INV
     assert lib.msar_expand_bwd_workspace_size(8, T, d, BF16, 4, kp(bad), ctypes.byref(n)) == INV
     assert lib.msar_expand_bwd_workspace_size(8, T, d, BF16, 3, kp(ks), ctypes.byref(n)) == UNS
+
+
+def test_msar_backward_per_source_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    T, d = 16, 1024
+    DH, DS, DCW, DQ, DG, DMG, DMW, WS = (B + 0x1000000, B + 0x2000000, B + 0x3000000, B + 0x3400000,
+                                         B + 0x3500000, B + 0x3600000, B + 0x3700000, B + 0x4000000)
+
+    def mp(stride, n_src=8, dcw=DCW):
+        return lib.msar_expand_bwd_ps(A, n_src, T * d, T, d, BF16, 4, ctypes.cast(ks, ctypes.c_void_p), B, stride,
+                                      B + 0x200000, None, 1e-6, None, B + 0x300000, 1e-6, DH, DS, T * d, dcw, DQ, DG,
+                                      DMG, DMW, WS, 1 << 30, None)
+    assert mp(0) == INV                           # the per-source entry needs a stride
+    assert mp(-4) == INV
+    assert mp(d * 24 - 4) == INV                  # sources' kernels would overlap
+    assert mp(d * 24, dcw=DQ - 64) == INV         # 8 kernel gradients run into dqueries
+    assert mp(d * 24 + 2) == UNS                  # kernels not 16-byte aligned

@@ -382,3 +382,37 @@ def test_msar_bwd_T32768_d4096():
     b = attnres.msar_expand_bwd(src, ks, cw, q, dense, None, 1e-6, None, mw, 1e-6)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_msar_bwd_per_source_T32768_d4096():
+    """The backward with each source's own kernels at the MSAR size, by the
+    same construction as the shared-kernel test: dh on a few clusters of 4
+    tokens, every gradient (each source's kernel gradient on its own) against
+    the oracle's per-source backward over the clusters' causal windows."""
+    T, d, N = 32768, 4096, 8
+    ks = (4, 8, 12)
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((4, d), (16.0 / d) ** 0.5, g)
+    cw = torch.stack([torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g) for k in ks]) for _ in range(N)])
+    mw = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g)
+    starts = [0, 9000, T - 4]
+    dh = torch.zeros((T, d), dtype=BF16, device="cuda")
+    for c in starts:
+        dh[c:c + 4] = torch.randn((4, d), generator=g, device="cuda").to(BF16)
+    got = attnres.msar_expand_bwd_ps(src, ks, cw, q, dh, None, 1e-6, None, mw, 1e-6)
+    attnres.attnres_sync_status()
+    cw_h, q_h, mw_h = (t.cpu().numpy().astype(np.float64) for t in (cw, q, mw))
+    ref_par = None
+    inside = torch.zeros(T, dtype=torch.bool, device="cuda")
+    for c in starts:
+        lo = max(0, c - 11)
+        win = src[:, lo:c + 4, :].float().cpu().numpy().astype(np.float64)
+        dwin = dh[lo:c + 4].float().cpu().numpy().astype(np.float64)
+        r = oracle.msar_ps_bwd(win, ks, cw_h, q_h, dwin, None, 1e-6, None, mw_h, 1e-6)
+        check_out(got[0][:, lo:c + 4], r[0], BF16, strict=False, what=f"dsrc rows {lo}..{c + 3}")
+        inside[lo:c + 4] = True
+        ref_par = list(r[1:]) if ref_par is None else [a + b for a, b in zip(ref_par, r[1:])]
+    assert torch.count_nonzero(got[0][:, ~inside]) == 0
+    for name, g_, r_ in zip(("dconv_w", "dqueries", "dgain", "dmix_gain", "dmix_w"), got[1:], ref_par):
+        check_out(g_, np.asarray(r_).reshape(tuple(g_.shape)), BF16, strict=False, what=name)

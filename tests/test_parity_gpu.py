@@ -821,6 +821,45 @@ def test_msar_bwd_empty_sequence_zeroes_parameter_gradients():
         assert torch.count_nonzero(t) == 0
 
 
+@pytest.mark.parametrize("dtype,n_src,T,d,ks", [(BF16, 8, 70, 4096, (4, 8, 12)), (F32, 3, 200, 1024, (4, 8, 12)),
+                                                 (BF16, 5, 45, 2048, (16, 5, 9)), (F32, 1, 33, 1024, (1, 2, 3))])
+def test_msar_bwd_per_source_kernels(dtype, n_src, T, d, ks):
+    """Backward with each source's own conv kernels (at a padded stride)
+    against the oracle's per-source backward; the padding of the kernel
+    gradients stays zero."""
+    rng = _rng(n_src * 5 + T + d)
+    src, q, _, mw, g, mg, dh = _msar_bwd_case(rng, n_src, T, d, dtype, ks, True)
+    kt = d * sum(ks)
+    cw = np.stack([np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel()
+                                   for k in ks]) for _ in range(n_src)])
+    cw_pad = np.zeros((n_src, kt + 64), np.float32)
+    cw_pad[:, :kt] = cw
+    got = attnres.msar_expand_bwd_ps(to_dev(src, dtype), ks, to_dev(cw_pad, F32), to_dev(q, F32), to_dev(dh, dtype),
+                                     to_dev(g, F32), 1e-6, to_dev(mg, F32), to_dev(mw, F32), 1e-6)
+    assert torch.count_nonzero(got[1][:, kt:]) == 0
+    got = (got[0], got[1][:, :kt]) + tuple(got[2:])
+    ref = oracle.msar_ps_bwd(src, ks, cw, q, dh, g, 1e-6, mg, mw, 1e-6)
+    _check_msar_grads(got, ref, dtype, f"per-source n_src={n_src} d={d}")
+
+
+def test_msar_bwd_per_source_equal_kernels_match_the_shared_backward():
+    """Equal per-source kernels: the sources', queries', gain's and mixer's
+    gradients equal the shared-kernel backward's bit for bit, and the
+    sources' kernel gradients add up to the shared one's."""
+    rng = _rng(97)
+    ks, T, d, n_src = (4, 8, 12), 120, 2048, 8
+    src, q, cw, mw, g, mg, dh = _msar_bwd_case(rng, n_src, T, d, BF16, ks, True)
+    dev = lambda x: to_dev(x, F32)
+    shared = attnres.msar_expand_bwd(to_dev(src, BF16), ks, dev(cw), dev(q), to_dev(dh, BF16), dev(g), 1e-6, dev(mg),
+                                     dev(mw), 1e-6)
+    per = attnres.msar_expand_bwd_ps(to_dev(src, BF16), ks, dev(np.stack([cw] * n_src)), dev(q), to_dev(dh, BF16),
+                                     dev(g), 1e-6, dev(mg), dev(mw), 1e-6)
+    for k in (0, 2, 3, 4, 5):
+        assert torch.equal(shared[k], per[k]), _MSAR_GRADS[k]
+    total = to_host(per[1]).sum(axis=0)
+    check_out(shared[1], total, F32, np.abs(total).max(), strict=False, what="summed kernel gradients")
+
+
 # --------------------------------------------------------------- hygiene
 
 def test_outputs_stay_inside_their_buffers():
