@@ -10,8 +10,9 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|mhar_block|msar|
-msar_block|msar_chunked|msar_ps|msar_bwd|msar_bwd_ps|full_depth|block_d2048|block_fused|block_bwd|
-read_bwd|mhar_bwd|decode) are for profiling and the design notes.
+msar_block|msar_chunked|msar_ps|msar_ws|msar_block_ws|msar_bwd|msar_bwd_ps|
+full_depth|block_d2048|block_fused|block_bwd|read_bwd|mhar_bwd|decode) are
+for profiling and the design notes.
 """
 from __future__ import annotations
 
@@ -998,6 +999,36 @@ class MsarBwdPerSourceWorkload(MsarBwdWorkload):
         return len(wins)
 
 
+class MsarWsWorkload(MsarWorkload):
+    """The MSAR read through the workspace chain (msar_expand_fwd_ws): the
+    conv streams written once, one read per stream, the sliced mixer; same
+    inputs and outputs as the fused read."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0):
+        super().__init__(T, d, N, seed)
+        self.name = "msar_read_workspace_chain"
+        self.launches_per_step = 1 + 4 + 2
+        self.dominant = "msar read, workspace chain (streams + 4 reads + mixer)"
+        self.dominant_src = "msar_bwd"
+        self.profile_tag = f"ncu_msar_ws_d{d}"
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres
+        super().setup(device)
+        nb = attnres.msar_expand_fwd_ws_workspace_size(self.N, self.T, self.d, torch.bfloat16)
+        self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.msar_expand_fwd_ws(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, None, self.mix_w,
+                                   1e-6, out=self.out, workspace=self.ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+
 class MsarBlockWorkload(MsarWorkload):
     """MSAR inside the two-phase Block schedule: one block of S=4 layers over
     N=8 cached sources, bf16, d=4096.  One step = phase 1 (every source
@@ -1234,6 +1265,41 @@ class FullDepthWorkload(BlockWorkload):
         return src.shape[1]
 
 
+class MsarBlockWsWorkload(MsarBlockWorkload):
+    """The MSAR two-phase block with phase 1 through the workspace chain
+    (msar_block_phase1_ws: the cached sources' streams written once, each
+    stream read by its 4 layers' queries with the tensor-core read), phase 2
+    as msar_block_phase2.  Same inputs and outputs as the fused schedule."""
+
+    def __init__(self, T=32768, d=4096, N=8, S=4, seed=0):
+        super().__init__(T, d, N, S, seed)
+        self.name = "msar_two_phase_block_workspace_chain"
+        self.launches_per_step = 1 + 4 + S
+        self.dominant = "msar phase 1, workspace chain (streams + 4 reads of 4 queries)"
+        self.dominant_src = "msar_bwd"
+        self.profile_tag = f"ncu_msar_phase1_ws_d{d}"
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres
+        super().setup(device)
+        nb = attnres.msar_block_phase1_ws_workspace_size(self.N, self.T, self.d, torch.bfloat16, self.S)
+        self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        attnres.msar_block_phase1_ws(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, o=self.o,
+                                     lse=self.lse, workspace=self.ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for s_ in range(self.S):
+            attnres.msar_block_phase2(self.o[s_], self.lse[s_], self.parts[s_] if s_ > 0 else None, self.ks,
+                                      self.conv_w, self.queries[s_], None, 1e-6, None, self.mix_w, 1e-6,
+                                      out=self.outs[s_], stream=stream)
+
+
 def make_workload(name, T=None):
     if name == "block":
         return BlockWorkload(T=T or 32768)
@@ -1259,6 +1325,10 @@ def make_workload(name, T=None):
         return MharBwdWorkload(T=T or 131072)
     if name == "msar_block":
         return MsarBlockWorkload(T=T or 32768)
+    if name == "msar_ws":
+        return MsarWsWorkload(T=T or 32768)
+    if name == "msar_block_ws":
+        return MsarBlockWsWorkload(T=T or 32768)
     if name == "msar_bwd":
         return MsarBwdWorkload(T=T or 32768)
     if name == "msar_bwd_ps":
@@ -1513,7 +1583,7 @@ def main():
     ap.add_argument("--workload", default="block",
                     choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
                              "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block",
-                             "msar_bwd", "msar_bwd_ps", "full_depth"])
+                             "msar_bwd", "msar_bwd_ps", "msar_ws", "msar_block_ws", "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

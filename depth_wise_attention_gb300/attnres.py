@@ -62,6 +62,12 @@ _SIGS = {
     "msar_expand_bwd_workspace_size": [_i64, _i64, _i64, ctypes.c_int, _i64, _vp, ctypes.POINTER(ctypes.c_size_t)],
     "msar_expand_bwd_ps": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _i64, _vp, _vp, _f, _vp, _vp,
                            _f, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "msar_expand_fwd_ws": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _i64, _vp, _vp, _f, _vp, _vp,
+                           _f, _vp, _vp, ctypes.c_size_t, _vp],
+    "msar_expand_fwd_ws_workspace_size": [_i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+    "msar_block_phase1_ws": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _i64, _vp, _f, _vp,
+                             _vp, _vp, ctypes.c_size_t, _vp],
+    "msar_block_phase1_ws_workspace_size": [_i64, _i64, _i64, ctypes.c_int, _i64, ctypes.POINTER(ctypes.c_size_t)],
     "attnres_status_string": [ctypes.c_int],
     "attnres_last_cuda_error": [],
     "attnres_sync_status": [_vp],
@@ -563,3 +569,63 @@ def msar_expand_bwd_ps(src, ksizes, conv_w, queries, dh, gain=None, eps=1e-6, mi
         _p(dgain), _p(dmix_gain), _p(dmix_w), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
     return dsrc, dconv_w, dqueries, dgain, dmix_gain, dmix_w
+
+
+def msar_expand_fwd_ws_workspace_size(n_src, T, d, dtype):
+    import torch
+    n = ctypes.c_size_t(0)
+    dt = BF16 if dtype == torch.bfloat16 else F32
+    _check("msar_expand_fwd_ws_workspace_size",
+           load().msar_expand_fwd_ws_workspace_size(n_src, T, d, dt, ctypes.byref(n)))
+    return n.value
+
+
+def msar_expand_fwd_ws(src, ksizes, conv_w, queries, gain=None, eps=1e-6, mix_gain=None, mix_w=None, mix_eps=1e-6,
+                       out=None, workspace=None, stream=None):
+    """MSAR read through the workspace chain.  conv_w: packed 1-D (shared
+    kernels) or [n_src, stride] (each source's own) -> out [T, d]."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    m = queries.shape[0]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if out is None:
+        out = torch.empty((T, d), dtype=src.dtype, device=src.device)
+    if workspace is None:
+        nbytes = msar_expand_fwd_ws_workspace_size(n_src, T, d, src.dtype)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=src.device)
+    cstride = conv_w.stride(0) if conv_w.dim() == 2 else 0
+    _check("msar_expand_fwd_ws", load().msar_expand_fwd_ws(
+        _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), cstride, _p(queries),
+        _p(gain), eps, _p(mix_gain), _p(mix_w), mix_eps, _p(out), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def msar_block_phase1_ws_workspace_size(n_src, T, d, dtype, S):
+    import torch
+    n = ctypes.c_size_t(0)
+    dt = BF16 if dtype == torch.bfloat16 else F32
+    _check("msar_block_phase1_ws_workspace_size",
+           load().msar_block_phase1_ws_workspace_size(n_src, T, d, dt, S, ctypes.byref(n)))
+    return n.value
+
+
+def msar_block_phase1_ws(src, ksizes, conv_w, queries, gain=None, eps=1e-6, o=None, lse=None, workspace=None,
+                         stream=None):
+    """MSAR phase 1 through the workspace chain: queries [S, m, d] ->
+    (o [S, m, T, d], lse [S, m, T])."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    S, m = queries.shape[0], queries.shape[1]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if o is None:
+        o = torch.empty((S, m, T, d), dtype=src.dtype, device=src.device)
+    if lse is None:
+        lse = torch.empty((S, m, T), dtype=torch.float32, device=src.device)
+    if workspace is None:
+        nbytes = msar_block_phase1_ws_workspace_size(n_src, T, d, src.dtype, S)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=src.device)
+    _check("msar_block_phase1_ws", load().msar_block_phase1_ws(
+        _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries), S, _p(gain), eps,
+        _p(o), _p(lse), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return o, lse

@@ -169,17 +169,20 @@ bool decode_shape(int nvec, int *cs, int *vpc) {
 }
 
 // Shared launch path of Full / phase 1 / MHAR.
+// out_q_stride: elements between the queries' outputs (0: T * d, packed)
 attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
                                    int64_t d, int64_t H, attnres_dtype_t dt, const float *queries,
                                    int64_t n_q, const float *gain, float eps, void *out, float *lse,
-                                   void *stream) {
+                                   void *stream, int64_t out_q_stride = 0) {
     attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
     if (st != ATTNRES_OK) return st;
     if (n_q < 1 || H < 1 || d % H != 0) return ATTNRES_ERR_INVALID_ARG;
     if (T > 0 && (!queries || !out)) return ATTNRES_ERR_INVALID_ARG;
+    const int64_t oqs = out_q_stride > 0 ? out_q_stride : T * d;
+    if (n_q > 1 && oqs < T * d) return ATTNRES_ERR_INVALID_ARG;
     const size_t es = esize(dt);
     const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
-    const size_t out_bytes = (size_t)n_q * (size_t)T * (size_t)d * es;
+    const size_t out_bytes = ((size_t)(n_q - 1) * (size_t)oqs + (size_t)T * (size_t)d) * es;
     if (overlap(out, out_bytes, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
     if (lse && overlap(lse, (size_t)n_q * H * T * 4, src, src_bytes)) return ATTNRES_ERR_INVALID_ARG;
     if (lse && overlap(lse, (size_t)n_q * H * T * 4, out, out_bytes)) return ATTNRES_ERR_INVALID_ARG;
@@ -207,7 +210,7 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
             a.gain = gain;
             a.eps = eps;
             a.out = static_cast<unsigned char *>(out);
-            a.out_q_stride_bytes = T * d * (int64_t)es;
+            a.out_q_stride_bytes = oqs * (int64_t)es;
             a.lse = lse;
             a.cs = cs;
             a.vpc = vpc;
@@ -286,7 +289,7 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
                 m.gain = gain;
                 m.eps = eps;
                 m.out = static_cast<unsigned char *>(out);
-                m.out_q_stride_bytes = T * d * 2;
+                m.out_q_stride_bytes = oqs * 2;
                 m.lse = lse;
                 m.nstages = nstages;
                 m.pitch = pitch;
@@ -384,7 +387,7 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     a.gain = gain;
     a.eps = eps;
     a.out = static_cast<unsigned char *>(out);
-    a.out_q_stride_bytes = T * d * (int64_t)es;
+    a.out_q_stride_bytes = oqs * (int64_t)es;
     a.lse = lse;
     a.tpr = tpr;
     a.tt = tt;
@@ -1164,6 +1167,166 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     return ATTNRES_OK;
 }
 
+// MSAR forward with a workspace: the conv streams are written once, each
+// stream is read by the forward read kernels, and (one-shot read) the mixer
+// runs over the per-stream reads.  Workspace regions start on 256-byte
+// boundaries.
+struct MsarFwdWsPlan {
+    int64_t tc_s;
+    size_t off_u, off_z, off_part, off_q, off_l, total;
+};
+
+MsarFwdWsPlan msar_fwd_ws_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt, bool oneshot, int64_t S) {
+    MsarFwdWsPlan p{};
+    p.tc_s = (T + 127) / 128;
+    if (p.tc_s < 32) p.tc_s = 32;
+    const size_t row = (size_t)T * (size_t)d * esize(dt);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    p.off_u = take(3 * (size_t)n_src * row);
+    if (oneshot) {
+        p.off_z = take(4 * row);
+        p.off_part = take((size_t)T * (size_t)(d / 1024) * 9 * 4);
+    } else {
+        p.off_q = take((size_t)4 * (size_t)S * (size_t)d * 4);
+        p.off_l = take((size_t)(S < 8 ? S : 8) * (size_t)T * 4);
+    }
+    p.total = off;
+    return p;
+}
+
+// the streams of every source into u (shared kernels, or source i's at i * conv_src_stride)
+attnres_status_t msar_write_streams(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                    attnres_dtype_t dt, const int32_t *ksizes, const float *conv_w,
+                                    int64_t conv_src_stride, int64_t tc_s, unsigned char *u, void *stream) {
+    MsarBwdArgs a{};
+    a.src = static_cast<const unsigned char *>(src);
+    a.src_stride_bytes = src_stride * (int64_t)esize(dt);
+    a.n_src = (int)n_src;
+    a.T = T;
+    a.d = (int)d;
+    for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
+    a.ktot = ksizes[0] + ksizes[1] + ksizes[2];
+    a.conv_w = conv_w;
+    a.conv_src_stride = conv_src_stride;
+    a.tc_s = tc_s;
+    a.u = u;
+    cudaError_t e = msar_bwd_streams(dt == ATTNRES_BF16 ? 1 : 0, a, stream);
+    return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "msar streams launch");
+}
+
+attnres_status_t launch_msar_read_ws(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                     attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                     int64_t conv_src_stride, const float *queries, const float *gain, float eps,
+                                     const float *mix_gain, const float *mix_w, float mix_eps, void *out, void *ws,
+                                     size_t ws_bytes, void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (!(mix_eps >= 0.f) || std::isinf(mix_eps)) return ATTNRES_ERR_INVALID_ARG;
+    st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
+    if (conv_src_stride < 0 || (conv_src_stride > 0 && n_src > 1 && conv_src_stride < d * ktot))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (T == 0) return ATTNRES_OK;
+    if (!conv_w || !queries || !mix_w || !out || !ws) return ATTNRES_ERR_INVALID_ARG;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t out_bytes = (size_t)T * (size_t)d * es;
+    if (overlap(out, out_bytes, src, src_bytes) || overlap(ws, ws_bytes, src, src_bytes) ||
+        overlap(ws, ws_bytes, out, out_bytes))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (d % 1024 != 0 || d > 16384) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(queries) || !aligned4(conv_w) || !aligned16(mix_w) ||
+        (gain && !aligned16(gain)) || (mix_gain && !aligned4(mix_gain)) || !aligned16(ws))
+        return ATTNRES_ERR_UNSUPPORTED;
+    const MsarFwdWsPlan p = msar_fwd_ws_plan(n_src, T, d, dt, true, 0);
+    if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    st = msar_write_streams(src, n_src, src_stride, T, d, dt, ksizes, conv_w, conv_src_stride, p.tc_s, w + p.off_u,
+                            stream);
+    if (st != ATTNRES_OK) return st;
+    const size_t row = (size_t)T * (size_t)d * es;
+    for (int64_t r = 0; r < 4; ++r) {
+        const void *sr = r == 0 ? src : static_cast<const void *>(w + p.off_u + (size_t)(r - 1) * (size_t)n_src * row);
+        st = launch_depth_read(sr, n_src, r == 0 ? src_stride : T * d, T, d, 1, dt, queries + r * d, 1, gain, eps,
+                               w + p.off_z + (size_t)r * row, nullptr, stream);
+        if (st != ATTNRES_OK) return st;
+    }
+    MsarBwdArgs a{};
+    a.T = T;
+    a.d = (int)d;
+    a.z = w + p.off_z;
+    a.dh = nullptr;
+    a.mix_gain = mix_gain;
+    a.mix_w = mix_w;
+    a.mix_eps = mix_eps;
+    a.mix_part = reinterpret_cast<float *>(w + p.off_part);
+    a.nsl = (int)(d / 1024);
+    a.tc_m = 128;
+    cudaError_t e = msar_fwd_mix(dt == ATTNRES_BF16 ? 1 : 0, a, out, stream);
+    return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "msar mixer launch");
+}
+
+attnres_status_t launch_msar_phase1_ws(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                       attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                       const float *queries, int64_t S, const float *gain, float eps, void *o,
+                                       float *lse, void *ws, size_t ws_bytes, void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (S < 1) return ATTNRES_ERR_INVALID_ARG;
+    if (T == 0) return ATTNRES_OK;
+    if (!conv_w || !queries || !o || !lse || !ws) return ATTNRES_ERR_INVALID_ARG;
+    st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t o_bytes = (size_t)S * 4 * (size_t)T * (size_t)d * es;
+    const size_t lse_bytes = (size_t)S * 4 * (size_t)T * sizeof(float);
+    if (overlap(o, o_bytes, src, src_bytes) || overlap(lse, lse_bytes, src, src_bytes) ||
+        overlap(lse, lse_bytes, o, o_bytes) || overlap(ws, ws_bytes, src, src_bytes) ||
+        overlap(ws, ws_bytes, o, o_bytes) || overlap(ws, ws_bytes, lse, lse_bytes))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (d % 512 != 0 || d > 16384) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(o) || !aligned4(lse) || !aligned16(queries) || !aligned4(conv_w) || (gain && !aligned16(gain)) ||
+        !aligned16(ws))
+        return ATTNRES_ERR_UNSUPPORTED;
+    const MsarFwdWsPlan p = msar_fwd_ws_plan(n_src, T, d, dt, false, S);
+    if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = msar_write_streams(src, n_src, src_stride, T, d, dt, ksizes, conv_w, 0, p.tc_s, w + p.off_u, stream);
+    if (st != ATTNRES_OK) return st;
+    // stream r's queries of every layer, contiguous: qbuf[r][s] = queries[s][r]
+    float *qbuf = reinterpret_cast<float *>(w + p.off_q);
+    cudaError_t e = cudaMemcpy2DAsync(qbuf, (size_t)d * 4, queries, (size_t)4 * d * 4, (size_t)d * 4, (size_t)S, cudaMemcpyDeviceToDevice, s);
+    for (int64_t r = 1; r < 4 && e == cudaSuccess; ++r)
+        e = cudaMemcpy2DAsync(qbuf + r * S * d, (size_t)d * 4, queries + r * d, (size_t)4 * d * 4, (size_t)d * 4,
+                              (size_t)S, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync");
+    float *lbuf = reinterpret_cast<float *>(w + p.off_l);
+    const size_t row = (size_t)T * (size_t)d * es;
+    for (int64_t r = 0; r < 4; ++r) {
+        const void *sr = r == 0 ? src : static_cast<const void *>(w + p.off_u + (size_t)(r - 1) * (size_t)n_src * row);
+        // layers in groups of up to 8 queries; o[s][r] is 4 T d elements after o[s-1][r]
+        for (int64_t s0 = 0; s0 < S; s0 += 8) {
+            const int64_t ns = S - s0 < 8 ? S - s0 : 8;
+            st = launch_depth_read(sr, n_src, r == 0 ? src_stride : T * d, T, d, 1, dt, qbuf + (r * S + s0) * d, ns,
+                                   gain, eps, static_cast<unsigned char *>(o) + (size_t)(s0 * 4 + r) * row, lbuf,
+                                   stream, 4 * T * d);
+            if (st != ATTNRES_OK) return st;
+            e = cudaMemcpy2DAsync(lse + (s0 * 4 + r) * T, (size_t)4 * T * 4, lbuf, (size_t)T * 4, (size_t)T * 4,
+                                  (size_t)ns, cudaMemcpyDeviceToDevice, s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync");
+        }
+    }
+    return ATTNRES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1404,6 +1567,43 @@ attnres_status_t msar_expand_bwd(const void *src, int64_t n_src, int64_t src_str
     return launch_msar_bwd(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, gain, eps, mix_gain,
                            mix_w, mix_eps, dh, dsrc, dsrc_stride, dconv_w, dqueries, dgain, dmix_gain, dmix_w,
                            workspace, workspace_bytes, stream);
+}
+
+attnres_status_t msar_expand_fwd_ws_workspace_size(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt,
+                                                  size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || n_src < 1 || T < 0 || d < 1)
+        return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    if (d % 1024 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    *bytes = msar_fwd_ws_plan(n_src, T, d, dt, true, 0).total;
+    return ATTNRES_OK;
+}
+
+attnres_status_t msar_expand_fwd_ws(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                    attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                    int64_t conv_src_stride, const float *queries, const float *gain, float eps,
+                                    const float *mix_gain, const float *mix_w, float mix_eps, void *out,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+    return launch_msar_read_ws(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, conv_src_stride, queries, gain,
+                               eps, mix_gain, mix_w, mix_eps, out, workspace, workspace_bytes, stream);
+}
+
+attnres_status_t msar_block_phase1_ws_workspace_size(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt,
+                                                    int64_t S, size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || n_src < 1 || T < 0 || d < 1 || S < 1)
+        return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    if (d % 512 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    *bytes = msar_fwd_ws_plan(n_src, T, d, dt, false, S).total;
+    return ATTNRES_OK;
+}
+
+attnres_status_t msar_block_phase1_ws(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                      attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                      const float *queries, int64_t S, const float *gain, float eps, void *o,
+                                      float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    return launch_msar_phase1_ws(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, S, gain, eps, o, lse,
+                                 workspace, workspace_bytes, stream);
 }
 
 const char *attnres_status_string(attnres_status_t s) {

@@ -1,4 +1,5 @@
-// msar_bwd.cu -- kernels of the backward of the MSAR read.
+// msar_bwd.cu -- kernels of the backward of the MSAR read (the streams and
+// mixer kernels also serve the forward read with a workspace, msar_expand_fwd_ws).
 //
 // The backward runs as a chain of steps over tensors in the caller's
 // workspace (attnres_api.cu, msar_expand_bwd):
@@ -242,7 +243,12 @@ __global__ void __launch_bounds__(MX_THREADS) msar_mix_stats_kernel(const MsarBw
         for (int it = 0; it < MX_CS / 256; ++it) {
             const int cl = it * 256 + lane * 8;
             float dh[8], z[4][8];
-            load8<Tin>(a.dh + (t * a.d + c0 + cl) * ES, dh);
+            if (a.dh) {
+                load8<Tin>(a.dh + (t * a.d + c0 + cl) * ES, dh);
+            } else {                                    // the forward's mixer: no dh sums
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dh[e] = 0.f;
+            }
 #pragma unroll
             for (int r = 0; r < 4; ++r) load8<Tin>(a.z + (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES, z[r]);
 #pragma unroll
@@ -265,6 +271,42 @@ __global__ void __launch_bounds__(MX_THREADS) msar_mix_stats_kernel(const MsarBw
 #pragma unroll
             for (int q = 0; q < 9; ++q) dst[q] = s[q];
         }
+    }
+}
+
+// The forward's mixer output from the per-slice sums of token t (added in
+// slice order): h = sum_r c_r Z^(r) with c_r = sigmoid(s_r / nu).  A warp per
+// token, 8 channels per lane per 256-channel step.
+template <typename Tin>
+__global__ void __launch_bounds__(256) msar_mix_out_kernel(const MsarBwdArgs a, unsigned char *out) {
+    constexpr int ES = sizeof(Tin);
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    const float inv_md = 1.f / (4.f * (float)a.d);
+    float tot[5];
+#pragma unroll
+    for (int q = 0; q < 5; ++q) tot[q] = 0.f;
+    for (int k = 0; k < a.nsl; ++k)
+#pragma unroll
+        for (int q = 0; q < 5; ++q) tot[q] += __ldg(a.mix_part + (t * a.nsl + k) * 9 + q);
+    const float ms = fmaf(tot[0], inv_md, a.mix_eps);
+    const float inv = ms > 0.f ? rsqrtf(ms) : 0.f;
+    float cr[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) cr[r] = 1.f / (1.f + __expf(-tot[1 + r] * inv));
+    for (int c = lane * 8; c < a.d; c += 256) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float z[8];
+            load8<Tin>(a.z + (((int64_t)r * a.T + t) * a.d + c) * ES, z);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = fmaf(cr[r], z[e], y[e]);
+        }
+        store8<Tin>(out + (t * a.d + c) * ES, y);
     }
 }
 
@@ -625,6 +667,25 @@ static cudaError_t launch_mix_t(const MsarBwdArgs &a, cudaStream_t s) {
     const dim3 agrid((unsigned)((4 * (int64_t)a.d / 8 + 255) / 256), (unsigned)((a.T + a.tc - 1) / a.tc));
     msar_mix_acc_kernel<Tin><<<agrid, 256, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+template <typename Tin>
+static cudaError_t launch_fwd_mix_t(const MsarBwdArgs &a, unsigned char *out, cudaStream_t s) {
+    const dim3 grid((unsigned)a.nsl, (unsigned)((a.T + a.tc_m - 1) / a.tc_m));
+    cudaError_t e = set_smem(msar_mix_stats_kernel<Tin>, MX_SMEM);
+    if (e != cudaSuccess) return e;
+    msar_mix_stats_kernel<Tin><<<grid, MX_THREADS, MX_SMEM, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    msar_mix_out_kernel<Tin><<<(unsigned)((a.T + 7) / 8), 256, 0, s>>>(a, out);
+    return cudaGetLastError();
+}
+
+cudaError_t msar_fwd_mix(int dt, const MsarBwdArgs &a, void *out, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a.d % MX_CS != 0 || a.nsl != a.d / MX_CS || a.dh != nullptr) return cudaErrorInvalidValue;
+    unsigned char *o = static_cast<unsigned char *>(out);
+    return dt == 1 ? launch_fwd_mix_t<__nv_bfloat16>(a, o, s) : launch_fwd_mix_t<float>(a, o, s);
 }
 
 cudaError_t msar_bwd_streams(int dt, const MsarBwdArgs &a, void *stream) {

@@ -25,7 +25,7 @@ struct MsarBwdArgs {
     unsigned char *u;               // [3][n_src][T][d] the conv streams (source dtype)
     unsigned char *z;               // [4][T][d] the per-stream reads
     unsigned char *dz;              // [4][T][d] their gradients
-    const unsigned char *dh;        // [T][d] the output gradient
+    const unsigned char *dh;        // [T][d] the output gradient (nullptr in the forward's mixer)
     const float *mix_gain;          // [4d] or nullptr
     const float *mix_w;             // [4d][4]
     float mix_eps;
@@ -41,6 +41,9 @@ struct MsarBwdArgs {
 };
 
 cudaError_t msar_bwd_streams(int dt, const MsarBwdArgs &a, void *stream);
+// the forward's mixer over Z (a.z; a.dh must be nullptr): the per-slice sums
+// into a.mix_part, then out[t] = sum_r c_r Z^(r)[t]
+cudaError_t msar_fwd_mix(int dt, const MsarBwdArgs &a, void *out, void *stream);
 // mixer backward (dz, mix_e) and the per-chunk partials of A; d a multiple
 // of 1024 with nsl = d / 1024 (cudaErrorInvalidValue otherwise)
 cudaError_t msar_bwd_mix(int dt, const MsarBwdArgs &a, void *stream);

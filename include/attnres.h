@@ -548,6 +548,64 @@ attnres_status_t msar_expand_bwd_workspace_size(int64_t n_src, int64_t T, int64_
                                                attnres_dtype_t dt, int64_t m,
                                                const int32_t *ksizes, size_t *bytes);
 
+/*
+ * msar_expand_fwd with a caller workspace: the same read as a chain that
+ * writes the conv streams once, reads each stream with the forward read
+ * kernels and mixes the per-stream reads.  The fused msar_expand_fwd never
+ * writes a stream (the pages' on-demand expansion, MSAR page, section 어떻게
+ * 쓰나) but synchronises a cluster of CTAs per token; on this GPU the chain
+ * is faster where the memory for it is available.  The per-stream reads are
+ * held in dtype dt before the mixer (the fused read keeps them in fp32), so
+ * bf16 results differ from msar_expand_fwd's within the bf16 tolerance.
+ *   conv_src_stride  0: one set of kernels for every source (msar_expand_fwd);
+ *                    > 0: source i's kernels at conv_w + i * conv_src_stride
+ *                    (msar_expand_fwd_ps; >= d * (k_1 + k_2 + k_3) with more
+ *                    than one source, else ATTNRES_ERR_INVALID_ARG)
+ *   workspace        device scratch of msar_expand_fwd_ws_workspace_size bytes
+ *                    (the streams and the per-stream reads: (3 n_src + 4) T d
+ *                    elements of dtype dt and T d / 1024 x 9 floats); must not
+ *                    overlap src or out
+ * Every other argument as msar_expand_fwd.  Limits: m = 4, kernel sizes
+ * 1..16, d a multiple of 1024 up to 16384 (else ATTNRES_ERR_UNSUPPORTED);
+ * queries, mix_w, gain, out and workspace 16-byte aligned, conv_w and
+ * mix_gain 4-byte.
+ */
+attnres_status_t msar_expand_fwd_ws(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                    int64_t d, attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                    const float *conv_w, int64_t conv_src_stride, const float *queries,
+                                    const float *gain, float eps, const float *mix_gain,
+                                    const float *mix_w, float mix_eps, void *out, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/* Workspace bytes msar_expand_fwd_ws needs for these sizes. */
+attnres_status_t msar_expand_fwd_ws_workspace_size(int64_t n_src, int64_t T, int64_t d,
+                                                  attnres_dtype_t dt, size_t *bytes);
+
+/*
+ * msar_block_phase1 with a caller workspace: every cached source's three conv
+ * streams are written once, then each stream (the sources themselves for
+ * stream 0) is read by that stream's queries of all S layers with the
+ * forward read kernels (up to 8 layers per launch), giving the same state o,
+ * lse in the same layout.  The streams are held in dtype dt before the read
+ * (the fused phase 1 keeps them in fp32).
+ *   workspace  device scratch of msar_block_phase1_ws_workspace_size bytes
+ *              (the streams: 3 n_src T d elements of dtype dt, plus the
+ *              queries regrouped by stream and one group's lse); must not
+ *              overlap src, o or lse
+ * Every other argument as msar_block_phase1, without its n_src <= 8 limit.
+ * Limits: d a multiple of 512 up to 16384 (else ATTNRES_ERR_UNSUPPORTED).
+ */
+attnres_status_t msar_block_phase1_ws(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                      int64_t d, attnres_dtype_t dt, int64_t m,
+                                      const int32_t *ksizes, const float *conv_w,
+                                      const float *queries, int64_t S, const float *gain, float eps,
+                                      void *o, float *lse, void *workspace, size_t workspace_bytes,
+                                      void *stream);
+
+/* Workspace bytes msar_block_phase1_ws needs for these sizes. */
+attnres_status_t msar_block_phase1_ws_workspace_size(int64_t n_src, int64_t T, int64_t d,
+                                                    attnres_dtype_t dt, int64_t S, size_t *bytes);
+
 /* Static description of a status code (never NULL). */
 const char *attnres_status_string(attnres_status_t status);
 

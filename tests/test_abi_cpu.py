@@ -336,3 +336,40 @@ def test_msar_backward_per_source_validation(lib):
     assert mp(d * 24 - 4) == INV                  # sources' kernels would overlap
     assert mp(d * 24, dcw=DQ - 64) == INV         # 8 kernel gradients run into dqueries
     assert mp(d * 24 + 2) == UNS                  # kernels not 16-byte aligned
+
+
+def test_msar_workspace_chain_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    bad = (ctypes.c_int32 * 3)(4, 0, 12)
+    kp = lambda k: ctypes.cast(k, ctypes.c_void_p)
+    T, d = 16, 1024
+    OUT, WS = B + 0x1000000, B + 0x4000000
+
+    def fw(k=ks, T=T, d=d, cstride=0, out=OUT, ws=WS, mix_eps=1e-6):
+        return lib.msar_expand_fwd_ws(A, 8, T * d, T, d, BF16, 4, kp(k), B, cstride, B + 0x200000, None, 1e-6, None,
+                                      B + 0x300000, mix_eps, out, ws, 1 << 30, None)
+    assert fw(T=0) == OK
+    assert fw(k=bad) == INV
+    assert fw(mix_eps=-1.0) == INV
+    assert fw(out=None) == INV
+    assert fw(ws=None) == INV
+    assert fw(cstride=-1) == INV
+    assert fw(cstride=d * 24 - 1) == INV           # sources' kernels would overlap
+    assert fw(out=A + 64) == INV                   # overlaps the sources
+    assert fw(ws=OUT - 64) == INV                  # workspace overlaps out
+    assert fw(d=1536) == UNS                       # the mixer slices need d % 1024 == 0
+    assert fw(out=OUT + 8) == UNS
+    n = ctypes.c_size_t(0)
+    assert lib.msar_expand_fwd_ws_workspace_size(8, T, d, BF16, None) == INV
+    assert lib.msar_expand_fwd_ws_workspace_size(8, T, 1536, BF16, ctypes.byref(n)) == UNS
+
+    def p1(S=4, o=OUT, lse=B + 0x3000000, ws=WS, T=T, d=d):
+        return lib.msar_block_phase1_ws(A, 8, T * d, T, d, BF16, 4, kp(ks), B, B + 0x200000, S, None, 1e-6, o, lse,
+                                        ws, 1 << 30, None)
+    assert p1(T=0) == OK
+    assert p1(S=0) == INV
+    assert p1(o=None) == INV
+    assert p1(ws=None) == INV
+    assert p1(o=A + 64) == INV
+    assert p1(d=768) == UNS                        # the streams kernel needs d % 512 == 0
+    assert lib.msar_block_phase1_ws_workspace_size(8, T, d, BF16, 0, ctypes.byref(n)) == INV

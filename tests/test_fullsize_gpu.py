@@ -416,3 +416,48 @@ def test_msar_bwd_per_source_T32768_d4096():
     assert torch.count_nonzero(got[0][:, ~inside]) == 0
     for name, g_, r_ in zip(("dconv_w", "dqueries", "dgain", "dmix_gain", "dmix_w"), got[1:], ref_par):
         check_out(g_, np.asarray(r_).reshape(tuple(g_.shape)), BF16, strict=False, what=name)
+
+
+def test_msar_workspace_chain_T32768_d4096():
+    """The MSAR read and MSAR phase 1 through the workspace chain at the MSAR
+    size: sampled tokens of the read against the oracle on causal windows,
+    and phase 1 followed by each layer's phase 2 against the one-shot oracle
+    read of the cached sources plus the layer's partial."""
+    T, d, N, S = 32768, 4096, 8, 4
+    ks = (4, 8, 12)
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((4, d), (16.0 / d) ** 0.5, g)
+    cw = torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g) for k in ks])
+    mw = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g)
+    out = attnres.msar_expand_fwd_ws(src, ks, cw, q, None, 1e-6, None, mw, 1e-6)
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T, n=100)
+    cw_h, q_h, mw_h = (t.cpu().numpy().astype(np.float64) for t in (cw, q, mw))
+    got = rows(out, idx)
+    ref = np.empty_like(got)
+    for j, t in enumerate(idx):
+        lo = max(0, int(t) - 11)
+        win = src[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
+        ref[j] = oracle.msar(win, ks, cw_h, q_h, None, 1e-6, None, mw_h, 1e-6)[-1]
+    check_out(got, ref, BF16, strict=False, what="workspace-chain read")
+    del out
+    qs = inputs.device_normal((S, 4, d), (16.0 / d) ** 0.5, g)
+    parts = torch.randn((S, T, d), generator=g, device="cuda").to(BF16)
+    o, lse = attnres.msar_block_phase1_ws(src, ks, cw, qs)
+    outs = [attnres.msar_block_phase2(o[s_], lse[s_], parts[s_] if s_ > 0 else None, ks, cw, qs[s_], None, 1e-6,
+                                      None, mw, 1e-6) for s_ in range(S)]
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T, n=40)
+    qs_h = qs.cpu().numpy().astype(np.float64)
+    for s_ in range(S):
+        got = rows(outs[s_], idx)
+        ref = np.empty_like(got)
+        for j, t in enumerate(idx):
+            lo = max(0, int(t) - 11)
+            win = src[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
+            if s_ > 0:
+                pw = parts[s_, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
+                win = np.concatenate([win, pw[None]])
+            ref[j] = oracle.msar(win, ks, cw_h, qs_h[s_], None, 1e-6, None, mw_h, 1e-6)[-1]
+        check_out(got, ref, BF16, strict=False, what=f"layer {s_ + 1} after the workspace phase 1")

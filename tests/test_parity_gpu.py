@@ -860,6 +860,80 @@ def test_msar_bwd_per_source_equal_kernels_match_the_shared_backward():
     check_out(shared[1], total, F32, np.abs(total).max(), strict=False, what="summed kernel gradients")
 
 
+# --------------------------------------------------------------- MSAR through the workspace chain
+
+@pytest.mark.parametrize("dtype,n_src,T,d,ks,per_source", [
+    (BF16, 8, 100, 4096, (4, 8, 12), False), (F32, 3, 300, 1024, (4, 8, 12), False),
+    (BF16, 5, 45, 2048, (16, 5, 9), False), (BF16, 8, 70, 4096, (4, 8, 12), True),
+    (F32, 1, 33, 1024, (1, 2, 3), True), (BF16, 12, 20, 1024, (4, 8, 12), False)])
+def test_msar_workspace_chain(dtype, n_src, T, d, ks, per_source):
+    """The MSAR read through the workspace chain (streams written once, one
+    read per stream, the sliced mixer) against the oracle, with shared and
+    with per-source kernels.  The per-stream reads are held in dtype before
+    the mixer, so bf16 results are held to the stated bar."""
+    rng = _rng(n_src * 13 + T + d)
+    src = _sources(rng, n_src, T, d, dtype)
+    q = _queries(rng, 4, d)
+    mk = lambda: np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel() for k in ks])
+    cw = np.stack([mk() for _ in range(n_src)]) if per_source else mk()
+    mw = (rng.standard_normal((4 * d, 4)) / math.sqrt(4 * d)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    mg = rng.uniform(0.5, 1.5, 4 * d).astype(np.float32)
+    out = attnres.msar_expand_fwd_ws(to_dev(src, dtype), ks, to_dev(cw, F32), to_dev(q, F32), to_dev(g, F32), 1e-6,
+                                     to_dev(mg, F32), to_dev(mw, F32), 1e-6)
+    ref = (oracle.msar_ps if per_source else oracle.msar)(src, ks, cw, q, g, 1e-6, mg, mw, 1e-6)
+    check_out(out, ref, dtype, np.abs(src).max() * 3, strict=dtype == F32)
+
+
+def _rounded_streams(cached, cw, ks):
+    """The 4 streams of every cached source as the workspace chain stores
+    them: stream 0 the sources, streams 1..3 the oracle's causal conv rounded
+    to bf16."""
+    N, T, d = cached.shape
+    out, off = [np.asarray(cached, np.float64)], 0
+    for k in ks:
+        kr = np.asarray(cw[off:off + d * k]).reshape(d, k)
+        off += d * k
+        out.append(np.stack([inputs.bf16_round(oracle.msar_conv(cached[i], kr).astype(np.float32))
+                             for i in range(N)]).astype(np.float64))
+    return out
+
+
+@pytest.mark.parametrize("dtype,N,S,T,d", [(BF16, 8, 4, 60, 4096), (F32, 5, 1, 33, 1024), (BF16, 3, 6, 45, 2048),
+                                           (BF16, 12, 9, 20, 512)])
+def test_msar_block_phase1_workspace_chain(dtype, N, S, T, d):
+    """Phase 1 through the workspace chain against the oracle's phase 1
+    (every layer's per-stream o and lse; more than 8 layers take two groups,
+    more than 8 sources the chunked read).  With bf16 the chain stores the
+    streams in bf16 before reading them (the fused phase 1 keeps them in
+    fp32), so its state is also checked exactly as the read of the rounded
+    streams: o with the strict bf16 bound and lse with the fp32 one."""
+    rng = _rng(N * 7 + S + T + d)
+    ks = (4, 8, 12)
+    cached, _, q, cw, _, g, _ = _msar_block(rng, N, S, T, d, dtype)
+    o, lse = attnres.msar_block_phase1_ws(to_dev(cached, dtype), ks, to_dev(cw, F32), to_dev(q, F32),
+                                          to_dev(g, F32), 1e-6)
+    ro, rl = oracle.msar_phase1(cached, ks, cw, q, g, 1e-6)
+    check_out(o, ro, dtype, np.abs(cached).max(), strict=dtype == F32, what="o")
+    if dtype == F32:
+        check_lse(lse, rl)
+        return
+    for r, U in enumerate(_rounded_streams(cached, cw, ks)):
+        o_r, l_r = oracle.block_phase1(U, q[:, r, :], g, 1e-6)
+        check_out(o[:, r], o_r, BF16, what=f"o of stream {r} (rounded streams)")
+        # The GPU forms a stream in fp32 and the oracle in fp64 before the bf16
+        # rounding, so now and then one element rounds to the neighbouring bf16
+        # value; that moves a score by at most one bf16 step (2^-7 relative) of
+        # that element's term |w_c g_c u_c| / rms(u).  Allow two such elements
+        # per token on top of the fp32 bound.
+        wg = q[:, r, :].astype(np.float64) * g
+        rms = np.sqrt((U ** 2).mean(axis=2) + 1e-6)                               # [N, T]
+        term = np.max(np.abs(wg[:, None, None, :] * U[None]), axis=3) / rms[None]  # [S, N, T]
+        tol = 1e-4 * (1.0 + np.abs(l_r)) + 2 * 2.0 ** -7 * term.max(axis=1)
+        err = np.abs(to_host(lse[:, r]) - l_r)
+        assert np.all(err <= tol), f"lse of stream {r} (rounded streams): max err {err.max()}"
+
+
 # --------------------------------------------------------------- hygiene
 
 def test_outputs_stay_inside_their_buffers():
