@@ -1266,15 +1266,17 @@ class FullDepthWorkload(BlockWorkload):
 
 
 class MsarBlockWsWorkload(MsarBlockWorkload):
-    """The MSAR two-phase block with phase 1 through the workspace chain
+    """The MSAR two-phase block through the workspace chains: phase 1
     (msar_block_phase1_ws: the cached sources' streams written once, each
-    stream read by its 4 layers' queries with the tensor-core read), phase 2
-    as msar_block_phase2.  Same inputs and outputs as the fused schedule."""
+    stream read by its 4 layers' queries with the tensor-core read) and
+    phase 2 per layer (msar_block_phase2_ws: the partial's streams, one Block
+    merge per stream, the sliced mixer).  Same inputs and outputs as the
+    fused schedule."""
 
     def __init__(self, T=32768, d=4096, N=8, S=4, seed=0):
         super().__init__(T, d, N, S, seed)
         self.name = "msar_two_phase_block_workspace_chain"
-        self.launches_per_step = 1 + 4 + S
+        self.launches_per_step = 1 + 4 + 2 + (S - 1) * (1 + 4 + 2)
         self.dominant = "msar phase 1, workspace chain (streams + 4 reads of 4 queries)"
         self.dominant_src = "msar_bwd"
         self.profile_tag = f"ncu_msar_phase1_ws_d{d}"
@@ -1285,6 +1287,8 @@ class MsarBlockWsWorkload(MsarBlockWorkload):
         super().setup(device)
         nb = attnres.msar_block_phase1_ws_workspace_size(self.N, self.T, self.d, torch.bfloat16, self.S)
         self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+        nb = attnres.msar_block_phase2_ws_workspace_size(self.T, self.d, torch.bfloat16)
+        self.ws2 = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
 
     def step(self, stream, ev=None):
         from depth_wise_attention_gb300 import attnres
@@ -1295,9 +1299,9 @@ class MsarBlockWsWorkload(MsarBlockWorkload):
         if ev is not None:
             ev[1].record(stream)
         for s_ in range(self.S):
-            attnres.msar_block_phase2(self.o[s_], self.lse[s_], self.parts[s_] if s_ > 0 else None, self.ks,
-                                      self.conv_w, self.queries[s_], None, 1e-6, None, self.mix_w, 1e-6,
-                                      out=self.outs[s_], stream=stream)
+            attnres.msar_block_phase2_ws(self.o[s_], self.lse[s_], self.parts[s_] if s_ > 0 else None, self.ks,
+                                         self.conv_w, self.queries[s_], None, 1e-6, None, self.mix_w, 1e-6,
+                                         out=self.outs[s_], workspace=self.ws2, stream=stream)
 
 
 def make_workload(name, T=None):

@@ -68,6 +68,9 @@ _SIGS = {
     "msar_block_phase1_ws": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _i64, _vp, _f, _vp,
                              _vp, _vp, ctypes.c_size_t, _vp],
     "msar_block_phase1_ws_workspace_size": [_i64, _i64, _i64, ctypes.c_int, _i64, ctypes.POINTER(ctypes.c_size_t)],
+    "msar_block_phase2_ws": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
+                             _vp, _vp, ctypes.c_size_t, _vp],
+    "msar_block_phase2_ws_workspace_size": [_i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
     "attnres_status_string": [ctypes.c_int],
     "attnres_last_cuda_error": [],
     "attnres_sync_status": [_vp],
@@ -629,3 +632,30 @@ def msar_block_phase1_ws(src, ksizes, conv_w, queries, gain=None, eps=1e-6, o=No
         _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries), S, _p(gain), eps,
         _p(o), _p(lse), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return o, lse
+
+
+def msar_block_phase2_ws_workspace_size(T, d, dtype):
+    import torch
+    n = ctypes.c_size_t(0)
+    dt = BF16 if dtype == torch.bfloat16 else F32
+    _check("msar_block_phase2_ws_workspace_size", load().msar_block_phase2_ws_workspace_size(T, d, dt, ctypes.byref(n)))
+    return n.value
+
+
+def msar_block_phase2_ws(o, lse, partial, ksizes, conv_w, query, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                         mix_eps=1e-6, out=None, workspace=None, stream=None):
+    """MSAR phase 2 of one layer through the workspace chain: o [m, T, d],
+    lse [m, T], partial [T, d] or None, query [m, d] -> out [T, d]."""
+    import torch
+    m, T, d = o.shape
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    if out is None:
+        out = torch.empty((T, d), dtype=o.dtype, device=o.device)
+    if workspace is None:
+        nbytes = msar_block_phase2_ws_workspace_size(T, d, o.dtype)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=o.device)
+    _check("msar_block_phase2_ws", load().msar_block_phase2_ws(
+        _p(o), _p(lse), _p(partial), T, d, _dt(o), m, ctypes.cast(ks, _vp), _p(conv_w), _p(query), _p(gain), eps,
+        _p(mix_gain), _p(mix_w), mix_eps, _p(out), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return out

@@ -1327,6 +1327,65 @@ attnres_status_t launch_msar_phase1_ws(const void *src, int64_t n_src, int64_t s
     return ATTNRES_OK;
 }
 
+// MSAR phase 2 with a workspace: the partial's three conv streams written
+// once, each stream merged into its phase-1 state by the Block merge kernel
+// (Z^(r) stored), then the sliced mixer.  No partial: the mixer over o.
+attnres_status_t launch_msar_phase2_ws(const void *o, const float *lse, const void *partial, int64_t T, int64_t d,
+                                       attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                       const float *query, const float *gain, float eps, const float *mix_gain,
+                                       const float *mix_w, float mix_eps, void *out, void *ws, size_t ws_bytes,
+                                       void *stream) {
+    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
+    if (T < 0 || d < 1 || !(eps >= 0.f) || std::isinf(eps) || !(mix_eps >= 0.f) || std::isinf(mix_eps))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / (4 * T)) return ATTNRES_ERR_INVALID_ARG;
+    if (T == 0) return ATTNRES_OK;
+    if (!o || !lse || !conv_w || !query || !mix_w || !out || !ws) return ATTNRES_ERR_INVALID_ARG;
+    attnres_status_t st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    const size_t es = esize(dt);
+    const size_t row = (size_t)T * (size_t)d * es;
+    if (overlap(out, row, o, 4 * row) || overlap(out, row, lse, (size_t)4 * T * 4) ||
+        (partial && overlap(out, row, partial, row)) || overlap(ws, ws_bytes, o, 4 * row) ||
+        overlap(ws, ws_bytes, lse, (size_t)4 * T * 4) || overlap(ws, ws_bytes, out, row) ||
+        (partial && overlap(ws, ws_bytes, partial, row)))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (d % 1024 != 0 || d > 16384) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(o) || !aligned4(lse) || (partial && !aligned16(partial)) || !aligned16(out) ||
+        !aligned16(query) || !aligned4(conv_w) || !aligned16(mix_w) || (gain && !aligned16(gain)) ||
+        (mix_gain && !aligned4(mix_gain)) || !aligned16(ws))
+        return ATTNRES_ERR_UNSUPPORTED;
+    const MsarFwdWsPlan p = msar_fwd_ws_plan(1, T, d, dt, true, 0);
+    if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const unsigned char *z = static_cast<const unsigned char *>(o);
+    if (partial) {
+        st = msar_write_streams(partial, 1, T * d, T, d, dt, ksizes, conv_w, 0, p.tc_s, w + p.off_u, stream);
+        if (st != ATTNRES_OK) return st;
+        for (int64_t r = 0; r < 4; ++r) {
+            const void *pr = r == 0 ? partial : static_cast<const void *>(w + p.off_u + (size_t)(r - 1) * row);
+            st = launch_phase2(static_cast<const unsigned char *>(o) + (size_t)r * row, lse + r * T, pr, nullptr,
+                               nullptr, false, T, d, 1, dt, query + r * d, gain, eps, w + p.off_z + (size_t)r * row,
+                               stream);
+            if (st != ATTNRES_OK) return st;
+        }
+        z = w + p.off_z;
+    }
+    MsarBwdArgs a{};
+    a.T = T;
+    a.d = (int)d;
+    a.z = const_cast<unsigned char *>(z);          // read only by the mixer
+    a.dh = nullptr;
+    a.mix_gain = mix_gain;
+    a.mix_w = mix_w;
+    a.mix_eps = mix_eps;
+    a.mix_part = reinterpret_cast<float *>(w + p.off_part);
+    a.nsl = (int)(d / 1024);
+    a.tc_m = 128;
+    cudaError_t e = msar_fwd_mix(dt == ATTNRES_BF16 ? 1 : 0, a, out, stream);
+    return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "msar mixer launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -1604,6 +1663,23 @@ attnres_status_t msar_block_phase1_ws(const void *src, int64_t n_src, int64_t sr
                                       float *lse, void *workspace, size_t workspace_bytes, void *stream) {
     return launch_msar_phase1_ws(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, S, gain, eps, o, lse,
                                  workspace, workspace_bytes, stream);
+}
+
+attnres_status_t msar_block_phase2_ws_workspace_size(int64_t T, int64_t d, attnres_dtype_t dt, size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || T < 0 || d < 1) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    if (d % 1024 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    *bytes = msar_fwd_ws_plan(1, T, d, dt, true, 0).total;
+    return ATTNRES_OK;
+}
+
+attnres_status_t msar_block_phase2_ws(const void *o, const float *lse, const void *partial, int64_t T, int64_t d,
+                                      attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                      const float *query, const float *gain, float eps, const float *mix_gain,
+                                      const float *mix_w, float mix_eps, void *out, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+    return launch_msar_phase2_ws(o, lse, partial, T, d, dt, m, ksizes, conv_w, query, gain, eps, mix_gain, mix_w,
+                                 mix_eps, out, workspace, workspace_bytes, stream);
 }
 
 const char *attnres_status_string(attnres_status_t s) {

@@ -606,6 +606,30 @@ attnres_status_t msar_block_phase1_ws(const void *src, int64_t n_src, int64_t sr
 attnres_status_t msar_block_phase1_ws_workspace_size(int64_t n_src, int64_t T, int64_t d,
                                                     attnres_dtype_t dt, int64_t S, size_t *bytes);
 
+/*
+ * msar_block_phase2 with a caller workspace: the partial's three conv streams
+ * are written once, each stream of the partial is merged into that stream's
+ * phase-1 state by the Block merge (attnres_block_phase2_merge's kernel, one
+ * launch per stream) and the merged streams Z^(r) go through the mixer as in
+ * msar_expand_fwd_ws.  partial == NULL mixes Z^(r) = o^(r).  The streams and
+ * the merged Z are held in dtype dt (the fused phase 2 keeps them in fp32).
+ *   workspace  device scratch of msar_block_phase2_ws_workspace_size bytes
+ *              (7 T d elements of dtype dt and T d / 1024 x 9 floats); must
+ *              not overlap o, lse, partial or out
+ * Every other argument as msar_block_phase2.  Limits: d a multiple of 1024 up
+ * to 16384 (else ATTNRES_ERR_UNSUPPORTED).
+ */
+attnres_status_t msar_block_phase2_ws(const void *o, const float *lse, const void *partial, int64_t T,
+                                      int64_t d, attnres_dtype_t dt, int64_t m,
+                                      const int32_t *ksizes, const float *conv_w, const float *query,
+                                      const float *gain, float eps, const float *mix_gain,
+                                      const float *mix_w, float mix_eps, void *out, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* Workspace bytes msar_block_phase2_ws needs for these sizes. */
+attnres_status_t msar_block_phase2_ws_workspace_size(int64_t T, int64_t d, attnres_dtype_t dt,
+                                                    size_t *bytes);
+
 /* Static description of a status code (never NULL). */
 const char *attnres_status_string(attnres_status_t status);
 

@@ -373,3 +373,20 @@ def test_msar_workspace_chain_validation(lib):
     assert p1(o=A + 64) == INV
     assert p1(d=768) == UNS                        # the streams kernel needs d % 512 == 0
     assert lib.msar_block_phase1_ws_workspace_size(8, T, d, BF16, 0, ctypes.byref(n)) == INV
+
+
+def test_msar_phase2_workspace_chain_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    T, d = 16, 1024
+
+    def p2(o=A, part=A + 0x2000000, out=B + 0x1000000, ws=B + 0x4000000, d=d, mix_eps=1e-6):
+        return lib.msar_block_phase2_ws(o, B + 0x3000000, part, T, d, BF16, 4, ctypes.cast(ks, ctypes.c_void_p), B,
+                                        B + 0x200000, None, 1e-6, None, B + 0x300000, mix_eps, out, ws, 1 << 30, None)
+    assert p2(o=None) == INV
+    assert p2(ws=None) == INV
+    assert p2(mix_eps=-1.0) == INV
+    assert p2(out=A + 64) == INV                   # overlaps the state
+    assert p2(ws=A + 0x2000000 - 64) == INV        # workspace overlaps the partial
+    assert p2(d=1536) == UNS
+    n = ctypes.c_size_t(0)
+    assert lib.msar_block_phase2_ws_workspace_size(T, 1536, BF16, ctypes.byref(n)) == UNS

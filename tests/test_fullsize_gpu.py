@@ -419,10 +419,11 @@ def test_msar_bwd_per_source_T32768_d4096():
 
 
 def test_msar_workspace_chain_T32768_d4096():
-    """The MSAR read and MSAR phase 1 through the workspace chain at the MSAR
-    size: sampled tokens of the read against the oracle on causal windows,
-    and phase 1 followed by each layer's phase 2 against the one-shot oracle
-    read of the cached sources plus the layer's partial."""
+    """The MSAR read and the MSAR two-phase block through the workspace chains
+    at the MSAR size: sampled tokens of the read against the oracle on causal
+    windows, and the chains' phase 1 followed by each layer's phase 2 against
+    the one-shot oracle read of the cached sources plus the layer's
+    partial."""
     T, d, N, S = 32768, 4096, 8, 4
     ks = (4, 8, 12)
     src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
@@ -445,8 +446,8 @@ def test_msar_workspace_chain_T32768_d4096():
     qs = inputs.device_normal((S, 4, d), (16.0 / d) ** 0.5, g)
     parts = torch.randn((S, T, d), generator=g, device="cuda").to(BF16)
     o, lse = attnres.msar_block_phase1_ws(src, ks, cw, qs)
-    outs = [attnres.msar_block_phase2(o[s_], lse[s_], parts[s_] if s_ > 0 else None, ks, cw, qs[s_], None, 1e-6,
-                                      None, mw, 1e-6) for s_ in range(S)]
+    outs = [attnres.msar_block_phase2_ws(o[s_], lse[s_], parts[s_] if s_ > 0 else None, ks, cw, qs[s_], None, 1e-6,
+                                         None, mw, 1e-6) for s_ in range(S)]
     attnres.attnres_sync_status()
     idx = sampled_tokens(T, n=40)
     qs_h = qs.cpu().numpy().astype(np.float64)
@@ -460,4 +461,4 @@ def test_msar_workspace_chain_T32768_d4096():
                 pw = parts[s_, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
                 win = np.concatenate([win, pw[None]])
             ref[j] = oracle.msar(win, ks, cw_h, qs_h[s_], None, 1e-6, None, mw_h, 1e-6)[-1]
-        check_out(got, ref, BF16, strict=False, what=f"layer {s_ + 1} after the workspace phase 1")
+        check_out(got, ref, BF16, strict=False, what=f"layer {s_ + 1} through the workspace chains")

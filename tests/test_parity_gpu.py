@@ -934,6 +934,29 @@ def test_msar_block_phase1_workspace_chain(dtype, N, S, T, d):
         assert np.all(err <= tol), f"lse of stream {r} (rounded streams): max err {err.max()}"
 
 
+@pytest.mark.parametrize("dtype,T,d,with_partial", [(BF16, 60, 4096, True), (F32, 45, 1024, True),
+                                                    (BF16, 130, 2048, True), (BF16, 33, 1024, False),
+                                                    (F32, 20, 2048, False)])
+def test_msar_block_phase2_workspace_chain(dtype, T, d, with_partial):
+    """Phase 2 through the workspace chain (the partial's streams, one Block
+    merge per stream, the sliced mixer) against the oracle on the same
+    phase-1 state; no partial mixes the state alone.  bf16 results are held
+    to the stated bar (the chain stores the partial's streams and the merged
+    streams in bf16)."""
+    rng = _rng(T + d + with_partial + 1)
+    ks = (4, 8, 12)
+    cached, parts, q, cw, mw, g, mg = _msar_block(rng, 4, 1, T, d, dtype, ks)
+    o, lse = oracle.msar_phase1(cached, ks, cw, q, g, 1e-6)
+    o1 = inputs.bf16_round(o[0].astype(np.float32)) if dtype == BF16 else o[0].astype(np.float32)
+    p = parts[0] if with_partial else None
+    out = attnres.msar_block_phase2_ws(to_dev(o1, dtype), to_dev(lse[0].astype(np.float32), F32),
+                                       to_dev(p, dtype) if with_partial else None, ks, to_dev(cw, F32),
+                                       to_dev(q[0], F32), to_dev(g, F32), 1e-6, to_dev(mg, F32), to_dev(mw, F32), 1e-6)
+    ref = oracle.msar_phase2(o1.astype(np.float64), lse[0].astype(np.float32).astype(np.float64), p, ks, cw, q[0], g,
+                             1e-6, mg, mw, 1e-6)
+    check_out(out, ref, dtype, np.abs(cached).max() * 3, strict=dtype == F32)
+
+
 # --------------------------------------------------------------- hygiene
 
 def test_outputs_stay_inside_their_buffers():
