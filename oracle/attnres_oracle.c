@@ -694,6 +694,71 @@ int oracle_msar_ps(const double *src, int64_t n_src, int64_t T, int64_t d, int64
     return rc;
 }
 
+/* Backward of the H^pre mixer (msar_mix) for one token, [MSAR 무엇과 다른가]:
+ *   dc_r   = dh . Z^(r);  dl_o = dc_o c_o (1 - c_o)     (c = sigmoid(l))
+ *   dzn    = sum_o dl_o P[:, o];  dP[:, o] += dl_o zn;  dmix_gain += dzn * zf / nu
+ *   dzf    = mg * dzn / nu - zf (sum_k mg_k dzn_k zf_k) / (m d nu^3)   (RMSNorm over m d)
+ *   dZ^(r) = c_r dh + dzf[r d .. (r+1) d)
+ * Z^(r) of the token at Zt + r * zstride, dZ^(r) written at dZt + r * dzstride;
+ * dmix_gain and dmix_w are added into; zf, zn, dzn [m d] and c, dl [m] are
+ * scratch. */
+static void msar_mix_bwd_token(const double *Zt, size_t zstride, const double *ht, int64_t m, int64_t d,
+                               const double *mix_gain, const double *mix_w, double mix_eps, double *zf, double *zn,
+                               double *dzn, double *c, double *dl, double *dZt, size_t dzstride, double *dmix_gain,
+                               double *dmix_w)
+{
+    const size_t md = (size_t)m * (size_t)d;
+    for (int64_t r = 0; r < m; ++r)
+        for (int64_t k = 0; k < d; ++k) zf[r * d + k] = Zt[(size_t)r * zstride + (size_t)k];
+    double ms = 0.0;
+    for (size_t k = 0; k < md; ++k) ms += zf[k] * zf[k];
+    const double nu = sqrt(ms / (double)md + mix_eps);
+    for (size_t k = 0; k < md; ++k) zn[k] = nu > 0.0 ? (mix_gain ? mix_gain[k] : 1.0) * zf[k] / nu : 0.0;
+    for (int64_t o = 0; o < m; ++o) {
+        double acc = 0.0;
+        for (size_t k = 0; k < md; ++k) acc += zn[k] * mix_w[k * m + o];
+        c[o] = 1.0 / (1.0 + exp(-acc));
+        double dc = 0.0;
+        for (int64_t k = 0; k < d; ++k) dc += ht[k] * zf[o * d + k];
+        dl[o] = dc * c[o] * (1.0 - c[o]);
+    }
+    double s = 0.0;
+    for (size_t k = 0; k < md; ++k) {
+        double acc = 0.0;
+        for (int64_t o = 0; o < m; ++o) {
+            acc += dl[o] * mix_w[k * m + o];
+            dmix_w[k * m + o] += dl[o] * zn[k];
+        }
+        dzn[k] = acc;
+        if (nu > 0.0) dmix_gain[k] += acc * zf[k] / nu;
+        s += (mix_gain ? mix_gain[k] : 1.0) * acc * zf[k];
+    }
+    for (int64_t r = 0; r < m; ++r)
+        for (int64_t k = 0; k < d; ++k) {
+            const size_t kk = (size_t)r * (size_t)d + (size_t)k;
+            double dzf = 0.0;
+            if (nu > 0.0)
+                dzf = (mix_gain ? mix_gain[kk] : 1.0) * dzn[kk] / nu - zf[kk] * s / ((double)md * nu * nu * nu);
+            dZt[(size_t)r * dzstride + (size_t)k] = c[r] * ht[k] + dzf;
+        }
+}
+
+/* Transpose of one causal depthwise conv (oracle_msar_conv) of source v with
+ * kernel cw [d][kr]: for u[t][c] = sum_j cw[c][j] v[t-j][c] and its gradient
+ * dui, dv[t-j][c] += cw[c][j] dui[t][c] and dcw[c][j] += dui[t][c] v[t-j][c]
+ * (both added into). */
+static void conv_transpose(const double *v, const double *dui, int64_t T, int64_t d, int64_t kr,
+                           const double *cw, double *dv, double *dcw)
+{
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = 0; k < d; ++k)
+            for (int64_t j = 0; j < kr; ++j)
+                if (t - j >= 0) {
+                    dv[(t - j) * d + k] += cw[k * kr + j] * dui[t * d + k];
+                    dcw[k * kr + j] += dui[t * d + k] * v[(t - j) * d + k];
+                }
+}
+
 /* Backward of the MSAR read (oracle_msar) for an output gradient dh[T][d].
  * The forward is taken apart as in oracle_msar: streams u_i^(r), per-stream
  * reads Z^(r) (read_one), and the H^pre mixer.  Chain rule, per token:
@@ -757,42 +822,9 @@ static int msar_bwd_impl(const double *src, int64_t n_src, int64_t T, int64_t d,
         }
     }
     /* mixer backward, per token */
-    for (int64_t t = 0; t < T && rc == 0; ++t) {
-        const double *ht = dh + t * d;
-        for (int64_t r = 0; r < m; ++r)
-            for (int64_t k = 0; k < d; ++k) zf[r * d + k] = Z[(size_t)r * per + (size_t)t * (size_t)d + k];
-        double ms = 0.0;
-        for (size_t k = 0; k < md; ++k) ms += zf[k] * zf[k];
-        const double nu = sqrt(ms / (double)md + mix_eps);
-        for (size_t k = 0; k < md; ++k) zn[k] = nu > 0.0 ? (mix_gain ? mix_gain[k] : 1.0) * zf[k] / nu : 0.0;
-        for (int64_t o = 0; o < m; ++o) {
-            double acc = 0.0;
-            for (size_t k = 0; k < md; ++k) acc += zn[k] * mix_w[k * m + o];
-            c[o] = 1.0 / (1.0 + exp(-acc));
-            double dc = 0.0;
-            for (int64_t k = 0; k < d; ++k) dc += ht[k] * zf[o * d + k];
-            dl[o] = dc * c[o] * (1.0 - c[o]);
-        }
-        double s = 0.0;
-        for (size_t k = 0; k < md; ++k) {
-            double acc = 0.0;
-            for (int64_t o = 0; o < m; ++o) {
-                acc += dl[o] * mix_w[k * m + o];
-                dmix_w[k * m + o] += dl[o] * zn[k];
-            }
-            dzn[k] = acc;
-            if (nu > 0.0) dmix_gain[k] += acc * zf[k] / nu;
-            s += (mix_gain ? mix_gain[k] : 1.0) * acc * zf[k];
-        }
-        for (int64_t r = 0; r < m; ++r)
-            for (int64_t k = 0; k < d; ++k) {
-                const size_t kk = (size_t)r * (size_t)d + (size_t)k;
-                double dzf = 0.0;
-                if (nu > 0.0)
-                    dzf = (mix_gain ? mix_gain[kk] : 1.0) * dzn[kk] / nu - zf[kk] * s / ((double)md * nu * nu * nu);
-                dZ[(size_t)r * per + (size_t)t * (size_t)d + k] = c[r] * ht[k] + dzf;
-            }
-    }
+    for (int64_t t = 0; t < T && rc == 0; ++t)
+        msar_mix_bwd_token(Z + (size_t)t * (size_t)d, per, dh + t * d, m, d, mix_gain, mix_w, mix_eps, zf, zn, dzn,
+                           c, dl, dZ + (size_t)t * (size_t)d, per, dmix_gain, dmix_w);
     /* per-stream read backward, then back through the streams */
     for (int64_t r = 0, off = 0; r < m && rc == 0; ++r) {
         rc = oracle_read_bwd(u + (size_t)r * (size_t)n_src * per, n_src, T, d, queries + r * d, 1, gain, eps,
@@ -807,16 +839,7 @@ static int msar_bwd_impl(const double *src, int64_t n_src, int64_t T, int64_t d,
         for (int64_t i = 0; i < n_src; ++i) {
             const double *cw = conv_w + i * conv_src_stride + off;
             double *dcw = dconv_w + i * conv_src_stride + off;
-            const double *v = src + (size_t)i * per;
-            const double *dui = du + (size_t)i * per;
-            double *dv = dsrc + (size_t)i * per;
-            for (int64_t t = 0; t < T; ++t)
-                for (int64_t k = 0; k < d; ++k)
-                    for (int64_t j = 0; j < kr; ++j)
-                        if (t - j >= 0) {
-                            dv[(t - j) * d + k] += cw[k * kr + j] * dui[t * d + k];
-                            dcw[k * kr + j] += dui[t * d + k] * v[(t - j) * d + k];
-                        }
+            conv_transpose(src + (size_t)i * per, du + (size_t)i * per, T, d, kr, cw, dsrc + (size_t)i * per, dcw);
         }
         off += d * kr;
     }
@@ -929,5 +952,150 @@ int oracle_msar_phase2(const double *o, const double *lse, const double *partial
         msar_mix(Z, m, d, mix_gain, mix_w, mix_eps, zf, logit, out + t * d, NULL);
     }
     free(up); free(Z); free(zf); free(logit); free(tmp);
+    return rc;
+}
+
+
+/* Backward of MSAR phase 2 for one layer (oracle_msar_phase2) for an output
+ * gradient dh[T][d], by the chain rule through its three steps: the partial's
+ * streams (msar_expand), each stream's merge into its phase-1 state
+ * ([Summary §3 Inference, Phase 2]; backward as oracle_block_phase2_bwd, the
+ * stream being the merge's partial and w^(r) its query), and the H^pre mixer
+ * over the merged states (msar_mix_bwd_token).  The partial's streams go back
+ * through the causal convolutions (conv_transpose).
+ * Outputs: d_o[m][T][d], d_lse[m][T], d_partial[T][d] (when partial != NULL),
+ * dconv_w (packed as conv_w; the partial's share, zero without a partial),
+ * dquery[m][d] and dgain[d] (the merges' shares), dmix_gain[m*d],
+ * dmix_w[m*d][m].  partial == NULL: Z^(r) = o^(r), so d_o = dZ and
+ * d_lse = 0. */
+int oracle_msar_phase2_bwd(const double *o, const double *lse, const double *partial, int64_t T, int64_t d,
+                           int64_t m, const int32_t *ksizes, const double *conv_w, const double *query,
+                           const double *gain, double eps, const double *mix_gain, const double *mix_w,
+                           double mix_eps, const double *dh, double *d_o, double *d_lse, double *d_partial,
+                           double *dconv_w, double *dquery, double *dgain, double *dmix_gain, double *dmix_w)
+{
+    if (!o || !lse || !ksizes || !conv_w || !query || !mix_w || !dh || !d_o || !d_lse || !dconv_w || !dquery ||
+        !dgain || !dmix_gain || !dmix_w || T < 0 || d < 1 || m < 1 || eps < 0 || mix_eps < 0)
+        return -1;
+    if (partial && !d_partial) return -1;
+    const size_t per = (size_t)T * (size_t)d, md = (size_t)m * (size_t)d;
+    int64_t ktot = 0;
+    for (int64_t r = 0; r + 1 < m; ++r) ktot += ksizes[r];
+    double *up = partial ? (double *)malloc(sizeof(double) * (size_t)m * per + 1) : NULL;     /* [r][T][d] */
+    double *Z = (double *)malloc(sizeof(double) * md * (size_t)T + 1);                       /* [r][T][d] */
+    double *dZ = (double *)malloc(sizeof(double) * md * (size_t)T + 1);
+    double *dup = (double *)malloc(sizeof(double) * per + 1);
+    double *dqr = (double *)malloc(sizeof(double) * (size_t)d);
+    double *dgr = (double *)malloc(sizeof(double) * (size_t)d);
+    double *zf = (double *)malloc(sizeof(double) * md + 1);
+    double *zn = (double *)malloc(sizeof(double) * md + 1);
+    double *dzn = (double *)malloc(sizeof(double) * md + 1);
+    double *c = (double *)malloc(sizeof(double) * (size_t)m);
+    double *dl = (double *)malloc(sizeof(double) * (size_t)m);
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+    int rc = (Z && dZ && dup && dqr && dgr && zf && zn && dzn && c && dl && tmp && (!partial || up)) ? 0 : -1;
+    for (int64_t k = 0; rc == 0 && k < d * ktot; ++k) dconv_w[k] = 0.0;
+    for (size_t k = 0; rc == 0 && k < md; ++k) {
+        dquery[k] = 0.0;
+        dmix_gain[k] = 0.0;
+        for (int64_t q = 0; q < m; ++q) dmix_w[k * m + q] = 0.0;
+    }
+    for (int64_t k = 0; rc == 0 && k < d; ++k) dgain[k] = 0.0;
+    for (size_t k = 0; rc == 0 && partial && k < per; ++k) d_partial[k] = 0.0;
+    /* forward: the partial's streams and the merged states */
+    if (rc == 0 && partial) rc = msar_expand(partial, T, d, m, ksizes, conv_w, up);
+    for (int64_t r = 0; r < m && rc == 0; ++r)
+        for (int64_t t = 0; t < T; ++t) {
+            const double *orow = o + (size_t)r * per + (size_t)t * (size_t)d;
+            double *zr = Z + (size_t)r * per + (size_t)t * (size_t)d;
+            if (!partial) { for (int64_t k = 0; k < d; ++k) zr[k] = orow[k]; continue; }
+            const double *prow = up + (size_t)r * per + (size_t)t * (size_t)d;
+            const double l = lse[r * T + t];
+            const double sp = score(query + r * d, prow, gain, d, eps, tmp);
+            const double M = l > sp ? l : sp;
+            const double a = exp(l - M), b = exp(sp - M);
+            for (int64_t k = 0; k < d; ++k) zr[k] = (a * orow[k] + b * prow[k]) / (a + b);
+        }
+    /* mixer backward, per token */
+    for (int64_t t = 0; t < T && rc == 0; ++t)
+        msar_mix_bwd_token(Z + (size_t)t * (size_t)d, per, dh + t * d, m, d, mix_gain, mix_w, mix_eps, zf, zn, dzn,
+                           c, dl, dZ + (size_t)t * (size_t)d, per, dmix_gain, dmix_w);
+    /* each stream's merge backward, then the partial's streams back through the convolutions */
+    for (int64_t r = 0, off = 0; r < m && rc == 0; ++r) {
+        rc = oracle_block_phase2_bwd(o + (size_t)r * per, lse + r * T, partial ? up + (size_t)r * per : NULL, T, d,
+                                     query + r * d, gain, eps, dZ + (size_t)r * per, d_o + (size_t)r * per,
+                                     d_lse + r * T, partial ? dup : NULL, dqr, dgr);
+        if (rc) break;
+        for (int64_t k = 0; k < d; ++k) { dquery[r * d + k] = dqr[k]; dgain[k] += dgr[k]; }
+        if (!partial) continue;
+        if (r == 0) {
+            for (size_t k = 0; k < per; ++k) d_partial[k] += dup[k];
+            continue;
+        }
+        const int64_t kr = ksizes[r - 1];
+        conv_transpose(partial, dup, T, d, kr, conv_w + off, d_partial, dconv_w + off);
+        off += d * kr;
+    }
+    free(up); free(Z); free(dZ); free(dup); free(dqr); free(dgr); free(zf); free(zn); free(dzn); free(c); free(dl);
+    free(tmp);
+    return rc;
+}
+
+/* Backward of MSAR phase 1 (oracle_msar_phase1) for gradients d_o[S][m][T][d]
+ * and d_lse[S][m][T] of its state: for each stream r, the read of the cached
+ * sources' streams u_i^(r) by the S layers' queries w_s^(r) is differentiated
+ * with its lse (oracle_read_bwd_lse), and the streams go back through the
+ * causal convolutions (conv_transpose).
+ * Outputs: dsrc[n_src][T][d], dconv_w (packed as conv_w), dqueries[S][m][d],
+ * dgain[d]. */
+int oracle_msar_phase1_bwd(const double *src, int64_t n_src, int64_t T, int64_t d, int64_t m,
+                           const int32_t *ksizes, const double *conv_w, const double *queries, int64_t S,
+                           const double *gain, double eps, const double *d_o, const double *d_lse, double *dsrc,
+                           double *dconv_w, double *dqueries, double *dgain)
+{
+    if (!src || !ksizes || !conv_w || !queries || !d_o || !d_lse || !dsrc || !dconv_w || !dqueries || !dgain ||
+        n_src < 1 || T < 0 || d < 1 || m < 1 || S < 1 || eps < 0)
+        return -1;
+    const size_t per = (size_t)T * (size_t)d;
+    int64_t ktot = 0;
+    for (int64_t r = 0; r + 1 < m; ++r) ktot += ksizes[r];
+    double *ue = (double *)malloc(sizeof(double) * (size_t)n_src * (size_t)m * per + 1);   /* [i][r][T][d] */
+    double *ur = (double *)malloc(sizeof(double) * (size_t)n_src * per + 1);               /* [i][T][d] */
+    double *du = (double *)malloc(sizeof(double) * (size_t)n_src * per + 1);
+    double *qr = (double *)malloc(sizeof(double) * (size_t)S * (size_t)d);
+    double *dor = (double *)malloc(sizeof(double) * (size_t)S * per + 1);
+    double *dlr = (double *)malloc(sizeof(double) * (size_t)S * (size_t)T + 1);
+    double *dqr = (double *)malloc(sizeof(double) * (size_t)S * (size_t)d);
+    double *dgr = (double *)malloc(sizeof(double) * (size_t)d);
+    int rc = (ue && ur && du && qr && dor && dlr && dqr && dgr) ? 0 : -1;
+    for (size_t k = 0; rc == 0 && k < (size_t)n_src * per; ++k) dsrc[k] = 0.0;
+    for (int64_t k = 0; rc == 0 && k < d * ktot; ++k) dconv_w[k] = 0.0;
+    for (int64_t k = 0; rc == 0 && k < d; ++k) dgain[k] = 0.0;
+    for (int64_t i = 0; i < n_src && rc == 0; ++i)
+        rc = msar_expand(src + (size_t)i * per, T, d, m, ksizes, conv_w, ue + (size_t)i * (size_t)m * per);
+    for (int64_t r = 0, off = 0; r < m && rc == 0; ++r) {
+        for (int64_t i = 0; i < n_src; ++i)
+            memcpy(ur + (size_t)i * per, ue + ((size_t)i * (size_t)m + (size_t)r) * per, sizeof(double) * per);
+        for (int64_t sl = 0; sl < S; ++sl) {
+            memcpy(qr + sl * d, queries + (sl * m + r) * d, sizeof(double) * (size_t)d);
+            memcpy(dor + (size_t)sl * per, d_o + ((size_t)sl * (size_t)m + (size_t)r) * per, sizeof(double) * per);
+            memcpy(dlr + sl * T, d_lse + (sl * m + r) * T, sizeof(double) * (size_t)T);
+        }
+        rc = oracle_read_bwd_lse(ur, n_src, T, d, qr, S, gain, eps, dor, dlr, du, dqr, dgr);
+        if (rc) break;
+        for (int64_t sl = 0; sl < S; ++sl)
+            memcpy(dqueries + (sl * m + r) * d, dqr + sl * d, sizeof(double) * (size_t)d);
+        for (int64_t k = 0; k < d; ++k) dgain[k] += dgr[k];
+        if (r == 0) {
+            for (size_t k = 0; k < (size_t)n_src * per; ++k) dsrc[k] += du[k];
+            continue;
+        }
+        const int64_t kr = ksizes[r - 1];
+        for (int64_t i = 0; i < n_src; ++i)
+            conv_transpose(src + (size_t)i * per, du + (size_t)i * per, T, d, kr, conv_w + off, dsrc + (size_t)i * per,
+                           dconv_w + off);
+        off += d * kr;
+    }
+    free(ue); free(ur); free(du); free(qr); free(dor); free(dlr); free(dqr); free(dgr);
     return rc;
 }

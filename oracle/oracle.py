@@ -75,6 +75,10 @@ def _load():
                                            _D, ctypes.c_double, _D, _D, _D, _D, _D, _D, _D]
         lib.oracle_msar_phase1.argtypes = [_D, _I64, _I64, _I64, _I64, _K, _D, _D, _I64, _D, ctypes.c_double,
                                            _D, _D]
+        lib.oracle_msar_phase2_bwd.argtypes = [_D, _D, _D, _I64, _I64, _I64, _K, _D, _D, _D, ctypes.c_double, _D, _D,
+                                               ctypes.c_double, _D, _D, _D, _D, _D, _D, _D, _D, _D]
+        lib.oracle_msar_phase1_bwd.argtypes = [_D, _I64, _I64, _I64, _I64, _K, _D, _D, _I64, _D, ctypes.c_double,
+                                               _D, _D, _D, _D, _D, _D]
         lib.oracle_msar_phase2.argtypes = [_D, _D, _D, _I64, _I64, _I64, _K, _D, _D, _D, ctypes.c_double, _D, _D,
                                            ctypes.c_double, _D]
         for f in ("oracle_full", "oracle_weighted_sum", "oracle_block_oneshot",
@@ -82,7 +86,7 @@ def _load():
                   "oracle_mhar_phase2", "oracle_read_bwd", "oracle_read_bwd_lse", "oracle_block_phase2_bwd",
                   "oracle_mhar_bwd", "oracle_mhar",
                   "oracle_msar_conv", "oracle_msar", "oracle_msar_bwd", "oracle_msar_ps", "oracle_msar_ps_bwd", "oracle_msar_phase1",
-                  "oracle_msar_phase2"):
+                  "oracle_msar_phase2", "oracle_msar_phase2_bwd", "oracle_msar_phase1_bwd"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -402,3 +406,38 @@ def msar_bwd(src, ksizes, conv_w, queries, dh, gain=None, eps=1e-6, mix_gain=Non
                                    float(mix_eps), _p(dh), _p(dsrc), _p(dcw), _p(dq), _p(dg), _p(dmg), _p(dmw)),
            "oracle_msar_bwd")
     return dsrc, dcw, dq, dg, dmg, dmw
+
+
+def msar_phase2_bwd(o, lse, partial, ksizes, conv_w, query, dh, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                    mix_eps=1e-6):
+    """Backward of msar_phase2 for dh [T,d] -> (d_o [m,T,d], d_lse [m,T],
+    d_partial [T,d] or None, dconv_w, dquery [m,d], dgain [d], dmix_gain
+    [m*d], dmix_w [m*d,m])."""
+    o, lse, partial, conv_w, query, dh = _f64(o), _f64(lse), _f64(partial), _f64(conv_w), _f64(query), _f64(dh)
+    gain, mix_gain, mix_w = _f64(gain), _f64(mix_gain), _f64(mix_w)
+    m, T, d = o.shape
+    ks = np.ascontiguousarray(ksizes, dtype=np.int32)
+    d_o, d_lse = np.empty((m, T, d)), np.empty((m, T))
+    d_p = np.empty((T, d)) if partial is not None else None
+    dcw, dq, dg = np.empty(conv_w.shape), np.empty((m, d)), np.empty(d)
+    dmg, dmw = np.empty(m * d), np.empty((m * d, m))
+    _check(_load().oracle_msar_phase2_bwd(_p(o), _p(lse), _p(partial), T, d, m,
+                                          ks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _p(conv_w), _p(query),
+                                          _p(gain), float(eps), _p(mix_gain), _p(mix_w), float(mix_eps), _p(dh),
+                                          _p(d_o), _p(d_lse), _p(d_p), _p(dcw), _p(dq), _p(dg), _p(dmg), _p(dmw)),
+           "oracle_msar_phase2_bwd")
+    return d_o, d_lse, d_p, dcw, dq, dg, dmg, dmw
+
+
+def msar_phase1_bwd(src, ksizes, conv_w, queries, d_o, d_lse, gain=None, eps=1e-6):
+    """Backward of msar_phase1 for d_o [S,m,T,d], d_lse [S,m,T] -> (dsrc
+    [n_src,T,d], dconv_w, dqueries [S,m,d], dgain [d])."""
+    src, conv_w, queries, d_o, d_lse, gain = _f64(src), _f64(conv_w), _f64(queries), _f64(d_o), _f64(d_lse), _f64(gain)
+    n_src, T, d = src.shape
+    S, m = queries.shape[0], queries.shape[1]
+    ks = np.ascontiguousarray(ksizes, dtype=np.int32)
+    dsrc, dcw, dq, dg = np.empty((n_src, T, d)), np.empty(conv_w.shape), np.empty((S, m, d)), np.empty(d)
+    _check(_load().oracle_msar_phase1_bwd(_p(src), n_src, T, d, m, ks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                          _p(conv_w), _p(queries), S, _p(gain), float(eps), _p(d_o), _p(d_lse),
+                                          _p(dsrc), _p(dcw), _p(dq), _p(dg)), "oracle_msar_phase1_bwd")
+    return dsrc, dcw, dq, dg

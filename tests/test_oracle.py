@@ -827,6 +827,91 @@ def test_msar_ps_bwd_equal_kernels_is_the_shared_backward():
     assert np.allclose(per[1].sum(axis=0), shared[1], atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("with_partial,ks", [(True, (2, 3, 4)), (False, (1, 4, 2)), (True, (1, 2, 3))])
+def test_msar_phase2_bwd_matches_finite_differences(with_partial, ks):
+    """Every gradient of MSAR phase 2 (the state o and lse, the partial, conv
+    kernels, stream queries, gain, mixer gain and projection) against central
+    differences of the (pinned) phase-2 forward oracle."""
+    rng = np.random.default_rng(201 + with_partial + sum(ks))
+    T, d = 6, 4
+    o = _rand(rng, 4, T, d)
+    lse = _rand(rng, 4, T, scale=0.7)
+    p = _rand(rng, T, d, scale=1.3) if with_partial else None
+    cw = _rand(rng, d * sum(ks), scale=0.6)
+    q = _rand(rng, 4, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d)
+    mg = rng.uniform(0.5, 1.5, 4 * d)
+    P = _rand(rng, 4 * d, 4, scale=0.5)
+    dh = _rand(rng, T, d)
+
+    def loss(o_, l_, p_, cw_, q_, g_, mg_, P_):
+        return float((oracle.msar_phase2(o_, l_, p_, ks, cw_, q_, g_, 1e-6, mg_, P_, 1e-6) * dh).sum())
+    got = oracle.msar_phase2_bwd(o, lse, p, ks, cw, q, dh, g, 1e-6, mg, P, 1e-6)
+    ref = _fd(loss, (o, lse, p, cw, q, g, mg, P))
+    for name, x, y in zip(("d_o", "d_lse", "d_partial", "dconv_w", "dquery", "dgain", "dmix_gain", "dmix_w"),
+                          got, ref):
+        if y is None:
+            assert x is None, name
+            continue
+        assert np.abs(x - y).max() <= 2e-6 * max(1.0, np.abs(y).max()), name
+
+
+def test_msar_phase1_bwd_matches_finite_differences():
+    """Every gradient of MSAR phase 1 (sources, conv kernels, every layer's
+    stream queries, gain) for gradients of both its outputs, o and lse,
+    against central differences of the (pinned) phase-1 forward oracle."""
+    rng = np.random.default_rng(207)
+    N, S, T, d, ks = 3, 2, 6, 4, (2, 3, 4)
+    src = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
+    cw = _rand(rng, d * sum(ks), scale=0.6)
+    q = _rand(rng, S, 4, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d)
+    d_o = _rand(rng, S, 4, T, d)
+    d_lse = _rand(rng, S, 4, T)
+
+    def loss(s_, cw_, q_, g_):
+        o, lse = oracle.msar_phase1(s_, ks, cw_, q_, g_, 1e-6)
+        return float((o * d_o).sum() + (lse * d_lse).sum())
+    got = oracle.msar_phase1_bwd(src, ks, cw, q, d_o, d_lse, g, 1e-6)
+    ref = _fd(loss, (src, cw, q, g))
+    for name, x, y in zip(("dsrc", "dconv_w", "dqueries", "dgain"), got, ref):
+        assert np.abs(x - y).max() <= 2e-6 * max(1.0, np.abs(y).max()), name
+
+
+@pytest.mark.parametrize("with_partial", [True, False])
+def test_msar_two_phase_bwd_equals_one_shot_bwd(with_partial):
+    """Phase 2's backward followed by phase 1's equals the backward of the
+    one-shot MSAR read of [cached sources, partial] (first layer: the cached
+    sources alone): the cached sources' and the partial's gradients, and the
+    kernels', queries', gain's and mixer's as the sums of the two phases'."""
+    rng = np.random.default_rng(211 + with_partial)
+    N, T, d, ks = 3, 7, 6, (4, 8, 12)
+    cached = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
+    p = _rand(rng, T, d, scale=1.2)
+    cw = _rand(rng, d * sum(ks), scale=0.4)
+    q = _rand(rng, 4, d, scale=1.5)
+    g = rng.uniform(0.5, 1.5, d)
+    mg = rng.uniform(0.5, 1.5, 4 * d)
+    P = _rand(rng, 4 * d, 4, scale=0.4)
+    dh = _rand(rng, T, d)
+    o, lse = oracle.msar_phase1(cached, ks, cw, q[None], g, 1e-6)
+    d_o, d_lse, d_p, dcw2, dq2, dg2, dmg, dmw = oracle.msar_phase2_bwd(o[0], lse[0], p if with_partial else None, ks,
+                                                                        cw, q, dh, g, 1e-6, mg, P, 1e-6)
+    dsrc, dcw1, dq1, dg1 = oracle.msar_phase1_bwd(cached, ks, cw, q[None], d_o[None], d_lse[None], g, 1e-6)
+    srcs = np.concatenate([cached, p[None]]) if with_partial else cached
+    r_src, r_cw, r_q, r_g, r_mg, r_mw = oracle.msar_bwd(srcs, ks, cw, q, dh, g, 1e-6, mg, P, 1e-6)
+    tol = dict(atol=1e-10, rtol=0)
+    assert np.allclose(dsrc, r_src[:N], **tol)
+    if with_partial:
+        assert np.allclose(d_p, r_src[N], **tol)
+    else:
+        assert d_p is None and np.count_nonzero(d_lse) == 0 and np.count_nonzero(dcw2) == 0
+    assert np.allclose(dcw1 + dcw2, r_cw, **tol)
+    assert np.allclose(dq1[0] + dq2, r_q, **tol)
+    assert np.allclose(dg1 + dg2, r_g, **tol)
+    assert np.allclose(dmg, r_mg, **tol) and np.allclose(dmw, r_mw, **tol)
+
+
 def _msar_block_inputs(rng, N, S, T, d, ks=(4, 8, 12)):
     cached = _rand(rng, N, T, d) * (1 + 0.5 * np.arange(N))[:, None, None]
     parts = _rand(rng, S, T, d)

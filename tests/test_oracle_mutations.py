@@ -60,6 +60,9 @@ MUTANTS = {
                                                 "const double *cw = conv_w + off;")],
     "msar_ps_bwd_kernel_grad_not_per_source": [("double *dcw = dconv_w + i * conv_src_stride + off;",
                                                 "double *dcw = dconv_w + off;")],
+    "msar_phase1_bwd_drops_dlse": [("rc = oracle_read_bwd_lse(ur, n_src, T, d, qr, S, gain, eps, dor, dlr, du, dqr, dgr);",
+                                    "rc = oracle_read_bwd_lse(ur, n_src, T, d, qr, S, gain, eps, dor, NULL, du, dqr, dgr);")],
+    "msar_phase2_bwd_drops_partial_identity_stream": [("for (size_t k = 0; k < per; ++k) d_partial[k] += dup[k];", "")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
