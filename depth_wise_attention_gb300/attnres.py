@@ -71,6 +71,13 @@ _SIGS = {
     "msar_block_phase2_ws": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
                              _vp, _vp, ctypes.c_size_t, _vp],
     "msar_block_phase2_ws_workspace_size": [_i64, _i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+    "msar_block_phase2_bwd": [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
+                              _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "msar_block_phase2_bwd_workspace_size": [_i64, _i64, ctypes.c_int, _i64, _vp, ctypes.POINTER(ctypes.c_size_t)],
+    "msar_block_phase1_bwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _i64, _vp, _f, _vp,
+                              _vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "msar_block_phase1_bwd_workspace_size": [_i64, _i64, _i64, ctypes.c_int, _i64, _vp, _i64,
+                                             ctypes.POINTER(ctypes.c_size_t)],
     "attnres_status_string": [ctypes.c_int],
     "attnres_last_cuda_error": [],
     "attnres_sync_status": [_vp],
@@ -659,3 +666,52 @@ def msar_block_phase2_ws(o, lse, partial, ksizes, conv_w, query, gain=None, eps=
         _p(mix_gain), _p(mix_w), mix_eps, _p(out), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
     return out
+
+
+def msar_block_phase2_bwd(o, lse, partial, ksizes, conv_w, query, dh, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
+                          mix_eps=1e-6, workspace=None, stream=None):
+    """Backward of msar_block_phase2 for dh [T, d] -> (d_o [m,T,d], d_lse
+    [m,T], d_partial [T,d] or None, dconv_w, dquery [m,d], dgain [d],
+    dmix_gain [m*d], dmix_w [m*d,m])."""
+    import torch
+    m, T, d = o.shape
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    dev, f32 = o.device, dict(dtype=torch.float32, device=o.device)
+    d_o = torch.empty_like(o)
+    d_lse = torch.empty((m, T), **f32)
+    d_p = torch.empty_like(partial) if partial is not None else None
+    dcw, dq, dg = torch.empty_like(conv_w, dtype=torch.float32), torch.empty((m, d), **f32), torch.empty((d,), **f32)
+    dmg, dmw = torch.empty((m * d,), **f32), torch.empty((m * d, m), **f32)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check("msar_block_phase2_bwd_workspace_size", load().msar_block_phase2_bwd_workspace_size(
+            T, d, _dt(o), m, ctypes.cast(ks, _vp), ctypes.byref(n)))
+        workspace = torch.empty((max(n.value, 16) + 3) // 4, dtype=torch.float32, device=dev)
+    _check("msar_block_phase2_bwd", load().msar_block_phase2_bwd(
+        _p(o), _p(lse), _p(partial), T, d, _dt(o), m, ctypes.cast(ks, _vp), _p(conv_w), _p(query), _p(gain), eps,
+        _p(mix_gain), _p(mix_w), mix_eps, _p(dh), _p(d_o), _p(d_lse), _p(d_p), _p(dcw), _p(dq), _p(dg), _p(dmg),
+        _p(dmw), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return d_o, d_lse, d_p, dcw, dq, dg, dmg, dmw
+
+
+def msar_block_phase1_bwd(src, ksizes, conv_w, queries, d_o, d_lse, gain=None, eps=1e-6, workspace=None,
+                          stream=None):
+    """Backward of msar_block_phase1 for d_o [S,m,T,d], d_lse [S,m,T] ->
+    (dsrc [n_src,T,d], dconv_w, dqueries [S,m,d], dgain [d])."""
+    import torch
+    n_src, T, d, stride = _src_geometry(src)
+    S, m = queries.shape[0], queries.shape[1]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    dev, f32 = src.device, dict(dtype=torch.float32, device=src.device)
+    dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=dev)
+    dcw, dq, dg = torch.empty_like(conv_w, dtype=torch.float32), torch.empty((S, m, d), **f32), torch.empty((d,), **f32)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check("msar_block_phase1_bwd_workspace_size", load().msar_block_phase1_bwd_workspace_size(
+            n_src, T, d, _dt(src), m, ctypes.cast(ks, _vp), S, ctypes.byref(n)))
+        workspace = torch.empty((max(n.value, 16) + 3) // 4, dtype=torch.float32, device=dev)
+    _check("msar_block_phase1_bwd", load().msar_block_phase1_bwd(
+        _p(src), n_src, stride, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries), S, _p(gain), eps,
+        _p(d_o), _p(d_lse), _p(dsrc), T * d, _p(dcw), _p(dq), _p(dg), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dsrc, dcw, dq, dg

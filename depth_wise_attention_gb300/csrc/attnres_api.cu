@@ -1386,6 +1386,319 @@ attnres_status_t launch_msar_phase2_ws(const void *o, const float *lse, const vo
     return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "msar mixer launch");
 }
 
+// Backward of MSAR's two-phase schedule.  Workspace regions start on 256-byte
+// boundaries; token chunks of the conv transpose and the mixer sums as the
+// one-shot backward's plan.
+struct MsarTwoPhaseBwdPlan {
+    int64_t tc, chunks, tc_s;
+    int nsl;
+    MergeBwdShape mb;
+    ReadBwdShape rb;
+    size_t mb_bytes, rb_bytes;
+    size_t off_u, off_z, off_dz, off_du, off_mb, off_rb, off_dg, off_part, off_e, off_mp, off_a, off_cp;
+    size_t off_q, off_do, off_dl, off_dq, total;
+};
+
+attnres_status_t msar_two_phase_bwd_plan(bool phase2, int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt,
+                                         const int32_t *ksizes, int64_t S, const DeviceInfo *dev,
+                                         MsarTwoPhaseBwdPlan *p) {
+    *p = MsarTwoPhaseBwdPlan{};
+    if (phase2) {
+        if (d % 1024 != 0 || d > 4096) return ATTNRES_ERR_UNSUPPORTED;
+        attnres_status_t st = merge_bwd_shape(T, d, dt, dev, &p->mb);
+        if (st != ATTNRES_OK) return st;
+        p->mb_bytes = merge_bwd_ws_bytes(p->mb, d);
+    } else {
+        if (d % 512 != 0 || d > 4096 || n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+        attnres_status_t st = read_bwd_shape(n_src, d, S, 1, dt, &p->rb);
+        if (st != ATTNRES_OK) return st;
+        p->rb_bytes = read_bwd_ws_bytes(dev->sms, p->rb, d);
+    }
+    p->tc = (T + 63) / 64;
+    if (p->tc < 32) p->tc = 32;
+    p->chunks = T > 0 ? (T + p->tc - 1) / p->tc : 0;
+    p->tc_s = (T + 127) / 128;
+    if (p->tc_s < 32) p->tc_s = 32;
+    p->nsl = (int)(d / 1024);
+    const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
+    const size_t es = esize(dt);
+    const size_t row = (size_t)T * (size_t)d * es;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    const int64_t ns = phase2 ? 1 : n_src;                  // sources expanded: the partial, or the cached ones
+    p->off_u = take(3 * (size_t)ns * row);
+    p->off_du = take(4 * (size_t)ns * row);
+    p->off_dg = take(4 * (size_t)d * 4);
+    p->off_cp = take((size_t)p->chunks * (size_t)ns * (size_t)ktot * (size_t)d * 4);
+    if (phase2) {
+        p->off_z = take(4 * row);
+        p->off_dz = take(4 * row);
+        p->off_mb = take(p->mb_bytes);
+        p->off_part = take((size_t)T * (size_t)p->nsl * 9 * 4);
+        p->off_e = take((size_t)T * 4 * 4);
+        p->off_mp = take((size_t)p->chunks * 16 * (size_t)d * 4);
+        p->off_a = take(16 * (size_t)d * 4);
+    } else {
+        p->off_rb = take(p->rb_bytes);
+        p->off_q = take((size_t)4 * (size_t)S * (size_t)d * 4);
+        p->off_do = take((size_t)S * row);
+        p->off_dl = take((size_t)S * (size_t)T * 4);
+        p->off_dq = take((size_t)S * (size_t)d * 4);
+    }
+    p->total = off;
+    return ATTNRES_OK;
+}
+
+// the conv transpose of ns sources' stream gradients (du [4][ns][T][d]) into
+// dsrc and dconv_w (one kernel set), and dgain from the streams' shares
+attnres_status_t msar_conv_back(const void *src, int64_t ns, int64_t src_stride, int64_t T, int64_t d,
+                                attnres_dtype_t dt, const int32_t *ksizes, const float *conv_w,
+                                const MsarTwoPhaseBwdPlan &p, unsigned char *w, void *dsrc, int64_t dsrc_stride,
+                                float *dconv_w, float *dgain, void *stream) {
+    MsarBwdArgs a{};
+    const size_t es = esize(dt);
+    a.src = static_cast<const unsigned char *>(src);
+    a.src_stride_bytes = src_stride * (int64_t)es;
+    a.n_src = (int)ns;
+    a.T = T;
+    a.d = (int)d;
+    for (int r = 0; r < 3; ++r) a.k[r] = ksizes[r];
+    a.ktot = ksizes[0] + ksizes[1] + ksizes[2];
+    a.conv_w = conv_w;
+    a.tc = p.tc;
+    a.du = w + p.off_du;
+    a.dsrc = static_cast<unsigned char *>(dsrc);
+    a.dsrc_stride_bytes = dsrc_stride * (int64_t)es;
+    a.conv_parts = reinterpret_cast<float *>(w + p.off_cp);
+    const int dti = dt == ATTNRES_BF16 ? 1 : 0;
+    cudaError_t e = msar_bwd_conv(dti, a, stream);
+    if (e == cudaSuccess) e = msar_bwd_conv_sum(a, a.conv_parts, p.chunks * ns, (int64_t)a.ktot * d, dconv_w, stream);
+    if (e == cudaSuccess && dgain)
+        e = msar_bwd_sum(reinterpret_cast<const float *>(w + p.off_dg), 4, d, dgain, 0, stream);
+    return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "msar conv transpose launch");
+}
+
+attnres_status_t launch_msar_phase2_bwd(const void *o, const float *lse, const void *partial, int64_t T, int64_t d,
+                                        attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                        const float *query, const float *gain, float eps, const float *mix_gain,
+                                        const float *mix_w, float mix_eps, const void *dh, void *d_o, float *d_lse,
+                                        void *d_partial, float *dconv_w, float *dquery, float *dgain,
+                                        float *dmix_gain, float *dmix_w, void *ws, size_t ws_bytes, void *stream) {
+    if (dt != ATTNRES_F32 && dt != ATTNRES_BF16) return ATTNRES_ERR_INVALID_ARG;
+    if (T < 0 || d < 1 || !(eps >= 0.f) || std::isinf(eps) || !(mix_eps >= 0.f) || std::isinf(mix_eps))
+        return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && d > INT64_MAX / (4 * T)) return ATTNRES_ERR_INVALID_ARG;
+    attnres_status_t st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    if (!conv_w || !query || !mix_w || !dconv_w || !dquery || !dmix_w) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!o || !lse || !dh || !d_o || !d_lse || !ws || (partial && !d_partial)))
+        return ATTNRES_ERR_INVALID_ARG;
+    const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
+    const size_t es = esize(dt);
+    const size_t row = (size_t)T * (size_t)d * es, lrow = (size_t)T * 4;
+    const size_t md = 4 * (size_t)d;
+    if (T > 0) {
+        // outputs against the inputs and one another; the workspace against everything
+        const void *in[4] = {o, lse, partial, dh};
+        const size_t inb[4] = {4 * row, 4 * lrow, row, row};
+        const void *outp[3] = {d_o, d_lse, d_partial};
+        const size_t outb[3] = {4 * row, 4 * lrow, row};
+        for (int x = 0; x < 3; ++x) {
+            if (!outp[x]) continue;
+            for (int y = 0; y < 4; ++y)
+                if (in[y] && overlap(outp[x], outb[x], in[y], inb[y])) return ATTNRES_ERR_INVALID_ARG;
+            for (int y = x + 1; y < 3; ++y)
+                if (outp[y] && overlap(outp[x], outb[x], outp[y], outb[y])) return ATTNRES_ERR_INVALID_ARG;
+            if (overlap(outp[x], outb[x], ws, ws_bytes)) return ATTNRES_ERR_INVALID_ARG;
+        }
+        for (int y = 0; y < 4; ++y)
+            if (in[y] && overlap(in[y], inb[y], ws, ws_bytes)) return ATTNRES_ERR_INVALID_ARG;
+    }
+    const void *pg[5] = {dconv_w, dquery, dgain, dmix_gain, dmix_w};
+    const size_t pn[5] = {(size_t)ktot * (size_t)d * 4, md * 4, (size_t)d * 4, md * 4, md * 16};
+    for (int x = 0; x < 5; ++x) {
+        if (!pg[x]) continue;
+        if (T > 0 && overlap(pg[x], pn[x], ws, ws_bytes)) return ATTNRES_ERR_INVALID_ARG;
+        for (int y = x + 1; y < 5; ++y)
+            if (pg[y] && overlap(pg[x], pn[x], pg[y], pn[y])) return ATTNRES_ERR_INVALID_ARG;
+    }
+    if (d % 1024 != 0 || d > 4096) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned16(conv_w) || !aligned16(query) || !aligned16(mix_w) || (gain && !aligned16(gain)) ||
+        (mix_gain && !aligned16(mix_gain)) || !aligned16(dmix_w) || !aligned4(dconv_w) || !aligned16(dquery) ||
+        (dgain && !aligned4(dgain)) || (dmix_gain && !aligned4(dmix_gain)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    if (T > 0 && (!aligned16(o) || !aligned4(lse) || (partial && !aligned16(partial)) || !aligned16(dh) ||
+                  !aligned16(d_o) || !aligned4(d_lse) || (d_partial && !aligned16(d_partial)) || !aligned16(ws)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarTwoPhaseBwdPlan p;
+    st = msar_two_phase_bwd_plan(true, 1, T, d, dt, ksizes, 0, dev, &p);
+    if (st != ATTNRES_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaSuccess;
+        for (int x = 0; x < 5 && e == cudaSuccess; ++x)
+            if (pg[x]) e = cudaMemsetAsync(const_cast<void *>(pg[x]), 0, pn[x], s);
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const int dti = dt == ATTNRES_BF16 ? 1 : 0;
+    // forward again: the partial's streams and the merged states
+    const unsigned char *z = static_cast<const unsigned char *>(o);
+    if (partial) {
+        st = msar_write_streams(partial, 1, T * d, T, d, dt, ksizes, conv_w, 0, p.tc_s, w + p.off_u, stream);
+        if (st != ATTNRES_OK) return st;
+        for (int64_t r = 0; r < 4; ++r) {
+            const void *pr = r == 0 ? partial : static_cast<const void *>(w + p.off_u + (size_t)(r - 1) * row);
+            st = launch_phase2(static_cast<const unsigned char *>(o) + (size_t)r * row, lse + r * T, pr, nullptr,
+                               nullptr, false, T, d, 1, dt, query + r * d, gain, eps, w + p.off_z + (size_t)r * row,
+                               stream);
+            if (st != ATTNRES_OK) return st;
+        }
+        z = w + p.off_z;
+    }
+    // the mixer's backward: dZ (straight into d_o without a partial) and its parameters
+    MsarBwdArgs a{};
+    a.T = T;
+    a.d = (int)d;
+    a.tc = p.tc;
+    a.tc_m = 128;
+    a.nsl = p.nsl;
+    a.z = const_cast<unsigned char *>(z);           // read only
+    a.dz = partial ? w + p.off_dz : static_cast<unsigned char *>(d_o);
+    a.dh = static_cast<const unsigned char *>(dh);
+    a.mix_gain = mix_gain;
+    a.mix_w = mix_w;
+    a.mix_eps = mix_eps;
+    a.mix_part = reinterpret_cast<float *>(w + p.off_part);
+    a.mix_e = reinterpret_cast<float *>(w + p.off_e);
+    a.mix_parts = reinterpret_cast<float *>(w + p.off_mp);
+    a.dmix_w = dmix_w;
+    a.dmix_gain = dmix_gain;
+    cudaError_t e = msar_bwd_mix(dti, a, stream);
+    float *A = reinterpret_cast<float *>(w + p.off_a);
+    if (e == cudaSuccess) e = msar_bwd_sum(a.mix_parts, p.chunks, 16 * (int64_t)d, A, 0, stream);
+    if (e == cudaSuccess) e = msar_bwd_mix_finish(a, A, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "msar mixer backward launch");
+    if (!partial) {
+        // Z = o: the state takes dZ, nothing reaches lse, the queries, the gain or the kernels
+        e = cudaMemsetAsync(d_lse, 0, 4 * lrow, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dquery, 0, md * 4, s);
+        if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dconv_w, 0, (size_t)ktot * (size_t)d * 4, s);
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    // each stream's merge backward, then the partial's streams back through the convolutions
+    float *dg = reinterpret_cast<float *>(w + p.off_dg);
+    for (int64_t r = 0; r < 4; ++r) {
+        const void *pr = r == 0 ? partial : static_cast<const void *>(w + p.off_u + (size_t)(r - 1) * row);
+        st = launch_merge_bwd(static_cast<const unsigned char *>(o) + (size_t)r * row, lse + r * T, pr, T, d, dt,
+                              query + r * d, gain, eps, w + p.off_dz + (size_t)r * row,
+                              static_cast<unsigned char *>(d_o) + (size_t)r * row, d_lse + r * T,
+                              w + p.off_du + (size_t)r * row, 0, dquery + r * d, dg + r * d, w + p.off_mb, p.mb_bytes,
+                              stream);
+        if (st != ATTNRES_OK) return st;
+    }
+    return msar_conv_back(partial, 1, T * d, T, d, dt, ksizes, conv_w, p, w, d_partial, T * d, dconv_w, dgain,
+                          stream);
+}
+
+attnres_status_t launch_msar_phase1_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                        attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                        const float *queries, int64_t S, const float *gain, float eps,
+                                        const void *d_o, const float *d_lse, void *dsrc, int64_t dsrc_stride,
+                                        float *dconv_w, float *dqueries, float *dgain, void *ws, size_t ws_bytes,
+                                        void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (S < 1) return ATTNRES_ERR_INVALID_ARG;
+    st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    if (!conv_w || !queries || !dconv_w || !dqueries) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!d_o || !d_lse || !dsrc || !ws)) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+    const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
+    const size_t es = esize(dt);
+    const size_t row = (size_t)T * (size_t)d * es;
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t dsrc_bytes = ((size_t)(n_src - 1) * (size_t)dsrc_stride + (size_t)T * (size_t)d) * es;
+    const size_t do_bytes = (size_t)S * 4 * row, dl_bytes = (size_t)S * 4 * (size_t)T * 4;
+    if (T > 0 && (overlap(dsrc, dsrc_bytes, src, src_bytes) || overlap(dsrc, dsrc_bytes, d_o, do_bytes) ||
+                  overlap(dsrc, dsrc_bytes, d_lse, dl_bytes) || overlap(ws, ws_bytes, src, src_bytes) ||
+                  overlap(ws, ws_bytes, dsrc, dsrc_bytes) || overlap(ws, ws_bytes, d_o, do_bytes) ||
+                  overlap(ws, ws_bytes, d_lse, dl_bytes)))
+        return ATTNRES_ERR_INVALID_ARG;
+    const void *pg[3] = {dconv_w, dqueries, dgain};
+    const size_t pn[3] = {(size_t)ktot * (size_t)d * 4, (size_t)S * 4 * (size_t)d * 4, (size_t)d * 4};
+    for (int x = 0; x < 3; ++x) {
+        if (!pg[x]) continue;
+        if (T > 0 && overlap(pg[x], pn[x], ws, ws_bytes)) return ATTNRES_ERR_INVALID_ARG;
+        for (int y = x + 1; y < 3; ++y)
+            if (pg[y] && overlap(pg[x], pn[x], pg[y], pn[y])) return ATTNRES_ERR_INVALID_ARG;
+    }
+    if (d % 512 != 0 || d > 4096 || n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
+    if (!aligned4(conv_w) || !aligned16(queries) || (gain && !aligned16(gain)) || !aligned4(dconv_w) ||
+        !aligned4(dqueries) || (dgain && !aligned4(dgain)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    if (T > 0 && (!aligned16(d_o) || !aligned4(d_lse) || !aligned16(dsrc) || (dsrc_stride * (int64_t)es) % 16 != 0 ||
+                  !aligned16(ws)))
+        return ATTNRES_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarTwoPhaseBwdPlan p;
+    st = msar_two_phase_bwd_plan(false, n_src, T, d, dt, ksizes, S, dev, &p);
+    if (st != ATTNRES_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaSuccess;
+        for (int x = 0; x < 3 && e == cudaSuccess; ++x)
+            if (pg[x]) e = cudaMemsetAsync(const_cast<void *>(pg[x]), 0, pn[x], s);
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    st = msar_write_streams(src, n_src, src_stride, T, d, dt, ksizes, conv_w, 0, p.tc_s, w + p.off_u, stream);
+    if (st != ATTNRES_OK) return st;
+    // stream r's queries of every layer, contiguous: qbuf[r][s] = queries[s][r]
+    float *qbuf = reinterpret_cast<float *>(w + p.off_q);
+    cudaError_t e = cudaSuccess;
+    for (int64_t r = 0; r < 4 && e == cudaSuccess; ++r)
+        e = cudaMemcpy2DAsync(qbuf + r * S * d, (size_t)d * 4, queries + r * d, (size_t)4 * d * 4, (size_t)d * 4,
+                              (size_t)S, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync");
+    unsigned char *dobuf = w + p.off_do;
+    float *dlbuf = reinterpret_cast<float *>(w + p.off_dl);
+    float *dqbuf = reinterpret_cast<float *>(w + p.off_dq);
+    float *dg = reinterpret_cast<float *>(w + p.off_dg);
+    for (int64_t r = 0; r < 4; ++r) {
+        // stream r's gradients of every layer, contiguous, then its read's backward
+        e = cudaMemcpy2DAsync(dobuf, row, static_cast<const unsigned char *>(d_o) + (size_t)r * row, 4 * row, row,
+                              (size_t)S, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(dlbuf, (size_t)T * 4, d_lse + r * T, (size_t)4 * T * 4, (size_t)T * 4, (size_t)S,
+                                  cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync");
+        const void *sr = r == 0 ? src : static_cast<const void *>(w + p.off_u + (size_t)(r - 1) * (size_t)n_src * row);
+        st = launch_read_bwd(sr, n_src, r == 0 ? src_stride : T * d, T, d, 1, dt, qbuf + r * S * d, S, gain, eps,
+                             dobuf, dlbuf, w + p.off_du + (size_t)r * (size_t)n_src * row, T * d, 0, dqbuf,
+                             dg + r * d, w + p.off_rb, p.rb_bytes, stream);
+        if (st != ATTNRES_OK) return st;
+        e = cudaMemcpy2DAsync(dqueries + r * d, (size_t)4 * d * 4, dqbuf, (size_t)d * 4, (size_t)d * 4, (size_t)S,
+                              cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync");
+    }
+    return msar_conv_back(src, n_src, src_stride, T, d, dt, ksizes, conv_w, p, w, dsrc, dsrc_stride, dconv_w, dgain,
+                          stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1680,6 +1993,62 @@ attnres_status_t msar_block_phase2_ws(const void *o, const float *lse, const voi
                                       size_t workspace_bytes, void *stream) {
     return launch_msar_phase2_ws(o, lse, partial, T, d, dt, m, ksizes, conv_w, query, gain, eps, mix_gain, mix_w,
                                  mix_eps, out, workspace, workspace_bytes, stream);
+}
+
+attnres_status_t msar_block_phase2_bwd_workspace_size(int64_t T, int64_t d, attnres_dtype_t dt, int64_t m,
+                                                     const int32_t *ksizes, size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || T < 0 || d < 1) return ATTNRES_ERR_INVALID_ARG;
+    attnres_status_t st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarTwoPhaseBwdPlan p;
+    st = msar_two_phase_bwd_plan(true, 1, T, d, dt, ksizes, 0, dev, &p);
+    if (st != ATTNRES_OK) return st;
+    *bytes = p.total;
+    return ATTNRES_OK;
+}
+
+attnres_status_t msar_block_phase2_bwd(const void *o, const float *lse, const void *partial, int64_t T, int64_t d,
+                                       attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                       const float *query, const float *gain, float eps, const float *mix_gain,
+                                       const float *mix_w, float mix_eps, const void *dh, void *d_o, float *d_lse,
+                                       void *d_partial, float *dconv_w, float *dquery, float *dgain,
+                                       float *dmix_gain, float *dmix_w, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+    return launch_msar_phase2_bwd(o, lse, partial, T, d, dt, m, ksizes, conv_w, query, gain, eps, mix_gain, mix_w,
+                                  mix_eps, dh, d_o, d_lse, d_partial, dconv_w, dquery, dgain, dmix_gain, dmix_w,
+                                  workspace, workspace_bytes, stream);
+}
+
+attnres_status_t msar_block_phase1_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt,
+                                                     int64_t m, const int32_t *ksizes, int64_t S, size_t *bytes) {
+    if (!bytes || (dt != ATTNRES_F32 && dt != ATTNRES_BF16) || n_src < 1 || T < 0 || d < 1 || S < 1)
+        return ATTNRES_ERR_INVALID_ARG;
+    attnres_status_t st = check_msar_kernels(m, ksizes);
+    if (st != ATTNRES_OK) return st;
+    if (T > 0 && d > INT64_MAX / T) return ATTNRES_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    MsarTwoPhaseBwdPlan p;
+    st = msar_two_phase_bwd_plan(false, n_src, T, d, dt, ksizes, S, dev, &p);
+    if (st != ATTNRES_OK) return st;
+    *bytes = p.total;
+    return ATTNRES_OK;
+}
+
+attnres_status_t msar_block_phase1_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                       attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
+                                       const float *queries, int64_t S, const float *gain, float eps,
+                                       const void *d_o, const float *d_lse, void *dsrc, int64_t dsrc_stride,
+                                       float *dconv_w, float *dqueries, float *dgain, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
+    return launch_msar_phase1_bwd(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, S, gain, eps, d_o,
+                                  d_lse, dsrc, dsrc_stride, dconv_w, dqueries, dgain, workspace, workspace_bytes,
+                                  stream);
 }
 
 const char *attnres_status_string(attnres_status_t s) {

@@ -630,6 +630,73 @@ attnres_status_t msar_block_phase2_ws(const void *o, const float *lse, const voi
 attnres_status_t msar_block_phase2_ws_workspace_size(int64_t T, int64_t d, attnres_dtype_t dt,
                                                     size_t *bytes);
 
+/*
+ * Backward of msar_block_phase2 (one layer of MSAR's two-phase schedule) for
+ * an output gradient dh.  Defined by the chain rule through phase 2's steps:
+ * the H^pre mixer over the merged streams (as msar_expand_bwd), each stream's
+ * online-softmax merge (b-lab.team summary, section 3, Phase 2; backward as
+ * attnres_block_phase2_bwd, the partial's stream r being that merge's partial
+ * and w^(r) its query), and the partial's causal convolutions (MSAR page,
+ * sections 무엇과 다른가 and 어떻게 쓰나).  Together with msar_block_phase1_bwd
+ * it equals msar_expand_bwd over [cached sources, partial].
+ *   o, lse, partial, T, d, dt, m, ksizes, conv_w, query, gain, eps, mix_gain,
+ *   mix_w, mix_eps   as msar_block_phase2 (the forward's inputs)
+ *   dh         [T][d] dtype dt
+ *   d_o        [m][T][d] dtype dt; d_lse [m][T] float: the gradients of the
+ *              phase-1 state (to msar_block_phase1_bwd); overwritten
+ *   d_partial  [T][d] dtype dt (required with a partial; NULL otherwise)
+ *   dconv_w    float, packed as conv_w: the partial's share (zero without one)
+ *   dquery     [m][d] float: the merges' share; dgain [d] float or NULL (the
+ *              merges' share); dmix_gain [m*d] or NULL, dmix_w [m*d][m]
+ *   workspace  device scratch of msar_block_phase2_bwd_workspace_size bytes
+ * All outputs are overwritten; parameter sums over tokens are in a fixed
+ * order.  Limits: m = 4, kernel sizes 1..16, d = 1024, 2048 or 4096 (else
+ * ATTNRES_ERR_UNSUPPORTED).  Overlapping outputs, or outputs overlapping the
+ * inputs or the workspace, are ATTNRES_ERR_INVALID_ARG.
+ */
+attnres_status_t msar_block_phase2_bwd(const void *o, const float *lse, const void *partial, int64_t T,
+                                       int64_t d, attnres_dtype_t dt, int64_t m,
+                                       const int32_t *ksizes, const float *conv_w, const float *query,
+                                       const float *gain, float eps, const float *mix_gain,
+                                       const float *mix_w, float mix_eps, const void *dh, void *d_o,
+                                       float *d_lse, void *d_partial, float *dconv_w, float *dquery,
+                                       float *dgain, float *dmix_gain, float *dmix_w, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+
+/* Workspace bytes msar_block_phase2_bwd needs for these sizes on the current device. */
+attnres_status_t msar_block_phase2_bwd_workspace_size(int64_t T, int64_t d, attnres_dtype_t dt, int64_t m,
+                                                     const int32_t *ksizes, size_t *bytes);
+
+/*
+ * Backward of msar_block_phase1 for gradients d_o [S][m][T][d] and d_lse
+ * [S][m][T] of its state (the sums of every layer's msar_block_phase2_bwd
+ * d_o and d_lse for the block).  Defined by the chain rule through phase 1:
+ * each stream's read of the cached sources' streams by the S layers' queries,
+ * with its log-sum-exp (attnres_block_phase1_bwd's formula), and the causal
+ * convolutions (MSAR page, section 무엇과 다른가; b-lab.team summary, section 3).
+ *   src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, S, gain,
+ *   eps        as msar_block_phase1
+ *   dsrc       [n_src] x [T][d] dtype dt, dsrc_stride apart; overwritten
+ *   dconv_w    float, packed as conv_w (the cached sources' share)
+ *   dqueries   [S][m][d] float (phase 1's share); dgain [d] float or NULL
+ *   workspace  device scratch of msar_block_phase1_bwd_workspace_size bytes
+ * Limits: m = 4, kernel sizes 1..16, d a multiple of 512 up to 4096, n_src <=
+ * 16 (else ATTNRES_ERR_UNSUPPORTED); errors otherwise as msar_expand_bwd.
+ */
+attnres_status_t msar_block_phase1_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
+                                       int64_t d, attnres_dtype_t dt, int64_t m,
+                                       const int32_t *ksizes, const float *conv_w,
+                                       const float *queries, int64_t S, const float *gain, float eps,
+                                       const void *d_o, const float *d_lse, void *dsrc,
+                                       int64_t dsrc_stride, float *dconv_w, float *dqueries,
+                                       float *dgain, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
+/* Workspace bytes msar_block_phase1_bwd needs for these sizes on the current device. */
+attnres_status_t msar_block_phase1_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d,
+                                                     attnres_dtype_t dt, int64_t m,
+                                                     const int32_t *ksizes, int64_t S, size_t *bytes);
+
 /* Static description of a status code (never NULL). */
 const char *attnres_status_string(attnres_status_t status);
 

@@ -1003,7 +1003,7 @@ int oracle_msar_phase2_bwd(const double *o, const double *lse, const double *par
     for (int64_t k = 0; rc == 0 && k < d; ++k) dgain[k] = 0.0;
     for (size_t k = 0; rc == 0 && partial && k < per; ++k) d_partial[k] = 0.0;
     /* forward: the partial's streams and the merged states */
-    if (rc == 0 && partial) rc = msar_expand(partial, T, d, m, ksizes, conv_w, up);
+    if (partial && rc == 0) rc = msar_expand(partial, T, d, m, ksizes, conv_w, up);
     for (int64_t r = 0; r < m && rc == 0; ++r)
         for (int64_t t = 0; t < T; ++t) {
             const double *orow = o + (size_t)r * per + (size_t)t * (size_t)d;

@@ -390,3 +390,37 @@ def test_msar_phase2_workspace_chain_validation(lib):
     assert p2(d=1536) == UNS
     n = ctypes.c_size_t(0)
     assert lib.msar_block_phase2_ws_workspace_size(T, 1536, BF16, ctypes.byref(n)) == UNS
+
+
+def test_msar_two_phase_backward_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    bad = (ctypes.c_int32 * 3)(4, 0, 12)
+    kp = lambda k: ctypes.cast(k, ctypes.c_void_p)
+    T, d = 16, 1024
+    O, L, P, DH = A, B, A + 0x1000000, A + 0x2000000
+    DO, DL, DP, WS = B + 0x1000000, B + 0x2000000, B + 0x3000000, B + 0x8000000
+    DCW, DQ, DG, DMG, DMW = B + 0x4000000, B + 0x4100000, B + 0x4200000, B + 0x4300000, B + 0x4400000
+
+    def p2(k=ks, part=P, do=DO, dl=DL, dp=DP, ws=WS, d=d, mix_eps=1e-6):
+        return lib.msar_block_phase2_bwd(O, L, part, T, d, BF16, 4, kp(k), B + 0x500000, B + 0x600000, None, 1e-6,
+                                         None, B + 0x700000, mix_eps, DH, do, dl, dp, DCW, DQ, DG, DMG, DMW, ws,
+                                         1 << 30, None)
+    assert p2(k=bad) == INV
+    assert p2(mix_eps=-1.0) == INV
+    assert p2(do=None) == INV
+    assert p2(dp=None) == INV                      # a partial needs its gradient buffer
+    assert p2(ws=None) == INV
+    assert p2(do=O + 64) == INV                    # d_o overlaps the state
+    assert p2(dp=DO + 64) == INV                   # outputs overlap
+    assert p2(d=1536) == UNS
+    assert p2(do=DO + 8) == UNS
+
+    def p1(k=ks, dsrc=B + 0x5000000, ws=WS, d=d, S=4):
+        return lib.msar_block_phase1_bwd(A, 8, T * d, T, d, BF16, 4, kp(k), B + 0x500000, B + 0x600000, S, None,
+                                         1e-6, DO, DL, dsrc, T * d, DCW, DQ, DG, ws, 1 << 30, None)
+    assert p1(k=bad) == INV
+    assert p1(S=0) == INV
+    assert p1(dsrc=None) == INV
+    assert p1(dsrc=A + 64) == INV                  # dsrc overlaps the sources
+    assert p1(ws=DO - 64) == INV                   # workspace overlaps d_o
+    assert p1(d=768) == UNS

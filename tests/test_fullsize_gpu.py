@@ -462,3 +462,46 @@ def test_msar_workspace_chain_T32768_d4096():
                 win = np.concatenate([win, pw[None]])
             ref[j] = oracle.msar(win, ks, cw_h, qs_h[s_], None, 1e-6, None, mw_h, 1e-6)[-1]
         check_out(got, ref, BF16, strict=False, what=f"layer {s_ + 1} through the workspace chains")
+
+
+def test_msar_two_phase_bwd_T32768_d4096():
+    """The backward of one MSAR two-phase layer at the MSAR size (N=8 cached
+    sources, T=32768), phase 2 then phase 1, with dh on three clusters of 4
+    tokens: every gradient against the oracle's one-shot backward of
+    [cached, partial] over the clusters' 15-row causal windows (the backward
+    is linear in dh and a token's read sees rows t-11..t), and the sources'
+    and the partial's gradients exactly zero elsewhere."""
+    T, d, N = 32768, 4096, 8
+    ks = (4, 8, 12)
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=0)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((1, 4, d), (16.0 / d) ** 0.5, g)
+    cw = torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g) for k in ks])
+    mw = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g)
+    part = torch.randn((T, d), generator=g, device="cuda").to(BF16)
+    starts = [0, 12345, T - 4]
+    dh = torch.zeros((T, d), dtype=BF16, device="cuda")
+    for c in starts:
+        dh[c:c + 4] = torch.randn((4, d), generator=g, device="cuda").to(BF16)
+    o, lse = attnres.msar_block_phase1(src, ks, cw, q)
+    d_o, d_l, d_p, dcw2, dq2, dg2, dmg, dmw = attnres.msar_block_phase2_bwd(o[0], lse[0], part, ks, cw, q[0], dh,
+                                                                            None, 1e-6, None, mw, 1e-6)
+    del o, lse
+    dsrc, dcw1, dq1, dg1 = attnres.msar_block_phase1_bwd(src, ks, cw, q, d_o[None], d_l[None])
+    attnres.attnres_sync_status()
+    cw_h, q_h, mw_h = (t.cpu().numpy().astype(np.float64) for t in (cw, q[0], mw))
+    ref_par = None
+    inside = torch.zeros(T, dtype=torch.bool, device="cuda")
+    for c in starts:
+        lo = max(0, c - 11)
+        win = torch.cat([src[:, lo:c + 4], part[None, lo:c + 4]]).float().cpu().numpy().astype(np.float64)
+        dwin = dh[lo:c + 4].float().cpu().numpy().astype(np.float64)
+        r = oracle.msar_bwd(win, ks, cw_h, q_h, dwin, None, 1e-6, None, mw_h, 1e-6)
+        check_out(dsrc[:, lo:c + 4], r[0][:N], BF16, strict=False, what=f"dsrc rows {lo}..{c + 3}")
+        check_out(d_p[lo:c + 4], r[0][N], BF16, strict=False, what=f"d_partial rows {lo}..{c + 3}")
+        inside[lo:c + 4] = True
+        ref_par = list(r[1:]) if ref_par is None else [a + b for a, b in zip(ref_par, r[1:])]
+    assert torch.count_nonzero(dsrc[:, ~inside]) == 0 and torch.count_nonzero(d_p[~inside]) == 0
+    got = (dcw1 + dcw2, dq1[0] + dq2, dg1 + dg2, dmg, dmw)
+    for name, g_, r_ in zip(("dconv_w", "dqueries", "dgain", "dmix_gain", "dmix_w"), got, ref_par):
+        check_out(g_, np.asarray(r_).reshape(tuple(g_.shape)), BF16, strict=False, what=name)

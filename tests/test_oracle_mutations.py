@@ -48,7 +48,8 @@ MUTANTS = {
                                 "double a = exp(l - M), b = exp(M - sp);\n            for (int64_t c = 0; c < d; ++c) zr[c]")],
     "msar_phase2_partial_identity_streams": [("if (rc == 0 && partial) rc = msar_expand(partial, T, d, m, ksizes, conv_w, up);",
                                               "if (rc == 0 && partial) rc = msar_expand(partial, T, d, 1, ksizes, conv_w, up);\n    for (int64_t r = 1; r < m && up; ++r) memcpy(up + (size_t)r * per, partial, sizeof(double) * per);")],
-    "msar_phase2_lse_of_stream_zero": [("const double l = lse[r * T + t];", "const double l = lse[t];")],
+    "msar_phase2_lse_of_stream_zero": [("const double l = lse[r * T + t];\n            double sp = score(",
+                                        "const double l = lse[t];\n            double sp = score(")],
     "msar_ps_first_source_kernels": [("conv_w + i * conv_src_stride,", "conv_w,")],
     "msar_bwd_sigmoid_derivative": [("dl[o] = dc * c[o] * (1.0 - c[o]);", "dl[o] = dc * c[o];")],
     "msar_bwd_mixer_rms_sign": [("/ nu - zf[kk] * s / ((double)md * nu * nu * nu);", "/ nu + zf[kk] * s / ((double)md * nu * nu * nu);")],

@@ -957,6 +957,80 @@ def test_msar_block_phase2_workspace_chain(dtype, T, d, with_partial):
     check_out(out, ref, dtype, np.abs(cached).max() * 3, strict=dtype == F32)
 
 
+# --------------------------------------------------------------- backward of MSAR's two-phase schedule
+
+def _check_all(got, ref, names, dtype, what):
+    for name, g_, r_ in zip(names, got, ref):
+        if r_ is None:
+            assert g_ is None, name
+            continue
+        r_ = np.asarray(r_).reshape(tuple(g_.shape))
+        check_out(g_, r_, dtype, np.abs(r_).max(), strict=False, what=f"{what} {name}")
+
+
+_P2B = ("d_o", "d_lse", "d_partial", "dconv_w", "dquery", "dgain", "dmix_gain", "dmix_w")
+
+
+@pytest.mark.parametrize("dtype,T,d,with_partial", [(BF16, 60, 4096, True), (F32, 45, 1024, True),
+                                                    (BF16, 33, 2048, False), (F32, 130, 1024, True),
+                                                    (F32, 20, 2048, False)])
+def test_msar_block_phase2_bwd(dtype, T, d, with_partial):
+    """Phase 2's backward against the oracle on the same phase-1 state: the
+    state's (o, lse), the partial's, the kernels', the stream queries', the
+    gain's and the mixer's gradients; no partial passes dZ to o."""
+    rng = _rng(T + d + 3 * with_partial)
+    ks = (4, 8, 12)
+    cached, parts, q, cw, mw, g, mg = _msar_block(rng, 4, 1, T, d, dtype, ks)
+    o, lse = oracle.msar_phase1(cached, ks, cw, q, g, 1e-6)
+    o1 = inputs.bf16_round(o[0].astype(np.float32)) if dtype == BF16 else o[0].astype(np.float32)
+    l1 = lse[0].astype(np.float32)
+    p = parts[0] if with_partial else None
+    dh = _sources(rng, 1, T, d, dtype, step=0)[0]
+    got = attnres.msar_block_phase2_bwd(to_dev(o1, dtype), to_dev(l1, F32), to_dev(p, dtype) if with_partial else None,
+                                        ks, to_dev(cw, F32), to_dev(q[0], F32), to_dev(dh, dtype), to_dev(g, F32), 1e-6,
+                                        to_dev(mg, F32), to_dev(mw, F32), 1e-6)
+    ref = oracle.msar_phase2_bwd(o1.astype(np.float64), l1.astype(np.float64), p, ks, cw, q[0], dh, g, 1e-6, mg, mw,
+                                 1e-6)
+    _check_all(got, ref, _P2B, dtype, f"phase 2 T={T} d={d}")
+
+
+@pytest.mark.parametrize("dtype,N,S,T,d", [(BF16, 8, 4, 60, 4096), (F32, 3, 2, 45, 1024), (BF16, 5, 6, 30, 2048),
+                                           (BF16, 12, 3, 20, 512)])
+def test_msar_block_phase1_bwd(dtype, N, S, T, d):
+    """Phase 1's backward against the oracle for gradients of every layer's
+    per-stream o and lse."""
+    rng = _rng(N * 3 + S + T + d)
+    ks = (4, 8, 12)
+    cached, _, q, cw, _, g, _ = _msar_block(rng, N, S, T, d, dtype, ks)
+    d_o = _sources(rng, S * 4, T, d, dtype, step=0).reshape(S, 4, T, d)
+    d_l = rng.standard_normal((S, 4, T)).astype(np.float32)
+    got = attnres.msar_block_phase1_bwd(to_dev(cached, dtype), ks, to_dev(cw, F32), to_dev(q, F32),
+                                        to_dev(d_o, dtype), to_dev(d_l, F32), to_dev(g, F32), 1e-6)
+    ref = oracle.msar_phase1_bwd(cached, ks, cw, q, d_o, d_l, g, 1e-6)
+    _check_all(got, ref, ("dsrc", "dconv_w", "dqueries", "dgain"), dtype, f"phase 1 N={N} S={S} d={d}")
+
+
+@pytest.mark.parametrize("dtype", [BF16, F32])
+def test_msar_two_phase_bwd_chain_equals_one_shot(dtype):
+    """The GPU chain (phase 2's backward of one layer, then phase 1's with its
+    state gradients) against the oracle's backward of the one-shot MSAR read
+    of [cached, partial]: every gradient, the two phases' shares added."""
+    rng = _rng(123)
+    N, T, d, ks = 4, 64, 2048, (4, 8, 12)
+    cached, parts, q, cw, mw, g, mg = _msar_block(rng, N, 1, T, d, dtype, ks)
+    dh = _sources(rng, 1, T, d, dtype, step=0)[0]
+    dv = lambda x: to_dev(x, F32)
+    src_d = to_dev(cached, dtype)
+    o, lse = attnres.msar_block_phase1(src_d, ks, dv(cw), dv(q), dv(g), 1e-6)
+    d_o, d_l, d_p, dcw2, dq2, dg2, dmg, dmw = attnres.msar_block_phase2_bwd(
+        o[0], lse[0], to_dev(parts[0], dtype), ks, dv(cw), dv(q[0]), to_dev(dh, dtype), dv(g), 1e-6, dv(mg), dv(mw),
+        1e-6)
+    dsrc, dcw1, dq1, dg1 = attnres.msar_block_phase1_bwd(src_d, ks, dv(cw), dv(q), d_o[None], d_l[None], dv(g), 1e-6)
+    r = oracle.msar_bwd(np.concatenate([cached, parts[0][None]]), ks, cw, q[0], dh, g, 1e-6, mg, mw, 1e-6)
+    got = (torch.cat([dsrc, d_p[None]]), dcw1 + dcw2, dq1[0] + dq2, dg1 + dg2, dmg, dmw)
+    _check_all(got, r, _MSAR_GRADS, dtype, "two-phase chain")
+
+
 # --------------------------------------------------------------- hygiene
 
 def test_outputs_stay_inside_their_buffers():
