@@ -10,13 +10,14 @@ than L2 (5.6 GB touched per step), so no explicit L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.  Other workloads (--workload mhar|mhar_block|msar|
-msar_block|msar_chunked|msar_ps|msar_ws|msar_block_ws|msar_bwd|msar_bwd_ps|
+msar_block|msar_chunked|msar_ps|msar_ws|msar_block_ws|msar_bwd|msar_bwd_ps|msar_block_bwd|
 full_depth|block_d2048|block_fused|block_bwd|read_bwd|mhar_bwd|decode) are
 for profiling and the design notes.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -1304,6 +1305,114 @@ class MsarBlockWsWorkload(MsarBlockWorkload):
                                          out=self.outs[s_], workspace=self.ws2, stream=stream)
 
 
+class MsarBlockBwdWorkload(MsarBlockWorkload):
+    """Backward of one MSAR two-phase block (N=8 cached sources, S=4 layers,
+    bf16, d=4096, T=32768) for dense output gradients dh ~ N(0, 1) of every
+    layer: phase 2's backward per layer (layers 2..4 with their partials,
+    layer 1 without), then phase 1's backward with the layers' state
+    gradients, as a training step would run it.  The phase-1 state is
+    computed once in setup.  Algorithmic bytes per token: the cached sources,
+    the partials, the state (o, lse), dh read; the sources' and the partials'
+    gradients written."""
+
+    def __init__(self, T=32768, d=4096, N=8, S=4, seed=0):
+        super().__init__(T, d, N, S, seed)
+        self.name = "msar_two_phase_block_backward"
+        b = 2
+        self.bytes_per_token = ((N + (S - 1) + S * 4 + S) * d * b + S * 4 * 4 + (N + (S - 1)) * d * b)
+        self.phase1_bytes_per_token = self.bytes_per_token
+        self.fma_per_token = None
+        # phase 2 with a partial: streams 1, merges 4, mixer 3 + 2 sums, merge backwards 4 x 2, conv 1 + 2 sums;
+        # without: mixer 3 + 2; phase 1: streams 1, 4 read backwards x 2, conv 1 + 2 sums
+        self.launches_per_step = (S - 1) * 21 + 5 + 12
+        self.dominant = "msar two-phase block backward (4 x phase 2 backward + phase 1 backward)"
+        self.dominant_src = "msar_bwd"
+        self.profile_tag = f"ncu_msar_block_bwd_d{d}"
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres
+        super().setup(device)
+        T, d, S, N = self.T, self.d, self.S, self.N
+        attnres.msar_block_phase1(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, o=self.o, lse=self.lse)
+        g = torch.Generator(device=device)
+        g.manual_seed(self.seed + 9)
+        self.dh = torch.randn((S, T, d), generator=g, device=device).to(torch.bfloat16)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.d_o = torch.empty_like(self.o)
+        self.d_lse = torch.empty((S, 4, T), **f32)
+        self.d_p = torch.empty((S, T, d), dtype=torch.bfloat16, device=device)
+        self.p2g = [(torch.empty_like(self.conv_w), torch.empty((4, d), **f32), torch.empty((d,), **f32),
+                     torch.empty((4 * d,), **f32), torch.empty((4 * d, 4), **f32)) for _ in range(S)]
+        self.p1g = (torch.empty_like(self.cache), torch.empty_like(self.conv_w), torch.empty((S, 4, d), **f32),
+                    torch.empty((d,), **f32))
+        ks = (ctypes.c_int32 * 3)(*self.ks)
+        n = ctypes.c_size_t(0)
+        attnres._check("ws", attnres.load().msar_block_phase2_bwd_workspace_size(
+            T, d, 1, 4, ctypes.cast(ks, ctypes.c_void_p), ctypes.byref(n)))
+        self.ws2 = torch.empty(((n.value + 3) // 4,), **f32)
+        attnres._check("ws", attnres.load().msar_block_phase1_bwd_workspace_size(
+            N, T, d, 1, 4, ctypes.cast(ks, ctypes.c_void_p), S, ctypes.byref(n)))
+        self.ws1 = torch.empty(((n.value + 3) // 4,), **f32)
+        self.out = self.p1g[0]
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        if ev is not None:
+            ev[0].record(stream)
+        for s_ in range(self.S):
+            p = self.parts[s_] if s_ > 0 else None
+            outs = (self.d_o[s_], self.d_lse[s_], self.d_p[s_] if s_ > 0 else None) + self.p2g[s_]
+            attnres.msar_block_phase2_bwd(self.o[s_], self.lse[s_], p, self.ks, self.conv_w, self.queries[s_],
+                                          self.dh[s_], None, 1e-6, None, self.mix_w, 1e-6, outs=outs,
+                                          workspace=self.ws2, stream=stream)
+        attnres.msar_block_phase1_bwd(self.cache, self.ks, self.conv_w, self.queries, self.d_o, self.d_lse, None,
+                                      1e-6, outs=self.p1g, workspace=self.ws1, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def setup_host(self):
+        self.h_cache = torch_pinned_like(self.cache)
+        self.h_dh = torch_pinned_like(self.dh)
+        self.h_out = torch_pinned_like(self.p1g[0])
+        self.h2d = (self.h_cache.numel() + self.h_dh.numel()) * 2
+        self.d2h = self.h_out.numel() * 2
+
+    def step_e2e(self, stream):
+        self.cache.copy_(self.h_cache, non_blocking=True)
+        self.dh.copy_(self.h_dh, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.p1g[0], non_blocking=True)
+
+    def oracle_sample(self, n_tokens, seed=1):
+        # per sampled token t: the 12-row causal windows and dh of every layer on row t alone
+        rng = np.random.default_rng(seed)
+        idx = np.sort(rng.choice(self.T, size=min(n_tokens, self.T), replace=False))
+        out = []
+        for t in idx:
+            lo = max(0, int(t) - 11)
+            win = self.cache[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
+            pw = self.parts[:, lo:int(t) + 1, :].float().cpu().numpy().astype(np.float64)
+            dw = np.zeros((self.S,) + win.shape[1:])
+            dw[:, -1] = self.dh[:, int(t)].float().cpu().numpy()
+            out.append((win, pw, dw))
+        return (out, self.conv_w.cpu().numpy().astype(np.float64), self.queries.cpu().numpy().astype(np.float64),
+                self.mix_w.cpu().numpy().astype(np.float64))
+
+    def run_oracle(self, sample):
+        from oracle import oracle
+        wins, cw, q, mw = sample
+        for win, pw, dw in wins:
+            o, lse = oracle.msar_phase1(win, self.ks, cw, q, None, 1e-6)
+            d_o, d_l = np.zeros_like(o), np.zeros_like(lse)
+            for s_ in range(self.S):
+                r = oracle.msar_phase2_bwd(o[s_], lse[s_], pw[s_] if s_ > 0 else None, self.ks, cw, q[s_], dw[s_],
+                                           None, 1e-6, None, mw, 1e-6)
+                d_o[s_], d_l[s_] = r[0], r[1]
+            oracle.msar_phase1_bwd(win, self.ks, cw, q, d_o, d_l, None, 1e-6)
+        return len(wins)
+
+
 def make_workload(name, T=None):
     if name == "block":
         return BlockWorkload(T=T or 32768)
@@ -1335,6 +1444,8 @@ def make_workload(name, T=None):
         return MsarBlockWsWorkload(T=T or 32768)
     if name == "msar_bwd":
         return MsarBwdWorkload(T=T or 32768)
+    if name == "msar_block_bwd":
+        return MsarBlockBwdWorkload(T=T or 32768)
     if name == "msar_bwd_ps":
         return MsarBwdPerSourceWorkload(T=T or 32768)
     if name == "block_fused":
@@ -1587,7 +1698,8 @@ def main():
     ap.add_argument("--workload", default="block",
                     choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
                              "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block",
-                             "msar_bwd", "msar_bwd_ps", "msar_ws", "msar_block_ws", "full_depth"])
+                             "msar_bwd", "msar_bwd_ps", "msar_ws", "msar_block_ws", "msar_block_bwd",
+                             "full_depth"])
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -669,19 +669,23 @@ def msar_block_phase2_ws(o, lse, partial, ksizes, conv_w, query, gain=None, eps=
 
 
 def msar_block_phase2_bwd(o, lse, partial, ksizes, conv_w, query, dh, gain=None, eps=1e-6, mix_gain=None, mix_w=None,
-                          mix_eps=1e-6, workspace=None, stream=None):
+                          mix_eps=1e-6, outs=None, workspace=None, stream=None):
     """Backward of msar_block_phase2 for dh [T, d] -> (d_o [m,T,d], d_lse
     [m,T], d_partial [T,d] or None, dconv_w, dquery [m,d], dgain [d],
-    dmix_gain [m*d], dmix_w [m*d,m])."""
+    dmix_gain [m*d], dmix_w [m*d,m]).  outs: those eight tensors to write
+    (else allocated here)."""
     import torch
     m, T, d = o.shape
     ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
     dev, f32 = o.device, dict(dtype=torch.float32, device=o.device)
-    d_o = torch.empty_like(o)
-    d_lse = torch.empty((m, T), **f32)
-    d_p = torch.empty_like(partial) if partial is not None else None
-    dcw, dq, dg = torch.empty_like(conv_w, dtype=torch.float32), torch.empty((m, d), **f32), torch.empty((d,), **f32)
-    dmg, dmw = torch.empty((m * d,), **f32), torch.empty((m * d, m), **f32)
+    if outs is not None:
+        d_o, d_lse, d_p, dcw, dq, dg, dmg, dmw = outs
+    else:
+        d_o = torch.empty_like(o)
+        d_lse = torch.empty((m, T), **f32)
+        d_p = torch.empty_like(partial) if partial is not None else None
+        dcw, dq, dg = torch.empty_like(conv_w, dtype=torch.float32), torch.empty((m, d), **f32), torch.empty((d,), **f32)
+        dmg, dmw = torch.empty((m * d,), **f32), torch.empty((m * d, m), **f32)
     if workspace is None:
         n = ctypes.c_size_t(0)
         _check("msar_block_phase2_bwd_workspace_size", load().msar_block_phase2_bwd_workspace_size(
@@ -694,17 +698,22 @@ def msar_block_phase2_bwd(o, lse, partial, ksizes, conv_w, query, dh, gain=None,
     return d_o, d_lse, d_p, dcw, dq, dg, dmg, dmw
 
 
-def msar_block_phase1_bwd(src, ksizes, conv_w, queries, d_o, d_lse, gain=None, eps=1e-6, workspace=None,
+def msar_block_phase1_bwd(src, ksizes, conv_w, queries, d_o, d_lse, gain=None, eps=1e-6, outs=None, workspace=None,
                           stream=None):
     """Backward of msar_block_phase1 for d_o [S,m,T,d], d_lse [S,m,T] ->
-    (dsrc [n_src,T,d], dconv_w, dqueries [S,m,d], dgain [d])."""
+    (dsrc [n_src,T,d], dconv_w, dqueries [S,m,d], dgain [d]).  outs: those
+    four tensors to write (else allocated here)."""
     import torch
     n_src, T, d, stride = _src_geometry(src)
     S, m = queries.shape[0], queries.shape[1]
     ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
     dev, f32 = src.device, dict(dtype=torch.float32, device=src.device)
-    dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=dev)
-    dcw, dq, dg = torch.empty_like(conv_w, dtype=torch.float32), torch.empty((S, m, d), **f32), torch.empty((d,), **f32)
+    if outs is not None:
+        dsrc, dcw, dq, dg = outs
+    else:
+        dsrc = torch.empty((n_src, T, d), dtype=src.dtype, device=dev)
+        dcw, dq, dg = (torch.empty_like(conv_w, dtype=torch.float32), torch.empty((S, m, d), **f32),
+                       torch.empty((d,), **f32))
     if workspace is None:
         n = ctypes.c_size_t(0)
         _check("msar_block_phase1_bwd_workspace_size", load().msar_block_phase1_bwd_workspace_size(
