@@ -1331,13 +1331,21 @@ class MsarBlockBwdWorkload(MsarBlockWorkload):
 
     def setup(self, device):
         import torch
-        from depth_wise_attention_gb300 import attnres
         super().setup(device)
-        T, d, S, N = self.T, self.d, self.S, self.N
-        attnres.msar_block_phase1(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, o=self.o, lse=self.lse)
+        T, d, S = self.T, self.d, self.S
         g = torch.Generator(device=device)
         g.manual_seed(self.seed + 9)
         self.dh = torch.randn((S, T, d), generator=g, device=device).to(torch.bfloat16)
+        self.device = device
+        self.ready = False
+
+    def _prepare(self):
+        # the CUDA arm's state: the block's phase-1 state and the output and
+        # workspace buffers (made in the first, untimed warm-up step)
+        import torch
+        from depth_wise_attention_gb300 import attnres
+        T, d, S, N, device = self.T, self.d, self.S, self.N, self.device
+        attnres.msar_block_phase1(self.cache, self.ks, self.conv_w, self.queries, None, 1e-6, o=self.o, lse=self.lse)
         f32 = dict(dtype=torch.float32, device=device)
         self.d_o = torch.empty_like(self.o)
         self.d_lse = torch.empty((S, 4, T), **f32)
@@ -1355,9 +1363,12 @@ class MsarBlockBwdWorkload(MsarBlockWorkload):
             N, T, d, 1, 4, ctypes.cast(ks, ctypes.c_void_p), S, ctypes.byref(n)))
         self.ws1 = torch.empty(((n.value + 3) // 4,), **f32)
         self.out = self.p1g[0]
+        self.ready = True
 
     def step(self, stream, ev=None):
         from depth_wise_attention_gb300 import attnres
+        if not self.ready:
+            self._prepare()
         if ev is not None:
             ev[0].record(stream)
         for s_ in range(self.S):
@@ -1372,6 +1383,8 @@ class MsarBlockBwdWorkload(MsarBlockWorkload):
             ev[1].record(stream)
 
     def setup_host(self):
+        if not self.ready:
+            self._prepare()
         self.h_cache = torch_pinned_like(self.cache)
         self.h_dh = torch_pinned_like(self.dh)
         self.h_out = torch_pinned_like(self.p1g[0])
