@@ -1426,6 +1426,11 @@ class MsarBlockBwdWorkload(MsarBlockWorkload):
         return len(wins)
 
 
+WORKLOADS = ["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
+             "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block", "msar_bwd", "msar_bwd_ps", "msar_ws",
+             "msar_block_ws", "msar_block_bwd", "full_depth"]
+
+
 def make_workload(name, T=None):
     if name == "block":
         return BlockWorkload(T=T or 32768)
@@ -1708,11 +1713,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workload", default="block",
-                    choices=["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
-                             "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block",
-                             "msar_bwd", "msar_bwd_ps", "msar_ws", "msar_block_ws", "msar_block_bwd",
-                             "full_depth"])
+    ap.add_argument("--workload", default="block", choices=WORKLOADS)
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
