@@ -1311,7 +1311,7 @@ class MsarBlockBwdWorkload(MsarBlockWorkload):
     layer: phase 2's backward per layer (layers 2..4 with their partials,
     layer 1 without), then phase 1's backward with the layers' state
     gradients, as a training step would run it.  The phase-1 state is
-    computed once in setup.  Algorithmic bytes per token: the cached sources,
+    computed once, in the first warm-up step.  Algorithmic bytes per token: the cached sources,
     the partials, the state (o, lse), dh read; the sources' and the partials'
     gradients written."""
 
