@@ -976,6 +976,13 @@ attnres_status_t launch_msar_phase2_host(const void *o, const float *lse, const 
     return launch_msar_phase2(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
 }
 
+// Tokens per CTA of the MSAR mixer kernels: 128, or more where the token
+// chunks would exceed the grid's y limit (65535).
+int64_t mix_tokens_per_cta(int64_t T) {
+    const int64_t need = (T + 65534) / 65535;
+    return need > 128 ? need : 128;
+}
+
 // MSAR backward: chunking and workspace layout.  Each region starts on a
 // 256-byte boundary of the workspace.
 struct MsarBwdPlan {
@@ -1001,7 +1008,7 @@ attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtyp
     p->chunks = T > 0 ? (T + p->tc - 1) / p->tc : 0;
     p->tc_s = (T + 127) / 128;
     if (p->tc_s < 32) p->tc_s = 32;
-    p->tc_m = 128;
+    p->tc_m = mix_tokens_per_cta(T);
     p->nsl = (int)(d / 1024);
     const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
     const size_t es = esize(dt);
@@ -1267,7 +1274,7 @@ attnres_status_t launch_msar_read_ws(const void *src, int64_t n_src, int64_t src
     a.mix_eps = mix_eps;
     a.mix_part = reinterpret_cast<float *>(w + p.off_part);
     a.nsl = (int)(d / 1024);
-    a.tc_m = 128;
+    a.tc_m = mix_tokens_per_cta(T);
     cudaError_t e = msar_fwd_mix(dt == ATTNRES_BF16 ? 1 : 0, a, out, stream);
     return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "msar mixer launch");
 }
@@ -1381,7 +1388,7 @@ attnres_status_t launch_msar_phase2_ws(const void *o, const float *lse, const vo
     a.mix_eps = mix_eps;
     a.mix_part = reinterpret_cast<float *>(w + p.off_part);
     a.nsl = (int)(d / 1024);
-    a.tc_m = 128;
+    a.tc_m = mix_tokens_per_cta(T);
     cudaError_t e = msar_fwd_mix(dt == ATTNRES_BF16 ? 1 : 0, a, out, stream);
     return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "msar mixer launch");
 }
@@ -1569,7 +1576,7 @@ attnres_status_t launch_msar_phase2_bwd(const void *o, const float *lse, const v
     a.T = T;
     a.d = (int)d;
     a.tc = p.tc;
-    a.tc_m = 128;
+    a.tc_m = mix_tokens_per_cta(T);
     a.nsl = p.nsl;
     a.z = const_cast<unsigned char *>(z);           // read only
     a.dz = partial ? w + p.off_dz : static_cast<unsigned char *>(d_o);
