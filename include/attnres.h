@@ -553,8 +553,8 @@ attnres_status_t msar_expand_bwd_workspace_size(int64_t n_src, int64_t T, int64_
  * writes the conv streams once, reads each stream with the forward read
  * kernels and mixes the per-stream reads.  The fused msar_expand_fwd never
  * writes a stream (the pages' on-demand expansion, MSAR page, section 어떻게
- * 쓰나) but synchronises a cluster of CTAs per token; on this GPU the chain
- * is faster where the memory for it is available.  The per-stream reads are
+ * 쓰나) but synchronises a cluster of CTAs per token; on GB300 the chain is
+ * faster where the memory for it is available.  The per-stream reads are
  * held in dtype dt before the mixer (the fused read keeps them in fp32), so
  * bf16 results differ from msar_expand_fwd's within the bf16 tolerance.
  *   conv_src_stride  0: one set of kernels for every source (msar_expand_fwd);
