@@ -64,6 +64,12 @@ MUTANTS = {
     "msar_phase1_bwd_drops_dlse": [("rc = oracle_read_bwd_lse(ur, n_src, T, d, qr, S, gain, eps, dor, dlr, du, dqr, dgr);",
                                     "rc = oracle_read_bwd_lse(ur, n_src, T, d, qr, S, gain, eps, dor, NULL, du, dqr, dgr);")],
     "msar_phase2_bwd_drops_partial_identity_stream": [("for (size_t k = 0; k < per; ++k) d_partial[k] += dup[k];", "")],
+    "msar_phase2_bwd_query_of_stream_zero": [("query + r * d, gain, eps, dZ + (size_t)r * per, d_o + (size_t)r * per,",
+                                              "query, gain, eps, dZ + (size_t)r * per, d_o + (size_t)r * per,")],
+    "msar_phase1_bwd_queries_stream_major": [("memcpy(qr + sl * d, queries + (sl * m + r) * d,",
+                                              "memcpy(qr + sl * d, queries + (r * S + sl) * d,")],
+    "msar_mix_bwd_gain_grad_missing_nu": [("if (nu > 0.0) dmix_gain[k] += acc * zf[k] / nu;",
+                                           "if (nu > 0.0) dmix_gain[k] += acc * zf[k];")],
     "update_drops_old_partial": [("p_out[t * d + c] = (p ? p[t * d + c] : 0.0) + f[t * d + c];",
                                   "p_out[t * d + c] = f[t * d + c];")],
     "mhar_phase2_lse_transposed": [("const double l = lse[hd * T + t];", "const double l = lse[t * H + hd];")],
