@@ -424,3 +424,17 @@ def test_msar_two_phase_backward_validation(lib):
     assert p1(dsrc=A + 64) == INV                  # dsrc overlaps the sources
     assert p1(ws=DO - 64) == INV                   # workspace overlaps d_o
     assert p1(d=768) == UNS
+
+
+def test_binding_covers_every_entry_point_and_fails_loudly_without_the_library(tmp_path):
+    """The ctypes binding declares a signature for exactly the functions the
+    header declares, and with no library there is an error, never a fallback."""
+    from depth_wise_attention_gb300 import attnres
+    assert set(attnres.header_functions()) == set(attnres._SIGS)
+    saved = attnres._lib
+    attnres._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            attnres.load(str(tmp_path / "libattnres.so"))
+    finally:
+        attnres._lib = saved
