@@ -542,7 +542,8 @@ attnres_status_t read_bwd_shape(int64_t n_src, int64_t d, int64_t n_q, int64_t H
     // queries per launch: up to 4 (two groups of two over the same staged
     // sources) with at most 8 sources where that kernel exists, else 2 (1
     // with more than 8 sources)
-    const int base = sh->ns == 16 ? 1 : 2;
+    int base = sh->ns == 16 ? 1 : 2;
+    if (max_nqc > 0 && base > max_nqc) base = max_nqc;
     if (sh->ns == 8 && n_q > 2 && (max_nqc == 0 || max_nqc > 2)) {
         const int want = n_q < 4 ? (int)n_q : 4;
         KernelRef kr;
@@ -1002,7 +1003,9 @@ attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtyp
     p->rb_bytes = read_bwd_ws_bytes(dev->sms, p->rb, d);
     // token chunks: the conv backward and A's partials in at most 64 chunks
     // of at least 32 tokens; the streams kernel in chunks of T/128 (at least
-    // 32); the mixer 128 tokens per CTA over d/1024 channel slices
+    // 32); the mixer over d/1024 channel slices, mix_tokens_per_cta(T)
+    // tokens per CTA (128, or more so that the token chunks stay within the
+    // grid's y limit of 65535)
     p->tc = (T + 63) / 64;
     if (p->tc < 32) p->tc = 32;
     p->chunks = T > 0 ? (T + p->tc - 1) / p->tc : 0;
@@ -1790,20 +1793,23 @@ attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_
                                           int64_t dsrc_stride, int accumulate, float *dqueries, float *dgain,
                                           void *stream) {
     // queries per pass: as many as the kernels take, unless their workspace
-    // outgrows the scratch array (then passes of two)
+    // outgrows the scratch array; then passes of two, then of one
     int max_nqc = 0;
     if (T > 0) {
         size_t need = 0;
         attnres_status_t st = attnres_read_bwd_workspace_size(n_src, T, d, n_q, dt, &need);
         if (st != ATTNRES_OK) return st;
         if (need > kBwdScratchFloats * sizeof(float)) {
-            ReadBwdShape sh;
             DeviceInfo *dev = nullptr;
-            st = read_bwd_shape(n_src, d, n_q, 1, dt, &sh, 2);
-            if (st == ATTNRES_OK) st = device_info(&dev);
+            st = device_info(&dev);
             if (st != ATTNRES_OK) return st;
-            if (read_bwd_ws_bytes(dev->sms, sh, d) > kBwdScratchFloats * sizeof(float)) return ATTNRES_ERR_UNSUPPORTED;
-            max_nqc = 2;
+            for (int cap = 2; cap >= 1 && max_nqc == 0; --cap) {
+                ReadBwdShape sh;
+                st = read_bwd_shape(n_src, d, n_q, 1, dt, &sh, cap);
+                if (st != ATTNRES_OK) return st;
+                if (read_bwd_ws_bytes(dev->sms, sh, d) <= kBwdScratchFloats * sizeof(float)) max_nqc = cap;
+            }
+            if (max_nqc == 0) return ATTNRES_ERR_UNSUPPORTED;
         }
     }
     void *ws = nullptr;

@@ -253,15 +253,29 @@ attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64
                                                 attnres_dtype_t dt, size_t *bytes);
 
 /*
- * attnres_read_bwd without a caller workspace: the same backward, with the
- * sums over the tokens reduced through a fixed 8 MB scratch array that the
- * library's image holds in device memory (its address is looked up once per
- * device); nothing is allocated.  The pages have no counterpart: this entry
- * point exists for callers that cannot hand out device memory (for instance
- * inside a captured CUDA graph).  Calls that would need more scratch than the
- * array holds return ATTNRES_ERR_UNSUPPORTED; all other arguments, limits and
- * errors are those of attnres_read_bwd.  The array is shared: calls on one
- * device must be ordered (one stream, or streams that wait for each other).
+ * attnres_read_bwd without a caller workspace.  The pages have no counterpart
+ * to this entry point.  It serves callers that cannot hand this library device
+ * memory: a runtime that reserves its whole device-memory budget up front and
+ * hands it out from its own pool, or code that may not call cudaMalloc or
+ * cudaFree on its hot path (those calls can synchronize the device, and can
+ * fail in the middle of a step).  The backward is attnres_read_bwd's, with its
+ * sums over the tokens reduced through a fixed scratch array of 8 MB that the
+ * library's image places in device memory (a file-scope __device__ array:
+ * every device that loads the library holds it until the process exits).
+ * No call allocates or frees memory.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and keeps it; that first
+ * call on each device should come before any stream capture.
+ * Limits: a call whose workspace would not fit in the array runs its queries
+ * in passes of two, then of one; if even one query per pass does not fit it
+ * returns ATTNRES_ERR_UNSUPPORTED.  Every other argument, limit and error is
+ * attnres_read_bwd's.
+ * Sharing: all calls on a device use the same array, which keeps what the
+ * last call left in it; each call writes every scratch value before reading
+ * it, so nothing needs clearing.  Calls that overlap on the GPU (on streams
+ * that do not wait for each other) race on the array and give wrong results:
+ * order them on one stream, or make the streams wait for each other.
  */
 attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_t src_stride,
                                           int64_t T, int64_t d, attnres_dtype_t dt,
