@@ -43,6 +43,7 @@ KERNEL_SOURCES = {
     "depth_read": [CSRC + "depth_read.cuh", CSRC + "common.cuh"],
     "phase2": [CSRC + "phase2.cuh", CSRC + "common.cuh", CSRC + "kernels_phase2.cu"],
     "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
+    "msar_tile": [CSRC + "msar_tile.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
     "msar_phase1": [CSRC + "msar_phase1.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "msar_phase2": [CSRC + "msar_phase2.cu", CSRC + "msar.h", CSRC + "common.cuh"],
@@ -803,9 +804,11 @@ class MsarWorkload(BlockWorkload):
         self.bytes_per_token = N * d * 2 + d * 2
         self.phase1_bytes_per_token = self.bytes_per_token
         self.launches_per_step = 1
-        self.dominant = "msar_kernel"
-        self.dominant_src = "msar"
-        self.profile_tag = f"ncu_msar_d{d}"
+        # bf16 with kernel sizes 4/8/12 and d a multiple of 256 runs the
+        # tile-batched kernel (one cluster exchange per tile of tokens)
+        self.dominant = "msar_tile_kernel"
+        self.dominant_src = "msar_tile"
+        self.profile_tag = f"ncu_msar_tile_d{d}"
         # The read is bound by fp32 arithmetic, not HBM: its roofline is the
         # CUDA-core FMA rate.  Multiply-adds per token: the causal convolutions
         # (N sources x d channels x (4+8+12) taps), per (source, stream) the
@@ -1174,7 +1177,7 @@ class MsarChunkedWorkload(MsarWorkload):
         self.name = "msar_chunked_prefill"
         self.chunk = chunk
         self.launches_per_step = (T + chunk - 1) // chunk
-        self.dominant = "msar_kernel (all chunks)"
+        self.dominant = "msar_tile_kernel (all chunks)"
 
     def config(self):
         c = super().config()

@@ -34,6 +34,7 @@ SOURCES = [
     "kernels_merge_bwd.cu",
     "kernels_decode.cu",
     "msar.cu",
+    "msar_tile.cu",
     "msar_phase1.cu",
     "msar_phase2.cu",
     "msar_bwd.cu",

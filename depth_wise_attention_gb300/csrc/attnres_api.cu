@@ -869,7 +869,13 @@ attnres_status_t launch_msar_read(const void *src, int64_t n_src, int64_t src_st
     a.mix_eps = mix_eps;
     a.out = static_cast<unsigned char *>(out);
     a.wait = wait_cfg(dev);
-    return launch_msar(dt == ATTNRES_BF16 ? 1 : 0, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
+    const int dti = dt == ATTNRES_BF16 ? 1 : 0;
+    // the tile-batched kernel where it applies (variant 1 keeps the per-token one)
+    if (g_kernel_variant.load() != 1 && msar_tile_applies(dti, a)) {
+        st = launch_msar_tile(a, dev->sms, stream, t_last_err, sizeof(t_last_err));
+        if (st != ATTNRES_ERR_UNSUPPORTED) return st;
+    }
+    return launch_msar(dti, a, dev->sms, stream, t_last_err, sizeof(t_last_err));
 }
 
 // MSAR in the two-phase Block schedule.  Kernel sizes as the one-shot read.

@@ -111,4 +111,10 @@ __device__ __forceinline__ float dot2(float2 a, float2 b) { return fmaf(a.x, b.x
 // Validated arguments in, launch out.  dt: 0 = f32, 1 = bf16.
 attnres_status_t launch_msar(int dt, MsarArgs a, int sms, void *stream, char *err, size_t errlen);
 
+// The tile-batched fused read (msar_tile.cu): bf16 sources, kernel sizes
+// 4/8/12 shared by all sources, d a multiple of 256 up to 4096.  Returns
+// ATTNRES_ERR_UNSUPPORTED when no cluster of it can be resident.
+bool msar_tile_applies(int dt, const MsarArgs &a);
+attnres_status_t launch_msar_tile(MsarArgs a, int sms, void *stream, char *err, size_t errlen);
+
 }  // namespace attnres

@@ -734,9 +734,65 @@ def test_msar_per_source_equal_kernels_equal_the_shared_read_bitwise():
     q = to_dev(_queries(rng, 4, d), F32)
     cw = np.concatenate([(rng.standard_normal((d, k)) / math.sqrt(k)).astype(np.float32).ravel() for k in ks])
     mw = to_dev((rng.standard_normal((4 * d, 4)) / math.sqrt(4 * d)).astype(np.float32), F32)
-    shared = attnres.msar_expand_fwd(src, ks, to_dev(cw, F32), q, mix_w=mw)
+    # the per-source read is the per-token kernel's PS form: compare it with
+    # the shared read of that same kernel (variant 1 keeps it for the shared
+    # kernels too)
+    attnres.attnres_debug_set_kernel_variant(1)
+    try:
+        shared = attnres.msar_expand_fwd(src, ks, to_dev(cw, F32), q, mix_w=mw)
+    finally:
+        attnres.attnres_debug_set_kernel_variant(0)
     per = attnres.msar_expand_fwd_ps(src, ks, to_dev(np.stack([cw] * n_src), F32), q, mix_w=mw)
     assert torch.equal(shared, per)
+
+
+def _msar_tile_case(n_src, T, d, seed):
+    x = inputs.msar_inputs(n_src, T, d, seed=seed)
+    rng = _rng(seed + 1)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    mg = rng.uniform(0.5, 1.5, 4 * d).astype(np.float32)
+    dev = (to_dev(x["src"], BF16), x["ksizes"], to_dev(x["conv_w"], F32), to_dev(x["queries"], F32),
+           to_dev(g, F32), 1e-6, to_dev(mg, F32), to_dev(x["mix_w"], F32), 1e-6)
+    ref = oracle.msar(x["src"], x["ksizes"], x["conv_w"], x["queries"], g, 1e-6, mg, x["mix_w"], 1e-6)
+    return dev, ref
+
+
+@pytest.mark.parametrize("n_src,T,d", [(8, 1, 4096), (8, 3, 4096), (8, 5, 4096), (5, 6, 4096), (1, 37, 4096),
+                                       (8, 131, 2048), (7, 9, 1024), (2, 64, 512), (8, 13, 256)])
+def test_msar_tile_kernel_shapes(n_src, T, d):
+    """The tile-batched read (bf16, kernel sizes 4/8/12, d a multiple of 256):
+    partial last tiles, one to eight sources, every cluster width from one CTA
+    (d = 256) to sixteen (d = 4096), against the oracle with the elementwise
+    bound."""
+    dev, ref = _msar_tile_case(n_src, T, d, seed=T * 7 + d + n_src)
+    out = attnres.msar_expand_fwd(*dev)
+    check_out(out, ref, BF16)
+
+
+@pytest.mark.parametrize("T,d", [(1000, 2048), (700, 4096)])
+def test_msar_tile_kernel_agrees_with_the_per_token_kernel(T, d):
+    """Many clusters of a few tiles each: the tile-batched read and the
+    per-token kernel (variant 1) both meet the bar against the oracle, and
+    they differ from each other by at most one bf16 rounding step per element
+    plus the float32 summation order."""
+    dev, ref = _msar_tile_case(8, T, d, seed=T + d)
+    tile = attnres.msar_expand_fwd(*dev)
+    attnres.attnres_debug_set_kernel_variant(1)
+    try:
+        per_token = attnres.msar_expand_fwd(*dev)
+    finally:
+        attnres.attnres_debug_set_kernel_variant(0)
+    check_out(tile, ref, BF16, what="tile kernel")
+    check_out(per_token, ref, BF16, what="per-token kernel")
+    a, b = to_host(tile), to_host(per_token)
+    assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.abs(b) + 1e-3 * np.abs(b).max())
+
+
+def test_msar_tile_kernel_is_deterministic():
+    dev, _ = _msar_tile_case(8, 77, 4096, seed=4)
+    a = attnres.msar_expand_fwd(*dev)
+    b = attnres.msar_expand_fwd(*dev)
+    assert torch.equal(a, b)
 
 
 # --------------------------------------------------------------- MSAR backward
