@@ -961,6 +961,50 @@ class MsarBwdWorkload(MsarWorkload):
         return len(wins)
 
 
+class MsarBwdChunkedWorkload(MsarBwdWorkload):
+    """The MSAR backward in chunks of 4096 tokens (msar_expand_bwd_chunk), each
+    given the 11 source rows before it, in order: the first chunk writes the
+    parameter gradients and the later ones add into them, and each chunk adds
+    its share of the history rows' gradient.  The workspace is sized for one
+    chunk (about an eighth of the one-call backward's)."""
+
+    def __init__(self, T=32768, d=4096, N=8, seed=0, chunk=4096):
+        super().__init__(T, d, N, seed)
+        self.name = "msar_read_backward_chunked"
+        self.chunk = chunk
+        self.launches_per_step *= (T + chunk - 1) // chunk
+        self.dominant = "msar backward, chunked (whole chain per chunk)"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} N={self.N} m=4 k=4/8/12 T={self.T} chunk={self.chunk}"
+        c["chunk"] = self.chunk
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres
+        super().setup(device)
+        del self.ws
+        nb = attnres.msar_expand_bwd_workspace_size(self.N, self.chunk, self.d, torch.bfloat16, self.ks)
+        self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+        self.workspace_bytes = nb
+
+    def step(self, stream, ev=None):
+        from depth_wise_attention_gb300 import attnres
+        hist = max(self.ks) - 1
+        if ev is not None:
+            ev[0].record(stream)
+        for c0 in range(0, self.T, self.chunk):
+            c1 = min(self.T, c0 + self.chunk)
+            h = min(hist, c0)
+            attnres.msar_expand_bwd_chunk(self.cache[:, c0 - h:c1], h, self.ks, self.conv_w, self.queries,
+                                          self.dh[c0:c1], self.dsrc[:, c0 - h:c1], self.grads, c0 > 0, None, 1e-6,
+                                          None, self.mix_w, 1e-6, workspace=self.ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+
 class MsarBwdPerSourceWorkload(MsarBwdWorkload):
     """The MSAR backward with each of the N=8 sources' own conv kernels
     (msar_expand_bwd_ps): kernels ~ N(0, 1/k) per source, each source's
@@ -1431,7 +1475,7 @@ class MsarBlockBwdWorkload(MsarBlockWorkload):
 
 WORKLOADS = ["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
              "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block", "msar_bwd", "msar_bwd_ps", "msar_ws",
-             "msar_block_ws", "msar_block_bwd", "full_depth"]
+             "msar_block_ws", "msar_block_bwd", "full_depth", "msar_bwd_chunked"]
 
 
 def make_workload(name, T=None):
@@ -1465,6 +1509,8 @@ def make_workload(name, T=None):
         return MsarBlockWsWorkload(T=T or 32768)
     if name == "msar_bwd":
         return MsarBwdWorkload(T=T or 32768)
+    if name == "msar_bwd_chunked":
+        return MsarBwdChunkedWorkload(T=T or 32768)
     if name == "msar_block_bwd":
         return MsarBlockBwdWorkload(T=T or 32768)
     if name == "msar_bwd_ps":

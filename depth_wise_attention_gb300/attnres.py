@@ -60,6 +60,9 @@ _SIGS = {
     "msar_expand_bwd": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
                         _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "msar_expand_bwd_workspace_size": [_i64, _i64, _i64, ctypes.c_int, _i64, _vp, ctypes.POINTER(ctypes.c_size_t)],
+    "msar_expand_bwd_chunk": [_vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _vp, _vp, _f, _vp,
+                              _vp, _f, _vp, _vp, _i64, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                              _vp],
     "msar_expand_bwd_ps": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _i64, _vp, _vp, _f, _vp, _vp,
                            _f, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "msar_expand_fwd_ws": [_vp, _i64, _i64, _i64, _i64, ctypes.c_int, _i64, _vp, _vp, _i64, _vp, _vp, _f, _vp, _vp,
@@ -588,6 +591,30 @@ def msar_expand_fwd_ws_workspace_size(n_src, T, d, dtype):
     _check("msar_expand_fwd_ws_workspace_size",
            load().msar_expand_fwd_ws_workspace_size(n_src, T, d, dt, ctypes.byref(n)))
     return n.value
+
+
+def msar_expand_bwd_chunk(src, t_prev, ksizes, conv_w, queries, dh, dsrc, grads, accumulate, gain=None, eps=1e-6,
+                          mix_gain=None, mix_w=None, mix_eps=1e-6, workspace=None, stream=None):
+    """Backward of one chunk: src [n_src, t_prev + T, d] (t_prev history rows
+    first), dh [T, d]; dsrc [n_src, t_prev + T, d] gets the chunk's rows
+    written and the history rows' share added; grads = (dconv_w, dqueries,
+    dgain, dmix_gain, dmix_w) are written (accumulate False) or added into."""
+    import torch
+    n_src, rows, d, stride = _src_geometry(src)
+    T = rows - t_prev
+    m = queries.shape[0]
+    ks = (ctypes.c_int32 * len(ksizes))(*[int(k) for k in ksizes])
+    _, _, _, dstride = _src_geometry(dsrc)
+    dconv_w, dqueries, dgain, dmix_gain, dmix_w = grads
+    if workspace is None:
+        nbytes = msar_expand_bwd_workspace_size(n_src, T, d, src.dtype, ksizes)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=src.device)
+    _check("msar_expand_bwd_chunk", load().msar_expand_bwd_chunk(
+        _p(src), n_src, stride, t_prev, T, d, _dt(src), m, ctypes.cast(ks, _vp), _p(conv_w), _p(queries), _p(gain),
+        eps, _p(mix_gain), _p(mix_w), mix_eps, _p(dh), _p(dsrc), dstride, 1 if accumulate else 0, _p(dconv_w),
+        _p(dqueries), _p(dgain), _p(dmix_gain), _p(dmix_w), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dsrc
 
 
 def msar_expand_fwd_ws(src, ksizes, conv_w, queries, gain=None, eps=1e-6, mix_gain=None, mix_w=None, mix_eps=1e-6,

@@ -997,7 +997,7 @@ struct MsarBwdPlan {
     int nsl;
     ReadBwdShape rb;
     size_t rb_bytes;
-    size_t off_u, off_z, off_dz, off_du, off_rb, off_dg, off_part, off_e, off_mp, off_a, off_cp, total;
+    size_t off_u, off_z, off_dz, off_du, off_rb, off_dg, off_dq, off_part, off_e, off_mp, off_a, off_cp, total;
 };
 
 attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt, const int32_t *ksizes,
@@ -1034,6 +1034,7 @@ attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtyp
     p->off_du = take(4 * (size_t)n_src * row);
     p->off_rb = take(p->rb_bytes);
     p->off_dg = take(4 * (size_t)d * 4);
+    p->off_dq = take(4 * (size_t)d * 4);
     p->off_part = take((size_t)T * (size_t)p->nsl * 9 * 4);
     p->off_e = take((size_t)T * 4 * 4);
     p->off_mp = take((size_t)p->chunks * 16 * (size_t)d * 4);
@@ -1046,22 +1047,29 @@ attnres_status_t msar_bwd_plan(int64_t n_src, int64_t T, int64_t d, attnres_dtyp
 // Backward of the MSAR read (msar_expand_fwd), as a chain of steps in the
 // caller's workspace: the streams, the per-stream reads Z^(r), the mixer's
 // backward, the per-stream read backward, and the causal convolutions'
-// transpose.
+// transpose.  A chunk of a longer sequence (msar_expand_bwd_chunk): src and
+// dsrc start t_prev history rows before the chunk's T rows; the history rows
+// feed the chunk's streams and kernel gradients, and get the chunk's share of
+// their gradient added into dsrc; with accumulate the parameter gradients are
+// added into their outputs.
 attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
                                  attnres_dtype_t dt, int64_t m, const int32_t *ksizes, const float *conv_w,
                                  const float *queries, const float *gain, float eps, const float *mix_gain,
                                  const float *mix_w, float mix_eps, const void *dh, void *dsrc,
                                  int64_t dsrc_stride, float *dconv_w, float *dqueries, float *dgain,
                                  float *dmix_gain, float *dmix_w, void *ws, size_t ws_bytes, void *stream,
-                                 int64_t conv_src_stride = 0) {
-    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+                                 int64_t conv_src_stride = 0, int64_t t_prev = 0, int accumulate = 0) {
+    if (T < 0 || t_prev < 0 || t_prev > INT64_MAX - T || (accumulate != 0 && accumulate != 1))
+        return ATTNRES_ERR_INVALID_ARG;
+    const int64_t rows = t_prev + T;                     // source rows per source, history included
+    attnres_status_t st = check_common(src, n_src, src_stride, rows, d, dt, eps);
     if (st != ATTNRES_OK) return st;
     if (!(mix_eps >= 0.f) || std::isinf(mix_eps)) return ATTNRES_ERR_INVALID_ARG;
     st = check_msar_kernels(m, ksizes);
     if (st != ATTNRES_OK) return st;
     if (!conv_w || !queries || !mix_w || !dconv_w || !dqueries || !dmix_w) return ATTNRES_ERR_INVALID_ARG;
     if (T > 0 && (!dh || !dsrc || !ws)) return ATTNRES_ERR_INVALID_ARG;
-    if (dsrc_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_stride < rows * d) return ATTNRES_ERR_INVALID_ARG;
     const int64_t ktot = (int64_t)ksizes[0] + ksizes[1] + ksizes[2];
     // per-source kernels: each source's set must not overlap the next one's
     if (conv_src_stride < 0 || (conv_src_stride > 0 && n_src > 1 && conv_src_stride < d * ktot))
@@ -1069,8 +1077,8 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     const int64_t n_sets = conv_src_stride > 0 ? n_src : 1;              // kernel sets (and gradients)
     const size_t cw_bytes = ((size_t)(n_sets - 1) * (size_t)conv_src_stride + (size_t)ktot * (size_t)d) * 4;
     const size_t es = esize(dt);
-    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
-    const size_t dsrc_bytes = ((size_t)(n_src - 1) * (size_t)dsrc_stride + (size_t)T * (size_t)d) * es;
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)rows * (size_t)d) * es;
+    const size_t dsrc_bytes = ((size_t)(n_src - 1) * (size_t)dsrc_stride + (size_t)rows * (size_t)d) * es;
     const size_t row_bytes = (size_t)T * (size_t)d * es;
     const size_t md = 4 * (size_t)d;
     if (T > 0 && (overlap(dsrc, dsrc_bytes, src, src_bytes) || overlap(dsrc, dsrc_bytes, dh, row_bytes) ||
@@ -1102,7 +1110,8 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     if (st != ATTNRES_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 0) {
-        // no tokens: every parameter gradient is zero
+        // no tokens: every parameter gradient is zero (nothing to add)
+        if (accumulate) return ATTNRES_OK;
         cudaError_t e = cudaSuccess;
         for (int x = 1; x < 5 && e == cudaSuccess; ++x)
             if (pg[x]) e = cudaMemsetAsync(const_cast<void *>(pg[x]), 0, pn[x], s);
@@ -1112,7 +1121,12 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     }
     if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
     unsigned char *w = static_cast<unsigned char *>(ws);
-    MsarBwdArgs a;
+    // from here on src and dsrc point at the chunk's first row
+    src = static_cast<const unsigned char *>(src) + t_prev * d * (int64_t)es;
+    dsrc = static_cast<unsigned char *>(dsrc) + t_prev * d * (int64_t)es;
+    MsarBwdArgs a{};
+    a.hist = t_prev;
+    a.acc = accumulate;
     a.src = static_cast<const unsigned char *>(src);
     a.src_stride_bytes = src_stride * (int64_t)es;
     a.n_src = (int)n_src;
@@ -1160,13 +1174,19 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
     if (e == cudaSuccess) e = msar_bwd_mix_finish(a, A, stream);
     if (e != cudaSuccess) return cuda_fail(e, "msar backward mixer sums launch");
     // the per-stream read backward: du^(r), dw_r and stream r's share of dgain
+    // (dw_r into a scratch row first when it adds into dqueries)
     float *dg = reinterpret_cast<float *>(w + p.off_dg);
+    float *dqw = accumulate ? reinterpret_cast<float *>(w + p.off_dq) : dqueries;
     for (int64_t r = 0; r < 4; ++r) {
         const void *sr = r == 0 ? src : static_cast<const void *>(a.u + (size_t)(r - 1) * per_stream * es);
         st = launch_read_bwd(sr, n_src, r == 0 ? src_stride : T * d, T, d, 1, dt, queries + r * d, 1, gain, eps,
                              a.dz + (size_t)r * row_bytes, nullptr, a.du + (size_t)r * per_stream * es, T * d, 0,
-                             dqueries + r * d, dg + r * d, w + p.off_rb, p.rb_bytes, stream);
+                             dqw + r * d, dg + r * d, w + p.off_rb, p.rb_bytes, stream);
         if (st != ATTNRES_OK) return st;
+    }
+    if (accumulate) {
+        e = msar_bwd_sum(dqw, 1, 4 * d, dqueries, 1, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "msar backward query sums launch");
     }
     e = msar_bwd_conv(dti, a, stream);
     if (conv_src_stride == 0) {
@@ -1178,7 +1198,7 @@ attnres_status_t launch_msar_bwd(const void *src, int64_t n_src, int64_t src_str
             e = msar_bwd_conv_sum(a, a.conv_parts + i * ktot * d, p.chunks, n_src * ktot * d,
                                   dconv_w + i * conv_src_stride, stream);
     }
-    if (e == cudaSuccess && dgain) e = msar_bwd_sum(dg, 4, d, dgain, 0, stream);
+    if (e == cudaSuccess && dgain) e = msar_bwd_sum(dg, 4, d, dgain, accumulate, stream);
     if (e != cudaSuccess) return cuda_fail(e, "msar backward conv launch");
     return ATTNRES_OK;
 }
@@ -1958,6 +1978,18 @@ attnres_status_t msar_expand_bwd(const void *src, int64_t n_src, int64_t src_str
     return launch_msar_bwd(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, gain, eps, mix_gain,
                            mix_w, mix_eps, dh, dsrc, dsrc_stride, dconv_w, dqueries, dgain, dmix_gain, dmix_w,
                            workspace, workspace_bytes, stream);
+}
+
+attnres_status_t msar_expand_bwd_chunk(const void *src, int64_t n_src, int64_t src_stride, int64_t T_prev,
+                                       int64_t T, int64_t d, attnres_dtype_t dt, int64_t m, const int32_t *ksizes,
+                                       const float *conv_w, const float *queries, const float *gain, float eps,
+                                       const float *mix_gain, const float *mix_w, float mix_eps, const void *dh,
+                                       void *dsrc, int64_t dsrc_stride, int accumulate, float *dconv_w,
+                                       float *dqueries, float *dgain, float *dmix_gain, float *dmix_w,
+                                       void *workspace, size_t workspace_bytes, void *stream) {
+    return launch_msar_bwd(src, n_src, src_stride, T, d, dt, m, ksizes, conv_w, queries, gain, eps, mix_gain,
+                           mix_w, mix_eps, dh, dsrc, dsrc_stride, dconv_w, dqueries, dgain, dmix_gain, dmix_w,
+                           workspace, workspace_bytes, stream, 0, T_prev, accumulate);
 }
 
 attnres_status_t msar_expand_fwd_ws_workspace_size(int64_t n_src, int64_t T, int64_t d, attnres_dtype_t dt,

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(ST_THREADS) msar_streams_kernel(const MsarBwdA
             for (int q = tid; q < CPS; q += ST_THREADS) {
                 const int rr = q / CPR, cc = q - rr * CPR;
                 const int64_t row = t0 - H + (int64_t)b * ST_RB + rr;
-                const bool ok = row >= 0 && row < t1;
+                const bool ok = row >= -a.hist && row < t1;
                 cp_async16(st + rr * ROWB + cc * 16, v + ((ok ? row : 0) * a.d + cb) * ES + cc * 16, ok);
             }
         }
@@ -423,8 +423,15 @@ __global__ void __launch_bounds__(256) msar_mix_finish_kernel(const MsarBwdArgs 
         const float4 ak = *reinterpret_cast<const float4 *>(A + k * 4);
         const float4 pk = __ldg(reinterpret_cast<const float4 *>(a.mix_w + k * 4));
         const float g = a.mix_gain ? __ldg(a.mix_gain + k) : 1.f;
-        *reinterpret_cast<float4 *>(a.dmix_w + k * 4) = make_float4(g * ak.x, g * ak.y, g * ak.z, g * ak.w);
-        if (a.dmix_gain) a.dmix_gain[k] = pk.x * ak.x + pk.y * ak.y + pk.z * ak.z + pk.w * ak.w;
+        float4 dw = make_float4(g * ak.x, g * ak.y, g * ak.z, g * ak.w);
+        float dg = pk.x * ak.x + pk.y * ak.y + pk.z * ak.z + pk.w * ak.w;
+        if (a.acc) {
+            const float4 ow = *reinterpret_cast<const float4 *>(a.dmix_w + k * 4);
+            dw = make_float4(ow.x + dw.x, ow.y + dw.y, ow.z + dw.z, ow.w + dw.w);
+            if (a.dmix_gain) dg += a.dmix_gain[k];
+        }
+        *reinterpret_cast<float4 *>(a.dmix_w + k * 4) = dw;
+        if (a.dmix_gain) a.dmix_gain[k] = dg;
     }
 }
 
@@ -474,7 +481,9 @@ __global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kern
     const int i = blockIdx.y;
     const int64_t t0 = (int64_t)blockIdx.z * a.tc;
     const int64_t t1 = t0 + a.tc < a.T ? t0 + a.tc : a.T;
-    const int64_t nsteps = t1 - t0 + H;           // step s is token t1 - 1 + H - s
+    // step s is token t1 - 1 + H - s; the first chunk walks on through the
+    // history rows (their dv gets this call's share, added in)
+    const int64_t nsteps = t1 - t0 + H + (blockIdx.z == 0 ? a.hist : 0);
     const int nb = (int)((nsteps + RB - 1) / RB);
     const int64_t rowb = (int64_t)a.d * ES;
     const int64_t ttop = t1 - 1 + H;
@@ -497,13 +506,13 @@ __global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kern
         const bool live = b < nb && s < nsteps;
         const int64_t trow = t * rowb;
         const uint32_t dst = sbase + (uint32_t)((b % CB_NS) * SG::BYTES + my_sb * CB_NROW * ROWB + my_cc * 16);
-        const bool okr = live && t < a.T;
+        const bool okr = live && t >= 0 && t < a.T;
 #pragma unroll
         for (int r = 0; r < 3; ++r)
             cp_async16(dst + r * ROWB, du_i + (r + 1) * sstride + (okr ? trow : 0), okr);
-        const bool ok0 = live && t < t1;
+        const bool ok0 = live && t >= 0 && t < t1;
         cp_async16(dst + 3 * ROWB, du_i + (ok0 ? trow : 0), ok0);
-        const bool okv = live && t - H >= 0;
+        const bool okv = live && t - H >= -a.hist;
         cp_async16(dst + 4 * ROWB, v_c + (okv ? trow - H * rowb : 0), okv);
         cp_async_commit();
     };
@@ -545,7 +554,13 @@ __global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kern
                 }
                 if (s >= H) {                                   // t < t1: dv[t] is complete
                     const float2 d0 = P2::ld(stage + (sb * CB_NROW + 3) * ROWB);      // du^(0)[t]
-                    P2::st(dp, make_float2(d0.x + pend[0].x, d0.y + pend[0].y));
+                    float2 dv = make_float2(d0.x + pend[0].x, d0.y + pend[0].y);
+                    if (s >= nsteps - (blockIdx.z == 0 ? a.hist : 0) && blockIdx.z == 0) {
+                        // a history row: add this call's share to what is there
+                        const float2 old = P2::ld(dp);
+                        dv = make_float2(old.x + dv.x, old.y + dv.y);
+                    }
+                    P2::st(dp, dv);
                     dp -= rowb;
                 }
 #pragma unroll
@@ -573,7 +588,7 @@ __global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kern
 #pragma unroll
                 for (int j = 0; j < CS::KM - 1; ++j) vw[j] = vw[j + 1];
                 vw[CS::KM - 1] = P2::ld(stage + (sb * CB_NROW + 4) * ROWB);
-                if (s >= H) {
+                if (s >= H && ttop - s >= 0) {
 #pragma unroll
                     for (int r = 0; r < 3; ++r) {
                         const float2 dn = P2::ld(stage + (sb * CB_NROW + r) * ROWB);  // du^(r)[t]
@@ -601,7 +616,7 @@ __global__ void __launch_bounds__(CB_THREADS, KA > 0 ? 2 : 1) msar_conv_bwd_kern
 // e = (koff_r + j) * d + c of every partial, summed over the partials in
 // order, lands at koff_r * d + c * k_r + j (conv_w's packing).
 __global__ void __launch_bounds__(256) msar_conv_sum_kernel(const float *parts, int64_t nparts, int64_t pstride, int d,
-                                                            int k0, int k1, int k2, float *out) {
+                                                            int k0, int k1, int k2, float *out, int accumulate) {
     const int ktot = k0 + k1 + k2;
     const int64_t n = (int64_t)ktot * d;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
@@ -610,7 +625,8 @@ __global__ void __launch_bounds__(256) msar_conv_sum_kernel(const float *parts, 
         const int jg = (int)(e / d), c = (int)(e - (int64_t)jg * d);
         const int kr = jg < k0 ? k0 : jg < k0 + k1 ? k1 : k2;
         const int koff = jg < k0 ? 0 : jg < k0 + k1 ? k0 : k0 + k1;
-        out[(int64_t)koff * d + (int64_t)c * kr + (jg - koff)] = s;
+        float *o = out + (int64_t)koff * d + (int64_t)c * kr + (jg - koff);
+        *o = accumulate ? *o + s : s;
     }
 }
 
@@ -715,7 +731,7 @@ cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, const float *parts, int64_t 
     const int64_t n = (int64_t)a.ktot * a.d;
     const int64_t blocks = (n + 255) / 256;
     msar_conv_sum_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        parts, nparts, part_stride, a.d, a.k[0], a.k[1], a.k[2], dconv_w);
+        parts, nparts, part_stride, a.d, a.k[0], a.k[1], a.k[2], dconv_w, a.acc);
     return cudaGetLastError();
 }
 

@@ -38,6 +38,12 @@ struct MsarBwdArgs {
     float *conv_parts;              // [chunks][n_src][ktot][d] partial sums of dconv_w (tap-major)
     float *dmix_w;                  // [4d][4]
     float *dmix_gain;               // [4d] or nullptr
+    // Chunked backward: src rows -hist .. -1 (and the matching dsrc rows)
+    // exist before row 0; the streams read them, the kernel gradients use
+    // them, and the conv transpose adds the chunk's share into their dsrc
+    // rows.  acc: the parameter gradients add into their outputs.
+    int64_t hist;
+    int acc;
 };
 
 cudaError_t msar_bwd_streams(int dt, const MsarBwdArgs &a, void *stream);
@@ -47,11 +53,12 @@ cudaError_t msar_fwd_mix(int dt, const MsarBwdArgs &a, void *out, void *stream);
 // mixer backward (dz, mix_e) and the per-chunk partials of A; d a multiple
 // of 1024 with nsl = d / 1024 (cudaErrorInvalidValue otherwise)
 cudaError_t msar_bwd_mix(int dt, const MsarBwdArgs &a, void *stream);
-// dmix_w and dmix_gain from A
+// dmix_w and dmix_gain from A (added into them when a.acc)
 cudaError_t msar_bwd_mix_finish(const MsarBwdArgs &a, const float *A, void *stream);
 cudaError_t msar_bwd_conv(int dt, const MsarBwdArgs &a, void *stream);
 // dconv_w (packed like conv_w) = the nparts conv partials at parts,
-// parts + part_stride, ... (floats) summed in order
+// parts + part_stride, ... (floats) summed in order (added into dconv_w when
+// a.acc)
 cudaError_t msar_bwd_conv_sum(const MsarBwdArgs &a, const float *parts, int64_t nparts, int64_t part_stride,
                               float *dconv_w, void *stream);
 // out[e] = (accumulate ? out[e] : 0) + sum_p parts[p][e] in order of p

@@ -556,6 +556,44 @@ attnres_status_t msar_expand_bwd_ps(const void *src, int64_t n_src, int64_t src_
                                     float *dmix_gain, float *dmix_w, void *workspace,
                                     size_t workspace_bytes, void *stream);
 
+/*
+ * msar_expand_bwd over one chunk of a longer sequence, so that the workspace
+ * is sized by the chunk's tokens, not the sequence's: the backward of the
+ * chunked prefill msar_expand_fwd_chunk.  src holds, per source, T_prev
+ * history rows followed by the chunk's T rows (as msar_expand_fwd_chunk); dh
+ * is the chunk's [T][d].  The causal convolutions read back into the history
+ * rows, so their transpose sends part of the chunk's gradient there.
+ * Defined by the chain rule of msar_expand_bwd (MSAR page, section 무엇과
+ * 다른가) over the chunk, with the chunked prefill of the dimensionstp.github.io
+ * review, sections 3-2 5) and 4-3.
+ *   src        [n_src] x [T_prev + T][d], src_stride (>= (T_prev+T)*d) apart
+ *   dsrc       [n_src] x [T_prev + T][d], dsrc_stride apart: the chunk's T
+ *              rows are overwritten; the chunk's share of the gradient of
+ *              the T_prev history rows is ADDED into the first T_prev rows
+ *   accumulate 0: the parameter gradients (dconv_w, dqueries, dgain,
+ *              dmix_gain, dmix_w) are overwritten; 1: the chunk's sums are
+ *              added into them
+ *   workspace  msar_expand_bwd_workspace_size(n_src, T, ...) bytes
+ * A whole sequence in order: chunk c of rows [t_c, t_{c+1}) with
+ * T_prev = min(t_c, max kernel size - 1) (src and dsrc pointing T_prev rows
+ * before t_c), accumulate = 0 for the first chunk and 1 after; then dsrc and
+ * every parameter gradient equal msar_expand_bwd's over the whole sequence
+ * (up to the order of the sums and one more rounding of the T_prev rows).
+ * Chunks must run in increasing order on one stream: a chunk overwrites its
+ * own rows, and the next chunk adds into their last T_prev.
+ * Every other argument, limit and error is msar_expand_bwd's; T_prev < 0 or
+ * accumulate not 0 or 1 is ATTNRES_ERR_INVALID_ARG.
+ */
+attnres_status_t msar_expand_bwd_chunk(const void *src, int64_t n_src, int64_t src_stride,
+                                       int64_t T_prev, int64_t T, int64_t d, attnres_dtype_t dt,
+                                       int64_t m, const int32_t *ksizes, const float *conv_w,
+                                       const float *queries, const float *gain, float eps,
+                                       const float *mix_gain, const float *mix_w, float mix_eps,
+                                       const void *dh, void *dsrc, int64_t dsrc_stride,
+                                       int accumulate, float *dconv_w, float *dqueries,
+                                       float *dgain, float *dmix_gain, float *dmix_w,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* Workspace bytes msar_expand_bwd (and msar_expand_bwd_ps) needs for these
  * sizes on the current device. */
 attnres_status_t msar_expand_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d,

@@ -384,6 +384,41 @@ def test_msar_bwd_T32768_d4096():
         assert torch.equal(x, y)
 
 
+def test_msar_bwd_chunked_T32768_d4096():
+    """The MSAR backward at the MSAR size in 8 chunks of 4096 tokens, each
+    with its 11 history rows, against the one-call backward: dsrc within the
+    bf16 elementwise bound (one more rounding of each chunk's history rows),
+    the parameter gradients within 2e-3 of their largest value; the chunk
+    workspace is an eighth of the one-call workspace (plus fixed parts)."""
+    T, d, N, chunk = 32768, 4096, 8, 4096
+    ks = (4, 8, 12)
+    src, g = inputs.device_sources(N, T, d, lambda n: 1.0 + n / 2.0, seed=2)
+    src = src.view(N, T, d)
+    q = inputs.device_normal((4, d), (16.0 / d) ** 0.5, g)
+    cw = torch.cat([inputs.device_normal((d * k,), (1.0 / k) ** 0.5, g) for k in ks])
+    mw = inputs.device_normal((4 * d, 4), (1.0 / (4 * d)) ** 0.5, g)
+    dh = torch.randn((T, d), generator=g, device="cuda").to(BF16)
+    one = attnres.msar_expand_bwd(src, ks, cw, q, dh, None, 1e-6, None, mw, 1e-6)
+    ws_one = attnres.msar_expand_bwd_workspace_size(N, T, d, BF16, ks)
+    ws_chunk = attnres.msar_expand_bwd_workspace_size(N, chunk, d, BF16, ks)
+    assert ws_chunk * 6 < ws_one
+    dsrc = torch.empty_like(src)
+    grads = (torch.empty_like(cw), torch.empty((4, d), device="cuda"), torch.empty((d,), device="cuda"),
+             torch.empty((4 * d,), device="cuda"), torch.empty((4 * d, 4), device="cuda"))
+    ws = torch.empty((ws_chunk + 3) // 4, dtype=torch.float32, device="cuda")
+    for c0 in range(0, T, chunk):
+        h = min(11, c0)
+        attnres.msar_expand_bwd_chunk(src[:, c0 - h:c0 + chunk], h, ks, cw, q, dh[c0:c0 + chunk],
+                                      dsrc[:, c0 - h:c0 + chunk], grads, c0 > 0, None, 1e-6, None, mw, 1e-6,
+                                      workspace=ws)
+    attnres.attnres_sync_status()
+    a, b = dsrc.float(), one[0].float()
+    bmax = b.abs().max()
+    assert bool(((a - b).abs() <= 2.0 ** -7 * b.abs() + 2e-3 * bmax).all())
+    for name, x, y in zip(("dconv_w", "dqueries", "dgain", "dmix_gain", "dmix_w"), grads, one[1:]):
+        assert float((x - y).abs().max()) <= 2e-3 * float(y.abs().max()), name
+
+
 def test_msar_bwd_per_source_T32768_d4096():
     """The backward with each source's own kernels at the MSAR size, by the
     same construction as the shared-kernel test: dh on a few clusters of 4

@@ -877,6 +877,79 @@ def test_msar_bwd_empty_sequence_zeroes_parameter_gradients():
         assert torch.count_nonzero(t) == 0
 
 
+def _msar_bwd_chunked_gpu(case, ks, dtype, bounds):
+    """msar_expand_bwd_chunk over the chunks [bounds[c], bounds[c+1]), in
+    order, each given min(t_c, max k - 1) history rows; the first chunk writes
+    the parameter gradients, the others add into them."""
+    src, q, cw, mw, g, mg, dh = case
+    dev = lambda x: to_dev(x, F32) if x is not None else None
+    n_src, T, d = src.shape
+    sd, dhd = to_dev(src, dtype), to_dev(dh, dtype)
+    dsrc = torch.full((n_src, T, d), float("nan"), dtype=dtype, device="cuda")
+    grads = (torch.full(cw.shape, float("nan"), device="cuda"), torch.full((4, d), float("nan"), device="cuda"),
+             torch.full((d,), float("nan"), device="cuda"), torch.full((4 * d,), float("nan"), device="cuda"),
+             torch.full((4 * d, 4), float("nan"), device="cuda"))
+    hist = max(ks) - 1
+    for c, (c0, c1) in enumerate(zip(bounds[:-1], bounds[1:])):
+        h = min(hist, c0)
+        attnres.msar_expand_bwd_chunk(sd[:, c0 - h:c1], h, ks, dev(cw), dev(q), dhd[c0:c1], dsrc[:, c0 - h:c1],
+                                      grads, c > 0, dev(g), 1e-6, dev(mg), dev(mw), 1e-6)
+    return (dsrc,) + grads
+
+
+@pytest.mark.parametrize("dtype,n_src,T,d,ks,bounds", [
+    (BF16, 8, 300, 1024, (4, 8, 12), (0, 5, 100, 180, 300)),
+    (F32, 5, 200, 2048, (4, 8, 12), (0, 64, 130, 200)),
+    (BF16, 4, 130, 1024, (16, 5, 9), (0, 40, 41, 130))])
+def test_msar_bwd_chunked_equals_one_call(dtype, n_src, T, d, ks, bounds):
+    """The backward in chunks of the sequence (each with its conv history
+    rows; short first chunks, a one-token chunk, kernels up to 16 taps) gives
+    the one-call backward's gradients: the sources' to one more rounding of
+    the history rows, the parameters' to the order of their sums (and, with
+    bf16, to the rounding of the intermediates: a chunk of at most 64 tokens
+    reads its streams with the few-token kernel, whose fp32 results can round
+    to the other neighbouring bf16 value); and both meet the bar against the
+    oracle."""
+    rng = _rng(T + d + n_src)
+    case = _msar_bwd_case(rng, n_src, T, d, dtype, ks, True)
+    got = _msar_bwd_chunked_gpu(case, ks, dtype, bounds)
+    one = _msar_bwd_gpu(case, ks, dtype)
+    for name, a_, b_ in zip(_MSAR_GRADS, got, one):
+        a_, b_ = to_host(a_), to_host(b_)
+        assert np.all(np.isfinite(a_)), name
+        bmax = np.abs(b_).max()
+        if name == "dsrc" and dtype == BF16:
+            assert np.all(np.abs(a_ - b_) <= 2.0 ** -7 * np.abs(b_) + 2e-3 * bmax), name
+        else:
+            tol = 2e-3 if dtype == BF16 else 1e-4
+            assert np.abs(a_ - b_).max() <= tol * bmax, (name, np.abs(a_ - b_).max(), bmax)
+    src, q, cw, mw, g, mg, dh = case
+    ref = oracle.msar_bwd(src, ks, cw, q, dh, g, 1e-6, mg, mw, 1e-6)
+    _check_msar_grads(got, ref, dtype, f"chunked n_src={n_src} T={T} d={d}")
+
+
+def test_msar_bwd_chunk_adds_into_history_rows_only():
+    """A chunk writes its own rows of dsrc and adds its share into the history
+    rows: with the history rows preset to 1, the result there is 1 plus the
+    gradient that the chunk alone sends back to them."""
+    rng = _rng(77)
+    ks, n_src, T, d = (4, 8, 12), 3, 40, 1024
+    src, q, cw, mw, g, mg, dh = _msar_bwd_case(rng, n_src, T, d, BF16, ks, False)
+    dev = lambda x: to_dev(x, F32)
+    sd = to_dev(src, BF16)
+    dh_last = to_dev(dh, BF16)[20:]
+    grads = (torch.empty(cw.shape, device="cuda"), torch.empty((4, d), device="cuda"), None, None,
+             torch.empty((4 * d, 4), device="cuda"))
+    a = torch.ones((n_src, 31, d), dtype=BF16, device="cuda")
+    attnres.msar_expand_bwd_chunk(sd[:, 9:40], 11, ks, dev(cw), dev(q), dh_last, a, grads, False, mix_w=dev(mw))
+    b = torch.zeros((n_src, 31, d), dtype=BF16, device="cuda")
+    attnres.msar_expand_bwd_chunk(sd[:, 9:40], 11, ks, dev(cw), dev(q), dh_last, b, grads, False, mix_w=dev(mw))
+    assert torch.equal(a[:, 11:], b[:, 11:])
+    # a's history rows are bf16(1 + share), b's bf16(share): equal to one rounding
+    assert torch.allclose(a[:, :11].float(), b[:, :11].float() + 1, rtol=2.0 ** -7, atol=2.0 ** -7)
+    assert torch.count_nonzero(b[:, :11]) > 0
+
+
 @pytest.mark.parametrize("dtype,n_src,T,d,ks", [(BF16, 8, 70, 4096, (4, 8, 12)), (F32, 3, 200, 1024, (4, 8, 12)),
                                                  (BF16, 5, 45, 2048, (16, 5, 9)), (F32, 1, 33, 1024, (1, 2, 3))])
 def test_msar_bwd_per_source_kernels(dtype, n_src, T, d, ks):
