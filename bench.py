@@ -430,6 +430,49 @@ class ReadBwdWorkload(BlockWorkload):
         return src.shape[1]
 
 
+class DeepReadBwdWorkload(ReadBwdWorkload):
+    """Backward of the deepest layer of Full AttnRes at depth: one query over
+    L = 64 sources ~ N(0, (1 + i/16)^2), bf16, d = 4096, T = 16384, output
+    gradient ~ N(0, 1).  More sources than one pass of the backward kernel
+    takes: chunks of 8 with their read states recomputed, the merge's
+    backward, and each chunk's backward with its lse gradient.  Algorithmic
+    bytes per token: the sources and the output gradient read, the sources'
+    gradients written."""
+
+    def __init__(self, T=16384, d=4096, L=64, seed=0):
+        super().__init__(T, d, L - 1, seed)
+        self.name = "attnres_read_backward_depth"
+        self.L = L
+        self.bytes_per_token = (2 * L + 1) * d * 2
+        self.phase1_bytes_per_token = self.bytes_per_token
+        C = (L + 7) // 8
+        self.launches_per_step = C + 1 + 2 * C + 2 * C
+        self.dominant = "read backward over 64 sources (whole chain)"
+        self.dominant_src = "read_bwd"
+        self.profile_tag = f"ncu_read_bwd_depth_d{d}_L{L}"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = f"{self.name} bf16 d={self.d} n_src={self.L} n_q=1 T={self.T}"
+        return c
+
+    def setup(self, device):
+        import torch
+        from depth_wise_attention_gb300 import attnres, inputs
+        T, d, L = self.T, self.d, self.L
+        self.src, g = inputs.device_sources(L, T, d, lambda n: 1.0 + n / 16.0, seed=self.seed, device=device)
+        self.src = self.src.view(L, T, d)
+        self.queries = inputs.device_normal((1, d), (16.0 / d) ** 0.5, g, device=device)
+        self.gain = torch.ones((d,), dtype=torch.float32, device=device)
+        self.dout = torch.randn((1, T, d), generator=g, device=device).to(torch.bfloat16)
+        self.dsrc = torch.empty_like(self.src)
+        self.dq = torch.empty((1, d), dtype=torch.float32, device=device)
+        self.dg = torch.empty((d,), dtype=torch.float32, device=device)
+        nb = attnres.attnres_read_bwd_workspace_size(L, T, d, 1, torch.bfloat16)
+        self.ws = torch.empty(((nb + 3) // 4,), dtype=torch.float32, device=device)
+        self.cache = self.src
+
+
 class BlockBwdWorkload(BlockWorkload):
     """Backward of the headline Block step (bf16, d=4096, N=8, S=4): the
     merge backward of each layer (layers 2..4 with their partials, layer 1
@@ -1475,7 +1518,7 @@ class MsarBlockBwdWorkload(MsarBlockWorkload):
 
 WORKLOADS = ["block", "block_d2048", "block_fused", "block_bwd", "read_bwd", "mhar_bwd", "mhar_block",
              "msar_chunked", "msar_ps", "decode", "mhar", "msar", "msar_block", "msar_bwd", "msar_bwd_ps", "msar_ws",
-             "msar_block_ws", "msar_block_bwd", "full_depth", "msar_bwd_chunked"]
+             "msar_block_ws", "msar_block_bwd", "full_depth", "msar_bwd_chunked", "depth_bwd"]
 
 
 def make_workload(name, T=None):
@@ -1511,6 +1554,8 @@ def make_workload(name, T=None):
         return MsarBwdWorkload(T=T or 32768)
     if name == "msar_bwd_chunked":
         return MsarBwdChunkedWorkload(T=T or 32768)
+    if name == "depth_bwd":
+        return DeepReadBwdWorkload(T=T or 16384)
     if name == "msar_block_bwd":
         return MsarBlockBwdWorkload(T=T or 32768)
     if name == "msar_bwd_ps":

@@ -38,6 +38,7 @@ SOURCES = [
     "msar_phase1.cu",
     "msar_phase2.cu",
     "msar_bwd.cu",
+    "state_merge_bwd.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

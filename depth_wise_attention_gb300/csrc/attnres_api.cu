@@ -20,6 +20,7 @@
 #include "phase2.cuh"
 #include "merge_bwd.cuh"
 #include "read_bwd.cuh"
+#include "state_merge_bwd.h"
 
 using namespace attnres;
 
@@ -786,6 +787,131 @@ attnres_status_t launch_merge_bwd(const void *o, const float *lse, const void *p
     void *fargs[] = {&f};
     e = cudaLaunchKernel(read_bwd_finish_fn(), dim3((unsigned)((d + 255) / 256)), dim3(256), fargs, 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "merge backward finish launch");
+    return ATTNRES_OK;
+}
+
+// ------------------------------------------------ read backward, > 16 sources
+// The sources in chunks of 8: each chunk's read state (o_c, lse_c) is
+// recomputed with the forward read kernels, the backward of the states'
+// online-softmax merge gives each chunk's d o_c and d lse_c
+// (state_merge_bwd.cu), and each chunk runs the read backward with its lse
+// gradient.  The chunks' query and gain gradients are summed in chunk order.
+constexpr int64_t kReadBwdChunk = 8;        // sources per chunk
+constexpr int64_t kReadBwdMaxChunks = 32;   // merge kernel limit: 256 sources
+
+struct ReadBwdManyPlan {
+    int64_t C;
+    size_t rb_bytes, off_o, off_lse, off_do, off_dlse, off_rb, off_dq, off_dg, total;
+};
+
+attnres_status_t read_bwd_many_plan(int64_t n_src, int64_t T, int64_t d, int64_t n_q, attnres_dtype_t dt,
+                                    const DeviceInfo *dev, ReadBwdManyPlan *p) {
+    p->C = (n_src + kReadBwdChunk - 1) / kReadBwdChunk;
+    if (p->C > kReadBwdMaxChunks) return ATTNRES_ERR_UNSUPPORTED;
+    // the largest workspace over the chunk sizes (a short last chunk may tile wider)
+    p->rb_bytes = 0;
+    const int64_t sizes[2] = {kReadBwdChunk, n_src - (p->C - 1) * kReadBwdChunk};
+    for (int64_t nc : sizes) {
+        ReadBwdShape sh;
+        attnres_status_t st = read_bwd_shape(nc, d, n_q, 1, dt, &sh);
+        if (st != ATTNRES_OK) return st;
+        const size_t b = read_bwd_ws_bytes(dev->sms, sh, d);
+        if (b > p->rb_bytes) p->rb_bytes = b;
+    }
+    const size_t es = esize(dt);
+    const size_t states = (size_t)p->C * (size_t)n_q * (size_t)T;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    p->off_o = take(states * (size_t)d * es);
+    p->off_lse = take(states * 4);
+    p->off_do = take(states * (size_t)d * es);
+    p->off_dlse = take(states * 4);
+    p->off_rb = take(p->rb_bytes);
+    p->off_dq = take((size_t)n_q * (size_t)d * 4);
+    p->off_dg = take((size_t)d * 4);
+    p->total = off;
+    return ATTNRES_OK;
+}
+
+attnres_status_t launch_read_bwd_many(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
+                                      attnres_dtype_t dt, const float *queries, int64_t n_q, const float *gain,
+                                      float eps, const void *dout, const float *dlse, void *dsrc,
+                                      int64_t dsrc_stride, int accumulate, float *dq, float *dgain, void *ws,
+                                      size_t ws_bytes, void *stream) {
+    attnres_status_t st = check_common(src, n_src, src_stride, T, d, dt, eps);
+    if (st != ATTNRES_OK) return st;
+    if (n_q < 1 || (accumulate != 0 && accumulate != 1)) return ATTNRES_ERR_INVALID_ARG;
+    if (T > 0 && (!queries || !dout || !dsrc || !dq || !ws)) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+    if (n_q > 8 || (n_src + kReadBwdChunk - 1) / kReadBwdChunk > kReadBwdMaxChunks) return ATTNRES_ERR_UNSUPPORTED;
+    const size_t es = esize(dt);
+    const size_t src_bytes = ((size_t)(n_src - 1) * (size_t)src_stride + (size_t)T * (size_t)d) * es;
+    const size_t dsrc_bytes = ((size_t)(n_src - 1) * (size_t)dsrc_stride + (size_t)T * (size_t)d) * es;
+    const size_t dout_bytes = (size_t)n_q * (size_t)T * (size_t)d * es;
+    const size_t dq_bytes = (size_t)n_q * (size_t)d * sizeof(float);
+    if (overlap(dsrc, dsrc_bytes, src, src_bytes) || overlap(dsrc, dsrc_bytes, dout, dout_bytes) ||
+        overlap(ws, ws_bytes, src, src_bytes) || overlap(ws, ws_bytes, dsrc, dsrc_bytes) ||
+        overlap(ws, ws_bytes, dout, dout_bytes) || overlap(dq, dq_bytes, ws, ws_bytes) ||
+        (dgain && (overlap(dgain, (size_t)d * 4, ws, ws_bytes) || overlap(dgain, (size_t)d * 4, dq, dq_bytes))) ||
+        (dlse && overlap(dsrc, dsrc_bytes, dlse, (size_t)n_q * (size_t)T * 4)))
+        return ATTNRES_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTNRES_OK) return st;
+    ReadBwdManyPlan p;
+    st = read_bwd_many_plan(n_src, T, d, n_q, dt, dev, &p);
+    if (st != ATTNRES_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(dq, 0, dq_bytes, s);
+        if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, s);
+        return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (ws_bytes < p.total) return ATTNRES_ERR_INVALID_ARG;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const size_t state_bytes = (size_t)n_q * (size_t)T * (size_t)d * es;   // one chunk's o
+    const unsigned char *sb = static_cast<const unsigned char *>(src);
+    unsigned char *db = static_cast<unsigned char *>(dsrc);
+    // each chunk's read state
+    for (int64_t c = 0; c < p.C; ++c) {
+        const int64_t nc = c + 1 < p.C ? kReadBwdChunk : n_src - c * kReadBwdChunk;
+        st = launch_depth_read(sb + (size_t)(c * kReadBwdChunk) * (size_t)src_stride * es, nc, src_stride, T, d, 1,
+                               dt, queries, n_q, gain, eps, w + p.off_o + (size_t)c * state_bytes,
+                               reinterpret_cast<float *>(w + p.off_lse) + (size_t)c * n_q * T, stream);
+        if (st != ATTNRES_OK) return st;
+    }
+    // the merge's backward: each chunk's d o_c and d lse_c
+    StateMergeBwdArgs m;
+    m.o = w + p.off_o;
+    m.lse = reinterpret_cast<const float *>(w + p.off_lse);
+    m.dh = static_cast<const unsigned char *>(dout);
+    m.dlse = dlse;
+    m.d_o = w + p.off_do;
+    m.d_lse = reinterpret_cast<float *>(w + p.off_dlse);
+    m.C = (int)p.C;
+    m.rows = n_q * T;
+    m.d = (int)d;
+    cudaError_t e = launch_state_merge_bwd(dt == ATTNRES_BF16 ? 1 : 0, m, dev->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "state merge backward launch");
+    // each chunk's read backward; its query and gain gradients summed in chunk order
+    float *dq_c = reinterpret_cast<float *>(w + p.off_dq);
+    float *dg_c = dgain ? reinterpret_cast<float *>(w + p.off_dg) : nullptr;
+    for (int64_t c = 0; c < p.C; ++c) {
+        const int64_t nc = c + 1 < p.C ? kReadBwdChunk : n_src - c * kReadBwdChunk;
+        st = launch_read_bwd(sb + (size_t)(c * kReadBwdChunk) * (size_t)src_stride * es, nc, src_stride, T, d, 1, dt,
+                             queries, n_q, gain, eps, w + p.off_do + (size_t)c * state_bytes,
+                             reinterpret_cast<const float *>(w + p.off_dlse) + (size_t)c * n_q * T,
+                             db + (size_t)(c * kReadBwdChunk) * (size_t)dsrc_stride * es, dsrc_stride, accumulate,
+                             dq_c, dg_c, w + p.off_rb, p.rb_bytes, stream);
+        if (st != ATTNRES_OK) return st;
+        e = msar_bwd_sum(dq_c, 1, n_q * d, dq, c > 0 ? 1 : 0, stream);
+        if (e == cudaSuccess && dgain) e = msar_bwd_sum(dg_c, 1, d, dgain, c > 0 ? 1 : 0, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "read backward chunk sums launch");
+    }
     return ATTNRES_OK;
 }
 
@@ -1788,6 +1914,19 @@ static attnres_status_t read_bwd_workspace(int64_t n_src, int64_t T, int64_t d, 
         d % H != 0)
         return ATTNRES_ERR_INVALID_ARG;
     if (d % 8 != 0) return ATTNRES_ERR_UNSUPPORTED;
+    if (n_src > 16 && H == 1) {
+        // more sources than one pass takes: chunks of 8 and their states
+        if (n_q > 8 || (n_src + kReadBwdChunk - 1) / kReadBwdChunk > kReadBwdMaxChunks)
+            return ATTNRES_ERR_UNSUPPORTED;
+        DeviceInfo *dev = nullptr;
+        attnres_status_t st = device_info(&dev);
+        if (st != ATTNRES_OK) return st;
+        ReadBwdManyPlan p;
+        st = read_bwd_many_plan(n_src, T, d, n_q, dt, dev, &p);
+        if (st != ATTNRES_OK) return st;
+        *bytes = p.total;
+        return ATTNRES_OK;
+    }
     ReadBwdShape sh;
     attnres_status_t st = read_bwd_shape(n_src, d, n_q, H, dt, &sh);
     if (st != ATTNRES_OK) return st;
@@ -1808,6 +1947,9 @@ attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_st
                                   float eps, const void *dout, void *dsrc, int64_t dsrc_stride, int accumulate,
                                   float *dqueries, float *dgain, void *workspace, size_t workspace_bytes,
                                   void *stream) {
+    if (n_src > 16)
+        return launch_read_bwd_many(src, n_src, src_stride, T, d, dt, queries, n_q, gain, eps, dout, nullptr, dsrc,
+                                    dsrc_stride, accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
     return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, dout, nullptr, dsrc,
                            dsrc_stride,
                            accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
@@ -1851,6 +1993,9 @@ attnres_status_t attnres_block_phase1_bwd(const void *src, int64_t n_src, int64_
                                           const float *gain, float eps, const void *d_o, const float *d_lse,
                                           void *dsrc, int64_t dsrc_stride, int accumulate, float *dqueries,
                                           float *dgain, void *workspace, size_t workspace_bytes, void *stream) {
+    if (n_src > 16)
+        return launch_read_bwd_many(src, n_src, src_stride, T, d, dt, queries, n_q, gain, eps, d_o, d_lse, dsrc,
+                                    dsrc_stride, accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
     return launch_read_bwd(src, n_src, src_stride, T, d, 1, dt, queries, n_q, gain, eps, d_o, d_lse, dsrc,
                            dsrc_stride, accumulate, dqueries, dgain, workspace, workspace_bytes, stream);
 }

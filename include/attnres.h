@@ -233,9 +233,19 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  * No output may overlap an input or the workspace.  T = 0 zeroes dqueries and
  * dgain.  The queries are taken in passes of 2 (of 1 with more than 8
  * sources) over the sources; later passes add into dsrc and dgain, so with
- * more than one pass a bf16 dsrc is rounded once per pass.  Limits:
- * n_src <= 16; the n_src + (queries of a pass) rows of a token tile must fit
- * two shared-memory stages (for d = 4096 bf16, n_src + 2 <= 13).
+ * more than one pass a bf16 dsrc is rounded once per pass.
+ * More than 16 sources (Full AttnRes past layer 16): the sources are taken in
+ * chunks of 8.  Each chunk's read state (o_c, lse_c) is recomputed, and the
+ * backward of the states' online-softmax merge (b-lab.team summary, section
+ * 3: LSE = log sum_c e^{lse_c}, beta_c = e^{lse_c - LSE}, h = sum_c beta_c o_c)
+ * gives d o_c = beta_c dout and d lse_c = beta_c (dout . o_c - dout . h).
+ * Then each chunk runs this backward with its lse gradient
+ * (attnres_block_phase1_bwd).  The states are held in dtype dt, so with bf16
+ * the query and gain gradients carry that rounding; the workspace then also
+ * holds the states (about 2 ceil(n_src/8) n_q T d elements of dt).
+ * Limits: at most 256 sources (32 chunks) and, above 16 sources, 8 queries;
+ * up to 16 sources, the n_src + (queries of a pass) rows of a token tile must
+ * fit two shared-memory stages (for d = 4096 bf16, n_src + 2 <= 13).
  */
 attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
                                   int64_t d, attnres_dtype_t dt, const float *queries, int64_t n_q,

@@ -157,13 +157,14 @@ def test_read_bwd_validation(lib):
     assert bw(dsrc=SRC + 64) == INV                    # overlaps the sources
     assert bw(ws=DO + 32) == INV                       # workspace overlaps dout
     assert bw(dq=WS + 64) == INV                       # dq overlaps the workspace
-    assert bw(n_src=17) == UNS
+    assert bw(n_src=257) == UNS                        # more than 32 chunks of 8 sources
     assert bw(dout=DO + 8) == UNS                      # misaligned
     assert bw(dg=None, T=0) != INV                     # dgain is optional
     n = ctypes.c_size_t(0)
     assert lib.attnres_read_bwd_workspace_size(9, 16, 64, 1, BF16, None) == INV
     assert lib.attnres_read_bwd_workspace_size(9, 16, 60, 1, BF16, ctypes.byref(n)) == UNS
-    assert lib.attnres_read_bwd_workspace_size(17, 16, 64, 1, BF16, ctypes.byref(n)) == UNS
+    assert lib.attnres_read_bwd_workspace_size(257, 16, 64, 1, BF16, ctypes.byref(n)) == UNS
+    assert lib.attnres_read_bwd_workspace_size(17, 16, 64, 9, BF16, ctypes.byref(n)) == UNS
     # more queries than one pass takes are accepted (passes of 2, or of 1 above 8 sources)
     for n_src, n_q in ((9, 3), (8, 5)):
         assert lib.attnres_read_bwd_workspace_size(n_src, 16, 64, n_q, BF16, ctypes.byref(n)) not in (INV, UNS)

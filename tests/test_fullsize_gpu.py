@@ -341,6 +341,31 @@ def test_read_bwd_T32768_d4096_bench_workload():
         assert np.abs(w - s_).max() <= 1e-4 * np.abs(w).max(), name
 
 
+def test_read_bwd_64_sources_T16384_d4096():
+    """The backward of the deepest layer of Full AttnRes at depth (64 sources,
+    T = 16384, d = 4096, bf16), past one pass of the backward kernel: sampled
+    source gradients against the oracle; the query and gain gradients equal
+    the sums of the two halves' runs."""
+    T, d, L = 16384, 4096, 64
+    src, g = inputs.device_sources(L, T, d, lambda n: 1.0 + n / 16.0, seed=4)
+    src = src.view(L, T, d)
+    q = inputs.device_normal((1, d), (16.0 / d) ** 0.5, g)
+    gain = torch.ones((d,), dtype=F32, device="cuda")
+    dout = torch.randn((1, T, d), generator=g, device="cuda").to(BF16)
+    dsrc, dq, dg = attnres.attnres_read_bwd(src, q, dout, gain)
+    attnres.attnres_sync_status()
+    idx = sampled_tokens(T, n=100)
+    ref = oracle.read_bwd(rows(src, idx), q.cpu().numpy().astype(np.float64), rows(dout, idx), None, 1e-6)
+    check_out(rows(dsrc, idx), ref[0], BF16, what="dsrc")
+    del dsrc
+    h = T // 2
+    parts = [attnres.attnres_read_bwd(src[:, a:b].contiguous(), q, dout[:, a:b].contiguous(), gain)[1:]
+             for a, b in ((0, h), (h, T))]
+    for name, whole, (x, y) in (("dq", dq, (parts[0][0], parts[1][0])), ("dgain", dg, (parts[0][1], parts[1][1]))):
+        w, s_ = to_host(whole), to_host(x) + to_host(y)
+        assert np.abs(w - s_).max() <= 1e-4 * np.abs(w).max(), name
+
+
 def test_msar_bwd_T32768_d4096():
     """Backward of the MSAR read at the MSAR size.  Every gradient is linear
     in dh and the read of token t sees source rows t-11..t only, so with dh

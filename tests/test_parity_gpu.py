@@ -412,6 +412,49 @@ def test_read_bwd(n_src, n_q, T, d, dtype, with_gain):
     _check_grads(got, oracle.read_bwd(src, q, dout, g, 1e-6), dtype, f"n_src={n_src}")
 
 
+@pytest.mark.parametrize("n_src,n_q,T,d,dtype,with_gain", [
+    (17, 1, 50, 1024, BF16, True), (33, 2, 40, 4096, BF16, False), (24, 4, 30, 512, F32, True),
+    (64, 1, 70, 2048, BF16, True), (20, 3, 100, 4096, BF16, True), (41, 1, 3, 1024, F32, False)])
+def test_read_bwd_many_sources(n_src, n_q, T, d, dtype, with_gain):
+    """More sources than one pass of the backward kernel takes (> 16): the
+    sources in chunks of 8, each chunk's read state recomputed, the backward of
+    the states' merge, then each chunk's backward with its lse gradient;
+    against the oracle's chain rule over all sources at once."""
+    rng = _rng(n_src * 3 + n_q + T + d)
+    src = _sources(rng, n_src, T, d, dtype, step=0.1)
+    q = _queries(rng, n_q, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gain else None
+    dout = _sources(rng, n_q, T, d, dtype, step=0)
+    got = attnres.attnres_read_bwd(to_dev(src, dtype), to_dev(q, F32), to_dev(dout, dtype),
+                                   to_dev(g, F32) if with_gain else None, 1e-6)
+    _check_grads_states(got, oracle.read_bwd(src, q, dout, g, 1e-6), dtype, f"n_src={n_src}")
+
+
+def _check_grads_states(got, ref, dtype, what):
+    """As _check_grads, but the chunks' states (o_c and beta_c dh) are held in
+    the source dtype between the steps, so the parameter gradients (sums over
+    the tokens) carry that rounding: they are held to the dtype's bar, as the
+    two-phase Block backward's are."""
+    dsrc, dq, dg = got
+    rs, rq, rg = ref
+    check_out(dsrc, rs, dtype, what=f"{what} dsrc")
+    for name, g_, r_ in (("dq", dq, rq), ("dgain", dg, rg)):
+        if g_ is not None:
+            check_out(g_, r_, dtype if dtype == BF16 else F32, np.abs(r_).max(), strict=False, what=f"{what} {name}")
+
+
+def test_block_phase1_bwd_many_sources_with_lse_gradient():
+    """The phase-1 backward (o and lse gradients) over 28 sources."""
+    rng = _rng(28)
+    n_src, n_q, T, d = 28, 2, 45, 1024
+    src = _sources(rng, n_src, T, d, BF16, step=0.1)
+    q = _queries(rng, n_q, d)
+    d_o = _sources(rng, n_q, T, d, BF16, step=0)
+    dlse = rng.standard_normal((n_q, T)).astype(np.float32)
+    got = attnres.attnres_block_phase1_bwd(to_dev(src, BF16), to_dev(q, F32), to_dev(d_o, BF16), to_dev(dlse, F32))
+    _check_grads_states(got, oracle.block_phase1_bwd(src, q, d_o, dlse, None, 1e-6), BF16, "phase 1, 28 sources")
+
+
 def test_read_bwd_accumulates_and_is_deterministic():
     rng = _rng(51)
     n_src, T, d = 9, 200, 4096
