@@ -7,6 +7,14 @@ Tolerances (written here once, used by every GPU parity test):
   result is at most 2^-8 relative; the bound leaves room for the float32
   arithmetic before it, or for the two-phase path's second rounding of its
   phase-1 state where the two errors do not line up).
+* bf16 chains (chain=True): paths that hold intermediates in bf16 between
+  their steps (the MSAR workspace chains and backwards, the two-phase
+  backwards, the read backward's chunk states) round up to about seven more
+  times before the output, each rounding at most 2^-8 relative to what it
+  rounds.  Elementwise they are held to 4x the bound above (measured worst
+  3.34x, on under 4% of the elements of a tensor), and per tensor to the
+  stated bar.  Their fp32 parameter gradients (sums over the tokens of those
+  intermediates) are held to the same pair of bounds.
 * f32 storage: max|gpu - ref| <= 1e-4 * max|v| over the sources (the stated
   bar), and elementwise <= 1e-5 * max|v|.
 * lse (float32): |gpu - ref| <= 1e-4 * (1 + |ref|).
@@ -27,7 +35,7 @@ def to_host(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def check_out(gpu, ref, dtype, src_absmax=None, strict=True, what="out"):
+def check_out(gpu, ref, dtype, src_absmax=None, strict=True, what="out", chain=False):
     gpu = to_host(gpu) if isinstance(gpu, torch.Tensor) else gpu
     ref = np.asarray(ref, np.float64)
     assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
@@ -37,8 +45,8 @@ def check_out(gpu, ref, dtype, src_absmax=None, strict=True, what="out"):
     if dtype == torch.bfloat16:
         assert err.max(initial=0.0) <= BF16_REL * rmax + 1e-30, \
             f"{what}: max err {err.max()} > {BF16_REL} * {rmax}"
-        if strict:
-            bound = 2.0 ** -7 * np.abs(ref) + 2e-3 * rmax
+        if strict or chain:
+            bound = (4.0 if chain else 1.0) * (2.0 ** -7 * np.abs(ref) + 2e-3 * rmax)
             bad = err > bound
             assert not bad.any(), f"{what}: {bad.sum()} elements beyond the elementwise bound, " \
                                   f"worst {err.max()}"

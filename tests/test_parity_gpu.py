@@ -440,7 +440,8 @@ def _check_grads_states(got, ref, dtype, what):
     check_out(dsrc, rs, dtype, what=f"{what} dsrc")
     for name, g_, r_ in (("dq", dq, rq), ("dgain", dg, rg)):
         if g_ is not None:
-            check_out(g_, r_, dtype if dtype == BF16 else F32, np.abs(r_).max(), strict=False, what=f"{what} {name}")
+            check_out(g_, r_, dtype if dtype == BF16 else F32, np.abs(r_).max(), strict=False, chain=dtype == BF16,
+                      what=f"{what} {name}")
 
 
 def test_block_phase1_bwd_many_sources_with_lse_gradient():
@@ -574,12 +575,13 @@ def test_block_two_phase_backward_equals_one_shot(dtype, N, S, T, d):
         rs, rq, _ = oracle.read_bwd(srcs, q[s_][None], dh[s_][None], None, 1e-6)
         ref_cached += rs[:N]
         if s_ > 0:
-            check_out(dpart[s_], rs[N], dtype, np.abs(rs[N]).max() * 4 + 1e-30, strict=False,
+            check_out(dpart[s_], rs[N], dtype, np.abs(rs[N]).max() * 4 + 1e-30, strict=False, chain=dtype == BF16,
                       what=f"layer {s_ + 1} d_partial")
         # the chain's intermediates (o, d_o) are stored in the source dtype,
         # so its parameter gradients carry that rounding
         gq = to_host(dq1)[s_] + dq2[s_]
-        check_out(gq, rq[0], dtype, np.abs(rq[0]).max() + 1e-30, strict=False, what=f"layer {s_ + 1} dq")
+        check_out(gq, rq[0], dtype, np.abs(rq[0]).max() + 1e-30, strict=False, chain=dtype == BF16,
+                  what=f"layer {s_ + 1} dq")
     check_out(dsrc, ref_cached, dtype, what="cached sources' gradient")
 
 
@@ -868,7 +870,7 @@ def _check_msar_grads(got, ref, dtype, what):
     roundings too."""
     for name, g_, r_ in zip(_MSAR_GRADS, got, ref):
         r_ = np.asarray(r_).reshape(tuple(g_.shape))
-        check_out(g_, r_, dtype, np.abs(r_).max(), strict=False, what=f"{what} {name}")
+        check_out(g_, r_, dtype, np.abs(r_).max(), strict=False, chain=dtype == BF16, what=f"{what} {name}")
 
 
 @pytest.mark.parametrize("dtype,n_src,T,d,ks,with_gains", [
@@ -1137,7 +1139,7 @@ def _check_all(got, ref, names, dtype, what):
             assert g_ is None, name
             continue
         r_ = np.asarray(r_).reshape(tuple(g_.shape))
-        check_out(g_, r_, dtype, np.abs(r_).max(), strict=False, what=f"{what} {name}")
+        check_out(g_, r_, dtype, np.abs(r_).max(), strict=False, chain=dtype == BF16, what=f"{what} {name}")
 
 
 _P2B = ("d_o", "d_lse", "d_partial", "dconv_w", "dquery", "dgain", "dmix_gain", "dmix_w")
