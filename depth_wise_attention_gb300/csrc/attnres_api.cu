@@ -245,11 +245,16 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     // CTAs per SM) when its chunks are nearly full and numerous: measured at
     // d = 4096 from 24 sources on with a last chunk of 5..8 rows (up to 7%
     // faster at 64 sources; slower at d = 2048, so only d = 4096 is built).
+    // One query over at most 4 sources at d = 4096 (the first layers of Full
+    // AttnRes at depth): the one-token kernel costs about the same whatever
+    // its rows, and the general kernel's tiles of several tokens are faster
+    // (measured at T = 16384: 0.12-0.26 ms against 0.28 ms).
     const int kv = g_kernel_variant.load();
     const bool chunked = n_src > 8;
     const bool chunked_wins = n_src >= 24 && (n_src % 8 == 0 || n_src % 8 >= 5);
+    const bool few_rows = d == 4096 && n_q == 1 && H == 1 && n_src <= 4;
     if (dt == ATTNRES_BF16 && n_q <= 4 && (d == 1024 || d == 2048 || d == 4096) && kv != 1 &&
-        (!chunked || (d == 4096 && (chunked_wins || kv == 2)))) {
+        (!few_rows || kv == 2) && (!chunked || (d == 4096 && (chunked_wins || kv == 2)))) {
         const bool two = !chunked && d <= 1024;
         const int nw = d <= 2048 ? 8 : 16;
         const int ks = (int)(d / (16 * nw));
