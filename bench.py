@@ -1017,6 +1017,7 @@ class MsarBwdChunkedWorkload(MsarBwdWorkload):
         self.chunk = chunk
         self.launches_per_step *= (T + chunk - 1) // chunk
         self.dominant = "msar backward, chunked (whole chain per chunk)"
+        self.profile_tag = f"ncu_msar_bwd_chunked_d{d}"
 
     def config(self):
         c = super().config()
