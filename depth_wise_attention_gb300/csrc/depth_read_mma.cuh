@@ -223,34 +223,35 @@ __device__ __forceinline__ void dm_query_fragments_packed(const DepthReadMmaArgs
         }
 }
 
-// Pass 1 with dm_query_fragments_packed.  On return lanes (i = g4, t4 = 2q,
-// 2q+1) hold dot_qi and lanes 4i.. hold sum(v_i^2).
+// Pass 1 with dm_query_fragments_packed.  The sums of squares come from the
+// tensor cores too, as the diagonal of the Gram matrix G = X X^T: the
+// ldmatrix fragment of X is already the B fragment of X^T (lane (g4, t4)
+// holds X[g4][2t4..2t4+1] and X[g4][8+2t4..]), so one MMA per k-step
+// replaces the unpacking and packed FMAs (products exact, sums fp32).  With
+// one or two queries the dots take one MMA per two k-steps, and the Gram MMAs
+// fill the idle tensor pipe; with more queries (dm_pass1_rows8) they would
+// lengthen the per-token chain, measured 1.7% slower there.  On return lanes
+// (i = g4, t4 = 2q, 2q+1) hold dot_qi and lane (i, i/2) holds sum(v_i^2).
 template <int KS>
 __device__ __forceinline__ void dm_pass1_rows8_packed(uint32_t sa, const uint32_t (&bq)[KS / 2][2], int t4,
                                                       float &dot, float &ssq) {
-    float d1[2][4];
+    float d1[2][4], gr[2][4];
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) d1[u][e] = 0.f;
-    float2 sq = make_float2(0.f, 0.f);
+        for (int e = 0; e < 4; ++e) { d1[u][e] = 0.f; gr[u][e] = 0.f; }
 #pragma unroll
     for (int s2 = 0; s2 < KS / 2; ++s2) {
         uint32_t x0, x1, x2, x3;            // k-step a: (x0, x1); k-step b: (x2, x3)
         ldsm_x4(sa + 64 * s2, x0, x1, x2, x3);
         mma_full(d1[s2 & 1], x0, x2, x1, x3, bq[s2][0], bq[s2][1]);
-        const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
-        sq = ffma2(f0, f0, sq);
-        sq = ffma2(f1, f1, sq);
-        sq = ffma2(f2, f2, sq);
-        sq = ffma2(f3, f3, sq);
+        mma_rows8(gr[0], x0, x1, x0, x1);
+        mma_rows8(gr[1], x2, x3, x2, x3);
     }
     const float part = (t4 & 1) ? (d1[0][2] + d1[1][2]) + (d1[0][3] + d1[1][3])
                                 : (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
     dot = part + __shfl_xor_sync(0xffffffffu, part, 1);
-    ssq = sq.x + sq.y;
-    ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
-    ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+    ssq = (threadIdx.x & 4) ? gr[0][1] + gr[1][1] : gr[0][0] + gr[1][0];
 }
 
 // Sum over the wph warps of a head (starting at gw0) of the partial sum of
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) depth_read_mma_kerne
         constexpr int RS = L::RS;
         float *rb = red + (size_t)(it & 1) * 40 * RS;
         if (!PACK || (t4 & 1) == 0) rb[(dq * 8 + g4) * RS + warp] = dot;
-        if (t4 == 0) rb[(32 + g4) * RS + warp] = ssq;
+        if (t4 == (g4 >> 1)) rb[(32 + g4) * RS + warp] = ssq;
         // the previous item's output bulk stores must have read their shared rows
         // before the barrier that lets the producer refill that stage
         if (lane < a.n_q && it >= 1) bulk_wait_read0();
@@ -800,7 +801,7 @@ __global__ void __launch_bounds__(NW * 32, 1) depth_read_mma_multi_kernel(const 
         else dm_pass1_rows8<KS>(sa, bq, dot, ssq);
         float *rb = red + (size_t)(it & 1) * 40 * RS;
         if (!PACK || (t4 & 1) == 0) rb[(dq * 8 + g4) * RS + warp] = dot;
-        if (t4 == 0) rb[(32 + g4) * RS + warp] = ssq;
+        if (t4 == (g4 >> 1)) rb[(32 + g4) * RS + warp] = ssq;
         if (it >= 1) {
             // the stage consumed at it-1 is refilled after the barrier below with
             // item it-1+nstages: its output rows (if it held a token's last chunk)
