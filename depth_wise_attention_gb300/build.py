@@ -27,6 +27,7 @@ SOURCES = [
     "kernels_phase2.cu",
     "kernels_phase2_mh.cu",
     "kernels_mma.cu",
+    "kernels_bwd_split.cu",
     "kernels_mma_multi.cu",
     "kernels_bwd.cu",
     "kernels_bwd_mh.cu",

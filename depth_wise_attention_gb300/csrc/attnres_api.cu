@@ -20,6 +20,7 @@
 #include "phase2.cuh"
 #include "merge_bwd.cuh"
 #include "read_bwd.cuh"
+#include "read_bwd_split.cuh"
 #include "state_merge_bwd.h"
 
 using namespace attnres;
@@ -565,6 +566,135 @@ size_t read_bwd_ws_bytes(int sms, const ReadBwdShape &sh, int64_t d) {
     return (size_t)sms * (size_t)sh.tt * (size_t)sh.nqc * (size_t)d * sizeof(float);
 }
 
+// The two-kernel form (read_bwd_split.cuh) takes a pass of 3 or 4 queries
+// with bf16 sources, at most 8 of them, d = 2048 or 4096 and heads of at
+// least 256 channels (debug kernel variant 1 keeps the one-kernel form).
+bool read_bwd_split_applies(attnres_dtype_t dt, int64_t n_src, int64_t nq, int64_t d, int64_t H) {
+    if (g_kernel_variant.load() == 1) return false;
+    return dt == ATTNRES_BF16 && n_src >= 1 && n_src <= 8 && (nq == 3 || nq == 4) && (d == 2048 || d == 4096) &&
+           H >= 1 && H <= RC_NW && d % H == 0 && (d / H) % 256 == 0;
+}
+
+struct ReadBwdSplitShape {
+    int chunks = 0;          // apply CTAs along the tokens (partials of U)
+    int64_t tpc = 0;         // tokens per apply CTA
+    int nstages = 0;         // half-row stages of the coefficient kernel
+    uint32_t pitch = 0, stage_bytes = 0;
+    size_t smem = 0;
+    size_t off_coef = 0;     // coefficients after the partials of U
+    size_t total = 0;
+};
+
+attnres_status_t read_bwd_split_shape(int64_t T, int64_t d, int64_t H, const DeviceInfo *dev,
+                                      ReadBwdSplitShape *sh) {
+    KernelRef kc, ka;
+    if (!lookup_read_bwd_split(4, (int)d, &kc, &ka)) return ATTNRES_ERR_UNSUPPORTED;
+    sh->pitch = (uint32_t)d + 16;
+    sh->stage_bytes = 12u * sh->pitch;
+    size_t budget = kSmemBudget;
+    if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
+    if (budget <= RC_AUX_BYTES) return ATTNRES_ERR_UNSUPPORTED;
+    int ns = (int)((budget - RC_AUX_BYTES) / sh->stage_bytes);
+    if (ns > RC_MAX_STAGES) ns = RC_MAX_STAGES;
+    if (ns < 2) return ATTNRES_ERR_UNSUPPORTED;
+    sh->nstages = ns;
+    sh->smem = (size_t)ns * sh->stage_bytes + RC_AUX_BYTES;
+    int occ = 0;
+    attnres_status_t st = prepare_kernel(ka.fn, RA_RING_BYTES, RA_THREADS, &occ);
+    if (st != ATTNRES_OK) return st;
+    // one wave of apply CTAs: d / 1024 channel slices times token ranges
+    const int64_t slices = d / RA_W;
+    int64_t chunks = ((int64_t)occ * dev->sms + slices - 1) / slices;
+    if (chunks > T) chunks = T;
+    if (chunks < 1) chunks = 1;
+    sh->tpc = (T + chunks - 1) / chunks;
+    sh->chunks = (int)(T > 0 ? (T + sh->tpc - 1) / sh->tpc : 0);
+    const size_t ws_u = ((size_t)sh->chunks * 4 * (size_t)d * sizeof(float) + 255) / 256 * 256;
+    sh->off_coef = ws_u;
+    sh->total = ws_u + (size_t)T * (size_t)H * RC_NV * sizeof(float);
+    return ATTNRES_OK;
+}
+
+// Workspace launch_read_bwd needs for these arguments: the larger of the
+// kernel forms its query passes take.
+attnres_status_t read_bwd_ws_need(int64_t n_src, int64_t T, int64_t d, int64_t H, int64_t n_q,
+                                  attnres_dtype_t dt, const DeviceInfo *dev, const ReadBwdShape &sh, size_t *bytes) {
+    const int64_t nq_last = n_q - (n_q - 1) / sh.nqc * sh.nqc;
+    const int64_t nq_first = n_q < sh.nqc ? n_q : sh.nqc;
+    const bool sp0 = read_bwd_split_applies(dt, n_src, nq_first, d, H);
+    const bool sp1 = read_bwd_split_applies(dt, n_src, nq_last, d, H);
+    size_t need = (!sp0 || !sp1) ? read_bwd_ws_bytes(dev->sms, sh, d) : 0;
+    if (sp0 || sp1) {
+        ReadBwdSplitShape ss;
+        attnres_status_t st = read_bwd_split_shape(T, d, H, dev, &ss);
+        if (st != ATTNRES_OK) return st;
+        if (ss.total > need) need = ss.total;
+    }
+    *bytes = need;
+    return ATTNRES_OK;
+}
+
+// One pass of nq queries in the two-kernel form: the coefficient kernel (one
+// CTA per SM) writes every token's coefficients after the partials of U in
+// the workspace, the apply kernel writes dv and the partials.
+attnres_status_t launch_read_bwd_split_pass(const ReadBwdArgs &a, int nq, int64_t H, const ReadBwdSplitShape &ss,
+                                            int sms, void *stream) {
+    KernelRef kc, ka;
+    if (!lookup_read_bwd_split(nq, a.d, &kc, &ka)) return ATTNRES_ERR_UNSUPPORTED;
+    int occ = 0;
+    attnres_status_t st = prepare_kernel(kc.fn, ss.smem, RC_NW * 32, &occ);
+    if (st == ATTNRES_OK) st = prepare_kernel(ka.fn, RA_RING_BYTES, RA_THREADS, &occ);
+    if (st != ATTNRES_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float *coef = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(a.ws) + ss.off_coef);
+    ReadBwdCoefArgs c;
+    c.src = a.src;
+    c.src_stride_bytes = a.src_stride_bytes;
+    c.n_src = a.n_src;
+    c.T = a.T;
+    c.d = a.d;
+    c.n_q = nq;
+    c.H = (int)H;
+    c.queries = a.queries;
+    c.gain = a.gain;
+    c.eps = a.eps;
+    c.inv_dh = a.inv_dh;
+    c.dout = a.dout;
+    c.dlse = a.dlse;
+    c.coef = coef;
+    c.nstages = ss.nstages;
+    c.pitch = ss.pitch;
+    c.stage_bytes = ss.stage_bytes;
+    c.wait = a.wait;
+    const int grid = (int)(a.T < sms ? a.T : sms);
+    void *cargs[] = {&c};
+    cudaError_t e = cudaLaunchKernel(kc.fn, dim3(grid), dim3(RC_NW * 32), cargs, ss.smem, s);
+    if (e != cudaSuccess) return cuda_fail(e, "read_bwd coefficient launch");
+    ReadBwdApplyArgs p;
+    p.src = a.src;
+    p.src_stride_bytes = a.src_stride_bytes;
+    p.n_src = a.n_src;
+    p.T = a.T;
+    p.d = a.d;
+    p.H = (int)H;
+    p.dh = (int)(a.d / H);
+    p.n_q = nq;
+    p.queries = a.queries;
+    p.gain = a.gain;
+    p.dout = a.dout;
+    p.coef = coef;
+    p.dsrc = a.dsrc;
+    p.dsrc_stride_bytes = a.dsrc_stride_bytes;
+    p.accumulate = a.accumulate;
+    p.ws = a.ws;
+    p.tpc = ss.tpc;
+    void *pargs[] = {&p};
+    e = cudaLaunchKernel(ka.fn, dim3((unsigned)(a.d / RA_W), (unsigned)ss.chunks), dim3(RA_THREADS), pargs,
+                         RA_RING_BYTES, s);
+    if (e != cudaSuccess) return cuda_fail(e, "read_bwd apply launch");
+    return ATTNRES_OK;
+}
+
 attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
                                  int64_t H, attnres_dtype_t dt, const float *queries, int64_t n_q,
                                  const float *gain, float eps, const void *dout, const float *dlse, void *dsrc,
@@ -604,13 +734,19 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
     }
-    if (ws_bytes < read_bwd_ws_bytes(dev->sms, sh, d)) return ATTNRES_ERR_INVALID_ARG;
+    size_t need = 0;
+    st = read_bwd_ws_need(n_src, T, d, H, n_q, dt, dev, sh, &need);
+    if (st != ATTNRES_OK) return st;
+    if (ws_bytes < need) return ATTNRES_ERR_INVALID_ARG;
     // kernels of every pass (a last pass may take fewer queries): up to 2
-    // queries one group, 3 or 4 two groups of two
+    // queries one group, 3 or 4 two groups of two, or the two-kernel form
     KernelRef kr[2];
+    bool split[2];
     const int nq_last = (int)(n_q - (n_q - 1) / sh.nqc * sh.nqc);
     for (int v = 0; v < 2; ++v) {
-        const int nq = v == 0 ? sh.nqc : nq_last;
+        const int nq = v == 0 ? (int)(n_q < sh.nqc ? n_q : sh.nqc) : nq_last;
+        split[v] = read_bwd_split_applies(dt, n_src, nq, d, H);
+        if (split[v]) continue;
         const int dti = dt == ATTNRES_BF16 ? 1 : 0;
         const bool ok = nq > 2 ? lookup_read_bwd_qg(dti, sh.vpt, sh.mh, sh.hg, &kr[v])
                         : sh.mh ? lookup_read_bwd_mh(dti, nq, sh.ns, sh.vpt, sh.hg, &kr[v])
@@ -621,16 +757,25 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
     const uint32_t stage_bytes = (uint32_t)(((size_t)(n_src + sh.nqc) * row_pitch + 127) / 128 * 128);
     size_t budget = kSmemBudget;
     if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
-    size_t aux = kr[0].aux_smem > kr[1].aux_smem ? kr[0].aux_smem : kr[1].aux_smem;
+    size_t aux = 0;
+    for (int v = 0; v < 2; ++v)
+        if (!split[v] && kr[v].aux_smem > aux) aux = kr[v].aux_smem;
     if (budget <= aux) return ATTNRES_ERR_UNSUPPORTED;
     int nstages = (int)((budget - aux) / stage_bytes);
     if (nstages > RB_MAX_STAGES) nstages = RB_MAX_STAGES;
-    if (nstages < 2) return ATTNRES_ERR_UNSUPPORTED;
+    if (nstages < 2 && (!split[0] || !split[1])) return ATTNRES_ERR_UNSUPPORTED;
     const size_t smem = (size_t)nstages * stage_bytes + aux;
     for (int v = 0; v < 2; ++v) {
+        if (split[v]) continue;
         int occ = 0;
         st = prepare_kernel(kr[v].fn, smem, RB_THREADS, &occ);
         if (st != ATTNRES_OK) return st;
+    }
+    ReadBwdSplitShape ss;
+    if (split[0] || split[1]) {
+        st = read_bwd_split_shape(T, d, H, dev, &ss);
+        if (st != ATTNRES_OK) return st;
+        if (!aligned16(src) || (src_stride * (int64_t)es) % 16 != 0) return ATTNRES_ERR_UNSUPPORTED;
     }
     ReadBwdArgs a;
     a.src = static_cast<const unsigned char *>(src);
@@ -664,13 +809,22 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         a.dout = static_cast<const unsigned char *>(dout) + (size_t)q0 * (size_t)T * (size_t)d * es;
         a.dlse = dlse ? dlse + q0 * T : nullptr;
         a.accumulate = q0 == 0 ? accumulate : 1;
-        void *args[] = {&a};
-        const void *fn = kr[nq == sh.nqc ? 0 : 1].fn;
-        cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(RB_THREADS), args, smem, static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e, "read_bwd launch");
+        const bool sp = nq == (n_q < sh.nqc ? n_q : sh.nqc) ? split[0] : split[1];
+        int nparts = grid * sh.tt;
+        if (sp) {
+            st = launch_read_bwd_split_pass(a, nq, H, ss, dev->sms, stream);
+            if (st != ATTNRES_OK) return st;
+            nparts = ss.chunks;
+        } else {
+            void *args[] = {&a};
+            const void *fn = kr[nq == sh.nqc ? 0 : 1].fn;
+            cudaError_t e =
+                cudaLaunchKernel(fn, dim3(grid), dim3(RB_THREADS), args, smem, static_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) return cuda_fail(e, "read_bwd launch");
+        }
         ReadBwdFinishArgs f;
         f.ws = a.ws;
-        f.nparts = grid * sh.tt;
+        f.nparts = nparts;
         f.n_q = nq;
         f.d = (int)d;
         f.queries = a.queries;
@@ -679,8 +833,9 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         f.dgain = dgain;
         f.accumulate_dgain = q0 > 0 ? 1 : 0;
         void *fargs[] = {&f};
-        const int fgrid = (int)((d + 255) / 256);
-        e = cudaLaunchKernel(read_bwd_finish_fn(), dim3(fgrid), dim3(256), fargs, 0, static_cast<cudaStream_t>(stream));
+        const int fgrid = (int)((d + 31) / 32);          // 32 channels per CTA
+        cudaError_t e =
+            cudaLaunchKernel(read_bwd_finish_fn(), dim3(fgrid), dim3(256), fargs, 0, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "read_bwd finish launch");
     }
     return ATTNRES_OK;
@@ -790,7 +945,7 @@ attnres_status_t launch_merge_bwd(const void *o, const float *lse, const void *p
     f.dgain = dgain;
     f.accumulate_dgain = 0;
     void *fargs[] = {&f};
-    e = cudaLaunchKernel(read_bwd_finish_fn(), dim3((unsigned)((d + 255) / 256)), dim3(256), fargs, 0, s);
+    e = cudaLaunchKernel(read_bwd_finish_fn(), dim3((unsigned)((d + 31) / 32)), dim3(256), fargs, 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "merge backward finish launch");
     return ATTNRES_OK;
 }
@@ -820,7 +975,9 @@ attnres_status_t read_bwd_many_plan(int64_t n_src, int64_t T, int64_t d, int64_t
         ReadBwdShape sh;
         attnres_status_t st = read_bwd_shape(nc, d, n_q, 1, dt, &sh);
         if (st != ATTNRES_OK) return st;
-        const size_t b = read_bwd_ws_bytes(dev->sms, sh, d);
+        size_t b = 0;
+        st = read_bwd_ws_need(nc, T, d, 1, n_q, dt, dev, sh, &b);
+        if (st != ATTNRES_OK) return st;
         if (b > p->rb_bytes) p->rb_bytes = b;
     }
     const size_t es = esize(dt);
@@ -1579,7 +1736,8 @@ attnres_status_t msar_two_phase_bwd_plan(bool phase2, int64_t n_src, int64_t T, 
         if (d % 512 != 0 || d > 4096 || n_src > 16) return ATTNRES_ERR_UNSUPPORTED;
         attnres_status_t st = read_bwd_shape(n_src, d, S, 1, dt, &p->rb);
         if (st != ATTNRES_OK) return st;
-        p->rb_bytes = read_bwd_ws_bytes(dev->sms, p->rb, d);
+        st = read_bwd_ws_need(n_src, T, d, 1, S, dt, dev, p->rb, &p->rb_bytes);
+        if (st != ATTNRES_OK) return st;
     }
     p->tc = (T + 63) / 64;
     if (p->tc < 32) p->tc = 32;
@@ -1938,8 +2096,7 @@ static attnres_status_t read_bwd_workspace(int64_t n_src, int64_t T, int64_t d, 
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != ATTNRES_OK) return st;
-    *bytes = read_bwd_ws_bytes(dev->sms, sh, d);
-    return ATTNRES_OK;
+    return read_bwd_ws_need(n_src, T, d, H, n_q, dt, dev, sh, bytes);
 }
 
 attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t n_q,
@@ -1980,7 +2137,10 @@ attnres_status_t attnres_read_bwd_noalloc(const void *src, int64_t n_src, int64_
                 ReadBwdShape sh;
                 st = read_bwd_shape(n_src, d, n_q, 1, dt, &sh, cap);
                 if (st != ATTNRES_OK) return st;
-                if (read_bwd_ws_bytes(dev->sms, sh, d) <= kBwdScratchFloats * sizeof(float)) max_nqc = cap;
+                size_t b = 0;
+                st = read_bwd_ws_need(n_src, T, d, 1, n_q, dt, dev, sh, &b);
+                if (st != ATTNRES_OK) return st;
+                if (b <= kBwdScratchFloats * sizeof(float)) max_nqc = cap;
             }
             if (max_nqc == 0) return ATTNRES_ERR_UNSUPPORTED;
         }

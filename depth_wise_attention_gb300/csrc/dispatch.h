@@ -40,6 +40,9 @@ bool lookup_merge_bwd(int dt, int vpt, KernelRef *out);
 // read_bwd_kernel in per-head mode (MHAR backward), hg reduction groups per warp
 bool lookup_read_bwd_mh(int dt, int nq, int ns, int vpt, int hg, KernelRef *out);
 const void *read_bwd_finish_fn();
+// the two-kernel read backward (read_bwd_split.cuh): read_bwd_coef_kernel and
+// read_bwd_apply_kernel for nq = 3 or 4 queries at d = 2048 or 4096
+bool lookup_read_bwd_split(int nq, int d, KernelRef *coef, KernelRef *apply);
 
 // phase2_merge_kernel<T, vpt, upd, mh>: upd = fused partial-sum update, mh = per-head merge
 bool lookup_phase2(int dt, int vpt, bool upd, bool mh, KernelRef *out);

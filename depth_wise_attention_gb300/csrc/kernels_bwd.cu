@@ -5,20 +5,32 @@
 
 namespace attnres {
 
-// One thread per channel; the partials are summed in partial order, so the
-// result does not depend on scheduling.
+// 256 threads: 32 channels times 8 groups of partials (group j takes
+// partials j, j+8, ...); the groups are then added in order, so the result
+// does not depend on scheduling.
 __global__ void __launch_bounds__(256) read_bwd_finish_kernel(const ReadBwdFinishArgs a) {
-    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < a.d; c += gridDim.x * blockDim.x) {
-        const float g = a.gain ? __ldg(a.gain + c) : 1.f;
-        float dgc = 0.f;
-        for (int q = 0; q < a.n_q; ++q) {
-            float u = 0.f;
-            for (int p = 0; p < a.nparts; ++p) u += a.ws[((size_t)p * a.n_q + q) * a.d + c];
-            a.dq[(size_t)q * a.d + c] = g * u;
-            dgc = fmaf(__ldg(a.queries + (size_t)q * a.d + c), u, dgc);
+    __shared__ float red[8][32];
+    const int lane = threadIdx.x & 31, j = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
+    const bool ok = c < a.d;
+    const float g = ok && a.gain ? __ldg(a.gain + c) : 1.f;
+    float dgc = 0.f;
+    for (int q = 0; q < a.n_q; ++q) {
+        float u = 0.f;
+        if (ok)
+            for (int p = j; p < a.nparts; p += 8) u += a.ws[((size_t)p * a.n_q + q) * a.d + c];
+        red[j][lane] = u;
+        __syncthreads();
+        if (j == 0 && ok) {
+            float s = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s += red[k][lane];
+            a.dq[(size_t)q * a.d + c] = g * s;
+            dgc = fmaf(__ldg(a.queries + (size_t)q * a.d + c), s, dgc);
         }
-        if (a.dgain) a.dgain[c] = a.accumulate_dgain ? a.dgain[c] + dgc : dgc;
+        __syncthreads();
     }
+    if (j == 0 && ok && a.dgain) a.dgain[c] = a.accumulate_dgain ? a.dgain[c] + dgc : dgc;
 }
 
 template <typename T, int NQ, int NS, int VPT>

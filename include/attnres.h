@@ -231,9 +231,17 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  *              the tokens go through it and are reduced in a fixed order, so
  *              results are bitwise reproducible
  * No output may overlap an input or the workspace.  T = 0 zeroes dqueries and
- * dgain.  The queries are taken in passes of 2 (of 1 with more than 8
- * sources) over the sources; later passes add into dsrc and dgain, so with
- * more than one pass a bf16 dsrc is rounded once per pass.
+ * dgain.  The queries are taken in passes over the sources (up to 4 per pass
+ * with at most 8 sources, else 2, and 1 with more than 8 sources); later
+ * passes add into dsrc and dgain, so with more than one pass a bf16 dsrc is
+ * rounded once per pass.  A pass of 3 or 4 queries over at most 8 bf16
+ * sources at d = 2048 or 4096 runs as two kernels: the first takes each
+ * token's row sums on the tensor cores and writes the token's coefficients
+ * (alpha_qi, ds_qi / r_i and the v_i term, 72 floats) to the workspace, the
+ * second forms dsrc and the sums over the tokens in slices of channels.  It
+ * reads the sources and dout twice and rounds a bf16 dsrc once.  Other
+ * passes of 3 or 4 queries run two groups of two in one kernel, the second
+ * group adding into the bf16 dsrc the first has rounded.
  * More than 16 sources (Full AttnRes past layer 16): the sources are taken in
  * chunks of 8.  Each chunk's read state (o_c, lse_c) is recomputed, and the
  * backward of the states' online-softmax merge (b-lab.team summary, section
@@ -256,8 +264,10 @@ attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_st
 
 /*
  * Workspace bytes attnres_read_bwd needs for these sizes on the current
- * device (an upper bound: one partial row of d floats per query of a pass for
- * every token row a CTA holds, one CTA per SM).  No device work is done.
+ * device (an upper bound: partial rows of d floats per query of a pass, one
+ * for every token row a CTA holds, one CTA per SM, or one per token range of
+ * the two-kernel form; for that form also 72 floats per token and head, so
+ * the size grows with T).  No device work is done.
  */
 attnres_status_t attnres_read_bwd_workspace_size(int64_t n_src, int64_t T, int64_t d, int64_t n_q,
                                                 attnres_dtype_t dt, size_t *bytes);

@@ -503,6 +503,82 @@ def test_block_phase1_bwd(n_src, n_q, T, d, dtype, with_lse):
     _check_grads(got, oracle.block_phase1_bwd(src, q, d_o, dl, g, 1e-6), dtype, f"n_q={n_q}")
 
 
+@pytest.fixture(params=[0, 1], ids=["two-kernel", "one-kernel"])
+def bwd_variant(request):
+    """Kernel variant 0 runs the read backward of 3-4 queries (bf16, <= 8
+    sources, d = 2048 or 4096, heads of >= 256 channels) as two kernels (row
+    coefficients, then channel slices); variant 1 keeps the one-kernel form."""
+    attnres.attnres_debug_set_kernel_variant(request.param)
+    yield request.param
+    attnres.attnres_debug_set_kernel_variant(0)
+
+
+@pytest.mark.parametrize("n_src,n_q,T,d,H,with_gain,with_lse", [
+    (8, 4, 300, 4096, 1, True, True),       # Block phase 1's backward, lse gradient
+    (8, 4, 77, 4096, 8, True, False),       # the MHAR workload's heads (512 channels)
+    (5, 3, 151, 2048, 1, False, True),      # fewer tokens than SMs, 3 queries
+    (1, 4, 1, 4096, 1, True, False),        # one source, one token
+    (8, 3, 40, 4096, 16, False, False),     # heads of 256 channels
+    (3, 4, 1000, 2048, 2, True, False),     # two heads, one per half row
+    (7, 4, 9, 2048, 4, True, False)])
+def test_read_bwd_both_forms(bwd_variant, n_src, n_q, T, d, H, with_gain, with_lse):
+    """The read backward with 3-4 queries under both kernel forms against the
+    oracle's chain rule (per head for H > 1; with Block phase 1's lse
+    gradient where given)."""
+    rng = _rng(n_src * 13 + n_q * 7 + T + d + H)
+    src = _sources(rng, n_src, T, d, BF16, step=0.25)
+    q = _queries(rng, n_q, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gain else None
+    dout = _sources(rng, n_q, T, d, BF16, step=0)
+    sd, qd, od = to_dev(src, BF16), to_dev(q, F32), to_dev(dout, BF16)
+    gd = to_dev(g, F32) if with_gain else None
+    if with_lse:
+        dl = rng.standard_normal((n_q, T)).astype(np.float32)
+        got = attnres.attnres_block_phase1_bwd(sd, qd, od, to_dev(dl, F32), gd, 1e-6)
+        ref = oracle.block_phase1_bwd(src, q, dout, dl, g, 1e-6)
+    elif H == 1:
+        got = attnres.attnres_read_bwd(sd, qd, od, gd, 1e-6)
+        ref = oracle.read_bwd(src, q, dout, g, 1e-6)
+    else:
+        qh = q.reshape(n_q, H, d // H)
+        got = attnres.mhar_read_bwd(sd, to_dev(qh, F32), od, gd, 1e-6)
+        ref = oracle.mhar_bwd(src, qh, dout, g, 1e-6)
+    _check_grads(got, ref, BF16, f"variant {bwd_variant} H={H}")
+
+
+def test_read_bwd_two_kernel_form_is_deterministic_accumulates_and_agrees_with_one_kernel():
+    """Two runs of the two-kernel form agree bitwise; with accumulate it adds
+    into the given source gradients; and it agrees with the one-kernel form
+    within the bf16 bar.  (The one-kernel form rounds dsrc to bf16 after its
+    first group of two queries and adds the second group to that, so it
+    carries two roundings; the two-kernel form rounds once.  Against the
+    oracle the two-kernel form is within half a bf16 step, see
+    test_read_bwd_both_forms.)"""
+    rng = _rng(53)
+    n_src, n_q, T, d = 8, 4, 500, 4096
+    src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.25), BF16)
+    q = to_dev(_queries(rng, n_q, d), F32)
+    dout = to_dev(_sources(rng, n_q, T, d, BF16, step=0), BF16)
+    g = to_dev(rng.uniform(0.5, 1.5, d).astype(np.float32), F32)
+    a = attnres.attnres_read_bwd(src, q, dout, g)
+    b = attnres.attnres_read_bwd(src, q, dout, g)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    base = to_dev(_sources(rng, n_src, T, d, BF16), BF16)
+    acc = base.clone()
+    attnres.attnres_read_bwd(src, q, dout, g, dsrc=acc, accumulate=True)
+    check_out(acc, to_host(base) + to_host(a[0]), BF16, what="accumulated dsrc")
+    attnres.attnres_debug_set_kernel_variant(1)
+    try:
+        c = attnres.attnres_read_bwd(src, q, dout, g)
+    finally:
+        attnres.attnres_debug_set_kernel_variant(0)
+    check_out(a[0], to_host(c[0]).astype(np.float64), BF16, what="dsrc of the two forms")
+    for name, u, v in (("dq", a[1], c[1]), ("dgain", a[2], c[2])):
+        u, v = to_host(u).astype(np.float64), to_host(v).astype(np.float64)
+        assert np.abs(u - v).max() <= 1e-4 * np.abs(v).max(), name
+
+
 @pytest.mark.parametrize("T,d,dtype,with_gain,with_partial", [
     (100, 4096, BF16, True, True), (37, 2048, BF16, False, True), (50, 256, F32, True, True),
     (333, 1000, F32, True, True), (20, 512, BF16, True, False), (1, 64, F32, False, True)])

@@ -83,9 +83,9 @@ def test_noalloc_backward_rejects_sizes_beyond_its_scratch():
 
 
 def test_noalloc_backward_with_four_queries_at_d4096():
-    """Four queries at d = 4096 would need a 10 MB workspace in one pass; the
-    no-allocation backward then takes passes of two within its 8 MB scratch,
-    and its gradients agree with the oracle."""
+    """Four queries at d = 4096: the no-allocation backward takes the
+    two-kernel form when its workspace (which grows with T) fits the 8 MB
+    scratch, else passes of two; its gradients agree with the oracle."""
     from _helpers import check_out, to_host
     from oracle import oracle
     g = torch.Generator(device="cuda")
