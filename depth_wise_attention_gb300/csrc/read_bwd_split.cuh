@@ -28,9 +28,10 @@
 // up the ring of stages.
 // Nothing else is written, so no row has to stay in shared memory after its
 // sums: the rows stream through a ring of half-row stages (all 8 source rows
-// and the query gradient rows of one half of the channels), each released by
-// an mbarrier that every warp arrives on, which keeps 1.5 tokens of loads in
-// flight where two whole-row stages would leave one.
+// and the query gradient rows of one half of the channels), which keeps 1.5
+// tokens of loads in flight where two whole-row stages would leave one; the
+// warp that finishes a half last refills its stage (a shared counter), so no
+// warp waits for another to release a stage.
 //
 // read_bwd_apply_kernel: a CTA owns 1024 channels (4 per thread) and a
 // contiguous range of tokens; it reads the tokens' coefficients (staged in
@@ -53,6 +54,7 @@ constexpr int RC_MAX_STAGES = 8;
 constexpr int RC_NV = 72;             // row sums per column: (w*g).v 32, dout.v 32, v.v 8
 constexpr int RC_RS = 36;             // table row stride in floats (32 columns, float4-aligned)
 constexpr size_t RC_AUX_BYTES = 256 + (size_t)2 * RC_NV * RC_RS * 4;
+constexpr bool RC_GRAM = true;        // sums of squares: Gram MMAs (true) or packed FMAs
 
 struct ReadBwdCoefArgs {
     const unsigned char *src;         // source 0, token 0 (bf16)
@@ -74,6 +76,10 @@ struct ReadBwdCoefArgs {
     uint32_t stage_bytes;             // 12 rows
     WaitCfg wait;
 };
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
 
 // Fragments of the queries (gain folded in) for the warp's channels of one
 // half row, query q = g4/2, bf16 hi part in column 2q, lo part in 2q+1.
@@ -100,8 +106,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *stages = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.nstages * a.stage_bytes);
-    uint64_t *empty = full + RC_MAX_STAGES;
-    uint64_t *tfull = empty + RC_MAX_STAGES;      // [2] table of token it&1 written
+    // warps done with each stage; the last one to finish a half refills its stage
+    unsigned *done = reinterpret_cast<unsigned *>(full + RC_MAX_STAGES);
+    unsigned *imax = done + RC_MAX_STAGES;         // halves issued so far
+    uint64_t *tfull = full + 2 * RC_MAX_STAGES;   // [2] table of token it&1 written
     uint64_t *tfree = tfull + 2;                  // [2] table of token it&1 read
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tfree + 2);
     float *red = reinterpret_cast<float *>(smem + (size_t)a.nstages * a.stage_bytes + 256);
@@ -114,8 +122,9 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
     if (tid == 0) {
         for (int s = 0; s < a.nstages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NW);
+            done[s] = 0;
         }
+        *imax = 0;
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], NW * 32);
             mbar_init(&tfree[b], a.H * 32);
@@ -139,11 +148,11 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
     const int n_halves = 2 * n_items;
 
     // ------------------------------------------------------------ producer
-    // warp 0, lane 0: half k (token item k/2, channel half k%2) into stage k % nstages
-    const bool producer = (warp == 0) && !a.wait.inject_stall;
-    uint64_t pol = 0;
-    if (producer) pol = l2_policy_evict_first();
-    int issued = 0;
+    // half k (token item k/2, channel half k%2) into stage k % nstages: the
+    // first nstages by thread 0, each later one by lane 0 of the warp that
+    // finishes the half nstages before it last
+    const bool may_issue = !a.wait.inject_stall;
+    const uint64_t pol = l2_policy_evict_first();
     auto issue = [&](int k) {
         const int s = k % a.nstages;
         const int64_t t = blockIdx.x + (int64_t)(k >> 1) * gstride;
@@ -156,9 +165,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
         for (int q = 0; q < a.n_q; ++q)
             bulk_g2s(dst + (size_t)(8 + q) * a.pitch, a.dout + (int64_t)q * a.T * a.d * 2 + off,
                      (uint32_t)half_bytes, &full[s], pol);
+        atomicMax(imax, (unsigned)(k + 1));
     };
-    if (producer && lane == 0)
-        for (; issued < n_halves && issued < a.nstages; ++issued) issue(issued);
+    if (tid == 0 && may_issue)
+        for (int k = 0; k < n_halves && k < a.nstages; ++k) issue(k);
 
     // ------------------------------------------------------------ constants
     uint32_t bq[2][KSH][2];
@@ -169,7 +179,12 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
     // block lane/8 of a 32-channel group of this warp's slice
     const uint32_t colb = (uint32_t)(warp * CWH + 8 * (lane >> 3)) * 2;
     const uint32_t lrow_x = (uint32_t)(lane & 7) * a.pitch + colb;
-    const uint32_t lrow_d = (uint32_t)(8 + (lane & 3)) * a.pitch + colb;
+    // gradient rows as the B operand of the packed dots (ldmatrix .x2, lanes
+    // 0..15): matrix j = (lane/8)&1 holds channels +8j, its rows 0..3 the
+    // gradient rows at the first k-step of the 32-channel group, rows 4..7 at
+    // the second (+16 channels)
+    const uint32_t lrow_d = (uint32_t)(8 + (lane & 3)) * a.pitch +
+                            (uint32_t)(warp * CWH + 8 * ((lane >> 3) & 1) + 16 * ((lane >> 2) & 1)) * 2;
     const uint32_t stage0 = smem_u32(stages);
     // table columns: one per warp with one head (both halves summed), else one
     // per (half, warp) ("virtual warp" of CWH channels, in row order)
@@ -229,7 +244,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
         }
     };
 
-    float d1[2][4], dd[2][4];
+    float d1[2][4], dd[2][4], gr[2][4];
     float2 sq = make_float2(0.f, 0.f);
     for (int k = 0; k < n_halves; ++k) {
         const int it = k >> 1, h = k & 1;
@@ -240,7 +255,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) { d1[u][e] = 0.f; dd[u][e] = 0.f; }
+                for (int e = 0; e < 4; ++e) { d1[u][e] = 0.f; dd[u][e] = 0.f; gr[u][e] = 0.f; }
             sq = make_float2(0.f, 0.f);
         }
         mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
@@ -249,52 +264,66 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
         auto pass = [&](const uint32_t(&b)[KSH][2]) {
 #pragma unroll
             for (int s2 = 0; s2 < KSH / 2; ++s2) {
-                uint32_t x0, x1, x2, x3, e0, e1, e2, e3;
+                uint32_t x0, x1, x2, x3, e0, e1;
                 ldsm_x4(sb + lrow_x + 64 * s2, x0, x1, x2, x3);
-                ldsm_x4(sb + lrow_d + 64 * s2, e0, e1, e2, e3);
+                ldsm_x2(sb + lrow_d + 64 * s2, e0, e1);
                 mma_rows8(d1[0], x0, x1, b[2 * s2][0], b[2 * s2][1]);
                 mma_rows8(d1[1], x2, x3, b[2 * s2 + 1][0], b[2 * s2 + 1][1]);
-                mma_rows8(dd[0], x0, x1, e0, e1);
-                mma_rows8(dd[1], x2, x3, e2, e3);
-                const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
-                sq = ffma2(f0, f0, sq);
-                sq = ffma2(f1, f1, sq);
-                sq = ffma2(f2, f2, sq);
-                sq = ffma2(f3, f3, sq);
+                // rows 0..7: sources at the first k-step, 8..15 at the second;
+                // columns 0..3 meet the first, 4..7 the second k-step's gradients
+                mma_full(dd[s2 & 1], x0, x2, x1, x3, e0, e1);
+                if constexpr (RC_GRAM) {
+                    mma_rows8(gr[0], x0, x1, x0, x1);
+                    mma_rows8(gr[1], x2, x3, x2, x3);
+                } else {
+                    const float2 f0 = bf2_to_f2(x0), f1 = bf2_to_f2(x1), f2 = bf2_to_f2(x2), f3 = bf2_to_f2(x3);
+                    sq = ffma2(f0, f0, sq);
+                    sq = ffma2(f1, f1, sq);
+                    sq = ffma2(f2, f2, sq);
+                    sq = ffma2(f3, f3, sq);
+                }
             }
         };
         if (h == 0) pass(bq[0]);
         else pass(bq[1]);
-        // this warp is done with the stage; the producer refills it once every
-        // warp is
+        // this warp is done with the stage; the last warp to be refills it
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (producer) {
-            if (lane == 0 && issued < n_halves && !*abort_flag &&
-                mbar_wait_bounded(&empty[s], par, abort_flag, a.wait)) {
-                issue(issued);
-                ++issued;
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&done[s], 1u) == NW - 1) {
+                done[s] = 0;
+                if (k + a.nstages < n_halves && may_issue && !*abort_flag) issue(k + a.nstages);
             }
-            __syncwarp();
         }
+        __syncwarp();
         if (per_half || h == 1) {
             // the first write of this token's table waits until the coefficient
             // warps of the token two before have read it
             if ((h == 0 || !per_half) && it >= 2)
                 mbar_wait_bounded(&tfree[it & 1], (uint32_t)((it >> 1) - 1) & 1u, abort_flag, a.wait);
             // lane (i = g4, q = t4): (w_q*g).v_i in columns 2q (hi) + 2q+1 (lo);
-            // lane (i, t4): dout.v_i of queries 2t4 and 2t4+1
+            // lane (i, t4 < 2): dout.v_i of queries 2t4 and 2t4+1, the first
+            // k-steps' part in c0, c1 here, the second's in c2, c3 of lane t4+2
             const float dw = (d1[0][0] + d1[1][0]) + (d1[0][1] + d1[1][1]);
-            const float dq0 = dd[0][0] + dd[1][0], dq1 = dd[0][1] + dd[1][1];
-            float ss = sq.x + sq.y;
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            float dq0 = (t4 < 2) ? dd[0][0] + dd[1][0] : dd[0][2] + dd[1][2];
+            float dq1 = (t4 < 2) ? dd[0][1] + dd[1][1] : dd[0][3] + dd[1][3];
+            dq0 += __shfl_xor_sync(0xffffffffu, dq0, 2);
+            dq1 += __shfl_xor_sync(0xffffffffu, dq1, 2);
+            float ss;
+            if constexpr (RC_GRAM) {
+                // the Gram diagonal: lane (i, i/2), element i&1
+                ss = (g4 & 1) ? gr[0][1] + gr[1][1] : gr[0][0] + gr[1][0];
+            } else {
+                ss = sq.x + sq.y;
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            }
             const int col = per_half ? h * NW + warp : warp;
             float *rb = red + (size_t)(it & 1) * RC_NV * RS;
             if (t4 < NQ) rb[(t4 * 8 + g4) * RS + col] = dw;
             if (2 * t4 < NQ) rb[(32 + 2 * t4 * 8 + g4) * RS + col] = dq0;
             if (2 * t4 + 1 < NQ) rb[(32 + (2 * t4 + 1) * 8 + g4) * RS + col] = dq1;
-            if (t4 == 0) rb[(64 + g4) * RS + col] = ss;
+            if (t4 == (RC_GRAM ? g4 >> 1 : 0)) rb[(64 + g4) * RS + col] = ss;
         }
         if (h == 1) {
             mbar_arrive(&tfull[it & 1]);
@@ -318,8 +347,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
     }
     if (pend_it >= 0) coefficients();
     // copies still in flight (only after an abort) must land before the CTA exits
-    if (producer && lane == 0) {
+    __syncthreads();
+    if (tid == 0) {
         int never = 0;
+        const int issued = (int)*imax;
         for (int k = issued > a.nstages ? issued - a.nstages : 0; k < issued; ++k)
             mbar_wait_bounded(&full[k % a.nstages], (uint32_t)(k / a.nstages) & 1u, &never, a.wait);
     }
