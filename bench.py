@@ -45,6 +45,8 @@ KERNEL_SOURCES = {
     "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "msar_tile": [CSRC + "msar_tile.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
+    "read_bwd_split": [CSRC + "read_bwd_split.cuh", CSRC + "depth_read_mma.cuh", CSRC + "common.cuh",
+                       CSRC + "kernels_bwd_split.cu", CSRC + "kernels_bwd.cu"],
     "msar_phase1": [CSRC + "msar_phase1.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "msar_phase2": [CSRC + "msar_phase2.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "merge_bwd": [CSRC + "merge_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_merge_bwd.cu"],
@@ -477,7 +479,8 @@ class BlockBwdWorkload(BlockWorkload):
     """Backward of the headline Block step (bf16, d=4096, N=8, S=4): the
     merge backward of each layer (layers 2..4 with their partials, layer 1
     without, which passes its gradient straight to o), then phase 1's backward
-    for the four layers' o and lse gradients (two passes of two queries).
+    for the four layers' o and lse gradients (one pass of four queries in the
+    two-kernel form: row coefficients, then channel slices).
     Algorithmic bytes per token: the merge backward reads o, p and dh and
     writes d_o and d_partial (3 layers), layer 1 copies dh to d_o, and phase
     1's backward reads the 8 sources and the 4 d_o rows and writes the 8
@@ -489,9 +492,11 @@ class BlockBwdWorkload(BlockWorkload):
         self.phase1_bytes_per_token = (2 * N + S) * d * b + S * 4
         self.merge_bwd_bytes_per_token = 5 * d * b + 2 * 4
         self.bytes_per_token = self.phase1_bytes_per_token + (S - 1) * self.merge_bwd_bytes_per_token + 2 * d * b
-        self.launches_per_step = (S - 1) * 2 + 1 + 2 * ((S + 1) // 2)
-        self.dominant = "phase-1 backward (read_bwd_kernel passes + reductions)"
-        self.dominant_src = "read_bwd"
+        # merges (kernel + reduction each), layer 1's copy, phase 1's backward
+        # (coefficient kernel, apply kernel, reduction)
+        self.launches_per_step = (S - 1) * 2 + 1 + 3
+        self.dominant = "phase-1 backward (read_bwd_coef_kernel + read_bwd_apply_kernel + reduction)"
+        self.dominant_src = "read_bwd_split"
         self.profile_tag = f"ncu_block_bwd_phase1_d{d}"
 
     def config(self):
@@ -578,10 +583,10 @@ class BlockBwdWorkload(BlockWorkload):
 class MharBwdWorkload(ReadBwdWorkload):
     """Backward of the MHAR read at the MHAR workload's sizes: 4 queries of
     H=8 heads over N=8 sources, bf16, d=4096: the sources', the queries' and
-    the gain's gradients for a given output gradient.  The kernel takes the
-    queries in two passes of two (the second adds into the source
-    gradients); the algorithmic bytes are one pass's: read the sources and
-    the 4 output gradients, write the sources' gradients."""
+    the gain's gradients for a given output gradient, in the two-kernel form
+    (per-head row coefficients, then channel slices).  The algorithmic bytes
+    are one pass's: read the sources and the 4 output gradients, write the
+    sources' gradients."""
 
     def __init__(self, T=131072, d=4096, N=8, H=8, n_q=4, seed=0):
         BlockWorkload.__init__(self, T, d, N, 4, seed, name="mhar_read_backward")
@@ -589,9 +594,9 @@ class MharBwdWorkload(ReadBwdWorkload):
         self.H, self.n_q = H, n_q
         self.bytes_per_token = (2 * N + n_q) * d * b
         self.phase1_bytes_per_token = self.bytes_per_token
-        self.launches_per_step = 2 * ((n_q + 1) // 2)   # per pass: streaming kernel + reduction
-        self.dominant = "mhar read backward (read_bwd_kernel per-head passes + reductions)"
-        self.dominant_src = "read_bwd_mh"
+        self.launches_per_step = 3                      # coefficient kernel, apply kernel, reduction
+        self.dominant = "mhar read backward (read_bwd_coef_kernel per head + read_bwd_apply_kernel + reduction)"
+        self.dominant_src = "read_bwd_split"
         self.profile_tag = f"ncu_mhar_bwd_d{d}_H{H}"
 
     def config(self):
