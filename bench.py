@@ -47,6 +47,8 @@ KERNEL_SOURCES = {
     "read_bwd": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu"],
     "read_bwd_split": [CSRC + "read_bwd_split.cuh", CSRC + "depth_read_mma.cuh", CSRC + "common.cuh",
                        CSRC + "kernels_bwd_split.cu", CSRC + "kernels_bwd.cu"],
+    "read_bwd_many": [CSRC + "read_bwd_many.cuh", CSRC + "read_bwd_split.cuh", CSRC + "depth_read_mma.cuh",
+                      CSRC + "common.cuh", CSRC + "kernels_bwd_split.cu", CSRC + "kernels_bwd.cu"],
     "msar_phase1": [CSRC + "msar_phase1.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "msar_phase2": [CSRC + "msar_phase2.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "merge_bwd": [CSRC + "merge_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_merge_bwd.cu"],
@@ -435,11 +437,9 @@ class ReadBwdWorkload(BlockWorkload):
 class DeepReadBwdWorkload(ReadBwdWorkload):
     """Backward of the deepest layer of Full AttnRes at depth: one query over
     L = 64 sources ~ N(0, (1 + i/16)^2), bf16, d = 4096, T = 16384, output
-    gradient ~ N(0, 1).  More sources than one pass of the backward kernel
-    takes: chunks of 8 with their read states recomputed, the merge's
-    backward, and each chunk's backward with its lse gradient.  Algorithmic
-    bytes per token: the sources and the output gradient read, the sources'
-    gradients written."""
+    gradient ~ N(0, 1), in the two-kernel form (coefficients over all the
+    sources, then channel slices).  Algorithmic bytes per token: the sources
+    and the output gradient read, the sources' gradients written."""
 
     def __init__(self, T=16384, d=4096, L=64, seed=0):
         super().__init__(T, d, L - 1, seed)
@@ -447,10 +447,9 @@ class DeepReadBwdWorkload(ReadBwdWorkload):
         self.L = L
         self.bytes_per_token = (2 * L + 1) * d * 2
         self.phase1_bytes_per_token = self.bytes_per_token
-        C = (L + 7) // 8
-        self.launches_per_step = C + 1 + 2 * C + 2 * C
-        self.dominant = "read backward over 64 sources (whole chain)"
-        self.dominant_src = "read_bwd"
+        self.launches_per_step = 3                      # coefficient kernel, apply kernel, reduction
+        self.dominant = "read backward over 64 sources (read_bwd_coef_many_kernel + read_bwd_apply_many_kernel + reduction)"
+        self.dominant_src = "read_bwd_many"
         self.profile_tag = f"ncu_read_bwd_depth_d{d}_L{L}"
 
     def config(self):

@@ -21,6 +21,7 @@
 #include "merge_bwd.cuh"
 #include "read_bwd.cuh"
 #include "read_bwd_split.cuh"
+#include "read_bwd_many.cuh"
 #include "state_merge_bwd.h"
 
 using namespace attnres;
@@ -999,6 +1000,56 @@ attnres_status_t read_bwd_many_plan(int64_t n_src, int64_t T, int64_t d, int64_t
     return ATTNRES_OK;
 }
 
+// One query over 17..64 bf16 sources at d = 2048 or 4096 takes the
+// two-kernel form (read_bwd_many.cuh) instead of the chunked chain (debug
+// kernel variant 1 keeps the chain).
+bool read_bwd_many_split_applies(attnres_dtype_t dt, int64_t n_src, int64_t n_q, int64_t d) {
+    if (g_kernel_variant.load() == 1) return false;
+    return dt == ATTNRES_BF16 && n_q == 1 && n_src > 16 && n_src <= 8 * RM_MAXC && (d == 2048 || d == 4096);
+}
+
+struct ReadBwdManySplitShape {
+    int C = 0;               // chunks of 8 sources
+    int chunks = 0;          // apply CTAs along the tokens (partials of U)
+    int64_t tpc = 0;         // tokens per apply CTA
+    int nstages = 0;         // half-row stages of the coefficient kernel
+    uint32_t pitch = 0, stage_bytes = 0;
+    size_t smem = 0;
+    size_t off_coef = 0;     // coefficients after the partials of U
+    size_t total = 0;
+};
+
+attnres_status_t read_bwd_many_split_shape(int64_t n_src, int64_t T, int64_t d, const DeviceInfo *dev,
+                                           ReadBwdManySplitShape *sh) {
+    KernelRef kc, ka;
+    if (!lookup_read_bwd_many((int)d, &kc, &ka)) return ATTNRES_ERR_UNSUPPORTED;
+    sh->C = (int)((n_src + 7) / 8);
+    sh->pitch = (uint32_t)d + 16;                 // half a row of bf16 (d bytes), padded
+    sh->stage_bytes = (uint32_t)RM_ROWS * sh->pitch;
+    size_t budget = kSmemBudget;
+    if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
+    if (budget <= RM_AUX_BYTES) return ATTNRES_ERR_UNSUPPORTED;
+    int ns = (int)((budget - RM_AUX_BYTES) / sh->stage_bytes);
+    if (ns > RC_MAX_STAGES) ns = RC_MAX_STAGES;
+    if (ns < 2) return ATTNRES_ERR_UNSUPPORTED;
+    sh->nstages = ns;
+    sh->smem = (size_t)ns * sh->stage_bytes + RM_AUX_BYTES;
+    int occ = 0;
+    attnres_status_t st = prepare_kernel(ka.fn, RM_RING_BYTES, RA_THREADS, &occ);
+    if (st != ATTNRES_OK) return st;
+    // one wave of apply CTAs: d / 1024 channel slices times token ranges
+    const int64_t slices = d / RA_W;
+    int64_t chunks = ((int64_t)occ * dev->sms + slices - 1) / slices;
+    if (chunks > T) chunks = T;
+    if (chunks < 1) chunks = 1;
+    sh->tpc = (T + chunks - 1) / chunks;
+    sh->chunks = (int)(T > 0 ? (T + sh->tpc - 1) / sh->tpc : 0);
+    const size_t ws_u = ((size_t)sh->chunks * (size_t)d * sizeof(float) + 255) / 256 * 256;
+    sh->off_coef = ws_u;
+    sh->total = ws_u + (size_t)T * (size_t)sh->C * RM_NV * sizeof(float);
+    return ATTNRES_OK;
+}
+
 attnres_status_t launch_read_bwd_many(const void *src, int64_t n_src, int64_t src_stride, int64_t T, int64_t d,
                                       attnres_dtype_t dt, const float *queries, int64_t n_q, const float *gain,
                                       float eps, const void *dout, const float *dlse, void *dsrc,
@@ -1024,10 +1075,87 @@ attnres_status_t launch_read_bwd_many(const void *src, int64_t n_src, int64_t sr
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != ATTNRES_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (read_bwd_many_split_applies(dt, n_src, n_q, d)) {
+        ReadBwdManySplitShape sh;
+        st = read_bwd_many_split_shape(n_src, T, d, dev, &sh);
+        if (st != ATTNRES_OK) return st;
+        if (T == 0) {
+            cudaError_t e = cudaMemsetAsync(dq, 0, dq_bytes, s);
+            if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, s);
+            return e == cudaSuccess ? ATTNRES_OK : cuda_fail(e, "cudaMemsetAsync");
+        }
+        if (ws_bytes < sh.total) return ATTNRES_ERR_INVALID_ARG;
+        if (!aligned16(src) || (src_stride * (int64_t)es) % 16 != 0 || !aligned16(dout) || !aligned16(dsrc) ||
+            (dsrc_stride * (int64_t)es) % 16 != 0 || !aligned16(queries) || (gain && !aligned16(gain)) ||
+            !aligned4(dq) || (dgain && !aligned4(dgain)) || !aligned16(ws) || (dlse && !aligned4(dlse)))
+            return ATTNRES_ERR_UNSUPPORTED;
+        KernelRef kc, ka;
+        if (!lookup_read_bwd_many((int)d, &kc, &ka)) return ATTNRES_ERR_UNSUPPORTED;
+        int occ = 0;
+        st = prepare_kernel(kc.fn, sh.smem, RC_NW * 32, &occ);
+        if (st != ATTNRES_OK) return st;
+        float *coef = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + sh.off_coef);
+        ReadBwdCoefManyArgs c;
+        c.src = static_cast<const unsigned char *>(src);
+        c.src_stride_bytes = src_stride * (int64_t)es;
+        c.n_src = (int)n_src;
+        c.C = sh.C;
+        c.T = T;
+        c.d = (int)d;
+        c.query = queries;
+        c.gain = gain;
+        c.eps = eps;
+        c.inv_d = 1.f / (float)d;
+        c.dout = static_cast<const unsigned char *>(dout);
+        c.dlse = dlse;
+        c.coef = coef;
+        c.nstages = sh.nstages;
+        c.pitch = sh.pitch;
+        c.stage_bytes = sh.stage_bytes;
+        c.wait = wait_cfg(dev);
+        const int grid = (int)(T < dev->sms ? T : dev->sms);
+        void *cargs[] = {&c};
+        cudaError_t e = cudaLaunchKernel(kc.fn, dim3(grid), dim3(RC_NW * 32), cargs, sh.smem, s);
+        if (e != cudaSuccess) return cuda_fail(e, "read_bwd many-source coefficient launch");
+        ReadBwdApplyManyArgs p;
+        p.src = c.src;
+        p.src_stride_bytes = c.src_stride_bytes;
+        p.n_src = (int)n_src;
+        p.C = sh.C;
+        p.T = T;
+        p.d = (int)d;
+        p.query = queries;
+        p.gain = gain;
+        p.dout = c.dout;
+        p.coef = coef;
+        p.dsrc = static_cast<unsigned char *>(dsrc);
+        p.dsrc_stride_bytes = dsrc_stride * (int64_t)es;
+        p.accumulate = accumulate;
+        p.ws = static_cast<float *>(ws);
+        p.tpc = sh.tpc;
+        void *pargs[] = {&p};
+        e = cudaLaunchKernel(ka.fn, dim3((unsigned)(d / RA_W), (unsigned)sh.chunks), dim3(RA_THREADS), pargs,
+                             RM_RING_BYTES, s);
+        if (e != cudaSuccess) return cuda_fail(e, "read_bwd many-source apply launch");
+        ReadBwdFinishArgs f;
+        f.ws = p.ws;
+        f.nparts = sh.chunks;
+        f.n_q = 1;
+        f.d = (int)d;
+        f.queries = queries;
+        f.gain = gain;
+        f.dq = dq;
+        f.dgain = dgain;
+        f.accumulate_dgain = 0;
+        void *fargs[] = {&f};
+        e = cudaLaunchKernel(read_bwd_finish_fn(), dim3((unsigned)((d + 31) / 32)), dim3(256), fargs, 0, s);
+        if (e != cudaSuccess) return cuda_fail(e, "read_bwd finish launch");
+        return ATTNRES_OK;
+    }
     ReadBwdManyPlan p;
     st = read_bwd_many_plan(n_src, T, d, n_q, dt, dev, &p);
     if (st != ATTNRES_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 0) {
         cudaError_t e = cudaMemsetAsync(dq, 0, dq_bytes, s);
         if (e == cudaSuccess && dgain) e = cudaMemsetAsync(dgain, 0, (size_t)d * 4, s);
@@ -2084,6 +2212,13 @@ static attnres_status_t read_bwd_workspace(int64_t n_src, int64_t T, int64_t d, 
         DeviceInfo *dev = nullptr;
         attnres_status_t st = device_info(&dev);
         if (st != ATTNRES_OK) return st;
+        if (read_bwd_many_split_applies(dt, n_src, n_q, d)) {
+            ReadBwdManySplitShape sh;
+            st = read_bwd_many_split_shape(n_src, T, d, dev, &sh);
+            if (st != ATTNRES_OK) return st;
+            *bytes = sh.total;
+            return ATTNRES_OK;
+        }
         ReadBwdManyPlan p;
         st = read_bwd_many_plan(n_src, T, d, n_q, dt, dev, &p);
         if (st != ATTNRES_OK) return st;

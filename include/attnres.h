@@ -242,7 +242,11 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  * reads the sources and dout twice and rounds a bf16 dsrc once.  Other
  * passes of 3 or 4 queries run two groups of two in one kernel, the second
  * group adding into the bf16 dsrc the first has rounded.
- * More than 16 sources (Full AttnRes past layer 16): the sources are taken in
+ * More than 16 sources (Full AttnRes past layer 16): with one query, bf16,
+ * at most 64 sources and d = 2048 or 4096, two kernels (the first streams
+ * every source once and writes each token's coefficients, 72 floats per
+ * chunk of 8 sources, to the workspace; the second forms dsrc and the sums
+ * over the tokens in slices of channels).  Otherwise the sources are taken in
  * chunks of 8.  Each chunk's read state (o_c, lse_c) is recomputed, and the
  * backward of the states' online-softmax merge (b-lab.team summary, section
  * 3: LSE = log sum_c e^{lse_c}, beta_c = e^{lse_c - LSE}, h = sum_c beta_c o_c)

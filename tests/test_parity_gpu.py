@@ -456,6 +456,65 @@ def test_block_phase1_bwd_many_sources_with_lse_gradient():
     _check_grads_states(got, oracle.block_phase1_bwd(src, q, d_o, dlse, None, 1e-6), BF16, "phase 1, 28 sources")
 
 
+@pytest.fixture(params=[0, 1], ids=["two-kernel", "chain"])
+def many_variant(request):
+    """Kernel variant 0 runs the backward of one query over 17..64 bf16
+    sources at d = 2048 or 4096 as two kernels (coefficients over all the
+    sources, then channel slices); variant 1 keeps the chunked chain."""
+    attnres.attnres_debug_set_kernel_variant(request.param)
+    yield request.param
+    attnres.attnres_debug_set_kernel_variant(0)
+
+
+@pytest.mark.parametrize("n_src,T,d,with_gain,with_lse", [
+    (17, 100, 4096, True, False),        # one source past two chunks
+    (40, 7, 2048, True, True),           # five full chunks, the lse gradient
+    (64, 300, 4096, False, True),        # the deepest Full-at-depth layer
+    (23, 1, 4096, True, False),          # one token, a short last chunk
+    (33, 160, 2048, False, False)])      # a one-source last chunk
+def test_read_bwd_many_sources_both_forms(many_variant, n_src, T, d, with_gain, with_lse):
+    """The backward of one query over many sources under both forms against
+    the oracle's chain rule over all the sources at once.  The two-kernel
+    form keeps nothing in bf16 between its steps and is held to the strict
+    bar; the chain holds the chunks' states in bf16 (see _check_grads_states)."""
+    rng = _rng(n_src * 7 + T + d)
+    src = _sources(rng, n_src, T, d, BF16, step=0.1)
+    q = _queries(rng, 1, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gain else None
+    dout = _sources(rng, 1, T, d, BF16, step=0)
+    sd, qd, od = to_dev(src, BF16), to_dev(q, F32), to_dev(dout, BF16)
+    gd = to_dev(g, F32) if with_gain else None
+    if with_lse:
+        dl = rng.standard_normal((1, T)).astype(np.float32)
+        got = attnres.attnres_block_phase1_bwd(sd, qd, od, to_dev(dl, F32), gd, 1e-6)
+        ref = oracle.block_phase1_bwd(src, q, dout, dl, g, 1e-6)
+    else:
+        got = attnres.attnres_read_bwd(sd, qd, od, gd, 1e-6)
+        ref = oracle.read_bwd(src, q, dout, g, 1e-6)
+    what = f"variant {many_variant}, {n_src} sources"
+    if many_variant == 0:
+        _check_grads(got, ref, BF16, what)
+    else:
+        _check_grads_states(got, ref, BF16, what)
+
+
+def test_read_bwd_many_sources_two_kernel_form_is_deterministic_and_accumulates():
+    rng = _rng(54)
+    n_src, T, d = 48, 250, 4096
+    src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.1), BF16)
+    q = to_dev(_queries(rng, 1, d), F32)
+    dout = to_dev(_sources(rng, 1, T, d, BF16, step=0), BF16)
+    g = to_dev(rng.uniform(0.5, 1.5, d).astype(np.float32), F32)
+    a = attnres.attnres_read_bwd(src, q, dout, g)
+    b = attnres.attnres_read_bwd(src, q, dout, g)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    base = to_dev(_sources(rng, n_src, T, d, BF16), BF16)
+    acc = base.clone()
+    attnres.attnres_read_bwd(src, q, dout, g, dsrc=acc, accumulate=True)
+    check_out(acc, to_host(base) + to_host(a[0]), BF16, what="accumulated dsrc")
+
+
 def test_read_bwd_accumulates_and_is_deterministic():
     rng = _rng(51)
     n_src, T, d = 9, 200, 4096
