@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
         }
         *imax = 0;
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], NW * 32);
-            mbar_init(&tfree[b], 32);
+            mbar_init(&tfull[b], NW);
+            mbar_init(&tfree[b], 1);
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -143,8 +143,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
 
     // ------------------------------------------------------------ producer
     // part k (token item k / ppt, chunk (k % ppt) / 2, half k % 2) into stage
-    // k % nstages: the first nstages by thread 0, each later one by lane 0 of
-    // the warp that finishes the part nstages before it last
+    // k % nstages, by a whole warp: lane 0 arms the stage's barrier, then lane
+    // i copies row i (one lane issuing every copy was the pace of the ring).
+    // The first nstages by warp 0, each later one by the warp that finishes
+    // the part nstages before it last.
     const bool may_issue = !a.wait.inject_stall;
     const uint64_t pol_first = l2_policy_evict_first();
     auto issue = [&](int k) {
@@ -155,19 +157,24 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
         const int64_t t = blockIdx.x + (int64_t)it * gstride;
         const int64_t off = (t * a.d + (int64_t)h * (a.d / 2)) * 2;
         unsigned char *dst = stages + (size_t)s * a.stage_bytes;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)half_bytes * (uint32_t)(nc + 1));
-        for (int i = 0; i < nc; ++i)
-            bulk_g2s(dst + (size_t)i * a.pitch, a.src + (int64_t)(8 * c + i) * a.src_stride_bytes + off,
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)half_bytes * (uint32_t)(nc + 1));
+            atomicMax(imax, (unsigned)(k + 1));
+        }
+        __syncwarp();
+        if (lane < nc) {
+            bulk_g2s(dst + (size_t)lane * a.pitch, a.src + (int64_t)(8 * c + lane) * a.src_stride_bytes + off,
                      (uint32_t)half_bytes, &full[s], pol_first);
-        // the gradient row is read again for every chunk: no evict-first hint
-        asm volatile(
-            "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                smem_u32(dst + (size_t)8 * a.pitch)),
-            "l"(a.dout + off), "r"((uint32_t)half_bytes), "r"(smem_u32(&full[s]))
-            : "memory");
-        atomicMax(imax, (unsigned)(k + 1));
+        } else if (lane == 8) {
+            // the gradient row is read again for every chunk: no evict-first hint
+            asm volatile(
+                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(dst + (size_t)8 * a.pitch)),
+                "l"(a.dout + off), "r"((uint32_t)half_bytes), "r"(smem_u32(&full[s]))
+                : "memory");
+        }
     };
-    if (tid == 0 && may_issue)
+    if (warp == 0 && may_issue)
         for (int k = 0; k < n_parts && k < a.nstages; ++k) issue(k);
 
     // ------------------------------------------------------------ constants
@@ -211,7 +218,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
                 }
             }
         }
-        mbar_arrive(&tfree[it & 1]);                      // this lane's reads are done
+        // the warp's reads are done: one arrival per warp (its lanes' reads are
+        // ordered before lane 0's release by the warp barrier)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfree[it & 1]);
         float rinv[2], score[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -292,13 +302,15 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
         else pass(bw[1]);
         // this warp is done with the stage; the last warp to be refills it
         __syncwarp();
+        int refill = 0;
         if (lane == 0) {
             __threadfence_block();
             if (atomicAdd(&done[s], 1u) == NW - 1) {
                 done[s] = 0;
-                if (k + a.nstages < n_parts && may_issue && !*abort_flag) issue(k + a.nstages);
+                refill = k + a.nstages < n_parts && may_issue && !*abort_flag;
             }
         }
+        if (__shfl_sync(0xffffffffu, refill, 0)) issue(k + a.nstages);
         __syncwarp();
         if (h == 1) {
             // the chunk's sums: lane (i, 0) (w*g).v_i = columns 0 + 1 (first
@@ -315,7 +327,9 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
             if (t4 < 2) rb[(c * RM_NV + 8 * t4 + g4) * RS + warp] = v;
             if (t4 == (g4 >> 1)) rb[(c * RM_NV + 16 + g4) * RS + warp] = ssq;
             if (c == C - 1) {
-                mbar_arrive(&tfull[it & 1]);
+                // the warp's table writes are done: one arrival per warp
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tfull[it & 1]);
                 // the coefficient duty rotates over the warps; the lse gradient
                 // is fetched now, the work done one half row later
                 if (warp == it % NW) {

@@ -19,9 +19,9 @@
 // double-buffered table, then per head one warp forms the softmax and the
 // coefficients and writes them: coef[t][head] = {alpha[q*8+i] (32),
 // b[q*8+i] (32), c[i] (8)}.  The table is handed over by mbarriers, not a
-// CTA barrier (every thread arrives on "full" after its writes; the
-// coefficient warps wait on it and arrive on "free" after their reads, which
-// the writers of the token two later wait on), the coefficient duty
+// CTA barrier (each warp arrives on "full" after its writes; the coefficient
+// warps wait on it and arrive on "free" after their reads, which the writers
+// of the token two later wait on), the coefficient duty
 // rotates over the warps from token to token, and a warp does a token's
 // coefficients after its first half of the next token (the lse gradient
 // fetched when the duty is taken), so neither the softmax nor its loads hold
@@ -126,8 +126,8 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
         }
         *imax = 0;
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], NW * 32);
-            mbar_init(&tfree[b], a.H * 32);
+            mbar_init(&tfull[b], NW);
+            mbar_init(&tfree[b], a.H);
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -148,9 +148,11 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
     const int n_halves = 2 * n_items;
 
     // ------------------------------------------------------------ producer
-    // half k (token item k/2, channel half k%2) into stage k % nstages: the
-    // first nstages by thread 0, each later one by lane 0 of the warp that
-    // finishes the half nstages before it last
+    // half k (token item k/2, channel half k%2) into stage k % nstages, by a
+    // whole warp: lane 0 arms the stage's barrier, then lane i copies row i
+    // (a single lane issuing every row's bulk copy was the pace of the ring).
+    // The first nstages by warp 0, each later one by the warp that finishes
+    // the half nstages before it last.
     const bool may_issue = !a.wait.inject_stall;
     const uint64_t pol = l2_policy_evict_first();
     auto issue = [&](int k) {
@@ -158,16 +160,19 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
         const int64_t t = blockIdx.x + (int64_t)(k >> 1) * gstride;
         const int64_t off = (t * a.d + (int64_t)(k & 1) * (a.d / 2)) * 2;
         unsigned char *dst = stages + (size_t)s * a.stage_bytes;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)half_bytes * (uint32_t)(a.n_src + a.n_q));
-        for (int i = 0; i < a.n_src; ++i)
-            bulk_g2s(dst + (size_t)i * a.pitch, a.src + (int64_t)i * a.src_stride_bytes + off, (uint32_t)half_bytes,
-                     &full[s], pol);
-        for (int q = 0; q < a.n_q; ++q)
-            bulk_g2s(dst + (size_t)(8 + q) * a.pitch, a.dout + (int64_t)q * a.T * a.d * 2 + off,
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)half_bytes * (uint32_t)(a.n_src + a.n_q));
+            atomicMax(imax, (unsigned)(k + 1));
+        }
+        __syncwarp();
+        if (lane < a.n_src)
+            bulk_g2s(dst + (size_t)lane * a.pitch, a.src + (int64_t)lane * a.src_stride_bytes + off,
                      (uint32_t)half_bytes, &full[s], pol);
-        atomicMax(imax, (unsigned)(k + 1));
+        else if (lane >= 8 && lane - 8 < a.n_q)
+            bulk_g2s(dst + (size_t)lane * a.pitch, a.dout + (int64_t)(lane - 8) * a.T * a.d * 2 + off,
+                     (uint32_t)half_bytes, &full[s], pol);
     };
-    if (tid == 0 && may_issue)
+    if (warp == 0 && may_issue)
         for (int k = 0; k < n_halves && k < a.nstages; ++k) issue(k);
 
     // ------------------------------------------------------------ constants
@@ -220,7 +225,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
                 for (int c = 0; c < ncol; ++c) { ss += ps[c]; sw += pw[c]; sd += pd[c]; }
             }
         }
-        mbar_arrive(&tfree[it & 1]);                      // this lane's reads are done
+        // the warp's reads are done: one arrival per warp (its lanes' reads are
+        // ordered before lane 0's release by the warp barrier)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfree[it & 1]);
         const bool pv = q < a.n_q && i < a.n_src;
         const float ms = fmaf(ss, a.inv_dh, a.eps);
         const float rinv = ms > 0.f ? rsqrtf(ms) : 0.f;  // 1 / r_i (0 for a zero key)
@@ -288,13 +296,15 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
         else pass(bq[1]);
         // this warp is done with the stage; the last warp to be refills it
         __syncwarp();
+        int refill = 0;
         if (lane == 0) {
             __threadfence_block();
             if (atomicAdd(&done[s], 1u) == NW - 1) {
                 done[s] = 0;
-                if (k + a.nstages < n_halves && may_issue && !*abort_flag) issue(k + a.nstages);
+                refill = k + a.nstages < n_halves && may_issue && !*abort_flag;
             }
         }
+        if (__shfl_sync(0xffffffffu, refill, 0)) issue(k + a.nstages);
         __syncwarp();
         if (per_half || h == 1) {
             // the first write of this token's table waits until the coefficient
@@ -326,7 +336,9 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
             if (t4 == (RC_GRAM ? g4 >> 1 : 0)) rb[(64 + g4) * RS + col] = ss;
         }
         if (h == 1) {
-            mbar_arrive(&tfull[it & 1]);
+            // the warp's table writes are done: one arrival per warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tfull[it & 1]);
             // head whose coefficients this warp forms for this token (the duty
             // rotates: head hd goes to warp (hd + it*H) % NW); the work itself
             // waits until after this warp's first half of the next token, when
