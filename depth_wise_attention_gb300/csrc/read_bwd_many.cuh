@@ -149,8 +149,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
     // the part nstages before it last.
     const bool may_issue = !a.wait.inject_stall;
     const uint64_t pol_first = l2_policy_evict_first();
-    auto issue = [&](int k) {
-        const int s = k % a.nstages;
+    auto issue = [&](int k, int s) {               // s = k % nstages
         const int it = k / ppt, pc = k - it * ppt;
         const int c = pc >> 1, h = pc & 1;
         const int nc = a.n_src - 8 * c < 8 ? a.n_src - 8 * c : 8;
@@ -175,7 +174,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
         }
     };
     if (warp == 0 && may_issue)
-        for (int k = 0; k < n_parts && k < a.nstages; ++k) issue(k);
+        for (int k = 0; k < n_parts && k < a.nstages; ++k) issue(k, k);
 
     // ------------------------------------------------------------ constants
     uint32_t bw[2][KS2][2];
@@ -267,11 +266,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
     };
 
     float d1[2][4], gr[2][4];
+    int s = 0, it = 0, pc = 0;                    // stage of part k and its parity; token item, part in it
+    uint32_t par = 0;
     for (int k = 0; k < n_parts; ++k) {
-        const int it = k / ppt, pc = k - it * ppt;
         const int c = pc >> 1, h = pc & 1;
-        const int s = k % a.nstages;
-        const uint32_t par = (uint32_t)(k / a.nstages) & 1u;
         const int64_t t = blockIdx.x + (int64_t)it * gstride;
         if (h == 0) {
 #pragma unroll
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
                 refill = k + a.nstages < n_parts && may_issue && !*abort_flag;
             }
         }
-        if (__shfl_sync(0xffffffffu, refill, 0)) issue(k + a.nstages);
+        if (__shfl_sync(0xffffffffu, refill, 0)) issue(k + a.nstages, s);
         __syncwarp();
         if (h == 1) {
             // the chunk's sums: lane (i, 0) (w*g).v_i = columns 0 + 1 (first
@@ -332,7 +330,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
                 if (lane == 0) mbar_arrive(&tfull[it & 1]);
                 // the coefficient duty rotates over the warps; the lse gradient
                 // is fetched now, the work done one half row later
-                if (warp == it % NW) {
+                if (warp == (it & (NW - 1))) {
                     pend_it = it;
                     pend_t = t;
                     pend_dl = a.dlse != nullptr ? __ldg(a.dlse + t) : 0.f;
@@ -342,6 +340,8 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_many_kernel(const
             coefficients();
             pend_it = -1;
         }
+        if (++s == a.nstages) { s = 0; par ^= 1u; }
+        if (++pc == ppt) { pc = 0; ++it; }
     }
     if (pend_it >= 0) coefficients();
     // copies still in flight (only after an abort) must land before the CTA exits
@@ -401,11 +401,14 @@ __global__ void __launch_bounds__(RA_THREADS, 2) read_bwd_apply_many_kernel(cons
     auto slot_addr = [&](int slot, int row) { return ring0 + (uint32_t)((slot * RM_ROWS + row) * RA_THREADS) * 8; };
     // unit u = (token t0 + u / C, chunk u % C): the chunk's rows, and with the
     // first chunk the gradient row, into ring slot `slot` (one commit group
-    // per unit, empty past the range)
-    auto issue = [&](int64_t u, int slot) {
-        if (u < nunits) {
-            const int64_t tt = t0 + u / C;
-            const int ch = (int)(u % C);
+    // per unit, empty past the range).  Units are issued in order; the next
+    // one's token and chunk are counted, not divided out.
+    int64_t iu = 0, it_tok = t0;
+    int it_ch = 0;
+    auto issue = [&](int slot) {
+        if (iu < nunits) {
+            const int64_t tt = it_tok;
+            const int ch = it_ch;
             const int nc = a.n_src - 8 * ch < 8 ? a.n_src - 8 * ch : 8;
             const size_t off = ((size_t)tt * a.d + c) * 2;
             for (int i = 0; i < nc; ++i)
@@ -413,12 +416,13 @@ __global__ void __launch_bounds__(RA_THREADS, 2) read_bwd_apply_many_kernel(cons
             if (ch == 0) cp_async8(slot_addr(slot, 8), a.dout + off);
         }
         cp_async_commit();
+        ++iu;
+        if (++it_ch == C) { it_ch = 0; ++it_tok; }
     };
-    issue(0, 0);
-    issue(1, 1);
+    issue(0);
+    issue(1);
 
     int slot = 0;
-    int64_t u = 0;
     for (int64_t tb = t0; tb < t1; tb += RM_TB) {
         const int nb = t1 - tb < RM_TB ? (int)(t1 - tb) : RM_TB;
         __syncthreads();                                    // the previous batch is consumed
@@ -433,10 +437,10 @@ __global__ void __launch_bounds__(RA_THREADS, 2) read_bwd_apply_many_kernel(cons
             const int64_t t = tb + tok;
             const size_t off = ((size_t)t * a.d + c) * 2;
             float2 dl[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            for (int ch = 0; ch < C; ++ch, ++u) {
+            for (int ch = 0; ch < C; ++ch) {
                 // unit u+2 into the slot unit u-1 used (this thread's reads of it
                 // are consumed by the arithmetic below before this issue)
-                issue(u + 2, slot == 0 ? RA_DEPTH - 1 : slot - 1);
+                issue(slot == 0 ? RA_DEPTH - 1 : slot - 1);     // unit u + 2
                 cp_async_wait<2>();                         // unit u's rows have landed
                 if (ch == 0) {
                     const uint2 r = lds64(slot_addr(slot, 8));

@@ -155,8 +155,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
     // the half nstages before it last.
     const bool may_issue = !a.wait.inject_stall;
     const uint64_t pol = l2_policy_evict_first();
-    auto issue = [&](int k) {
-        const int s = k % a.nstages;
+    auto issue = [&](int k, int s) {               // s = k % nstages
         const int64_t t = blockIdx.x + (int64_t)(k >> 1) * gstride;
         const int64_t off = (t * a.d + (int64_t)(k & 1) * (a.d / 2)) * 2;
         unsigned char *dst = stages + (size_t)s * a.stage_bytes;
@@ -173,7 +172,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
                      (uint32_t)half_bytes, &full[s], pol);
     };
     if (warp == 0 && may_issue)
-        for (int k = 0; k < n_halves && k < a.nstages; ++k) issue(k);
+        for (int k = 0; k < n_halves && k < a.nstages; ++k) issue(k, k);
 
     // ------------------------------------------------------------ constants
     uint32_t bq[2][KSH][2];
@@ -254,10 +253,10 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
 
     float d1[2][4], dd[2][4], gr[2][4];
     float2 sq = make_float2(0.f, 0.f);
+    int s = 0;                                    // stage of half k, and its phase parity
+    uint32_t par = 0;
     for (int k = 0; k < n_halves; ++k) {
         const int it = k >> 1, h = k & 1;
-        const int s = k % a.nstages;
-        const uint32_t par = (uint32_t)(k / a.nstages) & 1u;
         const int64_t t = blockIdx.x + (int64_t)it * gstride;
         if (h == 0 || per_half) {
 #pragma unroll
@@ -304,7 +303,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
                 refill = k + a.nstages < n_halves && may_issue && !*abort_flag;
             }
         }
-        if (__shfl_sync(0xffffffffu, refill, 0)) issue(k + a.nstages);
+        if (__shfl_sync(0xffffffffu, refill, 0)) issue(k + a.nstages, s);
         __syncwarp();
         if (per_half || h == 1) {
             // the first write of this token's table waits until the coefficient
@@ -344,7 +343,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
             // waits until after this warp's first half of the next token, when
             // every warp has long written the table, and the lse gradient it
             // needs is fetched now
-            const int hd = (int)(((int64_t)warp - (int64_t)it * a.H) % NW + NW) % NW;
+            const int hd = (warp - it * a.H) & (NW - 1);
             if (hd < a.H) {
                 pend_it = it;
                 pend_t = t;
@@ -356,6 +355,7 @@ __global__ void __launch_bounds__(RC_NW * 32, 1) read_bwd_coef_kernel(const Read
             coefficients();
             pend_it = -1;
         }
+        if (++s == a.nstages) { s = 0; par ^= 1u; }
     }
     if (pend_it >= 0) coefficients();
     // copies still in flight (only after an abort) must land before the CTA exits
