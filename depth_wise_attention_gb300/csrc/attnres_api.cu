@@ -21,6 +21,7 @@
 #include "merge_bwd.cuh"
 #include "read_bwd.cuh"
 #include "read_bwd_split.cuh"
+#include "read_bwd_one.cuh"
 #include "read_bwd_many.cuh"
 #include "state_merge_bwd.h"
 
@@ -616,6 +617,61 @@ attnres_status_t read_bwd_split_shape(int64_t T, int64_t d, int64_t H, const Dev
     return ATTNRES_OK;
 }
 
+// The one-kernel ring form (read_bwd_one.cuh) takes a pass of one query over
+// 3 to 8 bf16 sources at d = 2048 or 4096 whose rows can be bulk-copied
+// (measured at T = 32768, d = 4096: 0.54 vs 0.55 ms at 3 sources, 0.80 vs
+// 1.02 ms at 8; debug kernel variant 1 keeps read_bwd_kernel).  Its
+// workspace, one partial of U per CTA, is within read_bwd_ws_bytes.
+bool read_bwd_one_applies(attnres_dtype_t dt, int64_t n_src, int64_t nq, int64_t d, int64_t H, const void *src,
+                          int64_t src_stride) {
+    if (g_kernel_variant.load() == 1) return false;
+    return dt == ATTNRES_BF16 && n_src >= 3 && n_src <= 8 && nq == 1 && H == 1 && (d == 2048 || d == 4096) &&
+           aligned16(src) && (src_stride * 2) % 16 == 0;
+}
+
+// One pass of one query in the one-kernel ring form: one CTA per SM, U as one
+// partial per CTA at the start of the workspace (*nparts of them).
+attnres_status_t launch_read_bwd_one_pass(const ReadBwdArgs &a, const DeviceInfo *dev, void *stream, int *nparts) {
+    KernelRef kr;
+    if (!lookup_read_bwd_one(a.d, &kr)) return ATTNRES_ERR_UNSUPPORTED;
+    ReadBwdOneArgs o;
+    o.pitch = (uint32_t)a.d + 16;
+    o.stage_bytes = (uint32_t)R1_ROWS * o.pitch;
+    size_t budget = kSmemBudget;
+    if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
+    if (budget <= R1_AUX_BYTES) return ATTNRES_ERR_UNSUPPORTED;
+    int ns = (int)((budget - R1_AUX_BYTES) / o.stage_bytes);
+    if (ns > R1_MAX_STAGES) ns = R1_MAX_STAGES;
+    if (ns < 4) return ATTNRES_ERR_UNSUPPORTED;     // two tokens' stages are held at a time
+    const size_t smem = (size_t)ns * o.stage_bytes + R1_AUX_BYTES;
+    int occ = 0;
+    attnres_status_t st = prepare_kernel(kr.fn, smem, R1_NW * 32, &occ);
+    if (st != ATTNRES_OK) return st;
+    o.src = a.src;
+    o.src_stride_bytes = a.src_stride_bytes;
+    o.n_src = a.n_src;
+    o.T = a.T;
+    o.d = a.d;
+    o.query = a.queries;
+    o.gain = a.gain;
+    o.eps = a.eps;
+    o.inv_d = a.inv_dh;
+    o.dout = a.dout;
+    o.dlse = a.dlse;
+    o.dsrc = a.dsrc;
+    o.dsrc_stride_bytes = a.dsrc_stride_bytes;
+    o.accumulate = a.accumulate;
+    o.ws = a.ws;
+    o.nstages = ns;
+    o.wait = a.wait;
+    const int grid = (int)(a.T < dev->sms ? a.T : dev->sms);
+    void *args[] = {&o};
+    cudaError_t e = cudaLaunchKernel(kr.fn, dim3(grid), dim3(R1_NW * 32), args, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "read_bwd one-query launch");
+    *nparts = grid;
+    return ATTNRES_OK;
+}
+
 // Workspace launch_read_bwd needs for these arguments: the larger of the
 // kernel forms its query passes take.
 attnres_status_t read_bwd_ws_need(int64_t n_src, int64_t T, int64_t d, int64_t H, int64_t n_q,
@@ -742,12 +798,14 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
     // kernels of every pass (a last pass may take fewer queries): up to 2
     // queries one group, 3 or 4 two groups of two, or the two-kernel form
     KernelRef kr[2];
-    bool split[2];
+    bool split[2], one[2], plain[2];
     const int nq_last = (int)(n_q - (n_q - 1) / sh.nqc * sh.nqc);
     for (int v = 0; v < 2; ++v) {
         const int nq = v == 0 ? (int)(n_q < sh.nqc ? n_q : sh.nqc) : nq_last;
         split[v] = read_bwd_split_applies(dt, n_src, nq, d, H);
-        if (split[v]) continue;
+        one[v] = !split[v] && read_bwd_one_applies(dt, n_src, nq, d, H, src, src_stride);
+        plain[v] = !split[v] && !one[v];
+        if (!plain[v]) continue;
         const int dti = dt == ATTNRES_BF16 ? 1 : 0;
         const bool ok = nq > 2 ? lookup_read_bwd_qg(dti, sh.vpt, sh.mh, sh.hg, &kr[v])
                         : sh.mh ? lookup_read_bwd_mh(dti, nq, sh.ns, sh.vpt, sh.hg, &kr[v])
@@ -760,14 +818,14 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
     if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
     size_t aux = 0;
     for (int v = 0; v < 2; ++v)
-        if (!split[v] && kr[v].aux_smem > aux) aux = kr[v].aux_smem;
+        if (plain[v] && kr[v].aux_smem > aux) aux = kr[v].aux_smem;
     if (budget <= aux) return ATTNRES_ERR_UNSUPPORTED;
     int nstages = (int)((budget - aux) / stage_bytes);
     if (nstages > RB_MAX_STAGES) nstages = RB_MAX_STAGES;
-    if (nstages < 2 && (!split[0] || !split[1])) return ATTNRES_ERR_UNSUPPORTED;
+    if (nstages < 2 && (plain[0] || plain[1])) return ATTNRES_ERR_UNSUPPORTED;
     const size_t smem = (size_t)nstages * stage_bytes + aux;
     for (int v = 0; v < 2; ++v) {
-        if (split[v]) continue;
+        if (!plain[v]) continue;
         int occ = 0;
         st = prepare_kernel(kr[v].fn, smem, RB_THREADS, &occ);
         if (st != ATTNRES_OK) return st;
@@ -810,12 +868,15 @@ attnres_status_t launch_read_bwd(const void *src, int64_t n_src, int64_t src_str
         a.dout = static_cast<const unsigned char *>(dout) + (size_t)q0 * (size_t)T * (size_t)d * es;
         a.dlse = dlse ? dlse + q0 * T : nullptr;
         a.accumulate = q0 == 0 ? accumulate : 1;
-        const bool sp = nq == (n_q < sh.nqc ? n_q : sh.nqc) ? split[0] : split[1];
+        const int pv = nq == (n_q < sh.nqc ? n_q : sh.nqc) ? 0 : 1;
         int nparts = grid * sh.tt;
-        if (sp) {
+        if (split[pv]) {
             st = launch_read_bwd_split_pass(a, nq, H, ss, dev->sms, stream);
             if (st != ATTNRES_OK) return st;
             nparts = ss.chunks;
+        } else if (one[pv]) {
+            st = launch_read_bwd_one_pass(a, dev, stream, &nparts);
+            if (st != ATTNRES_OK) return st;
         } else {
             void *args[] = {&a};
             const void *fn = kr[nq == sh.nqc ? 0 : 1].fn;

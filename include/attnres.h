@@ -241,7 +241,10 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  * second forms dsrc and the sums over the tokens in slices of channels.  It
  * reads the sources and dout twice and rounds a bf16 dsrc once.  Other
  * passes of 3 or 4 queries run two groups of two in one kernel, the second
- * group adding into the bf16 dsrc the first has rounded.
+ * group adding into the bf16 dsrc the first has rounded.  A pass of one query
+ * over 3 to 8 bf16 sources at d = 2048 or 4096 (src and src_stride 16-byte
+ * aligned) reads them once through a ring of half-row stages, one CTA per
+ * SM, with one partial of the sums over the tokens per CTA.
  * More than 16 sources (Full AttnRes past layer 16): with one query, bf16,
  * at most 64 sources and d = 2048 or 4096, two kernels (the first streams
  * every source once and writes each token's coefficients, 72 floats per

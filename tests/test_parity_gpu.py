@@ -638,6 +638,73 @@ def test_read_bwd_two_kernel_form_is_deterministic_accumulates_and_agrees_with_o
         assert np.abs(u - v).max() <= 1e-4 * np.abs(v).max(), name
 
 
+@pytest.fixture(params=[0, 1], ids=["ring", "whole-token"])
+def one_variant(request):
+    """Kernel variant 0 runs the read backward of one query over 3 to 8 bf16
+    sources (d = 2048 or 4096) in the ring of half-row stages; variant 1 keeps
+    the kernel with whole-token stages."""
+    attnres.attnres_debug_set_kernel_variant(request.param)
+    yield request.param
+    attnres.attnres_debug_set_kernel_variant(0)
+
+
+@pytest.mark.parametrize("n_src,T,d,with_gain,with_lse", [
+    (8, 300, 4096, True, False),     # the MSAR per-stream read backward's shape
+    (8, 300, 4096, True, True),      # Block phase 1's backward with one query, lse gradient
+    (3, 151, 2048, False, True),     # fewer tokens than SMs
+    (3, 1, 4096, True, False),       # one token (one CTA, one step of the pipeline)
+    (5, 1000, 2048, True, False),    # several tokens per CTA, ragged ring
+    (7, 9, 4096, False, False)])
+def test_read_bwd_one_query_both_forms(one_variant, n_src, T, d, with_gain, with_lse):
+    """The read backward of one query over 3 to 8 sources under both kernel
+    forms against the oracle's chain rule (with Block phase 1's lse gradient
+    where given)."""
+    rng = _rng(n_src * 17 + T + d + 3 * with_lse)
+    src = _sources(rng, n_src, T, d, BF16, step=0.25)
+    q = _queries(rng, 1, d)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32) if with_gain else None
+    dout = _sources(rng, 1, T, d, BF16, step=0)
+    sd, qd, od = to_dev(src, BF16), to_dev(q, F32), to_dev(dout, BF16)
+    gd = to_dev(g, F32) if with_gain else None
+    if with_lse:
+        dl = rng.standard_normal((1, T)).astype(np.float32)
+        got = attnres.attnres_block_phase1_bwd(sd, qd, od, to_dev(dl, F32), gd, 1e-6)
+        ref = oracle.block_phase1_bwd(src, q, dout, dl, g, 1e-6)
+    else:
+        got = attnres.attnres_read_bwd(sd, qd, od, gd, 1e-6)
+        ref = oracle.read_bwd(src, q, dout, g, 1e-6)
+    _check_grads(got, ref, BF16, f"variant {one_variant}")
+
+
+def test_read_bwd_one_query_ring_is_deterministic_accumulates_and_agrees_with_whole_token_form():
+    """Two runs of the ring form agree bitwise; with accumulate it adds into
+    the given source gradients; and it agrees with the whole-token form within
+    the bf16 bar (both round dsrc once; their sums run in different orders)."""
+    rng = _rng(59)
+    n_src, T, d = 8, 700, 4096
+    src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.25), BF16)
+    q = to_dev(_queries(rng, 1, d), F32)
+    dout = to_dev(_sources(rng, 1, T, d, BF16, step=0), BF16)
+    g = to_dev(rng.uniform(0.5, 1.5, d).astype(np.float32), F32)
+    a = attnres.attnres_read_bwd(src, q, dout, g)
+    b = attnres.attnres_read_bwd(src, q, dout, g)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    base = to_dev(_sources(rng, n_src, T, d, BF16), BF16)
+    acc = base.clone()
+    attnres.attnres_read_bwd(src, q, dout, g, dsrc=acc, accumulate=True)
+    check_out(acc, to_host(base) + to_host(a[0]), BF16, what="accumulated dsrc")
+    attnres.attnres_debug_set_kernel_variant(1)
+    try:
+        c = attnres.attnres_read_bwd(src, q, dout, g)
+    finally:
+        attnres.attnres_debug_set_kernel_variant(0)
+    check_out(a[0], to_host(c[0]).astype(np.float64), BF16, what="dsrc of the two forms")
+    for name, u, v in (("dq", a[1], c[1]), ("dgain", a[2], c[2])):
+        u, v = to_host(u).astype(np.float64), to_host(v).astype(np.float64)
+        assert np.abs(u - v).max() <= 1e-4 * np.abs(v).max(), name
+
+
 @pytest.mark.parametrize("T,d,dtype,with_gain,with_partial", [
     (100, 4096, BF16, True, True), (37, 2048, BF16, False, True), (50, 256, F32, True, True),
     (333, 1000, F32, True, True), (20, 512, BF16, True, False), (1, 64, F32, False, True)])
