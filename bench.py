@@ -55,7 +55,12 @@ KERNEL_SOURCES = {
     "read_bwd_mh": [CSRC + "read_bwd.cuh", CSRC + "common.cuh", CSRC + "kernels_bwd.cu", CSRC + "kernels_bwd_mh.cu"],
     "depth_read_decode": [CSRC + "depth_read_decode.cuh", CSRC + "common.cuh", CSRC + "kernels_decode.cu"],
     "msar_bwd": [CSRC + "msar_bwd.cu", CSRC + "msar_bwd.h", CSRC + "msar.h", CSRC + "common.cuh",
-                 CSRC + "read_bwd.cuh", CSRC + "kernels_bwd.cu", CSRC + "depth_read_mma.cuh", CSRC + "kernels_mma.cu"],
+                 CSRC + "read_bwd.cuh", CSRC + "kernels_bwd.cu", CSRC + "depth_read_mma.cuh", CSRC + "kernels_mma.cu",
+                 CSRC + "read_bwd_one.cuh", CSRC + "read_bwd_many.cuh", CSRC + "read_bwd_split.cuh",
+                 CSRC + "kernels_bwd_split.cu"],
+    "read_bwd_one": [CSRC + "read_bwd_one.cuh", CSRC + "read_bwd_many.cuh", CSRC + "read_bwd_split.cuh",
+                     CSRC + "depth_read_mma.cuh", CSRC + "read_bwd.cuh", CSRC + "common.cuh",
+                     CSRC + "kernels_bwd_split.cu", CSRC + "kernels_bwd.cu"],
 }
 
 

@@ -73,9 +73,6 @@ __device__ __forceinline__ uint2 ldg64(const void *p) {
     asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
-__device__ __forceinline__ void stg32_cs(void *p, uint32_t v) {
-    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // A lane's CPL channels (4: one 8-byte piece, 2: one 4-byte piece) of a
 // stage row as floats, and back.
