@@ -618,14 +618,14 @@ attnres_status_t read_bwd_split_shape(int64_t T, int64_t d, int64_t H, const Dev
 }
 
 // The one-kernel ring form (read_bwd_one.cuh) takes a pass of one query over
-// 3 to 8 bf16 sources at d = 2048 or 4096 whose rows can be bulk-copied
+// 3 to 16 bf16 sources at d = 2048 or 4096 whose rows can be bulk-copied
 // (measured at T = 32768, d = 4096: 0.54 vs 0.55 ms at 3 sources, 0.80 vs
 // 1.02 ms at 8; debug kernel variant 1 keeps read_bwd_kernel).  Its
 // workspace, one partial of U per CTA, is within read_bwd_ws_bytes.
 bool read_bwd_one_applies(attnres_dtype_t dt, int64_t n_src, int64_t nq, int64_t d, int64_t H, const void *src,
                           int64_t src_stride) {
     if (g_kernel_variant.load() == 1) return false;
-    return dt == ATTNRES_BF16 && n_src >= 3 && n_src <= 8 && nq == 1 && H == 1 && (d == 2048 || d == 4096) &&
+    return dt == ATTNRES_BF16 && n_src >= 3 && n_src <= 16 && nq == 1 && H == 1 && (d == 2048 || d == 4096) &&
            aligned16(src) && (src_stride * 2) % 16 == 0;
 }
 
@@ -633,17 +633,21 @@ bool read_bwd_one_applies(attnres_dtype_t dt, int64_t n_src, int64_t nq, int64_t
 // partial per CTA at the start of the workspace (*nparts of them).
 attnres_status_t launch_read_bwd_one_pass(const ReadBwdArgs &a, const DeviceInfo *dev, void *stream, int *nparts) {
     KernelRef kr;
-    if (!lookup_read_bwd_one(a.d, &kr)) return ATTNRES_ERR_UNSUPPORTED;
+    if (!lookup_read_bwd_one(a.d, a.n_src, &kr)) return ATTNRES_ERR_UNSUPPORTED;
     ReadBwdOneArgs o;
     o.pitch = (uint32_t)a.d + 16;
-    o.stage_bytes = (uint32_t)R1_ROWS * o.pitch;
+    // up to 8 sources: 8 source rows and the gradient row, two tokens' stages
+    // held at a time; more: the n_src source rows and the gradient row, one
+    // token's stages held
+    const bool pipelined = a.n_src <= 8;
+    o.stage_bytes = (uint32_t)(pipelined ? R1_ROWS : a.n_src + 1) * o.pitch;
     size_t budget = kSmemBudget;
     if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
-    if (budget <= R1_AUX_BYTES) return ATTNRES_ERR_UNSUPPORTED;
-    int ns = (int)((budget - R1_AUX_BYTES) / o.stage_bytes);
+    if (budget <= kr.aux_smem) return ATTNRES_ERR_UNSUPPORTED;
+    int ns = (int)((budget - kr.aux_smem) / o.stage_bytes);
     if (ns > R1_MAX_STAGES) ns = R1_MAX_STAGES;
-    if (ns < 4) return ATTNRES_ERR_UNSUPPORTED;     // two tokens' stages are held at a time
-    const size_t smem = (size_t)ns * o.stage_bytes + R1_AUX_BYTES;
+    if (ns < (pipelined ? 4 : 3)) return ATTNRES_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)ns * o.stage_bytes + kr.aux_smem;
     int occ = 0;
     attnres_status_t st = prepare_kernel(kr.fn, smem, R1_NW * 32, &occ);
     if (st != ATTNRES_OK) return st;

@@ -45,8 +45,9 @@ const void *read_bwd_finish_fn();
 bool lookup_read_bwd_split(int nq, int d, KernelRef *coef, KernelRef *apply);
 // its form for one query over 17..64 sources (read_bwd_many.cuh)
 bool lookup_read_bwd_many(int d, KernelRef *coef, KernelRef *apply);
-// One query over at most 8 bf16 sources in one kernel, d = 2048 or 4096.
-bool lookup_read_bwd_one(int d, KernelRef *kr);
+// One query over at most 16 bf16 sources in one kernel, d = 2048 or 4096
+// (the pipelined kernel up to 8 sources, the one-barrier kernel above).
+bool lookup_read_bwd_one(int d, int n_src, KernelRef *kr);
 
 // phase2_merge_kernel<T, vpt, upd, mh>: upd = fused partial-sum update, mh = per-head merge
 bool lookup_phase2(int dt, int vpt, bool upd, bool mh, KernelRef *out);

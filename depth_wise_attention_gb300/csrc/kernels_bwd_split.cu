@@ -1,7 +1,7 @@
 // Instantiations of the two-kernel read backward: 3 or 4 queries
 // (read_bwd_split.cuh; 4 k-steps per warp and half row at d = 2048, 8 at
 // 4096), one query over 17..64 sources (read_bwd_many.cuh), and one query
-// over at most 8 sources in one kernel (read_bwd_one.cuh).
+// over 3..16 sources in one kernel (read_bwd_one.cuh).
 #include "dispatch.h"
 #include "read_bwd_split.cuh"
 #include "read_bwd_many.cuh"
@@ -38,13 +38,18 @@ bool lookup_read_bwd_many(int d, KernelRef *coef, KernelRef *apply) {
     return true;
 }
 
-bool lookup_read_bwd_one(int d, KernelRef *kr) {
+bool lookup_read_bwd_one(int d, int n_src, KernelRef *kr) {
     const void *f = nullptr;
-    if (d == 2048) f = reinterpret_cast<const void *>(&read_bwd_one_kernel<2>);
-    if (d == 4096) f = reinterpret_cast<const void *>(&read_bwd_one_kernel<4>);
+    if (n_src <= 8) {
+        if (d == 2048) f = reinterpret_cast<const void *>(&read_bwd_one_kernel<2>);
+        if (d == 4096) f = reinterpret_cast<const void *>(&read_bwd_one_kernel<4>);
+    } else {
+        if (d == 2048) f = reinterpret_cast<const void *>(&read_bwd_one16_kernel<4>);
+        if (d == 4096) f = reinterpret_cast<const void *>(&read_bwd_one16_kernel<8>);
+    }
     if (!f) return false;
     kr->fn = f;
-    kr->aux_smem = R1_AUX_BYTES;
+    kr->aux_smem = n_src <= 8 ? R1_AUX_BYTES : R16_AUX_BYTES;
     return true;
 }
 

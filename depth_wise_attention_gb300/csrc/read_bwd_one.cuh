@@ -1,6 +1,7 @@
 // read_bwd_one.cuh -- the backward of the depth read for one query over 3 to
-// 8 bf16 sources, in one kernel (sm_103a): the per-stream read backward of
-// MSAR, the shallow layers of Full AttnRes, a single-query read.
+// 16 bf16 sources, in one kernel (sm_103a): the per-stream read backward of
+// MSAR, a Block layer's read (the block representations and the partial
+// sum), the shallow layers of Full AttnRes.
 //
 // Same operation as read_bwd.cuh with n_q = 1 (per token, alpha recomputed
 // from the sources, r_i = sqrt(mean(v_i^2) + eps)):
@@ -359,6 +360,284 @@ __global__ void __launch_bounds__(R1_NW * 32, 1) read_bwd_one_kernel(const ReadB
     }
 
     // this CTA's U: one partial per CTA
+    if (!*abort_flag) {
+        float *wrow = a.ws + (size_t)blockIdx.x * a.d;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float *p = wrow + h * (a.d / 2) + warp * CWH + CPL * lane;
+            if constexpr (CPL == 4)
+                *reinterpret_cast<float4 *>(p) = make_float4(U[h][0].x, U[h][0].y, U[h][1].x, U[h][1].y);
+            else
+                *reinterpret_cast<float2 *>(p) = U[h][0];
+        }
+    }
+    // copies still in flight (only after an abort) must land before the CTA exits
+    __syncthreads();
+    if (tid == 0) {
+        int never = 0;
+        const int issued = (int)*imax;
+        for (int k = issued > a.nstages ? issued - a.nstages : 0; k < issued; ++k)
+            mbar_wait_bounded(&full[k % a.nstages], (uint32_t)(k / a.nstages) & 1u, &never, a.wait);
+    }
+}
+
+
+// 9 to 16 sources (a Block layer's read in training: the N block
+// representations and the partial sum): the same per-token work with the
+// sources as the 16 rows of one k-step (one MMA per 16 channels for the two
+// row dots, two for the Gram diagonal), stages of the n_src source rows and
+// the gradient row, and the simpler schedule of one CTA barrier per token
+// with every warp forming the coefficients (lanes i = 0..15): holding two
+// tokens' stages, as the pipelined schedule above does, would leave too few
+// in flight at these row counts.
+constexpr int R16_RS = 20;            // table row stride in floats (16 warps + pad, float4-aligned)
+constexpr size_t R16_AUX_BYTES = 256 + (size_t)2 * 48 * R16_RS * 4;
+
+// KS: MMA k-steps (16 channels) per warp and half row: d / (2 * 16 * R1_NW).
+template <int KS>
+__global__ void __launch_bounds__(R1_NW * 32, 1) read_bwd_one16_kernel(const ReadBwdOneArgs a) {
+    constexpr int NW = R1_NW;
+    constexpr int CWH = KS * 16;                  // channels per warp and half row
+    constexpr int CPL = CWH / 32;                 // channels per lane in the gradient pass
+    constexpr int NP = CPL / 2;
+    constexpr int RS = R16_RS;
+    static_assert(CPL == 2 || CPL == 4, "d = 2048 or 4096");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.nstages * a.stage_bytes);
+    unsigned *done = reinterpret_cast<unsigned *>(full + R1_MAX_STAGES);   // warps done with a stage
+    unsigned *imax = done + R1_MAX_STAGES;                                 // halves issued so far
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(imax + 1);
+    float *red = reinterpret_cast<float *>(smem + (size_t)a.nstages * a.stage_bytes + 256);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int half_bytes = a.d;                   // d/2 bf16 channels
+    const int ns = a.n_src;                       // the gradient row follows the sources
+
+    if (tid == 0) {
+        for (int s = 0; s < a.nstages; ++s) {
+            mbar_init(&full[s], 1);
+            done[s] = 0;
+        }
+        *imax = 0;
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    for (int b = tid * 16; b < a.nstages * (int)a.stage_bytes; b += NW * 32 * 16)
+        *reinterpret_cast<uint4 *>(stages + b) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    const int gstride = gridDim.x;
+    const int n_items = blockIdx.x < a.T ? (int)((a.T - blockIdx.x + gstride - 1) / gstride) : 0;
+    const int n_halves = 2 * n_items;
+
+    // half k (token item k/2, channel half k%2) into stage k % nstages by a
+    // whole warp: lane 0 arms the barrier, lane i < n_src copies source row
+    // i, lane n_src the gradient row; with accumulate the half rows of dsrc
+    // go to L2 as well.  The first nstages by warp 0, each later one by the
+    // warp that finishes the half nstages before it last.
+    const bool may_issue = !a.wait.inject_stall;
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue = [&](int k, int s) {               // s = k % nstages
+        const int64_t t = blockIdx.x + (int64_t)(k >> 1) * gstride;
+        const int64_t off = (t * a.d + (int64_t)(k & 1) * (a.d / 2)) * 2;
+        unsigned char *dst = stages + (size_t)s * a.stage_bytes;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)half_bytes * (uint32_t)(ns + 1));
+            atomicMax(imax, (unsigned)(k + 1));
+        }
+        __syncwarp();
+        if (lane < ns)
+            bulk_g2s(dst + (size_t)lane * a.pitch, a.src + (int64_t)lane * a.src_stride_bytes + off,
+                     (uint32_t)half_bytes, &full[s], pol);
+        else if (lane == ns)
+            bulk_g2s(dst + (size_t)ns * a.pitch, a.dout + off, (uint32_t)half_bytes, &full[s], pol);
+        if (a.accumulate && lane < ns)
+            bulk_prefetch_l2(a.dsrc + (int64_t)lane * a.dsrc_stride_bytes + off, (uint32_t)half_bytes);
+    };
+    if (warp == 0 && may_issue)
+        for (int k = 0; k < n_halves && k < a.nstages; ++k) issue(k, k);
+
+    // ------------------------------------------------------------ constants
+    // B fragments: column 0 the query's bf16 hi part, 1 its lo part, 2 the
+    // gradient row (read at run time), 3..7 zero
+    uint32_t bq[2][KS][2];
+    {
+        DepthReadMmaArgs m;
+        m.queries = a.query;
+        m.gain = a.gain;
+        m.d = a.d;
+        m.n_q = 1;
+        dm_query_fragments<KS>(m, warp * CWH, g4, t4, bq[0]);
+        dm_query_fragments<KS>(m, a.d / 2 + warp * CWH, g4, t4, bq[1]);
+    }
+    // ldmatrix rows: lanes 0..7 / 8..15 give rows 0..7 / 8..15 of the first 8
+    // channels of a k-step, lanes 16..31 the same rows 8 channels on; rows of
+    // absent sources read row 0 (their outputs are never used)
+    const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
+    const uint32_t lrow_x = (uint32_t)(lr < ns ? lr : 0) * a.pitch + (uint32_t)(warp * CWH + 8 * (lane >> 4)) * 2;
+    const bool dlane = g4 == 2;
+    const uint32_t drow = (uint32_t)ns * a.pitch + (uint32_t)(warp * CWH + 2 * t4) * 2;
+    const uint32_t bcol = (uint32_t)(warp * CWH + CPL * lane) * 2;
+    float2 wg[2][NP], U[2][NP];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int c = h * (a.d / 2) + warp * CWH + CPL * lane + 2 * p;
+            float2 w = make_float2(__ldg(a.query + c), __ldg(a.query + c + 1));
+            if (a.gain) { w.x *= __ldg(a.gain + c); w.y *= __ldg(a.gain + c + 1); }
+            wg[h][p] = w;
+            U[h][p] = make_float2(0.f, 0.f);
+        }
+    const uint32_t stage0 = smem_u32(stages);
+    const int i16 = lane & 15;                    // the source of this lane's softmax values
+
+    float d1[2][4], g0[4], g1[4];
+    int s = 0;                                    // stage of the next half, and its phase parity
+    uint32_t par = 0;
+    for (int it = 0; it < n_items; ++it) {
+        const int64_t t = blockIdx.x + (int64_t)it * gstride;
+        const float dl = a.dlse != nullptr ? __ldg(a.dlse + t) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { d1[0][e] = 0.f; d1[1][e] = 0.f; g0[e] = 0.f; g1[e] = 0.f; }
+        int sh[2];
+        // ---------------- the row sums over both halves
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mbar_wait_bounded(&full[s], par, abort_flag, a.wait);
+            const uint32_t sb = stage0 + (uint32_t)s * a.stage_bytes;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t x0, x1, x2, x3;           // rows 0..7 / 8..15 of channels 0..7, then 8..15
+                ldsm_x4(sb + lrow_x + 32 * ks, x0, x1, x2, x3);
+                uint32_t b0 = bq[h][ks][0], b1 = bq[h][ks][1];
+                if (dlane) {
+                    b0 = lds32u(sb + drow + 32 * ks);
+                    b1 = lds32u(sb + drow + 32 * ks + 16);
+                }
+                mma_full(d1[ks & 1], x0, x1, x2, x3, b0, b1);
+                mma_full(g0, x0, x1, x2, x3, x0, x2);   // B = sources 0..7: the diagonal of rows 0..7
+                mma_full(g1, x0, x1, x2, x3, x1, x3);   // B = sources 8..15: the diagonal of rows 8..15
+            }
+            sh[h] = s;
+            if (++s == a.nstages) { s = 0; par ^= 1u; }
+        }
+        // lane (i, 0): (w*g).v of sources i and i+8 (columns 0 + 1); lane (i, 1):
+        // dout.v of sources i and i+8 (column 2); lane (i, i/2): v.v of source
+        // i (rows 0..7 against sources 0..7) and i+8 (rows 8..15 against 8..15)
+        {
+            float *rb = red + (size_t)(it & 1) * 48 * RS;
+            const float e0 = d1[0][0] + d1[1][0], e1 = d1[0][1] + d1[1][1];
+            const float e2 = d1[0][2] + d1[1][2], e3 = d1[0][3] + d1[1][3];
+            if (t4 == 0) {
+                rb[g4 * RS + warp] = e0 + e1;
+                rb[(8 + g4) * RS + warp] = e2 + e3;
+            } else if (t4 == 1) {
+                rb[(16 + g4) * RS + warp] = e0;
+                rb[(24 + g4) * RS + warp] = e2;
+            }
+            if (t4 == (g4 >> 1)) {
+                rb[(32 + g4) * RS + warp] = (g4 & 1) ? g0[1] : g0[0];
+                rb[(40 + g4) * RS + warp] = (g4 & 1) ? g1[3] : g1[2];
+            }
+        }
+        // the table of token it is complete; the one of token it-1 (the other
+        // buffer) was read by every warp before it arrived here
+        __syncthreads();
+
+        // ---------------- coefficients (every warp, lanes i = lane % 16)
+        float alpha, bco, cco;
+        {
+            const float *rb = red + (size_t)(it & 1) * 48 * RS;
+            const float *pw = rb + i16 * RS, *pd = rb + (16 + i16) * RS, *ps = rb + (32 + i16) * RS;
+            float sw = 0.f, sd = 0.f, ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; w += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(ps + w);
+                const float4 y = *reinterpret_cast<const float4 *>(pw + w);
+                const float4 z = *reinterpret_cast<const float4 *>(pd + w);
+                ss += (x.x + x.y) + (x.z + x.w);
+                sw += (y.x + y.y) + (y.z + y.w);
+                sd += (z.x + z.y) + (z.z + z.w);
+            }
+            const bool pv = i16 < ns;
+            const float ms = fmaf(ss, a.inv_d, a.eps);
+            const float rinv = ms > 0.f ? rsqrtf(ms) : 0.f;      // 1 / r_i (0 for a zero key)
+            const float score = pv ? sw * rinv : -INFINITY;
+            const float mx = seg_max<16>(score);
+            const float e = pv ? __expf(score - mx) : 0.f;
+            const float es = seg_sum<16>(e);
+            alpha = pv ? e / es : 0.f;
+            const float mean = seg_sum<16>(pv ? alpha * sd : 0.f);
+            const float ds = pv ? alpha * (sd - mean + dl) : 0.f;
+            bco = ds * rinv;
+            cco = pv ? -ds * sw * rinv * rinv * rinv * a.inv_d : 0.f;
+        }
+
+        // ---------------- dv and U from the same stages, half by half
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t sb = stage0 + (uint32_t)sh[h] * a.stage_bytes + bcol;
+            const int64_t goff = (t * a.d + (int64_t)h * (a.d / 2)) * 2 + (int64_t)bcol;
+            float2 dg[NP];
+            r1_load<CPL>(sb + (uint32_t)ns * a.pitch, dg);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i >= ns) break;
+                const float al = __shfl_sync(0xffffffffu, alpha, i);
+                const float bi = __shfl_sync(0xffffffffu, bco, i);
+                const float ci = __shfl_sync(0xffffffffu, cco, i);
+                unsigned char *gp = a.dsrc + (int64_t)i * a.dsrc_stride_bytes + goff;
+                uint2 zr = make_uint2(0u, 0u);
+                if (a.accumulate) {
+                    if constexpr (CPL == 4) zr = ldg64(gp);
+                    else zr.x = *reinterpret_cast<const uint32_t *>(gp);
+                }
+                float2 x[NP], y[NP];
+                r1_load<CPL>(sb + (uint32_t)i * a.pitch, x);
+#pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    y[p] = fmul2(make_float2(ci, ci), x[p]);
+                    y[p] = ffma2(make_float2(al, al), dg[p], y[p]);
+                    y[p] = ffma2(make_float2(bi, bi), wg[h][p], y[p]);
+                    U[h][p] = ffma2(make_float2(bi, bi), x[p], U[h][p]);
+                }
+                if (a.accumulate) {
+                    const float2 z0 = bf2_to_f2(zr.x);
+                    y[0] = make_float2(y[0].x + z0.x, y[0].y + z0.y);
+                    if constexpr (CPL == 4) {
+                        const float2 z1 = bf2_to_f2(zr.y);
+                        y[1] = make_float2(y[1].x + z1.x, y[1].y + z1.y);
+                    }
+                }
+                if (!*abort_flag) {
+                    if constexpr (CPL == 4)
+                        stg64_cs(gp, make_uint2(f2_to_bf2(y[0].x, y[0].y), f2_to_bf2(y[1].x, y[1].y)));
+                    else
+                        stg32_cs(gp, f2_to_bf2(y[0].x, y[0].y));
+                }
+            }
+            // this warp is done with the stage; the last warp to be refills it
+            __syncwarp();
+            const int k = 2 * it + h;
+            int refill = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                if (atomicAdd(&done[sh[h]], 1u) == NW - 1) {
+                    done[sh[h]] = 0;
+                    refill = k + a.nstages < n_halves && may_issue && !*abort_flag;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, refill, 0)) issue(k + a.nstages, sh[h]);
+            __syncwarp();
+        }
+    }
+
     if (!*abort_flag) {
         float *wrow = a.ws + (size_t)blockIdx.x * a.d;
 #pragma unroll

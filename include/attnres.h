@@ -242,7 +242,7 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  * reads the sources and dout twice and rounds a bf16 dsrc once.  Other
  * passes of 3 or 4 queries run two groups of two in one kernel, the second
  * group adding into the bf16 dsrc the first has rounded.  A pass of one query
- * over 3 to 8 bf16 sources at d = 2048 or 4096 (src and src_stride 16-byte
+ * over 3 to 16 bf16 sources at d = 2048 or 4096 (src and src_stride 16-byte
  * aligned) reads them once through a ring of half-row stages, one CTA per
  * SM, with one partial of the sums over the tokens per CTA.
  * More than 16 sources (Full AttnRes past layer 16): with one query, bf16,
@@ -259,8 +259,9 @@ attnres_status_t mhar_phase2_merge(const void *o, const float *lse, const void *
  * the query and gain gradients carry that rounding; the workspace then also
  * holds the states (about 2 ceil(n_src/8) n_q T d elements of dt).
  * Limits: at most 256 sources (32 chunks) and, above 16 sources, 8 queries;
- * up to 16 sources, the n_src + (queries of a pass) rows of a token tile must
- * fit two shared-memory stages (for d = 4096 bf16, n_src + 2 <= 13).
+ * up to 16 sources, outside the ring form, the n_src + (queries of a pass)
+ * rows of a token tile must fit two shared-memory stages (for d = 4096 bf16,
+ * n_src + 2 <= 13).
  */
 attnres_status_t attnres_read_bwd(const void *src, int64_t n_src, int64_t src_stride, int64_t T,
                                   int64_t d, attnres_dtype_t dt, const float *queries, int64_t n_q,

@@ -679,9 +679,9 @@ def test_read_bwd_two_kernel_form_is_deterministic_accumulates_and_agrees_with_o
 
 @pytest.fixture(params=[0, 1], ids=["ring", "whole-token"])
 def one_variant(request):
-    """Kernel variant 0 runs the read backward of one query over 3 to 8 bf16
-    sources (d = 2048 or 4096) in the ring of half-row stages; variant 1 keeps
-    the kernel with whole-token stages."""
+    """Kernel variant 0 runs the read backward of one query over 3 to 16 bf16
+    sources (d = 2048 or 4096) through a ring of half-row stages; variant 1
+    keeps the kernel with whole-token stages."""
     attnres.attnres_debug_set_kernel_variant(request.param)
     yield request.param
     attnres.attnres_debug_set_kernel_variant(0)
@@ -693,9 +693,15 @@ def one_variant(request):
     (3, 151, 2048, False, True),     # fewer tokens than SMs
     (3, 1, 4096, True, False),       # one token (one CTA, one step of the pipeline)
     (5, 1000, 2048, True, False),    # several tokens per CTA, ragged ring
-    (7, 9, 4096, False, False)])
+    (7, 9, 4096, False, False),
+    (9, 300, 4096, True, False),     # a Block layer's read: 8 block representations and the partial
+    (9, 300, 4096, True, True),
+    (12, 151, 2048, False, True),
+    (16, 700, 4096, True, False),    # three stages
+    (13, 1, 4096, True, False),
+    (11, 1000, 2048, True, False)])
 def test_read_bwd_one_query_both_forms(one_variant, n_src, T, d, with_gain, with_lse):
-    """The read backward of one query over 3 to 8 sources under both kernel
+    """The read backward of one query over 3 to 16 sources under both kernel
     forms against the oracle's chain rule (with Block phase 1's lse gradient
     where given)."""
     rng = _rng(n_src * 17 + T + d + 3 * with_lse)
@@ -705,6 +711,12 @@ def test_read_bwd_one_query_both_forms(one_variant, n_src, T, d, with_gain, with
     dout = _sources(rng, 1, T, d, BF16, step=0)
     sd, qd, od = to_dev(src, BF16), to_dev(q, F32), to_dev(dout, BF16)
     gd = to_dev(g, F32) if with_gain else None
+    if one_variant == 1 and d == 4096 and n_src > 12:
+        # the whole-token kernel's two stages hold at most 13 rows at d = 4096
+        # (the sources and the gradient row): only the ring form takes more
+        with pytest.raises(attnres.AttnResError):
+            attnres.attnres_read_bwd(sd, qd, od, gd, 1e-6)
+        return
     if with_lse:
         dl = rng.standard_normal((1, T)).astype(np.float32)
         got = attnres.attnres_block_phase1_bwd(sd, qd, od, to_dev(dl, F32), gd, 1e-6)
@@ -728,12 +740,13 @@ def test_read_bwd_one_query_both_forms(one_variant, n_src, T, d, with_gain, with
                 check_out(g_, r_, BF16, what=name)
 
 
-def test_read_bwd_one_query_ring_is_deterministic_accumulates_and_agrees_with_whole_token_form():
+@pytest.mark.parametrize("n_src", [8, 9])
+def test_read_bwd_one_query_ring_is_deterministic_accumulates_and_agrees_with_whole_token_form(n_src):
     """Two runs of the ring form agree bitwise; with accumulate it adds into
     the given source gradients; and it agrees with the whole-token form within
     the bf16 bar (both round dsrc once; their sums run in different orders)."""
-    rng = _rng(59)
-    n_src, T, d = 8, 700, 4096
+    rng = _rng(59 + n_src)
+    T, d = 700, 4096
     src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.25), BF16)
     q = to_dev(_queries(rng, 1, d), F32)
     dout = to_dev(_sources(rng, 1, T, d, BF16, step=0), BF16)
