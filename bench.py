@@ -57,10 +57,10 @@ KERNEL_SOURCES = {
     "msar_bwd": [CSRC + "msar_bwd.cu", CSRC + "msar_bwd.h", CSRC + "msar.h", CSRC + "common.cuh",
                  CSRC + "read_bwd.cuh", CSRC + "kernels_bwd.cu", CSRC + "depth_read_mma.cuh", CSRC + "kernels_mma.cu",
                  CSRC + "read_bwd_one.cuh", CSRC + "read_bwd_many.cuh", CSRC + "read_bwd_split.cuh",
-                 CSRC + "kernels_bwd_split.cu"],
+                 CSRC + "kernels_bwd_one.cu"],
     "read_bwd_one": [CSRC + "read_bwd_one.cuh", CSRC + "read_bwd_many.cuh", CSRC + "read_bwd_split.cuh",
                      CSRC + "depth_read_mma.cuh", CSRC + "read_bwd.cuh", CSRC + "common.cuh",
-                     CSRC + "kernels_bwd_split.cu", CSRC + "kernels_bwd.cu"],
+                     CSRC + "kernels_bwd_one.cu", CSRC + "kernels_bwd.cu"],
 }
 
 
@@ -364,7 +364,8 @@ class ReadBwdWorkload(BlockWorkload):
     """Backward of one Block layer's read in training: the layer's query over
     its 9 sources (the N=8 block reps and the partial sum), bf16, d=4096: the
     sources', the query's and the gain's gradients for a given output
-    gradient.  Sources as the Block workload; output gradient ~ N(0, 1)."""
+    gradient, in one kernel through a ring of half-row stages.  Sources as the
+    Block workload; output gradient ~ N(0, 1)."""
 
     def __init__(self, T=32768, d=4096, N=8, seed=0):
         super().__init__(T, d, N, 4, seed, name="attnres_read_backward")
@@ -374,8 +375,8 @@ class ReadBwdWorkload(BlockWorkload):
         self.bytes_per_token = (2 * n_src + 1) * d * b
         self.phase1_bytes_per_token = self.bytes_per_token
         self.launches_per_step = 2            # streaming kernel + the workspace reduction
-        self.dominant = "read_bwd_kernel"
-        self.dominant_src = "read_bwd"
+        self.dominant = "read_bwd_one16_kernel (one query through a ring of half-row stages)"
+        self.dominant_src = "read_bwd_one"
         self.profile_tag = f"ncu_read_bwd_d{d}"
 
     def config(self):

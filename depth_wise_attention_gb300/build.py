@@ -28,6 +28,7 @@ SOURCES = [
     "kernels_phase2_mh.cu",
     "kernels_mma.cu",
     "kernels_bwd_split.cu",
+    "kernels_bwd_one.cu",
     "kernels_mma_multi.cu",
     "kernels_bwd.cu",
     "kernels_bwd_mh.cu",

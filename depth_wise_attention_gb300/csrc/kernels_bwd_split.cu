@@ -1,11 +1,9 @@
 // Instantiations of the two-kernel read backward: 3 or 4 queries
 // (read_bwd_split.cuh; 4 k-steps per warp and half row at d = 2048, 8 at
-// 4096), one query over 17..64 sources (read_bwd_many.cuh), and one query
-// over 3..16 sources in one kernel (read_bwd_one.cuh).
+// 4096), and one query over 17..64 sources (read_bwd_many.cuh).
 #include "dispatch.h"
 #include "read_bwd_split.cuh"
 #include "read_bwd_many.cuh"
-#include "read_bwd_one.cuh"
 
 namespace attnres {
 
@@ -35,21 +33,6 @@ bool lookup_read_bwd_many(int d, KernelRef *coef, KernelRef *apply) {
     coef->aux_smem = RM_AUX_BYTES;
     apply->fn = reinterpret_cast<const void *>(&read_bwd_apply_many_kernel<1>);
     apply->aux_smem = 0;
-    return true;
-}
-
-bool lookup_read_bwd_one(int d, int n_src, KernelRef *kr) {
-    const void *f = nullptr;
-    if (n_src <= 8) {
-        if (d == 2048) f = reinterpret_cast<const void *>(&read_bwd_one_kernel<2>);
-        if (d == 4096) f = reinterpret_cast<const void *>(&read_bwd_one_kernel<4>);
-    } else {
-        if (d == 2048) f = reinterpret_cast<const void *>(&read_bwd_one16_kernel<4>);
-        if (d == 4096) f = reinterpret_cast<const void *>(&read_bwd_one16_kernel<8>);
-    }
-    if (!f) return false;
-    kr->fn = f;
-    kr->aux_smem = n_src <= 8 ? R1_AUX_BYTES : R16_AUX_BYTES;
     return true;
 }
 

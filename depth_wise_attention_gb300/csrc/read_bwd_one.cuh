@@ -69,6 +69,9 @@ struct ReadBwdOneArgs {
     WaitCfg wait;
 };
 
+__device__ __forceinline__ void stg32_cs(void *p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint2 ldg64(const void *p) {
     uint2 v;
     asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));

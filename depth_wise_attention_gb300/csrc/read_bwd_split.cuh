@@ -402,9 +402,6 @@ __device__ __forceinline__ uint2 ldg64_nc(const void *p) {
 __device__ __forceinline__ void stg64_cs(void *p, uint2 v) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
-__device__ __forceinline__ void stg32_cs(void *p, uint32_t v) {
-    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ void cp_async8(uint32_t dst_smem, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst_smem), "l"(src) : "memory");
