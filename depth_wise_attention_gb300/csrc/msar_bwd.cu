@@ -72,6 +72,14 @@ template <int KA, int KB, int KC> struct ConvShape {
     __host__ __device__ static constexpr int off(int r) { return r == 0 ? 0 : r == 1 ? K0 : K0 + K1; }
 };
 
+// lcm(rb, km) / rb: stages after which a window of km slots, advanced one
+// slot per step, is back at its first slot
+__host__ __device__ constexpr int ring_group(int rb, int km) {
+    int g = 1;
+    while ((g * rb) % km != 0) ++g;
+    return g;
+}
+
 // ---------------------------------------------------------------- step 1
 // CTA = (slice of ST_CB channels, source i, chunk of tc_s tokens); a thread
 // owns two adjacent channels with their three kernels in registers and a
@@ -133,7 +141,11 @@ __global__ void __launch_bounds__(ST_THREADS) msar_streams_kernel(const MsarBwdA
 #pragma unroll
     for (int b = 0; b < ST_NS - 1; ++b) issue(b);
 
-    float2 win[CS::KM];              // win[j] = v[row - j]
+    // win is a ring: v[row - j] at step q (row = t0 - H + q) sits in slot
+    // (q - j) % KM.  Steps are taken in groups of lcm(ST_RB, KM), so every slot
+    // index is a compile-time constant (no window shifts).
+    constexpr int G = ring_group(ST_RB, CS::KM);
+    float2 win[CS::KM];
 #pragma unroll
     for (int j = 0; j < CS::KM; ++j) win[j] = make_float2(0.f, 0.f);
     // output pointers of the three streams at token t0, one row apart per step
@@ -141,30 +153,35 @@ __global__ void __launch_bounds__(ST_THREADS) msar_streams_kernel(const MsarBwdA
     unsigned char *up[3];
 #pragma unroll
     for (int r = 0; r < 3; ++r) up[r] = a.u + (((int64_t)r * a.n_src + i) * a.T + t0) * rowb + (int64_t)c * ES;
-    for (int b = 0; b < nb; ++b) {
-        cp_async_wait<ST_NS - 2>();
-        __syncthreads();
-        issue(b + ST_NS - 1);
-        const unsigned char *stage = smem + (b % ST_NS) * ST_RB * ROWB + 2 * tid * ES;
+    for (int b0 = 0; b0 < nb; b0 += G) {
 #pragma unroll
-        for (int rr = 0; rr < ST_RB; ++rr) {
-            const int64_t row = t0 - H + (int64_t)b * ST_RB + rr;
+        for (int gs = 0; gs < G; ++gs) {
+            const int b = b0 + gs;
+            if (b >= nb) break;
+            cp_async_wait<ST_NS - 2>();
+            __syncthreads();
+            issue(b + ST_NS - 1);
+            const unsigned char *stage = smem + (b % ST_NS) * ST_RB * ROWB + 2 * tid * ES;
 #pragma unroll
-            for (int j = CS::KM - 1; j > 0; --j) win[j] = win[j - 1];
-            win[0] = P2::ld(stage + rr * ROWB);
-            if (row >= t0 && row < t1) {
+            for (int rr = 0; rr < ST_RB; ++rr) {
+                const int64_t row = t0 - H + (int64_t)b * ST_RB + rr;
+                const int ph = (gs * ST_RB + rr) % CS::KM;      // q % KM
+                win[ph] = P2::ld(stage + rr * ROWB);
+                if (row >= t0 && row < t1) {
 #pragma unroll
-                for (int r = 0; r < 3; ++r) {
-                    // even and odd taps in two independent chains
-                    float2 ae = make_float2(0.f, 0.f), ao = make_float2(0.f, 0.f);
+                    for (int r = 0; r < 3; ++r) {
+                        // even and odd taps in two independent chains
+                        float2 ae = make_float2(0.f, 0.f), ao = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < CS::k(r); ++j)
-                        if (CS::FIXED || j < a.k[r]) {
-                            if (j & 1) ao = ffma2(w[CS::off(r) + j], win[j], ao);
-                            else ae = ffma2(w[CS::off(r) + j], win[j], ae);
-                        }
-                    P2::st(up[r], make_float2(ae.x + ao.x, ae.y + ao.y));
-                    up[r] += rowb;
+                        for (int j = 0; j < CS::k(r); ++j)
+                            if (CS::FIXED || j < a.k[r]) {
+                                const float2 x = win[(ph - j + CS::KM) % CS::KM];
+                                if (j & 1) ao = ffma2(w[CS::off(r) + j], x, ao);
+                                else ae = ffma2(w[CS::off(r) + j], x, ae);
+                            }
+                        P2::st(up[r], make_float2(ae.x + ao.x, ae.y + ao.y));
+                        up[r] += rowb;
+                    }
                 }
             }
         }
