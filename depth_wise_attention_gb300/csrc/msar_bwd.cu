@@ -241,6 +241,35 @@ template <> __device__ __forceinline__ void store8<float>(unsigned char *p, cons
     *reinterpret_cast<float4 *>(p + 16) = make_float4(x[4], x[5], x[6], x[7]);
 }
 
+// 8 channels of one row as loaded (one 16-byte load for bf16, two for fp32),
+// widened later: lets a step's loads be issued before the step before it is
+// computed and stored.
+template <typename Tin> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const unsigned char *p) { u = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ void widen(float (&x)[8]) const {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = bf2_to_f2(w[e]);
+            x[2 * e] = f.x;
+            x[2 * e + 1] = f.y;
+        }
+    }
+};
+template <> struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const unsigned char *p) {
+        a = *reinterpret_cast<const float4 *>(p);
+        b = *reinterpret_cast<const float4 *>(p + 16);
+    }
+    __device__ __forceinline__ void widen(float (&x)[8]) const {
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+};
+
 // Per (token, slice): s[0] = sum zf^2, s[1+o] = sum g zf P[:, o], s[5+r] = dh . Z^(r)
 // over the slice's channels -> mix_part[t][slice][9].
 template <typename Tin>
@@ -256,18 +285,28 @@ __global__ void __launch_bounds__(MX_THREADS) msar_mix_stats_kernel(const MsarBw
         float s[9];
 #pragma unroll
         for (int q = 0; q < 9; ++q) s[q] = 0.f;
-#pragma unroll 1
+        // each 256-channel step's rows are loaded one step ahead (two steps in flight)
+        Raw8<Tin> rdh[2], rz[2][4];
+        auto fetch = [&](int it, int bf) {
+            const int cl = it * 256 + lane * 8;
+            if (a.dh) rdh[bf].load(a.dh + (t * a.d + c0 + cl) * ES);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) rz[bf][r].load(a.z + (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES);
+        };
+        fetch(0, 0);
+#pragma unroll
         for (int it = 0; it < MX_CS / 256; ++it) {
             const int cl = it * 256 + lane * 8;
+            if (it + 1 < MX_CS / 256) fetch(it + 1, (it + 1) & 1);
             float dh[8], z[4][8];
             if (a.dh) {
-                load8<Tin>(a.dh + (t * a.d + c0 + cl) * ES, dh);
+                rdh[it & 1].widen(dh);
             } else {                                    // the forward's mixer: no dh sums
 #pragma unroll
                 for (int e = 0; e < 8; ++e) dh[e] = 0.f;
             }
 #pragma unroll
-            for (int r = 0; r < 4; ++r) load8<Tin>(a.z + (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES, z[r]);
+            for (int r = 0; r < 4; ++r) rz[it & 1][r].widen(z[r]);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -360,16 +399,27 @@ __global__ void __launch_bounds__(MX_THREADS) msar_mix_dz_kernel(const MsarBwdAr
         const float k3 = s2 * inv * inv * inv * inv_md;
         if (sl == 0 && lane == 0)
             *reinterpret_cast<float4 *>(a.mix_e + t * 4) = make_float4(dl[0] * inv, dl[1] * inv, dl[2] * inv, dl[3] * inv);
-#pragma unroll 1
+        // each 256-channel step's rows are loaded one step ahead (two steps in
+        // flight; the loads of a step are issued before the stores of the one before)
+        Raw8<Tin> rdh[2], rz[2][4];
+        auto fetch = [&](int it, int bf) {
+            const int cl = it * 256 + lane * 8;
+            rdh[bf].load(a.dh + (t * a.d + c0 + cl) * ES);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) rz[bf][r].load(a.z + (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES);
+        };
+        fetch(0, 0);
+#pragma unroll
         for (int it = 0; it < MX_CS / 256; ++it) {
             const int cl = it * 256 + lane * 8;
+            if (it + 1 < MX_CS / 256) fetch(it + 1, (it + 1) & 1);
             float dh[8];
-            load8<Tin>(a.dh + (t * a.d + c0 + cl) * ES, dh);
+            rdh[it & 1].widen(dh);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int64_t off = (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES;
                 float z[8], y[8];
-                load8<Tin>(a.z + off, z);
+                rz[it & 1][r].widen(z);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float4 p = gp[gp_index(r, cl + e)];
@@ -384,11 +434,11 @@ __global__ void __launch_bounds__(MX_THREADS) msar_mix_dz_kernel(const MsarBwdAr
 
 // A[k][o] = sum_t zf_t[k] e_t[o] over a chunk of tokens: one thread per 8
 // adjacent elements k of the flattened m d vector (one 16-byte load per
-// token), four tokens' loads at a time; per-chunk partials in mix_parts.
+// token), eight tokens' loads at a time; per-chunk partials in mix_parts.
 template <typename Tin>
 __global__ void __launch_bounds__(256) msar_mix_acc_kernel(const MsarBwdArgs a) {
     constexpr int ES = sizeof(Tin);
-    constexpr int U = 4;
+    constexpr int U = 8;
     const int64_t md = 4 * (int64_t)a.d;
     const int64_t k8 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;   // elements k8 .. k8 + 7
     if (k8 >= md) return;
@@ -404,29 +454,34 @@ __global__ void __launch_bounds__(256) msar_mix_acc_kernel(const MsarBwdArgs a) 
 #pragma unroll
         for (int o = 0; o < 4; ++o) acc[e][o] = 0.f;
     for (int64_t t = t0; t < t1; t += U) {
-        float z[U][8];
+        Raw8<Tin> zraw[U];
         float4 ev[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool ok = t + u < t1;
             if (ok) {
-                load8<Tin>(zr + (t + u) * rowb, z[u]);
+                zraw[u].load(zr + (t + u) * rowb);
                 ev[u] = __ldg(reinterpret_cast<const float4 *>(a.mix_e) + (t + u));
             } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) z[u][e] = 0.f;
                 ev[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+        for (int u = 0; u < U; ++u) {
+            float z[8];
+            if (t + u < t1) zraw[u].widen(z);
+            else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) z[e] = 0.f;
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                acc[e][0] = fmaf(z[u][e], ev[u].x, acc[e][0]);
-                acc[e][1] = fmaf(z[u][e], ev[u].y, acc[e][1]);
-                acc[e][2] = fmaf(z[u][e], ev[u].z, acc[e][2]);
-                acc[e][3] = fmaf(z[u][e], ev[u].w, acc[e][3]);
+                acc[e][0] = fmaf(z[e], ev[u].x, acc[e][0]);
+                acc[e][1] = fmaf(z[e], ev[u].y, acc[e][1]);
+                acc[e][2] = fmaf(z[e], ev[u].z, acc[e][2]);
+                acc[e][3] = fmaf(z[e], ev[u].w, acc[e][3]);
             }
+        }
     }
     float4 *wp = reinterpret_cast<float4 *>(a.mix_parts + (size_t)blockIdx.y * (size_t)(md * 4)) + k8;
 #pragma unroll
