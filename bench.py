@@ -1236,6 +1236,7 @@ class MsarPerSourceWorkload(MsarWorkload):
         super().__init__(T, d, N, seed)
         self.name = "msar_per_source_kernels"
         self.dominant = "msar_kernel (per-source kernels)"
+        self.dominant_src = "msar"
         self.profile_tag = f"ncu_msar_per_source_d{d}"
 
     def setup(self, device):
