@@ -330,6 +330,85 @@ __global__ void __launch_bounds__(MX_THREADS) msar_mix_stats_kernel(const MsarBw
     }
 }
 
+// The forward's mixer sums, as msar_mix_stats_kernel without dh (s[5..8] = 0).
+// A warp takes two tokens at a time: every g*P value read from shared memory
+// (16 bytes per channel and stream, the kernel's largest traffic) serves both,
+// and their eight rows per 256-channel step are in flight together (measured
+// 0.27 ms faster per MSAR two-phase block through the chains; the backward's
+// kernels, with dh and dZ, lost more to the extra registers than they gained).
+template <typename Tin>
+__global__ void __launch_bounds__(MX_THREADS) msar_fwd_mix_stats_kernel(const MsarBwdArgs a) {
+    constexpr bool DH = false;
+    constexpr int ES = sizeof(Tin);
+    constexpr int NSTEP = MX_CS / 256;
+    constexpr int TPW = 2;
+    extern __shared__ __align__(16) float4 gp[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sl = blockIdx.x, c0 = sl * MX_CS;
+    stage_gp(a, gp, c0);
+    const int64_t t0 = (int64_t)blockIdx.y * a.tc_m;
+    const int64_t t1 = t0 + a.tc_m < a.T ? t0 + a.tc_m : a.T;
+    for (int64_t tb = t0 + (int64_t)warp * TPW; tb < t1; tb += (MX_THREADS / 32) * TPW) {
+        const int nt = t1 - tb < TPW ? (int)(t1 - tb) : TPW;
+        float s[TPW][9];
+#pragma unroll
+        for (int u = 0; u < TPW; ++u)
+#pragma unroll
+            for (int q = 0; q < 9; ++q) s[u][q] = 0.f;
+#pragma unroll
+        for (int it = 0; it < NSTEP; ++it) {
+            // (no later step's loads above this point: hoisting them spills)
+            asm volatile("" ::: "memory");
+            const int cl = it * 256 + lane * 8;
+            Raw8<Tin> rdh[TPW], rz[TPW][4];
+#pragma unroll
+            for (int u = 0; u < TPW; ++u) {
+                const int64_t t = tb + (u < nt ? u : 0);  // a missing second token rereads the first
+                if (DH) rdh[u].load(a.dh + (t * a.d + c0 + cl) * ES);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) rz[u][r].load(a.z + (((int64_t)r * a.T + t) * a.d + c0 + cl) * ES);
+            }
+            float dh[TPW][8];
+            if (DH) {
+#pragma unroll
+                for (int u = 0; u < TPW; ++u) rdh[u].widen(dh[u]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float z[TPW][8];
+#pragma unroll
+                for (int u = 0; u < TPW; ++u) rz[u][r].widen(z[u]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 p = gp[gp_index(r, cl + e)];
+#pragma unroll
+                    for (int u = 0; u < TPW; ++u) {
+                        s[u][0] = fmaf(z[u][e], z[u][e], s[u][0]);
+                        s[u][1] = fmaf(z[u][e], p.x, s[u][1]);
+                        s[u][2] = fmaf(z[u][e], p.y, s[u][2]);
+                        s[u][3] = fmaf(z[u][e], p.z, s[u][3]);
+                        s[u][4] = fmaf(z[u][e], p.w, s[u][4]);
+                        if (DH) s[u][5 + r] = fmaf(dh[u][e], z[u][e], s[u][5 + r]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < TPW; ++u)
+#pragma unroll
+            for (int q = 0; q < (DH ? 9 : 5); ++q) s[u][q] = seg_sum<32>(s[u][q]);
+        if (lane == 0) {
+#pragma unroll
+            for (int u = 0; u < TPW; ++u) {
+                if (u >= nt) break;
+                float *dst = a.mix_part + ((tb + u) * a.nsl + sl) * 9;
+#pragma unroll
+                for (int q = 0; q < 9; ++q) dst[q] = s[u][q];
+            }
+        }
+    }
+}
+
 // The forward's mixer output from the per-slice sums of token t (added in
 // slice order): h = sum_r c_r Z^(r) with c_r = sigmoid(s_r / nu).  A warp per
 // token, 8 channels per lane per 256-channel step.
@@ -771,9 +850,9 @@ static cudaError_t launch_mix_t(const MsarBwdArgs &a, cudaStream_t s) {
 template <typename Tin>
 static cudaError_t launch_fwd_mix_t(const MsarBwdArgs &a, unsigned char *out, cudaStream_t s) {
     const dim3 grid((unsigned)a.nsl, (unsigned)((a.T + a.tc_m - 1) / a.tc_m));
-    cudaError_t e = set_smem(msar_mix_stats_kernel<Tin>, MX_SMEM);
+    cudaError_t e = set_smem(msar_fwd_mix_stats_kernel<Tin>, MX_SMEM);
     if (e != cudaSuccess) return e;
-    msar_mix_stats_kernel<Tin><<<grid, MX_THREADS, MX_SMEM, s>>>(a);
+    msar_fwd_mix_stats_kernel<Tin><<<grid, MX_THREADS, MX_SMEM, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     msar_mix_out_kernel<Tin><<<(unsigned)((a.T + 7) / 8), 256, 0, s>>>(a, out);
