@@ -699,7 +699,8 @@ def one_variant(request):
     (12, 151, 2048, False, True),
     (16, 700, 4096, True, False),    # three stages
     (13, 1, 4096, True, False),
-    (11, 1000, 2048, True, False)])
+    (11, 1000, 2048, True, False),
+    (16, 300, 2048, False, True)])
 def test_read_bwd_one_query_both_forms(one_variant, n_src, T, d, with_gain, with_lse):
     """The read backward of one query over 3 to 16 sources under both kernel
     forms against the oracle's chain rule (with Block phase 1's lse gradient
@@ -740,13 +741,14 @@ def test_read_bwd_one_query_both_forms(one_variant, n_src, T, d, with_gain, with
                 check_out(g_, r_, BF16, what=name)
 
 
-@pytest.mark.parametrize("n_src", [8, 9])
-def test_read_bwd_one_query_ring_is_deterministic_accumulates_and_agrees_with_whole_token_form(n_src):
+@pytest.mark.parametrize("n_src,d", [(8, 4096), (9, 4096), (5, 2048), (12, 2048)])
+def test_read_bwd_one_query_ring_is_deterministic_accumulates_and_agrees_with_whole_token_form(n_src, d):
     """Two runs of the ring form agree bitwise; with accumulate it adds into
-    the given source gradients; and it agrees with the whole-token form within
-    the bf16 bar (both round dsrc once; their sums run in different orders)."""
-    rng = _rng(59 + n_src)
-    T, d = 700, 4096
+    the given source gradients (8-byte pieces per lane at d = 4096, 4-byte at
+    2048); and it agrees with the whole-token form within the bf16 bar (both
+    round dsrc once; their sums run in different orders)."""
+    rng = _rng(59 + n_src + d)
+    T = 700
     src = to_dev(_sources(rng, n_src, T, d, BF16, step=0.25), BF16)
     q = to_dev(_queries(rng, 1, d), F32)
     dout = to_dev(_sources(rng, 1, T, d, BF16, step=0), BF16)
