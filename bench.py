@@ -40,7 +40,7 @@ CSRC = "depth_wise_attention_gb300/csrc/"
 KERNEL_SOURCES = {
     "depth_read_mma": [CSRC + "depth_read_mma.cuh", CSRC + "common.cuh", CSRC + "kernels_mma.cu"],
     "depth_read_mma_multi": [CSRC + "depth_read_mma.cuh", CSRC + "common.cuh", CSRC + "kernels_mma_multi.cu"],
-    "depth_read": [CSRC + "depth_read.cuh", CSRC + "common.cuh"],
+    "depth_read": [CSRC + "depth_read.cuh", CSRC + "common.cuh", CSRC + "dr_inst.cuh", CSRC + "kernels_bf16_multi.cu"],
     "phase2": [CSRC + "phase2.cuh", CSRC + "common.cuh", CSRC + "kernels_phase2.cu"],
     "msar": [CSRC + "msar.cu", CSRC + "msar.h", CSRC + "common.cuh"],
     "msar_tile": [CSRC + "msar_tile.cu", CSRC + "msar.h", CSRC + "common.cuh"],
@@ -1307,8 +1307,8 @@ class FullDepthWorkload(BlockWorkload):
         self.bytes_per_token = sum((l + 1) * d * 2 for l in range(1, L + 1))
         self.phase1_bytes_per_token = (L + 1) * d * 2           # the deepest layer's read
         self.launches_per_step = L
-        self.dominant = "depth_read_mma_multi_kernel (Full, layer 64)"
-        self.dominant_src = "depth_read_mma_multi"
+        self.dominant = "depth_read_kernel (Full, layer 64: the general kernel, 6-source chunks)"
+        self.dominant_src = "depth_read"
         self.profile_tag = f"ncu_full_depth_d{d}"
 
     def config(self):

@@ -43,6 +43,7 @@ std::atomic<int> g_kernel_variant{0};   // 0 automatic, 1 general (CUDA-core) de
 constexpr int kMaxDevices = 64;
 constexpr size_t kStageMaxBytes = 64 * 1024;        // one ring stage
 constexpr size_t kSmemBudget = 227 * 1024;         // stages + aux, per CTA (sm_103a opt-in limit)
+constexpr size_t kCtaReserve = 1024;              // shared memory the runtime reserves per CTA
 
 struct DeviceInfo {
     std::once_flag once;
@@ -243,18 +244,21 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     // (8 warps, two CTAs per SM); d = 1024 two tokens per item (8 warps x 128
     // channels), which fills all 16 MMA rows.
     // > 8 sources: one token per item, its sources in chunks of 8 folded in by
-    // an online softmax.  An item costs about the same whatever its rows, so
-    // the chunked kernel only beats the general kernel's 4-source chunks (two
-    // CTAs per SM) when its chunks are nearly full and numerous: measured at
-    // d = 4096 from 24 sources on with a last chunk of 5..8 rows (up to 7%
-    // faster at 64 sources; slower at d = 2048, so only d = 4096 is built).
+    // an online softmax (only d = 4096 is built: slower than the general
+    // kernel at d = 2048).  An item costs about the same whatever its rows
+    // and queries.  Measured at d = 4096, T = 16384, 9..64 sources: for one
+    // query and one head the general kernel's 6-source chunks (two CTAs per
+    // SM) are faster at every count (60.3 ms summed against 70.7 ms); for
+    // two to four queries the chunked kernel is faster from 10 sources on
+    // (15.2 against 22.9 ms over 9, 14, ..., 64 sources at two queries); for
+    // heads (MHAR) it is faster at every count (1.91 against 3.95 ms at 64).
     // One query over at most 4 sources at d = 4096 (the first layers of Full
     // AttnRes at depth): the one-token kernel costs about the same whatever
     // its rows, and the general kernel's tiles of several tokens are faster
     // (measured at T = 16384: 0.12-0.26 ms against 0.28 ms).
     const int kv = g_kernel_variant.load();
     const bool chunked = n_src > 8;
-    const bool chunked_wins = n_src >= 24 && (n_src % 8 == 0 || n_src % 8 >= 5);
+    const bool chunked_wins = H > 1 || (n_q >= 2 && n_src >= 10);
     const bool few_rows = d == 4096 && n_q == 1 && H == 1 && n_src <= 4;
     if (dt == ATTNRES_BF16 && n_q <= 4 && (d == 1024 || d == 2048 || d == 4096) && kv != 1 &&
         (!few_rows || kv == 2) && (!chunked || (d == 4096 && (chunked_wins || kv == 2)))) {
@@ -346,19 +350,7 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     if (chunk < 1) return ATTNRES_ERR_UNSUPPORTED;
     if (chunk > DR_CMAX) chunk = DR_CMAX;
     if (chunk > n_src) chunk = (int)n_src;
-    int max_stages = DR_MAX_STAGES;
-    if (n_src > chunk) {
-        // Chunked (online-softmax) reads: half-size stages, at most three, so
-        // that two CTAs share an SM and hide each other's per-chunk latency
-        // (Full at depth, 64 sources at d=4096: 3.3 -> 4.1 TB/s measured).
-        const int half = (int)(kStageMaxBytes / 2 / ((size_t)tt * row_bytes));
-        if (half >= 1) {
-            chunk = half > DR_CMAX ? DR_CMAX : half;
-            max_stages = 3;
-        }
-    }
-    const int nchunks = (int)((n_src + chunk - 1) / chunk);
-    const bool multi = nchunks > 1;
+    const bool multi = n_src > chunk;
 
     KernelRef kr;
     if (!lookup_depth_read(dt == ATTNRES_BF16 ? 1 : 0, nq_pad, vpt, mh, multi, &kr))
@@ -369,10 +361,30 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
     if (st != ATTNRES_OK) return st;
 
     const uint32_t src_pitch = (uint32_t)(tt * row_bytes);
-    const uint32_t stage_bytes = (uint32_t)(((size_t)chunk * src_pitch + 127) / 128 * 128);
     size_t budget = kSmemBudget;
     if ((size_t)dev->smem_optin < budget) budget = (size_t)dev->smem_optin;
     if (budget <= kr.aux_smem) return ATTNRES_ERR_UNSUPPORTED;
+    int max_stages = DR_MAX_STAGES;
+    if (multi) {
+        // Chunked (online-softmax) reads: two CTAs per SM, so that they hide
+        // each other's per-chunk latency, with two stages each and the
+        // largest chunk that fits.  Each chunk costs a CTA-wide reduction
+        // whatever its rows, so fewer, larger chunks win over more stages:
+        // Full at depth, 9..64 sources at d = 4096 (8 KB per source and
+        // stage): 4-source chunks x 3 stages 69.9 ms, 4 x 2 70.0 ms, 6 x 2
+        // 60.0 ms; 8 x 2 (one CTA per SM) 86.9 ms.  The same shape at d =
+        // 1024 and 2048 gains the same 15%.
+        const size_t half = budget / 2;
+        const size_t need = kr.aux_smem + kCtaReserve;
+        int fit = 0;
+        while (fit < chunk && need + 2 * (((size_t)(fit + 1) * src_pitch + 127) / 128 * 128) <= half) ++fit;
+        if (fit >= 1) {
+            chunk = fit;
+            max_stages = 2;
+        }
+    }
+    const int nchunks = (int)((n_src + chunk - 1) / chunk);
+    const uint32_t stage_bytes = (uint32_t)(((size_t)chunk * src_pitch + 127) / 128 * 128);
     int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
     if (nstages > max_stages) nstages = max_stages;
     if (nstages < 2) return ATTNRES_ERR_UNSUPPORTED;

@@ -1629,6 +1629,28 @@ def test_chunked_read_both_kernels(kernel_variant3, n_src, n_q, H, T, d):
     check_lse(lse, rl)
 
 
+@pytest.mark.parametrize("dt,n_src,n_q,H,T,d", [(F32, 10, 1, 1, 45, 4096), (F32, 19, 2, 1, 70, 2048),
+                                                (BF16, 25, 1, 1, 130, 1024), (BF16, 13, 1, 1, 77, 2048),
+                                                (BF16, 20, 1, 1, 33, 256), (BF16, 14, 1, 4, 29, 4096),
+                                                (BF16, 37, 3, 1, 19, 4096)])
+def test_general_kernel_chunk_shapes(dt, n_src, n_q, H, T, d):
+    """The general kernel's chunked reads at the chunk sizes its two-stage
+    rule picks for each row width (3 sources per stage for 16 KB rows, 6 for
+    8 KB, 8 for 4 KB): full and ragged last chunks, f32 and bf16, heads."""
+    rng = _rng(n_src * 19 + n_q * 3 + H + T + d)
+    src = _sources(rng, n_src, T, d, dt, step=1 / 16)
+    q = (rng.standard_normal((n_q, H, d // H)) * math.sqrt(16.0 / (d // H))).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    attnres.attnres_debug_set_kernel_variant(1)
+    try:
+        out, lse = attnres.mhar_fwd(to_dev(src, dt), to_dev(q, F32), to_dev(g, F32), 1e-6, want_lse=True)
+    finally:
+        attnres.attnres_debug_set_kernel_variant(0)
+    ro, rl = oracle.mhar(src, q, g, 1e-6, want_lse=True)
+    check_out(out, ro, dt, np.abs(src).max())
+    check_lse(lse, rl)
+
+
 def test_chunked_read_keeps_non_finite_tokens_apart(kernel_variant3):
     """Tokens whose first chunk holds infinities get non-finite outputs; the
     rows that a partial last chunk leaves unloaded must not carry them into
