@@ -427,6 +427,75 @@ def test_msar_two_phase_backward_validation(lib):
     assert p1(d=768) == UNS
 
 
+def test_read_bwd_noalloc_validation(lib):
+    """The no-allocation backward sizes its passes with attnres_read_bwd's
+    workspace rules first, so those rejections come before the device is
+    touched."""
+    SRC, Q, DO, DS, DQ, DG = A, B, B + 0x100000, A + 0x1000000, B + 0x200000, B + 0x300000
+
+    def na(n_src=9, T=16, d=64, n_q=1, dt=BF16):
+        return lib.attnres_read_bwd_noalloc(SRC, n_src, T * d, T, d, dt, Q, n_q, None, 1e-6, DO, DS, T * d, 0,
+                                            DQ, DG, None)
+    assert na(n_q=0) == INV
+    assert na(dt=7) == INV
+    assert na(d=60) == UNS                           # rows not a whole number of 16-byte vectors
+    assert na(n_src=257) == UNS                      # more than 32 chunks of 8 sources
+    assert na(n_src=17, n_q=9) == UNS                # more than 8 queries over more than 16 sources
+
+
+def test_msar_backward_chunk_validation(lib):
+    """The chunked MSAR backward: history rows widen every source and source-
+    gradient extent, and T_prev / accumulate have their own checks."""
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    bad = (ctypes.c_int32 * 3)(4, 0, 12)
+    kp = lambda k: ctypes.cast(k, ctypes.c_void_p)
+    T, d, H = 16, 1024, 11
+    DH, DS, DCW, DQ, DG, DMG, DMW, WS = (B + 0x1000000, B + 0x2000000, B + 0x3000000, B + 0x3100000,
+                                         B + 0x3200000, B + 0x3300000, B + 0x3400000, B + 0x4000000)
+
+    def mc(t_prev=H, n_src=8, T=T, d=d, k=ks, sstride=None, ds=DS, dstride=None, acc=0, dh=DH, ws=WS):
+        rows = t_prev + T if t_prev >= 0 else T
+        sstride = rows * d if sstride is None else sstride
+        dstride = rows * d if dstride is None else dstride
+        return lib.msar_expand_bwd_chunk(A, n_src, sstride, t_prev, T, d, BF16, 4, kp(k), B, B + 0x200000, None,
+                                         1e-6, None, B + 0x300000, 1e-6, dh, ds, dstride, acc, DCW, DQ, DG, DMG,
+                                         DMW, ws, 1 << 30, None)
+    assert mc(t_prev=-1) == INV
+    assert mc(acc=2) == INV
+    assert mc(acc=-1) == INV
+    assert mc(k=bad) == INV
+    assert mc(sstride=T * d) == INV                  # the history rows would overlap the next source
+    assert mc(dstride=(H + T) * d - 1) == INV        # so would the gradient rows
+    assert mc(ds=A + 64) == INV                      # dsrc overlaps the sources' history rows
+    assert mc(ws=DS + 64) == INV                     # workspace overlaps dsrc
+    assert mc(d=256) == UNS
+    assert mc(n_src=17) == UNS
+    assert mc(dh=DH + 8) == UNS
+    # T_prev = 0 is the plain backward's argument set; both pass the host checks
+    assert mc(t_prev=0) not in (INV, UNS)
+    assert mc() not in (INV, UNS)
+
+
+def test_msar_two_phase_backward_workspace_size_validation(lib):
+    ks = (ctypes.c_int32 * 3)(4, 8, 12)
+    bad = (ctypes.c_int32 * 3)(4, 0, 12)
+    kp = lambda k: ctypes.cast(k, ctypes.c_void_p)
+    n = ctypes.c_size_t(0)
+    p2 = lambda T=16, d=1024, dt=BF16, m=4, k=ks, out=ctypes.byref(n): \
+        lib.msar_block_phase2_bwd_workspace_size(T, d, dt, m, kp(k), out)
+    p1 = lambda n_src=8, T=16, d=1024, dt=BF16, m=4, k=ks, S=4, out=ctypes.byref(n): \
+        lib.msar_block_phase1_bwd_workspace_size(n_src, T, d, dt, m, kp(k), S, out)
+    for f in (p1, p2):
+        assert f(out=None) == INV
+        assert f(dt=7) == INV
+        assert f(T=-1) == INV
+        assert f(d=0) == INV
+        assert f(k=bad) == INV
+        assert f(m=3) == UNS
+    assert p1(n_src=0) == INV
+    assert p1(S=0) == INV
+
+
 def test_binding_covers_every_entry_point_and_fails_loudly_without_the_library(tmp_path):
     """The ctypes binding declares a signature for exactly the functions the
     header declares, and with no library there is an error, never a fallback."""
