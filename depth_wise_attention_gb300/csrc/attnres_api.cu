@@ -382,17 +382,31 @@ attnres_status_t launch_depth_read(const void *src, int64_t n_src, int64_t src_s
             chunk = fit;
             max_stages = 2;
         }
+        const int cap = dr_chunk_cap(vpt, true);
+        if (chunk > cap) chunk = cap;
     }
     const int nchunks = (int)((n_src + chunk - 1) / chunk);
     const uint32_t stage_bytes = (uint32_t)(((size_t)chunk * src_pitch + 127) / 128 * 128);
     int nstages = (int)((budget - kr.aux_smem) / stage_bytes);
     if (nstages > max_stages) nstages = max_stages;
     if (nstages < 2) return ATTNRES_ERR_UNSUPPORTED;
-    const size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
+    size_t smem = (size_t)nstages * stage_bytes + kr.aux_smem;
 
     int occ = 0;
     st = prepare_kernel(kr.fn, smem, DR_THREADS, &occ);
     if (st != ATTNRES_OK) return st;
+    if (max_stages == 2 && occ < 2) {
+        // the kernel's registers leave room for one CTA per SM (several
+        // queries): it takes the stages the second CTA would have had
+        int more = (int)((budget - kr.aux_smem) / stage_bytes);
+        if (more > DR_MAX_STAGES) more = DR_MAX_STAGES;
+        if (more > nstages) {
+            nstages = more;
+            smem = (size_t)nstages * stage_bytes + kr.aux_smem;
+            st = prepare_kernel(kr.fn, smem, DR_THREADS, &occ);
+            if (st != ATTNRES_OK) return st;
+        }
+    }
 
     DepthReadArgs a;
     a.src = static_cast<const unsigned char *>(src);

@@ -41,6 +41,14 @@ constexpr int DR_THREADS = DR_CONSUMER_WARPS * 32;
 constexpr int DR_CMAX = 8;        // sources per stage, at most
 constexpr int DR_MAX_STAGES = 4;
 
+// Sources per chunk an instance takes, so that its source loops have a
+// compile-time length: the chunked instances with two vectors per thread
+// (8 KB per source and stage at d = 1024..4096) get 6, the most that two
+// stages fit with two CTAs per SM; the host caps the chunk at this value.
+__host__ __device__ constexpr int dr_chunk_cap(int vpt, bool multi) {
+    return multi && vpt == 2 ? 6 : DR_CMAX;
+}
+
 struct DepthReadArgs {
     const unsigned char *src;     // source 0, row 0
     int64_t src_stride_bytes;     // bytes between consecutive sources
@@ -97,6 +105,7 @@ __global__ void __launch_bounds__(DR_THREADS, 1) depth_read_kernel(const DepthRe
     constexpr int NP = EPV / 2;
     constexpr int HS = L::HS, V = L::V, R = L::R, NPAIR = L::NPAIR, PJ = L::PJ;
     constexpr int CMAX = DR_CMAX;
+    constexpr int CK = dr_chunk_cap(VPT, MULTI);            // sources per chunk, at most
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *stages = smem;
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(DR_THREADS, 1) depth_read_kernel(const DepthRe
 #pragma unroll
         for (int i = 0; i < CMAX; ++i) {
             float2 t2[HS][1 + NQ];
-            if (i < nc) {
+            if (i < CK && i < nc) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
                     const int h = MH ? k : 0;
@@ -345,7 +354,7 @@ __global__ void __launch_bounds__(DR_THREADS, 1) depth_read_kernel(const DepthRe
         }
 #pragma unroll
         for (int i = 0; i < CMAX; ++i) {
-            if (i < nc) {
+            if (i < CK && i < nc) {
                 float al[HS][NQ];
 #pragma unroll
                 for (int h = 0; h < HS; ++h) {
